@@ -1,0 +1,390 @@
+"""Benchmark of the hybrid-batch step: one Mistral-7B-shaped decoder layer plus
+its 32000-entry LM head at token budget tau = 512 -- a 448-token prefill chunk
+at start positions 0, 512 and 1536 (cycled) with 64 piggybacked decodes whose
+contexts are uniform in [128, 4096].
+
+Prints one JSON line.  ``value`` is hybrid-batch tokens/s (rows of the
+stacked batch per second) over the timed steps with inputs resident in HBM;
+``e2e`` is the same metric through the host-buffer C entry point with the
+host<->device copies inside the timed region.  ``--impl reference`` times the
+CPU oracle on a bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+TAU, BD, STARTS = 512, 64, (0, 512, 1536)
+PAGE = 16
+METRIC = "hybrid-step tokens/s at tau=512 (Mistral-7B-shaped layer + LM head)"
+UNIT = "tokens/s"
+WORKLOAD = ("Mistral-7B-shaped layer (H=4096, 32q/8kv heads x 128, FFN 14336) + final norm + "
+            "LM head 32000; Lp=448 chunk at start {0,512,1536} (cycled) + Bd=64 decodes, "
+            "ctx U[128,4096]; bf16 weights N(0,0.02), random N(0,1) KV pages")
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def config_block(n):
+    return {"workload": WORKLOAD, "layers": 1, "tau": TAU, "lp": TAU - BD, "bd": BD,
+            "starts": list(STARTS), "page_size": PAGE, "parallelism": f"replicas x{n}",
+            "l2": "inputs larger than L2 (weights 436 MB + LM head 262 MB + KV ~0.55 GB per step)"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sms.append(float(f[0]))
+                maxs.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sms.sort()
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(maxs), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ------------------------------------------------------------------ peaks
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ our arm
+
+def setup_gpu(seed=0):
+    import torch
+
+    import chunked_prefill_hybrid_sar_gb300 as sar
+    from chunked_prefill_hybrid_sar_gb300 import harness
+
+    dims = synth.MISTRAL_LAYER
+    gen = synth.generator(seed, "cuda")
+    layers = [synth.layer_weights(gen, dims, torch.bfloat16, "cuda")]
+    head = synth.head_weights(gen, dims, torch.bfloat16, "cuda")
+    m = harness.load_model(dims, layers, head, max_tokens=TAU, max_decodes=BD)
+    del layers, head
+    cg = synth.generator(seed + 1)
+    ctxs = synth.uniform_int(cg, BD, 128, 4096)
+    need = sum(math.ceil((c + 1) / PAGE) for c in ctxs) + len(STARTS) * (2048 // PAGE)
+    kv = sar.KVCache(m, PAGE, need)
+    # random N(0,1) key/value histories everywhere; prompt pages get rewritten by the prior chunks
+    for kind in (0, 1):
+        pv = harness.page_view(kv, 0, kind, dims)
+        pv.copy_(torch.randn(pv.shape, generator=gen, device="cuda", dtype=torch.float32).to(torch.bfloat16))
+    alloc = harness.PageAllocator(range(need))
+    dec_bt = [alloc.take(math.ceil((c + 1) / PAGE)) for c in ctxs]
+    decs = [(100 + i, c, dec_bt[i]) for i, c in enumerate(ctxs)]
+    lp = TAU - BD
+    cases = []
+    for s in STARTS:
+        bt = alloc.take(2048 // PAGE)
+        prompt = synth.normal(gen, (s + lp, dims.hidden), dtype=torch.bfloat16, device="cuda")
+        for s0 in range(0, s, 512):  # the prompt's earlier chunks
+            m.step(kv, sar.Batch((s, s0, 512, bt), []), prompt[s0:s0 + 512].contiguous())
+        dec_in = synth.normal(gen, (BD, dims.hidden), dtype=torch.bfloat16, device="cuda")
+        x = torch.cat([prompt[s:s + lp], dec_in]).contiguous()
+        cases.append((sar.Batch((s, s, lp, bt), decs), x))
+    torch.cuda.synchronize()
+    m.sync_status()
+    return dims, m, kv, cases, ctxs
+
+
+def decode_attention_bytes(dims, ctxs):
+    """Algorithmic HBM bytes of one decode-attention launch: every key and value
+    of every decode's context (ctx + 1 keys incl. the new one) once, plus its
+    query and output rows."""
+    kv = sum(c + 1 for c in ctxs) * dims.n_kv_heads * dims.head_dim * 2 * 2
+    qo = len(ctxs) * dims.q_dim * 2 * 2
+    return kv + qo
+
+
+def gemm_flops(dims, rows):
+    return {"gemm_qkv": 2 * rows * dims.hidden * (dims.q_dim + 2 * dims.kv_dim),
+            "gemm_o": 2 * rows * dims.q_dim * dims.hidden,
+            "gemm_gateup": 2 * rows * dims.hidden * 2 * dims.ffn,
+            "gemm_down": 2 * rows * dims.ffn * dims.hidden}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import chunked_prefill_hybrid_sar_gb300 as sar
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dims, m, kv, cases, ctxs = setup_gpu()
+    hid = torch.empty(TAU, dims.hidden, dtype=torch.bfloat16, device="cuda")
+    logits = torch.empty(BD + 1, dims.vocab, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        b, x = cases[i % len(cases)]
+        m.step(kv, b, x, hidden_out=hid, logits_out=logits)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    m.sync_status()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # timed region: device events on the launching stream
+    launches0 = sar.launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        t0 = time.perf_counter()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        barrier()
+        wall = time.perf_counter() - t0
+    launches = sar.launch_count() - launches0
+    ms = ev0.elapsed_time(ev1)
+    m.sync_status()
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = t.item()
+    rows = TAU * args.steps * world
+    value = rows / (ms / 1e3)
+
+    # per-kernel times: the same steps again with an event pair around every kernel
+    m.profile(True)
+    for i in range(args.steps):
+        step(i)
+    prof = m.profile_read()
+    m.profile(False)
+    hbm, tf_burst, tf_sust, peak_src = peaks()
+    total = sum(v[0] for v in prof.values()) or 1.0
+    kernels = {}
+    for k, (t, n) in prof.items():
+        if n:
+            kernels[k] = {"ms_per_launch": t / n, "share": t / total, "launches": n}
+    flops = gemm_flops(dims, TAU)
+    for k, f in flops.items():
+        if k in kernels:
+            kernels[k]["tflops"] = f / (kernels[k]["ms_per_launch"] * 1e-3) / 1e12
+    dab = decode_attention_bytes(dims, ctxs)
+    if "decode_attn" in kernels:
+        kernels["decode_attn"]["gbs"] = dab / (kernels["decode_attn"]["ms_per_launch"] * 1e-3) / 1e9
+    head_bytes = dims.vocab * dims.hidden * 2
+    if "gemm_head" in kernels:
+        kernels["gemm_head"]["gbs"] = head_bytes / (kernels["gemm_head"]["ms_per_launch"] * 1e-3) / 1e9
+    dom = max(kernels, key=lambda k: kernels[k]["share"])
+    if dom in flops:
+        ach = kernels[dom]["tflops"]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": tf_sust, "unit": "TFLOP/s",
+                "frac": ach / tf_sust, "traffic": None,
+                "peak_source": f"{peak_src} bf16 sustained", "algorithmic_per_launch": flops[dom]}
+    else:
+        byts = dab if dom == "decode_attn" else head_bytes
+        ach = byts / (kernels[dom]["ms_per_launch"] * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "traffic": None, "peak_source": f"{peak_src} HBM copy",
+                "algorithmic_per_launch": byts}
+
+    # step roofline: sum over operators of max(T_math, T_mem), measured peaks
+    def op_t(fl, by):
+        return max(fl / (tf_sust * 1e12), by / (hbm * 1e9))
+    wb = 2 * dims.hidden
+    t_roof = (op_t(flops["gemm_qkv"], wb * (dims.q_dim + 2 * dims.kv_dim) + TAU * wb * 2)
+              + op_t(flops["gemm_o"], wb * dims.q_dim)
+              + op_t(flops["gemm_gateup"], wb * 2 * dims.ffn)
+              + op_t(flops["gemm_down"], 2 * dims.ffn * dims.hidden)
+              + op_t(0, dab) + op_t(2 * (BD + 1) * dims.hidden * dims.vocab, head_bytes)
+              + 4 * op_t(0, TAU * wb * 2))
+
+    # end to end: host buffers through the host entry point
+    pin_in = [x.cpu().pin_memory() for _, x in cases]
+    h_hid = torch.empty(TAU, dims.hidden, dtype=torch.bfloat16).pin_memory()
+    h_log = torch.empty(BD + 1, dims.vocab, dtype=torch.float32).pin_memory()
+    for i in range(2):
+        m.step_host(kv, cases[i % 3][0], pin_in[i % 3], hidden_out=h_hid, logits_out=h_log)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        m.step_host(kv, cases[i % 3][0], pin_in[i % 3], hidden_out=h_hid, logits_out=h_log)
+    barrier()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = t.item()
+    e2e = {"value": TAU * args.steps * world / e2e_s, "unit": UNIT,
+           "h2d_bytes_per_step": TAU * dims.hidden * 2,
+           "d2h_bytes_per_step": TAU * dims.hidden * 2 + (BD + 1) * dims.vocab * 4}
+
+    out = None
+    if rank == 0:
+        cpu = cpu_baseline(args) if (world == 1 and not args.no_cpu) else None
+        out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
+               "data": "synthetic (seeded random-init weights and KV histories)",
+               "config": config_block(world), "e2e": e2e, "gpu_launches": launches,
+               "roofline": roof, "step_roofline_ms": t_roof * 1e3,
+               "step_roofline_frac": (t_roof * 1e3) / (ms / args.steps),
+               "kernels": kernels, "clocks": clk.summary(), "wall_s": wall, "cpu_baseline": cpu}
+        print(json.dumps(out))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return out
+
+
+# ------------------------------------------------------------------ oracle arm
+
+def oracle_sample(n_decode=8, start=0, seed=3):
+    """A bounded sample of the workload for the CPU oracle: one hybrid step
+    with the 448-token chunk at `start` and `n_decode` of the decodes."""
+    import torch
+
+    from oracle import model as om
+
+    dims = synth.MISTRAL_LAYER
+    case = synth.mistral_layer_case(seed, n_decode=n_decode, tau=TAU, starts=(start,))
+    # keep the chunk at Lp = 448 rows as in the workload
+    lp = TAU - BD
+    gen = synth.generator(seed + 11)
+    prompt = synth.normal(gen, (start + lp, dims.hidden), dtype=torch.bfloat16)
+    w = om.layer_weights_np(case["layers"][0])
+    head = om.layer_weights_np(case["head"])
+    parts = [om.Part(x=om.to_np(prompt), lo=start, is_prefill=True)]
+    for i, c in enumerate(case["ctxs"]):
+        k, v = case["histories"][i]
+        parts.append(om.Part(x=om.to_np(case["decode_inputs"][i:i + 1]), lo=c,
+                             given=[om.LayerCache(om.to_np(k), om.to_np(v))]))
+    rows = lp + n_decode
+    return dims, w, head, parts, rows
+
+
+def cpu_baseline(args):
+    from oracle import model as om
+
+    dims, w, head, parts, rows = oracle_sample()
+    t0 = time.perf_counter()
+    om.hybrid_step([w], head, dims, parts)
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    return {"value": rows / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"one oracle hybrid step (float64 NumPy): 448-row chunk at start 0 + 8 decodes "
+                      f"of the workload's shape ({rows} rows, {dt:.1f} s)"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    from oracle import model as om
+
+    dims, w, head, parts, rows = oracle_sample()
+    for _ in range(min(args.warmup, 1)):
+        om.hybrid_step([w], head, dims, parts)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        om.hybrid_step([w], head, dims, parts)
+    dt = time.perf_counter() - t0
+    value = rows * args.steps / dt
+    cores = len(os.sched_getaffinity(0))
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": config_block(world),
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                            "sample": f"per step one oracle hybrid step: 448-row chunk + 8 decodes ({rows} rows)"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=6)
+    ap.add_argument("--impl", choices=["sar", "reference"], default="sar")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        if args.steps > 3:
+            args.steps = 3  # each oracle step takes seconds
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

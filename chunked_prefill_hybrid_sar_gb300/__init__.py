@@ -1,0 +1,224 @@
+"""Hybrid-batch decoder step (chunked prefill + piggybacked decodes) on GB300.
+
+Thin Python face of ``libsar.so``: the classes below only marshal torch
+tensors (device memory and streams) and host lists into the C ABI of
+``include/sar.h``; every step runs in the library's CUDA kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+from ._lib import (SAR_EPI_BF16, SAR_EPI_F32, SAR_EPI_RESIDUAL, SAR_EPI_SWIGLU, SAR_GEMM_AUTO,
+                   SAR_GEMM_M128_N128, SAR_GEMM_M128_N256, SAR_GEMM_M256_N128, SAR_GEMM_SWAP,
+                   SAR_IN_HIDDEN, SAR_IN_TOKENS, KERNEL_KINDS, SarError, check, lib)
+
+__all__ = ["Model", "KVCache", "Scheduler", "Batch", "SarError", "lib", "check", "gemm", "rmsnorm",
+           "launch_count", "KERNEL_KINDS", "SAR_IN_HIDDEN", "SAR_IN_TOKENS"]
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def launch_count() -> int:
+    return int(lib().sar_launch_count())
+
+
+class Batch:
+    """Owns the ctypes descriptor of one hybrid batch (chunk first, then decodes).
+
+    ``prefill``: ``(req, start_pos, len, block_table)`` or ``None``;
+    ``decodes``: iterable of ``(req, ctx_len, block_table)``.
+    """
+
+    def __init__(self, prefill, decodes, in_kind=SAR_IN_HIDDEN):
+        self._keep = []
+        b = _lib.sar_batch()
+        b.in_kind = in_kind
+        if prefill is not None:
+            req, start, n, bt = prefill
+            arr = _lib.i32_array(bt)
+            self._keep.append(arr)
+            b.has_prefill = 1
+            b.prefill = _lib.sar_prefill(req, start, n, arr, len(bt))
+        decodes = list(decodes)
+        dec = (_lib.sar_decode * max(1, len(decodes)))()
+        for i, (req, ctx, bt) in enumerate(decodes):
+            arr = _lib.i32_array(bt)
+            self._keep.append(arr)
+            dec[i] = _lib.sar_decode(req, ctx, arr, len(bt))
+        self._keep.append(dec)
+        b.n_decode = len(decodes)
+        b.decode = dec
+        self.c = b
+        self.lp = prefill[2] if prefill is not None else 0
+        self.bd = len(decodes)
+
+    @property
+    def rows(self) -> int:
+        return self.lp + self.bd
+
+    @property
+    def logit_rows(self) -> int:
+        return (1 if self.lp else 0) + self.bd
+
+
+class Model:
+    def __init__(self, dims, max_tokens: int, max_decodes: int):
+        self.dims = dims
+        d = _lib.sar_dims(dims.n_layers, dims.hidden, dims.n_q_heads, dims.n_kv_heads, dims.head_dim,
+                          dims.ffn, dims.vocab, dims.rms_eps, dims.rope_base, max_tokens, max_decodes)
+        h = ctypes.c_void_p()
+        check(lib().sar_model_create(ctypes.byref(d), ctypes.byref(h)))
+        self.h = h
+
+    def set_layer(self, layer: int, w: dict, stream=None) -> None:
+        lw = _lib.sar_layer_weights(*[_ptr(w[n]) for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd",
+                                                          "norm1", "norm2")])
+        check(lib().sar_model_set_layer(self.h, layer, ctypes.byref(lw), _stream(stream)))
+
+    def set_head(self, embed=None, final_norm=None, lm_head=None, stream=None) -> None:
+        check(lib().sar_model_set_head(self.h, _ptr(embed), _ptr(final_norm), _ptr(lm_head),
+                                       _stream(stream)))
+
+    def step(self, kv: "KVCache", batch: Batch, inp, hidden_out=None, logits_out=None,
+             layer_out=None, stream=None) -> None:
+        check(lib().sar_step(self.h, kv.h, ctypes.byref(batch.c), _ptr(inp), _ptr(hidden_out),
+                             _ptr(logits_out), _ptr(layer_out), _stream(stream)))
+
+    def step_host(self, kv: "KVCache", batch: Batch, inp, hidden_out=None, logits_out=None,
+                  stream=None) -> None:
+        check(lib().sar_step_host(self.h, kv.h, ctypes.byref(batch.c), _ptr(inp), _ptr(hidden_out),
+                                  _ptr(logits_out), None, _stream(stream)))
+
+    def sample_greedy(self, logits, rows: int, out, stream=None) -> None:
+        check(lib().sar_sample_greedy(self.h, _ptr(logits), rows, _ptr(out), _stream(stream)))
+
+    def sync_status(self) -> None:
+        check(lib().sar_sync_status(self.h))
+
+    def profile(self, on: bool) -> None:
+        check(lib().sar_profile_enable(self.h, 1 if on else 0))
+
+    def profile_read(self) -> dict:
+        n = len(KERNEL_KINDS)
+        ms = (ctypes.c_double * n)()
+        cnt = (ctypes.c_int64 * n)()
+        check(lib().sar_profile_read(self.h, ms, cnt, n))
+        return {k: (ms[i], int(cnt[i])) for i, k in enumerate(KERNEL_KINDS)}
+
+    def debug_buffer(self, which: int) -> int:
+        p = ctypes.c_void_p()
+        check(lib().sar_model_debug_buffer(self.h, which, ctypes.byref(p)))
+        return p.value
+
+    def close(self) -> None:
+        if self.h:
+            check(lib().sar_model_destroy(self.h))
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class KVCache:
+    def __init__(self, model: Model, page_size: int, num_pages: int):
+        h = ctypes.c_void_p()
+        check(lib().sar_kv_create(model.h, page_size, num_pages, ctypes.byref(h)))
+        self.h = h
+        self.model = model
+        self.page_size = page_size
+        self.num_pages = num_pages
+
+    def layer_ptr(self, layer: int, kind: int) -> int:
+        p = ctypes.c_void_p()
+        check(lib().sar_kv_layer_ptr(self.h, layer, kind, ctypes.byref(p)))
+        return p.value
+
+    def close(self) -> None:
+        if self.h:
+            check(lib().sar_kv_destroy(self.h))
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Scheduler:
+    """Stall-free scheduler (host only)."""
+
+    def __init__(self, tau: int, tile: int, page_size: int, num_pages: int, max_batch: int):
+        cfg = _lib.sar_sched_cfg(tau, tile, page_size, num_pages, max_batch)
+        h = ctypes.c_void_p()
+        check(lib().sar_sched_create(ctypes.byref(cfg), ctypes.byref(h)))
+        self.h = h
+
+    def add(self, req: int, arrival: float, prompt_len: int, output_len: int, prompt_tokens=None):
+        arr = _lib.i32_array(prompt_tokens) if prompt_tokens is not None else None
+        check(lib().sar_sched_add(self.h, req, arrival, prompt_len, output_len, arr))
+
+    def next(self, now: float):
+        """Returns ``(prefill, decodes, tokens, c_batch)`` with Python lists copied out."""
+        b = _lib.sar_batch()
+        tok = _lib.P_i32()
+        check(lib().sar_sched_next(self.h, now, ctypes.byref(b), ctypes.byref(tok)))
+        pre = None
+        if b.has_prefill:
+            p = b.prefill
+            pre = (p.req, p.start_pos, p.len, [p.block_table[i] for i in range(p.n_blocks)])
+        decs = []
+        for i in range(b.n_decode):
+            dd = b.decode[i]
+            decs.append((dd.req, dd.ctx_len, [dd.block_table[j] for j in range(dd.n_blocks)]))
+        m = (pre[2] if pre else 0) + len(decs)
+        tokens = [tok[i] for i in range(m)] if bool(tok) else None
+        return pre, decs, tokens, b
+
+    def commit(self, sampled) -> int:
+        arr = _lib.i32_array(sampled)
+        n = ctypes.c_int32()
+        check(lib().sar_sched_commit(self.h, arr, len(list(sampled)), ctypes.byref(n)))
+        return n.value
+
+    def stats(self):
+        v = [ctypes.c_int32() for _ in range(4)]
+        check(lib().sar_sched_stats(self.h, *[ctypes.byref(x) for x in v]))
+        return tuple(x.value for x in v)
+
+    def close(self) -> None:
+        if self.h:
+            check(lib().sar_sched_destroy(self.h))
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def gemm(a, w, c, residual=None, epilogue=SAR_EPI_BF16, variant=SAR_GEMM_AUTO, stream=None) -> None:
+    M, K = a.shape
+    N = w.shape[0]
+    check(lib().sar_op_gemm(_ptr(a), _ptr(w), _ptr(c), _ptr(residual), M, N, K, epilogue, variant,
+                            _stream(stream)))
+
+
+def rmsnorm(x, gain, y, eps: float, stream=None) -> None:
+    check(lib().sar_op_rmsnorm(_ptr(x), _ptr(gain), _ptr(y), x.shape[0], x.shape[1], eps,
+                               _stream(stream)))

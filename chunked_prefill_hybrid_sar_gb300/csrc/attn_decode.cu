@@ -1,0 +1,381 @@
+// Paged decode attention: every decode row's query heads against that
+// request's own paged K/V history (the "Decode uses PagedAttention" half of
+// the split, SARATHI technique write-up section 3.3; reading notes part 2
+// section 3: "each decode looks up its own history KV").
+//
+// HBM-bound (about 4 flops per byte), so the design is about streaming pages:
+//   * one CTA = (work item, KV head); a work item is a range of a decode's
+//     keys (long contexts are split so every SM has work, then merged);
+//   * the query heads of one GQA group share every K/V byte that is loaded;
+//   * each of the 4 warps owns a private 3-deep ring of 16-key blocks
+//     (K and V, 2 x 4 KB at head_dim 128) filled by cp.async.bulk straight
+//     from the page (one contiguous run per block) -- no page gather, no
+//     register staging;
+//   * a lane owns head_dim/32 consecutive dimensions; the 16 x group partial
+//     dot products are reduced with a halving butterfly (15.5 shuffles per
+//     head per block instead of 80), softmax runs online in base 2;
+//   * the 4 warps' (max, sum, acc) are merged in shared memory; split items
+//     write unnormalised partials that decode_combine_kernel merges.
+#include <float.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace sar {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kStages = 3;   // per-warp ring depth (16-key blocks)
+constexpr int kBlockKeys = 16;
+
+// One halving step of the butterfly: the NV >> STEP values in v[] are split
+// in two, the lane keeps the half chosen by its bit `16 >> STEP` and adds the
+// partner lane's copy of that half.
+template <int NV, int STEP>
+__device__ __forceinline__ void butterfly_step(float (&v)[NV], int lane) {
+  constexpr int mask = 16 >> STEP;
+  constexpr int half = (NV >> STEP) / 2;
+  const bool upper = (lane & mask) != 0;
+#pragma unroll
+  for (int j = 0; j < half; ++j) {
+    const float send = upper ? v[j] : v[j + half];
+    const float keep = upper ? v[j + half] : v[j];
+    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+  }
+}
+
+template <int D, int GP>
+__global__ void __launch_bounds__(kWarps * 32, 2) decode_attn_kernel(DecodeAttnArgs a) {
+  constexpr int DPL = D / 32;            // dimensions per lane
+  constexpr int NV = kBlockKeys * GP;    // partial dots per block: 16 keys x GP heads
+  constexpr int NVL = NV >= 32 ? NV / 32 : 1;
+  constexpr int BLK_BYTES = kBlockKeys * D * 2;
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // layout: [warp][stage][K | V] blocks, then p buffers, merge area, barriers
+  uint8_t* ring = smem + warp * kStages * 2 * BLK_BYTES;
+  float* pbuf = reinterpret_cast<float*>(smem + kWarps * kStages * 2 * BLK_BYTES) + warp * NV;
+  float* mrg = reinterpret_cast<float*>(smem + kWarps * kStages * 2 * BLK_BYTES) + kWarps * NV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(mrg + kWarps * GP * (D + 2)) + warp * kStages;
+
+  const int4 item = reinterpret_cast<const int4*>(a.items)[blockIdx.x];
+  const int b = item.x, kbeg = item.y, kend = item.z, part = item.w;
+  const int kh = blockIdx.y;
+  const int G = a.qh / a.kvh;
+  const int* bt = a.bt + a.bt_off[b];
+  const int btlen = a.bt_len[b];
+  const int nblk = (kend - kbeg + kBlockKeys - 1) / kBlockKeys;
+
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // Issue block `j` of this CTA's range into stage s (lane 0 only).
+  auto issue = [&](int j, int s) -> bool {
+    const int key0 = kbeg + j * kBlockKeys;
+    const int bi = key0 / a.page_size;
+    int page = (bi < btlen) ? bt[bi] : -1;
+    if (page < 0 || page >= a.num_pages) {
+      report(a.err, SAR_ERR_BOUNDS, SITE_DECODE_BOUNDS, key0);
+      return false;
+    }
+    const int off = key0 - bi * a.page_size;
+    const size_t elem = (((size_t)page * a.kvh + kh) * a.page_size + off) * D;
+    const uint32_t bar = smem_u32(&bars[s]);
+    uint8_t* dst = ring + s * 2 * BLK_BYTES;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_expect_tx(bar, 2 * BLK_BYTES);
+    bulk_g2s(smem_u32(dst), a.k_cache + elem, BLK_BYTES, bar);
+    bulk_g2s(smem_u32(dst + BLK_BYTES), a.v_cache + elem, BLK_BYTES, bar);
+    return true;
+  };
+
+  // query heads of this KV head, pre-scaled so that softmax runs in base 2
+  const float qscale = rsqrtf((float)D) * 1.4426950408889634f;
+  float q[GP][DPL];
+#pragma unroll
+  for (int h = 0; h < GP; ++h) {
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) q[h][e] = 0.f;
+    if (h < G) {
+      const __nv_bfloat16* qp = a.qkv + (size_t)b * a.ld + (size_t)(kh * G + h) * D + lane * DPL;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) q[h][e] = __bfloat162float(qp[e]) * qscale;
+    }
+  }
+
+  float m_run[GP], acc[GP][DPL];
+#pragma unroll
+  for (int h = 0; h < GP; ++h) {
+    m_run[h] = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
+  }
+  float l_part = 0.f;  // this lane's share of its own head's denominator
+
+  // my blocks: j = warp, warp + 4, ...
+  const int my_n = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
+  bool ok = true;
+  int issued = 0, consumed = 0;  // blocks put in flight / taken out (lane 0's view)
+  if (lane == 0) {
+    for (int i = 0; i < kStages && i < my_n && ok; ++i) {
+      ok = issue(warp + i * kWarps, i);
+      if (ok) ++issued;
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+
+  for (int i = 0; i < my_n && ok; ++i) {
+    const int s = i % kStages;
+    const uint32_t par = (uint32_t)((i / kStages) & 1);
+    int got = 0;
+    if (lane == 0) got = mbar_wait(smem_u32(&bars[s]), par, a.err, SITE_DECODE_PIPE) ? 1 : 0;
+    got = __shfl_sync(0xffffffffu, got, 0);
+    if (!got) {
+      ok = false;
+      break;
+    }
+    ++consumed;
+    const int j = warp + i * kWarps;
+    const int key0 = kbeg + j * kBlockKeys;
+    const int nk = min(kBlockKeys, kend - key0);
+    const uint8_t* kb = ring + s * 2 * BLK_BYTES;
+    const uint8_t* vb = kb + BLK_BYTES;
+
+    // ---- scores: partial dots over this lane's dims, then butterfly ----
+    float v[NV];
+#pragma unroll
+    for (int k = 0; k < kBlockKeys; ++k) {
+      float kf[DPL];
+      if constexpr (DPL == 4) {
+        const uint2 kv = *reinterpret_cast<const uint2*>(kb + (k * D + lane * 4) * 2);
+        kf[0] = bf16lo(kv.x); kf[1] = bf16hi(kv.x); kf[2] = bf16lo(kv.y); kf[3] = bf16hi(kv.y);
+      } else {
+        const uint32_t kv = *reinterpret_cast<const uint32_t*>(kb + (k * D + lane * 2) * 2);
+        kf[0] = bf16lo(kv); kf[1] = bf16hi(kv);
+      }
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        float d = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) d = fmaf(q[h][e], kf[e], d);
+        v[h * kBlockKeys + k] = d;
+      }
+    }
+    butterfly_step<NV, 0>(v, lane);
+    butterfly_step<NV, 1>(v, lane);
+    butterfly_step<NV, 2>(v, lane);
+    butterfly_step<NV, 3>(v, lane);
+    if constexpr (NV >= 32) {
+      butterfly_step<NV, 4>(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+    }
+    // lane now holds scores of indices [base, base + NVL): index = head*16 + key
+    const int base = NV >= 32 ? lane * NVL : (lane >> 1);
+    const int myh = base / kBlockKeys;
+    float bmax = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < NVL; ++t) {
+      const int key = (base + t) % kBlockKeys;
+      if (key >= nk) v[t] = -INFINITY;
+      bmax = fmaxf(bmax, v[t]);
+    }
+    // lanes of one head: a contiguous group of 16/NVL lanes (NV >= 32), or all (NV == 16)
+    constexpr int GROUP = NV >= 32 ? kBlockKeys / NVL : 32;
+#pragma unroll
+    for (int o = (NV >= 32 ? 1 : 2); o < GROUP; o <<= 1)
+      bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
+    float alpha[GP];
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {
+      const int src = NV >= 32 ? h * GROUP : 0;
+      const float bm = __shfl_sync(0xffffffffu, bmax, src);
+      const float mn = fmaxf(m_run[h], bm);
+      alpha[h] = exp2f(m_run[h] - mn);
+      m_run[h] = mn;
+    }
+    float psum = 0.f;
+    float mh = m_run[0], am = alpha[0];
+#pragma unroll
+    for (int h = 1; h < GP; ++h)
+      if (h == myh) {
+        mh = m_run[h];
+        am = alpha[h];
+      }
+#pragma unroll
+    for (int t = 0; t < NVL; ++t) {
+      const float p = exp2f(v[t] - mh);
+      psum += p;
+      const int idx = base + t;
+      pbuf[(idx % kBlockKeys) * GP + idx / kBlockKeys] = p;  // [key][head]
+    }
+    if (NV < 32 && (lane & 1)) psum = 0.f;  // lane pairs hold the same value
+    l_part = l_part * am + psum;
+    __syncwarp();
+
+    // ---- acc = acc * alpha + P V ----
+#pragma unroll
+    for (int h = 0; h < GP; ++h)
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc[h][e] *= alpha[h];
+#pragma unroll 4
+    for (int k = 0; k < nk; ++k) {
+      float vf[DPL];
+      if constexpr (DPL == 4) {
+        const uint2 vv = *reinterpret_cast<const uint2*>(vb + (k * D + lane * 4) * 2);
+        vf[0] = bf16lo(vv.x); vf[1] = bf16hi(vv.x); vf[2] = bf16lo(vv.y); vf[3] = bf16hi(vv.y);
+      } else {
+        const uint32_t vv = *reinterpret_cast<const uint32_t*>(vb + (k * D + lane * 2) * 2);
+        vf[0] = bf16lo(vv); vf[1] = bf16hi(vv);
+      }
+      float p[GP];
+      if constexpr (GP >= 4) {
+#pragma unroll
+        for (int h = 0; h < GP; h += 4) {
+          const float4 p4 = *reinterpret_cast<const float4*>(&pbuf[k * GP + h]);
+          p[h] = p4.x; p[h + 1] = p4.y; p[h + 2] = p4.z; p[h + 3] = p4.w;
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < GP; ++h) p[h] = pbuf[k * GP + h];
+      }
+#pragma unroll
+      for (int h = 0; h < GP; ++h)
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(p[h], vf[e], acc[h][e]);
+    }
+    __syncwarp();
+    // refill this stage with block i + kStages
+    if (i + kStages < my_n) {
+      int r = 1;
+      if (lane == 0) {
+        r = issue(warp + (i + kStages) * kWarps, s) ? 1 : 0;
+        issued += r;
+      }
+      if (!__shfl_sync(0xffffffffu, r, 0)) ok = false;
+    }
+  }
+  // never leave with copies in flight: wait (bounded) for any not consumed
+  if (lane == 0) {
+    for (int i = consumed; i < issued; ++i)
+      mbar_wait(smem_u32(&bars[i % kStages]), (uint32_t)((i / kStages) & 1), a.err, SITE_DECODE_PIPE);
+  }
+  __syncwarp();
+
+  // ---- per-warp denominators, then merge the 4 warps ----
+  float lsum = l_part;
+  {
+    constexpr int GROUP = NV >= 32 ? kBlockKeys / NVL : 32;
+#pragma unroll
+    for (int o = 1; o < GROUP; o <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+  }
+  float* my = mrg + warp * GP * (D + 2);
+#pragma unroll
+  for (int h = 0; h < GP; ++h) {
+    constexpr int GROUP = NV >= 32 ? kBlockKeys / NVL : 32;
+    const float lh = __shfl_sync(0xffffffffu, lsum, NV >= 32 ? h * GROUP : 0);
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) my[h * (D + 2) + lane * DPL + e] = acc[h][e];
+    if (lane == 0) {
+      my[h * (D + 2) + D] = m_run[h];
+      my[h * (D + 2) + D + 1] = lh;
+    }
+  }
+  __syncthreads();
+  // 128 threads: thread t handles (head, dim) pairs
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int h = idx / D, dd = idx - h * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mrg[w * GP * (D + 2) + h * (D + 2) + D]);
+    float L = 0.f, A = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float* src = mrg + w * GP * (D + 2) + h * (D + 2);
+      const float sc = (src[D] == -INFINITY) ? 0.f : exp2f(src[D] - M);
+      L = fmaf(src[D + 1], sc, L);
+      A = fmaf(src[dd], sc, A);
+    }
+    const int hq = kh * G + h;
+    if (part < 0) {
+      a.out[(size_t)b * a.ld_out + (size_t)hq * D + dd] = __float2bfloat16_rn(A / L);
+    } else {
+      float* pp = a.partials + ((size_t)part * a.qh + hq) * (D + 2);
+      pp[dd] = A;
+      if (dd == 0) {
+        pp[D] = M;
+        pp[D + 1] = L;
+      }
+    }
+  }
+}
+
+// Merges the split partial results of each decode: out = sum_i A_i 2^(m_i - M) / sum_i L_i 2^(m_i - M).
+template <int D>
+__global__ void decode_combine_kernel(DecodeAttnArgs a) {
+  const int b = blockIdx.x;
+  const int hq = blockIdx.y;
+  const int cnt = a.parts_count[b];
+  if (cnt <= 1) return;
+  const int p0 = a.parts_begin[b];
+  const int dd = threadIdx.x;
+  float M = -INFINITY;
+  for (int i = 0; i < cnt; ++i) M = fmaxf(M, a.partials[((size_t)(p0 + i) * a.qh + hq) * (D + 2) + D]);
+  float L = 0.f, A = 0.f;
+  for (int i = 0; i < cnt; ++i) {
+    const float* pp = a.partials + ((size_t)(p0 + i) * a.qh + hq) * (D + 2);
+    const float sc = exp2f(pp[D] - M);
+    L = fmaf(pp[D + 1], sc, L);
+    A = fmaf(pp[dd], sc, A);
+  }
+  a.out[(size_t)b * a.ld_out + (size_t)hq * D + dd] = __float2bfloat16_rn(A / L);
+}
+
+template <int D, int GP>
+int launch_impl(const DecodeAttnArgs& a, cudaStream_t s) {
+  constexpr int NV = kBlockKeys * GP;
+  const size_t smem = (size_t)kWarps * kStages * 2 * kBlockKeys * D * 2 + (size_t)kWarps * NV * 4 +
+                      (size_t)kWarps * GP * (D + 2) * 4 + (size_t)kWarps * kStages * 8 + 16;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<D, GP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_error(e, "decode attention attribute");
+    attr = true;
+  }
+  decode_attn_kernel<D, GP><<<dim3(a.n_items, a.kvh), kWarps * 32, smem, s>>>(a);
+  count_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error(e, "decode attention launch");
+  if (a.partials) {
+    decode_combine_kernel<D><<<dim3(a.n_decode, a.qh), D, 0, s>>>(a);
+    count_launches(1);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_error(e, "decode combine launch");
+  }
+  return SAR_OK;
+}
+
+}  // namespace
+
+int launch_decode_attention(const DecodeAttnArgs& a, cudaStream_t s) {
+  if (a.n_items <= 0) return SAR_OK;
+  const int G = a.qh / a.kvh;
+  if (a.qh % a.kvh || G > 8 || (a.d != 64 && a.d != 128) || a.page_size % kBlockKeys)
+    return set_error(SAR_ERR_UNSUPPORTED, "decode attention: head_dim 64/128, group <= 8, page % 16");
+  const int GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
+#define SAR_DEC(DD, GG) \
+  if (a.d == DD && GP == GG) return launch_impl<DD, GG>(a, s);
+  SAR_DEC(128, 1) SAR_DEC(128, 2) SAR_DEC(128, 4) SAR_DEC(128, 8)
+  SAR_DEC(64, 1) SAR_DEC(64, 2) SAR_DEC(64, 4) SAR_DEC(64, 8)
+#undef SAR_DEC
+  return set_error(SAR_ERR_UNSUPPORTED, "decode attention: no kernel for this shape");
+}
+
+}  // namespace sar

@@ -1,0 +1,555 @@
+// Projection / FFN / LM-head GEMM on the 5th-generation tensor cores.
+//
+// C = epilogue(A . W^T) with A = activations [M, K] and W = weights [N, K],
+// both bf16 and K-major.  This is the "one GEMM per weight over the stacked
+// [Lp+Bd, H] rows" of the hybrid step ("SARATHI: Efficient LLM Inference by
+// Piggybacking Decodes with Chunked Prefills", reading notes, part 2 section 3).
+//
+// Structure (persistent, one CTA per SM, 192 threads):
+//   warp 0       TMA producer: 64-wide K slabs of the A and B tiles into a ring
+//                of shared-memory stages (128-byte swizzle), mbarrier tx counts.
+//   warp 1       allocates tensor memory; lane 0 issues tcgen05.mma
+//                (kind::f16, bf16 x bf16 -> fp32, M = 128, N = bn, K = 16) and
+//                tcgen05.commit's each stage back to the producer.
+//   warps 2..5   epilogue: tcgen05.ld of the fp32 accumulator (each warp owns
+//                the 32 TMEM lanes of its warp-id % 4), fused epilogue, global
+//                stores.  Two accumulators alternate so the epilogue of one
+//                tile overlaps the MMAs of the next.
+//
+// Tilings: non-swap puts 128 token rows on the MMA M side (msub = 2 stacks two
+// such MMAs on one weight tile for 256-row tiles); swap puts 128 weight rows
+// on the M side and the tokens (padded to 16) on the N side, so a step with
+// few rows pays no 128-row quantisation.  Every wait is bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <string>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace sar {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBK = 64;                   // K elements per stage (128 bytes)
+constexpr int kTileA = 128 * kBK * 2;     // one 128-row slab: 16 KB
+constexpr int kSmemLimit = 232448;        // 227 KB of dynamic shared memory
+constexpr int kBarBytes = 1024;           // barriers + TMEM slot (+ alignment)
+constexpr int kSwapXchg = 64 * 17 * 4;    // swap-mode SwiGLU exchange buffer
+
+// ---- tcgen05 wrappers ------------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns: thread t of the warp gets lane
+// (warp quarter base + t), columns [col, col + 16).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row atoms 1024 bytes apart (stride byte offset), sm_100 version.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                   // leading byte offset (unused for SW128 K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset
+  d |= (uint64_t)1 << 46;                   // descriptor version
+  d |= (uint64_t)2 << 61;                   // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
+
+struct Params {
+  int M, N, K;
+  int bn, m_tiles, n_tiles, k_blocks, stages, stage_bytes, tmem_cols;
+  void* c;
+  const void* r;
+  int* err;
+};
+
+__device__ __forceinline__ void next_stage(int& stage, uint32_t& phase, int stages) {
+  if (++stage == stages) {
+    stage = 0;
+    phase ^= 1u;
+  }
+}
+
+// Warp-uniform wait: lane 0 polls, the result is broadcast.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* err, int site) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err, site) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+template <int EPI, bool SWAP, int MSUB>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int stages = p.stages;
+  uint8_t* bar_area = smem + stages * p.stage_bytes;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(bar_area);
+  uint64_t* empty_bar = full_bar + stages;
+  uint64_t* accf_bar = empty_bar + stages;  // [2]
+  uint64_t* acce_bar = accf_bar + 2;        // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
+  float* xchg = reinterpret_cast<float*>(bar_area + kBarBytes);  // swap SwiGLU only
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&accf_bar[s]), 1);
+      mbar_init(smem_u32(&acce_bar[s]), 128);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int n_tiles_total = p.m_tiles * p.n_tiles;
+  const int acc_cols = MSUB * p.bn;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_a);
+      tma_prefetch_desc(&tm_b);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < n_tiles_total && ok; t += gridDim.x) {
+        const int mt = t % p.m_tiles;
+        const int nt = t / p.m_tiles;
+        // A rows: tokens (non-swap) or weights (swap); B rows: the other one.
+        const int a_row = SWAP ? nt * 128 : mt * 128 * MSUB;
+        const int b_row = SWAP ? mt * p.bn : nt * p.bn;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.err, SITE_GEMM_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + stage * p.stage_bytes;
+          const uint32_t fb = smem_u32(&full_bar[stage]);
+          mbar_expect_tx(fb, (uint32_t)p.stage_bytes);
+#pragma unroll
+          for (int s = 0; s < MSUB; ++s)
+            tma_load_2d(smem_u32(st + s * kTileA), &tm_a, kb * kBK, a_row + s * 128, fb);
+          tma_load_2d(smem_u32(st + MSUB * kTileA), &tm_b, kb * kBK, b_row, fb);
+          next_stage(stage, phase, stages);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(p.bn);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int i = 0;
+      for (int t = blockIdx.x; t < n_tiles_total && ok; t += gridDim.x, ++i) {
+        const int acc = i & 1;
+        const uint32_t accph = (uint32_t)((i >> 1) & 1);
+        if (!mbar_wait(smem_u32(&acce_bar[acc]), accph ^ 1u, p.err, SITE_GEMM_MMA)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * acc_cols);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.err, SITE_GEMM_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + stage * p.stage_bytes);
+          const uint32_t b_base = a_base + MSUB * kTileA;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t bdesc = sw128_desc(b_base + kk * 32);
+#pragma unroll
+            for (int s = 0; s < MSUB; ++s) {
+              const uint64_t adesc = sw128_desc(a_base + s * kTileA + kk * 32);
+              mma_bf16(d_tmem + (uint32_t)(s * p.bn), adesc, bdesc, idesc, (kb | kk) != 0);
+            }
+          }
+          mma_commit(smem_u32(&empty_bar[stage]));
+          next_stage(stage, phase, stages);
+        }
+        if (ok) mma_commit(smem_u32(&accf_bar[acc]));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: warps 2..5 ----------------
+    const int q = warp & 3;             // TMEM lane quarter this warp may access
+    const int lrow = q * 32 + lane;     // accumulator lane = row of the MMA's M side
+    int i = 0;
+    bool alive = true;  // false once a wait gave up: loads/stores stop, barriers stay matched
+    for (int t = blockIdx.x; t < n_tiles_total; t += gridDim.x, ++i) {
+      const int mt = t % p.m_tiles;
+      const int nt = t / p.m_tiles;
+      const int acc = i & 1;
+      const uint32_t accph = (uint32_t)((i >> 1) & 1);
+      if (alive) alive = warp_wait(smem_u32(&accf_bar[acc]), accph, p.err, SITE_GEMM_EPILOGUE);
+      if (!alive && !(SWAP && EPI == SAR_EPI_SWIGLU)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * acc_cols);
+
+      if constexpr (!SWAP) {
+#pragma unroll 1
+        for (int s = 0; s < MSUB; ++s) {
+          const int row = (mt * MSUB + s) * 128 + lrow;
+          const bool row_ok = row < p.M;
+          const uint32_t sbase = tbase + (uint32_t)(s * p.bn);
+          if constexpr (EPI == SAR_EPI_SWIGLU) {
+            // packed columns [h*128, h*128+64) gate, [h*128+64, h*128+128) up
+            const int F = p.N >> 1;
+            __nv_bfloat16* C = reinterpret_cast<__nv_bfloat16*>(p.c);
+#pragma unroll 1
+            for (int h = 0; h < p.bn / 128; ++h) {
+#pragma unroll 1
+              for (int j = 0; j < 4; ++j) {
+                uint32_t g[16], u[16];
+                tmem_ld16(sbase + h * 128 + j * 16, g);
+                tmem_ld16(sbase + h * 128 + 64 + j * 16, u);
+                tmem_wait_ld();
+                const int ocol = nt * (p.bn / 2) + h * 64 + j * 16;
+                if (row_ok && ocol < F) {
+                  uint32_t o[8];
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) {
+                    const float a0 = silu(__uint_as_float(g[2 * e])) * __uint_as_float(u[2 * e]);
+                    const float a1 = silu(__uint_as_float(g[2 * e + 1])) * __uint_as_float(u[2 * e + 1]);
+                    o[e] = pack_bf16(a0, a1);
+                  }
+                  uint4* dst = reinterpret_cast<uint4*>(C + (size_t)row * F + ocol);
+                  dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                  dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+              }
+            }
+          } else {
+#pragma unroll 1
+            for (int j = 0; j < p.bn / 16; ++j) {
+              uint32_t v[16];
+              tmem_ld16(sbase + j * 16, v);
+              tmem_wait_ld();
+              const int col = nt * p.bn + j * 16;
+              if (!row_ok || col >= p.N) continue;
+              if constexpr (EPI == SAR_EPI_F32) {
+                float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.c) + (size_t)row * p.N + col);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                       __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+              } else {
+                float f[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]);
+                if constexpr (EPI == SAR_EPI_RESIDUAL) {
+                  const uint4* rs = reinterpret_cast<const uint4*>(
+                      reinterpret_cast<const __nv_bfloat16*>(p.r) + (size_t)row * p.N + col);
+                  const uint4 r0 = rs[0], r1 = rs[1];
+                  const uint32_t rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) {
+                    f[2 * e] += bf16lo(rr[e]);
+                    f[2 * e + 1] += bf16hi(rr[e]);
+                  }
+                }
+                uint32_t o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = pack_bf16(f[2 * e], f[2 * e + 1]);
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.c) + (size_t)row * p.N + col);
+                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+              }
+            }
+          }
+        }
+      } else {
+        // swap: accumulator lane = weight row, TMEM column = token
+        const int tok0 = mt * p.bn;
+        if constexpr (EPI == SAR_EPI_SWIGLU) {
+          // A tile = one packed block pair: lanes 0..63 gate, 64..127 up
+          const int F = p.N >> 1;
+          const int ocol = nt * 64 + (lrow & 63);
+          __nv_bfloat16* C = reinterpret_cast<__nv_bfloat16*>(p.c);
+#pragma unroll 1
+          for (int j = 0; j < p.bn / 16; ++j) {
+            uint32_t v[16];
+            if (alive) {
+              tmem_ld16(tbase + j * 16, v);
+              tmem_wait_ld();
+            }
+            if (alive && lrow >= 64) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) xchg[(lrow - 64) * 17 + e] = __uint_as_float(v[e]);
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (alive && lrow < 64 && ocol < F) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int m = tok0 + j * 16 + e;
+                if (m < p.M) {
+                  const float a = silu(__uint_as_float(v[e])) * xchg[lrow * 17 + e];
+                  C[(size_t)m * F + ocol] = __float2bfloat16_rn(a);
+                }
+              }
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+          }
+        } else {
+          const int n = nt * 128 + lrow;
+#pragma unroll 1
+          for (int j = 0; j < p.bn / 16; ++j) {
+            uint32_t v[16];
+            tmem_ld16(tbase + j * 16, v);
+            tmem_wait_ld();
+            if (n >= p.N) continue;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int m = tok0 + j * 16 + e;
+              if (m >= p.M) break;
+              const size_t idx = (size_t)m * p.N + n;
+              float f = __uint_as_float(v[e]);
+              if constexpr (EPI == SAR_EPI_F32) {
+                reinterpret_cast<float*>(p.c)[idx] = f;
+              } else {
+                if constexpr (EPI == SAR_EPI_RESIDUAL)
+                  f += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.r)[idx]);
+                reinterpret_cast<__nv_bfloat16*>(p.c)[idx] = __float2bfloat16_rn(f);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      if (alive) mbar_arrive(smem_u32(&acce_bar[acc]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+  }
+}
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, Params);
+
+template <int EPI, bool SWAP, int MSUB>
+const void* kernel_ptr() {
+  return reinterpret_cast<const void*>(&gemm_tc_kernel<EPI, SWAP, MSUB>);
+}
+
+const void* pick_kernel(int epi, bool swap, int msub) {
+#define SAR_PICK(E)                                              \
+  if (epi == E) {                                                \
+    if (swap) return kernel_ptr<E, true, 1>();                   \
+    return msub == 2 ? kernel_ptr<E, false, 2>() : kernel_ptr<E, false, 1>(); \
+  }
+  SAR_PICK(SAR_EPI_BF16)
+  SAR_PICK(SAR_EPI_RESIDUAL)
+  SAR_PICK(SAR_EPI_SWIGLU)
+  SAR_PICK(SAR_EPI_F32)
+#undef SAR_PICK
+  return nullptr;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+int pow2_at_least(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+int make_tmap_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return set_error(SAR_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (cols * 2) % 16 || rows == 0 || box_rows == 0 ||
+      box_rows > 256)
+    return set_error(SAR_ERR_INVALID_ARG, "tensor map: pointer/stride not 16-byte aligned or bad box");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(SAR_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
+  return SAR_OK;
+}
+
+int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg) {
+  if (M < 1 || N < 64 || K < 64 || N % 64 || K % 64)
+    return set_error(SAR_ERR_UNSUPPORTED, "gemm: need M >= 1, N and K multiples of 64");
+  if (epi == SAR_EPI_SWIGLU && N % 128)
+    return set_error(SAR_ERR_UNSUPPORTED, "gemm: SwiGLU needs whole 64-row gate/up block pairs");
+  const int sms = num_sms();
+  GemmCfg c;
+  if (variant == SAR_GEMM_AUTO) {
+    if (M <= 256) {
+      variant = SAR_GEMM_SWAP;
+    } else {
+      // makespan estimate: waves x per-tile MMA work
+      auto cost = [&](int msub, int bn) {
+        const long tiles = (long)((M + 128 * msub - 1) / (128 * msub)) * ((N + bn - 1) / bn);
+        return ((tiles + sms - 1) / sms) * (long)msub * bn * 1000 + tiles;  // tie-break: fewer tiles
+      };
+      variant = SAR_GEMM_M128_N256;
+      long best = (N % 256 == 0) ? cost(1, 256) : -1;
+      if (best < 0 || cost(1, 128) < best) { variant = SAR_GEMM_M128_N128; best = cost(1, 128); }
+      if (cost(2, 128) < best) variant = SAR_GEMM_M256_N128;
+    }
+  }
+  switch (variant) {
+    case SAR_GEMM_M128_N128: c.swap = 0; c.msub = 1; c.bn = 128; break;
+    case SAR_GEMM_M128_N256: c.swap = 0; c.msub = 1; c.bn = 256; break;
+    case SAR_GEMM_M256_N128: c.swap = 0; c.msub = 2; c.bn = 128; break;
+    case SAR_GEMM_SWAP:
+      if (M > 256) return set_error(SAR_ERR_UNSUPPORTED, "gemm: swap tiling needs M <= 256");
+      c.swap = 1; c.msub = 1; c.bn = (M + 15) / 16 * 16; break;
+    default: return set_error(SAR_ERR_INVALID_ARG, "gemm: unknown variant");
+  }
+  if (!c.swap && N % c.bn && epi == SAR_EPI_SWIGLU)
+    return set_error(SAR_ERR_UNSUPPORTED, "gemm: SwiGLU tiles must not straddle N");
+  if (c.swap) {
+    c.m_tiles = 1;
+    c.n_tiles = (N + 127) / 128;
+    c.a_box_rows = 128;   // weights
+    c.b_box_rows = c.bn;  // tokens
+  } else {
+    c.m_tiles = (M + 128 * c.msub - 1) / (128 * c.msub);
+    c.n_tiles = (N + c.bn - 1) / c.bn;
+    c.a_box_rows = 128;   // tokens
+    c.b_box_rows = c.bn;  // weights
+  }
+  const int stage_bytes = c.msub * kTileA + c.bn * kBK * 2;
+  const int extra = kBarBytes + 1024 + ((c.swap && epi == SAR_EPI_SWIGLU) ? kSwapXchg : 0);
+  c.stages = std::min(8, (kSmemLimit - extra) / stage_bytes);
+  if (c.stages < 2) return set_error(SAR_ERR_UNSUPPORTED, "gemm: tile does not fit shared memory");
+  c.smem = c.stages * stage_bytes + extra;
+  c.grid = std::min(c.m_tiles * c.n_tiles, sms);
+  *cfg = c;
+  return SAR_OK;
+}
+
+int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMap& w_map, int M, int N,
+                int K, int epi, void* c, const void* residual, int* err, cudaStream_t s) {
+  const void* fn = pick_kernel(epi, cfg.swap != 0, cfg.msub);
+  if (!fn) return set_error(SAR_ERR_INVALID_ARG, "gemm: unknown epilogue");
+  if (epi == SAR_EPI_RESIDUAL && residual == nullptr)
+    return set_error(SAR_ERR_INVALID_ARG, "gemm: residual epilogue without residual");
+  Params p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.bn = cfg.bn;
+  p.m_tiles = cfg.m_tiles;
+  p.n_tiles = cfg.n_tiles;
+  p.k_blocks = K / kBK;
+  p.stages = cfg.stages;
+  p.stage_bytes = cfg.msub * kTileA + cfg.bn * kBK * 2;
+  p.tmem_cols = pow2_at_least(2 * cfg.msub * cfg.bn);
+  p.c = c;
+  p.r = residual;
+  p.err = err;
+  static bool attr_done[4][2][3] = {};
+  bool& done = attr_done[epi][cfg.swap][cfg.msub];
+  if (!done) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (e != cudaSuccess) return cuda_error(e, "gemm: set smem attribute");
+    done = true;
+  }
+  const CUtensorMap& ta = cfg.swap ? w_map : act_map;
+  const CUtensorMap& tb = cfg.swap ? act_map : w_map;
+  void* args[] = {const_cast<CUtensorMap*>(&ta), const_cast<CUtensorMap*>(&tb), &p};
+  cudaError_t e = cudaLaunchKernel(fn, dim3(cfg.grid), dim3(kThreads), args, (size_t)cfg.smem, s);
+  if (e != cudaSuccess) return cuda_error(e, "gemm launch");
+  count_launches(1);
+  return SAR_OK;
+}
+
+}  // namespace sar

@@ -1,0 +1,100 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/sar.h"
+#include "../../include/sar_ops.h"
+
+namespace sar {
+
+// ---- errors / bookkeeping (api.cpp) ----------------------------------------
+int set_error(int code, const std::string& msg);
+int cuda_error(cudaError_t e, const char* what);
+void count_launches(int64_t n);
+int num_sms();
+
+// ---- GEMM (gemm_tc.cu) -----------------------------------------------------
+
+// Encodes a 2D bf16 tensor map over row-major [rows, cols] with a
+// 64-column x box_rows box and 128-byte swizzle.
+int make_tmap_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
+                   uint32_t box_rows);
+
+struct GemmCfg {
+  int swap = 0;     // weights on the MMA M side
+  int msub = 1;     // 128-row A sub-tiles per tile (non-swap only)
+  int bn = 256;     // MMA N extent: weight rows (non-swap) or token rows (swap)
+  int m_tiles = 0;  // tiles along the token dimension
+  int n_tiles = 0;  // tiles along the weight-row dimension
+  int stages = 0;
+  int smem = 0;
+  int grid = 0;
+  // box rows the two tensor maps must be encoded with
+  int a_box_rows = 128;
+  int b_box_rows = 256;
+};
+
+// Picks a tiling for C[M, .] = A[M, K] . W[N, K]^T (variant = SAR_GEMM_*).
+// Returns SAR_OK or SAR_ERR_UNSUPPORTED.
+int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg);
+
+// Launches with maps already encoded: `act_map` over the activations (rows M),
+// `w_map` over the weights; which one is the MMA's A operand depends on cfg.swap.
+int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMap& w_map, int M,
+                int N, int K, int epi, void* c, const void* residual, int* err, cudaStream_t s);
+
+// ---- elementwise kernels (elementwise.cu) ----------------------------------
+int launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* gain, __nv_bfloat16* y, int rows,
+                   int hidden, float eps, const int32_t* row_index, cudaStream_t s);
+int launch_embed(const int32_t* tokens, const __nv_bfloat16* table, __nv_bfloat16* out, int rows,
+                 int hidden, int vocab, int* err, cudaStream_t s);
+struct RopeArgs {
+  __nv_bfloat16* qkv;        // [M, (qh + 2 kvh) * d]
+  const int32_t* pos;        // [M]
+  const int32_t* slot;       // [M] page * page_size + offset
+  const double* inv_freq;    // [d/2]
+  __nv_bfloat16* k_cache;    // layer base [num_pages][kvh][page][d]
+  __nv_bfloat16* v_cache;
+  int M, qh, kvh, d, page_size, num_pages;
+  int* err;
+};
+int launch_rope_append(const RopeArgs& a, cudaStream_t s);
+int launch_argmax(const float* logits, int rows, int vocab, int32_t* out, cudaStream_t s);
+
+// ---- attention (attn_decode.cu, attn_chunk.cu) -----------------------------
+struct DecodeAttnArgs {
+  const __nv_bfloat16* qkv;  // decode rows start here; row stride ld
+  __nv_bfloat16* out;        // decode rows of the attention output; row stride ld_out
+  const __nv_bfloat16* k_cache;
+  const __nv_bfloat16* v_cache;
+  const int32_t* items;      // [n_items][4]: decode b, key_begin, key_end, part (-1 = final)
+  const int32_t* nkeys;      // [n_decode] keys each decode attends to (ctx + 1)
+  const int32_t* bt_off;     // [n_decode] offset into bt
+  const int32_t* bt_len;     // [n_decode]
+  const int32_t* bt;         // flattened block tables
+  const int32_t* parts_begin;  // [n_decode] first partial index (or -1)
+  const int32_t* parts_count;  // [n_decode]
+  float* partials;           // [n_parts][qh][d + 2]
+  int n_items, n_decode, ld, ld_out, qh, kvh, d, page_size, num_pages;
+  int* err;
+};
+int launch_decode_attention(const DecodeAttnArgs& a, cudaStream_t s);
+
+struct ChunkAttnArgs {
+  const __nv_bfloat16* qkv;  // chunk rows [0, len); row stride ld
+  __nv_bfloat16* out;        // [len, qh*d]; row stride ld_out
+  const __nv_bfloat16* k_cache;
+  const __nv_bfloat16* v_cache;
+  const int32_t* bt;         // block table of the prompt
+  int bt_len, start_pos, len, ld, ld_out, qh, kvh, d, page_size, num_pages;
+  int* err;
+};
+int launch_chunk_attention(const ChunkAttnArgs& a, cudaStream_t s);
+
+}  // namespace sar

@@ -1,0 +1,746 @@
+// Model, paged KV cache and the hybrid step: host orchestration of the kernels.
+//
+// One step ("SARATHI: Efficient LLM Inference by Piggybacking Decodes with
+// Chunked Prefills", reading notes, part 2 section 3 -- merge, split, merge):
+//   rows [0, Lp) are the prefill chunk, rows [Lp, Lp+Bd) the decodes, all in
+//   one [M, H] residual buffer; per layer
+//     RMSNorm -> QKV GEMM (all rows) -> rotary + KV-page append (all rows) ->
+//     chunk attention on rows [0, Lp) | decode attention on rows [Lp, M),
+//     both reading the pages and writing disjoint row ranges of one buffer ->
+//     O GEMM + residual -> RMSNorm -> gate/up GEMM with SiLU*up epilogue ->
+//     down GEMM + residual;
+//   then the final norm on the rows whose next token is sampled and the LM head.
+// The per-step metadata (positions, page slots, block tables, the decode
+// work split) is planned on the host and shipped in one async copy.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+using sar::set_error;
+using sar::cuda_error;
+
+namespace {
+
+constexpr int kMetaRing = 4;
+
+struct LayerW {
+  __nv_bfloat16 *wqkv = nullptr, *wo = nullptr, *wgu = nullptr, *wd = nullptr;
+  __nv_bfloat16 *n1 = nullptr, *n2 = nullptr;
+  CUtensorMap m_qkv[2], m_o[2], m_gu[2], m_d[2];  // weight maps, box rows 128 / 256
+  bool set = false;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct EventPair {
+  cudaEvent_t a = nullptr, b = nullptr;
+  int kind = 0;
+};
+
+}  // namespace
+
+struct sar_model {
+  sar_dims d{};
+  int qkv_n = 0;        // (qh + 2 kvh) * head_dim
+  int qd = 0, kvd = 0;  // q width, kv width
+  uint8_t* arena = nullptr;
+  std::vector<LayerW> L;
+  __nv_bfloat16 *embed = nullptr, *final_norm = nullptr, *lm_head = nullptr;
+  CUtensorMap m_head[2];
+  bool head_set = false;
+  double* inv_freq = nullptr;
+  // workspace
+  uint8_t* ws = nullptr;
+  __nv_bfloat16 *xn = nullptr, *qkv = nullptr, *attn = nullptr, *act = nullptr, *hres = nullptr,
+                *hrows = nullptr, *in_stage = nullptr;
+  float* partials = nullptr;
+  size_t partials_cap = 0;  // floats
+  float* logits_stage = nullptr;
+  int* err = nullptr;
+  // step metadata: pinned host ring + device buffer
+  int32_t* meta_host[kMetaRing] = {};
+  cudaEvent_t meta_ev[kMetaRing] = {};
+  size_t meta_cap = 0;  // int32 elements per buffer
+  int meta_slot = 0;
+  int32_t* meta_dev = nullptr;
+  size_t meta_dev_cap = 0;
+  // profiling
+  bool prof = false;
+  std::vector<EventPair> ev_used, ev_free;
+  double prof_ms[SAR_K_COUNT] = {};
+  int64_t prof_n[SAR_K_COUNT] = {};
+};
+
+struct sar_kv {
+  const sar_model* m = nullptr;
+  int page_size = 0, num_pages = 0;
+  __nv_bfloat16 *k = nullptr, *v = nullptr;
+  size_t layer_elems = 0;
+};
+
+namespace {
+
+int check(cudaError_t e, const char* what) { return cuda_error(e, what); }
+
+#define SAR_TRY(x)                  \
+  do {                              \
+    int _rc = (x);                  \
+    if (_rc != SAR_OK) return _rc;  \
+  } while (0)
+
+// ---- profiling helpers -----------------------------------------------------
+EventPair* prof_begin(sar_model* m, int kind, cudaStream_t s) {
+  if (!m->prof) return nullptr;
+  EventPair ep;
+  if (!m->ev_free.empty()) {
+    ep = m->ev_free.back();
+    m->ev_free.pop_back();
+  } else {
+    cudaEventCreate(&ep.a);
+    cudaEventCreate(&ep.b);
+  }
+  ep.kind = kind;
+  cudaEventRecord(ep.a, s);
+  m->ev_used.push_back(ep);
+  return &m->ev_used.back();
+}
+void prof_end(sar_model* m, cudaStream_t s) {
+  if (!m->prof || m->ev_used.empty()) return;
+  cudaEventRecord(m->ev_used.back().b, s);
+}
+
+struct Prof {
+  sar_model* m;
+  cudaStream_t s;
+  Prof(sar_model* m_, int kind, cudaStream_t s_) : m(m_), s(s_) { prof_begin(m, kind, s); }
+  ~Prof() { prof_end(m, s); }
+};
+
+int weight_maps(CUtensorMap (&maps)[2], const void* w, int rows, int cols) {
+  SAR_TRY(sar::make_tmap_bf16(&maps[0], w, rows, cols, 128));
+  SAR_TRY(sar::make_tmap_bf16(&maps[1], w, rows, cols, 256));
+  return SAR_OK;
+}
+
+// GEMM over `rows` activation rows with the weight maps of one matrix.
+int run_gemm(sar_model* m, const __nv_bfloat16* a, int rows, const CUtensorMap (&wmaps)[2], int N, int K,
+             int epi, void* c, const void* r, cudaStream_t s) {
+  sar::GemmCfg cfg;
+  SAR_TRY(sar::gemm_config(rows, N, K, epi, SAR_GEMM_AUTO, &cfg));
+  CUtensorMap amap;
+  SAR_TRY(sar::make_tmap_bf16(&amap, a, rows, K, cfg.swap ? cfg.b_box_rows : cfg.a_box_rows));
+  const CUtensorMap& wm = cfg.swap ? wmaps[0] : wmaps[cfg.bn == 256 ? 1 : 0];
+  return sar::gemm_launch(cfg, amap, wm, rows, N, K, epi, c, r, m->err, s);
+}
+
+// ---- step planning -----------------------------------------------------------
+struct Plan {
+  int M = 0, Lp = 0, Bd = 0, R = 0;
+  // offsets into the metadata block (int32 elements)
+  size_t o_pos = 0, o_slot = 0, o_pbt = 0, o_nkeys = 0, o_btoff = 0, o_btlen = 0, o_pbeg = 0, o_pcnt = 0,
+         o_items = 0, o_bt = 0, o_rows = 0, total = 0;
+  int n_items = 0, n_parts = 0, pbt_len = 0;
+};
+
+int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* p, std::vector<int32_t>* meta) {
+  const sar_dims& d = m->d;
+  if (b->n_decode < 0 || (b->n_decode > 0 && !b->decode)) return set_error(SAR_ERR_INVALID_ARG, "step: bad decode list");
+  const int Lp = b->has_prefill ? b->prefill.len : 0;
+  if (b->has_prefill && (b->prefill.len <= 0 || b->prefill.start_pos < 0 || !b->prefill.block_table))
+    return set_error(SAR_ERR_INVALID_ARG, "step: bad prefill chunk");
+  const int Bd = b->n_decode;
+  const int M = Lp + Bd;
+  if (M == 0) return set_error(SAR_ERR_INVALID_ARG, "step: empty batch");
+  if (M > d.max_tokens) return set_error(SAR_ERR_INVALID_ARG, "step: Lp + Bd exceeds max_tokens");
+  if (Bd > d.max_decodes) return set_error(SAR_ERR_INVALID_ARG, "step: Bd exceeds max_decodes");
+  if (b->in_kind != SAR_IN_HIDDEN && b->in_kind != SAR_IN_TOKENS) return set_error(SAR_ERR_INVALID_ARG, "step: bad in_kind");
+  if (b->in_kind == SAR_IN_TOKENS && (d.vocab == 0 || !m->embed)) return set_error(SAR_ERR_INVALID_ARG, "step: token input without an embedding");
+  const int ps = kv->page_size;
+  auto check_bt = [&](const int32_t* bt, int nb, int last_pos) -> int {
+    if (nb < 0 || (int64_t)nb * ps <= last_pos) return set_error(SAR_ERR_INVALID_ARG, "step: block table does not cover the positions");
+    const int need = last_pos / ps + 1;
+    for (int i = 0; i < need; ++i)
+      if (bt[i] < 0 || bt[i] >= kv->num_pages) return set_error(SAR_ERR_BOUNDS, "step: page id out of range");
+    return SAR_OK;
+  };
+  if (b->has_prefill) SAR_TRY(check_bt(b->prefill.block_table, b->prefill.n_blocks, b->prefill.start_pos + Lp - 1));
+  int64_t total_keys = 0;
+  for (int i = 0; i < Bd; ++i) {
+    const sar_decode& dc = b->decode[i];
+    if (dc.ctx_len < 0 || !dc.block_table) return set_error(SAR_ERR_INVALID_ARG, "step: bad decode entry");
+    SAR_TRY(check_bt(dc.block_table, dc.n_blocks, dc.ctx_len));
+    total_keys += dc.ctx_len + 1;
+  }
+  // decode work split: key ranges of `split` keys, enough CTAs to fill the GPU
+  const int sms = sar::num_sms();
+  int64_t split = (total_keys * d.n_kv_heads) / (8LL * sms);
+  split = std::max<int64_t>(128, std::min<int64_t>(1024, (split + 15) / 16 * 16));
+  std::vector<int32_t> items, pbeg(Bd, -1), pcnt(Bd, 0), nkeys(Bd), btoff(Bd), btlen(Bd), bt;
+  std::vector<int32_t> tail_items;
+  int n_parts = 0;
+  for (int i = 0; i < Bd; ++i) {
+    const sar_decode& dc = b->decode[i];
+    const int nk = dc.ctx_len + 1;
+    nkeys[i] = nk;
+    btoff[i] = (int32_t)bt.size();
+    const int nb = (dc.ctx_len / ps) + 1;
+    btlen[i] = nb;
+    bt.insert(bt.end(), dc.block_table, dc.block_table + nb);
+    const int ns = (int)((nk + split - 1) / split);
+    pcnt[i] = ns;
+    if (ns > 1) {
+      pbeg[i] = n_parts;
+    }
+    for (int sidx = 0; sidx < ns; ++sidx) {
+      const int k0 = (int)(sidx * split), k1 = std::min<int>(nk, (int)((sidx + 1) * split));
+      const int part = ns > 1 ? n_parts + sidx : -1;
+      auto& dst = (k1 - k0 == split) ? items : tail_items;  // full ranges first
+      dst.insert(dst.end(), {i, k0, k1, part});
+    }
+    if (ns > 1) n_parts += ns;
+  }
+  items.insert(items.end(), tail_items.begin(), tail_items.end());
+  // rows whose logits are returned: the chunk's last row, then every decode row
+  std::vector<int32_t> rows;
+  if (Lp > 0) rows.push_back(Lp - 1);
+  for (int i = 0; i < Bd; ++i) rows.push_back(Lp + i);
+
+  p->M = M;
+  p->Lp = Lp;
+  p->Bd = Bd;
+  p->R = (int)rows.size();
+  p->n_items = (int)items.size() / 4;
+  p->n_parts = n_parts;
+  p->pbt_len = b->has_prefill ? (b->prefill.start_pos + Lp - 1) / ps + 1 : 0;
+  size_t o = 0;
+  auto take = [&](size_t n) { size_t r = o; o += (n + 3) & ~size_t(3); return r; };  // 16-byte aligned pieces
+  p->o_pos = take(M);
+  p->o_slot = take(M);
+  p->o_pbt = take(p->pbt_len);
+  p->o_nkeys = take(Bd);
+  p->o_btoff = take(Bd);
+  p->o_btlen = take(Bd);
+  p->o_pbeg = take(Bd);
+  p->o_pcnt = take(Bd);
+  p->o_items = take(items.size());
+  p->o_bt = take(bt.size());
+  p->o_rows = take(rows.size());
+  p->total = o;
+  meta->assign(o, 0);
+  int32_t* mt = meta->data();
+  for (int i = 0; i < Lp; ++i) {
+    const int pos = b->prefill.start_pos + i;
+    mt[p->o_pos + i] = pos;
+    mt[p->o_slot + i] = b->prefill.block_table[pos / ps] * ps + pos % ps;
+  }
+  for (int i = 0; i < Bd; ++i) {
+    const int pos = b->decode[i].ctx_len;
+    mt[p->o_pos + Lp + i] = pos;
+    mt[p->o_slot + Lp + i] = b->decode[i].block_table[pos / ps] * ps + pos % ps;
+  }
+  if (p->pbt_len) std::memcpy(mt + p->o_pbt, b->prefill.block_table, p->pbt_len * 4);
+  std::memcpy(mt + p->o_nkeys, nkeys.data(), Bd * 4);
+  std::memcpy(mt + p->o_btoff, btoff.data(), Bd * 4);
+  std::memcpy(mt + p->o_btlen, btlen.data(), Bd * 4);
+  std::memcpy(mt + p->o_pbeg, pbeg.data(), Bd * 4);
+  std::memcpy(mt + p->o_pcnt, pcnt.data(), Bd * 4);
+  std::memcpy(mt + p->o_items, items.data(), items.size() * 4);
+  std::memcpy(mt + p->o_bt, bt.data(), bt.size() * 4);
+  std::memcpy(mt + p->o_rows, rows.data(), rows.size() * 4);
+  return SAR_OK;
+}
+
+int ensure_meta(sar_model* m, size_t n) {
+  if (n > m->meta_cap) {
+    for (int i = 0; i < kMetaRing; ++i) {
+      if (m->meta_host[i]) {
+        cudaEventSynchronize(m->meta_ev[i]);
+        cudaFreeHost(m->meta_host[i]);
+        m->meta_host[i] = nullptr;
+      }
+    }
+    size_t cap = std::max<size_t>(n * 2, 1 << 16);
+    for (int i = 0; i < kMetaRing; ++i)
+      SAR_TRY(check(cudaMallocHost(&m->meta_host[i], cap * 4), "meta pinned buffer"));
+    m->meta_cap = cap;
+  }
+  if (n > m->meta_dev_cap) {
+    if (m->meta_dev) {
+      SAR_TRY(check(cudaDeviceSynchronize(), "meta resize sync"));
+      cudaFree(m->meta_dev);
+      m->meta_dev = nullptr;
+    }
+    size_t cap = std::max<size_t>(n * 2, 1 << 16);
+    SAR_TRY(check(cudaMalloc(&m->meta_dev, cap * 4), "meta device buffer"));
+    m->meta_dev_cap = cap;
+  }
+  return SAR_OK;
+}
+
+int ensure_partials(sar_model* m, size_t floats) {
+  if (floats <= m->partials_cap) return SAR_OK;
+  if (m->partials) {
+    SAR_TRY(check(cudaDeviceSynchronize(), "partials resize sync"));
+    cudaFree(m->partials);
+    m->partials = nullptr;
+  }
+  size_t cap = std::max<size_t>(floats * 2, 1 << 20);
+  SAR_TRY(check(cudaMalloc(&m->partials, cap * 4), "decode partials"));
+  m->partials_cap = cap;
+  return SAR_OK;
+}
+
+// The step proper, on device buffers.
+int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, __nv_bfloat16* h,
+             float* logits, void* layer_out, cudaStream_t s) {
+  const sar_dims& d = m->d;
+  for (int l = 0; l < d.n_layers; ++l)
+    if (!m->L[l].set) return set_error(SAR_ERR_INVALID_ARG, "step: layer weights not set");
+  if (logits && (d.vocab == 0 || !m->head_set)) return set_error(SAR_ERR_INVALID_ARG, "step: logits requested without a head");
+  Plan p;
+  std::vector<int32_t> meta;
+  SAR_TRY(validate_and_plan(m, kv, b, &p, &meta));
+  SAR_TRY(ensure_meta(m, p.total));
+  SAR_TRY(ensure_partials(m, (size_t)std::max(p.n_parts, 1) * d.n_q_heads * (d.head_dim + 2)));
+  // stage the metadata through a pinned ring buffer
+  const int slot = m->meta_slot;
+  m->meta_slot = (slot + 1) % kMetaRing;
+  SAR_TRY(check(cudaEventSynchronize(m->meta_ev[slot]), "meta ring wait"));
+  std::memcpy(m->meta_host[slot], meta.data(), p.total * 4);
+  SAR_TRY(check(cudaMemcpyAsync(m->meta_dev, m->meta_host[slot], p.total * 4, cudaMemcpyHostToDevice, s), "meta copy"));
+  SAR_TRY(check(cudaEventRecord(m->meta_ev[slot], s), "meta event"));
+  const int32_t* md = m->meta_dev;
+  const int M = p.M, H = d.hidden;
+
+  // a0: stacked rows (chunk first, then decodes)
+  {
+    Prof pr(m, SAR_K_EMBED, s);
+    if (b->in_kind == SAR_IN_TOKENS) {
+      SAR_TRY(sar::launch_embed(static_cast<const int32_t*>(in), m->embed, h, M, H, d.vocab, m->err, s));
+    } else if (in != h) {
+      SAR_TRY(check(cudaMemcpyAsync(h, in, (size_t)M * H * 2, cudaMemcpyDeviceToDevice, s), "input copy"));
+    }
+  }
+  for (int l = 0; l < d.n_layers; ++l) {
+    LayerW& w = m->L[l];
+    {
+      Prof pr(m, SAR_K_RMSNORM, s);
+      SAR_TRY(sar::launch_rmsnorm(h, w.n1, m->xn, M, H, d.rms_eps, nullptr, s));
+    }
+    {
+      Prof pr(m, SAR_K_GEMM_QKV, s);
+      SAR_TRY(run_gemm(m, m->xn, M, w.m_qkv, m->qkv_n, H, SAR_EPI_BF16, m->qkv, nullptr, s));
+    }
+    __nv_bfloat16* kc = kv->k + (size_t)l * kv->layer_elems;
+    __nv_bfloat16* vc = kv->v + (size_t)l * kv->layer_elems;
+    {
+      Prof pr(m, SAR_K_ROPE_APPEND, s);
+      sar::RopeArgs ra;
+      ra.qkv = m->qkv;
+      ra.pos = md + p.o_pos;
+      ra.slot = md + p.o_slot;
+      ra.inv_freq = m->inv_freq;
+      ra.k_cache = kc;
+      ra.v_cache = vc;
+      ra.M = M;
+      ra.qh = d.n_q_heads;
+      ra.kvh = d.n_kv_heads;
+      ra.d = d.head_dim;
+      ra.page_size = kv->page_size;
+      ra.num_pages = kv->num_pages;
+      ra.err = m->err;
+      SAR_TRY(sar::launch_rope_append(ra, s));
+    }
+    if (p.Lp > 0) {
+      Prof pr(m, SAR_K_CHUNK_ATTN, s);
+      sar::ChunkAttnArgs ca;
+      ca.qkv = m->qkv;
+      ca.out = m->attn;
+      ca.k_cache = kc;
+      ca.v_cache = vc;
+      ca.bt = md + p.o_pbt;
+      ca.bt_len = p.pbt_len;
+      ca.start_pos = b->prefill.start_pos;
+      ca.len = p.Lp;
+      ca.ld = m->qkv_n;
+      ca.ld_out = m->qd;
+      ca.qh = d.n_q_heads;
+      ca.kvh = d.n_kv_heads;
+      ca.d = d.head_dim;
+      ca.page_size = kv->page_size;
+      ca.num_pages = kv->num_pages;
+      ca.err = m->err;
+      SAR_TRY(sar::launch_chunk_attention(ca, s));
+    }
+    if (p.Bd > 0) {
+      Prof pr(m, SAR_K_DECODE_ATTN, s);
+      sar::DecodeAttnArgs da;
+      da.qkv = m->qkv + (size_t)p.Lp * m->qkv_n;  // zero-copy row split
+      da.out = m->attn + (size_t)p.Lp * m->qd;
+      da.k_cache = kc;
+      da.v_cache = vc;
+      da.items = md + p.o_items;
+      da.nkeys = md + p.o_nkeys;
+      da.bt_off = md + p.o_btoff;
+      da.bt_len = md + p.o_btlen;
+      da.bt = md + p.o_bt;
+      da.parts_begin = md + p.o_pbeg;
+      da.parts_count = md + p.o_pcnt;
+      da.partials = p.n_parts > 0 ? m->partials : nullptr;
+      da.n_items = p.n_items;
+      da.n_decode = p.Bd;
+      da.ld = m->qkv_n;
+      da.ld_out = m->qd;
+      da.qh = d.n_q_heads;
+      da.kvh = d.n_kv_heads;
+      da.d = d.head_dim;
+      da.page_size = kv->page_size;
+      da.num_pages = kv->num_pages;
+      da.err = m->err;
+      SAR_TRY(sar::launch_decode_attention(da, s));
+    }
+    {
+      Prof pr(m, SAR_K_GEMM_O, s);
+      SAR_TRY(run_gemm(m, m->attn, M, w.m_o, H, m->qd, SAR_EPI_RESIDUAL, h, h, s));
+    }
+    {
+      Prof pr(m, SAR_K_RMSNORM, s);
+      SAR_TRY(sar::launch_rmsnorm(h, w.n2, m->xn, M, H, d.rms_eps, nullptr, s));
+    }
+    {
+      Prof pr(m, SAR_K_GEMM_GATEUP, s);
+      SAR_TRY(run_gemm(m, m->xn, M, w.m_gu, 2 * d.ffn, H, SAR_EPI_SWIGLU, m->act, nullptr, s));
+    }
+    {
+      Prof pr(m, SAR_K_GEMM_DOWN, s);
+      SAR_TRY(run_gemm(m, m->act, M, w.m_d, H, d.ffn, SAR_EPI_RESIDUAL, h, h, s));
+    }
+    if (layer_out)
+      SAR_TRY(check(cudaMemcpyAsync(static_cast<__nv_bfloat16*>(layer_out) + (size_t)l * M * H, h, (size_t)M * H * 2,
+                                    cudaMemcpyDeviceToDevice, s),
+                    "layer output copy"));
+  }
+  if (logits) {
+    {
+      Prof pr(m, SAR_K_HEAD_NORM, s);
+      SAR_TRY(sar::launch_rmsnorm(h, m->final_norm, m->hrows, p.R, H, d.rms_eps, md + p.o_rows, s));
+    }
+    {
+      Prof pr(m, SAR_K_GEMM_HEAD, s);
+      SAR_TRY(run_gemm(m, m->hrows, p.R, m->m_head, d.vocab, H, SAR_EPI_F32, logits, nullptr, s));
+    }
+  }
+  return SAR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sar_model_create(const sar_dims* dims, sar_model** out) {
+  if (!dims || !out) return set_error(SAR_ERR_INVALID_ARG, "model: null argument");
+  const sar_dims& d = *dims;
+  if (d.n_layers <= 0 || d.hidden <= 0 || d.n_q_heads <= 0 || d.n_kv_heads <= 0 || d.ffn <= 0 || d.vocab < 0 ||
+      d.max_tokens <= 0 || d.max_decodes < 0 || d.max_decodes > d.max_tokens)
+    return set_error(SAR_ERR_INVALID_ARG, "model: bad dims");
+  if (d.head_dim != 64 && d.head_dim != 128) return set_error(SAR_ERR_UNSUPPORTED, "model: head_dim must be 64 or 128");
+  if (d.n_q_heads % d.n_kv_heads || d.n_q_heads / d.n_kv_heads > 8)
+    return set_error(SAR_ERR_UNSUPPORTED, "model: n_q_heads must be 1..8 times n_kv_heads");
+  if (d.hidden % 64 || d.ffn % 64 || (d.n_q_heads * d.head_dim) % 64 || (d.n_kv_heads * d.head_dim) % 64)
+    return set_error(SAR_ERR_UNSUPPORTED, "model: widths must be multiples of 64");
+  sar_model* m = new sar_model();
+  m->d = d;
+  m->qd = d.n_q_heads * d.head_dim;
+  m->kvd = d.n_kv_heads * d.head_dim;
+  m->qkv_n = m->qd + 2 * m->kvd;
+  const size_t H = d.hidden, F = d.ffn;
+  const size_t per_layer = align256((size_t)m->qkv_n * H * 2) + align256(H * m->qd * 2) + align256(2 * F * H * 2) +
+                           align256(H * F * 2) + 2 * align256(H * 2);
+  const size_t head = d.vocab ? 2 * align256((size_t)d.vocab * H * 2) + align256(H * 2) : 0;
+  cudaError_t e = cudaMalloc(&m->arena, per_layer * d.n_layers + head);
+  if (e != cudaSuccess) {
+    delete m;
+    return cuda_error(e, "model: weight arena");
+  }
+  m->L.resize(d.n_layers);
+  uint8_t* p = m->arena;
+  auto take = [&](size_t bytes) { uint8_t* r = p; p += align256(bytes); return reinterpret_cast<__nv_bfloat16*>(r); };
+  for (int l = 0; l < d.n_layers; ++l) {
+    LayerW& w = m->L[l];
+    w.wqkv = take((size_t)m->qkv_n * H * 2);
+    w.wo = take(H * m->qd * 2);
+    w.wgu = take(2 * F * H * 2);
+    w.wd = take(H * F * 2);
+    w.n1 = take(H * 2);
+    w.n2 = take(H * 2);
+  }
+  if (d.vocab) {
+    m->embed = take((size_t)d.vocab * H * 2);
+    m->lm_head = take((size_t)d.vocab * H * 2);
+    m->final_norm = take(H * 2);
+  }
+  // step workspace
+  const size_t T = d.max_tokens;
+  const size_t R = (size_t)d.max_decodes + 1;
+  const size_t ws = align256(T * H * 2) + align256(T * m->qkv_n * 2) + align256(T * m->qd * 2) + align256(T * F * 2) +
+                    align256(T * H * 2) + align256(R * H * 2) + align256(T * H * 2) + 256;
+  e = cudaMalloc(&m->ws, ws);
+  if (e == cudaSuccess) e = cudaMalloc(&m->err, 16);
+  if (e == cudaSuccess) e = cudaMemset(m->err, 0, 16);
+  if (e == cudaSuccess) e = cudaMalloc(&m->inv_freq, d.head_dim / 2 * sizeof(double));
+  if (e != cudaSuccess) {
+    sar_model_destroy(m);
+    return cuda_error(e, "model: workspace");
+  }
+  p = m->ws;
+  m->xn = take(T * H * 2);
+  m->qkv = take(T * m->qkv_n * 2);
+  m->attn = take(T * m->qd * 2);
+  m->act = take(T * F * 2);
+  m->hres = take(T * H * 2);
+  m->hrows = take(R * H * 2);
+  m->in_stage = take(T * H * 2);
+  // rotary frequencies base^(-2i/d), double precision
+  std::vector<double> inv(d.head_dim / 2);
+  for (int i = 0; i < d.head_dim / 2; ++i) inv[i] = std::pow((double)d.rope_base, -2.0 * i / d.head_dim);
+  e = cudaMemcpy(m->inv_freq, inv.data(), inv.size() * sizeof(double), cudaMemcpyHostToDevice);
+  for (int i = 0; i < kMetaRing && e == cudaSuccess; ++i) {
+    e = cudaEventCreateWithFlags(&m->meta_ev[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(m->meta_ev[i], 0);
+  }
+  if (e != cudaSuccess) {
+    sar_model_destroy(m);
+    return cuda_error(e, "model: init");
+  }
+  *out = m;
+  return SAR_OK;
+}
+
+int sar_model_set_layer(sar_model* m, int32_t layer, const sar_layer_weights* w, void* stream) {
+  if (!m || !w || layer < 0 || layer >= m->d.n_layers) return set_error(SAR_ERR_INVALID_ARG, "set_layer: bad argument");
+  if (!w->wq || !w->wk || !w->wv || !w->wo || !w->wg || !w->wu || !w->wd || !w->norm1 || !w->norm2)
+    return set_error(SAR_ERR_INVALID_ARG, "set_layer: null weight");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LayerW& L = m->L[layer];
+  const size_t H = m->d.hidden, F = m->d.ffn;
+  auto cp = [&](void* dst, const void* src, size_t bytes) {
+    return check(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s), "set_layer copy");
+  };
+  SAR_TRY(cp(L.wqkv, w->wq, (size_t)m->qd * H * 2));
+  SAR_TRY(cp(L.wqkv + (size_t)m->qd * H, w->wk, (size_t)m->kvd * H * 2));
+  SAR_TRY(cp(L.wqkv + (size_t)(m->qd + m->kvd) * H, w->wv, (size_t)m->kvd * H * 2));
+  SAR_TRY(cp(L.wo, w->wo, H * m->qd * 2));
+  // gate/up interleaved in 64-row blocks: [g 64][u 64][g 64][u 64]...
+  const size_t blk = 64 * H * 2;
+  SAR_TRY(check(cudaMemcpy2DAsync(L.wgu, 2 * blk, w->wg, blk, blk, F / 64, cudaMemcpyDeviceToDevice, s), "gate pack"));
+  SAR_TRY(check(cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(L.wgu) + blk, 2 * blk, w->wu, blk, blk, F / 64,
+                                  cudaMemcpyDeviceToDevice, s),
+                "up pack"));
+  SAR_TRY(cp(L.wd, w->wd, H * F * 2));
+  SAR_TRY(cp(L.n1, w->norm1, H * 2));
+  SAR_TRY(cp(L.n2, w->norm2, H * 2));
+  SAR_TRY(weight_maps(L.m_qkv, L.wqkv, m->qkv_n, H));
+  SAR_TRY(weight_maps(L.m_o, L.wo, H, m->qd));
+  SAR_TRY(weight_maps(L.m_gu, L.wgu, 2 * F, H));
+  SAR_TRY(weight_maps(L.m_d, L.wd, H, F));
+  L.set = true;
+  return SAR_OK;
+}
+
+int sar_model_set_head(sar_model* m, const void* embed, const void* final_norm, const void* lm_head, void* stream) {
+  if (!m) return set_error(SAR_ERR_INVALID_ARG, "set_head: null model");
+  if (m->d.vocab == 0) return set_error(SAR_ERR_INVALID_ARG, "set_head: model has no vocabulary");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t H = m->d.hidden, V = m->d.vocab;
+  if (embed) SAR_TRY(check(cudaMemcpyAsync(m->embed, embed, V * H * 2, cudaMemcpyDeviceToDevice, s), "embed copy"));
+  if (final_norm) SAR_TRY(check(cudaMemcpyAsync(m->final_norm, final_norm, H * 2, cudaMemcpyDeviceToDevice, s), "norm copy"));
+  if (lm_head) {
+    SAR_TRY(check(cudaMemcpyAsync(m->lm_head, lm_head, V * H * 2, cudaMemcpyDeviceToDevice, s), "head copy"));
+    SAR_TRY(weight_maps(m->m_head, m->lm_head, (int)V, (int)H));
+  }
+  if (final_norm && lm_head) m->head_set = true;
+  return SAR_OK;
+}
+
+int sar_model_destroy(sar_model* m) {
+  if (!m) return SAR_OK;
+  cudaDeviceSynchronize();
+  for (int i = 0; i < kMetaRing; ++i) {
+    if (m->meta_host[i]) cudaFreeHost(m->meta_host[i]);
+    if (m->meta_ev[i]) cudaEventDestroy(m->meta_ev[i]);
+  }
+  for (auto& ep : m->ev_used) { cudaEventDestroy(ep.a); cudaEventDestroy(ep.b); }
+  for (auto& ep : m->ev_free) { cudaEventDestroy(ep.a); cudaEventDestroy(ep.b); }
+  cudaFree(m->meta_dev);
+  cudaFree(m->partials);
+  cudaFree(m->inv_freq);
+  cudaFree(m->err);
+  cudaFree(m->ws);
+  cudaFree(m->arena);
+  delete m;
+  return SAR_OK;
+}
+
+int sar_sync_status(sar_model* m) {
+  if (!m) return set_error(SAR_ERR_INVALID_ARG, "sync_status: null model");
+  int h[4] = {0, 0, 0, 0};
+  SAR_TRY(check(cudaDeviceSynchronize(), "sync_status: device synchronise"));
+  SAR_TRY(check(cudaMemcpy(h, m->err, 16, cudaMemcpyDeviceToHost), "sync_status: read flags"));
+  SAR_TRY(check(cudaMemset(m->err, 0, 16), "sync_status: clear flags"));
+  if (h[0] != 0)
+    return set_error(h[0], "device flag: code " + std::to_string(h[0]) + " at site " + std::to_string(h[1]) +
+                               " (detail " + std::to_string(h[2]) + ")");
+  return SAR_OK;
+}
+
+int sar_kv_create(const sar_model* m, int32_t page_size, int32_t num_pages, sar_kv** out) {
+  if (!m || !out) return set_error(SAR_ERR_INVALID_ARG, "kv: null argument");
+  if (page_size != 16 && page_size != 32 && page_size != 64) return set_error(SAR_ERR_INVALID_ARG, "kv: page size must be 16, 32 or 64");
+  if (num_pages <= 0) return set_error(SAR_ERR_INVALID_ARG, "kv: no pages");
+  sar_kv* kv = new sar_kv();
+  kv->m = m;
+  kv->page_size = page_size;
+  kv->num_pages = num_pages;
+  kv->layer_elems = (size_t)num_pages * m->d.n_kv_heads * page_size * m->d.head_dim;
+  const size_t bytes = kv->layer_elems * m->d.n_layers * 2;
+  cudaError_t e = cudaMalloc(&kv->k, bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&kv->v, bytes);
+  if (e == cudaSuccess) e = cudaMemset(kv->k, 0, bytes);
+  if (e == cudaSuccess) e = cudaMemset(kv->v, 0, bytes);
+  if (e != cudaSuccess) {
+    cudaFree(kv->k);
+    cudaFree(kv->v);
+    delete kv;
+    return cuda_error(e, "kv: arena");
+  }
+  *out = kv;
+  return SAR_OK;
+}
+
+int sar_kv_layer_ptr(sar_kv* kv, int32_t layer, int32_t kind, void** out) {
+  if (!kv || !out || layer < 0 || layer >= kv->m->d.n_layers || (kind != 0 && kind != 1))
+    return set_error(SAR_ERR_INVALID_ARG, "kv_layer_ptr: bad argument");
+  *out = (kind == 0 ? kv->k : kv->v) + (size_t)layer * kv->layer_elems;
+  return SAR_OK;
+}
+
+int sar_kv_destroy(sar_kv* kv) {
+  if (!kv) return SAR_OK;
+  cudaDeviceSynchronize();
+  cudaFree(kv->k);
+  cudaFree(kv->v);
+  delete kv;
+  return SAR_OK;
+}
+
+int sar_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, void* hidden_out, float* logits_out,
+             void* layer_out, void* stream) {
+  if (!m || !kv || !b || !in) return set_error(SAR_ERR_INVALID_ARG, "step: null argument");
+  if (kv->m != m) return set_error(SAR_ERR_INVALID_ARG, "step: KV cache belongs to another model");
+  __nv_bfloat16* h = hidden_out ? static_cast<__nv_bfloat16*>(hidden_out) : m->hres;
+  return run_step(m, kv, b, in, h, logits_out, layer_out, static_cast<cudaStream_t>(stream));
+}
+
+int sar_step_host(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, void* hidden_out, float* logits_out,
+                  void* layer_out, void* stream) {
+  if (!m || !kv || !b || !in) return set_error(SAR_ERR_INVALID_ARG, "step_host: null argument");
+  if (layer_out) return set_error(SAR_ERR_INVALID_ARG, "step_host: layer outputs are only returned on device");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int M = (b->has_prefill ? b->prefill.len : 0) + b->n_decode;
+  if (M <= 0 || M > m->d.max_tokens) return set_error(SAR_ERR_INVALID_ARG, "step_host: bad row count");
+  const int R = (b->has_prefill ? 1 : 0) + b->n_decode;
+  const size_t in_bytes = b->in_kind == SAR_IN_TOKENS ? (size_t)M * 4 : (size_t)M * m->d.hidden * 2;
+  SAR_TRY(check(cudaMemcpyAsync(m->in_stage, in, in_bytes, cudaMemcpyHostToDevice, s), "step_host: input copy"));
+  if (logits_out && !m->logits_stage) {
+    SAR_TRY(check(cudaMalloc(&m->logits_stage, (size_t)(m->d.max_decodes + 1) * m->d.vocab * 4), "step_host: logits stage"));
+  }
+  SAR_TRY(run_step(m, kv, b, m->in_stage, m->hres, logits_out ? m->logits_stage : nullptr, nullptr, s));
+  if (hidden_out)
+    SAR_TRY(check(cudaMemcpyAsync(hidden_out, m->hres, (size_t)M * m->d.hidden * 2, cudaMemcpyDeviceToHost, s), "step_host: hidden copy"));
+  if (logits_out)
+    SAR_TRY(check(cudaMemcpyAsync(logits_out, m->logits_stage, (size_t)R * m->d.vocab * 4, cudaMemcpyDeviceToHost, s),
+                  "step_host: logits copy"));
+  return check(cudaStreamSynchronize(s), "step_host: synchronise");
+}
+
+int sar_sample_greedy(sar_model* m, const float* logits, int32_t rows, int32_t* tokens_out, void* stream) {
+  if (!m || !logits || !tokens_out || rows < 0) return set_error(SAR_ERR_INVALID_ARG, "sample: bad argument");
+  if (m->d.vocab == 0) return set_error(SAR_ERR_INVALID_ARG, "sample: model has no vocabulary");
+  return sar::launch_argmax(logits, rows, m->d.vocab, tokens_out, static_cast<cudaStream_t>(stream));
+}
+
+int sar_profile_enable(sar_model* m, int32_t on) {
+  if (!m) return set_error(SAR_ERR_INVALID_ARG, "profile: null model");
+  m->prof = on != 0;
+  return SAR_OK;
+}
+
+int sar_profile_read(sar_model* m, double* ms, int64_t* launches, int32_t n_kinds) {
+  if (!m) return set_error(SAR_ERR_INVALID_ARG, "profile: null model");
+  SAR_TRY(check(cudaDeviceSynchronize(), "profile: synchronise"));
+  for (auto& ep : m->ev_used) {
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, ep.a, ep.b) == cudaSuccess) {
+      m->prof_ms[ep.kind] += t;
+      m->prof_n[ep.kind] += 1;
+    }
+    m->ev_free.push_back(ep);
+  }
+  m->ev_used.clear();
+  for (int k = 0; k < n_kinds && k < SAR_K_COUNT; ++k) {
+    if (ms) ms[k] = m->prof_ms[k];
+    if (launches) launches[k] = m->prof_n[k];
+  }
+  for (int k = 0; k < SAR_K_COUNT; ++k) {
+    m->prof_ms[k] = 0.0;
+    m->prof_n[k] = 0;
+  }
+  return SAR_OK;
+}
+
+int sar_model_debug_buffer(sar_model* m, int32_t which, void** out) {
+  if (!m || !out) return set_error(SAR_ERR_INVALID_ARG, "debug_buffer: null argument");
+  switch (which) {
+    case 0: *out = m->xn; break;
+    case 1: *out = m->qkv; break;
+    case 2: *out = m->attn; break;
+    case 3: *out = m->act; break;
+    case 4: *out = m->hres; break;
+    default: return set_error(SAR_ERR_INVALID_ARG, "debug_buffer: unknown buffer");
+  }
+  return SAR_OK;
+}
+
+// ---- single-kernel entry points ------------------------------------------------
+
+int sar_op_gemm(const void* a, const void* w, void* c, const void* residual, int32_t M, int32_t N, int32_t K,
+                int32_t epilogue, int32_t variant, void* stream) {
+  if (!a || !w || !c) return set_error(SAR_ERR_INVALID_ARG, "op_gemm: null pointer");
+  if (epilogue < SAR_EPI_BF16 || epilogue > SAR_EPI_F32) return set_error(SAR_ERR_INVALID_ARG, "op_gemm: bad epilogue");
+  static int* err = nullptr;
+  if (!err) {
+    SAR_TRY(check(cudaMalloc(&err, 16), "op_gemm: flag buffer"));
+    SAR_TRY(check(cudaMemset(err, 0, 16), "op_gemm: flag buffer"));
+  }
+  sar::GemmCfg cfg;
+  SAR_TRY(sar::gemm_config(M, N, K, epilogue, variant, &cfg));
+  CUtensorMap amap, wmap;
+  SAR_TRY(sar::make_tmap_bf16(&amap, a, M, K, cfg.swap ? cfg.b_box_rows : cfg.a_box_rows));
+  SAR_TRY(sar::make_tmap_bf16(&wmap, w, N, K, cfg.swap ? cfg.a_box_rows : cfg.b_box_rows));
+  return sar::gemm_launch(cfg, amap, wmap, M, N, K, epilogue, c, residual, err, static_cast<cudaStream_t>(stream));
+}
+
+int sar_op_rmsnorm(const void* x, const void* gain, void* y, int32_t rows, int32_t hidden, float eps, void* stream) {
+  if (!x || !gain || !y || rows < 0 || hidden <= 0) return set_error(SAR_ERR_INVALID_ARG, "op_rmsnorm: bad argument");
+  return sar::launch_rmsnorm(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(gain),
+                             static_cast<__nv_bfloat16*>(y), rows, hidden, eps, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,258 @@
+/*
+ * sar.h -- C ABI of the hybrid-batch decoder step (chunked prefill + piggybacked
+ * decodes) for one GB300 GPU.
+ *
+ * The step follows the scheme of "SARATHI: Efficient LLM Inference by
+ * Piggybacking Decodes with Chunked Prefills" (reading notes, part 2 section 3,
+ * "merge / split / merge"): one prefill chunk of Lp tokens and Bd decode tokens
+ * are stacked into a single [Lp+Bd, H] activation; every projection runs as one
+ * GEMM over all rows; attention is split by row range (the chunk attends
+ * causally to its own keys and to the earlier chunks' keys in the paged KV
+ * cache; each decode attends to its own paged history); the two attention
+ * outputs are written back into one contiguous buffer.  The scheduler entry
+ * points restate Algorithm 3 (stall-free batching) of "Taming
+ * Throughput-Latency Tradeoff in LLM Inference with Sarathi-Serve" (section 2,
+ * Q2 item 2; section 3 flowchart).
+ *
+ * Conventions
+ *  - Every call returns an int status (SAR_OK = 0).  On failure
+ *    sar_last_error() returns a thread-local message.  Validation errors are
+ *    returned before anything is launched.
+ *  - "device" pointers are CUDA device addresses on the current device;
+ *    "host" pointers are ordinary host memory.  A stream argument is a
+ *    cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - Matrices are row-major.  Weights use the linear-layer layout
+ *    [out_features, in_features].  Activations are bf16 [rows, hidden].
+ *  - Work on a stream is asynchronous; device-side error flags (a wait that
+ *    gave up, an index out of bounds) are read back by sar_sync_status().
+ */
+#ifndef SAR_H
+#define SAR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+enum {
+  SAR_OK = 0,
+  SAR_ERR_INVALID_ARG = 1, /* bad argument or batch descriptor               */
+  SAR_ERR_NO_PAGES = 2,    /* KV page pool exhausted (scheduler)             */
+  SAR_ERR_OOM = 3,         /* device allocation failed                        */
+  SAR_ERR_CUDA = 4,        /* a CUDA runtime call failed                      */
+  SAR_ERR_BOUNDS = 5,      /* a device-side bounds check fired               */
+  SAR_ERR_TIMEOUT = 6,     /* a device-side wait gave up (kernel returned)   */
+  SAR_ERR_UNSUPPORTED = 7  /* shape outside what the kernels implement       */
+};
+
+typedef struct sar_model sar_model;
+typedef struct sar_kv sar_kv;
+typedef struct sar_sched sar_sched;
+
+/* Thread-local text of the last error (never NULL). */
+const char* sar_last_error(void);
+
+/* Number of kernels this library has launched in this process. */
+int64_t sar_launch_count(void);
+
+/* ---- model ------------------------------------------------------------- */
+
+/* Decoder shape (Llama/Mistral-style: RMSNorm, GQA attention with rotary
+ * embedding, SwiGLU FFN).  head_dim must be 64 or 128; hidden, ffn and
+ * n_q_heads*head_dim multiples of 64; n_q_heads a multiple of n_kv_heads with
+ * at most 8 query heads per KV head.  vocab = 0 means no embedding / head.
+ * max_tokens bounds Lp+Bd of any step (sizes the step workspace);
+ * max_decodes bounds Bd. */
+typedef struct sar_dims {
+  int32_t n_layers;
+  int32_t hidden;
+  int32_t n_q_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t ffn;
+  int32_t vocab;
+  float rms_eps;
+  float rope_base;
+  int32_t max_tokens;
+  int32_t max_decodes;
+} sar_dims;
+
+/* One layer's weights: device bf16, [out, in] row-major; norm gains bf16 [hidden]. */
+typedef struct sar_layer_weights {
+  const void* wq; /* [n_q_heads*head_dim, hidden]  */
+  const void* wk; /* [n_kv_heads*head_dim, hidden] */
+  const void* wv; /* [n_kv_heads*head_dim, hidden] */
+  const void* wo; /* [hidden, n_q_heads*head_dim]  */
+  const void* wg; /* [ffn, hidden] */
+  const void* wu; /* [ffn, hidden] */
+  const void* wd; /* [hidden, ffn] */
+  const void* norm1;
+  const void* norm2;
+} sar_layer_weights;
+
+/* Creates a model on the current device and allocates its weight arena and
+ * step workspace (sized by max_tokens).  The model owns that memory until
+ * sar_model_destroy. */
+int sar_model_create(const sar_dims* dims, sar_model** out);
+
+/* Copies layer `layer`'s weights into the model's arena, repacking them
+ * (Q/K/V fused into one [q+2kv, hidden] matrix; gate and up interleaved in
+ * blocks of 64 rows so one GEMM epilogue forms silu(gate)*up).  Runs on
+ * `stream`; the caller may free its tensors once the stream has passed the
+ * copies (e.g. after a stream synchronise). */
+int sar_model_set_layer(sar_model* m, int32_t layer, const sar_layer_weights* w, void* stream);
+
+/* Copies the embedding [vocab, hidden], final norm gain [hidden] and LM head
+ * [vocab, hidden] (device bf16).  Any of them may be NULL if unused. */
+int sar_model_set_head(sar_model* m, const void* embed, const void* final_norm,
+                       const void* lm_head, void* stream);
+
+int sar_model_destroy(sar_model* m);
+
+/* Reads back and clears the model's device error flags (synchronises the
+ * device).  Returns SAR_OK, SAR_ERR_TIMEOUT or SAR_ERR_BOUNDS. */
+int sar_sync_status(sar_model* m);
+
+/* ---- paged KV cache ---------------------------------------------------- */
+
+/* One device arena for K and one for V, each laid out
+ * [n_layers][num_pages][n_kv_heads][page_size][head_dim] bf16, zeroed.
+ * page_size must be 16, 32 or 64 tokens. */
+int sar_kv_create(const sar_model* m, int32_t page_size, int32_t num_pages, sar_kv** out);
+
+/* Device address of layer `layer`'s K (kind 0) or V (kind 1) pages, so that a
+ * caller can inject cache state (e.g. a recorded or synthetic history). */
+int sar_kv_layer_ptr(sar_kv* kv, int32_t layer, int32_t kind, void** out);
+
+int sar_kv_destroy(sar_kv* kv);
+
+/* ---- one hybrid step --------------------------------------------------- */
+
+/* A prefill chunk: prompt positions [start_pos, start_pos+len) of request
+ * `req`.  block_table (host int32[n_blocks]) lists the request's pages in
+ * position order and must cover positions [0, start_pos+len). */
+typedef struct sar_prefill {
+  int32_t req;
+  int32_t start_pos;
+  int32_t len;
+  const int32_t* block_table;
+  int32_t n_blocks;
+} sar_prefill;
+
+/* A decode: ctx_len tokens are already cached; the new token sits at position
+ * ctx_len, is appended at slot ctx_len and attends to ctx_len+1 keys.
+ * block_table must cover positions [0, ctx_len]. */
+typedef struct sar_decode {
+  int32_t req;
+  int32_t ctx_len;
+  const int32_t* block_table;
+  int32_t n_blocks;
+} sar_decode;
+
+enum { SAR_IN_HIDDEN = 0, SAR_IN_TOKENS = 1 };
+
+/* At most one chunk (rows [0, Lp)) followed by n_decode decodes (rows
+ * [Lp, Lp+n_decode)) -- the batch Algorithm 3 builds. */
+typedef struct sar_batch {
+  int32_t has_prefill;
+  sar_prefill prefill;
+  int32_t n_decode;
+  const sar_decode* decode; /* host array [n_decode] */
+  int32_t in_kind;          /* SAR_IN_HIDDEN or SAR_IN_TOKENS */
+} sar_batch;
+
+/* Runs every layer over the stacked rows M = Lp + n_decode and then the head.
+ *   in         device: bf16 [M, hidden] (SAR_IN_HIDDEN) or int32 [M] token ids
+ *   hidden_out device bf16 [M, hidden]: last layer's residual stream (before
+ *              the final norm); may be NULL
+ *   logits_out device fp32 [R, vocab], R = has_prefill + n_decode: logits of
+ *              the chunk's last row (if any) then of every decode row; may be
+ *              NULL (head skipped); must be NULL when vocab = 0
+ *   layer_out  device bf16 [n_layers, M, hidden]: every layer's output; may be NULL
+ * New K/V of all rows are written into `kv`.  Asynchronous on `stream`; the
+ * host block tables are consumed before the call returns. */
+int sar_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, void* hidden_out,
+             float* logits_out, void* layer_out, void* stream);
+
+/* Same step with HOST buffers (in, hidden_out, logits_out, layer_out as
+ * above, each in host memory, NULL where unused).  Copies inputs to the
+ * device and results back on `stream` and returns once they are in host
+ * memory.  Pinned host memory makes the copies asynchronous to the host. */
+int sar_step_host(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, void* hidden_out,
+                  float* logits_out, void* layer_out, void* stream);
+
+/* Greedy sampling: tokens_out[r] = argmax_v logits[r, v] (lowest index on
+ * ties), device fp32 [rows, vocab] -> device int32 [rows]. */
+int sar_sample_greedy(sar_model* m, const float* logits, int32_t rows, int32_t* tokens_out,
+                      void* stream);
+
+/* ---- per-kernel timing (CUDA events on the step's stream) -------------- */
+
+enum {
+  SAR_K_EMBED = 0,
+  SAR_K_RMSNORM,
+  SAR_K_GEMM_QKV,
+  SAR_K_ROPE_APPEND,
+  SAR_K_CHUNK_ATTN,
+  SAR_K_DECODE_ATTN,
+  SAR_K_GEMM_O,
+  SAR_K_GEMM_GATEUP,
+  SAR_K_GEMM_DOWN,
+  SAR_K_HEAD_NORM,
+  SAR_K_GEMM_HEAD,
+  SAR_K_COUNT
+};
+
+/* When on, sar_step records an event pair around every kernel group. */
+int sar_profile_enable(sar_model* m, int32_t on);
+
+/* Synchronises, then returns per kind the accumulated milliseconds and the
+ * number of timed launches since the last reset, and resets them. */
+int sar_profile_read(sar_model* m, double* ms, int64_t* launches, int32_t n_kinds);
+
+/* ---- stall-free scheduler (host only) ---------------------------------- */
+
+/* tau: token budget, rounded down to a multiple of `tile` (must be >= tile).
+ * page_size/num_pages: the KV pool the scheduler hands pages from.
+ * max_batch: most requests holding pages at once. */
+typedef struct sar_sched_cfg {
+  int32_t tau;
+  int32_t tile;
+  int32_t page_size;
+  int32_t num_pages;
+  int32_t max_batch;
+} sar_sched_cfg;
+
+int sar_sched_create(const sar_sched_cfg* cfg, sar_sched** out);
+
+/* Queues a request.  prompt_tokens (host int32[prompt_len]) may be NULL; when
+ * every queued request has them, sar_sched_next also returns input ids. */
+int sar_sched_add(sar_sched* s, int32_t req, double arrival, int32_t prompt_len,
+                  int32_t output_len, const int32_t* prompt_tokens);
+
+/* Builds the next batch at time `now` (requests with arrival <= now are
+ * eligible): all running decodes, then at most one prefill chunk.  `out`
+ * points into scheduler-owned memory valid until the next call.  tokens_out
+ * (nullable) receives a pointer to M input ids, or NULL if unknown.
+ * Returns SAR_ERR_NO_PAGES if a decode needs a page and none is free. */
+int sar_sched_next(sar_sched* s, double now, sar_batch* out, const int32_t** tokens_out);
+
+/* Advances state with the sampled token of every logits row of the last
+ * batch (chunk's last row first, then decodes).  n_finished (nullable)
+ * receives how many requests completed; their pages are returned. */
+int sar_sched_commit(sar_sched* s, const int32_t* sampled, int32_t n_sampled,
+                     int32_t* n_finished);
+
+/* Queue sizes: waiting, running, finished, free pages. */
+int sar_sched_stats(const sar_sched* s, int32_t* waiting, int32_t* running, int32_t* finished,
+                    int32_t* free_pages);
+
+int sar_sched_destroy(sar_sched* s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAR_H */

@@ -1,0 +1,70 @@
+/*
+ * sar_ops.h -- single-kernel entry points of the hybrid step, for per-kernel
+ * parity tests and for the tile-quantisation sweep.
+ *
+ * The GEMM is the "one GEMM per weight over all [Lp+Bd, H] rows" of
+ * "SARATHI: Efficient LLM Inference by Piggybacking Decodes with Chunked
+ * Prefills" (reading notes, part 2 section 3).  Its row-tile choice is what the
+ * same notes' part 3 section 3 (tile quantisation: 257 rows need a third
+ * 128-row block) and the Sarathi-Serve digest (section 2, Q2 item 3: 257 vs
+ * 256 tokens costs +32% prefill time) are about; the variants below let a
+ * caller pick the tiling and measure it.
+ */
+#ifndef SAR_OPS_H
+#define SAR_OPS_H
+
+#include <stdint.h>
+
+#include "sar.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Epilogues applied to the fp32 accumulator D = A . W^T. */
+enum {
+  SAR_EPI_BF16 = 0,     /* C bf16 [M, N] = D                                         */
+  SAR_EPI_RESIDUAL = 1, /* C bf16 [M, N] = D + R (R bf16 [M, N]; R may equal C)      */
+  SAR_EPI_SWIGLU = 2,   /* W is gate/up interleaved in 64-row blocks, [2F, K]; C bf16
+                           [M, F] = silu(D_gate) * D_up                               */
+  SAR_EPI_F32 = 3       /* C fp32 [M, N] = D                                         */
+};
+
+/* Tilings.  All run tcgen05 MMAs (bf16 x bf16 -> fp32 in tensor memory) fed by
+ * TMA from 128-byte-swizzled shared memory, in a persistent kernel. */
+enum {
+  SAR_GEMM_AUTO = 0,  /* the library's choice for (M, N, K)                        */
+  SAR_GEMM_M128_N128 = 1, /* 128 token rows x 128 weight rows per tile              */
+  SAR_GEMM_M128_N256 = 2, /* 128 token rows x 256 weight rows per tile              */
+  SAR_GEMM_SWAP = 3,      /* weights on the MMA's M side (128 rows), tokens on its N
+                             side padded to 16 (M <= 256): no 128-row quantisation */
+  SAR_GEMM_M256_N128 = 4  /* 256 token rows (two 128-row MMAs sharing one weight
+                             tile) x 128 weight rows per tile                        */
+};
+
+/* C = epilogue(A . W^T).  A bf16 [M, K], W bf16 [N, K] (device, row-major,
+ * 16-byte aligned, K a multiple of 64, N a multiple of 64, M >= 1).
+ * For SAR_EPI_SWIGLU, N is 2F (the packed rows) and C has F columns.
+ * Returns SAR_ERR_UNSUPPORTED for shapes a variant cannot take. */
+int sar_op_gemm(const void* a, const void* w, void* c, const void* residual, int32_t M, int32_t N,
+                int32_t K, int32_t epilogue, int32_t variant, void* stream);
+
+/* y = x * rsqrt(mean(x^2) + eps) * gain per row; bf16 [rows, hidden]. */
+int sar_op_rmsnorm(const void* x, const void* gain, void* y, int32_t rows, int32_t hidden,
+                   float eps, void* stream);
+
+/* Device address of a step workspace buffer, valid until sar_model_destroy;
+ * after a step on a one-layer model it holds that layer's intermediates.
+ *   0: normed rows     bf16 [max_tokens, hidden]
+ *   1: q|k|v rows      bf16 [max_tokens, (n_q_heads + 2 n_kv_heads) * head_dim]
+ *                      (q and k after the rotary embedding)
+ *   2: attention rows  bf16 [max_tokens, n_q_heads * head_dim]
+ *   3: SwiGLU rows     bf16 [max_tokens, ffn]
+ *   4: residual stream bf16 [max_tokens, hidden] (when the step had no hidden_out) */
+int sar_model_debug_buffer(sar_model* m, int32_t which, void** out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAR_OPS_H */

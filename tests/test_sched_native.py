@@ -1,0 +1,90 @@
+"""The library's C++ stall-free scheduler agrees bit for bit with the oracle's
+restatement of Algorithm 3: same batches, same block tables, same input ids."""
+
+import json
+import os
+
+import pytest
+
+import chunked_prefill_hybrid_sar_gb300 as sar
+import synth
+from oracle import sched as osch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def replay(trace, tau, tile=128, page_size=16, num_pages=4000, max_batch=64, dt=0.013,
+           with_tokens=False, max_steps=100000):
+    """Drive both schedulers with the same `now` sequence and sampled tokens."""
+    o = osch.StallFreeScheduler(tau, tile, page_size, num_pages, max_batch)
+    c = sar.Scheduler(tau, tile, page_size, num_pages, max_batch)
+    toks = synth.prompt_tokens(5, trace, 1000) if with_tokens else {}
+    for r in trace:
+        pt = toks.get(r.req)
+        o.add(r.req, r.arrival, r.prompt_len, r.output_len, pt)
+        c.add(r.req, r.arrival, r.prompt_len, r.output_len, pt)
+    now, steps = 0.0, 0
+    while not o.idle():
+        ob = o.next(now)
+        pre, decs, tokens, _ = c.next(now)
+        exp = tuple(ob.prefill) if ob.prefill else None
+        assert (tuple(pre) if pre else None) == exp, (steps, pre, exp)
+        assert decs == ob.decodes, steps
+        if with_tokens:
+            assert tokens == ob.tokens, steps
+        n = (1 if ob.prefill else 0) + len(ob.decodes)
+        sampled = [(steps * 7 + i) % 1000 for i in range(n)]
+        o.commit(sampled)
+        c.commit(sampled)
+        now += dt if n else 0.25
+        steps += 1
+        assert steps < max_steps
+    assert c.stats()[:3] == (0, 0, len(trace))
+    return steps
+
+
+def test_figure4_timeline_native():
+    with open(os.path.join(GOLDEN, "figure4_schedule.json")) as f:
+        g = json.load(f)
+    c = sar.Scheduler(g["tau"], g["tile"], g["page_size"], g["num_pages"], g["max_batch"])
+    for r in g["requests"]:
+        c.add(r["req"], r["arrival"], r["prompt_len"], r["output_len"])
+    for it in g["iterations"]:
+        pre, decs, _, _ = c.next(it["now"])
+        assert (list(pre[:3]) if pre else None) == it["prefill"]
+        assert [d[0] for d in decs] == it["decodes"]
+        c.commit([7] * ((1 if pre else 0) + len(decs)))
+
+
+@pytest.mark.parametrize("tau", [256, 512, 1024])
+def test_native_matches_oracle_on_serving_trace(tau):
+    # the serving workload's shape (Poisson arrivals, lognormal lengths), scaled down
+    trace = synth.request_trace(0, 64, rate=4.0, prompt_median=1024, prompt_clip=(64, 8192),
+                                out_median=64, out_clip=(16, 256))
+    replay(trace, tau, dt=0.02)
+
+
+def test_native_matches_oracle_with_prompt_tokens_and_small_pool():
+    trace = synth.request_trace(1, 40, rate=50.0, prompt_median=200, prompt_clip=(1, 900),
+                                out_median=12, out_clip=(1, 60))
+    replay(trace, 256, num_pages=120, max_batch=6, with_tokens=True)
+
+
+def test_native_reports_pool_exhaustion():
+    c = sar.Scheduler(128, 128, 16, 3, 4)
+    c.add(0, 0.0, 16, 40)
+    c.next(0.0)
+    c.commit([1])
+    with pytest.raises(sar.SarError) as e:
+        for _ in range(40):
+            c.next(0.0)
+            c.commit([1])
+    assert e.value.code == 2
+
+
+def test_commit_needs_one_token_per_row():
+    c = sar.Scheduler(128, 128, 16, 8, 4)
+    c.add(0, 0.0, 10, 2)
+    c.next(0.0)
+    with pytest.raises(sar.SarError):
+        c.commit([1, 2])
