@@ -109,3 +109,16 @@ def test_gemm_unsupported_shapes_are_rejected():
         sar.gemm(a, w, c, variant=sar.SAR_GEMM_SWAP)
     with pytest.raises(sar.SarError):
         sar.gemm(a[:, :100], w[:, :100], c)
+
+
+@pytest.mark.parametrize("rows,hidden", [(1, 256), (260, 256), (512, 4096), (3, 7168)])
+def test_rmsnorm_kernel(rows, hidden):
+    g = synth.generator(4)
+    x = synth.normal(g, (rows, hidden), 2.0, dtype=torch.bfloat16)
+    gain = (1 + 0.3 * synth.normal(g, (hidden,))).to(torch.bfloat16)
+    y = torch.empty_like(x, device=DEV)
+    sar.rmsnorm(x.to(DEV), gain.to(DEV), y, 1e-5)
+    torch.cuda.synchronize()
+    xd = x.double()
+    ref = xd / torch.sqrt((xd * xd).mean(-1, keepdim=True) + 1e-5) * gain.double()
+    close(y, ref)
