@@ -10,12 +10,20 @@ from __future__ import annotations
 import ctypes
 
 from . import _lib
-from ._lib import (SAR_EPI_BF16, SAR_EPI_F32, SAR_EPI_RESIDUAL, SAR_EPI_SWIGLU, SAR_GEMM_AUTO,
+from ._lib import (SAR_EPI_F32, SAR_EPI_RESIDUAL, SAR_EPI_STORE, SAR_EPI_SWIGLU, SAR_GEMM_AUTO,
                    SAR_GEMM_M128_N128, SAR_GEMM_M128_N256, SAR_GEMM_M256_N128, SAR_GEMM_SWAP,
-                   SAR_IN_HIDDEN, SAR_IN_TOKENS, KERNEL_KINDS, SarError, check, lib)
+                   SAR_IN_HIDDEN, SAR_IN_TOKENS, SAR_STORAGE_BF16, SAR_STORAGE_F16, KERNEL_KINDS,
+                   SarError, check, lib)
 
 __all__ = ["Model", "KVCache", "Scheduler", "Batch", "SarError", "lib", "check", "gemm", "rmsnorm",
-           "launch_count", "KERNEL_KINDS", "SAR_IN_HIDDEN", "SAR_IN_TOKENS"]
+           "launch_count", "KERNEL_KINDS", "SAR_IN_HIDDEN", "SAR_IN_TOKENS", "SAR_STORAGE_F16",
+           "SAR_STORAGE_BF16", "storage_dtype"]
+
+
+def storage_dtype(storage: int):
+    """torch dtype of a storage code."""
+    import torch
+    return torch.bfloat16 if storage == SAR_STORAGE_BF16 else torch.float16
 
 
 def _ptr(t) -> int | None:
@@ -73,10 +81,14 @@ class Batch:
 
 
 class Model:
-    def __init__(self, dims, max_tokens: int, max_decodes: int):
+    """Weights are given in bf16; ``storage`` picks the internal 16-bit type."""
+
+    def __init__(self, dims, max_tokens: int, max_decodes: int, storage: int = SAR_STORAGE_F16):
         self.dims = dims
+        self.storage = storage
         d = _lib.sar_dims(dims.n_layers, dims.hidden, dims.n_q_heads, dims.n_kv_heads, dims.head_dim,
-                          dims.ffn, dims.vocab, dims.rms_eps, dims.rope_base, max_tokens, max_decodes)
+                          dims.ffn, dims.vocab, dims.rms_eps, dims.rope_base, max_tokens, max_decodes,
+                          storage)
         h = ctypes.c_void_p()
         check(lib().sar_model_create(ctypes.byref(d), ctypes.byref(h)))
         self.h = h
@@ -139,6 +151,7 @@ class KVCache:
         check(lib().sar_kv_create(model.h, page_size, num_pages, ctypes.byref(h)))
         self.h = h
         self.model = model
+        self.storage = model.storage
         self.page_size = page_size
         self.num_pages = num_pages
 
@@ -212,13 +225,20 @@ class Scheduler:
             pass
 
 
-def gemm(a, w, c, residual=None, epilogue=SAR_EPI_BF16, variant=SAR_GEMM_AUTO, stream=None) -> None:
+def _storage_of(t) -> int:
+    import torch
+    return SAR_STORAGE_BF16 if t.dtype == torch.bfloat16 else SAR_STORAGE_F16
+
+
+def gemm(a, w, c, residual=None, epilogue=SAR_EPI_STORE, variant=SAR_GEMM_AUTO, stream=None) -> None:
+    """C = epilogue(a . w^T); the storage type is taken from ``a`` (fp16 or bf16)."""
     M, K = a.shape
     N = w.shape[0]
     check(lib().sar_op_gemm(_ptr(a), _ptr(w), _ptr(c), _ptr(residual), M, N, K, epilogue, variant,
-                            _stream(stream)))
+                            _storage_of(a), _stream(stream)))
 
 
 def rmsnorm(x, gain, y, eps: float, stream=None) -> None:
+    """y (fp16/bf16) = rmsnorm of fp32 rows x with fp32 gain."""
     check(lib().sar_op_rmsnorm(_ptr(x), _ptr(gain), _ptr(y), x.shape[0], x.shape[1], eps,
-                               _stream(stream)))
+                               _storage_of(y), _stream(stream)))

@@ -26,7 +26,8 @@ SAR_ERR_UNSUPPORTED = 7
 SAR_IN_HIDDEN = 0
 SAR_IN_TOKENS = 1
 
-SAR_EPI_BF16, SAR_EPI_RESIDUAL, SAR_EPI_SWIGLU, SAR_EPI_F32 = 0, 1, 2, 3
+SAR_STORAGE_F16, SAR_STORAGE_BF16 = 0, 1
+SAR_EPI_STORE, SAR_EPI_RESIDUAL, SAR_EPI_SWIGLU, SAR_EPI_F32 = 0, 1, 2, 3
 SAR_GEMM_AUTO, SAR_GEMM_M128_N128, SAR_GEMM_M128_N256, SAR_GEMM_SWAP, SAR_GEMM_M256_N128 = 0, 1, 2, 3, 4
 
 KERNEL_KINDS = ("embed", "rmsnorm", "gemm_qkv", "rope_append", "chunk_attn", "decode_attn", "gemm_o",
@@ -41,7 +42,8 @@ P_i32 = ctypes.POINTER(ctypes.c_int32)
 class sar_dims(ctypes.Structure):
     _fields_ = [("n_layers", i32), ("hidden", i32), ("n_q_heads", i32), ("n_kv_heads", i32),
                 ("head_dim", i32), ("ffn", i32), ("vocab", i32), ("rms_eps", ctypes.c_float),
-                ("rope_base", ctypes.c_float), ("max_tokens", i32), ("max_decodes", i32)]
+                ("rope_base", ctypes.c_float), ("max_tokens", i32), ("max_decodes", i32),
+                ("storage", i32)]
 
 
 class sar_layer_weights(ctypes.Structure):
@@ -90,8 +92,8 @@ SIGNATURES = {
     "sar_sched_commit": (i32, [vp, P_i32, i32, P_i32]),
     "sar_sched_stats": (i32, [vp, P_i32, P_i32, P_i32, P_i32]),
     "sar_sched_destroy": (i32, [vp]),
-    "sar_op_gemm": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
-    "sar_op_rmsnorm": (i32, [vp, vp, vp, i32, i32, ctypes.c_float, vp]),
+    "sar_op_gemm": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
+    "sar_op_rmsnorm": (i32, [vp, vp, vp, i32, i32, ctypes.c_float, i32, vp]),
     "sar_model_debug_buffer": (i32, [vp, i32, ctypes.POINTER(vp)]),
 }
 

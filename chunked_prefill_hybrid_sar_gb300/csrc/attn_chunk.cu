@@ -6,7 +6,7 @@
 // correct, same page section 3.1).  Chunk k re-reads the KV of the k earlier
 // chunks -- the N(N-1)/2 re-read of the Sarathi-Serve digest, section 4.
 //
-// Tiled online-softmax attention on warp-level bf16 MMAs (m16n8k16, fp32
+// Tiled online-softmax attention on warp-level 16-bit MMAs (m16n8k16, fp32
 // accumulate): a CTA owns 64 query rows of one query head (16 per warp); K/V
 // tiles of 64 keys are gathered page by page with 16-byte cp.async into an
 // XOR-swizzled shared layout (conflict-free ldmatrix), double buffered.
@@ -34,13 +34,23 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
+// D += A . B on a 16x8x16 tile, fp32 accumulate; A and B both of the storage type T.
+template <typename T>
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  if constexpr (Elem<T>::kMmaFormat == 1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
 }
 
 // byte offset of (row, 16-byte chunk) in a [rows][D] bf16 tile, chunks XOR-swizzled by row % 8
@@ -49,7 +59,7 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)(row * (D * 2) + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int D>
+template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a) {
   constexpr int CH = D / 8;  // 16-byte chunks per row
   constexpr int TILE = kBKV * D * 2;
@@ -72,7 +82,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
   for (int c = threadIdx.x; c < kBQ * CH; c += kThreads) {
     const int r = c / CH, ch = c % CH;
     const bool ok = r < nq;
-    const __nv_bfloat16* src = a.qkv + (size_t)(q0 + (ok ? r : 0)) * a.ld + (size_t)hq * D + ch * 8;
+    const T* src = static_cast<const T*>(a.qkv) + (size_t)(q0 + (ok ? r : 0)) * a.ld + (size_t)hq * D + ch * 8;
     cp_async16(sq_u + swz<D>(r, ch), src, ok ? 16 : 0);
   }
   auto load_kv = [&](int t, int stage) {
@@ -90,8 +100,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
         page = 0;
       }
       const size_t elem = (((size_t)page * a.kvh + kh) * a.page_size + (pos - bi * a.page_size)) * D + ch * 8;
-      const __nv_bfloat16* ks = ok ? a.k_cache + elem : a.k_cache;
-      const __nv_bfloat16* vs = ok ? a.v_cache + elem : a.v_cache;
+      const T* ks = static_cast<const T*>(a.k_cache) + (ok ? elem : 0);
+      const T* vs = static_cast<const T*>(a.v_cache) + (ok ? elem : 0);
       cp_async16(kbase + swz<D>(r, ch), ks, ok ? 16 : 0);
       cp_async16(vbase + swz<D>(r, ch), vs, ok ? 16 : 0);
     }
@@ -136,8 +146,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
         uint32_t b0, b1, b2, b3;
         const int mi = lane >> 3;
         ldsm_x4(kbase + swz<D>(j * 8 + (lane & 7), kk * 2 + mi), b0, b1, b2, b3);
-        mma16816(s[j], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
-        mma16816(s[j], qf[kk + 1][0], qf[kk + 1][1], qf[kk + 1][2], qf[kk + 1][3], b2, b3);
+        mma16816<T>(s[j], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+        mma16816<T>(s[j], qf[kk + 1][0], qf[kk + 1][1], qf[kk + 1][2], qf[kk + 1][3], b2, b3);
       }
     }
     // ---- causal mask + online softmax (base 2) ----
@@ -172,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
       const float p2 = exp2f(s[j][2] - ref1), p3 = exp2f(s[j][3] - ref1);
       rs0 += p0 + p1;
       rs1 += p2 + p3;
-      pf[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
-      pf[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
+      pf[j >> 1][(j & 1) * 2 + 0] = Elem<T>::pack(p0, p1);
+      pf[j >> 1][(j & 1) * 2 + 1] = Elem<T>::pack(p2, p3);
     }
     l0 = l0 * al0 + rs0;
     l1 = l1 * al1 + rs1;
@@ -192,8 +202,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
         uint32_t b0, b1, b2, b3;
         const int mi = lane >> 3;
         ldsm_x4_t(vbase + swz<D>(kt * 16 + (mi & 1) * 8 + (lane & 7), j + (mi >> 1)), b0, b1, b2, b3);
-        mma16816(o[j], pf[kt][0], pf[kt][1], pf[kt][2], pf[kt][3], b0, b1);
-        mma16816(o[j + 1], pf[kt][0], pf[kt][1], pf[kt][2], pf[kt][3], b2, b3);
+        mma16816<T>(o[j], pf[kt][0], pf[kt][1], pf[kt][2], pf[kt][3], b0, b1);
+        mma16816<T>(o[j + 1], pf[kt][0], pf[kt][1], pf[kt][2], pf[kt][3], b2, b3);
       }
     }
     __syncthreads();  // stage (t & 1) is refilled at iteration t + 1
@@ -208,26 +218,27 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
   const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
   const int row0 = q0 + r_lo, row1 = row0 + 8;
 #pragma unroll
+  T* out = static_cast<T*>(a.out);
   for (int j = 0; j < D / 8; ++j) {
     const int col = hq * D + j * 8 + 2 * (lane & 3);
     if (r_lo < nq)
-      *reinterpret_cast<uint32_t*>(a.out + (size_t)row0 * a.ld_out + col) = pack_bf16(o[j][0] * inv0, o[j][1] * inv0);
+      *reinterpret_cast<uint32_t*>(out + (size_t)row0 * a.ld_out + col) = Elem<T>::pack(o[j][0] * inv0, o[j][1] * inv0);
     if (r_lo + 8 < nq)
-      *reinterpret_cast<uint32_t*>(a.out + (size_t)row1 * a.ld_out + col) = pack_bf16(o[j][2] * inv1, o[j][3] * inv1);
+      *reinterpret_cast<uint32_t*>(out + (size_t)row1 * a.ld_out + col) = Elem<T>::pack(o[j][2] * inv1, o[j][3] * inv1);
   }
 }
 
-template <int D>
+template <typename T, int D>
 int launch_impl(const ChunkAttnArgs& a, cudaStream_t s) {
   const size_t smem = (size_t)kBQ * D * 2 + (size_t)2 * 2 * kBKV * D * 2;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(chunk_attn_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_error(e, "chunk attention attribute");
     attr = true;
   }
   dim3 grid((a.len + kBQ - 1) / kBQ, a.qh);
-  chunk_attn_kernel<D><<<grid, kThreads, smem, s>>>(a);
+  chunk_attn_kernel<T, D><<<grid, kThreads, smem, s>>>(a);
   count_launches(1);
   return cuda_error(cudaGetLastError(), "chunk attention launch");
 }
@@ -237,8 +248,9 @@ int launch_impl(const ChunkAttnArgs& a, cudaStream_t s) {
 int launch_chunk_attention(const ChunkAttnArgs& a, cudaStream_t s) {
   if (a.len <= 0) return SAR_OK;
   if (a.qh % a.kvh) return set_error(SAR_ERR_UNSUPPORTED, "chunk attention: qh % kvh");
-  if (a.d == 128) return launch_impl<128>(a, s);
-  if (a.d == 64) return launch_impl<64>(a, s);
+  const bool bf = a.storage == SAR_STORAGE_BF16;
+  if (a.d == 128) return bf ? launch_impl<__nv_bfloat16, 128>(a, s) : launch_impl<__half, 128>(a, s);
+  if (a.d == 64) return bf ? launch_impl<__nv_bfloat16, 64>(a, s) : launch_impl<__half, 64>(a, s);
   return set_error(SAR_ERR_UNSUPPORTED, "chunk attention: head_dim must be 64 or 128");
 }
 

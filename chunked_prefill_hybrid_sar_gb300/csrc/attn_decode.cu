@@ -45,7 +45,7 @@ __device__ __forceinline__ void butterfly_step(float (&v)[NV], int lane) {
   }
 }
 
-template <int D, int GP>
+template <typename T, int D, int GP>
 __global__ void __launch_bounds__(kWarps * 32, 2) decode_attn_kernel(DecodeAttnArgs a) {
   constexpr int DPL = D / 32;            // dimensions per lane
   constexpr int NV = kBlockKeys * GP;    // partial dots per block: 16 keys x GP heads
@@ -90,8 +90,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_attn_kernel(DecodeAttnA
     uint8_t* dst = ring + s * 2 * BLK_BYTES;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_expect_tx(bar, 2 * BLK_BYTES);
-    bulk_g2s(smem_u32(dst), a.k_cache + elem, BLK_BYTES, bar);
-    bulk_g2s(smem_u32(dst + BLK_BYTES), a.v_cache + elem, BLK_BYTES, bar);
+    bulk_g2s(smem_u32(dst), static_cast<const T*>(a.k_cache) + elem, BLK_BYTES, bar);
+    bulk_g2s(smem_u32(dst + BLK_BYTES), static_cast<const T*>(a.v_cache) + elem, BLK_BYTES, bar);
     return true;
   };
 
@@ -103,9 +103,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_attn_kernel(DecodeAttnA
 #pragma unroll
     for (int e = 0; e < DPL; ++e) q[h][e] = 0.f;
     if (h < G) {
-      const __nv_bfloat16* qp = a.qkv + (size_t)b * a.ld + (size_t)(kh * G + h) * D + lane * DPL;
+      const T* qp = static_cast<const T*>(a.qkv) + (size_t)b * a.ld + (size_t)(kh * G + h) * D + lane * DPL;
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) q[h][e] = __bfloat162float(qp[e]) * qscale;
+      for (int e = 0; e < DPL; ++e) q[h][e] = Elem<T>::to(qp[e]) * qscale;
     }
   }
 
@@ -154,10 +154,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_attn_kernel(DecodeAttnA
       float kf[DPL];
       if constexpr (DPL == 4) {
         const uint2 kv = *reinterpret_cast<const uint2*>(kb + (k * D + lane * 4) * 2);
-        kf[0] = bf16lo(kv.x); kf[1] = bf16hi(kv.x); kf[2] = bf16lo(kv.y); kf[3] = bf16hi(kv.y);
+        kf[0] = Elem<T>::lo(kv.x); kf[1] = Elem<T>::hi(kv.x); kf[2] = Elem<T>::lo(kv.y); kf[3] = Elem<T>::hi(kv.y);
       } else {
         const uint32_t kv = *reinterpret_cast<const uint32_t*>(kb + (k * D + lane * 2) * 2);
-        kf[0] = bf16lo(kv); kf[1] = bf16hi(kv);
+        kf[0] = Elem<T>::lo(kv); kf[1] = Elem<T>::hi(kv);
       }
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
@@ -229,10 +229,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_attn_kernel(DecodeAttnA
       float vf[DPL];
       if constexpr (DPL == 4) {
         const uint2 vv = *reinterpret_cast<const uint2*>(vb + (k * D + lane * 4) * 2);
-        vf[0] = bf16lo(vv.x); vf[1] = bf16hi(vv.x); vf[2] = bf16lo(vv.y); vf[3] = bf16hi(vv.y);
+        vf[0] = Elem<T>::lo(vv.x); vf[1] = Elem<T>::hi(vv.x); vf[2] = Elem<T>::lo(vv.y); vf[3] = Elem<T>::hi(vv.y);
       } else {
         const uint32_t vv = *reinterpret_cast<const uint32_t*>(vb + (k * D + lane * 2) * 2);
-        vf[0] = bf16lo(vv); vf[1] = bf16hi(vv);
+        vf[0] = Elem<T>::lo(vv); vf[1] = Elem<T>::hi(vv);
       }
       float p[GP];
       if constexpr (GP >= 4) {
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_attn_kernel(DecodeAttnA
     }
     const int hq = kh * G + h;
     if (part < 0) {
-      a.out[(size_t)b * a.ld_out + (size_t)hq * D + dd] = __float2bfloat16_rn(A / L);
+      static_cast<T*>(a.out)[(size_t)b * a.ld_out + (size_t)hq * D + dd] = Elem<T>::from(A / L);
     } else {
       float* pp = a.partials + ((size_t)part * a.qh + hq) * (D + 2);
       pp[dd] = A;
@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_attn_kernel(DecodeAttnA
 }
 
 // Merges the split partial results of each decode: out = sum_i A_i 2^(m_i - M) / sum_i L_i 2^(m_i - M).
-template <int D>
+template <typename T, int D>
 __global__ void decode_combine_kernel(DecodeAttnArgs a) {
   const int b = blockIdx.x;
   const int hq = blockIdx.y;
@@ -334,27 +334,27 @@ __global__ void decode_combine_kernel(DecodeAttnArgs a) {
     L = fmaf(pp[D + 1], sc, L);
     A = fmaf(pp[dd], sc, A);
   }
-  a.out[(size_t)b * a.ld_out + (size_t)hq * D + dd] = __float2bfloat16_rn(A / L);
+  static_cast<T*>(a.out)[(size_t)b * a.ld_out + (size_t)hq * D + dd] = Elem<T>::from(A / L);
 }
 
-template <int D, int GP>
+template <typename T, int D, int GP>
 int launch_impl(const DecodeAttnArgs& a, cudaStream_t s) {
   constexpr int NV = kBlockKeys * GP;
   const size_t smem = (size_t)kWarps * kStages * 2 * kBlockKeys * D * 2 + (size_t)kWarps * NV * 4 +
                       (size_t)kWarps * GP * (D + 2) * 4 + (size_t)kWarps * kStages * 8 + 16;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<D, GP>,
+    cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<T, D, GP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_error(e, "decode attention attribute");
     attr = true;
   }
-  decode_attn_kernel<D, GP><<<dim3(a.n_items, a.kvh), kWarps * 32, smem, s>>>(a);
+  decode_attn_kernel<T, D, GP><<<dim3(a.n_items, a.kvh), kWarps * 32, smem, s>>>(a);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "decode attention launch");
   if (a.partials) {
-    decode_combine_kernel<D><<<dim3(a.n_decode, a.qh), D, 0, s>>>(a);
+    decode_combine_kernel<T, D><<<dim3(a.n_decode, a.qh), D, 0, s>>>(a);
     count_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "decode combine launch");
@@ -370,8 +370,10 @@ int launch_decode_attention(const DecodeAttnArgs& a, cudaStream_t s) {
   if (a.qh % a.kvh || G > 8 || (a.d != 64 && a.d != 128) || a.page_size % kBlockKeys)
     return set_error(SAR_ERR_UNSUPPORTED, "decode attention: head_dim 64/128, group <= 8, page % 16");
   const int GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
-#define SAR_DEC(DD, GG) \
-  if (a.d == DD && GP == GG) return launch_impl<DD, GG>(a, s);
+#define SAR_DEC(DD, GG)                                                             \
+  if (a.d == DD && GP == GG)                                                         \
+    return a.storage == SAR_STORAGE_BF16 ? launch_impl<__nv_bfloat16, DD, GG>(a, s) \
+                                         : launch_impl<__half, DD, GG>(a, s);
   SAR_DEC(128, 1) SAR_DEC(128, 2) SAR_DEC(128, 4) SAR_DEC(128, 8)
   SAR_DEC(64, 1) SAR_DEC(64, 2) SAR_DEC(64, 4) SAR_DEC(64, 8)
 #undef SAR_DEC

@@ -159,3 +159,45 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 }  // namespace sar
+
+#include <cuda_fp16.h>
+
+namespace sar {
+
+// ---- storage element traits --------------------------------------------------
+// The step stores activations, weights and the KV cache in one 16-bit type T
+// (fp16 or bf16) and accumulates in fp32.  Elem<T> converts packed pairs.
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<__half> {
+  static constexpr uint32_t kMmaFormat = 0;  // tcgen05 kind::f16 operand format: F16
+  __device__ static __forceinline__ float lo(uint32_t v) {
+    return __half2float(__ushort_as_half((unsigned short)(v & 0xffffu)));
+  }
+  __device__ static __forceinline__ float hi(uint32_t v) {
+    return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
+  }
+  __device__ static __forceinline__ uint32_t pack(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static __forceinline__ __half from(float a) { return __float2half_rn(a); }
+  __device__ static __forceinline__ float to(__half a) { return __half2float(a); }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr uint32_t kMmaFormat = 1;  // BF16
+  __device__ static __forceinline__ float lo(uint32_t v) { return __uint_as_float(v << 16); }
+  __device__ static __forceinline__ float hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+  __device__ static __forceinline__ uint32_t pack(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static __forceinline__ __nv_bfloat16 from(float a) { return __float2bfloat16_rn(a); }
+  __device__ static __forceinline__ float to(__nv_bfloat16 a) { return __bfloat162float(a); }
+};
+
+}  // namespace sar

@@ -3,6 +3,8 @@
 // and read/write each byte once with 16-byte accesses where the layout allows.
 #include <float.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -24,61 +26,80 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
-// y[r] = x[src(r)] * rsqrt(mean(x^2) + eps) * gain, fp32 reduction.  The
-// normalisation ahead of attention and FFN, and the final norm ahead of the
-// LM head ("insert an explicit sync before LayerNorm", SARATHI technique
-// write-up, section 6.1).
-__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat16* __restrict__ x,
-                                                              const __nv_bfloat16* __restrict__ g,
-                                                              __nv_bfloat16* __restrict__ y,
-                                                              int hidden, float eps,
+// y[r] = x[src(r)] * rsqrt(mean(x^2) + eps) * gain with x the fp32 residual
+// stream, fp32 reduction, y in the storage type T.  The normalisation ahead of
+// attention and FFN, and the final norm ahead of the LM head ("insert an
+// explicit sync before LayerNorm", SARATHI technique write-up, section 6.1).
+template <typename T>
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* __restrict__ x,
+                                                              const float* __restrict__ g,
+                                                              T* __restrict__ y, int hidden, float eps,
                                                               const int32_t* __restrict__ ridx) {
   __shared__ float red[32];
   const int r = blockIdx.x;
   const int src = ridx ? ridx[r] : r;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)src * hidden);
-  const uint4* gr = reinterpret_cast<const uint4*>(g);
-  uint4* yr = reinterpret_cast<uint4*>(y + (size_t)r * hidden);
-  const int nv = hidden >> 3;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)src * hidden);
+  const float4* gr = reinterpret_cast<const float4*>(g);
+  uint2* yr = reinterpret_cast<uint2*>(y + (size_t)r * hidden);
+  const int nv = hidden >> 2;
   float ss = 0.f;
   for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-    const uint4 v = xr[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float a = bf16lo(w[e]), b = bf16hi(w[e]);
-      ss = fmaf(a, a, ss);
-      ss = fmaf(b, b, ss);
-    }
+    const float4 v = xr[i];
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
   }
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / (float)hidden + eps);
   for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-    const uint4 v = xr[i];
-    const uint4 gv = gr[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      o[e] = pack_bf16(bf16lo(w[e]) * inv * bf16lo(gw[e]), bf16hi(w[e]) * inv * bf16hi(gw[e]));
-    yr[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    const float4 v = xr[i];
+    const float4 gv = gr[i];
+    yr[i] = make_uint2(Elem<T>::pack(v.x * inv * gv.x, v.y * inv * gv.y),
+                       Elem<T>::pack(v.z * inv * gv.z, v.w * inv * gv.w));
   }
 }
 
-__global__ void embed_kernel(const int32_t* __restrict__ tok, const __nv_bfloat16* __restrict__ table,
-                             __nv_bfloat16* __restrict__ out, int hidden, int vocab, int* err) {
+// Embedding rows of the storage type into the fp32 residual stream.
+template <typename T>
+__global__ void embed_kernel(const int32_t* __restrict__ tok, const T* __restrict__ table,
+                             float* __restrict__ out, int hidden, int vocab, int* err) {
   const int r = blockIdx.x;
   const int t = tok[r];
-  uint4* dst = reinterpret_cast<uint4*>(out + (size_t)r * hidden);
-  const int nv = hidden >> 3;
+  float4* dst = reinterpret_cast<float4*>(out + (size_t)r * hidden);
+  const int nv = hidden >> 2;
   if (t < 0 || t >= vocab) {
     if (threadIdx.x == 0) report(err, SAR_ERR_BOUNDS, SITE_EMBED_BOUNDS, t);
-    for (int i = threadIdx.x; i < nv; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
-  const uint4* src = reinterpret_cast<const uint4*>(table + (size_t)t * hidden);
-  for (int i = threadIdx.x; i < nv; i += blockDim.x) dst[i] = src[i];
+  const uint2* src = reinterpret_cast<const uint2*>(table + (size_t)t * hidden);
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+    const uint2 v = src[i];
+    dst[i] = make_float4(Elem<T>::lo(v.x), Elem<T>::hi(v.x), Elem<T>::lo(v.y), Elem<T>::hi(v.y));
+  }
+}
+
+// bf16 -> fp32 (input rows into the residual stream, norm gains).
+__global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ src, float* __restrict__ dst, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = __bfloat162float(src[i]);
+}
+
+// bf16 weight rows -> storage type T, row r of the source landing on row
+// map(r) of the destination: identity, or the gate/up interleave (64-row
+// blocks, gate first when `up` is 0).
+template <typename T>
+__global__ void convert_rows_kernel(const __nv_bfloat16* __restrict__ src, T* __restrict__ dst, int rows,
+                                    int cols, int interleave, int up) {
+  const int r = blockIdx.x;
+  const int dr = interleave ? (r / 64) * 128 + up * 64 + (r % 64) : r;
+  const uint32_t* s = reinterpret_cast<const uint32_t*>(src + (size_t)r * cols);
+  uint32_t* d = reinterpret_cast<uint32_t*>(dst + (size_t)dr * cols);
+  for (int i = threadIdx.x; i < (cols >> 1); i += blockDim.x) {
+    const uint32_t v = s[i];
+    d[i] = Elem<T>::pack(bf16lo(v), bf16hi(v));
+  }
 }
 
 // Rotary embedding of the q and k heads of one row at its absolute position
@@ -87,6 +108,7 @@ __global__ void embed_kernel(const int32_t* __restrict__ tok, const __nv_bfloat1
 // the rotated k and the v of that row are written into the row's page slot.
 // The angle pos * theta_i is formed and reduced modulo 2*pi in double
 // precision once per (row, frequency), so long positions keep fp32 accuracy.
+template <typename T>
 __global__ void rope_append_kernel(RopeArgs a) {
   __shared__ float cs[64], sn[64];
   const int r = blockIdx.x;
@@ -108,33 +130,35 @@ __global__ void rope_append_kernel(RopeArgs a) {
   const bool slot_ok = slot >= 0 && page < a.num_pages;
   if (!slot_ok && threadIdx.x == 0) report(a.err, SAR_ERR_BOUNDS, SITE_ROPE_BOUNDS, slot);
   const int width = (a.qh + 2 * a.kvh) * a.d;
-  __nv_bfloat16* row = a.qkv + (size_t)r * width;
+  T* row = reinterpret_cast<T*>(a.qkv) + (size_t)r * width;
+  T* k_cache = reinterpret_cast<T*>(a.k_cache);
+  T* v_cache = reinterpret_cast<T*>(a.v_cache);
   const int n_pairs = (a.qh + a.kvh) * half;
   for (int idx = threadIdx.x; idx < n_pairs; idx += blockDim.x) {
     const int h = idx / half;
     const int i = idx - h * half;
-    __nv_bfloat16* base = row + h * a.d;
-    const float x1 = __bfloat162float(base[i]);
-    const float x2 = __bfloat162float(base[i + half]);
+    T* base = row + h * a.d;
+    const float x1 = Elem<T>::to(base[i]);
+    const float x2 = Elem<T>::to(base[i + half]);
     const float c = cs[i], s = sn[i];
-    const __nv_bfloat16 y1 = __float2bfloat16_rn(x1 * c - x2 * s);
-    const __nv_bfloat16 y2 = __float2bfloat16_rn(x2 * c + x1 * s);
+    const T y1 = Elem<T>::from(x1 * c - x2 * s);
+    const T y2 = Elem<T>::from(x2 * c + x1 * s);
     base[i] = y1;
     base[i + half] = y2;
     if (h >= a.qh && slot_ok) {
       const int kh = h - a.qh;
-      __nv_bfloat16* kc = a.k_cache + (((size_t)page * a.kvh + kh) * a.page_size + off) * a.d;
+      T* kc = k_cache + (((size_t)page * a.kvh + kh) * a.page_size + off) * a.d;
       kc[i] = y1;
       kc[i + half] = y2;
     }
   }
   if (slot_ok) {
-    const __nv_bfloat16* vrow = row + (a.qh + a.kvh) * a.d;
+    const T* vrow = row + (a.qh + a.kvh) * a.d;
     const int nv = a.kvh * a.d;
     for (int idx = threadIdx.x; idx < nv; idx += blockDim.x) {
       const int kh = idx / a.d;
       const int j = idx - kh * a.d;
-      a.v_cache[(((size_t)page * a.kvh + kh) * a.page_size + off) * a.d + j] = vrow[idx];
+      v_cache[(((size_t)page * a.kvh + kh) * a.page_size + off) * a.d + j] = vrow[idx];
     }
   }
 }
@@ -188,27 +212,60 @@ __global__ void __launch_bounds__(1024) argmax_kernel(const float* __restrict__ 
 
 }  // namespace
 
-int launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* gain, __nv_bfloat16* y, int rows,
-                   int hidden, float eps, const int32_t* row_index, cudaStream_t s) {
+int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hidden, float eps,
+                   const int32_t* row_index, int storage, cudaStream_t s) {
   if (rows <= 0) return SAR_OK;
-  if (hidden % 8) return set_error(SAR_ERR_UNSUPPORTED, "rmsnorm: hidden must be a multiple of 8");
-  rmsnorm_kernel<<<rows, kNormThreads, 0, s>>>(x, gain, y, hidden, eps, row_index);
+  if (hidden % 4) return set_error(SAR_ERR_UNSUPPORTED, "rmsnorm: hidden must be a multiple of 4");
+  if (storage == SAR_STORAGE_BF16)
+    rmsnorm_kernel<__nv_bfloat16><<<rows, kNormThreads, 0, s>>>(x, gain, static_cast<__nv_bfloat16*>(y), hidden,
+                                                               eps, row_index);
+  else
+    rmsnorm_kernel<__half><<<rows, kNormThreads, 0, s>>>(x, gain, static_cast<__half*>(y), hidden, eps, row_index);
   count_launches(1);
   return cuda_error(cudaGetLastError(), "rmsnorm launch");
 }
 
-int launch_embed(const int32_t* tokens, const __nv_bfloat16* table, __nv_bfloat16* out, int rows,
-                 int hidden, int vocab, int* err, cudaStream_t s) {
+int launch_embed(const int32_t* tokens, const void* table, float* out, int rows, int hidden, int vocab,
+                 int storage, int* err, cudaStream_t s) {
   if (rows <= 0) return SAR_OK;
-  embed_kernel<<<rows, 256, 0, s>>>(tokens, table, out, hidden, vocab, err);
+  if (storage == SAR_STORAGE_BF16)
+    embed_kernel<__nv_bfloat16><<<rows, 256, 0, s>>>(tokens, static_cast<const __nv_bfloat16*>(table), out, hidden,
+                                                     vocab, err);
+  else
+    embed_kernel<__half><<<rows, 256, 0, s>>>(tokens, static_cast<const __half*>(table), out, hidden, vocab, err);
   count_launches(1);
   return cuda_error(cudaGetLastError(), "embed launch");
+}
+
+int launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s) {
+  if (n == 0) return SAR_OK;
+  const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
+  bf16_to_f32_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), dst, n);
+  count_launches(1);
+  return cuda_error(cudaGetLastError(), "bf16 to fp32 launch");
+}
+
+int launch_convert_rows(const void* src, void* dst, int rows, int cols, int interleave, int up, int storage,
+                        cudaStream_t s) {
+  if (rows <= 0) return SAR_OK;
+  if (cols % 2) return set_error(SAR_ERR_UNSUPPORTED, "convert: odd row width");
+  const __nv_bfloat16* sp = static_cast<const __nv_bfloat16*>(src);
+  if (storage == SAR_STORAGE_BF16)
+    convert_rows_kernel<__nv_bfloat16><<<rows, 256, 0, s>>>(sp, static_cast<__nv_bfloat16*>(dst), rows, cols,
+                                                           interleave, up);
+  else
+    convert_rows_kernel<__half><<<rows, 256, 0, s>>>(sp, static_cast<__half*>(dst), rows, cols, interleave, up);
+  count_launches(1);
+  return cuda_error(cudaGetLastError(), "convert launch");
 }
 
 int launch_rope_append(const RopeArgs& a, cudaStream_t s) {
   if (a.M <= 0) return SAR_OK;
   if (a.d > 128 || a.d % 2) return set_error(SAR_ERR_UNSUPPORTED, "rope: head_dim > 128");
-  rope_append_kernel<<<a.M, 256, 0, s>>>(a);
+  if (a.storage == SAR_STORAGE_BF16)
+    rope_append_kernel<__nv_bfloat16><<<a.M, 256, 0, s>>>(a);
+  else
+    rope_append_kernel<__half><<<a.M, 256, 0, s>>>(a);
   count_launches(1);
   return cuda_error(cudaGetLastError(), "rope launch");
 }

@@ -105,10 +105,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// Instruction descriptor, kind::f16: fp32 accumulator, A and B of format
+// `fmt` (0 = f16, 1 = bf16; both operands always the same type), both
 // K-major, M = 128, N = n.
-__device__ __forceinline__ uint32_t idesc_bf16(int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+__device__ __forceinline__ uint32_t idesc_f16kind(int n, uint32_t fmt) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
@@ -137,7 +138,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* er
   return ok != 0;
 }
 
-template <int EPI, bool SWAP, int MSUB>
+template <typename T, int EPI, bool SWAP, int MSUB>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const Params p) {
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(p.bn);
+      const uint32_t idesc = idesc_f16kind(p.bn, Elem<T>::kMmaFormat);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (EPI == SAR_EPI_SWIGLU) {
             // packed columns [h*128, h*128+64) gate, [h*128+64, h*128+128) up
             const int F = p.N >> 1;
-            __nv_bfloat16* C = reinterpret_cast<__nv_bfloat16*>(p.c);
+            T* C = reinterpret_cast<T*>(p.c);
 #pragma unroll 1
             for (int h = 0; h < p.bn / 128; ++h) {
 #pragma unroll 1
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   for (int e = 0; e < 8; ++e) {
                     const float a0 = silu(__uint_as_float(g[2 * e])) * __uint_as_float(u[2 * e]);
                     const float a1 = silu(__uint_as_float(g[2 * e + 1])) * __uint_as_float(u[2 * e + 1]);
-                    o[e] = pack_bf16(a0, a1);
+                    o[e] = Elem<T>::pack(a0, a1);
                   }
                   uint4* dst = reinterpret_cast<uint4*>(C + (size_t)row * F + ocol);
                   dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -308,25 +309,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 4; ++e)
                   dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
                                        __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
-              } else {
-                float f[16];
+              } else if constexpr (EPI == SAR_EPI_RESIDUAL) {
+                // fp32 residual stream: C = D + R, both fp32 (R may equal C)
+                const float4* rs = reinterpret_cast<const float4*>(
+                    reinterpret_cast<const float*>(p.r) + (size_t)row * p.N + col);
+                float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.c) + (size_t)row * p.N + col);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]);
-                if constexpr (EPI == SAR_EPI_RESIDUAL) {
-                  const uint4* rs = reinterpret_cast<const uint4*>(
-                      reinterpret_cast<const __nv_bfloat16*>(p.r) + (size_t)row * p.N + col);
-                  const uint4 r0 = rs[0], r1 = rs[1];
-                  const uint32_t rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) {
-                    f[2 * e] += bf16lo(rr[e]);
-                    f[2 * e + 1] += bf16hi(rr[e]);
-                  }
+                for (int e = 0; e < 4; ++e) {
+                  const float4 r4 = rs[e];
+                  dst[e] = make_float4(__uint_as_float(v[4 * e]) + r4.x, __uint_as_float(v[4 * e + 1]) + r4.y,
+                                       __uint_as_float(v[4 * e + 2]) + r4.z, __uint_as_float(v[4 * e + 3]) + r4.w);
                 }
+              } else {
                 uint32_t o[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = pack_bf16(f[2 * e], f[2 * e + 1]);
-                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.c) + (size_t)row * p.N + col);
+                for (int e = 0; e < 8; ++e) o[e] = Elem<T>::pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.c) + (size_t)row * p.N + col);
                 dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
                 dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
               }
@@ -340,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // A tile = one packed block pair: lanes 0..63 gate, 64..127 up
           const int F = p.N >> 1;
           const int ocol = nt * 64 + (lrow & 63);
-          __nv_bfloat16* C = reinterpret_cast<__nv_bfloat16*>(p.c);
+          T* C = reinterpret_cast<T*>(p.c);
 #pragma unroll 1
           for (int j = 0; j < p.bn / 16; ++j) {
             uint32_t v[16];
@@ -359,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int m = tok0 + j * 16 + e;
                 if (m < p.M) {
                   const float a = silu(__uint_as_float(v[e])) * xchg[lrow * 17 + e];
-                  C[(size_t)m * F + ocol] = __float2bfloat16_rn(a);
+                  C[(size_t)m * F + ocol] = Elem<T>::from(a);
                 }
               }
             }
@@ -381,10 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               float f = __uint_as_float(v[e]);
               if constexpr (EPI == SAR_EPI_F32) {
                 reinterpret_cast<float*>(p.c)[idx] = f;
+              } else if constexpr (EPI == SAR_EPI_RESIDUAL) {
+                reinterpret_cast<float*>(p.c)[idx] = f + reinterpret_cast<const float*>(p.r)[idx];
               } else {
-                if constexpr (EPI == SAR_EPI_RESIDUAL)
-                  f += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.r)[idx]);
-                reinterpret_cast<__nv_bfloat16*>(p.c)[idx] = __float2bfloat16_rn(f);
+                reinterpret_cast<T*>(p.c)[idx] = Elem<T>::from(f);
               }
             }
           }
@@ -403,25 +401,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-using KernelFn = void (*)(CUtensorMap, CUtensorMap, Params);
-
-template <int EPI, bool SWAP, int MSUB>
+template <typename T, int EPI, bool SWAP, int MSUB>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&gemm_tc_kernel<EPI, SWAP, MSUB>);
+  return reinterpret_cast<const void*>(&gemm_tc_kernel<T, EPI, SWAP, MSUB>);
 }
 
-const void* pick_kernel(int epi, bool swap, int msub) {
-#define SAR_PICK(E)                                              \
-  if (epi == E) {                                                \
-    if (swap) return kernel_ptr<E, true, 1>();                   \
-    return msub == 2 ? kernel_ptr<E, false, 2>() : kernel_ptr<E, false, 1>(); \
+template <typename T>
+const void* pick_kernel_t(int epi, bool swap, int msub) {
+#define SAR_PICK(E)                                                                 \
+  if (epi == E) {                                                                   \
+    if (swap) return kernel_ptr<T, E, true, 1>();                                   \
+    return msub == 2 ? kernel_ptr<T, E, false, 2>() : kernel_ptr<T, E, false, 1>(); \
   }
-  SAR_PICK(SAR_EPI_BF16)
+  SAR_PICK(SAR_EPI_STORE)
   SAR_PICK(SAR_EPI_RESIDUAL)
   SAR_PICK(SAR_EPI_SWIGLU)
   SAR_PICK(SAR_EPI_F32)
 #undef SAR_PICK
   return nullptr;
+}
+
+const void* pick_kernel(int storage, int epi, bool swap, int msub) {
+  return storage == SAR_STORAGE_BF16 ? pick_kernel_t<__nv_bfloat16>(epi, swap, msub)
+                                     : pick_kernel_t<__half>(epi, swap, msub);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -445,7 +447,8 @@ int pow2_at_least(int v) {
 
 }  // namespace
 
-int make_tmap_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+int make_tmap_16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                 int storage) {
   auto fn = encode_fn();
   if (!fn) return set_error(SAR_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (cols * 2) % 16 || rows == 0 || box_rows == 0 ||
@@ -455,7 +458,9 @@ int make_tmap_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t co
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+  const CUtensorMapDataType dt =
+      storage == SAR_STORAGE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(map, dt, 2, const_cast<void*>(ptr), dims, strides, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return set_error(SAR_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
@@ -517,8 +522,8 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg) {
 }
 
 int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMap& w_map, int M, int N,
-                int K, int epi, void* c, const void* residual, int* err, cudaStream_t s) {
-  const void* fn = pick_kernel(epi, cfg.swap != 0, cfg.msub);
+                int K, int epi, int storage, void* c, const void* residual, int* err, cudaStream_t s) {
+  const void* fn = pick_kernel(storage, epi, cfg.swap != 0, cfg.msub);
   if (!fn) return set_error(SAR_ERR_INVALID_ARG, "gemm: unknown epilogue");
   if (epi == SAR_EPI_RESIDUAL && residual == nullptr)
     return set_error(SAR_ERR_INVALID_ARG, "gemm: residual epilogue without residual");
@@ -536,8 +541,8 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   p.c = c;
   p.r = residual;
   p.err = err;
-  static bool attr_done[4][2][3] = {};
-  bool& done = attr_done[epi][cfg.swap][cfg.msub];
+  static bool attr_done[2][4][2][3] = {};
+  bool& done = attr_done[storage == SAR_STORAGE_BF16][epi][cfg.swap][cfg.msub];
   if (!done) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return cuda_error(e, "gemm: set smem attribute");

@@ -21,10 +21,10 @@ int num_sms();
 
 // ---- GEMM (gemm_tc.cu) -----------------------------------------------------
 
-// Encodes a 2D bf16 tensor map over row-major [rows, cols] with a
-// 64-column x box_rows box and 128-byte swizzle.
-int make_tmap_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
-                   uint32_t box_rows);
+// Encodes a 2D 16-bit (storage type) tensor map over row-major [rows, cols]
+// with a 64-column x box_rows box and 128-byte swizzle.
+int make_tmap_16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                 int storage);
 
 struct GemmCfg {
   int swap = 0;     // weights on the MMA M side
@@ -47,21 +47,28 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg);
 // Launches with maps already encoded: `act_map` over the activations (rows M),
 // `w_map` over the weights; which one is the MMA's A operand depends on cfg.swap.
 int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMap& w_map, int M,
-                int N, int K, int epi, void* c, const void* residual, int* err, cudaStream_t s);
+                int N, int K, int epi, int storage, void* c, const void* residual, int* err,
+                cudaStream_t s);
 
 // ---- elementwise kernels (elementwise.cu) ----------------------------------
-int launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* gain, __nv_bfloat16* y, int rows,
-                   int hidden, float eps, const int32_t* row_index, cudaStream_t s);
-int launch_embed(const int32_t* tokens, const __nv_bfloat16* table, __nv_bfloat16* out, int rows,
-                 int hidden, int vocab, int* err, cudaStream_t s);
+// x: fp32 residual rows; y: storage-type rows; row_index (optional) gathers rows.
+int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hidden, float eps,
+                   const int32_t* row_index, int storage, cudaStream_t s);
+int launch_embed(const int32_t* tokens, const void* table, float* out, int rows, int hidden, int vocab,
+                 int storage, int* err, cudaStream_t s);
+int launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s);
+// bf16 rows -> storage type; interleave=1 places row r of gate (up=0) or up
+// (up=1) into the 64-row-block gate/up packing.
+int launch_convert_rows(const void* src, void* dst, int rows, int cols, int interleave, int up, int storage,
+                        cudaStream_t s);
 struct RopeArgs {
-  __nv_bfloat16* qkv;        // [M, (qh + 2 kvh) * d]
+  void* qkv;                 // [M, (qh + 2 kvh) * d], storage type
   const int32_t* pos;        // [M]
   const int32_t* slot;       // [M] page * page_size + offset
   const double* inv_freq;    // [d/2]
-  __nv_bfloat16* k_cache;    // layer base [num_pages][kvh][page][d]
-  __nv_bfloat16* v_cache;
-  int M, qh, kvh, d, page_size, num_pages;
+  void* k_cache;             // layer base [num_pages][kvh][page][d], storage type
+  void* v_cache;
+  int M, qh, kvh, d, page_size, num_pages, storage;
   int* err;
 };
 int launch_rope_append(const RopeArgs& a, cudaStream_t s);
@@ -69,10 +76,10 @@ int launch_argmax(const float* logits, int rows, int vocab, int32_t* out, cudaSt
 
 // ---- attention (attn_decode.cu, attn_chunk.cu) -----------------------------
 struct DecodeAttnArgs {
-  const __nv_bfloat16* qkv;  // decode rows start here; row stride ld
-  __nv_bfloat16* out;        // decode rows of the attention output; row stride ld_out
-  const __nv_bfloat16* k_cache;
-  const __nv_bfloat16* v_cache;
+  const void* qkv;           // decode rows start here; row stride ld (storage type)
+  void* out;                 // decode rows of the attention output; row stride ld_out
+  const void* k_cache;
+  const void* v_cache;
   const int32_t* items;      // [n_items][4]: decode b, key_begin, key_end, part (-1 = final)
   const int32_t* nkeys;      // [n_decode] keys each decode attends to (ctx + 1)
   const int32_t* bt_off;     // [n_decode] offset into bt
@@ -81,18 +88,18 @@ struct DecodeAttnArgs {
   const int32_t* parts_begin;  // [n_decode] first partial index (or -1)
   const int32_t* parts_count;  // [n_decode]
   float* partials;           // [n_parts][qh][d + 2]
-  int n_items, n_decode, ld, ld_out, qh, kvh, d, page_size, num_pages;
+  int n_items, n_decode, ld, ld_out, qh, kvh, d, page_size, num_pages, storage;
   int* err;
 };
 int launch_decode_attention(const DecodeAttnArgs& a, cudaStream_t s);
 
 struct ChunkAttnArgs {
-  const __nv_bfloat16* qkv;  // chunk rows [0, len); row stride ld
-  __nv_bfloat16* out;        // [len, qh*d]; row stride ld_out
-  const __nv_bfloat16* k_cache;
-  const __nv_bfloat16* v_cache;
+  const void* qkv;           // chunk rows [0, len); row stride ld (storage type)
+  void* out;                 // [len, qh*d]; row stride ld_out
+  const void* k_cache;
+  const void* v_cache;
   const int32_t* bt;         // block table of the prompt
-  int bt_len, start_pos, len, ld, ld_out, qh, kvh, d, page_size, num_pages;
+  int bt_len, start_pos, len, ld, ld_out, qh, kvh, d, page_size, num_pages, storage;
   int* err;
 };
 int launch_chunk_attention(const ChunkAttnArgs& a, cudaStream_t s);

@@ -30,9 +30,11 @@ namespace {
 
 constexpr int kMetaRing = 4;
 
+using st16 = uint16_t;  // one element of the storage type (fp16 or bf16)
+
 struct LayerW {
-  __nv_bfloat16 *wqkv = nullptr, *wo = nullptr, *wgu = nullptr, *wd = nullptr;
-  __nv_bfloat16 *n1 = nullptr, *n2 = nullptr;
+  st16 *wqkv = nullptr, *wo = nullptr, *wgu = nullptr, *wd = nullptr;
+  float *n1 = nullptr, *n2 = nullptr;
   CUtensorMap m_qkv[2], m_o[2], m_gu[2], m_d[2];  // weight maps, box rows 128 / 256
   bool set = false;
 };
@@ -52,14 +54,16 @@ struct sar_model {
   int qd = 0, kvd = 0;  // q width, kv width
   uint8_t* arena = nullptr;
   std::vector<LayerW> L;
-  __nv_bfloat16 *embed = nullptr, *final_norm = nullptr, *lm_head = nullptr;
+  st16 *embed = nullptr, *lm_head = nullptr;
+  float* final_norm = nullptr;
   CUtensorMap m_head[2];
   bool head_set = false;
   double* inv_freq = nullptr;
   // workspace
   uint8_t* ws = nullptr;
-  __nv_bfloat16 *xn = nullptr, *qkv = nullptr, *attn = nullptr, *act = nullptr, *hres = nullptr,
-                *hrows = nullptr, *in_stage = nullptr;
+  st16 *xn = nullptr, *qkv = nullptr, *attn = nullptr, *act = nullptr, *hrows = nullptr;
+  float* hres = nullptr;  // residual stream, fp32
+  void* in_stage = nullptr;
   float* partials = nullptr;
   size_t partials_cap = 0;  // floats
   float* logits_stage = nullptr;
@@ -81,7 +85,7 @@ struct sar_model {
 struct sar_kv {
   const sar_model* m = nullptr;
   int page_size = 0, num_pages = 0;
-  __nv_bfloat16 *k = nullptr, *v = nullptr;
+  uint16_t *k = nullptr, *v = nullptr;
   size_t layer_elems = 0;
 };
 
@@ -123,21 +127,21 @@ struct Prof {
   ~Prof() { prof_end(m, s); }
 };
 
-int weight_maps(CUtensorMap (&maps)[2], const void* w, int rows, int cols) {
-  SAR_TRY(sar::make_tmap_bf16(&maps[0], w, rows, cols, 128));
-  SAR_TRY(sar::make_tmap_bf16(&maps[1], w, rows, cols, 256));
+int weight_maps(CUtensorMap (&maps)[2], const void* w, int rows, int cols, int storage) {
+  SAR_TRY(sar::make_tmap_16(&maps[0], w, rows, cols, 128, storage));
+  SAR_TRY(sar::make_tmap_16(&maps[1], w, rows, cols, 256, storage));
   return SAR_OK;
 }
 
 // GEMM over `rows` activation rows with the weight maps of one matrix.
-int run_gemm(sar_model* m, const __nv_bfloat16* a, int rows, const CUtensorMap (&wmaps)[2], int N, int K,
-             int epi, void* c, const void* r, cudaStream_t s) {
+int run_gemm(sar_model* m, const st16* a, int rows, const CUtensorMap (&wmaps)[2], int N, int K, int epi,
+             void* c, const void* r, cudaStream_t s) {
   sar::GemmCfg cfg;
   SAR_TRY(sar::gemm_config(rows, N, K, epi, SAR_GEMM_AUTO, &cfg));
   CUtensorMap amap;
-  SAR_TRY(sar::make_tmap_bf16(&amap, a, rows, K, cfg.swap ? cfg.b_box_rows : cfg.a_box_rows));
+  SAR_TRY(sar::make_tmap_16(&amap, a, rows, K, cfg.swap ? cfg.b_box_rows : cfg.a_box_rows, m->d.storage));
   const CUtensorMap& wm = cfg.swap ? wmaps[0] : wmaps[cfg.bn == 256 ? 1 : 0];
-  return sar::gemm_launch(cfg, amap, wm, rows, N, K, epi, c, r, m->err, s);
+  return sar::gemm_launch(cfg, amap, wm, rows, N, K, epi, m->d.storage, c, r, m->err, s);
 }
 
 // ---- step planning -----------------------------------------------------------
@@ -298,8 +302,8 @@ int ensure_partials(sar_model* m, size_t floats) {
 }
 
 // The step proper, on device buffers.
-int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, __nv_bfloat16* h,
-             float* logits, void* layer_out, cudaStream_t s) {
+int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float* h, float* logits,
+             void* layer_out, cudaStream_t s) {
   const sar_dims& d = m->d;
   for (int l = 0; l < d.n_layers; ++l)
     if (!m->L[l].set) return set_error(SAR_ERR_INVALID_ARG, "step: layer weights not set");
@@ -323,23 +327,23 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, __nv_
   {
     Prof pr(m, SAR_K_EMBED, s);
     if (b->in_kind == SAR_IN_TOKENS) {
-      SAR_TRY(sar::launch_embed(static_cast<const int32_t*>(in), m->embed, h, M, H, d.vocab, m->err, s));
-    } else if (in != h) {
-      SAR_TRY(check(cudaMemcpyAsync(h, in, (size_t)M * H * 2, cudaMemcpyDeviceToDevice, s), "input copy"));
+      SAR_TRY(sar::launch_embed(static_cast<const int32_t*>(in), m->embed, h, M, H, d.vocab, d.storage, m->err, s));
+    } else {
+      SAR_TRY(sar::launch_bf16_to_f32(in, h, (size_t)M * H, s));  // bf16 rows into the fp32 residual
     }
   }
   for (int l = 0; l < d.n_layers; ++l) {
     LayerW& w = m->L[l];
     {
       Prof pr(m, SAR_K_RMSNORM, s);
-      SAR_TRY(sar::launch_rmsnorm(h, w.n1, m->xn, M, H, d.rms_eps, nullptr, s));
+      SAR_TRY(sar::launch_rmsnorm(h, w.n1, m->xn, M, H, d.rms_eps, nullptr, d.storage, s));
     }
     {
       Prof pr(m, SAR_K_GEMM_QKV, s);
-      SAR_TRY(run_gemm(m, m->xn, M, w.m_qkv, m->qkv_n, H, SAR_EPI_BF16, m->qkv, nullptr, s));
+      SAR_TRY(run_gemm(m, m->xn, M, w.m_qkv, m->qkv_n, H, SAR_EPI_STORE, m->qkv, nullptr, s));
     }
-    __nv_bfloat16* kc = kv->k + (size_t)l * kv->layer_elems;
-    __nv_bfloat16* vc = kv->v + (size_t)l * kv->layer_elems;
+    uint16_t* kc = kv->k + (size_t)l * kv->layer_elems;
+    uint16_t* vc = kv->v + (size_t)l * kv->layer_elems;
     {
       Prof pr(m, SAR_K_ROPE_APPEND, s);
       sar::RopeArgs ra;
@@ -355,6 +359,7 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, __nv_
       ra.d = d.head_dim;
       ra.page_size = kv->page_size;
       ra.num_pages = kv->num_pages;
+      ra.storage = d.storage;
       ra.err = m->err;
       SAR_TRY(sar::launch_rope_append(ra, s));
     }
@@ -376,6 +381,7 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, __nv_
       ca.d = d.head_dim;
       ca.page_size = kv->page_size;
       ca.num_pages = kv->num_pages;
+      ca.storage = d.storage;
       ca.err = m->err;
       SAR_TRY(sar::launch_chunk_attention(ca, s));
     }
@@ -384,6 +390,7 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, __nv_
       sar::DecodeAttnArgs da;
       da.qkv = m->qkv + (size_t)p.Lp * m->qkv_n;  // zero-copy row split
       da.out = m->attn + (size_t)p.Lp * m->qd;
+      da.storage = d.storage;
       da.k_cache = kc;
       da.v_cache = vc;
       da.items = md + p.o_items;
@@ -412,7 +419,7 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, __nv_
     }
     {
       Prof pr(m, SAR_K_RMSNORM, s);
-      SAR_TRY(sar::launch_rmsnorm(h, w.n2, m->xn, M, H, d.rms_eps, nullptr, s));
+      SAR_TRY(sar::launch_rmsnorm(h, w.n2, m->xn, M, H, d.rms_eps, nullptr, d.storage, s));
     }
     {
       Prof pr(m, SAR_K_GEMM_GATEUP, s);
@@ -423,14 +430,14 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, __nv_
       SAR_TRY(run_gemm(m, m->act, M, w.m_d, H, d.ffn, SAR_EPI_RESIDUAL, h, h, s));
     }
     if (layer_out)
-      SAR_TRY(check(cudaMemcpyAsync(static_cast<__nv_bfloat16*>(layer_out) + (size_t)l * M * H, h, (size_t)M * H * 2,
+      SAR_TRY(check(cudaMemcpyAsync(static_cast<float*>(layer_out) + (size_t)l * M * H, h, (size_t)M * H * 4,
                                     cudaMemcpyDeviceToDevice, s),
                     "layer output copy"));
   }
   if (logits) {
     {
       Prof pr(m, SAR_K_HEAD_NORM, s);
-      SAR_TRY(sar::launch_rmsnorm(h, m->final_norm, m->hrows, p.R, H, d.rms_eps, md + p.o_rows, s));
+      SAR_TRY(sar::launch_rmsnorm(h, m->final_norm, m->hrows, p.R, H, d.rms_eps, md + p.o_rows, d.storage, s));
     }
     {
       Prof pr(m, SAR_K_GEMM_HEAD, s);
@@ -455,6 +462,8 @@ int sar_model_create(const sar_dims* dims, sar_model** out) {
     return set_error(SAR_ERR_UNSUPPORTED, "model: n_q_heads must be 1..8 times n_kv_heads");
   if (d.hidden % 64 || d.ffn % 64 || (d.n_q_heads * d.head_dim) % 64 || (d.n_kv_heads * d.head_dim) % 64)
     return set_error(SAR_ERR_UNSUPPORTED, "model: widths must be multiples of 64");
+  if (d.storage != SAR_STORAGE_F16 && d.storage != SAR_STORAGE_BF16)
+    return set_error(SAR_ERR_INVALID_ARG, "model: storage must be SAR_STORAGE_F16 or SAR_STORAGE_BF16");
   sar_model* m = new sar_model();
   m->d = d;
   m->qd = d.n_q_heads * d.head_dim;
@@ -462,8 +471,8 @@ int sar_model_create(const sar_dims* dims, sar_model** out) {
   m->qkv_n = m->qd + 2 * m->kvd;
   const size_t H = d.hidden, F = d.ffn;
   const size_t per_layer = align256((size_t)m->qkv_n * H * 2) + align256(H * m->qd * 2) + align256(2 * F * H * 2) +
-                           align256(H * F * 2) + 2 * align256(H * 2);
-  const size_t head = d.vocab ? 2 * align256((size_t)d.vocab * H * 2) + align256(H * 2) : 0;
+                           align256(H * F * 2) + 2 * align256(H * 4);
+  const size_t head = d.vocab ? 2 * align256((size_t)d.vocab * H * 2) + align256(H * 4) : 0;
   cudaError_t e = cudaMalloc(&m->arena, per_layer * d.n_layers + head);
   if (e != cudaSuccess) {
     delete m;
@@ -471,26 +480,27 @@ int sar_model_create(const sar_dims* dims, sar_model** out) {
   }
   m->L.resize(d.n_layers);
   uint8_t* p = m->arena;
-  auto take = [&](size_t bytes) { uint8_t* r = p; p += align256(bytes); return reinterpret_cast<__nv_bfloat16*>(r); };
+  auto take = [&](size_t bytes) { uint8_t* r = p; p += align256(bytes); return reinterpret_cast<st16*>(r); };
+  auto takef = [&](size_t bytes) { uint8_t* r = p; p += align256(bytes); return reinterpret_cast<float*>(r); };
   for (int l = 0; l < d.n_layers; ++l) {
     LayerW& w = m->L[l];
     w.wqkv = take((size_t)m->qkv_n * H * 2);
     w.wo = take(H * m->qd * 2);
     w.wgu = take(2 * F * H * 2);
     w.wd = take(H * F * 2);
-    w.n1 = take(H * 2);
-    w.n2 = take(H * 2);
+    w.n1 = takef(H * 4);
+    w.n2 = takef(H * 4);
   }
   if (d.vocab) {
     m->embed = take((size_t)d.vocab * H * 2);
     m->lm_head = take((size_t)d.vocab * H * 2);
-    m->final_norm = take(H * 2);
+    m->final_norm = takef(H * 4);
   }
   // step workspace
   const size_t T = d.max_tokens;
   const size_t R = (size_t)d.max_decodes + 1;
   const size_t ws = align256(T * H * 2) + align256(T * m->qkv_n * 2) + align256(T * m->qd * 2) + align256(T * F * 2) +
-                    align256(T * H * 2) + align256(R * H * 2) + align256(T * H * 2) + 256;
+                    align256(T * H * 4) + align256(R * H * 2) + align256(T * H * 2) + 256;
   e = cudaMalloc(&m->ws, ws);
   if (e == cudaSuccess) e = cudaMalloc(&m->err, 16);
   if (e == cudaSuccess) e = cudaMemset(m->err, 0, 16);
@@ -504,7 +514,7 @@ int sar_model_create(const sar_dims* dims, sar_model** out) {
   m->qkv = take(T * m->qkv_n * 2);
   m->attn = take(T * m->qd * 2);
   m->act = take(T * F * 2);
-  m->hres = take(T * H * 2);
+  m->hres = takef(T * H * 4);
   m->hrows = take(R * H * 2);
   m->in_stage = take(T * H * 2);
   // rotary frequencies base^(-2i/d), double precision
@@ -529,27 +539,21 @@ int sar_model_set_layer(sar_model* m, int32_t layer, const sar_layer_weights* w,
     return set_error(SAR_ERR_INVALID_ARG, "set_layer: null weight");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   LayerW& L = m->L[layer];
-  const size_t H = m->d.hidden, F = m->d.ffn;
-  auto cp = [&](void* dst, const void* src, size_t bytes) {
-    return check(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s), "set_layer copy");
-  };
-  SAR_TRY(cp(L.wqkv, w->wq, (size_t)m->qd * H * 2));
-  SAR_TRY(cp(L.wqkv + (size_t)m->qd * H, w->wk, (size_t)m->kvd * H * 2));
-  SAR_TRY(cp(L.wqkv + (size_t)(m->qd + m->kvd) * H, w->wv, (size_t)m->kvd * H * 2));
-  SAR_TRY(cp(L.wo, w->wo, H * m->qd * 2));
-  // gate/up interleaved in 64-row blocks: [g 64][u 64][g 64][u 64]...
-  const size_t blk = 64 * H * 2;
-  SAR_TRY(check(cudaMemcpy2DAsync(L.wgu, 2 * blk, w->wg, blk, blk, F / 64, cudaMemcpyDeviceToDevice, s), "gate pack"));
-  SAR_TRY(check(cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(L.wgu) + blk, 2 * blk, w->wu, blk, blk, F / 64,
-                                  cudaMemcpyDeviceToDevice, s),
-                "up pack"));
-  SAR_TRY(cp(L.wd, w->wd, H * F * 2));
-  SAR_TRY(cp(L.n1, w->norm1, H * 2));
-  SAR_TRY(cp(L.n2, w->norm2, H * 2));
-  SAR_TRY(weight_maps(L.m_qkv, L.wqkv, m->qkv_n, H));
-  SAR_TRY(weight_maps(L.m_o, L.wo, H, m->qd));
-  SAR_TRY(weight_maps(L.m_gu, L.wgu, 2 * F, H));
-  SAR_TRY(weight_maps(L.m_d, L.wd, H, F));
+  const int H = m->d.hidden, F = m->d.ffn, st = m->d.storage;
+  // bf16 in, storage type out; Q/K/V stacked, gate/up interleaved in 64-row blocks
+  SAR_TRY(sar::launch_convert_rows(w->wq, L.wqkv, m->qd, H, 0, 0, st, s));
+  SAR_TRY(sar::launch_convert_rows(w->wk, L.wqkv + (size_t)m->qd * H, m->kvd, H, 0, 0, st, s));
+  SAR_TRY(sar::launch_convert_rows(w->wv, L.wqkv + (size_t)(m->qd + m->kvd) * H, m->kvd, H, 0, 0, st, s));
+  SAR_TRY(sar::launch_convert_rows(w->wo, L.wo, H, m->qd, 0, 0, st, s));
+  SAR_TRY(sar::launch_convert_rows(w->wg, L.wgu, F, H, 1, 0, st, s));
+  SAR_TRY(sar::launch_convert_rows(w->wu, L.wgu, F, H, 1, 1, st, s));
+  SAR_TRY(sar::launch_convert_rows(w->wd, L.wd, H, F, 0, 0, st, s));
+  SAR_TRY(sar::launch_bf16_to_f32(w->norm1, L.n1, H, s));
+  SAR_TRY(sar::launch_bf16_to_f32(w->norm2, L.n2, H, s));
+  SAR_TRY(weight_maps(L.m_qkv, L.wqkv, m->qkv_n, H, st));
+  SAR_TRY(weight_maps(L.m_o, L.wo, H, m->qd, st));
+  SAR_TRY(weight_maps(L.m_gu, L.wgu, 2 * F, H, st));
+  SAR_TRY(weight_maps(L.m_d, L.wd, H, F, st));
   L.set = true;
   return SAR_OK;
 }
@@ -558,12 +562,12 @@ int sar_model_set_head(sar_model* m, const void* embed, const void* final_norm, 
   if (!m) return set_error(SAR_ERR_INVALID_ARG, "set_head: null model");
   if (m->d.vocab == 0) return set_error(SAR_ERR_INVALID_ARG, "set_head: model has no vocabulary");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t H = m->d.hidden, V = m->d.vocab;
-  if (embed) SAR_TRY(check(cudaMemcpyAsync(m->embed, embed, V * H * 2, cudaMemcpyDeviceToDevice, s), "embed copy"));
-  if (final_norm) SAR_TRY(check(cudaMemcpyAsync(m->final_norm, final_norm, H * 2, cudaMemcpyDeviceToDevice, s), "norm copy"));
+  const int H = m->d.hidden, V = m->d.vocab, st = m->d.storage;
+  if (embed) SAR_TRY(sar::launch_convert_rows(embed, m->embed, V, H, 0, 0, st, s));
+  if (final_norm) SAR_TRY(sar::launch_bf16_to_f32(final_norm, m->final_norm, H, s));
   if (lm_head) {
-    SAR_TRY(check(cudaMemcpyAsync(m->lm_head, lm_head, V * H * 2, cudaMemcpyDeviceToDevice, s), "head copy"));
-    SAR_TRY(weight_maps(m->m_head, m->lm_head, (int)V, (int)H));
+    SAR_TRY(sar::launch_convert_rows(lm_head, m->lm_head, V, H, 0, 0, st, s));
+    SAR_TRY(weight_maps(m->m_head, m->lm_head, V, H, st));
   }
   if (final_norm && lm_head) m->head_set = true;
   return SAR_OK;
@@ -644,7 +648,7 @@ int sar_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, void*
              void* layer_out, void* stream) {
   if (!m || !kv || !b || !in) return set_error(SAR_ERR_INVALID_ARG, "step: null argument");
   if (kv->m != m) return set_error(SAR_ERR_INVALID_ARG, "step: KV cache belongs to another model");
-  __nv_bfloat16* h = hidden_out ? static_cast<__nv_bfloat16*>(hidden_out) : m->hres;
+  float* h = hidden_out ? static_cast<float*>(hidden_out) : m->hres;
   return run_step(m, kv, b, in, h, logits_out, layer_out, static_cast<cudaStream_t>(stream));
 }
 
@@ -663,7 +667,7 @@ int sar_step_host(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, 
   }
   SAR_TRY(run_step(m, kv, b, m->in_stage, m->hres, logits_out ? m->logits_stage : nullptr, nullptr, s));
   if (hidden_out)
-    SAR_TRY(check(cudaMemcpyAsync(hidden_out, m->hres, (size_t)M * m->d.hidden * 2, cudaMemcpyDeviceToHost, s), "step_host: hidden copy"));
+    SAR_TRY(check(cudaMemcpyAsync(hidden_out, m->hres, (size_t)M * m->d.hidden * 4, cudaMemcpyDeviceToHost, s), "step_host: hidden copy"));
   if (logits_out)
     SAR_TRY(check(cudaMemcpyAsync(logits_out, m->logits_stage, (size_t)R * m->d.vocab * 4, cudaMemcpyDeviceToHost, s),
                   "step_host: logits copy"));
@@ -721,9 +725,10 @@ int sar_model_debug_buffer(sar_model* m, int32_t which, void** out) {
 // ---- single-kernel entry points ------------------------------------------------
 
 int sar_op_gemm(const void* a, const void* w, void* c, const void* residual, int32_t M, int32_t N, int32_t K,
-                int32_t epilogue, int32_t variant, void* stream) {
+                int32_t epilogue, int32_t variant, int32_t storage, void* stream) {
   if (!a || !w || !c) return set_error(SAR_ERR_INVALID_ARG, "op_gemm: null pointer");
-  if (epilogue < SAR_EPI_BF16 || epilogue > SAR_EPI_F32) return set_error(SAR_ERR_INVALID_ARG, "op_gemm: bad epilogue");
+  if (epilogue < SAR_EPI_STORE || epilogue > SAR_EPI_F32) return set_error(SAR_ERR_INVALID_ARG, "op_gemm: bad epilogue");
+  if (storage != SAR_STORAGE_F16 && storage != SAR_STORAGE_BF16) return set_error(SAR_ERR_INVALID_ARG, "op_gemm: bad storage");
   static int* err = nullptr;
   if (!err) {
     SAR_TRY(check(cudaMalloc(&err, 16), "op_gemm: flag buffer"));
@@ -732,15 +737,17 @@ int sar_op_gemm(const void* a, const void* w, void* c, const void* residual, int
   sar::GemmCfg cfg;
   SAR_TRY(sar::gemm_config(M, N, K, epilogue, variant, &cfg));
   CUtensorMap amap, wmap;
-  SAR_TRY(sar::make_tmap_bf16(&amap, a, M, K, cfg.swap ? cfg.b_box_rows : cfg.a_box_rows));
-  SAR_TRY(sar::make_tmap_bf16(&wmap, w, N, K, cfg.swap ? cfg.a_box_rows : cfg.b_box_rows));
-  return sar::gemm_launch(cfg, amap, wmap, M, N, K, epilogue, c, residual, err, static_cast<cudaStream_t>(stream));
+  SAR_TRY(sar::make_tmap_16(&amap, a, M, K, cfg.swap ? cfg.b_box_rows : cfg.a_box_rows, storage));
+  SAR_TRY(sar::make_tmap_16(&wmap, w, N, K, cfg.swap ? cfg.a_box_rows : cfg.b_box_rows, storage));
+  return sar::gemm_launch(cfg, amap, wmap, M, N, K, epilogue, storage, c, residual, err, static_cast<cudaStream_t>(stream));
 }
 
-int sar_op_rmsnorm(const void* x, const void* gain, void* y, int32_t rows, int32_t hidden, float eps, void* stream) {
+int sar_op_rmsnorm(const void* x, const void* gain, void* y, int32_t rows, int32_t hidden, float eps, int32_t storage,
+                   void* stream) {
   if (!x || !gain || !y || rows < 0 || hidden <= 0) return set_error(SAR_ERR_INVALID_ARG, "op_rmsnorm: bad argument");
-  return sar::launch_rmsnorm(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(gain),
-                             static_cast<__nv_bfloat16*>(y), rows, hidden, eps, nullptr, static_cast<cudaStream_t>(stream));
+  if (storage != SAR_STORAGE_F16 && storage != SAR_STORAGE_BF16) return set_error(SAR_ERR_INVALID_ARG, "op_rmsnorm: bad storage");
+  return sar::launch_rmsnorm(static_cast<const float*>(x), static_cast<const float*>(gain), y, rows, hidden, eps,
+                             nullptr, storage, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -64,6 +64,7 @@ def run_trace(model, kv, trace, prompt_tokens: dict, tau: int, tile: int = 128, 
     sampled_host = torch.empty(max_batch + 1, dtype=torch.int32).pin_memory()
     tok_host = torch.empty(tau, dtype=torch.int32).pin_memory()
     last_emit = {}
+    by_req = {r.req: r for r in trace}
     t0 = time.perf_counter()
     i = 0
     while True:
@@ -108,14 +109,11 @@ def run_trace(model, kv, trace, prompt_tokens: dict, tau: int, tile: int = 128, 
             res.batches.append((pre, decs))
             res.sampled.append(sampled)
         # latency bookkeeping: the chunk that completes a prompt emits its first token
-        req_by_arrival = {r.req: r for r in trace}
-        j = 0
         if pre is not None:
             req, start, n, _ = pre
-            if start + n == req_by_arrival[req].prompt_len:
-                res.ttft[req] = wall - req_by_arrival[req].arrival
+            if start + n == by_req[req].prompt_len:
+                res.ttft[req] = wall - by_req[req].arrival
                 last_emit[req] = wall
-            j = 1
         for (req, _, _) in decs:
             if req in last_emit:
                 res.tbt.append(wall - last_emit[req])

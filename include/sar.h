@@ -22,7 +22,10 @@
  *    "host" pointers are ordinary host memory.  A stream argument is a
  *    cudaStream_t passed as void* (NULL = legacy default stream).
  *  - Matrices are row-major.  Weights use the linear-layer layout
- *    [out_features, in_features].  Activations are bf16 [rows, hidden].
+ *    [out_features, in_features] and are passed in bf16.  Inside, the model
+ *    stores weights, activations and the KV cache in one 16-bit storage type
+ *    (fp16 by default, bf16 on request), accumulates every product in fp32
+ *    and carries the residual stream between layers in fp32.
  *  - Work on a stream is asynchronous; device-side error flags (a wait that
  *    gave up, an index out of bounds) are read back by sar_sync_status().
  */
@@ -59,12 +62,17 @@ int64_t sar_launch_count(void);
 
 /* ---- model ------------------------------------------------------------- */
 
+/* Storage type of weights, activations and KV pages.  fp16 keeps 3 more
+ * mantissa bits than bf16 at the same width and tensor-core rate; bf16 weights
+ * convert to it exactly (apart from magnitudes below 2^-14). */
+enum { SAR_STORAGE_F16 = 0, SAR_STORAGE_BF16 = 1 };
+
 /* Decoder shape (Llama/Mistral-style: RMSNorm, GQA attention with rotary
  * embedding, SwiGLU FFN).  head_dim must be 64 or 128; hidden, ffn and
  * n_q_heads*head_dim multiples of 64; n_q_heads a multiple of n_kv_heads with
  * at most 8 query heads per KV head.  vocab = 0 means no embedding / head.
  * max_tokens bounds Lp+Bd of any step (sizes the step workspace);
- * max_decodes bounds Bd. */
+ * max_decodes bounds Bd; storage is SAR_STORAGE_F16 or SAR_STORAGE_BF16. */
 typedef struct sar_dims {
   int32_t n_layers;
   int32_t hidden;
@@ -77,6 +85,7 @@ typedef struct sar_dims {
   float rope_base;
   int32_t max_tokens;
   int32_t max_decodes;
+  int32_t storage;
 } sar_dims;
 
 /* One layer's weights: device bf16, [out, in] row-major; norm gains bf16 [hidden]. */
@@ -97,9 +106,10 @@ typedef struct sar_layer_weights {
  * sar_model_destroy. */
 int sar_model_create(const sar_dims* dims, sar_model** out);
 
-/* Copies layer `layer`'s weights into the model's arena, repacking them
- * (Q/K/V fused into one [q+2kv, hidden] matrix; gate and up interleaved in
- * blocks of 64 rows so one GEMM epilogue forms silu(gate)*up).  Runs on
+/* Copies layer `layer`'s bf16 weights into the model's arena, converting
+ * them to the storage type and repacking them (Q/K/V fused into one
+ * [q+2kv, hidden] matrix; gate and up interleaved in blocks of 64 rows so one
+ * GEMM epilogue forms silu(gate)*up; norm gains kept in fp32).  Runs on
  * `stream`; the caller may free its tensors once the stream has passed the
  * copies (e.g. after a stream synchronise). */
 int sar_model_set_layer(sar_model* m, int32_t layer, const sar_layer_weights* w, void* stream);
@@ -118,7 +128,8 @@ int sar_sync_status(sar_model* m);
 /* ---- paged KV cache ---------------------------------------------------- */
 
 /* One device arena for K and one for V, each laid out
- * [n_layers][num_pages][n_kv_heads][page_size][head_dim] bf16, zeroed.
+ * [n_layers][num_pages][n_kv_heads][page_size][head_dim] in the model's
+ * storage type, zeroed.
  * page_size must be 16, 32 or 64 tokens. */
 int sar_kv_create(const sar_model* m, int32_t page_size, int32_t num_pages, sar_kv** out);
 
@@ -165,12 +176,12 @@ typedef struct sar_batch {
 
 /* Runs every layer over the stacked rows M = Lp + n_decode and then the head.
  *   in         device: bf16 [M, hidden] (SAR_IN_HIDDEN) or int32 [M] token ids
- *   hidden_out device bf16 [M, hidden]: last layer's residual stream (before
+ *   hidden_out device fp32 [M, hidden]: last layer's residual stream (before
  *              the final norm); may be NULL
  *   logits_out device fp32 [R, vocab], R = has_prefill + n_decode: logits of
  *              the chunk's last row (if any) then of every decode row; may be
  *              NULL (head skipped); must be NULL when vocab = 0
- *   layer_out  device bf16 [n_layers, M, hidden]: every layer's output; may be NULL
+ *   layer_out  device fp32 [n_layers, M, hidden]: every layer's output; may be NULL
  * New K/V of all rows are written into `kv`.  Asynchronous on `stream`; the
  * host block tables are consumed before the call returns. */
 int sar_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, void* hidden_out,

@@ -23,14 +23,14 @@ extern "C" {
 
 /* Epilogues applied to the fp32 accumulator D = A . W^T. */
 enum {
-  SAR_EPI_BF16 = 0,     /* C bf16 [M, N] = D                                         */
-  SAR_EPI_RESIDUAL = 1, /* C bf16 [M, N] = D + R (R bf16 [M, N]; R may equal C)      */
-  SAR_EPI_SWIGLU = 2,   /* W is gate/up interleaved in 64-row blocks, [2F, K]; C bf16
-                           [M, F] = silu(D_gate) * D_up                               */
+  SAR_EPI_STORE = 0,    /* C [M, N] in the storage type = D                          */
+  SAR_EPI_RESIDUAL = 1, /* C fp32 [M, N] = D + R (R fp32 [M, N]; R may equal C)      */
+  SAR_EPI_SWIGLU = 2,   /* W is gate/up interleaved in 64-row blocks, [2F, K]; C [M, F]
+                           in the storage type = silu(D_gate) * D_up                 */
   SAR_EPI_F32 = 3       /* C fp32 [M, N] = D                                         */
 };
 
-/* Tilings.  All run tcgen05 MMAs (bf16 x bf16 -> fp32 in tensor memory) fed by
+/* Tilings.  All run tcgen05 MMAs (16-bit x 16-bit -> fp32 in tensor memory) fed by
  * TMA from 128-byte-swizzled shared memory, in a persistent kernel. */
 enum {
   SAR_GEMM_AUTO = 0,  /* the library's choice for (M, N, K)                        */
@@ -42,25 +42,27 @@ enum {
                              tile) x 128 weight rows per tile                        */
 };
 
-/* C = epilogue(A . W^T).  A bf16 [M, K], W bf16 [N, K] (device, row-major,
- * 16-byte aligned, K a multiple of 64, N a multiple of 64, M >= 1).
- * For SAR_EPI_SWIGLU, N is 2F (the packed rows) and C has F columns.
- * Returns SAR_ERR_UNSUPPORTED for shapes a variant cannot take. */
+/* C = epilogue(A . W^T).  A [M, K], W [N, K] in the storage type `storage`
+ * (SAR_STORAGE_F16 or SAR_STORAGE_BF16; device, row-major, 16-byte aligned,
+ * K a multiple of 64, N a multiple of 64, M >= 1).  For SAR_EPI_SWIGLU, N is
+ * 2F (the packed rows) and C has F columns.  Returns SAR_ERR_UNSUPPORTED for
+ * shapes a variant cannot take. */
 int sar_op_gemm(const void* a, const void* w, void* c, const void* residual, int32_t M, int32_t N,
-                int32_t K, int32_t epilogue, int32_t variant, void* stream);
+                int32_t K, int32_t epilogue, int32_t variant, int32_t storage, void* stream);
 
-/* y = x * rsqrt(mean(x^2) + eps) * gain per row; bf16 [rows, hidden]. */
+/* y = x * rsqrt(mean(x^2) + eps) * gain per row: x fp32 [rows, hidden] (the
+ * residual stream), gain fp32 [hidden], y [rows, hidden] in `storage`. */
 int sar_op_rmsnorm(const void* x, const void* gain, void* y, int32_t rows, int32_t hidden,
-                   float eps, void* stream);
+                   float eps, int32_t storage, void* stream);
 
 /* Device address of a step workspace buffer, valid until sar_model_destroy;
  * after a step on a one-layer model it holds that layer's intermediates.
- *   0: normed rows     bf16 [max_tokens, hidden]
- *   1: q|k|v rows      bf16 [max_tokens, (n_q_heads + 2 n_kv_heads) * head_dim]
- *                      (q and k after the rotary embedding)
- *   2: attention rows  bf16 [max_tokens, n_q_heads * head_dim]
- *   3: SwiGLU rows     bf16 [max_tokens, ffn]
- *   4: residual stream bf16 [max_tokens, hidden] (when the step had no hidden_out) */
+ *   0: normed rows     [max_tokens, hidden] (storage type)
+ *   1: q|k|v rows      [max_tokens, (n_q_heads + 2 n_kv_heads) * head_dim]
+ *                      (storage type; q and k after the rotary embedding)
+ *   2: attention rows  [max_tokens, n_q_heads * head_dim] (storage type)
+ *   3: SwiGLU rows     [max_tokens, ffn] (storage type)
+ *   4: residual stream fp32 [max_tokens, hidden] (when the step had no hidden_out) */
 int sar_model_debug_buffer(sar_model* m, int32_t which, void** out);
 
 #ifdef __cplusplus

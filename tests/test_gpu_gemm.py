@@ -1,4 +1,5 @@
-"""The tcgen05 GEMM (all tilings, all epilogues) against float64 matmul of the same bf16 operands."""
+"""The tcgen05 GEMM (all tilings, all epilogues, fp16 and bf16 operands) against
+float64 matmul of the same operand values."""
 
 import pytest
 import torch
@@ -11,20 +12,25 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def operands(M, N, K, seed=0):
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def operands(M, N, K, seed=0, dtype=torch.float16):
     g = synth.generator(seed)
-    a = synth.normal(g, (M, K), dtype=torch.bfloat16)
-    w = synth.normal(g, (N, K), 0.05, dtype=torch.bfloat16)
-    r = synth.normal(g, (M, N), dtype=torch.bfloat16)
+    a = synth.normal(g, (M, K), dtype=torch.bfloat16).to(dtype)
+    w = synth.normal(g, (N, K), 0.05, dtype=torch.bfloat16).to(dtype)
+    r = synth.normal(g, (M, N), dtype=torch.float32)
     return a, w, r
 
 
-def close(got, ref, rel_tol=6e-3):
+def close(got, ref, dtype=torch.bfloat16, rel_tol=6e-3):
+    """Output rounded once to the storage type: half an ulp relative, plus accumulation noise."""
     got = got.double().cpu()
+    ulp = 2 ** -8 if dtype == torch.bfloat16 else 2 ** -11
     err = (got - ref).abs().max().item()
     scale = ref.abs().max().item()
     rel = ((got - ref).norm() / ref.norm()).item()
-    assert rel <= rel_tol and err <= 2 ** -7 * scale + 1e-3, (rel, err, scale)
+    assert rel <= rel_tol and err <= ulp * scale + 1e-3, (rel, err, scale)
 
 
 VARIANTS = {
@@ -41,27 +47,32 @@ SHAPES = [(1, 256, 256), (16, 512, 256), (65, 768, 512), (128, 256, 1024), (200,
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
 @pytest.mark.parametrize("variant", list(VARIANTS))
-def test_gemm_bf16(M, N, K, variant):
+@pytest.mark.parametrize("dt", list(DTYPES))
+def test_gemm_store(M, N, K, variant, dt):
     if variant == "swap" and M > 256:
         pytest.skip("swap tiling holds at most 256 token rows")
-    a, w, _ = operands(M, N, K)
-    c = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    dtype = DTYPES[dt]
+    a, w, _ = operands(M, N, K, dtype=dtype)
+    c = torch.empty(M, N, dtype=dtype, device=DEV)
     sar.gemm(a.to(DEV), w.to(DEV), c, variant=VARIANTS[variant])
     torch.cuda.synchronize()
-    close(c, a.double() @ w.double().T)
+    close(c, a.double() @ w.double().T, dtype)
 
 
 @pytest.mark.parametrize("M", [3, 130, 384])
-@pytest.mark.parametrize("variant", ["auto", "m128n256", "swap"])
-def test_gemm_residual_in_place(M, variant):
+@pytest.mark.parametrize("variant", ["auto", "m128n256", "swap", "m256n128"])
+@pytest.mark.parametrize("dt", list(DTYPES))
+def test_gemm_residual_in_place(M, variant, dt):
+    """fp32 residual stream: h = h + a . w^T in place, no rounding to 16 bits."""
     if variant == "swap" and M > 256:
         pytest.skip("swap tiling holds at most 256 token rows")
     N, K = 512, 512
-    a, w, r = operands(M, N, K, 1)
+    a, w, r = operands(M, N, K, 1, DTYPES[dt])
     h = r.to(DEV).clone()
     sar.gemm(a.to(DEV), w.to(DEV), h, residual=h, epilogue=sar.SAR_EPI_RESIDUAL, variant=VARIANTS[variant])
     torch.cuda.synchronize()
-    close(h, a.double() @ w.double().T + r.double())
+    ref = a.double() @ w.double().T + r.double()
+    assert ((h.double().cpu() - ref).abs().max() / ref.abs().max()).item() < 1e-5
 
 
 def pack_gate_up(wg, wu):
@@ -72,27 +83,30 @@ def pack_gate_up(wg, wu):
 
 @pytest.mark.parametrize("M", [5, 64, 200, 256, 384])
 @pytest.mark.parametrize("variant", ["auto", "m128n128", "m128n256", "swap", "m256n128"])
-def test_gemm_swiglu(M, variant):
+@pytest.mark.parametrize("dt", list(DTYPES))
+def test_gemm_swiglu(M, variant, dt):
     if variant == "swap" and M > 256:
         pytest.skip("swap tiling holds at most 256 token rows")
+    dtype = DTYPES[dt]
     F, K = 512, 256
     g = synth.generator(2)
-    a = synth.normal(g, (M, K), dtype=torch.bfloat16)
-    wg = synth.normal(g, (F, K), 0.05, dtype=torch.bfloat16)
-    wu = synth.normal(g, (F, K), 0.05, dtype=torch.bfloat16)
-    out = torch.empty(M, F, dtype=torch.bfloat16, device=DEV)
+    a = synth.normal(g, (M, K), dtype=torch.bfloat16).to(dtype)
+    wg = synth.normal(g, (F, K), 0.05, dtype=torch.bfloat16).to(dtype)
+    wu = synth.normal(g, (F, K), 0.05, dtype=torch.bfloat16).to(dtype)
+    out = torch.empty(M, F, dtype=dtype, device=DEV)
     sar.gemm(a.to(DEV), pack_gate_up(wg, wu).to(DEV), out, epilogue=sar.SAR_EPI_SWIGLU,
              variant=VARIANTS[variant])
     torch.cuda.synchronize()
     gg = a.double() @ wg.double().T
     uu = a.double() @ wu.double().T
-    close(out, gg / (1 + torch.exp(-gg)) * uu)
+    close(out, gg / (1 + torch.exp(-gg)) * uu, dtype)
 
 
 @pytest.mark.parametrize("M", [1, 65, 129])
-def test_gemm_f32_head(M):
+@pytest.mark.parametrize("dt", list(DTYPES))
+def test_gemm_f32_head(M, dt):
     N, K = 1024, 512
-    a, w, _ = operands(M, N, K, 3)
+    a, w, _ = operands(M, N, K, 3, DTYPES[dt])
     c = torch.empty(M, N, dtype=torch.float32, device=DEV)
     sar.gemm(a.to(DEV), w.to(DEV), c, epilogue=sar.SAR_EPI_F32)
     torch.cuda.synchronize()
@@ -102,9 +116,9 @@ def test_gemm_f32_head(M):
 
 
 def test_gemm_unsupported_shapes_are_rejected():
-    a = torch.zeros(300, 256, dtype=torch.bfloat16, device=DEV)
-    w = torch.zeros(256, 256, dtype=torch.bfloat16, device=DEV)
-    c = torch.zeros(300, 256, dtype=torch.bfloat16, device=DEV)
+    a = torch.zeros(300, 256, dtype=torch.float16, device=DEV)
+    w = torch.zeros(256, 256, dtype=torch.float16, device=DEV)
+    c = torch.zeros(300, 256, dtype=torch.float16, device=DEV)
     with pytest.raises(sar.SarError):
         sar.gemm(a, w, c, variant=sar.SAR_GEMM_SWAP)
     with pytest.raises(sar.SarError):
@@ -112,13 +126,14 @@ def test_gemm_unsupported_shapes_are_rejected():
 
 
 @pytest.mark.parametrize("rows,hidden", [(1, 256), (260, 256), (512, 4096), (3, 7168)])
-def test_rmsnorm_kernel(rows, hidden):
+@pytest.mark.parametrize("dt", list(DTYPES))
+def test_rmsnorm_kernel(rows, hidden, dt):
     g = synth.generator(4)
-    x = synth.normal(g, (rows, hidden), 2.0, dtype=torch.bfloat16)
-    gain = (1 + 0.3 * synth.normal(g, (hidden,))).to(torch.bfloat16)
-    y = torch.empty_like(x, device=DEV)
+    x = synth.normal(g, (rows, hidden), 2.0)
+    gain = 1 + 0.3 * synth.normal(g, (hidden,))
+    y = torch.empty(rows, hidden, dtype=DTYPES[dt], device=DEV)
     sar.rmsnorm(x.to(DEV), gain.to(DEV), y, 1e-5)
     torch.cuda.synchronize()
     xd = x.double()
     ref = xd / torch.sqrt((xd * xd).mean(-1, keepdim=True) + 1e-5) * gain.double()
-    close(y, ref)
+    close(y, ref, DTYPES[dt])
