@@ -95,6 +95,8 @@ SIGNATURES = {
     "sar_op_gemm": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
     "sar_op_rmsnorm": (i32, [vp, vp, vp, i32, i32, ctypes.c_float, i32, vp]),
     "sar_model_debug_buffer": (i32, [vp, i32, ctypes.POINTER(vp)]),
+    "sar_decode_attention_noalloc": (i32, [vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32,
+                                           vp, i32, vp, i32, i32, vp, vp]),
 }
 
 _lib = None

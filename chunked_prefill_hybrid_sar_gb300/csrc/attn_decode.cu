@@ -18,6 +18,8 @@
 //     write unnormalised partials that decode_combine_kernel merges.
 #include <float.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -45,7 +47,10 @@ __device__ __forceinline__ void butterfly_step(float (&v)[NV], int lane) {
   }
 }
 
-template <typename T, int D, int GP>
+// COMPUTED = false: work items come from the host-planned list `a.items`.
+// COMPUTED = true: CTA x covers split (x % max_splits) of decode (x / max_splits)
+// with fixed `split_keys` ranges and a padded [n_decode][bt_stride] block table.
+template <typename T, int D, int GP, bool COMPUTED = false>
 __global__ void __launch_bounds__(kWarps * 32, 2) decode_attn_kernel(DecodeAttnArgs a) {
   constexpr int DPL = D / 32;            // dimensions per lane
   constexpr int NV = kBlockKeys * GP;    // partial dots per block: 16 keys x GP heads
@@ -61,12 +66,33 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_attn_kernel(DecodeAttnA
   float* mrg = reinterpret_cast<float*>(smem + kWarps * kStages * 2 * BLK_BYTES) + kWarps * NV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(mrg + kWarps * GP * (D + 2)) + warp * kStages;
 
-  const int4 item = reinterpret_cast<const int4*>(a.items)[blockIdx.x];
-  const int b = item.x, kbeg = item.y, kend = item.z, part = item.w;
+  int b, kbeg, kend, part, btlen;
+  const int* bt;
+  if constexpr (COMPUTED) {
+    b = blockIdx.x / a.max_splits;
+    const int sidx = blockIdx.x - b * a.max_splits;
+    const int nk = a.ctx_lens[b] + 1;
+    if (nk < 1 || nk > a.max_splits * a.split_keys) {
+      if (threadIdx.x == 0 && sidx == 0) report(a.err, SAR_ERR_BOUNDS, SITE_DECODE_BOUNDS, nk);
+      return;
+    }
+    kbeg = sidx * a.split_keys;
+    if (kbeg >= nk) return;
+    kend = min(nk, kbeg + a.split_keys);
+    part = nk > a.split_keys ? b * a.max_splits + sidx : -1;
+    bt = a.bt + (size_t)b * a.bt_stride;
+    btlen = a.bt_stride;
+  } else {
+    const int4 item = reinterpret_cast<const int4*>(a.items)[blockIdx.x];
+    b = item.x;
+    kbeg = item.y;
+    kend = item.z;
+    part = item.w;
+    bt = a.bt + a.bt_off[b];
+    btlen = a.bt_len[b];
+  }
   const int kh = blockIdx.y;
   const int G = a.qh / a.kvh;
-  const int* bt = a.bt + a.bt_off[b];
-  const int btlen = a.bt_len[b];
   const int nblk = (kend - kbeg + kBlockKeys - 1) / kBlockKeys;
 
   if (lane == 0) {
@@ -317,13 +343,20 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_attn_kernel(DecodeAttnA
 }
 
 // Merges the split partial results of each decode: out = sum_i A_i 2^(m_i - M) / sum_i L_i 2^(m_i - M).
-template <typename T, int D>
+template <typename T, int D, bool COMPUTED = false>
 __global__ void decode_combine_kernel(DecodeAttnArgs a) {
   const int b = blockIdx.x;
   const int hq = blockIdx.y;
-  const int cnt = a.parts_count[b];
+  int cnt, p0;
+  if constexpr (COMPUTED) {
+    cnt = (a.ctx_lens[b] + a.split_keys) / a.split_keys;  // ceil((ctx + 1) / split)
+    if (cnt > a.max_splits || cnt < 1) return;           // flagged by the attention kernel
+    p0 = b * a.max_splits;
+  } else {
+    cnt = a.parts_count[b];
+    p0 = a.parts_begin[b];
+  }
   if (cnt <= 1) return;
-  const int p0 = a.parts_begin[b];
   const int dd = threadIdx.x;
   float M = -INFINITY;
   for (int i = 0; i < cnt; ++i) M = fmaxf(M, a.partials[((size_t)(p0 + i) * a.qh + hq) * (D + 2) + D]);
@@ -337,24 +370,25 @@ __global__ void decode_combine_kernel(DecodeAttnArgs a) {
   static_cast<T*>(a.out)[(size_t)b * a.ld_out + (size_t)hq * D + dd] = Elem<T>::from(A / L);
 }
 
-template <typename T, int D, int GP>
+template <typename T, int D, int GP, bool COMPUTED = false>
 int launch_impl(const DecodeAttnArgs& a, cudaStream_t s) {
   constexpr int NV = kBlockKeys * GP;
   const size_t smem = (size_t)kWarps * kStages * 2 * kBlockKeys * D * 2 + (size_t)kWarps * NV * 4 +
                       (size_t)kWarps * GP * (D + 2) * 4 + (size_t)kWarps * kStages * 8 + 16;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<T, D, GP>,
+    cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<T, D, GP, COMPUTED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_error(e, "decode attention attribute");
     attr = true;
   }
-  decode_attn_kernel<T, D, GP><<<dim3(a.n_items, a.kvh), kWarps * 32, smem, s>>>(a);
+  const int n_ctas = COMPUTED ? a.n_decode * a.max_splits : a.n_items;
+  decode_attn_kernel<T, D, GP, COMPUTED><<<dim3(n_ctas, a.kvh), kWarps * 32, smem, s>>>(a);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "decode attention launch");
   if (a.partials) {
-    decode_combine_kernel<T, D><<<dim3(a.n_decode, a.qh), D, 0, s>>>(a);
+    decode_combine_kernel<T, D, COMPUTED><<<dim3(a.n_decode, a.qh), D, 0, s>>>(a);
     count_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "decode combine launch");
@@ -381,3 +415,108 @@ int launch_decode_attention(const DecodeAttnArgs& a, cudaStream_t s) {
 }
 
 }  // namespace sar
+
+// ---------------------------------------------------------------------------
+// Decode attention for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc at all: code that runs while another
+// component is capturing a CUDA graph on the same stream, runtimes that hand
+// out a fixed memory budget up front and own every allocation, or hosts that
+// forbid allocation on the serving path.  This variant keeps the split
+// partial results in a file-scope device array of fixed size instead of the
+// model's workspace, and plans the key splits on the device instead of
+// shipping a host-planned list, so it needs neither a device allocation nor a
+// pinned staging buffer.  The array exists on every GPU that loads the
+// library, until the process exits.
+// ---------------------------------------------------------------------------
+
+namespace sar {
+namespace {
+
+constexpr size_t kStaticScratchFloats = size_t(2) << 20;  // 8 MiB of fp32 partials
+static __device__ __align__(256) float g_decode_scratch[kStaticScratchFloats];
+
+std::mutex g_scratch_mu;
+float* g_scratch_addr[256] = {};  // per device: device address of g_decode_scratch
+
+}  // namespace
+}  // namespace sar
+
+extern "C" int sar_decode_attention_noalloc(const void* q, int32_t q_stride, const void* k_pages,
+                                            const void* v_pages, int32_t num_pages, int32_t page_size,
+                                            int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                            int32_t n_decode, const int32_t* ctx_lens, int32_t max_ctx,
+                                            const int32_t* block_tables, int32_t bt_stride, void* out,
+                                            int32_t out_stride, int32_t storage, int32_t* err_flag,
+                                            void* stream) {
+  using namespace sar;
+  if (!q || !k_pages || !v_pages || !ctx_lens || !block_tables || !out)
+    return set_error(SAR_ERR_INVALID_ARG, "decode_attention_noalloc: null pointer");
+  if (n_decode <= 0 || max_ctx < 0 || num_pages <= 0 || bt_stride <= 0 || n_kv_heads <= 0 || page_size <= 0 ||
+      n_q_heads % n_kv_heads || (int64_t)(max_ctx / page_size + 1) > bt_stride)
+    return set_error(SAR_ERR_INVALID_ARG, "decode_attention_noalloc: bad sizes or block table too short");
+  if ((head_dim != 64 && head_dim != 128) || page_size % kBlockKeys || n_q_heads / n_kv_heads > 8 ||
+      q_stride < n_q_heads * head_dim || out_stride < n_q_heads * head_dim)
+    return set_error(SAR_ERR_UNSUPPORTED, "decode_attention_noalloc: shape not supported");
+  if (storage != SAR_STORAGE_F16 && storage != SAR_STORAGE_BF16)
+    return set_error(SAR_ERR_INVALID_ARG, "decode_attention_noalloc: bad storage");
+  // split length: the smallest power of two in [256, 4096] keys whose partials
+  // fit the static array; longer contexts are always split (so use the array)
+  const int64_t per_split = (int64_t)n_decode * n_q_heads * (head_dim + 2);
+  auto need = [&](int64_t sp) {
+    const int64_t ns = ((int64_t)max_ctx + sp) / sp;  // ceil((max_ctx + 1) / sp)
+    return ns > 1 ? ns * per_split : 0;
+  };
+  int64_t split = 256;
+  while (split < 4096 && need(split) > (int64_t)kStaticScratchFloats) split *= 2;
+  if (need(split) > (int64_t)kStaticScratchFloats)
+    return set_error(SAR_ERR_INVALID_ARG, "decode_attention_noalloc: partials exceed the 8 MiB static scratch");
+  const int64_t max_splits = ((int64_t)max_ctx + split) / split;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error(e, "decode_attention_noalloc: current device");
+  if (dev < 0 || dev >= 256) return set_error(SAR_ERR_UNSUPPORTED, "decode_attention_noalloc: device index");
+  float* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_decode_scratch);  // once per device, with it current
+      if (e != cudaSuccess) return cuda_error(e, "decode_attention_noalloc: scratch symbol address");
+      g_scratch_addr[dev] = static_cast<float*>(p);
+    }
+    scratch = g_scratch_addr[dev];
+  }
+  DecodeAttnArgs a{};
+  a.qkv = q;
+  a.out = out;
+  a.k_cache = k_pages;
+  a.v_cache = v_pages;
+  a.bt = block_tables;
+  a.partials = max_splits > 1 ? scratch : nullptr;
+  a.n_decode = n_decode;
+  a.ld = q_stride;
+  a.ld_out = out_stride;
+  a.qh = n_q_heads;
+  a.kvh = n_kv_heads;
+  a.d = head_dim;
+  a.page_size = page_size;
+  a.num_pages = num_pages;
+  a.storage = storage;
+  a.err = err_flag;
+  a.ctx_lens = ctx_lens;
+  a.split_keys = (int)split;
+  a.max_splits = (int)max_splits;
+  a.bt_stride = bt_stride;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int G = n_q_heads / n_kv_heads;
+  const int GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
+#define SAR_DEC_NA(DD, GG)                                                                 \
+  if (head_dim == DD && GP == GG)                                                          \
+    return storage == SAR_STORAGE_BF16 ? launch_impl<__nv_bfloat16, DD, GG, true>(a, s) \
+                                       : launch_impl<__half, DD, GG, true>(a, s);
+  SAR_DEC_NA(128, 1) SAR_DEC_NA(128, 2) SAR_DEC_NA(128, 4) SAR_DEC_NA(128, 8)
+  SAR_DEC_NA(64, 1) SAR_DEC_NA(64, 2) SAR_DEC_NA(64, 4) SAR_DEC_NA(64, 8)
+#undef SAR_DEC_NA
+  return set_error(SAR_ERR_UNSUPPORTED, "decode_attention_noalloc: no kernel for this shape");
+}

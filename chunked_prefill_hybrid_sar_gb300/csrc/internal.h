@@ -90,6 +90,9 @@ struct DecodeAttnArgs {
   float* partials;           // [n_parts][qh][d + 2]
   int n_items, n_decode, ld, ld_out, qh, kvh, d, page_size, num_pages, storage;
   int* err;
+  // device-computed work split (used by the entry point that allocates nothing)
+  const int32_t* ctx_lens = nullptr;  // [n_decode]
+  int split_keys = 0, max_splits = 0, bt_stride = 0;
 };
 int launch_decode_attention(const DecodeAttnArgs& a, cudaStream_t s);
 

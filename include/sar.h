@@ -199,6 +199,44 @@ int sar_step_host(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, 
 int sar_sample_greedy(sar_model* m, const float* logits, int32_t rows, int32_t* tokens_out,
                       void* stream);
 
+/* ---- decode attention without allocation ------------------------------- */
+
+/* Paged decode attention that allocates nothing.  The paper has no
+ * counterpart to this entry point.  It is for callers that cannot call
+ * cudaMalloc: code that runs while another component captures a CUDA graph on
+ * the same stream, runtimes that hand out a fixed memory budget up front and
+ * own every allocation, hosts that forbid allocation on the serving path.
+ * It computes what the decode rows of sar_step compute -- every decode's
+ * query heads against its own paged history of ctx_lens[b] + 1 keys -- but
+ * plans the key splits on the device and keeps the split partials in one
+ * file-scope device array of 8 MiB, so it needs no workspace and no pinned
+ * staging buffer.  Every GPU that loads the library holds that array until
+ * the process exits.
+ *   q            device rows of the storage type, row b at q + b*q_stride
+ *                (n_q_heads * head_dim values, already rotated)
+ *   k_pages/v_pages  device pages of one layer, [num_pages][n_kv_heads][page_size][head_dim]
+ *   ctx_lens     device int32 [n_decode]; max_ctx (host) bounds them
+ *   block_tables device int32 [n_decode][bt_stride], row b = decode b's pages in order
+ *   out          device rows of the storage type, row b at out + b*out_stride
+ *   storage      SAR_STORAGE_F16 or SAR_STORAGE_BF16 (q, pages and out)
+ *   err_flag     device int32[4] or NULL: first device-side failure (code, site, detail)
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.  Calls
+ * share the array and keep its last contents (every partial is written before
+ * it is read, so nothing needs clearing); two calls whose work overlaps on the
+ * GPU race on it.  Contexts are split into ranges of `split` keys, the
+ * smallest power of two in [256, 4096] for which the partials,
+ * n_decode * ceil((max_ctx+1)/split) * n_q_heads * (head_dim+2) * 4 bytes, fit
+ * in 8 MiB; when none does the call returns SAR_ERR_INVALID_ARG before any
+ * launch. */
+int sar_decode_attention_noalloc(const void* q, int32_t q_stride, const void* k_pages,
+                                 const void* v_pages, int32_t num_pages, int32_t page_size,
+                                 int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                 int32_t n_decode, const int32_t* ctx_lens, int32_t max_ctx,
+                                 const int32_t* block_tables, int32_t bt_stride, void* out,
+                                 int32_t out_stride, int32_t storage, int32_t* err_flag,
+                                 void* stream);
+
 /* ---- per-kernel timing (CUDA events on the step's stream) -------------- */
 
 enum {
