@@ -369,6 +369,118 @@ def run_reference(args):
     return out
 
 
+# ------------------------------------------------------------------ tile sweep
+
+SWEEP_ROWS = (128, 255, 256, 257, 384, 511, 512, 1024, 2048)
+SWEEP_DECODE_ONLY = (1, 8, 32, 64)
+
+
+def run_sweep(args):
+    """Tile-quantisation and budget sweep on the Mistral-shaped layer: per GEMM
+    and tiling, device time with L2 flushed between launches; then the full
+    hybrid step at each row count (Bd = 32 decodes at context 2048, the rest
+    one chunk); then the decode-only linear cost per token relative to 2048-row
+    steps.  Prints one JSON line."""
+    import torch
+
+    import chunked_prefill_hybrid_sar_gb300 as sar
+    from chunked_prefill_hybrid_sar_gb300 import harness
+
+    dims = synth.MISTRAL_LAYER
+    gen = synth.generator(0, "cuda")
+    w = synth.layer_weights(gen, dims, torch.bfloat16, "cuda")
+    f16 = {k: v.to(torch.float16) for k, v in w.items()}
+    wqkv = torch.cat([f16["wq"], f16["wk"], f16["wv"]])
+    wgu = torch.stack([f16["wg"].view(-1, 64, dims.hidden), f16["wu"].view(-1, 64, dims.hidden)], 1)
+    wgu = wgu.reshape(2 * dims.ffn, dims.hidden)
+    shapes = {"qkv": (wqkv, sar.SAR_EPI_STORE), "o": (f16["wo"], sar.SAR_EPI_RESIDUAL),
+              "gateup": (wgu, sar.SAR_EPI_SWIGLU), "down": (f16["wd"], sar.SAR_EPI_RESIDUAL)}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    variants = {"m128n128": sar.SAR_GEMM_M128_N128, "m128n256": sar.SAR_GEMM_M128_N256,
+                "m256n128": sar.SAR_GEMM_M256_N128, "swap": sar.SAR_GEMM_SWAP, "auto": sar.SAR_GEMM_AUTO}
+    _, _, tf_sust, _ = peaks()
+    lin_flops = 2 * (dims.hidden * (dims.q_dim + 2 * dims.kv_dim) + dims.q_dim * dims.hidden
+                     + 3 * dims.hidden * dims.ffn)
+
+    def time_gemm(M, name, variant, reps=5):
+        wt, epi = shapes[name]
+        K = wt.shape[1]
+        a = torch.randn(M, K, device="cuda").to(torch.float16)
+        if epi == sar.SAR_EPI_SWIGLU:
+            c = torch.empty(M, wt.shape[0] // 2, dtype=torch.float16, device="cuda")
+        elif epi == sar.SAR_EPI_RESIDUAL:
+            c = torch.zeros(M, wt.shape[0], dtype=torch.float32, device="cuda")
+        else:
+            c = torch.empty(M, wt.shape[0], dtype=torch.float16, device="cuda")
+        r = c if epi == sar.SAR_EPI_RESIDUAL else None
+        ts = []
+        for _ in range(reps + 1):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            sar.gemm(a, wt, c, residual=r, epilogue=epi, variant=variant)
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ts = sorted(ts[1:])
+        return ts[len(ts) // 2]
+
+    gemm = {}
+    for M in SWEEP_ROWS:
+        gemm[M] = {}
+        for vn, v in variants.items():
+            if vn == "swap" and M > 256:
+                continue
+            row = {}
+            for name in shapes:
+                try:
+                    row[name] = time_gemm(M, name, v)
+                except sar.SarError:
+                    row[name] = None
+            if all(x is not None for x in row.values()):
+                row["linear_ms"] = sum(row[n] for n in shapes)
+                row["tflops"] = M * lin_flops / (row["linear_ms"] * 1e-3) / 1e12
+                row["frac_of_sustained_peak"] = row["tflops"] / tf_sust
+            gemm[M][vn] = row
+    per_tok_2048 = gemm[2048]["auto"]["linear_ms"] / 2048
+    equiv = {}
+    for bd in SWEEP_DECODE_ONLY:
+        t = sum(time_gemm(bd, n, sar.SAR_GEMM_AUTO) for n in shapes)
+        equiv[bd] = {"linear_ms": t, "per_token_ms": t / bd,
+                     "prefill_token_equivalents": (t / bd) / per_tok_2048}
+    m = harness.load_model(dims, [w], None, max_tokens=2048, max_decodes=64)
+    bd = 32
+    need = bd * (2048 // PAGE + 1) + 2048 // PAGE + 8
+    kv = sar.KVCache(m, PAGE, need)
+    for kind in (0, 1):
+        pv = harness.page_view(kv, 0, kind, dims)
+        pv.copy_(torch.randn(pv.shape, generator=gen, device="cuda").to(pv.dtype))
+    alloc = harness.PageAllocator(range(need))
+    dec = [(i, 2048, alloc.take(2048 // PAGE + 1)) for i in range(bd)]
+    pbt = alloc.take(2048 // PAGE)
+    step = {}
+    for M in SWEEP_ROWS:
+        b = sar.Batch((99, 0, M - bd, pbt), dec)
+        x = torch.randn(M, dims.hidden, device="cuda").to(torch.bfloat16)
+        for _ in range(3):
+            m.step(kv, b, x)
+        torch.cuda.synchronize()
+        m.profile(True)
+        for _ in range(5):
+            flush.zero_()
+            m.step(kv, b, x)
+        prof = m.profile_read()
+        m.profile(False)
+        step[M] = {k: v[0] / v[1] for k, v in prof.items() if v[1]}
+        step[M]["linear_ms"] = sum(step[M].get(k, 0.0) for k in ("gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down"))
+    m.sync_status()
+    out = {"mode": "sweep", "workload": "Mistral-7B-shaped layer, rows Lp+Bd in " + str(list(SWEEP_ROWS)) +
+           ", Bd=32 decodes at ctx 2048; f16 storage; L2 flushed (256 MB write) before every timed launch",
+           "gemm_ms": gemm, "decode_only_equivalence": equiv, "step_kernel_ms": step}
+    print(json.dumps(out))
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -376,7 +488,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=6)
     ap.add_argument("--impl", choices=["sar", "reference"], default="sar")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    ap.add_argument("--mode", choices=["step", "sweep"], default="step",
+                    help="step: the tau=512 hybrid step (default); sweep: tile-quantisation sweep")
     args = ap.parse_args()
+    if args.mode == "sweep":
+        run_sweep(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
