@@ -7,7 +7,9 @@
 // chunks -- the N(N-1)/2 re-read of the Sarathi-Serve digest, section 4.
 //
 // Tiled online-softmax attention on warp-level 16-bit MMAs (m16n8k16, fp32
-// accumulate): a CTA owns 64 query rows of one query head (16 per warp); K/V
+// accumulate; the fp32 queries enter as a high and a low 16-bit part, so the
+// scores are as precise as the 16-bit keys allow): a CTA owns 64 query rows of
+// one query head (16 per warp); K/V
 // tiles of 64 keys are gathered page by page with 16-byte cp.async into an
 // XOR-swizzled shared layout (conflict-free ldmatrix), double buffered.
 // Keys past the causal limit are zero-filled and masked.
@@ -64,8 +66,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
   constexpr int CH = D / 8;  // 16-byte chunks per row
   constexpr int TILE = kBKV * D * 2;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* sq = smem;                     // [64][D]
-  uint8_t* skv = smem + kBQ * D * 2;      // [2 stages][K | V][64][D]
+  uint8_t* sq = smem;                     // [2][64][D]: q split into a high and a low part
+  uint8_t* skv = smem + 2 * kBQ * D * 2;  // [2 stages][K | V][64][D]
 
   const int qt = gridDim.x - 1 - blockIdx.x;  // longest (latest) query tiles first
   const int hq = blockIdx.y;
@@ -77,13 +79,28 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
   const int last_pos = a.start_pos + q0 + nq - 1;        // latest query position in this CTA
   const int n_tiles = last_pos / kBKV + 1;
   const uint32_t sq_u = smem_u32(sq), skv_u = smem_u32(skv);
+  const uint32_t sql_u = sq_u + kBQ * D * 2;
 
-  // ---- Q tile (rows past the chunk are zero) ----
+  // ---- Q tile from fp32 rows, split q = hi + lo in the storage type so that
+  // the scores keep about twice the storage precision (rows past the chunk are zero)
   for (int c = threadIdx.x; c < kBQ * CH; c += kThreads) {
     const int r = c / CH, ch = c % CH;
-    const bool ok = r < nq;
-    const T* src = static_cast<const T*>(a.qkv) + (size_t)(q0 + (ok ? r : 0)) * a.ld + (size_t)hq * D + ch * 8;
-    cp_async16(sq_u + swz<D>(r, ch), src, ok ? 16 : 0);
+    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (r < nq) {
+      const float4* src = reinterpret_cast<const float4*>(a.q32 + (size_t)(q0 + r) * a.ld32 + (size_t)hq * D + ch * 8);
+      const float4 x0 = src[0], x1 = src[1];
+      f[0] = x0.x; f[1] = x0.y; f[2] = x0.z; f[3] = x0.w; f[4] = x1.x; f[5] = x1.y; f[6] = x1.z; f[7] = x1.w;
+    }
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      hi[e] = Elem<T>::pack(f[2 * e], f[2 * e + 1]);
+      lo[e] = Elem<T>::pack(f[2 * e] - Elem<T>::lo(hi[e]), f[2 * e + 1] - Elem<T>::hi(hi[e]));
+    }
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sq_u + swz<D>(r, ch)), "r"(hi[0]), "r"(hi[1]),
+                 "r"(hi[2]), "r"(hi[3]) : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sql_u + swz<D>(r, ch)), "r"(lo[0]), "r"(lo[1]),
+                 "r"(lo[2]), "r"(lo[3]) : "memory");
   }
   auto load_kv = [&](int t, int stage) {
     const uint32_t kbase = skv_u + stage * 2 * TILE;
@@ -117,21 +134,12 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
   const int r_lo = warp * 16 + (lane >> 2);  // this thread's two query rows in the tile
   const int qpos0 = a.start_pos + q0 + r_lo;
   const int qpos1 = qpos0 + 8;
-  uint32_t qf[D / 16][4];
 
   for (int t = 0; t < n_tiles; ++t) {
     if (t + 1 < n_tiles) load_kv(t + 1, (t + 1) & 1);
     cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();
-    if (t == 0) {
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int mi = lane >> 3;
-        const int row = warp * 16 + (mi & 1) * 8 + (lane & 7);
-        ldsm_x4(sq_u + swz<D>(row, kk * 2 + (mi >> 1)), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-      }
-    }
     const uint32_t kbase = skv_u + (t & 1) * 2 * TILE;
     const uint32_t vbase = kbase + TILE;
 
@@ -140,14 +148,22 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
 #pragma unroll
     for (int j = 0; j < kBKV / 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
 #pragma unroll
-    for (int j = 0; j < kBKV / 8; ++j) {
+    for (int kk = 0; kk < D / 16; kk += 2) {
+      const int mi = lane >> 3;
+      const int qrow = warp * 16 + (mi & 1) * 8 + (lane & 7);
+      uint32_t qh0[4], qh1[4], ql0[4], ql1[4];
+      ldsm_x4(sq_u + swz<D>(qrow, kk * 2 + (mi >> 1)), qh0[0], qh0[1], qh0[2], qh0[3]);
+      ldsm_x4(sq_u + swz<D>(qrow, kk * 2 + 2 + (mi >> 1)), qh1[0], qh1[1], qh1[2], qh1[3]);
+      ldsm_x4(sql_u + swz<D>(qrow, kk * 2 + (mi >> 1)), ql0[0], ql0[1], ql0[2], ql0[3]);
+      ldsm_x4(sql_u + swz<D>(qrow, kk * 2 + 2 + (mi >> 1)), ql1[0], ql1[1], ql1[2], ql1[3]);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; kk += 2) {
+      for (int j = 0; j < kBKV / 8; ++j) {
         uint32_t b0, b1, b2, b3;
-        const int mi = lane >> 3;
         ldsm_x4(kbase + swz<D>(j * 8 + (lane & 7), kk * 2 + mi), b0, b1, b2, b3);
-        mma16816<T>(s[j], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
-        mma16816<T>(s[j], qf[kk + 1][0], qf[kk + 1][1], qf[kk + 1][2], qf[kk + 1][3], b2, b3);
+        mma16816<T>(s[j], qh0[0], qh0[1], qh0[2], qh0[3], b0, b1);
+        mma16816<T>(s[j], ql0[0], ql0[1], ql0[2], ql0[3], b0, b1);
+        mma16816<T>(s[j], qh1[0], qh1[1], qh1[2], qh1[3], b2, b3);
+        mma16816<T>(s[j], ql1[0], ql1[1], ql1[2], ql1[3], b2, b3);
       }
     }
     // ---- causal mask + online softmax (base 2) ----
@@ -230,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
 
 template <typename T, int D>
 int launch_impl(const ChunkAttnArgs& a, cudaStream_t s) {
-  const size_t smem = (size_t)kBQ * D * 2 + (size_t)2 * 2 * kBKV * D * 2;
+  const size_t smem = (size_t)2 * kBQ * D * 2 + (size_t)2 * 2 * kBKV * D * 2;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(chunk_attn_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

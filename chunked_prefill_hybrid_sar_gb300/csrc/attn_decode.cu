@@ -129,9 +129,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_attn_kernel(DecodeAttnA
 #pragma unroll
     for (int e = 0; e < DPL; ++e) q[h][e] = 0.f;
     if (h < G) {
-      const T* qp = static_cast<const T*>(a.qkv) + (size_t)b * a.ld + (size_t)(kh * G + h) * D + lane * DPL;
+      if (a.q32) {
+        const float* qp = a.q32 + (size_t)b * a.ld32 + (size_t)(kh * G + h) * D + lane * DPL;
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) q[h][e] = Elem<T>::to(qp[e]) * qscale;
+        for (int e = 0; e < DPL; ++e) q[h][e] = qp[e] * qscale;
+      } else {
+        const T* qp = static_cast<const T*>(a.qkv) + (size_t)b * a.ld + (size_t)(kh * G + h) * D + lane * DPL;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) q[h][e] = Elem<T>::to(qp[e]) * qscale;
+      }
     }
   }
 

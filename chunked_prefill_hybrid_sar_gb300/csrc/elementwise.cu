@@ -13,6 +13,7 @@ namespace sar {
 namespace {
 
 constexpr int kNormThreads = 256;
+constexpr int kNormMaxVec = 8;  // hidden <= 8 * 4 * 256 = 8192
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
   v = warp_sum(v);
@@ -42,21 +43,30 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* __re
   const float4* gr = reinterpret_cast<const float4*>(g);
   uint2* yr = reinterpret_cast<uint2*>(y + (size_t)r * hidden);
   const int nv = hidden >> 2;
+  // the row stays in registers between the reduction and the scaling pass
+  float4 v[kNormMaxVec];
   float ss = 0.f;
-  for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-    const float4 v = xr[i];
-    ss = fmaf(v.x, v.x, ss);
-    ss = fmaf(v.y, v.y, ss);
-    ss = fmaf(v.z, v.z, ss);
-    ss = fmaf(v.w, v.w, ss);
+#pragma unroll
+  for (int k = 0; k < kNormMaxVec; ++k) {
+    const int i = threadIdx.x + k * kNormThreads;
+    if (i < nv) {
+      v[k] = xr[i];
+      ss = fmaf(v[k].x, v[k].x, ss);
+      ss = fmaf(v[k].y, v[k].y, ss);
+      ss = fmaf(v[k].z, v[k].z, ss);
+      ss = fmaf(v[k].w, v[k].w, ss);
+    }
   }
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / (float)hidden + eps);
-  for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-    const float4 v = xr[i];
-    const float4 gv = gr[i];
-    yr[i] = make_uint2(Elem<T>::pack(v.x * inv * gv.x, v.y * inv * gv.y),
-                       Elem<T>::pack(v.z * inv * gv.z, v.w * inv * gv.w));
+#pragma unroll
+  for (int k = 0; k < kNormMaxVec; ++k) {
+    const int i = threadIdx.x + k * kNormThreads;
+    if (i < nv) {
+      const float4 gv = gr[i];
+      yr[i] = make_uint2(Elem<T>::pack(v[k].x * inv * gv.x, v[k].y * inv * gv.y),
+                         Elem<T>::pack(v[k].z * inv * gv.z, v[k].w * inv * gv.w));
+    }
   }
 }
 
@@ -80,10 +90,15 @@ __global__ void embed_kernel(const int32_t* __restrict__ tok, const T* __restric
   }
 }
 
-// bf16 -> fp32 (input rows into the residual stream, norm gains).
-__global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ src, float* __restrict__ dst, size_t n) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-    dst[i] = __bfloat162float(src[i]);
+// bf16 -> fp32 (input rows into the residual stream, norm gains), 8 values
+// (16 bytes in, 32 out) per thread; n is a multiple of 8.
+__global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ src, float* __restrict__ dst, size_t n8) {
+  const size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const uint4 v = reinterpret_cast<const uint4*>(src)[i];
+  float4* d = reinterpret_cast<float4*>(dst) + 2 * i;
+  d[0] = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
+  d[1] = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
 }
 
 // bf16 weight rows -> storage type T, row r of the source landing on row
@@ -106,6 +121,9 @@ __global__ void convert_rows_kernel(const __nv_bfloat16* __restrict__ src, T* __
 // (a chunk keeps numbering from its start position: "maintain an independent
 // position_id for each chunk", SARATHI technique write-up, section 6.1), then
 // the rotated k and the v of that row are written into the row's page slot.
+// Input is the QKV projection in fp32; q, k and v are rounded to the storage
+// type once, after the rotation, and the rotated q and k are also kept in
+// fp32 (in place) for the attention scores.
 // The angle pos * theta_i is formed and reduced modulo 2*pi in double
 // precision once per (row, frequency), so long positions keep fp32 accuracy.
 template <typename T>
@@ -131,6 +149,7 @@ __global__ void rope_append_kernel(RopeArgs a) {
   if (!slot_ok && threadIdx.x == 0) report(a.err, SAR_ERR_BOUNDS, SITE_ROPE_BOUNDS, slot);
   const int width = (a.qh + 2 * a.kvh) * a.d;
   T* row = reinterpret_cast<T*>(a.qkv) + (size_t)r * width;
+  float* row32 = a.qkv32 + (size_t)r * width;
   T* k_cache = reinterpret_cast<T*>(a.k_cache);
   T* v_cache = reinterpret_cast<T*>(a.v_cache);
   const int n_pairs = (a.qh + a.kvh) * half;
@@ -138,11 +157,16 @@ __global__ void rope_append_kernel(RopeArgs a) {
     const int h = idx / half;
     const int i = idx - h * half;
     T* base = row + h * a.d;
-    const float x1 = Elem<T>::to(base[i]);
-    const float x2 = Elem<T>::to(base[i + half]);
+    float* base32 = row32 + h * a.d;
+    const float x1 = base32[i];
+    const float x2 = base32[i + half];
     const float c = cs[i], s = sn[i];
-    const T y1 = Elem<T>::from(x1 * c - x2 * s);
-    const T y2 = Elem<T>::from(x2 * c + x1 * s);
+    const float r1 = x1 * c - x2 * s;
+    const float r2 = x2 * c + x1 * s;
+    base32[i] = r1;
+    base32[i + half] = r2;
+    const T y1 = Elem<T>::from(r1);
+    const T y2 = Elem<T>::from(r2);
     base[i] = y1;
     base[i + half] = y2;
     if (h >= a.qh && slot_ok) {
@@ -152,13 +176,18 @@ __global__ void rope_append_kernel(RopeArgs a) {
       kc[i + half] = y2;
     }
   }
-  if (slot_ok) {
-    const T* vrow = row + (a.qh + a.kvh) * a.d;
+  {
+    const float* vrow32 = row32 + (a.qh + a.kvh) * a.d;
+    T* vrow = row + (a.qh + a.kvh) * a.d;
     const int nv = a.kvh * a.d;
     for (int idx = threadIdx.x; idx < nv; idx += blockDim.x) {
-      const int kh = idx / a.d;
-      const int j = idx - kh * a.d;
-      v_cache[(((size_t)page * a.kvh + kh) * a.page_size + off) * a.d + j] = vrow[idx];
+      const T v = Elem<T>::from(vrow32[idx]);
+      vrow[idx] = v;
+      if (slot_ok) {
+        const int kh = idx / a.d;
+        const int j = idx - kh * a.d;
+        v_cache[(((size_t)page * a.kvh + kh) * a.page_size + off) * a.d + j] = v;
+      }
     }
   }
 }
@@ -215,7 +244,8 @@ __global__ void __launch_bounds__(1024) argmax_kernel(const float* __restrict__ 
 int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hidden, float eps,
                    const int32_t* row_index, int storage, cudaStream_t s) {
   if (rows <= 0) return SAR_OK;
-  if (hidden % 4) return set_error(SAR_ERR_UNSUPPORTED, "rmsnorm: hidden must be a multiple of 4");
+  if (hidden % 4 || hidden > 4 * kNormThreads * kNormMaxVec)
+    return set_error(SAR_ERR_UNSUPPORTED, "rmsnorm: hidden must be a multiple of 4 and at most 8192");
   if (storage == SAR_STORAGE_BF16)
     rmsnorm_kernel<__nv_bfloat16><<<rows, kNormThreads, 0, s>>>(x, gain, static_cast<__nv_bfloat16*>(y), hidden,
                                                                eps, row_index);
@@ -239,8 +269,9 @@ int launch_embed(const int32_t* tokens, const void* table, float* out, int rows,
 
 int launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s) {
   if (n == 0) return SAR_OK;
-  const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
-  bf16_to_f32_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), dst, n);
+  if (n % 8) return set_error(SAR_ERR_UNSUPPORTED, "bf16 to fp32: length must be a multiple of 8");
+  const size_t n8 = n / 8;
+  bf16_to_f32_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), dst, n8);
   count_launches(1);
   return cuda_error(cudaGetLastError(), "bf16 to fp32 launch");
 }

@@ -62,7 +62,8 @@ int launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s);
 int launch_convert_rows(const void* src, void* dst, int rows, int cols, int interleave, int up, int storage,
                         cudaStream_t s);
 struct RopeArgs {
-  void* qkv;                 // [M, (qh + 2 kvh) * d], storage type
+  float* qkv32;              // [M, (qh + 2 kvh) * d] fp32 projection in; rotated q, k out (in place)
+  void* qkv;                 // [M, (qh + 2 kvh) * d], storage type (written)
   const int32_t* pos;        // [M]
   const int32_t* slot;       // [M] page * page_size + offset
   const double* inv_freq;    // [d/2]
@@ -77,6 +78,8 @@ int launch_argmax(const float* logits, int rows, int vocab, int32_t* out, cudaSt
 // ---- attention (attn_decode.cu, attn_chunk.cu) -----------------------------
 struct DecodeAttnArgs {
   const void* qkv;           // decode rows start here; row stride ld (storage type)
+  const float* q32 = nullptr;  // when set: fp32 query rows (row stride ld32) used instead of qkv
+  int ld32 = 0;
   void* out;                 // decode rows of the attention output; row stride ld_out
   const void* k_cache;
   const void* v_cache;
@@ -97,7 +100,8 @@ struct DecodeAttnArgs {
 int launch_decode_attention(const DecodeAttnArgs& a, cudaStream_t s);
 
 struct ChunkAttnArgs {
-  const void* qkv;           // chunk rows [0, len); row stride ld (storage type)
+  const float* q32;          // chunk query rows [0, len) in fp32; row stride ld32
+  int ld32;
   void* out;                 // [len, qh*d]; row stride ld_out
   const void* k_cache;
   const void* v_cache;

@@ -62,7 +62,8 @@ struct sar_model {
   // workspace
   uint8_t* ws = nullptr;
   st16 *xn = nullptr, *qkv = nullptr, *attn = nullptr, *act = nullptr, *hrows = nullptr;
-  float* hres = nullptr;  // residual stream, fp32
+  float* hres = nullptr;   // residual stream, fp32
+  float* qkv32 = nullptr;  // QKV projection in fp32 (rotated q, k after the rotary kernel)
   void* in_stage = nullptr;
   float* partials = nullptr;
   size_t partials_cap = 0;  // floats
@@ -340,13 +341,14 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
     }
     {
       Prof pr(m, SAR_K_GEMM_QKV, s);
-      SAR_TRY(run_gemm(m, m->xn, M, w.m_qkv, m->qkv_n, H, SAR_EPI_STORE, m->qkv, nullptr, s));
+      SAR_TRY(run_gemm(m, m->xn, M, w.m_qkv, m->qkv_n, H, SAR_EPI_F32, m->qkv32, nullptr, s));
     }
     uint16_t* kc = kv->k + (size_t)l * kv->layer_elems;
     uint16_t* vc = kv->v + (size_t)l * kv->layer_elems;
     {
       Prof pr(m, SAR_K_ROPE_APPEND, s);
       sar::RopeArgs ra;
+      ra.qkv32 = m->qkv32;
       ra.qkv = m->qkv;
       ra.pos = md + p.o_pos;
       ra.slot = md + p.o_slot;
@@ -366,7 +368,8 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
     if (p.Lp > 0) {
       Prof pr(m, SAR_K_CHUNK_ATTN, s);
       sar::ChunkAttnArgs ca;
-      ca.qkv = m->qkv;
+      ca.q32 = m->qkv32;
+      ca.ld32 = m->qkv_n;
       ca.out = m->attn;
       ca.k_cache = kc;
       ca.v_cache = vc;
@@ -391,6 +394,8 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
       da.qkv = m->qkv + (size_t)p.Lp * m->qkv_n;  // zero-copy row split
       da.out = m->attn + (size_t)p.Lp * m->qd;
       da.storage = d.storage;
+      da.q32 = m->qkv32 + (size_t)p.Lp * m->qkv_n;
+      da.ld32 = m->qkv_n;
       da.k_cache = kc;
       da.v_cache = vc;
       da.items = md + p.o_items;
@@ -500,7 +505,7 @@ int sar_model_create(const sar_dims* dims, sar_model** out) {
   const size_t T = d.max_tokens;
   const size_t R = (size_t)d.max_decodes + 1;
   const size_t ws = align256(T * H * 2) + align256(T * m->qkv_n * 2) + align256(T * m->qd * 2) + align256(T * F * 2) +
-                    align256(T * H * 4) + align256(R * H * 2) + align256(T * H * 2) + 256;
+                    align256(T * H * 4) + align256(R * H * 2) + align256(T * H * 2) + align256(T * m->qkv_n * 4) + 256;
   e = cudaMalloc(&m->ws, ws);
   if (e == cudaSuccess) e = cudaMalloc(&m->err, 16);
   if (e == cudaSuccess) e = cudaMemset(m->err, 0, 16);
@@ -517,6 +522,7 @@ int sar_model_create(const sar_dims* dims, sar_model** out) {
   m->hres = takef(T * H * 4);
   m->hrows = take(R * H * 2);
   m->in_stage = take(T * H * 2);
+  m->qkv32 = takef(T * m->qkv_n * 4);
   // rotary frequencies base^(-2i/d), double precision
   std::vector<double> inv(d.head_dim / 2);
   for (int i = 0; i < d.head_dim / 2; ++i) inv[i] = std::pow((double)d.rope_base, -2.0 * i / d.head_dim);
@@ -717,6 +723,7 @@ int sar_model_debug_buffer(sar_model* m, int32_t which, void** out) {
     case 2: *out = m->attn; break;
     case 3: *out = m->act; break;
     case 4: *out = m->hres; break;
+    case 5: *out = m->qkv32; break;
     default: return set_error(SAR_ERR_INVALID_ARG, "debug_buffer: unknown buffer");
   }
   return SAR_OK;

@@ -62,7 +62,9 @@ int sar_op_rmsnorm(const void* x, const void* gain, void* y, int32_t rows, int32
  *                      (storage type; q and k after the rotary embedding)
  *   2: attention rows  [max_tokens, n_q_heads * head_dim] (storage type)
  *   3: SwiGLU rows     [max_tokens, ffn] (storage type)
- *   4: residual stream fp32 [max_tokens, hidden] (when the step had no hidden_out) */
+ *   4: residual stream fp32 [max_tokens, hidden] (when the step had no hidden_out)
+ *   5: q|k|v rows      fp32 [max_tokens, (n_q_heads + 2 n_kv_heads) * head_dim]
+ *                      (the projection; q and k rotated in place) */
 int sar_model_debug_buffer(sar_model* m, int32_t which, void** out);
 
 #ifdef __cplusplus
