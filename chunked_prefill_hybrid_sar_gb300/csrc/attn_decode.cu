@@ -7,7 +7,7 @@
 //   * one CTA = (work item, KV head); a work item is a range of a decode's
 //     keys (long contexts are split so every SM has work, then merged);
 //   * the query heads of one GQA group share every K/V byte that is loaded;
-//   * each of the 4 warps owns a private 3-deep ring of 16-key blocks
+//   * each of the 4 warps owns a private 2-deep ring of 16-key blocks
 //     (K and V, 2 x 4 KB at head_dim 128) filled by cp.async.bulk straight
 //     from the page (one contiguous run per block) -- no page gather, no
 //     register staging;
@@ -28,7 +28,7 @@ namespace sar {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kStages = 3;   // per-warp ring depth (16-key blocks)
+constexpr int kStages = 2;   // per-warp ring depth (16-key blocks); 3 CTAs fit an SM
 constexpr int kBlockKeys = 16;
 
 // One halving step of the butterfly: the NV >> STEP values in v[] are split
@@ -51,7 +51,7 @@ __device__ __forceinline__ void butterfly_step(float (&v)[NV], int lane) {
 // COMPUTED = true: CTA x covers split (x % max_splits) of decode (x / max_splits)
 // with fixed `split_keys` ranges and a padded [n_decode][bt_stride] block table.
 template <typename T, int D, int GP, bool COMPUTED = false>
-__global__ void __launch_bounds__(kWarps * 32, 2) decode_attn_kernel(DecodeAttnArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, GP >= 8 ? 2 : 3) decode_attn_kernel(DecodeAttnArgs a) {
   constexpr int DPL = D / 32;            // dimensions per lane
   constexpr int NV = kBlockKeys * GP;    // partial dots per block: 16 keys x GP heads
   constexpr int NVL = NV >= 32 ? NV / 32 : 1;

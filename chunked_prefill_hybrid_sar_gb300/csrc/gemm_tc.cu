@@ -39,6 +39,7 @@ constexpr int kTileA = 128 * kBK * 2;     // one 128-row slab: 16 KB
 constexpr int kSmemLimit = 232448;        // 227 KB of dynamic shared memory
 constexpr int kBarBytes = 1024;           // barriers + TMEM slot (+ alignment)
 constexpr int kSwapXchg = 64 * 17 * 4;    // swap-mode SwiGLU exchange buffer
+constexpr int kPrefetch = 16;             // K-slabs of the weight tile prefetched into L2 ahead
 
 // ---- tcgen05 wrappers ------------------------------------------------------
 
@@ -117,10 +118,27 @@ __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x));
 struct Params {
   int M, N, K;
   int bn, m_tiles, n_tiles, k_blocks, stages, stage_bytes, tmem_cols;
+  int splits, kb_per_split;  // split-K: `splits` K ranges per tile (residual epilogue only)
   void* c;
   const void* r;
   int* err;
 };
+
+// Work unit u -> (token tile, weight tile, K-slab range).  Token tiles vary
+// fastest so that CTAs running at the same time share one weight slab in L2.
+struct Unit {
+  int mt, nt, kb0, kb1;
+};
+__device__ __forceinline__ Unit unit_of(const Params& p, int u) {
+  Unit w;
+  w.mt = u % p.m_tiles;
+  const int r = u / p.m_tiles;
+  const int sp = r % p.splits;
+  w.nt = r / p.splits;
+  w.kb0 = sp * p.kb_per_split;
+  w.kb1 = min(p.k_blocks, w.kb0 + p.kb_per_split);
+  return w;
+}
 
 __device__ __forceinline__ void next_stage(int& stage, uint32_t& phase, int stages) {
   if (++stage == stages) {
@@ -176,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int n_tiles_total = p.m_tiles * p.n_tiles;
+  const int n_tiles_total = p.m_tiles * p.n_tiles * p.splits;  // work units
   const int acc_cols = MSUB * p.bn;
 
   if (warp == 0) {
@@ -187,12 +205,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < n_tiles_total && ok; t += gridDim.x) {
-        const int mt = t % p.m_tiles;
-        const int nt = t / p.m_tiles;
+        const Unit un = unit_of(p, t);
+        const int mt = un.mt, nt = un.nt;
         // A rows: tokens (non-swap) or weights (swap); B rows: the other one.
         const int a_row = SWAP ? nt * 128 : mt * 128 * MSUB;
         const int b_row = SWAP ? mt * p.bn : nt * p.bn;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        // the weight tile streams from HBM: pull it into L2 kPrefetch K-slabs ahead
+        // of the shared-memory ring so the ring's loads hit L2
+        const void* w_map = SWAP ? (const void*)&tm_a : (const void*)&tm_b;
+        const int w_row = SWAP ? a_row : b_row;
+        for (int kb = un.kb0; kb < un.kb0 + kPrefetch && kb < un.kb1; ++kb) tma_prefetch_l2(w_map, kb * kBK, w_row);
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
+          if (kb + kPrefetch < un.kb1) tma_prefetch_l2(w_map, (kb + kPrefetch) * kBK, w_row);
           if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.err, SITE_GEMM_PRODUCER)) {
             ok = false;
             break;
@@ -222,7 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(smem_u32(&acce_bar[acc]), accph ^ 1u, p.err, SITE_GEMM_MMA)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * acc_cols);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const Unit un = unit_of(p, t);
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.err, SITE_GEMM_MMA)) {
             ok = false;
             break;
@@ -236,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int s = 0; s < MSUB; ++s) {
               const uint64_t adesc = sw128_desc(a_base + s * kTileA + kk * 32);
-              mma_bf16(d_tmem + (uint32_t)(s * p.bn), adesc, bdesc, idesc, (kb | kk) != 0);
+              mma_bf16(d_tmem + (uint32_t)(s * p.bn), adesc, bdesc, idesc, (kb != un.kb0) || (kk != 0));
             }
           }
           mma_commit(smem_u32(&empty_bar[stage]));
@@ -253,8 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int i = 0;
     bool alive = true;  // false once a wait gave up: loads/stores stop, barriers stay matched
     for (int t = blockIdx.x; t < n_tiles_total; t += gridDim.x, ++i) {
-      const int mt = t % p.m_tiles;
-      const int nt = t / p.m_tiles;
+      const Unit un = unit_of(p, t);
+      const int mt = un.mt, nt = un.nt;
       const int acc = i & 1;
       const uint32_t accph = (uint32_t)((i >> 1) & 1);
       if (alive) alive = warp_wait(smem_u32(&accf_bar[acc]), accph, p.err, SITE_GEMM_EPILOGUE);
@@ -314,6 +339,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float4* rs = reinterpret_cast<const float4*>(
                     reinterpret_cast<const float*>(p.r) + (size_t)row * p.N + col);
                 float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.c) + (size_t)row * p.N + col);
+                if (p.splits > 1) {
+                  // split-K: every K range adds its share into C (== R) in place
+#pragma unroll
+                  for (int e = 0; e < 4; ++e)
+                    atomicAdd(&dst[e], make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                                   __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
+                  continue;
+                }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                   const float4 r4 = rs[e];
@@ -380,7 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               if constexpr (EPI == SAR_EPI_F32) {
                 reinterpret_cast<float*>(p.c)[idx] = f;
               } else if constexpr (EPI == SAR_EPI_RESIDUAL) {
-                reinterpret_cast<float*>(p.c)[idx] = f + reinterpret_cast<const float*>(p.r)[idx];
+                if (p.splits > 1)
+                  atomicAdd(reinterpret_cast<float*>(p.c) + idx, f);
+                else
+                  reinterpret_cast<float*>(p.c)[idx] = f + reinterpret_cast<const float*>(p.r)[idx];
               } else {
                 reinterpret_cast<T*>(p.c)[idx] = Elem<T>::from(f);
               }
@@ -467,21 +503,47 @@ int make_tmap_16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols
   return SAR_OK;
 }
 
-int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg) {
+int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in_place) {
   if (M < 1 || N < 64 || K < 64 || N % 64 || K % 64)
     return set_error(SAR_ERR_UNSUPPORTED, "gemm: need M >= 1, N and K multiples of 64");
   if (epi == SAR_EPI_SWIGLU && N % 128)
     return set_error(SAR_ERR_UNSUPPORTED, "gemm: SwiGLU needs whole 64-row gate/up block pairs");
   const int sms = num_sms();
+  const int k_blocks = K / kBK;
+  // split-K (K ranges added into an fp32 output in place) only for the
+  // in-place residual epilogue; pick the split count with the best makespan
+  const bool can_split = epi == SAR_EPI_RESIDUAL && in_place;
+  // SM clocks per 64-wide K slab of one tile: the larger of the MMA time
+  // (128 x bn x 64 takes 2*bn clocks per 128-row sub-tile) and the time to
+  // stream its operands into shared memory (about 64 bytes per clock per SM)
+  auto kslab_clocks = [](int msub, int bn) -> long {
+    return std::max<long>(2L * msub * bn, (msub * 16384L + bn * 128L) / 64);
+  };
+  auto best_split = [&](long tiles, long per_kb_work, int* splits) {
+    long best = -1;
+    for (int sp = 1; sp <= (can_split ? 4 : 1); ++sp) {
+      const long kb = (k_blocks + sp - 1) / sp;
+      if (sp > 1 && kb < 8) break;
+      const long units = tiles * sp;
+      // waves x unit work, plus a small charge per extra split for the atomic adds
+      const long c = ((units + sms - 1) / sms) * kb * per_kb_work * (sp > 1 ? 21 : 20) / 20;
+      if (best < 0 || c < best) {
+        best = c;
+        *splits = sp;
+      }
+    }
+    return best;
+  };
   GemmCfg c;
   if (variant == SAR_GEMM_AUTO) {
     if (M <= 256) {
       variant = SAR_GEMM_SWAP;
     } else {
-      // makespan estimate: waves x per-tile MMA work
+      // makespan estimate: waves x per-unit MMA work
       auto cost = [&](int msub, int bn) {
         const long tiles = (long)((M + 128 * msub - 1) / (128 * msub)) * ((N + bn - 1) / bn);
-        return ((tiles + sms - 1) / sms) * (long)msub * bn * 1000 + tiles;  // tie-break: fewer tiles
+        int sp = 1;
+        return best_split(tiles, kslab_clocks(msub, bn), &sp) * 1000 + tiles;  // tie-break: fewer tiles
       };
       variant = SAR_GEMM_M128_N256;
       long best = (N % 256 == 0) ? cost(1, 256) : -1;
@@ -516,7 +578,11 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg) {
   c.stages = std::min(8, (kSmemLimit - extra) / stage_bytes);
   if (c.stages < 2) return set_error(SAR_ERR_UNSUPPORTED, "gemm: tile does not fit shared memory");
   c.smem = c.stages * stage_bytes + extra;
-  c.grid = std::min(c.m_tiles * c.n_tiles, sms);
+  c.splits = 1;
+  best_split((long)c.m_tiles * c.n_tiles, c.swap ? kslab_clocks(1, c.bn) : kslab_clocks(c.msub, c.bn), &c.splits);
+  c.kb_per_split = (k_blocks + c.splits - 1) / c.splits;
+  c.splits = (k_blocks + c.kb_per_split - 1) / c.kb_per_split;  // no empty K range
+  c.grid = std::min(c.m_tiles * c.n_tiles * c.splits, sms);
   *cfg = c;
   return SAR_OK;
 }
@@ -535,6 +601,10 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   p.m_tiles = cfg.m_tiles;
   p.n_tiles = cfg.n_tiles;
   p.k_blocks = K / kBK;
+  p.splits = cfg.splits;
+  p.kb_per_split = cfg.kb_per_split;
+  if (cfg.splits > 1 && c != residual)
+    return set_error(SAR_ERR_INVALID_ARG, "gemm: split-K needs the residual output in place");
   p.stages = cfg.stages;
   p.stage_bytes = cfg.msub * kTileA + cfg.bn * kBK * 2;
   p.tmem_cols = pow2_at_least(2 * cfg.msub * cfg.bn);

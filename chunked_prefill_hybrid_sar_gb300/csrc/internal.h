@@ -38,11 +38,15 @@ struct GemmCfg {
   // box rows the two tensor maps must be encoded with
   int a_box_rows = 128;
   int b_box_rows = 256;
+  int splits = 1;        // K ranges per tile (in-place fp32 residual epilogue only)
+  int kb_per_split = 0;  // 64-wide K slabs per range
 };
 
 // Picks a tiling for C[M, .] = A[M, K] . W[N, K]^T (variant = SAR_GEMM_*).
 // Returns SAR_OK or SAR_ERR_UNSUPPORTED.
-int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg);
+// in_place: the residual epilogue writes into its own residual (C == R), which
+// allows split-K with atomic fp32 adds.
+int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in_place = false);
 
 // Launches with maps already encoded: `act_map` over the activations (rows M),
 // `w_map` over the weights; which one is the MMA's A operand depends on cfg.swap.

@@ -138,7 +138,7 @@ int weight_maps(CUtensorMap (&maps)[2], const void* w, int rows, int cols, int s
 int run_gemm(sar_model* m, const st16* a, int rows, const CUtensorMap (&wmaps)[2], int N, int K, int epi,
              void* c, const void* r, cudaStream_t s) {
   sar::GemmCfg cfg;
-  SAR_TRY(sar::gemm_config(rows, N, K, epi, SAR_GEMM_AUTO, &cfg));
+  SAR_TRY(sar::gemm_config(rows, N, K, epi, SAR_GEMM_AUTO, &cfg, c == r));
   CUtensorMap amap;
   SAR_TRY(sar::make_tmap_16(&amap, a, rows, K, cfg.swap ? cfg.b_box_rows : cfg.a_box_rows, m->d.storage));
   const CUtensorMap& wm = cfg.swap ? wmaps[0] : wmaps[cfg.bn == 256 ? 1 : 0];
@@ -742,7 +742,7 @@ int sar_op_gemm(const void* a, const void* w, void* c, const void* residual, int
     SAR_TRY(check(cudaMemset(err, 0, 16), "op_gemm: flag buffer"));
   }
   sar::GemmCfg cfg;
-  SAR_TRY(sar::gemm_config(M, N, K, epilogue, variant, &cfg));
+  SAR_TRY(sar::gemm_config(M, N, K, epilogue, variant, &cfg, epilogue == SAR_EPI_RESIDUAL && c == residual));
   CUtensorMap amap, wmap;
   SAR_TRY(sar::make_tmap_16(&amap, a, M, K, cfg.swap ? cfg.b_box_rows : cfg.a_box_rows, storage));
   SAR_TRY(sar::make_tmap_16(&wmap, w, N, K, cfg.swap ? cfg.a_box_rows : cfg.b_box_rows, storage));

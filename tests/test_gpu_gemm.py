@@ -137,3 +137,25 @@ def test_rmsnorm_kernel(rows, hidden, dt):
     xd = x.double()
     ref = xd / torch.sqrt((xd * xd).mean(-1, keepdim=True) + 1e-5) * gain.double()
     close(y, ref, DTYPES[dt])
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 1024, 4096), (300, 1024, 4096), (512, 2048, 8192)])
+def test_gemm_residual_split_k_in_place(M, N, K):
+    """Long-K residual GEMMs run split-K (K ranges added atomically into the fp32
+    residual); the result must equal one full-K accumulation up to fp32 rounding."""
+    a, w, r = operands(M, N, K, 5)
+    h = r.to(DEV).clone()
+    sar.gemm(a.to(DEV), w.to(DEV), h, residual=h, epilogue=sar.SAR_EPI_RESIDUAL)
+    torch.cuda.synchronize()
+    ref = a.double() @ w.double().T + r.double()
+    assert ((h.double().cpu() - ref).abs().max() / ref.abs().max()).item() < 1e-5
+
+
+def test_gemm_residual_out_of_place_does_not_split():
+    M, N, K = 64, 1024, 4096
+    a, w, r = operands(M, N, K, 6)
+    c = torch.empty(M, N, dtype=torch.float32, device=DEV)
+    sar.gemm(a.to(DEV), w.to(DEV), c, residual=r.to(DEV), epilogue=sar.SAR_EPI_RESIDUAL)
+    torch.cuda.synchronize()
+    ref = a.double() @ w.double().T + r.double()
+    assert ((c.double().cpu() - ref).abs().max() / ref.abs().max()).item() < 1e-5
