@@ -3,19 +3,21 @@
 // the split, SARATHI technique write-up section 3.3; reading notes part 2
 // section 3: "each decode looks up its own history KV").
 //
-// HBM-bound (about 4 flops per byte), so the design is about streaming pages:
+// HBM-bound (about 4 flops per byte), so the design is about streaming pages
+// with as few instructions per byte as possible:
 //   * one CTA = (work item, KV head); a work item is a range of a decode's
 //     keys (long contexts are split so every SM has work, then merged);
-//   * the query heads of one GQA group share every K/V byte that is loaded;
-//   * each of the 4 warps owns a private 2-deep ring of 16-key blocks
-//     (K and V, 2 x 4 KB at head_dim 128) filled by cp.async.bulk straight
-//     from the page (one contiguous run per block) -- no page gather, no
-//     register staging;
-//   * a lane owns head_dim/32 consecutive dimensions; the 16 x group partial
-//     dot products are reduced with a halving butterfly (15.5 shuffles per
-//     head per block instead of 80), softmax runs online in base 2;
-//   * the 4 warps' (max, sum, acc) are merged in shared memory; split items
-//     write unnormalised partials that decode_combine_kernel merges.
+//   * each of the 4 warps owns a private ring of 16-key blocks; one lane
+//     fills a block with 2-D TMA tensor loads of the page (64-dimension boxes,
+//     128-byte swizzle, so the ldmatrix reads below are bank-conflict free);
+//   * the query heads of one GQA group (up to 8) are the rows of a 16-row MMA
+//     tile: S = Q K^T and O += P V run on warp-level tensor-core MMAs
+//     (m16n8k16, fp32 accumulate), 48 per 16-key block; the fp32 queries enter
+//     as a high and a low 16-bit part so the scores keep fp32-like precision;
+//   * online softmax in base 2 on the accumulator fragments; the 4 warps'
+//     (max, sum, acc) are merged in shared memory; split items write
+//     unnormalised partials that decode_combine_kernel merges.
+#include <cuda.h>
 #include <float.h>
 
 #include <mutex>
@@ -28,43 +30,67 @@ namespace sar {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kStages = 2;   // per-warp ring depth (16-key blocks); 3 CTAs fit an SM
+constexpr int kStages = 3;    // per-warp ring depth (16-key blocks)
 constexpr int kBlockKeys = 16;
+constexpr int kMaxGroup = 8;  // query heads per KV head (rows of the MMA tile that are real)
 
-// One halving step of the butterfly: the NV >> STEP values in v[] are split
-// in two, the lane keeps the half chosen by its bit `16 >> STEP` and adds the
-// partner lane's copy of that half.
-template <int NV, int STEP>
-__device__ __forceinline__ void butterfly_step(float (&v)[NV], int lane) {
-  constexpr int mask = 16 >> STEP;
-  constexpr int half = (NV >> STEP) / 2;
-  const bool upper = (lane & mask) != 0;
-#pragma unroll
-  for (int j = 0; j < half; ++j) {
-    const float send = upper ? v[j] : v[j + half];
-    const float keep = upper ? v[j + half] : v[j];
-    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+template <typename T>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  if constexpr (Elem<T>::kMmaFormat == 1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   }
+}
+
+// Byte offset of (key row, 16-byte chunk over the whole head_dim) inside one
+// TMA-filled block: 64-dimension halves of 16 rows x 128 bytes, each written
+// with the 128-byte swizzle (chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t blk_off(int row, int chunk) {
+  const int h = chunk >> 3, c = chunk & 7;
+  return (uint32_t)(h * (kBlockKeys * 128) + row * 128 + ((c ^ (row & 7)) << 4));
 }
 
 // COMPUTED = false: work items come from the host-planned list `a.items`.
 // COMPUTED = true: CTA x covers split (x % max_splits) of decode (x / max_splits)
 // with fixed `split_keys` ranges and a padded [n_decode][bt_stride] block table.
-template <typename T, int D, int GP, bool COMPUTED = false>
-__global__ void __launch_bounds__(kWarps * 32, GP >= 8 ? 2 : 3) decode_attn_kernel(DecodeAttnArgs a) {
-  constexpr int DPL = D / 32;            // dimensions per lane
-  constexpr int NV = kBlockKeys * GP;    // partial dots per block: 16 keys x GP heads
-  constexpr int NVL = NV >= 32 ? NV / 32 : 1;
-  constexpr int BLK_BYTES = kBlockKeys * D * 2;
+template <typename T, int D, bool COMPUTED = false>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+    decode_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                       DecodeAttnArgs a) {
+  constexpr int HALVES = D / 64;
+  constexpr int BLK_BYTES = HALVES * kBlockKeys * 128;  // K (or V) of one 16-key block
+  constexpr int STAGE_BYTES = 2 * BLK_BYTES;
+  constexpr int NT = D / 8;                             // output n-tiles of 8 dimensions
+  constexpr int KT = D / 16;                            // k-steps over head_dim
 
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // layout: [warp][stage][K | V] blocks, then p buffers, merge area, barriers
-  uint8_t* ring = smem + warp * kStages * 2 * BLK_BYTES;
-  float* pbuf = reinterpret_cast<float*>(smem + kWarps * kStages * 2 * BLK_BYTES) + warp * NV;
-  float* mrg = reinterpret_cast<float*>(smem + kWarps * kStages * 2 * BLK_BYTES) + kWarps * NV;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(mrg + kWarps * GP * (D + 2)) + warp * kStages;
+  uint8_t* ring = smem + warp * kStages * STAGE_BYTES;
+  // after the key loop each warp's own ring holds its [row][D + 2] merge record
+  static_assert(kMaxGroup * (D + 2) * 4 <= kStages * STAGE_BYTES, "merge record must fit the ring");
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * STAGE_BYTES) + warp * kStages;
 
   int b, kbeg, kend, part, btlen;
   const int* bt;
@@ -98,6 +124,8 @@ __global__ void __launch_bounds__(kWarps * 32, GP >= 8 ? 2 : 3) decode_attn_kern
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
     fence_mbar_init();
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
   }
   __syncwarp();
 
@@ -105,55 +133,59 @@ __global__ void __launch_bounds__(kWarps * 32, GP >= 8 ? 2 : 3) decode_attn_kern
   auto issue = [&](int j, int s) -> bool {
     const int key0 = kbeg + j * kBlockKeys;
     const int bi = key0 / a.page_size;
-    int page = (bi < btlen) ? bt[bi] : -1;
+    const int page = (bi < btlen) ? bt[bi] : -1;
     if (page < 0 || page >= a.num_pages) {
       report(a.err, SAR_ERR_BOUNDS, SITE_DECODE_BOUNDS, key0);
       return false;
     }
-    const int off = key0 - bi * a.page_size;
-    const size_t elem = (((size_t)page * a.kvh + kh) * a.page_size + off) * D;
+    const int row = (page * a.kvh + kh) * a.page_size + (key0 - bi * a.page_size);
     const uint32_t bar = smem_u32(&bars[s]);
-    uint8_t* dst = ring + s * 2 * BLK_BYTES;
+    const uint32_t dst = smem_u32(ring + s * STAGE_BYTES);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_expect_tx(bar, 2 * BLK_BYTES);
-    bulk_g2s(smem_u32(dst), static_cast<const T*>(a.k_cache) + elem, BLK_BYTES, bar);
-    bulk_g2s(smem_u32(dst + BLK_BYTES), static_cast<const T*>(a.v_cache) + elem, BLK_BYTES, bar);
+    mbar_expect_tx(bar, STAGE_BYTES);
+#pragma unroll
+    for (int h = 0; h < HALVES; ++h) {
+      tma_load_2d(dst + h * kBlockKeys * 128, &tmk, h * 64, row, bar);
+      tma_load_2d(dst + BLK_BYTES + h * kBlockKeys * 128, &tmv, h * 64, row, bar);
+    }
     return true;
   };
 
-  // query heads of this KV head, pre-scaled so that softmax runs in base 2
-  const float qscale = rsqrtf((float)D) * 1.4426950408889634f;
-  float q[GP][DPL];
+  // ---- query fragments: rows = the group's heads (zero rows pad to 16), split hi + lo ----
+  const int g = lane >> 2, c4 = lane & 3;
+  const float qscale = rsqrtf((float)D) * 1.4426950408889634f;  // softmax in base 2
+  uint32_t qh[KT][2], ql[KT][2];  // registers a0 and a2 of the A fragment; a1, a3 (rows 8..15) are zero
 #pragma unroll
-  for (int h = 0; h < GP; ++h) {
+  for (int kk = 0; kk < KT; ++kk) {
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) q[h][e] = 0.f;
-    if (h < G) {
-      if (a.q32) {
-        const float* qp = a.q32 + (size_t)b * a.ld32 + (size_t)(kh * G + h) * D + lane * DPL;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) q[h][e] = qp[e] * qscale;
-      } else {
-        const T* qp = static_cast<const T*>(a.qkv) + (size_t)b * a.ld + (size_t)(kh * G + h) * D + lane * DPL;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) q[h][e] = Elem<T>::to(qp[e]) * qscale;
+    for (int r = 0; r < 2; ++r) {
+      const int col = kk * 16 + r * 8 + 2 * c4;
+      float x0 = 0.f, x1 = 0.f;
+      if (g < G) {
+        if (a.q32) {
+          const float* qp = a.q32 + (size_t)b * a.ld32 + (size_t)(kh * G + g) * D + col;
+          x0 = qp[0] * qscale;
+          x1 = qp[1] * qscale;
+        } else {
+          const T* qp = static_cast<const T*>(a.qkv) + (size_t)b * a.ld + (size_t)(kh * G + g) * D + col;
+          x0 = Elem<T>::to(qp[0]) * qscale;
+          x1 = Elem<T>::to(qp[1]) * qscale;
+        }
       }
+      const uint32_t hi = Elem<T>::pack(x0, x1);
+      qh[kk][r] = hi;
+      ql[kk][r] = Elem<T>::pack(x0 - Elem<T>::lo(hi), x1 - Elem<T>::hi(hi));
     }
   }
 
-  float m_run[GP], acc[GP][DPL];
+  float o[NT][4];
 #pragma unroll
-  for (int h = 0; h < GP; ++h) {
-    m_run[h] = -INFINITY;
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
-  }
-  float l_part = 0.f;  // this lane's share of its own head's denominator
+  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m_run = -INFINITY, l_part = 0.f;  // for query row g (this lane's share of the sum)
 
-  // my blocks: j = warp, warp + 4, ...
   const int my_n = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
   bool ok = true;
-  int issued = 0, consumed = 0;  // blocks put in flight / taken out (lane 0's view)
+  int issued = 0, consumed = 0;
   if (lane == 0) {
     for (int i = 0; i < kStages && i < my_n && ok; ++i) {
       ok = issue(warp + i * kWarps, i);
@@ -174,116 +206,57 @@ __global__ void __launch_bounds__(kWarps * 32, GP >= 8 ? 2 : 3) decode_attn_kern
     }
     ++consumed;
     const int j = warp + i * kWarps;
-    const int key0 = kbeg + j * kBlockKeys;
-    const int nk = min(kBlockKeys, kend - key0);
-    const uint8_t* kb = ring + s * 2 * BLK_BYTES;
-    const uint8_t* vb = kb + BLK_BYTES;
+    const int nk = min(kBlockKeys, kend - (kbeg + j * kBlockKeys));
+    const uint32_t kb = smem_u32(ring + s * STAGE_BYTES);
+    const uint32_t vb = kb + BLK_BYTES;
+    const int mi = lane >> 3;
 
-    // ---- scores: partial dots over this lane's dims, then butterfly ----
-    float v[NV];
+    // ---- S = Q K^T: 16 rows x 16 keys ----
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-    for (int k = 0; k < kBlockKeys; ++k) {
-      float kf[DPL];
-      if constexpr (DPL == 4) {
-        const uint2 kv = *reinterpret_cast<const uint2*>(kb + (k * D + lane * 4) * 2);
-        kf[0] = Elem<T>::lo(kv.x); kf[1] = Elem<T>::hi(kv.x); kf[2] = Elem<T>::lo(kv.y); kf[3] = Elem<T>::hi(kv.y);
-      } else {
-        const uint32_t kv = *reinterpret_cast<const uint32_t*>(kb + (k * D + lane * 2) * 2);
-        kf[0] = Elem<T>::lo(kv); kf[1] = Elem<T>::hi(kv);
-      }
+    for (int kk = 0; kk < KT; kk += 2) {
 #pragma unroll
-      for (int h = 0; h < GP; ++h) {
-        float d = 0.f;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) d = fmaf(q[h][e], kf[e], d);
-        v[h * kBlockKeys + k] = d;
+      for (int jn = 0; jn < 2; ++jn) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + blk_off(jn * 8 + (lane & 7), kk * 2 + mi), b0, b1, b2, b3);
+        mma16816<T>(sc[jn], qh[kk][0], 0u, qh[kk][1], 0u, b0, b1);
+        mma16816<T>(sc[jn], ql[kk][0], 0u, ql[kk][1], 0u, b0, b1);
+        mma16816<T>(sc[jn], qh[kk + 1][0], 0u, qh[kk + 1][1], 0u, b2, b3);
+        mma16816<T>(sc[jn], ql[kk + 1][0], 0u, ql[kk + 1][1], 0u, b2, b3);
       }
     }
-    butterfly_step<NV, 0>(v, lane);
-    butterfly_step<NV, 1>(v, lane);
-    butterfly_step<NV, 2>(v, lane);
-    butterfly_step<NV, 3>(v, lane);
-    if constexpr (NV >= 32) {
-      butterfly_step<NV, 4>(v, lane);
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-    }
-    // lane now holds scores of indices [base, base + NVL): index = head*16 + key
-    const int base = NV >= 32 ? lane * NVL : (lane >> 1);
-    const int myh = base / kBlockKeys;
-    float bmax = -INFINITY;
+    // ---- online softmax for row g over keys jn*8 + 2*c4 + e ----
+    float mx = -INFINITY;
 #pragma unroll
-    for (int t = 0; t < NVL; ++t) {
-      const int key = (base + t) % kBlockKeys;
-      if (key >= nk) v[t] = -INFINITY;
-      bmax = fmaxf(bmax, v[t]);
-    }
-    // lanes of one head: a contiguous group of 16/NVL lanes (NV >= 32), or all (NV == 16)
-    constexpr int GROUP = NV >= 32 ? kBlockKeys / NVL : 32;
+    for (int jn = 0; jn < 2; ++jn)
 #pragma unroll
-    for (int o = (NV >= 32 ? 1 : 2); o < GROUP; o <<= 1)
-      bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
-    float alpha[GP];
-#pragma unroll
-    for (int h = 0; h < GP; ++h) {
-      const int src = NV >= 32 ? h * GROUP : 0;
-      const float bm = __shfl_sync(0xffffffffu, bmax, src);
-      const float mn = fmaxf(m_run[h], bm);
-      alpha[h] = exp2f(m_run[h] - mn);
-      m_run[h] = mn;
-    }
-    float psum = 0.f;
-    float mh = m_run[0], am = alpha[0];
-#pragma unroll
-    for (int h = 1; h < GP; ++h)
-      if (h == myh) {
-        mh = m_run[h];
-        am = alpha[h];
+      for (int e = 0; e < 2; ++e) {
+        if (jn * 8 + 2 * c4 + e >= nk) sc[jn][e] = -INFINITY;
+        mx = fmaxf(mx, sc[jn][e]);
       }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mn = fmaxf(m_run, mx);  // finite: every block has at least one key
+    const float alpha = exp2f(m_run - mn);
+    m_run = mn;
+    const float p00 = exp2f(sc[0][0] - mn), p01 = exp2f(sc[0][1] - mn);
+    const float p10 = exp2f(sc[1][0] - mn), p11 = exp2f(sc[1][1] - mn);
+    l_part = l_part * alpha + (p00 + p01 + p10 + p11);
+    const uint32_t pa0 = Elem<T>::pack(p00, p01), pa2 = Elem<T>::pack(p10, p11);
+    // ---- O = O * alpha + P V ----
 #pragma unroll
-    for (int t = 0; t < NVL; ++t) {
-      const float p = exp2f(v[t] - mh);
-      psum += p;
-      const int idx = base + t;
-      pbuf[(idx % kBlockKeys) * GP + idx / kBlockKeys] = p;  // [key][head]
+    for (int n = 0; n < NT; ++n) {
+      o[n][0] *= alpha;
+      o[n][1] *= alpha;
     }
-    if (NV < 32 && (lane & 1)) psum = 0.f;  // lane pairs hold the same value
-    l_part = l_part * am + psum;
-    __syncwarp();
-
-    // ---- acc = acc * alpha + P V ----
 #pragma unroll
-    for (int h = 0; h < GP; ++h)
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) acc[h][e] *= alpha[h];
-#pragma unroll 4
-    for (int k = 0; k < nk; ++k) {
-      float vf[DPL];
-      if constexpr (DPL == 4) {
-        const uint2 vv = *reinterpret_cast<const uint2*>(vb + (k * D + lane * 4) * 2);
-        vf[0] = Elem<T>::lo(vv.x); vf[1] = Elem<T>::hi(vv.x); vf[2] = Elem<T>::lo(vv.y); vf[3] = Elem<T>::hi(vv.y);
-      } else {
-        const uint32_t vv = *reinterpret_cast<const uint32_t*>(vb + (k * D + lane * 2) * 2);
-        vf[0] = Elem<T>::lo(vv); vf[1] = Elem<T>::hi(vv);
-      }
-      float p[GP];
-      if constexpr (GP >= 4) {
-#pragma unroll
-        for (int h = 0; h < GP; h += 4) {
-          const float4 p4 = *reinterpret_cast<const float4*>(&pbuf[k * GP + h]);
-          p[h] = p4.x; p[h + 1] = p4.y; p[h + 2] = p4.z; p[h + 3] = p4.w;
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < GP; ++h) p[h] = pbuf[k * GP + h];
-      }
-#pragma unroll
-      for (int h = 0; h < GP; ++h)
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(p[h], vf[e], acc[h][e]);
+    for (int n = 0; n < NT; n += 2) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(vb + blk_off((mi & 1) * 8 + (lane & 7), n + (mi >> 1)), b0, b1, b2, b3);
+      mma16816<T>(o[n], pa0, 0u, pa2, 0u, b0, b1);
+      mma16816<T>(o[n + 1], pa0, 0u, pa2, 0u, b2, b3);
     }
     __syncwarp();
-    // refill this stage with block i + kStages
     if (i + kStages < my_n) {
       int r = 1;
       if (lane == 0) {
@@ -300,36 +273,33 @@ __global__ void __launch_bounds__(kWarps * 32, GP >= 8 ? 2 : 3) decode_attn_kern
   }
   __syncwarp();
 
-  // ---- per-warp denominators, then merge the 4 warps ----
+  // ---- per-warp row state into shared memory, then merge the 4 warps ----
   float lsum = l_part;
-  {
-    constexpr int GROUP = NV >= 32 ? kBlockKeys / NVL : 32;
+  lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+  lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+  float* my = reinterpret_cast<float*>(ring);
+  if (g < G) {
 #pragma unroll
-    for (int o = 1; o < GROUP; o <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-  }
-  float* my = mrg + warp * GP * (D + 2);
-#pragma unroll
-  for (int h = 0; h < GP; ++h) {
-    constexpr int GROUP = NV >= 32 ? kBlockKeys / NVL : 32;
-    const float lh = __shfl_sync(0xffffffffu, lsum, NV >= 32 ? h * GROUP : 0);
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) my[h * (D + 2) + lane * DPL + e] = acc[h][e];
-    if (lane == 0) {
-      my[h * (D + 2) + D] = m_run[h];
-      my[h * (D + 2) + D + 1] = lh;
+    for (int n = 0; n < NT; ++n) {
+      my[g * (D + 2) + n * 8 + 2 * c4] = o[n][0];
+      my[g * (D + 2) + n * 8 + 2 * c4 + 1] = o[n][1];
+    }
+    if (c4 == 0) {
+      my[g * (D + 2) + D] = m_run;
+      my[g * (D + 2) + D + 1] = lsum;
     }
   }
   __syncthreads();
-  // 128 threads: thread t handles (head, dim) pairs
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int h = idx / D, dd = idx - h * D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mrg[w * GP * (D + 2) + h * (D + 2) + D]);
+    for (int w = 0; w < kWarps; ++w)
+      M = fmaxf(M, reinterpret_cast<const float*>(smem + w * kStages * STAGE_BYTES)[h * (D + 2) + D]);
     float L = 0.f, A = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      const float* src = mrg + w * GP * (D + 2) + h * (D + 2);
+      const float* src = reinterpret_cast<const float*>(smem + w * kStages * STAGE_BYTES) + h * (D + 2);
       const float sc = (src[D] == -INFINITY) ? 0.f : exp2f(src[D] - M);
       L = fmaf(src[D + 1], sc, L);
       A = fmaf(src[dd], sc, A);
@@ -376,20 +346,19 @@ __global__ void decode_combine_kernel(DecodeAttnArgs a) {
   static_cast<T*>(a.out)[(size_t)b * a.ld_out + (size_t)hq * D + dd] = Elem<T>::from(A / L);
 }
 
-template <typename T, int D, int GP, bool COMPUTED = false>
-int launch_impl(const DecodeAttnArgs& a, cudaStream_t s) {
-  constexpr int NV = kBlockKeys * GP;
-  const size_t smem = (size_t)kWarps * kStages * 2 * kBlockKeys * D * 2 + (size_t)kWarps * NV * 4 +
-                      (size_t)kWarps * GP * (D + 2) * 4 + (size_t)kWarps * kStages * 8 + 16;
+template <typename T, int D, bool COMPUTED = false>
+int launch_impl(const DecodeAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t s) {
+  constexpr int STAGE_BYTES = 2 * (D / 64) * kBlockKeys * 128;
+  const size_t smem = 1024 + (size_t)kWarps * kStages * STAGE_BYTES + (size_t)kWarps * kStages * 8;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<T, D, GP, COMPUTED>,
+    cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<T, D, COMPUTED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_error(e, "decode attention attribute");
     attr = true;
   }
   const int n_ctas = COMPUTED ? a.n_decode * a.max_splits : a.n_items;
-  decode_attn_kernel<T, D, GP, COMPUTED><<<dim3(n_ctas, a.kvh), kWarps * 32, smem, s>>>(a);
+  decode_attn_kernel<T, D, COMPUTED><<<dim3(n_ctas, a.kvh), kWarps * 32, smem, s>>>(tmk, tmv, a);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "decode attention launch");
@@ -402,22 +371,31 @@ int launch_impl(const DecodeAttnArgs& a, cudaStream_t s) {
   return SAR_OK;
 }
 
+template <bool COMPUTED>
+int dispatch(const DecodeAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t s) {
+  const bool bf = a.storage == SAR_STORAGE_BF16;
+  if (a.d == 128) return bf ? launch_impl<__nv_bfloat16, 128, COMPUTED>(a, tmk, tmv, s)
+                            : launch_impl<__half, 128, COMPUTED>(a, tmk, tmv, s);
+  if (a.d == 64) return bf ? launch_impl<__nv_bfloat16, 64, COMPUTED>(a, tmk, tmv, s)
+                           : launch_impl<__half, 64, COMPUTED>(a, tmk, tmv, s);
+  return set_error(SAR_ERR_UNSUPPORTED, "decode attention: head_dim must be 64 or 128");
+}
+
 }  // namespace
 
-int launch_decode_attention(const DecodeAttnArgs& a, cudaStream_t s) {
+int make_kv_tmap(CUtensorMap* map, const void* pages, int num_pages, int kvh, int page_size, int head_dim,
+                 int storage) {
+  // rows = (page, head, slot) triples, columns = head_dim; boxes of 16 slots x 64 dimensions
+  return make_tmap_16(map, pages, (uint64_t)num_pages * kvh * page_size, head_dim, kBlockKeys, storage);
+}
+
+int launch_decode_attention(const DecodeAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                            cudaStream_t s) {
   if (a.n_items <= 0) return SAR_OK;
   const int G = a.qh / a.kvh;
-  if (a.qh % a.kvh || G > 8 || (a.d != 64 && a.d != 128) || a.page_size % kBlockKeys)
+  if (a.qh % a.kvh || G > kMaxGroup || (a.d != 64 && a.d != 128) || a.page_size % kBlockKeys)
     return set_error(SAR_ERR_UNSUPPORTED, "decode attention: head_dim 64/128, group <= 8, page % 16");
-  const int GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
-#define SAR_DEC(DD, GG)                                                             \
-  if (a.d == DD && GP == GG)                                                         \
-    return a.storage == SAR_STORAGE_BF16 ? launch_impl<__nv_bfloat16, DD, GG>(a, s) \
-                                         : launch_impl<__half, DD, GG>(a, s);
-  SAR_DEC(128, 1) SAR_DEC(128, 2) SAR_DEC(128, 4) SAR_DEC(128, 8)
-  SAR_DEC(64, 1) SAR_DEC(64, 2) SAR_DEC(64, 4) SAR_DEC(64, 8)
-#undef SAR_DEC
-  return set_error(SAR_ERR_UNSUPPORTED, "decode attention: no kernel for this shape");
+  return dispatch<false>(a, tmk, tmv, s);
 }
 
 }  // namespace sar
@@ -515,14 +493,9 @@ extern "C" int sar_decode_attention_noalloc(const void* q, int32_t q_stride, con
   a.max_splits = (int)max_splits;
   a.bt_stride = bt_stride;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int G = n_q_heads / n_kv_heads;
-  const int GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
-#define SAR_DEC_NA(DD, GG)                                                                 \
-  if (head_dim == DD && GP == GG)                                                          \
-    return storage == SAR_STORAGE_BF16 ? launch_impl<__nv_bfloat16, DD, GG, true>(a, s) \
-                                       : launch_impl<__half, DD, GG, true>(a, s);
-  SAR_DEC_NA(128, 1) SAR_DEC_NA(128, 2) SAR_DEC_NA(128, 4) SAR_DEC_NA(128, 8)
-  SAR_DEC_NA(64, 1) SAR_DEC_NA(64, 2) SAR_DEC_NA(64, 4) SAR_DEC_NA(64, 8)
-#undef SAR_DEC_NA
-  return set_error(SAR_ERR_UNSUPPORTED, "decode_attention_noalloc: no kernel for this shape");
+  CUtensorMap tmk, tmv;  // host-side descriptors of the caller's pages (no device memory)
+  int rc = make_kv_tmap(&tmk, k_pages, num_pages, n_kv_heads, page_size, head_dim, storage);
+  if (rc == SAR_OK) rc = make_kv_tmap(&tmv, v_pages, num_pages, n_kv_heads, page_size, head_dim, storage);
+  if (rc != SAR_OK) return rc;
+  return dispatch<true>(a, tmk, tmv, s);
 }

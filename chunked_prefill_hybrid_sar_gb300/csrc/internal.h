@@ -101,7 +101,12 @@ struct DecodeAttnArgs {
   const int32_t* ctx_lens = nullptr;  // [n_decode]
   int split_keys = 0, max_splits = 0, bt_stride = 0;
 };
-int launch_decode_attention(const DecodeAttnArgs& a, cudaStream_t s);
+// Tensor map over one layer's K or V pages viewed as rows of head_dim values
+// (one row per page x head x slot), 16-row x 64-column boxes, 128-byte swizzle.
+int make_kv_tmap(CUtensorMap* map, const void* pages, int num_pages, int kvh, int page_size, int head_dim,
+                 int storage);
+int launch_decode_attention(const DecodeAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                            cudaStream_t s);
 
 struct ChunkAttnArgs {
   const float* q32;          // chunk query rows [0, len) in fp32; row stride ld32

@@ -88,6 +88,7 @@ struct sar_kv {
   int page_size = 0, num_pages = 0;
   uint16_t *k = nullptr, *v = nullptr;
   size_t layer_elems = 0;
+  std::vector<CUtensorMap> tmk, tmv;  // per layer: decode attention's view of the pages
 };
 
 namespace {
@@ -416,7 +417,7 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
       da.page_size = kv->page_size;
       da.num_pages = kv->num_pages;
       da.err = m->err;
-      SAR_TRY(sar::launch_decode_attention(da, s));
+      SAR_TRY(sar::launch_decode_attention(da, kv->tmk[l], kv->tmv[l], s));
     }
     {
       Prof pr(m, SAR_K_GEMM_O, s);
@@ -629,6 +630,19 @@ int sar_kv_create(const sar_model* m, int32_t page_size, int32_t num_pages, sar_
     cudaFree(kv->v);
     delete kv;
     return cuda_error(e, "kv: arena");
+  }
+  kv->tmk.resize(m->d.n_layers);
+  kv->tmv.resize(m->d.n_layers);
+  for (int l = 0; l < m->d.n_layers; ++l) {
+    int rc = sar::make_kv_tmap(&kv->tmk[l], kv->k + (size_t)l * kv->layer_elems, num_pages, m->d.n_kv_heads,
+                               page_size, m->d.head_dim, m->d.storage);
+    if (rc == SAR_OK)
+      rc = sar::make_kv_tmap(&kv->tmv[l], kv->v + (size_t)l * kv->layer_elems, num_pages, m->d.n_kv_heads,
+                             page_size, m->d.head_dim, m->d.storage);
+    if (rc != SAR_OK) {
+      sar_kv_destroy(kv);
+      return rc;
+    }
   }
   *out = kv;
   return SAR_OK;
