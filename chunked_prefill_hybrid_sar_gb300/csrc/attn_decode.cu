@@ -151,6 +151,18 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     return true;
   };
 
+  // first pages in flight before the query loads, so their latencies overlap
+  const int my_n = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
+  bool ok = true;
+  int issued = 0, consumed = 0;
+  if (lane == 0) {
+    for (int i = 0; i < kStages && i < my_n && ok; ++i) {
+      ok = issue(warp + i * kWarps, i);
+      if (ok) ++issued;
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+
   // ---- query fragments: rows = the group's heads (zero rows pad to 16), split hi + lo ----
   const int g = lane >> 2, c4 = lane & 3;
   const float qscale = rsqrtf((float)D) * 1.4426950408889634f;  // softmax in base 2
@@ -183,16 +195,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m_run = -INFINITY, l_part = 0.f;  // for query row g (this lane's share of the sum)
 
-  const int my_n = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
-  bool ok = true;
-  int issued = 0, consumed = 0;
-  if (lane == 0) {
-    for (int i = 0; i < kStages && i < my_n && ok; ++i) {
-      ok = issue(warp + i * kWarps, i);
-      if (ok) ++issued;
-    }
-  }
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 
   for (int i = 0; i < my_n && ok; ++i) {
     const int s = i % kStages;
