@@ -16,6 +16,13 @@
 //                stores.  Two accumulators alternate so the epilogue of one
 //                tile overlaps the MMAs of the next.
 //
+// Clusters (non-swap): the CTAs of a 2- or 4-CTA cluster take consecutive
+// token tiles of one weight tile; each fetches 1/cl of the weight rows of every
+// K slab and multicasts them into all the cluster's shared memories, so the
+// weights leave L2 once per cluster.  A stage is refilled only after every
+// CTA's MMAs released it (the empty barrier counts one multicast commit per
+// CTA).
+//
 // Tilings: non-swap puts 128 token rows on the MMA M side (msub = 2 stacks two
 // such MMAs on one weight tile for 256-row tiles); swap puts 128 weight rows
 // on the M side and the tokens (padded to 16) on the N side, so a step with
@@ -72,6 +79,15 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Arrive on the same barrier offset in every CTA of `mask` once this thread's
+// MMAs so far have completed.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -119,20 +135,24 @@ struct Params {
   int M, N, K;
   int bn, m_tiles, n_tiles, k_blocks, stages, stage_bytes, tmem_cols;
   int splits, kb_per_split;  // split-K: `splits` K ranges per tile (residual epilogue only)
+  int cl, m_groups;          // cluster size sharing one weight tile (multicast); token-tile groups
   void* c;
   const void* r;
   int* err;
 };
 
-// Work unit u -> (token tile, weight tile, K-slab range).  Token tiles vary
-// fastest so that CTAs running at the same time share one weight slab in L2.
+// Work unit u of a cluster -> (token tile, weight tile, K-slab range).  The
+// `cl` CTAs of a cluster take consecutive token tiles of one weight tile (and
+// share that tile by multicast); token-tile groups vary fastest so clusters
+// running at the same time also share the weight slab in L2.
 struct Unit {
   int mt, nt, kb0, kb1;
 };
-__device__ __forceinline__ Unit unit_of(const Params& p, int u) {
+__device__ __forceinline__ Unit unit_of(const Params& p, int u, int rank) {
   Unit w;
-  w.mt = u % p.m_tiles;
-  const int r = u / p.m_tiles;
+  const int mg = u % p.m_groups;
+  w.mt = mg * p.cl + rank;
+  const int r = u / p.m_groups;
   const int sp = r % p.splits;
   w.nt = r / p.splits;
   w.kb0 = sp * p.kb_per_split;
@@ -177,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
-      mbar_init(smem_u32(&empty_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), (uint32_t)p.cl);  // released by every CTA of the cluster
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&accf_bar[s]), 1);
@@ -191,10 +211,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (p.cl > 1) cluster_sync();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int n_tiles_total = p.m_tiles * p.n_tiles * p.splits;  // work units
+  const int rank = p.cl > 1 ? (int)cluster_ctarank() : 0;
+  const int cid = blockIdx.x / p.cl, n_clusters = gridDim.x / p.cl;
+  const uint16_t cl_mask = (uint16_t)((1u << p.cl) - 1u);
+  const int n_tiles_total = p.m_groups * p.n_tiles * p.splits;  // work units per cluster
   const int acc_cols = MSUB * p.bn;
 
   if (warp == 0) {
@@ -204,8 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < n_tiles_total && ok; t += gridDim.x) {
-        const Unit un = unit_of(p, t);
+      for (int t = cid; t < n_tiles_total && ok; t += n_clusters) {
+        const Unit un = unit_of(p, t, rank);
         const int mt = un.mt, nt = un.nt;
         // A rows: tokens (non-swap) or weights (swap); B rows: the other one.
         const int a_row = SWAP ? nt * 128 : mt * 128 * MSUB;
@@ -213,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the weight tile streams from HBM: pull it into L2 kPrefetch K-slabs ahead
         // of the shared-memory ring so the ring's loads hit L2
         const void* w_map = SWAP ? (const void*)&tm_a : (const void*)&tm_b;
-        const int w_row = SWAP ? a_row : b_row;
+        const int slice = p.bn / p.cl;  // weight rows this CTA fetches (and multicasts)
+        const int w_row = SWAP ? a_row : b_row + rank * slice;
         for (int kb = un.kb0; kb < un.kb0 + kPrefetch && kb < un.kb1; ++kb) tma_prefetch_l2(w_map, kb * kBK, w_row);
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (kb + kPrefetch < un.kb1) tma_prefetch_l2(w_map, (kb + kPrefetch) * kBK, w_row);
@@ -227,7 +252,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int s = 0; s < MSUB; ++s)
             tma_load_2d(smem_u32(st + s * kTileA), &tm_a, kb * kBK, a_row + s * 128, fb);
-          tma_load_2d(smem_u32(st + MSUB * kTileA), &tm_b, kb * kBK, b_row, fb);
+          if (p.cl > 1)
+            tma_load_2d_mc(smem_u32(st + MSUB * kTileA + rank * slice * 128), &tm_b, kb * kBK, b_row + rank * slice,
+                           fb, cl_mask);
+          else
+            tma_load_2d(smem_u32(st + MSUB * kTileA), &tm_b, kb * kBK, b_row, fb);
+          next_stage(stage, phase, stages);
+        }
+      }
+      if (p.cl > 1) {
+        // every CTA of the cluster has released the last fills: no peer will
+        // arrive on this CTA's barriers after it leaves
+        for (int i = 0; i < stages && ok; ++i) {
+          ok = mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.err, SITE_GEMM_PRODUCER);
           next_stage(stage, phase, stages);
         }
       }
@@ -240,13 +277,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       int i = 0;
-      for (int t = blockIdx.x; t < n_tiles_total && ok; t += gridDim.x, ++i) {
+      for (int t = cid; t < n_tiles_total && ok; t += n_clusters, ++i) {
         const int acc = i & 1;
         const uint32_t accph = (uint32_t)((i >> 1) & 1);
         if (!mbar_wait(smem_u32(&acce_bar[acc]), accph ^ 1u, p.err, SITE_GEMM_MMA)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * acc_cols);
-        const Unit un = unit_of(p, t);
+        const Unit un = unit_of(p, t, rank);
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.err, SITE_GEMM_MMA)) {
             ok = false;
@@ -264,7 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16(d_tmem + (uint32_t)(s * p.bn), adesc, bdesc, idesc, (kb != un.kb0) || (kk != 0));
             }
           }
-          mma_commit(smem_u32(&empty_bar[stage]));
+          if (p.cl > 1)
+            mma_commit_mc(smem_u32(&empty_bar[stage]), cl_mask);
+          else
+            mma_commit(smem_u32(&empty_bar[stage]));
           next_stage(stage, phase, stages);
         }
         if (ok) mma_commit(smem_u32(&accf_bar[acc]));
@@ -277,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lrow = q * 32 + lane;     // accumulator lane = row of the MMA's M side
     int i = 0;
     bool alive = true;  // false once a wait gave up: loads/stores stop, barriers stay matched
-    for (int t = blockIdx.x; t < n_tiles_total; t += gridDim.x, ++i) {
-      const Unit un = unit_of(p, t);
+    for (int t = cid; t < n_tiles_total; t += n_clusters, ++i) {
+      const Unit un = unit_of(p, t, rank);
       const int mt = un.mt, nt = un.nt;
       const int acc = i & 1;
       const uint32_t accph = (uint32_t)((i >> 1) & 1);
@@ -431,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (p.cl > 1) cluster_sync();  // no CTA leaves while a peer may still address it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
@@ -504,6 +545,9 @@ int make_tmap_16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols
 }
 
 int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in_place) {
+  const int cl_flag = variant & (SAR_GEMM_CLUSTER_1 | SAR_GEMM_CLUSTER_2 | SAR_GEMM_CLUSTER_4);
+  variant &= ~(SAR_GEMM_CLUSTER_1 | SAR_GEMM_CLUSTER_2 | SAR_GEMM_CLUSTER_4);
+  if (cl_flag & (cl_flag - 1)) return set_error(SAR_ERR_INVALID_ARG, "gemm: more than one cluster flag");
   if (M < 1 || N < 64 || K < 64 || N % 64 || K % 64)
     return set_error(SAR_ERR_UNSUPPORTED, "gemm: need M >= 1, N and K multiples of 64");
   if (epi == SAR_EPI_SWIGLU && N % 128)
@@ -563,16 +607,31 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
   if (!c.swap && N % c.bn && epi == SAR_EPI_SWIGLU)
     return set_error(SAR_ERR_UNSUPPORTED, "gemm: SwiGLU tiles must not straddle N");
   if (c.swap) {
+    if (cl_flag > SAR_GEMM_CLUSTER_1) return set_error(SAR_ERR_UNSUPPORTED, "gemm: swap tiling takes no cluster");
     c.m_tiles = 1;
     c.n_tiles = (N + 127) / 128;
     c.a_box_rows = 128;   // weights
     c.b_box_rows = c.bn;  // tokens
+    c.cl = 1;
   } else {
     c.m_tiles = (M + 128 * c.msub - 1) / (128 * c.msub);
     c.n_tiles = (N + c.bn - 1) / c.bn;
-    c.a_box_rows = 128;   // tokens
-    c.b_box_rows = c.bn;  // weights
+    // token tiles of one weight tile run as a cluster that multicasts the tile
+    if (cl_flag == SAR_GEMM_CLUSTER_1) c.cl = 1;
+    else if (cl_flag == SAR_GEMM_CLUSTER_2) c.cl = 2;
+    else if (cl_flag == SAR_GEMM_CLUSTER_4) c.cl = 4;
+    else {
+      // pairs only: a GPC's SMs do not divide into clusters of 4, which then
+      // leaves SMs idle; and only when the work spans two or more waves (below
+      // that the cluster launch costs more than the L2 traffic it saves)
+      const long units = (long)c.m_tiles * c.n_tiles;
+      c.cl = (c.m_tiles % 2 == 0 && units >= 2L * sms) ? 2 : 1;
+    }
+    if (c.m_tiles % c.cl) return set_error(SAR_ERR_UNSUPPORTED, "gemm: cluster size does not divide the token tiles");
+    c.a_box_rows = 128;          // tokens
+    c.b_box_rows = c.bn / c.cl;  // this CTA's slice of the weight tile
   }
+  c.m_groups = c.m_tiles / c.cl;
   const int stage_bytes = c.msub * kTileA + c.bn * kBK * 2;
   const int extra = kBarBytes + 1024 + ((c.swap && epi == SAR_EPI_SWIGLU) ? kSwapXchg : 0);
   c.stages = std::min(8, (kSmemLimit - extra) / stage_bytes);
@@ -582,7 +641,7 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
   best_split((long)c.m_tiles * c.n_tiles, c.swap ? kslab_clocks(1, c.bn) : kslab_clocks(c.msub, c.bn), &c.splits);
   c.kb_per_split = (k_blocks + c.splits - 1) / c.splits;
   c.splits = (k_blocks + c.kb_per_split - 1) / c.kb_per_split;  // no empty K range
-  c.grid = std::min(c.m_tiles * c.n_tiles * c.splits, sms);
+  c.grid = std::min(c.m_tiles * c.n_tiles * c.splits, sms) / c.cl * c.cl;  // whole clusters; refined at launch
   *cfg = c;
   return SAR_OK;
 }
@@ -608,9 +667,14 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   p.stages = cfg.stages;
   p.stage_bytes = cfg.msub * kTileA + cfg.bn * kBK * 2;
   p.tmem_cols = pow2_at_least(2 * cfg.msub * cfg.bn);
+  p.cl = cfg.cl;
+  p.m_groups = cfg.m_groups;
   p.c = c;
   p.r = residual;
   p.err = err;
+  if (cfg.cl < 1 || cfg.m_tiles % cfg.cl || cfg.m_groups * cfg.cl != cfg.m_tiles || cfg.bn % (8 * cfg.cl) ||
+      (cfg.swap && cfg.cl != 1))
+    return set_error(SAR_ERR_INVALID_ARG, "gemm: inconsistent cluster configuration");
   static bool attr_done[2][4][2][3] = {};
   bool& done = attr_done[storage == SAR_STORAGE_BF16][epi][cfg.swap][cfg.msub];
   if (!done) {
@@ -621,7 +685,33 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   const CUtensorMap& ta = cfg.swap ? w_map : act_map;
   const CUtensorMap& tb = cfg.swap ? act_map : w_map;
   void* args[] = {const_cast<CUtensorMap*>(&ta), const_cast<CUtensorMap*>(&tb), &p};
-  cudaError_t e = cudaLaunchKernel(fn, dim3(cfg.grid), dim3(kThreads), args, (size_t)cfg.smem, s);
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = (size_t)cfg.smem;
+  lc.stream = s;
+  int grid = cfg.grid;
+  if (cfg.cl > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cfg.cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    // persistent grid: as many whole clusters as can be resident at once (the
+    // SMs of a GPC need not divide into clusters evenly)
+    static int max_clusters[2][4][3][5][2] = {};
+    int& mc = max_clusters[storage == SAR_STORAGE_BF16][epi][cfg.msub][cfg.cl][cfg.bn == 256];
+    if (mc == 0) {
+      lc.gridDim = dim3(cfg.cl * 64);
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&mc, fn, &lc);
+      if (e != cudaSuccess || mc < 1) return cuda_error(e != cudaSuccess ? e : cudaErrorInvalidConfiguration,
+                                                         "gemm: cluster occupancy");
+    }
+    grid = std::min(cfg.m_groups * cfg.n_tiles * cfg.splits, mc) * cfg.cl;
+  }
+  lc.gridDim = dim3(grid);
+  cudaError_t e = cudaLaunchKernelExC(&lc, fn, args);
   if (e != cudaSuccess) return cuda_error(e, "gemm launch");
   count_launches(1);
   return SAR_OK;

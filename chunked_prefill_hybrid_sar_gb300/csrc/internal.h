@@ -40,7 +40,18 @@ struct GemmCfg {
   int b_box_rows = 256;
   int splits = 1;        // K ranges per tile (in-place fp32 residual epilogue only)
   int kb_per_split = 0;  // 64-wide K slabs per range
+  int cl = 1;            // CTAs per cluster sharing a weight tile by multicast (non-swap)
+  int m_groups = 0;      // token-tile groups of cl tiles
 };
+
+// Box rows of the weight maps a model keeps per matrix (index i: 32 << i); the
+// GEMM reads the weight tile through the map whose box is bn / cl rows
+// (swap tiling: 128).
+constexpr int kWeightBoxes = 4;
+inline int weight_box_index(const GemmCfg& c) {
+  const int rows = c.swap ? c.a_box_rows : c.b_box_rows;
+  return rows == 32 ? 0 : rows == 64 ? 1 : rows == 128 ? 2 : 3;
+}
 
 // Picks a tiling for C[M, .] = A[M, K] . W[N, K]^T (variant = SAR_GEMM_*).
 // Returns SAR_OK or SAR_ERR_UNSUPPORTED.

@@ -31,11 +31,12 @@ namespace {
 constexpr int kMetaRing = 4;
 
 using st16 = uint16_t;  // one element of the storage type (fp16 or bf16)
+using WMaps = CUtensorMap[sar::kWeightBoxes];  // one weight matrix, every box height
 
 struct LayerW {
   st16 *wqkv = nullptr, *wo = nullptr, *wgu = nullptr, *wd = nullptr;
   float *n1 = nullptr, *n2 = nullptr;
-  CUtensorMap m_qkv[2], m_o[2], m_gu[2], m_d[2];  // weight maps, box rows 128 / 256
+  WMaps m_qkv, m_o, m_gu, m_d;  // weight maps, box rows 32 / 64 / 128 / 256
   bool set = false;
 };
 
@@ -56,7 +57,7 @@ struct sar_model {
   std::vector<LayerW> L;
   st16 *embed = nullptr, *lm_head = nullptr;
   float* final_norm = nullptr;
-  CUtensorMap m_head[2];
+  WMaps m_head;
   bool head_set = false;
   double* inv_freq = nullptr;
   // workspace
@@ -129,20 +130,19 @@ struct Prof {
   ~Prof() { prof_end(m, s); }
 };
 
-int weight_maps(CUtensorMap (&maps)[2], const void* w, int rows, int cols, int storage) {
-  SAR_TRY(sar::make_tmap_16(&maps[0], w, rows, cols, 128, storage));
-  SAR_TRY(sar::make_tmap_16(&maps[1], w, rows, cols, 256, storage));
+int weight_maps(WMaps& maps, const void* w, int rows, int cols, int storage) {
+  for (int i = 0; i < sar::kWeightBoxes; ++i) SAR_TRY(sar::make_tmap_16(&maps[i], w, rows, cols, 32u << i, storage));
   return SAR_OK;
 }
 
 // GEMM over `rows` activation rows with the weight maps of one matrix.
-int run_gemm(sar_model* m, const st16* a, int rows, const CUtensorMap (&wmaps)[2], int N, int K, int epi,
+int run_gemm(sar_model* m, const st16* a, int rows, const WMaps& wmaps, int N, int K, int epi,
              void* c, const void* r, cudaStream_t s) {
   sar::GemmCfg cfg;
   SAR_TRY(sar::gemm_config(rows, N, K, epi, SAR_GEMM_AUTO, &cfg, c == r));
   CUtensorMap amap;
   SAR_TRY(sar::make_tmap_16(&amap, a, rows, K, cfg.swap ? cfg.b_box_rows : cfg.a_box_rows, m->d.storage));
-  const CUtensorMap& wm = cfg.swap ? wmaps[0] : wmaps[cfg.bn == 256 ? 1 : 0];
+  const CUtensorMap& wm = wmaps[sar::weight_box_index(cfg)];
   return sar::gemm_launch(cfg, amap, wm, rows, N, K, epi, m->d.storage, c, r, m->err, s);
 }
 

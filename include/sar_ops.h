@@ -38,8 +38,18 @@ enum {
   SAR_GEMM_M128_N256 = 2, /* 128 token rows x 256 weight rows per tile              */
   SAR_GEMM_SWAP = 3,      /* weights on the MMA's M side (128 rows), tokens on its N
                              side padded to 16 (M <= 256): no 128-row quantisation */
-  SAR_GEMM_M256_N128 = 4  /* 256 token rows (two 128-row MMAs sharing one weight
+  SAR_GEMM_M256_N128 = 4, /* 256 token rows (two 128-row MMAs sharing one weight
                              tile) x 128 weight rows per tile                        */
+  /* Optional flags OR-ed into a non-swap tiling (or AUTO): how many CTAs of a
+   * thread-block cluster share one weight tile.  Each fetches 1/c of the tile's
+   * rows from L2 and multicasts it to all, so the weights leave L2 once per
+   * cluster instead of once per token tile.  Without a flag the library takes
+   * 2 when the token tiles are even in number and the tiles fill two or more
+   * waves of the SMs, else 1.  A size the token tiles do not divide into
+   * returns SAR_ERR_UNSUPPORTED. */
+  SAR_GEMM_CLUSTER_1 = 0x100,
+  SAR_GEMM_CLUSTER_2 = 0x200,
+  SAR_GEMM_CLUSTER_4 = 0x400
 };
 
 /* C = epilogue(A . W^T).  A [M, K], W [N, K] in the storage type `storage`
