@@ -13,6 +13,7 @@ CPU oracle on a bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -371,7 +372,7 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ tile sweep
 
-SWEEP_ROWS = (128, 255, 256, 257, 384, 511, 512, 1024, 2048)
+SWEEP_ROWS = synth.SWEEP_ROWS
 SWEEP_DECODE_ONLY = (1, 8, 32, 64)
 
 
@@ -481,6 +482,126 @@ def run_sweep(args):
     return out
 
 
+# ------------------------------------------------------------------ serving trace
+
+def run_trace_mode(args):
+    """The 32-layer Mistral-7B shape served from a request trace (256 requests,
+    Poisson arrivals at 4 req/s, lognormal prompt / output lengths) by the
+    stall-free scheduler at each token budget, arrivals on the wall clock.
+    One JSON line with tokens/s, step latency and TTFT / TBT percentiles per
+    budget."""
+    import torch
+
+    import chunked_prefill_hybrid_sar_gb300 as sar
+    from chunked_prefill_hybrid_sar_gb300 import harness, serve
+
+    taus = [int(t) for t in args.taus.split(",")]
+    dims = synth.MISTRAL_7B
+    m, _ = harness.load_synthetic_model(0, dims, max_tokens=max(taus), max_decodes=256)
+    free, _ = torch.cuda.mem_get_info()
+    page_bytes = dims.n_layers * 2 * dims.kv_dim * PAGE * 2
+    n_pages = int(free * 0.8) // page_bytes
+    kv = sar.KVCache(m, PAGE, n_pages)
+    trace = synth.request_trace(0, args.requests, rate=4.0, prompt_median=1024, prompt_clip=(64, 8192),
+                                out_median=256, out_clip=(16, 1024))
+    toks = synth.prompt_tokens(1, trace, dims.vocab)
+    runs = {}
+    for tau in taus:
+        res = serve.run_trace(m, kv, trace, toks, tau=tau, keep_batches=False)
+        m.sync_status()
+        st = sorted(res.step_ms)
+        summ = res.summary()
+        summ["step_ms_p50"] = st[len(st) // 2] if st else None
+        summ["step_ms_p90"] = st[int(0.9 * (len(st) - 1))] if st else None
+        summ["rows_per_step"] = res.rows / max(1, len(st))
+        summ["tokens_per_s_wall"] = res.rows / res.wall_s
+        runs[tau] = summ
+    out = {"mode": "trace", "workload": f"Mistral-7B shape, 32 layers + 32000 head, f16 storage; "
+           f"{args.requests} requests, Poisson 4 req/s, prompt lognormal(median 1024, sigma 1, clip 64-8192), "
+           f"output lognormal(median 256, sigma 1, clip 16-1024), greedy sampling, wall-clock arrivals",
+           "kv_pages": n_pages, "page_size": PAGE, "per_tau": runs}
+    print(json.dumps(out))
+    return out
+
+
+# ------------------------------------------------------------------ long prompt
+
+def run_long_prompt(args):
+    """The Yi-34B shape (60 layers, 64000 head) prefilling one 16384-token
+    prompt in chunks of C tokens, each step carrying 128 decodes (contexts
+    uniform in [512, 8192], random KV): per chunk size the prefill time, the
+    chunk-attention time and the prior-chunk KV re-read the chunking implies
+    (N(N-1)/2 chunk loads per layer)."""
+    import torch
+
+    import chunked_prefill_hybrid_sar_gb300 as sar
+    from chunked_prefill_hybrid_sar_gb300 import harness
+
+    chunks = [int(c) for c in args.chunks.split(",")]
+    dims = synth.YI_34B
+    if args.layers:
+        dims = dataclasses.replace(dims, n_layers=args.layers)
+    plen, n_dec = 16384, 128
+    m, _ = harness.load_synthetic_model(0, dims, max_tokens=max(chunks) + n_dec, max_decodes=n_dec)
+    tokens, ctxs = synth.long_prompt_case(0, dims, prompt_len=plen, n_decode=n_dec, ctx_range=(512, 8192))
+    n_pages = plen // PAGE + sum(c // PAGE + 1 for c in ctxs) + 8
+    kv = sar.KVCache(m, PAGE, n_pages)
+    gen = synth.generator(2, "cuda")
+    for l in range(dims.n_layers):
+        for kind in (0, 1):
+            pv = harness.page_view(kv, l, kind, dims)
+            pv.copy_(torch.randn(pv.shape, generator=gen, device="cuda").to(pv.dtype))
+    alloc = harness.PageAllocator(range(n_pages))
+    pbt = alloc.take(plen // PAGE)
+    decs = [(100 + i, c, alloc.take(c // PAGE + 1)) for i, c in enumerate(ctxs)]
+    tok = tokens.cuda()
+    dec_tok = (torch.arange(n_dec, dtype=torch.int32, device="cuda") * 7 + 3) % dims.vocab
+    logits = torch.empty(1 + n_dec, dims.vocab, dtype=torch.float32, device="cuda")
+    xs = {C: [torch.cat([tok[s:s + C], dec_tok]).contiguous() for s in range(0, plen, C)] for C in chunks}
+    stream = torch.cuda.current_stream()
+
+    def prefill(C, events=None):
+        for i, s in enumerate(range(0, plen, C)):
+            if events is not None:
+                events[i][0].record(stream)
+            m.step(kv, sar.Batch((0, s, C, pbt), decs, in_kind=sar.SAR_IN_TOKENS), xs[C][i], logits_out=logits)
+            if events is not None:
+                events[i][1].record(stream)
+
+    if not args.no_warmup:
+        prefill(max(chunks))
+    torch.cuda.synchronize()
+    kv_tok = dims.n_layers * 2 * dims.kv_dim * 2  # K and V bytes of one token over all layers
+    per_c = {}
+    for C in chunks:
+        n = plen // C
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        prefill(C, ev)
+        torch.cuda.synchronize()
+        step_ms = [a.elapsed_time(b) for a, b in ev]
+        m.profile(True)
+        prefill(C)
+        prof = m.profile_read()
+        m.profile(False)
+        ca_ms = prof["chunk_attn"][0]
+        reread = n * (n - 1) // 2 * C * kv_tok
+        own = n * C * kv_tok
+        per_c[C] = {"steps": n, "prefill_ms": sum(step_ms), "step_ms_mean": sum(step_ms) / n,
+                    "step_ms_first": step_ms[0], "step_ms_last": step_ms[-1],
+                    "prompt_tokens_per_s": plen / (sum(step_ms) * 1e-3),
+                    "hybrid_tokens_per_s": n * (C + n_dec) / (sum(step_ms) * 1e-3),
+                    "chunk_attn_ms": ca_ms, "decode_attn_ms": prof["decode_attn"][0],
+                    "prior_chunk_kv_bytes": reread, "own_chunk_kv_bytes": own,
+                    "chunk_attn_kv_gbs": (reread + own) / (ca_ms * 1e-3) / 1e9 if ca_ms else None,
+                    "kernel_ms": {k: v[0] for k, v in prof.items() if v[1]}}
+    m.sync_status()
+    out = {"mode": "long-prompt", "workload": f"Yi-34B shape ({dims.n_layers} layers, H 7168, 56q/8kv x 128, "
+           f"FFN 20480, head 64000), f16 storage; one {plen}-token prompt in chunks of C with {n_dec} decodes "
+           f"per step (ctx U[512,8192], random KV)", "per_chunk": per_c}
+    print(json.dumps(out))
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -488,11 +609,23 @@ def main():
     ap.add_argument("--warmup", type=int, default=6)
     ap.add_argument("--impl", choices=["sar", "reference"], default="sar")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
-    ap.add_argument("--mode", choices=["step", "sweep"], default="step",
-                    help="step: the tau=512 hybrid step (default); sweep: tile-quantisation sweep")
+    ap.add_argument("--mode", choices=["step", "sweep", "trace", "long-prompt"], default="step",
+                    help="step: the tau=512 hybrid step (default); sweep: tile-quantisation sweep; "
+                         "trace: 32-layer serving trace; long-prompt: 60-layer chunked 16k prefill")
+    ap.add_argument("--taus", default="256,512,1024", help="trace mode: token budgets")
+    ap.add_argument("--requests", type=int, default=256, help="trace mode: requests of the trace")
+    ap.add_argument("--chunks", default="256,512,1024", help="long-prompt mode: chunk sizes")
+    ap.add_argument("--layers", type=int, default=0, help="long-prompt mode: fewer layers (profiling)")
+    ap.add_argument("--no-warmup", action="store_true", help="long-prompt mode: no untimed prefill first")
     args = ap.parse_args()
     if args.mode == "sweep":
         run_sweep(args)
+        return
+    if args.mode == "trace":
+        run_trace_mode(args)
+        return
+    if args.mode == "long-prompt":
+        run_long_prompt(args)
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -1,5 +1,6 @@
 // Error reporting and small process-wide bookkeeping of the C ABI.
 #include <atomic>
+#include <cstdlib>
 #include <string>
 
 #include "internal.h"
@@ -23,6 +24,14 @@ int cuda_error(cudaError_t e, const char* what) {
 }
 
 void count_launches(int64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("SAR_PDL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
 
 int num_sms() {
   int dev = 0, n = 0;

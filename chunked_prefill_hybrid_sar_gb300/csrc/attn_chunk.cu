@@ -63,6 +63,8 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   constexpr int CH = D / 8;  // 16-byte chunks per row
   constexpr int TILE = kBKV * D * 2;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -254,9 +256,10 @@ int launch_impl(const ChunkAttnArgs& a, cudaStream_t s) {
     attr = true;
   }
   dim3 grid((a.len + kBQ - 1) / kBQ, a.qh);
-  chunk_attn_kernel<T, D><<<grid, kThreads, smem, s>>>(a);
+  cudaError_t e = launch_pdl(chunk_attn_kernel<T, D>, grid, dim3(kThreads), smem, s, a);
+  if (e != cudaSuccess) return cuda_error(e, "chunk attention launch");
   count_launches(1);
-  return cuda_error(cudaGetLastError(), "chunk attention launch");
+  return SAR_OK;
 }
 
 }  // namespace

@@ -91,6 +91,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   // after the key loop each warp's own ring holds its [row][D + 2] merge record
   static_assert(kMaxGroup * (D + 2) * 4 <= kStages * STAGE_BYTES, "merge record must fit the ring");
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * STAGE_BYTES) + warp * kStages;
+  pdl_wait();
+  pdl_launch_dependents();
 
   int b, kbeg, kend, part, btlen;
   const int* bt;
@@ -323,6 +325,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 // Merges the split partial results of each decode: out = sum_i A_i 2^(m_i - M) / sum_i L_i 2^(m_i - M).
 template <typename T, int D, bool COMPUTED = false>
 __global__ void decode_combine_kernel(DecodeAttnArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int b = blockIdx.x;
   const int hq = blockIdx.y;
   int cnt, p0;
@@ -360,12 +364,12 @@ int launch_impl(const DecodeAttnArgs& a, const CUtensorMap& tmk, const CUtensorM
     attr = true;
   }
   const int n_ctas = COMPUTED ? a.n_decode * a.max_splits : a.n_items;
-  decode_attn_kernel<T, D, COMPUTED><<<dim3(n_ctas, a.kvh), kWarps * 32, smem, s>>>(tmk, tmv, a);
+  launch_pdl(decode_attn_kernel<T, D, COMPUTED>, dim3(n_ctas, a.kvh), dim3(kWarps * 32), smem, s, tmk, tmv, a);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "decode attention launch");
   if (a.partials) {
-    decode_combine_kernel<T, D, COMPUTED><<<dim3(a.n_decode, a.qh), D, 0, s>>>(a);
+    launch_pdl(decode_combine_kernel<T, D, COMPUTED>, dim3(a.n_decode, a.qh), dim3(D), 0, s, a);
     count_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "decode combine launch");

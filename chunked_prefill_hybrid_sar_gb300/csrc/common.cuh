@@ -140,6 +140,14 @@ __device__ __forceinline__ void tma_prefetch_l2(const void* tmap, int32_t c0, in
                : "memory");
 }
 
+// Programmatic dependent launch.  pdl_wait(): until the previous kernel of the
+// stream has completed and its writes are visible (returns at once for a
+// kernel launched normally); nothing global that a previous kernel writes or
+// reads may be touched before it.  pdl_launch_dependents(): the next kernel
+// may start launching once every CTA of this one has called it or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // TMA load whose data and complete_tx land at the same shared-memory offsets in
 // every CTA of the cluster named by `mask`.
 __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,

@@ -31,26 +31,76 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // stream, fp32 reduction, y in the storage type T.  The normalisation ahead of
 // attention and FFN, and the final norm ahead of the LM head ("insert an
 // explicit sync before LayerNorm", SARATHI technique write-up, section 6.1).
-template <typename T>
-__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* __restrict__ x,
-                                                              const float* __restrict__ g,
-                                                              T* __restrict__ y, int hidden, float eps,
-                                                              const int32_t* __restrict__ ridx) {
+//
+// SRC selects where row r comes from: kSrcResidual reads the fp32 stream;
+// kSrcRows (bf16 rows of the stacked batch) and kSrcTokens (embedding rows of
+// token ids, storage type) are the step's first norm, which also writes the
+// row into the fp32 stream `h`.  `zero` (optional): row r of it, zero_cols
+// floats, is cleared (the LM head's split-K accumulator).
+enum { kSrcResidual = 0, kSrcRows = 1, kSrcTokens = 2 };
+
+struct NormArgs {
+  const float* x;         // kSrcResidual
+  const void* in;         // kSrcRows: bf16 [rows, hidden]; kSrcTokens: int32 ids
+  const void* table;      // kSrcTokens: [vocab, hidden] storage type
+  float* h;               // kSrcRows / kSrcTokens: fp32 copy of the input row
+  const float* g;
+  void* y;
+  const int32_t* ridx;    // kSrcResidual: optional source row per output row
+  float* zero;
+  int zero_cols;
+  int hidden, vocab;
+  float eps;
+  int* err;
+};
+
+template <typename T, int SRC>
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float red[32];
   const int r = blockIdx.x;
-  const int src = ridx ? ridx[r] : r;
-  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)src * hidden);
-  const float4* gr = reinterpret_cast<const float4*>(g);
-  uint2* yr = reinterpret_cast<uint2*>(y + (size_t)r * hidden);
-  const int nv = hidden >> 2;
-  // the row stays in registers between the reduction and the scaling pass
+  const int nv = a.hidden >> 2;
   float4 v[kNormMaxVec];
+  bool ok = true;
+  if constexpr (SRC == kSrcResidual) {
+    const int src = a.ridx ? a.ridx[r] : r;
+    const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)src * a.hidden);
+#pragma unroll
+    for (int k = 0; k < kNormMaxVec; ++k) {
+      const int i = threadIdx.x + k * kNormThreads;
+      if (i < nv) v[k] = xr[i];
+    }
+  } else {
+    const uint2* sr;
+    if constexpr (SRC == kSrcRows) {
+      sr = reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.in) + (size_t)r * a.hidden);
+    } else {
+      const int t = static_cast<const int32_t*>(a.in)[r];
+      ok = t >= 0 && t < a.vocab;
+      if (!ok && threadIdx.x == 0) report(a.err, SAR_ERR_BOUNDS, SITE_EMBED_BOUNDS, t);
+      sr = reinterpret_cast<const uint2*>(static_cast<const T*>(a.table) + (size_t)(ok ? t : 0) * a.hidden);
+    }
+    float4* hr = reinterpret_cast<float4*>(a.h + (size_t)r * a.hidden);
+#pragma unroll
+    for (int k = 0; k < kNormMaxVec; ++k) {
+      const int i = threadIdx.x + k * kNormThreads;
+      if (i < nv) {
+        const uint2 u = sr[i];
+        if constexpr (SRC == kSrcRows)
+          v[k] = make_float4(bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y));
+        else
+          v[k] = make_float4(Elem<T>::lo(u.x), Elem<T>::hi(u.x), Elem<T>::lo(u.y), Elem<T>::hi(u.y));
+        if (!ok) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        hr[i] = v[k];
+      }
+    }
+  }
   float ss = 0.f;
 #pragma unroll
   for (int k = 0; k < kNormMaxVec; ++k) {
     const int i = threadIdx.x + k * kNormThreads;
     if (i < nv) {
-      v[k] = xr[i];
       ss = fmaf(v[k].x, v[k].x, ss);
       ss = fmaf(v[k].y, v[k].y, ss);
       ss = fmaf(v[k].z, v[k].z, ss);
@@ -58,7 +108,9 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* __re
     }
   }
   ss = block_sum(ss, red);
-  const float inv = rsqrtf(ss / (float)hidden + eps);
+  const float inv = rsqrtf(ss / (float)a.hidden + a.eps);
+  const float4* gr = reinterpret_cast<const float4*>(a.g);
+  uint2* yr = reinterpret_cast<uint2*>(static_cast<T*>(a.y) + (size_t)r * a.hidden);
 #pragma unroll
   for (int k = 0; k < kNormMaxVec; ++k) {
     const int i = threadIdx.x + k * kNormThreads;
@@ -68,12 +120,23 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* __re
                          Elem<T>::pack(v[k].z * inv * gv.z, v[k].w * inv * gv.w));
     }
   }
+  if (a.zero) {
+    float* zr = a.zero + (size_t)r * a.zero_cols;
+    if ((a.zero_cols & 3) == 0) {
+      float4* z4 = reinterpret_cast<float4*>(zr);
+      for (int i = threadIdx.x; i < (a.zero_cols >> 2); i += kNormThreads) z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      for (int i = threadIdx.x; i < a.zero_cols; i += kNormThreads) zr[i] = 0.f;
+    }
+  }
 }
 
 // Embedding rows of the storage type into the fp32 residual stream.
 template <typename T>
 __global__ void embed_kernel(const int32_t* __restrict__ tok, const T* __restrict__ table,
                              float* __restrict__ out, int hidden, int vocab, int* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int r = blockIdx.x;
   const int t = tok[r];
   float4* dst = reinterpret_cast<float4*>(out + (size_t)r * hidden);
@@ -93,6 +156,8 @@ __global__ void embed_kernel(const int32_t* __restrict__ tok, const T* __restric
 // bf16 -> fp32 (input rows into the residual stream, norm gains), 8 values
 // (16 bytes in, 32 out) per thread; n is a multiple of 8.
 __global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ src, float* __restrict__ dst, size_t n8) {
+  pdl_wait();
+  pdl_launch_dependents();
   const size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
   if (i >= n8) return;
   const uint4 v = reinterpret_cast<const uint4*>(src)[i];
@@ -107,6 +172,8 @@ __global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ src, float*
 template <typename T>
 __global__ void convert_rows_kernel(const __nv_bfloat16* __restrict__ src, T* __restrict__ dst, int rows,
                                     int cols, int interleave, int up) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int r = blockIdx.x;
   const int dr = interleave ? (r / 64) * 128 + up * 64 + (r % 64) : r;
   const uint32_t* s = reinterpret_cast<const uint32_t*>(src + (size_t)r * cols);
@@ -128,6 +195,8 @@ __global__ void convert_rows_kernel(const __nv_bfloat16* __restrict__ src, T* __
 // precision once per (row, frequency), so long positions keep fp32 accuracy.
 template <typename T>
 __global__ void rope_append_kernel(RopeArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float cs[64], sn[64];
   const int r = blockIdx.x;
   const int pos = a.pos[r];
@@ -195,6 +264,8 @@ __global__ void rope_append_kernel(RopeArgs a) {
 // Greedy sampling: lowest index among the maxima of each row.
 __global__ void __launch_bounds__(1024) argmax_kernel(const float* __restrict__ logits, int vocab,
                                                      int32_t* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float bv[32];
   __shared__ int bi[32];
   const float* row = logits + (size_t)blockIdx.x * vocab;
@@ -242,27 +313,64 @@ __global__ void __launch_bounds__(1024) argmax_kernel(const float* __restrict__ 
 }  // namespace
 
 int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hidden, float eps,
-                   const int32_t* row_index, int storage, cudaStream_t s) {
+                   const int32_t* row_index, int storage, cudaStream_t s, float* zero, int zero_cols) {
   if (rows <= 0) return SAR_OK;
   if (hidden % 4 || hidden > 4 * kNormThreads * kNormMaxVec)
     return set_error(SAR_ERR_UNSUPPORTED, "rmsnorm: hidden must be a multiple of 4 and at most 8192");
-  if (storage == SAR_STORAGE_BF16)
-    rmsnorm_kernel<__nv_bfloat16><<<rows, kNormThreads, 0, s>>>(x, gain, static_cast<__nv_bfloat16*>(y), hidden,
-                                                               eps, row_index);
-  else
-    rmsnorm_kernel<__half><<<rows, kNormThreads, 0, s>>>(x, gain, static_cast<__half*>(y), hidden, eps, row_index);
+  NormArgs a = {};
+  a.x = x;
+  a.g = gain;
+  a.y = y;
+  a.ridx = row_index;
+  a.zero = zero;
+  a.zero_cols = zero_cols;
+  a.hidden = hidden;
+  a.eps = eps;
+  cudaError_t e = storage == SAR_STORAGE_BF16
+                      ? launch_pdl(rmsnorm_kernel<__nv_bfloat16, kSrcResidual>, dim3(rows), dim3(kNormThreads), 0, s, a)
+                      : launch_pdl(rmsnorm_kernel<__half, kSrcResidual>, dim3(rows), dim3(kNormThreads), 0, s, a);
+  if (e != cudaSuccess) return cuda_error(e, "rmsnorm launch");
   count_launches(1);
-  return cuda_error(cudaGetLastError(), "rmsnorm launch");
+  return SAR_OK;
+}
+
+int launch_input_norm(int in_kind, const void* in, const void* table, int vocab, float* h, const float* gain,
+                      void* y, int rows, int hidden, float eps, int storage, int* err, cudaStream_t s) {
+  if (rows <= 0) return SAR_OK;
+  if (hidden % 4 || hidden > 4 * kNormThreads * kNormMaxVec)
+    return set_error(SAR_ERR_UNSUPPORTED, "rmsnorm: hidden must be a multiple of 4 and at most 8192");
+  NormArgs a = {};
+  a.in = in;
+  a.table = table;
+  a.h = h;
+  a.g = gain;
+  a.y = y;
+  a.hidden = hidden;
+  a.vocab = vocab;
+  a.eps = eps;
+  a.err = err;
+  const bool bf = storage == SAR_STORAGE_BF16;
+  const dim3 g(rows), b(kNormThreads);
+  cudaError_t e;
+  if (in_kind == SAR_IN_TOKENS)
+    e = bf ? launch_pdl(rmsnorm_kernel<__nv_bfloat16, kSrcTokens>, g, b, 0, s, a)
+           : launch_pdl(rmsnorm_kernel<__half, kSrcTokens>, g, b, 0, s, a);
+  else
+    e = bf ? launch_pdl(rmsnorm_kernel<__nv_bfloat16, kSrcRows>, g, b, 0, s, a)
+           : launch_pdl(rmsnorm_kernel<__half, kSrcRows>, g, b, 0, s, a);
+  if (e != cudaSuccess) return cuda_error(e, "input norm launch");
+  count_launches(1);
+  return SAR_OK;
 }
 
 int launch_embed(const int32_t* tokens, const void* table, float* out, int rows, int hidden, int vocab,
                  int storage, int* err, cudaStream_t s) {
   if (rows <= 0) return SAR_OK;
   if (storage == SAR_STORAGE_BF16)
-    embed_kernel<__nv_bfloat16><<<rows, 256, 0, s>>>(tokens, static_cast<const __nv_bfloat16*>(table), out, hidden,
+    launch_pdl(embed_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, tokens, static_cast<const __nv_bfloat16*>(table), out, hidden,
                                                      vocab, err);
   else
-    embed_kernel<__half><<<rows, 256, 0, s>>>(tokens, static_cast<const __half*>(table), out, hidden, vocab, err);
+    launch_pdl(embed_kernel<__half>, dim3(rows), dim3(256), 0, s, tokens, static_cast<const __half*>(table), out, hidden, vocab, err);
   count_launches(1);
   return cuda_error(cudaGetLastError(), "embed launch");
 }
@@ -271,7 +379,7 @@ int launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s) {
   if (n == 0) return SAR_OK;
   if (n % 8) return set_error(SAR_ERR_UNSUPPORTED, "bf16 to fp32: length must be a multiple of 8");
   const size_t n8 = n / 8;
-  bf16_to_f32_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), dst, n8);
+  launch_pdl(bf16_to_f32_kernel, dim3((unsigned)((n8 + 255) / 256)), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(src), dst, n8);
   count_launches(1);
   return cuda_error(cudaGetLastError(), "bf16 to fp32 launch");
 }
@@ -282,10 +390,10 @@ int launch_convert_rows(const void* src, void* dst, int rows, int cols, int inte
   if (cols % 2) return set_error(SAR_ERR_UNSUPPORTED, "convert: odd row width");
   const __nv_bfloat16* sp = static_cast<const __nv_bfloat16*>(src);
   if (storage == SAR_STORAGE_BF16)
-    convert_rows_kernel<__nv_bfloat16><<<rows, 256, 0, s>>>(sp, static_cast<__nv_bfloat16*>(dst), rows, cols,
+    launch_pdl(convert_rows_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, sp, static_cast<__nv_bfloat16*>(dst), rows, cols,
                                                            interleave, up);
   else
-    convert_rows_kernel<__half><<<rows, 256, 0, s>>>(sp, static_cast<__half*>(dst), rows, cols, interleave, up);
+    launch_pdl(convert_rows_kernel<__half>, dim3(rows), dim3(256), 0, s, sp, static_cast<__half*>(dst), rows, cols, interleave, up);
   count_launches(1);
   return cuda_error(cudaGetLastError(), "convert launch");
 }
@@ -294,16 +402,16 @@ int launch_rope_append(const RopeArgs& a, cudaStream_t s) {
   if (a.M <= 0) return SAR_OK;
   if (a.d > 128 || a.d % 2) return set_error(SAR_ERR_UNSUPPORTED, "rope: head_dim > 128");
   if (a.storage == SAR_STORAGE_BF16)
-    rope_append_kernel<__nv_bfloat16><<<a.M, 256, 0, s>>>(a);
+    launch_pdl(rope_append_kernel<__nv_bfloat16>, dim3(a.M), dim3(256), 0, s, a);
   else
-    rope_append_kernel<__half><<<a.M, 256, 0, s>>>(a);
+    launch_pdl(rope_append_kernel<__half>, dim3(a.M), dim3(256), 0, s, a);
   count_launches(1);
   return cuda_error(cudaGetLastError(), "rope launch");
 }
 
 int launch_argmax(const float* logits, int rows, int vocab, int32_t* out, cudaStream_t s) {
   if (rows <= 0) return SAR_OK;
-  argmax_kernel<<<rows, 1024, 0, s>>>(logits, vocab, out);
+  launch_pdl(argmax_kernel, dim3(rows), dim3(1024), 0, s, logits, vocab, out);
   count_launches(1);
   return cuda_error(cudaGetLastError(), "argmax launch");
 }

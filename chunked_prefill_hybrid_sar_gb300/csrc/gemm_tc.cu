@@ -50,17 +50,50 @@ constexpr int kPrefetch = 16;             // K-slabs of the weight tile prefetch
 
 // ---- tcgen05 wrappers ------------------------------------------------------
 
+// PAIR: the CTA pair of a 2-CTA cluster allocates the same columns in both
+// SMs' tensor memory (one warp of each CTA executes these).
+template <bool PAIR>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-               "r"(ncols)
-               : "memory");
+  if constexpr (PAIR)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
 }
+template <bool PAIR>
 __device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if constexpr (PAIR)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
+template <bool PAIR>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
+  if constexpr (PAIR)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+// TMA load into this CTA's shared memory whose completion is signalled on an
+// mbarrier of either CTA of the pair (`bar` a cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -69,13 +102,35 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
+// PAIR: one thread of the leader CTA issues an M = 256 MMA over the pair:
+// A rows 0..127 and B rows 0..N/2-1 from the leader's shared memory, the rest
+// from the peer's (same offsets); D rows 0..127 land in the leader's tensor
+// memory, 128..255 in the peer's.
+template <bool PAIR>
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  if constexpr (PAIR)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Completion of the pair's MMAs so far, signalled on the same barrier offset
+// in both CTAs (mask 0b11).
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
       : "memory");
 }
 
@@ -124,9 +179,9 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 
 // Instruction descriptor, kind::f16: fp32 accumulator, A and B of format
 // `fmt` (0 = f16, 1 = bf16; both operands always the same type), both
-// K-major, M = 128, N = n.
-__device__ __forceinline__ uint32_t idesc_f16kind(int n, uint32_t fmt) {
-  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+// K-major, M = m (128, or 256 over a CTA pair), N = n.
+__device__ __forceinline__ uint32_t idesc_f16kind(int m, int n, uint32_t fmt) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
@@ -176,7 +231,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* er
   return ok != 0;
 }
 
-template <typename T, int EPI, bool SWAP, int MSUB>
+template <typename T, int EPI, bool SWAP, int MSUB, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const Params p) {
@@ -197,23 +252,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
-      mbar_init(smem_u32(&empty_bar[s]), (uint32_t)p.cl);  // released by every CTA of the cluster
+      // multicast: released by every CTA of the cluster; pair: by the leader's MMAs
+      mbar_init(smem_u32(&empty_bar[s]), PAIR ? 1u : (uint32_t)p.cl);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&accf_bar[s]), 1);
-      mbar_init(smem_u32(&acce_bar[s]), 128);
+      // pair: one arrival per epilogue warp of both CTAs (only the leader's is waited on)
+      mbar_init(smem_u32(&acce_bar[s]), PAIR ? 8u : 128u);
     }
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
-    tmem_relinquish();
+    tmem_alloc<PAIR>(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
+    tmem_relinquish<PAIR>();
   }
   tc_fence_before();
   __syncthreads();
   if (p.cl > 1) cluster_sync();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_launch_dependents();
 
   const int rank = p.cl > 1 ? (int)cluster_ctarank() : 0;
   const int cid = blockIdx.x / p.cl, n_clusters = gridDim.x / p.cl;
@@ -237,17 +296,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the weight tile streams from HBM: pull it into L2 kPrefetch K-slabs ahead
         // of the shared-memory ring so the ring's loads hit L2
         const void* w_map = SWAP ? (const void*)&tm_a : (const void*)&tm_b;
-        const int slice = p.bn / p.cl;  // weight rows this CTA fetches (and multicasts)
+        // weight rows this CTA fetches: its multicast slice, or its half of the pair's tile
+        const int slice = PAIR ? p.bn / 2 : p.bn / p.cl;
         const int w_row = SWAP ? a_row : b_row + rank * slice;
-        for (int kb = un.kb0; kb < un.kb0 + kPrefetch && kb < un.kb1; ++kb) tma_prefetch_l2(w_map, kb * kBK, w_row);
+        // (swap tiling: one CTA per weight tile, no reuse to gain from L2)
+        if (!SWAP)
+          for (int kb = un.kb0; kb < un.kb0 + kPrefetch && kb < un.kb1; ++kb) tma_prefetch_l2(w_map, kb * kBK, w_row);
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
-          if (kb + kPrefetch < un.kb1) tma_prefetch_l2(w_map, (kb + kPrefetch) * kBK, w_row);
+          if (!SWAP && kb + kPrefetch < un.kb1) tma_prefetch_l2(w_map, (kb + kPrefetch) * kBK, w_row);
           if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.err, SITE_GEMM_PRODUCER)) {
             ok = false;
             break;
           }
           uint8_t* st = smem + stage * p.stage_bytes;
           const uint32_t fb = smem_u32(&full_bar[stage]);
+          if constexpr (PAIR) {
+            // both CTAs' loads count on the leader's barrier, which the leader's MMA waits on
+            const uint32_t fb_lead = cluster_addr(fb, 0);
+            if (rank == 0) mbar_expect_tx(fb, 2u * (uint32_t)p.stage_bytes);
+            tma_load_2d_pair(smem_u32(st), &tm_a, kb * kBK, a_row, fb_lead);
+            tma_load_2d_pair(smem_u32(st + kTileA), &tm_b, kb * kBK, b_row + rank * slice, fb_lead);
+            next_stage(stage, phase, stages);
+            continue;
+          }
           mbar_expect_tx(fb, (uint32_t)p.stage_bytes);
 #pragma unroll
           for (int s = 0; s < MSUB; ++s)
@@ -271,8 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16kind(p.bn, Elem<T>::kMmaFormat);
+    // pair: the leader issues the MMAs of both CTAs
+    if (lane == 0 && (!PAIR || rank == 0)) {
+      const uint32_t idesc = idesc_f16kind(PAIR ? 256 : 128, p.bn, Elem<T>::kMmaFormat);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -298,16 +370,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int s = 0; s < MSUB; ++s) {
               const uint64_t adesc = sw128_desc(a_base + s * kTileA + kk * 32);
-              mma_bf16(d_tmem + (uint32_t)(s * p.bn), adesc, bdesc, idesc, (kb != un.kb0) || (kk != 0));
+              mma_f16<PAIR>(d_tmem + (uint32_t)(s * p.bn), adesc, bdesc, idesc, (kb != un.kb0) || (kk != 0));
             }
           }
-          if (p.cl > 1)
+          if (PAIR)
+            mma_commit_pair(smem_u32(&empty_bar[stage]));
+          else if (p.cl > 1)
             mma_commit_mc(smem_u32(&empty_bar[stage]), cl_mask);
           else
             mma_commit(smem_u32(&empty_bar[stage]));
           next_stage(stage, phase, stages);
         }
-        if (ok) mma_commit(smem_u32(&accf_bar[acc]));
+        if (ok) {
+          if (PAIR)
+            mma_commit_pair(smem_u32(&accf_bar[acc]));
+          else
+            mma_commit(smem_u32(&accf_bar[acc]));
+        }
       }
     }
     __syncwarp();
@@ -465,7 +544,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      if (alive) mbar_arrive(smem_u32(&acce_bar[acc]));
+      if constexpr (PAIR) {
+        __syncwarp();
+        if (alive && lane == 0) mbar_arrive_cluster(cluster_addr(smem_u32(&acce_bar[acc]), 0));
+      } else {
+        if (alive) mbar_arrive(smem_u32(&acce_bar[acc]));
+      }
     }
   }
 
@@ -474,21 +558,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (p.cl > 1) cluster_sync();  // no CTA leaves while a peer may still address it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+    tmem_dealloc<PAIR>(tmem_base, (uint32_t)p.tmem_cols);
   }
 }
 
-template <typename T, int EPI, bool SWAP, int MSUB>
+template <typename T, int EPI, bool SWAP, int MSUB, bool PAIR>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&gemm_tc_kernel<T, EPI, SWAP, MSUB>);
+  return reinterpret_cast<const void*>(&gemm_tc_kernel<T, EPI, SWAP, MSUB, PAIR>);
 }
 
 template <typename T>
-const void* pick_kernel_t(int epi, bool swap, int msub) {
-#define SAR_PICK(E)                                                                 \
-  if (epi == E) {                                                                   \
-    if (swap) return kernel_ptr<T, E, true, 1>();                                   \
-    return msub == 2 ? kernel_ptr<T, E, false, 2>() : kernel_ptr<T, E, false, 1>(); \
+const void* pick_kernel_t(int epi, bool swap, int msub, bool pair) {
+#define SAR_PICK(E)                                                                               \
+  if (epi == E) {                                                                                 \
+    if (swap) return kernel_ptr<T, E, true, 1, false>();                                          \
+    if (pair) return kernel_ptr<T, E, false, 1, true>();                                          \
+    return msub == 2 ? kernel_ptr<T, E, false, 2, false>() : kernel_ptr<T, E, false, 1, false>(); \
   }
   SAR_PICK(SAR_EPI_STORE)
   SAR_PICK(SAR_EPI_RESIDUAL)
@@ -498,9 +583,9 @@ const void* pick_kernel_t(int epi, bool swap, int msub) {
   return nullptr;
 }
 
-const void* pick_kernel(int storage, int epi, bool swap, int msub) {
-  return storage == SAR_STORAGE_BF16 ? pick_kernel_t<__nv_bfloat16>(epi, swap, msub)
-                                     : pick_kernel_t<__half>(epi, swap, msub);
+const void* pick_kernel(int storage, int epi, bool swap, int msub, bool pair) {
+  return storage == SAR_STORAGE_BF16 ? pick_kernel_t<__nv_bfloat16>(epi, swap, msub, pair)
+                                     : pick_kernel_t<__half>(epi, swap, msub, pair);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -560,8 +645,9 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
   // SM clocks per 64-wide K slab of one tile: the larger of the MMA time
   // (128 x bn x 64 takes 2*bn clocks per 128-row sub-tile) and the time to
   // stream its operands into shared memory (about 64 bytes per clock per SM)
-  auto kslab_clocks = [](int msub, int bn) -> long {
-    return std::max<long>(2L * msub * bn, (msub * 16384L + bn * 128L) / 64);
+  // (a pair tile: each SM computes its 128 rows x bn and loads half the weight rows)
+  auto kslab_clocks = [](int msub, int bn, bool pair = false) -> long {
+    return std::max<long>(2L * msub * bn, (msub * 16384L + (pair ? bn / 2 : bn) * 128L) / 64);
   };
   auto best_split = [&](long tiles, long per_kb_work, int* splits) {
     long best = -1;
@@ -599,6 +685,8 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
     case SAR_GEMM_M128_N128: c.swap = 0; c.msub = 1; c.bn = 128; break;
     case SAR_GEMM_M128_N256: c.swap = 0; c.msub = 1; c.bn = 256; break;
     case SAR_GEMM_M256_N128: c.swap = 0; c.msub = 2; c.bn = 128; break;
+    case SAR_GEMM_PAIR_N256: c.swap = 0; c.msub = 1; c.bn = 256; c.pair = 1; break;
+    case SAR_GEMM_PAIR_N128: c.swap = 0; c.msub = 1; c.bn = 128; c.pair = 1; break;
     case SAR_GEMM_SWAP:
       if (M > 256) return set_error(SAR_ERR_UNSUPPORTED, "gemm: swap tiling needs M <= 256");
       c.swap = 1; c.msub = 1; c.bn = (M + 15) / 16 * 16; break;
@@ -617,7 +705,12 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
     c.m_tiles = (M + 128 * c.msub - 1) / (128 * c.msub);
     c.n_tiles = (N + c.bn - 1) / c.bn;
     // token tiles of one weight tile run as a cluster that multicasts the tile
-    if (cl_flag == SAR_GEMM_CLUSTER_1) c.cl = 1;
+    if (c.pair) {
+      if (cl_flag && cl_flag != SAR_GEMM_CLUSTER_2)
+        return set_error(SAR_ERR_UNSUPPORTED, "gemm: a pair tiling is a cluster of 2");
+      c.cl = 2;
+      c.m_tiles += c.m_tiles & 1;  // an odd last tile pairs with an all-padding one
+    } else if (cl_flag == SAR_GEMM_CLUSTER_1) c.cl = 1;
     else if (cl_flag == SAR_GEMM_CLUSTER_2) c.cl = 2;
     else if (cl_flag == SAR_GEMM_CLUSTER_4) c.cl = 4;
     else {
@@ -629,16 +722,18 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
     }
     if (c.m_tiles % c.cl) return set_error(SAR_ERR_UNSUPPORTED, "gemm: cluster size does not divide the token tiles");
     c.a_box_rows = 128;          // tokens
-    c.b_box_rows = c.bn / c.cl;  // this CTA's slice of the weight tile
+    c.b_box_rows = c.bn / c.cl;  // this CTA's slice (or half) of the weight tile
   }
   c.m_groups = c.m_tiles / c.cl;
-  const int stage_bytes = c.msub * kTileA + c.bn * kBK * 2;
+  const int stage_bytes = c.msub * kTileA + (c.pair ? c.bn / 2 : c.bn) * kBK * 2;
+  c.stage_bytes = stage_bytes;
   const int extra = kBarBytes + 1024 + ((c.swap && epi == SAR_EPI_SWIGLU) ? kSwapXchg : 0);
   c.stages = std::min(8, (kSmemLimit - extra) / stage_bytes);
   if (c.stages < 2) return set_error(SAR_ERR_UNSUPPORTED, "gemm: tile does not fit shared memory");
   c.smem = c.stages * stage_bytes + extra;
   c.splits = 1;
-  best_split((long)c.m_tiles * c.n_tiles, c.swap ? kslab_clocks(1, c.bn) : kslab_clocks(c.msub, c.bn), &c.splits);
+  best_split((long)c.m_tiles * c.n_tiles, c.swap ? kslab_clocks(1, c.bn) : kslab_clocks(c.msub, c.bn, c.pair),
+             &c.splits);
   c.kb_per_split = (k_blocks + c.splits - 1) / c.splits;
   c.splits = (k_blocks + c.kb_per_split - 1) / c.kb_per_split;  // no empty K range
   c.grid = std::min(c.m_tiles * c.n_tiles * c.splits, sms) / c.cl * c.cl;  // whole clusters; refined at launch
@@ -648,7 +743,7 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
 
 int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMap& w_map, int M, int N,
                 int K, int epi, int storage, void* c, const void* residual, int* err, cudaStream_t s) {
-  const void* fn = pick_kernel(storage, epi, cfg.swap != 0, cfg.msub);
+  const void* fn = pick_kernel(storage, epi, cfg.swap != 0, cfg.msub, cfg.pair != 0);
   if (!fn) return set_error(SAR_ERR_INVALID_ARG, "gemm: unknown epilogue");
   if (epi == SAR_EPI_RESIDUAL && residual == nullptr)
     return set_error(SAR_ERR_INVALID_ARG, "gemm: residual epilogue without residual");
@@ -665,7 +760,7 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   if (cfg.splits > 1 && c != residual)
     return set_error(SAR_ERR_INVALID_ARG, "gemm: split-K needs the residual output in place");
   p.stages = cfg.stages;
-  p.stage_bytes = cfg.msub * kTileA + cfg.bn * kBK * 2;
+  p.stage_bytes = cfg.stage_bytes;
   p.tmem_cols = pow2_at_least(2 * cfg.msub * cfg.bn);
   p.cl = cfg.cl;
   p.m_groups = cfg.m_groups;
@@ -673,10 +768,11 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   p.r = residual;
   p.err = err;
   if (cfg.cl < 1 || cfg.m_tiles % cfg.cl || cfg.m_groups * cfg.cl != cfg.m_tiles || cfg.bn % (8 * cfg.cl) ||
-      (cfg.swap && cfg.cl != 1))
+      (cfg.swap && cfg.cl != 1) || (cfg.pair && (cfg.cl != 2 || cfg.msub != 1 || cfg.swap)) ||
+      cfg.stage_bytes != cfg.msub * kTileA + (cfg.pair ? cfg.bn / 2 : cfg.bn) * kBK * 2)
     return set_error(SAR_ERR_INVALID_ARG, "gemm: inconsistent cluster configuration");
-  static bool attr_done[2][4][2][3] = {};
-  bool& done = attr_done[storage == SAR_STORAGE_BF16][epi][cfg.swap][cfg.msub];
+  static bool attr_done[2][4][2][3][2] = {};
+  bool& done = attr_done[storage == SAR_STORAGE_BF16][epi][cfg.swap][cfg.msub][cfg.pair];
   if (!done) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return cuda_error(e, "gemm: set smem attribute");
@@ -686,25 +782,31 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   const CUtensorMap& tb = cfg.swap ? act_map : w_map;
   void* args[] = {const_cast<CUtensorMap*>(&ta), const_cast<CUtensorMap*>(&tb), &p};
   cudaLaunchConfig_t lc = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   lc.blockDim = dim3(kThreads);
   lc.dynamicSmemBytes = (size_t)cfg.smem;
   lc.stream = s;
+  lc.attrs = attr;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  lc.numAttrs = 1;
   int grid = cfg.grid;
   if (cfg.cl > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cfg.cl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cfg.cl;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    lc.numAttrs = 2;
     // persistent grid: as many whole clusters as can be resident at once (the
     // SMs of a GPC need not divide into clusters evenly)
-    static int max_clusters[2][4][3][5][2] = {};
-    int& mc = max_clusters[storage == SAR_STORAGE_BF16][epi][cfg.msub][cfg.cl][cfg.bn == 256];
+    static int max_clusters[2][4][3][5][2][2] = {};
+    int& mc = max_clusters[storage == SAR_STORAGE_BF16][epi][cfg.msub][cfg.cl][cfg.bn == 256][cfg.pair];
     if (mc == 0) {
-      lc.gridDim = dim3(cfg.cl * 64);
-      cudaError_t e = cudaOccupancyMaxActiveClusters(&mc, fn, &lc);
+      cudaLaunchConfig_t qc = lc;  // the cluster shape alone
+      qc.gridDim = dim3(cfg.cl * 64);
+      qc.attrs = &attr[1];
+      qc.numAttrs = 1;
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&mc, fn, &qc);
       if (e != cudaSuccess || mc < 1) return cuda_error(e != cudaSuccess ? e : cudaErrorInvalidConfiguration,
                                                          "gemm: cluster occupancy");
     }

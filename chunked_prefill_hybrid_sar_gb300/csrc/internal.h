@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 
 #include "../../include/sar.h"
 #include "../../include/sar_ops.h"
@@ -18,6 +19,29 @@ int set_error(int code, const std::string& msg);
 int cuda_error(cudaError_t e, const char* what);
 void count_launches(int64_t n);
 int num_sms();
+
+// Kernels of a step are launched with programmatic stream serialisation: the
+// next kernel's CTAs may become resident while the previous kernel drains and
+// run their set-up (barriers, tensor memory, descriptor prefetch), then wait
+// in pdl_wait() until the previous kernel has completed.  SAR_PDL=0 in the
+// environment launches them normally.
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- GEMM (gemm_tc.cu) -----------------------------------------------------
 
@@ -40,6 +64,8 @@ struct GemmCfg {
   int b_box_rows = 256;
   int splits = 1;        // K ranges per tile (in-place fp32 residual epilogue only)
   int kb_per_split = 0;  // 64-wide K slabs per range
+  int pair = 0;          // 2-CTA tiles: M = 256 MMAs over a CTA pair (cl = 2)
+  int stage_bytes = 0;   // shared memory of one pipeline stage (per CTA)
   int cl = 1;            // CTAs per cluster sharing a weight tile by multicast (non-swap)
   int m_groups = 0;      // token-tile groups of cl tiles
 };
@@ -68,7 +94,13 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
 // ---- elementwise kernels (elementwise.cu) ----------------------------------
 // x: fp32 residual rows; y: storage-type rows; row_index (optional) gathers rows.
 int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hidden, float eps,
-                   const int32_t* row_index, int storage, cudaStream_t s);
+                   const int32_t* row_index, int storage, cudaStream_t s, float* zero = nullptr,
+                   int zero_cols = 0);
+// The step's first kernel: stacked input rows (bf16 hidden rows, or token ids
+// looked up in `table`) into the fp32 residual stream h and, normalised with
+// `gain`, into y (storage type).
+int launch_input_norm(int in_kind, const void* in, const void* table, int vocab, float* h, const float* gain,
+                      void* y, int rows, int hidden, float eps, int storage, int* err, cudaStream_t s);
 int launch_embed(const int32_t* tokens, const void* table, float* out, int rows, int hidden, int vocab,
                  int storage, int* err, cudaStream_t s);
 int launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s);

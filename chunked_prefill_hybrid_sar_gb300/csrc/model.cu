@@ -325,18 +325,15 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
   const int32_t* md = m->meta_dev;
   const int M = p.M, H = d.hidden;
 
-  // a0: stacked rows (chunk first, then decodes)
-  {
-    Prof pr(m, SAR_K_EMBED, s);
-    if (b->in_kind == SAR_IN_TOKENS) {
-      SAR_TRY(sar::launch_embed(static_cast<const int32_t*>(in), m->embed, h, M, H, d.vocab, d.storage, m->err, s));
-    } else {
-      SAR_TRY(sar::launch_bf16_to_f32(in, h, (size_t)M * H, s));  // bf16 rows into the fp32 residual
-    }
-  }
   for (int l = 0; l < d.n_layers; ++l) {
     LayerW& w = m->L[l];
-    {
+    if (l == 0) {
+      // a0 + a1: stacked rows (chunk first, then decodes) into the fp32
+      // residual stream, normalised for layer 0 in the same pass
+      Prof pr(m, SAR_K_EMBED, s);
+      SAR_TRY(sar::launch_input_norm(b->in_kind, in, m->embed, d.vocab, h, w.n1, m->xn, M, H, d.rms_eps, d.storage,
+                                     m->err, s));
+    } else {
       Prof pr(m, SAR_K_RMSNORM, s);
       SAR_TRY(sar::launch_rmsnorm(h, w.n1, m->xn, M, H, d.rms_eps, nullptr, d.storage, s));
     }
@@ -443,11 +440,13 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
   if (logits) {
     {
       Prof pr(m, SAR_K_HEAD_NORM, s);
-      SAR_TRY(sar::launch_rmsnorm(h, m->final_norm, m->hrows, p.R, H, d.rms_eps, md + p.o_rows, d.storage, s));
+      // also clears the logits rows: the head GEMM adds its K ranges into them
+      SAR_TRY(sar::launch_rmsnorm(h, m->final_norm, m->hrows, p.R, H, d.rms_eps, md + p.o_rows, d.storage, s,
+                                  logits, d.vocab));
     }
     {
       Prof pr(m, SAR_K_GEMM_HEAD, s);
-      SAR_TRY(run_gemm(m, m->hrows, p.R, m->m_head, d.vocab, H, SAR_EPI_F32, logits, nullptr, s));
+      SAR_TRY(run_gemm(m, m->hrows, p.R, m->m_head, d.vocab, H, SAR_EPI_RESIDUAL, logits, logits, s));
     }
   }
   return SAR_OK;

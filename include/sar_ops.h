@@ -40,6 +40,11 @@ enum {
                              side padded to 16 (M <= 256): no 128-row quantisation */
   SAR_GEMM_M256_N128 = 4, /* 256 token rows (two 128-row MMAs sharing one weight
                              tile) x 128 weight rows per tile                        */
+  SAR_GEMM_PAIR_N256 = 5, /* 256 token rows x 256 weight rows per tile over a pair of
+                             CTAs (2-CTA cluster): one M = 256 MMA reads each CTA's
+                             128 token rows and half of the weight rows, so each SM
+                             loads half the weight tile                             */
+  SAR_GEMM_PAIR_N128 = 6, /* the same with 128 weight rows per tile                 */
   /* Optional flags OR-ed into a non-swap tiling (or AUTO): how many CTAs of a
    * thread-block cluster share one weight tile.  Each fetches 1/c of the tile's
    * rows from L2 and multicasts it to all, so the weights leave L2 once per

@@ -211,3 +211,41 @@ def mistral_layer_case(seed: int = 0, n_decode: int = 64, tau: int = 512, starts
     hist = [kv_history(gen, 1, c, d, torch.bfloat16, device)[0] for c in ctxs] if with_history else None
     return dict(dims=d, layers=layers, head=head, lp=lp, tau=tau, starts=tuple(starts),
                 prompts=prompts, ctxs=ctxs, decode_inputs=decode_inputs, histories=hist)
+
+
+SWEEP_ROWS = (128, 255, 256, 257, 384, 511, 512, 1024, 2048)
+
+
+def tile_sweep_case(seed: int = 0, rows=SWEEP_ROWS, n_decode: int = 32, ctx: int = 2048,
+                    device: str = "cpu"):
+    """One Mistral-shaped layer (no head) stepped at several batch sizes
+    ``M = Lp + n_decode``: a prompt of ``max(rows) - n_decode`` N(0,1) rows
+    whose first ``Lp`` rows form the chunk (start 0) of each step, plus
+    ``n_decode`` decodes at context ``ctx`` with random N(0,1) K/V histories
+    and one N(0,1) input row each.  Draw order after the weights: the prompt,
+    the decode inputs, then the histories."""
+    d = dataclasses.replace(MISTRAL_LAYER, vocab=0)
+    layers, _, gen = model_weights(seed, d, torch.bfloat16, device)
+    prompt = normal(gen, (max(rows) - n_decode, d.hidden), 1.0, torch.bfloat16, device)
+    decode_inputs = normal(gen, (n_decode, d.hidden), 1.0, torch.bfloat16, device)
+    hist = [kv_history(gen, 1, ctx, d, torch.bfloat16, device)[0] for _ in range(n_decode)]
+    return dict(dims=d, layers=layers, rows=tuple(rows), prompt=prompt, ctx=ctx,
+                decode_inputs=decode_inputs, histories=hist)
+
+
+def long_prompt_case(seed: int, d: Dims, prompt_len: int = 16384, n_decode: int = 128,
+                     ctx_range=(512, 8192)):
+    """Token ids of one long prompt (uniform in ``[0, vocab)``) and the context
+    lengths of the decodes piggybacked on each of its chunks (uniform in
+    ``ctx_range``), drawn in that order from a CPU generator seeded ``seed``."""
+    gen = generator(seed)
+    prompt = torch.randint(0, d.vocab, (prompt_len,), generator=gen, dtype=torch.int64).to(torch.int32)
+    ctxs = uniform_int(gen, n_decode, ctx_range[0], ctx_range[1])
+    return prompt, ctxs
+
+
+def decode_history(seed: int, n_layers: int, ctx: int, d: Dims):
+    """Random N(0,1) K/V history of one decode, from its own CPU generator
+    seeded ``seed``, so that either side can draw it again when it needs it
+    instead of holding every decode's history at once."""
+    return kv_history(generator(seed), n_layers, ctx, d, torch.bfloat16)

@@ -39,6 +39,8 @@ VARIANTS = {
     "m128n256": sar.SAR_GEMM_M128_N256,
     "m256n128": sar.SAR_GEMM_M256_N128,
     "swap": sar.SAR_GEMM_SWAP,
+    "pair256": sar.SAR_GEMM_PAIR_N256,
+    "pair128": sar.SAR_GEMM_PAIR_N128,
 }
 
 SHAPES = [(1, 256, 256), (16, 512, 256), (65, 768, 512), (128, 256, 1024), (200, 1024, 256),
@@ -60,7 +62,7 @@ def test_gemm_store(M, N, K, variant, dt):
 
 
 @pytest.mark.parametrize("M", [3, 130, 384])
-@pytest.mark.parametrize("variant", ["auto", "m128n256", "swap", "m256n128"])
+@pytest.mark.parametrize("variant", ["auto", "m128n256", "swap", "m256n128", "pair256", "pair128"])
 @pytest.mark.parametrize("dt", list(DTYPES))
 def test_gemm_residual_in_place(M, variant, dt):
     """fp32 residual stream: h = h + a . w^T in place, no rounding to 16 bits."""
@@ -82,7 +84,7 @@ def pack_gate_up(wg, wu):
 
 
 @pytest.mark.parametrize("M", [5, 64, 200, 256, 384])
-@pytest.mark.parametrize("variant", ["auto", "m128n128", "m128n256", "swap", "m256n128"])
+@pytest.mark.parametrize("variant", ["auto", "m128n128", "m128n256", "swap", "m256n128", "pair256", "pair128"])
 @pytest.mark.parametrize("dt", list(DTYPES))
 def test_gemm_swiglu(M, variant, dt):
     if variant == "swap" and M > 256:
@@ -220,3 +222,22 @@ def test_gemm_cluster_rejects_sizes_that_do_not_divide():
         sar.gemm(a, w, c, variant=sar.SAR_GEMM_M128_N128 | sar.SAR_GEMM_CLUSTER_2)
     with pytest.raises(sar.SarError):
         sar.gemm(a[:200], w, c[:200], variant=sar.SAR_GEMM_SWAP | sar.SAR_GEMM_CLUSTER_2)
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 28672, 4096), (512, 4096, 14336), (1000, 6144, 4096)])
+def test_gemm_pair_large(M, N, K):
+    """CTA-pair tiles at projection shapes: store and split-K residual in place."""
+    a, w, r = operands(M, N, K, 9)
+    a, w = a.to(DEV), w.to(DEV)
+    c = torch.empty(M, N, dtype=torch.float32, device=DEV)
+    sar.gemm(a, w, c, epilogue=sar.SAR_EPI_F32, variant=sar.SAR_GEMM_PAIR_N256)
+    h = r.to(DEV).clone()
+    sar.gemm(a, w, h, residual=h, epilogue=sar.SAR_EPI_RESIDUAL, variant=sar.SAR_GEMM_PAIR_N256)
+    torch.cuda.synchronize()
+    # products of 16-bit operands are exact; what remains is fp32 accumulation
+    # over K terms in the tensor core's order, which grows like sqrt(K)
+    tol = max(1e-5, 3e-7 * K ** 0.5)
+    ref = a.double().cpu() @ w.double().cpu().T
+    assert ((c.double().cpu() - ref).abs().max() / ref.abs().max()).item() < tol
+    ref = ref + r.double()
+    assert ((h.double().cpu() - ref).abs().max() / ref.abs().max()).item() < tol

@@ -1,0 +1,72 @@
+"""The Mistral-shaped layer stepped at batch sizes on both sides of the GEMM
+tile edges (M = Lp + 32 in {128, 255, 256, 257, 384, 511, 512, 1024, 2048}):
+32 decodes at context 2048 with random histories plus one chunk at start 0.
+Every row of every step is compared with the oracle (same bars as the step
+tests).
+
+The oracle runs once, over the longest chunk and the decodes: attention is
+causal, so the first Lp rows of a one-shot forward over the longest prompt are
+the rows a chunk of Lp rows at start 0 emits, and a decode row depends only on
+its own history and input.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import chunked_prefill_hybrid_sar_gb300 as sar
+import synth
+from chunked_prefill_hybrid_sar_gb300 import harness
+from oracle import model as om
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, REL_L2 = 3e-2, 1e-2
+PS = 16
+
+
+def assert_close(got, ref, what):
+    err = np.abs(got - ref).max()
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert err <= MAX_ABS and rel <= REL_L2, f"{what}: max-abs {err:.3e}, rel-L2 {rel:.3e}"
+
+
+@pytest.fixture(scope="module")
+def sweep():
+    case = synth.tile_sweep_case(0)
+    dims, bd, ctx = case["dims"], len(case["histories"]), case["ctx"]
+    m = harness.load_model(dims, case["layers"], None, max_tokens=max(case["rows"]), max_decodes=bd)
+    n_pages = bd * (ctx // PS + 1) + max(case["rows"]) // PS + 8
+    kv = sar.KVCache(m, PS, n_pages)
+    alloc = harness.PageAllocator(synth.page_permutation(synth.generator(5), n_pages))
+    dec_bt = []
+    for k, v in case["histories"]:
+        bt = alloc.take(ctx // PS + 1)
+        harness.write_history(kv, dims, 0, k, v, bt)
+        dec_bt.append(bt)
+    prompt_bt = alloc.take(max(case["rows"]) // PS)
+    torch.cuda.synchronize()
+    w = om.layer_weights_np(case["layers"][0])
+    chunk_ref, _ = om.forward([w], dims, om.to_np(case["prompt"]))
+    parts = [om.Part(x=om.to_np(case["decode_inputs"][i:i + 1]), lo=ctx,
+                     given=[om.LayerCache(om.to_np(k), om.to_np(v))])
+             for i, (k, v) in enumerate(case["histories"])]
+    dec_ref, _ = om.hybrid_step([w], None, dims, parts)
+    return case, m, kv, dec_bt, prompt_bt, chunk_ref[0], dec_ref[0]
+
+
+@pytest.mark.parametrize("M", synth.SWEEP_ROWS)
+def test_rows_at_tile_edges_match_oracle(sweep, M):
+    case, m, kv, dec_bt, prompt_bt, chunk_ref, dec_ref = sweep
+    dims, ctx = case["dims"], case["ctx"]
+    bd = len(dec_bt)
+    lp = M - bd
+    decs = [(100 + i, ctx, dec_bt[i]) for i in range(bd)]
+    x = torch.cat([case["prompt"][:lp], case["decode_inputs"]]).cuda()
+    hid = torch.empty(M, dims.hidden, dtype=torch.float32, device="cuda")
+    m.step(kv, sar.Batch((0, 0, lp, prompt_bt), decs), x, hidden_out=hid)
+    m.sync_status()
+    torch.cuda.synchronize()
+    got = hid.cpu().numpy().astype(np.float64)
+    assert_close(got[:lp], chunk_ref[:lp], f"M={M} chunk rows")
+    assert_close(got[lp:], dec_ref, f"M={M} decode rows")
