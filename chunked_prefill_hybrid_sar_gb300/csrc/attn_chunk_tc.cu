@@ -1,0 +1,381 @@
+// Prefill-chunk attention on the 5th-generation tensor cores (head_dim 128,
+// pages of a multiple of 16 keys).  The chunk's queries attend causally to the keys of the
+// prompt's earlier chunks in the paged KV cache and to their own keys, which
+// the rotary/append kernel has already written into the pages ("Prefill uses
+// FlashAttention-2", SARATHI technique write-up section 3.3; cross-chunk
+// attention, same page section 3.1; chunk k re-reads the KV of the k earlier
+// chunks, Sarathi-Serve digest section 4).
+//
+// One CTA = 128 query rows of one query head (192 threads):
+//   warp 0      TMA producer: each 128-key block is 8 runs of 16 keys x 2 dim
+//               halves of K and of V (one box each: 16 keys x 64 dims of one
+//               page, 128-byte swizzle) into a 2-stage ring.
+//   warp 1      tensor memory (512 columns) and the single MMA-issuing thread:
+//               S_j = Q K_j^T (M 128 x N 128 x K 128; the fp32 queries enter
+//               as a high and a low 16-bit part, two MMAs each) into one of two
+//               S buffers, one block ahead of the softmax; then O += P_j V_j
+//               with P_j read from tensor memory and V_j as an MN-major operand.
+//   warps 2..5  one query row per thread (its TMEM lane): load and split the
+//               query, then per block the online softmax in base 2 on the S row,
+//               P (16-bit) written back over S for the next MMA; O is rescaled
+//               in tensor memory only when a row's maximum grows by more than
+//               2^8 (the stale maximum keeps P <= 256 otherwise); finally
+//               O / l is stored.
+// Every wait is bounded; a timeout records SAR_ERR_TIMEOUT.
+#include <float.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc05.cuh"
+
+namespace sar {
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBQ = 128;                       // query rows per CTA (TMEM lanes)
+constexpr int kBKV = 128;                      // keys per block
+constexpr int kRun = 16;                       // keys per TMA box (page sizes are multiples of it)
+constexpr int kRunsPerBlock = kBKV / kRun;
+constexpr int kThreads = 192;
+constexpr int kRegion = 128 * 128;             // [128 rows][128 bytes]: 64 dims of 128 rows
+constexpr int kQBytes = 2 * kRegion;           // one 16-bit copy of the Q tile (two dim halves)
+constexpr int kKVBytes = 2 * kRegion;          // K (or V) of one block
+constexpr int kStages = 2;
+constexpr int kBarOff = 2 * kQBytes + kStages * 2 * kKVBytes;  // after Q hi, Q lo, stages
+constexpr int kSmem = 1024 + kBarOff + 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 128;               // S buffer b at columns [b*128, b*128+128); P overwrites the first 64
+constexpr uint32_t kColO = 256;
+constexpr float kRescale = 8.f;                // log2 of the growth tolerated before rescaling O
+
+struct Bars {
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_done, q_ready, mma_done;
+  uint32_t tmem_slot;
+};
+
+// Instruction descriptor, kind::f16: fp32 accumulate, A and B of format fmt,
+// A K-major, B K-major (b_mn = 0) or MN-major (1), M = 128, N = 128.
+__device__ __forceinline__ uint32_t idesc_128x128(uint32_t fmt, uint32_t b_mn) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (b_mn << 16) | ((uint32_t)(128 >> 3) << 17) |
+         ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, int* err, int site) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err, site) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_attn_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                         const ChunkAttnArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  // Q hi, Q lo, then per stage K then V; each a pair of 16 KB dim-half regions
+  const uint32_t q_hi = sbase, q_lo = sbase + kQBytes;
+  auto k_reg = [&](int s) { return sbase + 2 * kQBytes + (uint32_t)(s * 2 * kKVBytes); };
+  auto v_reg = [&](int s) { return sbase + 2 * kQBytes + (uint32_t)(s * 2 * kKVBytes + kKVBytes); };
+  Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int qt = gridDim.x - 1 - blockIdx.x;  // longest causal ranges first
+  const int hq = blockIdx.y;
+  const int G = a.qh / a.kvh;
+  const int kh = hq / G;
+  const int q0 = qt * kBQ;
+  const int rows = min(kBQ, a.len - q0);
+  const int n_keys = a.start_pos + q0 + rows;  // keys of the last row of this tile, inclusive of it
+  const int nb = (n_keys + kBKV - 1) / kBKV;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bars->kv_full[s]), 1);
+      mbar_init(smem_u32(&bars->kv_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars->s_full[s]), 1);
+      mbar_init(smem_u32(&bars->p_full[s]), 4);
+    }
+    mbar_init(smem_u32(&bars->o_done), 1);
+    mbar_init(smem_u32(&bars->q_ready), 4);
+    mbar_init(smem_u32(&bars->mma_done), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc<false>(smem_u32(&bars->tmem_slot), kTmemCols);
+    tmem_relinquish<false>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  pdl_wait();
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      const int last_run = (n_keys - 1) / kRun;
+      bool ok = (n_keys - 1) / a.page_size < a.bt_len;
+      if (!ok) report(a.err, SAR_ERR_BOUNDS, SITE_CHUNK_BOUNDS, n_keys);
+      for (int j = 0; j < nb && ok; ++j) {
+        const int s = j % kStages;
+        if (!mbar_wait(smem_u32(&bars->kv_empty[s]), (uint32_t)(((j / kStages) & 1) ^ 1), a.err, SITE_CHUNK_PIPE)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&bars->kv_full[s]);
+        mbar_expect_tx(fb, 2u * kKVBytes);
+#pragma unroll 1
+        for (int g = 0; g < kRunsPerBlock; ++g) {
+          // runs past the last key repeat the last one (finite data, masked)
+          const int key = min(j * kRunsPerBlock + g, last_run) * kRun;
+          const int bi = key / a.page_size;
+          int page = a.bt[bi];
+          if (page < 0 || page >= a.num_pages) {
+            report(a.err, SAR_ERR_BOUNDS, SITE_CHUNK_BOUNDS, page);
+            page = 0;
+          }
+          const int row = (page * a.kvh + kh) * a.page_size + (key - bi * a.page_size);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tma_load_2d(k_reg(s) + h * kRegion + g * (kRun * 128), &tmk, h * 64, row, fb);
+            tma_load_2d(v_reg(s) + h * kRegion + g * (kRun * 128), &tmv, h * 64, row, fb);
+          }
+        }
+      }
+      // no copy may still be in flight when the CTA leaves
+      const int first = max(0, nb - kStages);
+      for (int j = first; j < nb && ok; ++j)
+        ok = mbar_wait(smem_u32(&bars->kv_empty[j % kStages]), (uint32_t)((j / kStages) & 1), a.err,
+                       SITE_CHUNK_PIPE);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issue ----------------
+    if (lane == 0) {
+      const uint32_t fmt = Elem<T>::kMmaFormat;
+      const uint32_t id_s = idesc_128x128(fmt, 0), id_pv = idesc_128x128(fmt, 1);
+      bool ok = mbar_wait(smem_u32(&bars->q_ready), 0, a.err, SITE_CHUNK_PIPE);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % kStages;
+        if (!mbar_wait(smem_u32(&bars->kv_full[s]), (uint32_t)((j / kStages) & 1), a.err, SITE_CHUNK_PIPE))
+          return false;
+        tc_fence_after();
+        const uint32_t d = tmem + (kColS * (uint32_t)(j & 1));
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (uint32_t)((kk >> 2) * kRegion + (kk & 3) * 32);
+          const uint64_t bdesc = sw128_desc(k_reg(s) + off);
+          mma_f16<false>(d, sw128_desc(q_hi + off), bdesc, id_s, kk != 0);
+          mma_f16<false>(d, sw128_desc(q_lo + off), bdesc, id_s, 1);
+        }
+        mma_commit(smem_u32(&bars->s_full[j & 1]));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < nb && ok; ++j) {
+        if (j + 1 < nb && !(ok = issue_s(j + 1))) break;
+        if (!(ok = mbar_wait(smem_u32(&bars->p_full[j & 1]), (uint32_t)((j >> 1) & 1), a.err, SITE_CHUNK_PIPE)))
+          break;
+        tc_fence_after();
+        const int s = j % kStages;
+#pragma unroll
+        for (int kk = 0; kk < kBKV / 16; ++kk) {
+          // 16 keys per step: P columns (two keys per 32-bit column), V rows
+          const uint64_t bdesc = sw128_desc_mn(v_reg(s) + kk * (16 * 128), kRegion, 1024);
+          mma_f16_ts(tmem + kColO, tmem + (kColS * (uint32_t)(j & 1)) + kk * 8, bdesc, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&bars->kv_empty[s]));
+        mma_commit(smem_u32(&bars->o_done));
+      }
+      // every MMA issued has completed before tensor memory is released
+      mma_commit(smem_u32(&bars->mma_done));
+      mbar_wait(smem_u32(&bars->mma_done), 0, a.err, SITE_CHUNK_PIPE);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- softmax / epilogue: one query row per thread ----------------
+    const int qq = warp & 3;
+    const int r = qq * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(qq * 32) << 16);
+    const bool valid = r < rows;
+    const int pos = a.start_pos + q0 + r;  // this row's position; keys <= pos are visible
+    {
+      // query row -> scaled, split into 16-bit high and low parts, swizzled as the MMA reads it
+      const float qscale = rsqrtf((float)kD) * 1.4426950408889634f;
+      const float* qp = a.q32 + (size_t)(q0 + r) * a.ld32 + (size_t)hq * kD;
+#pragma unroll 1
+      for (int c = 0; c < kD / 8; ++c) {
+        float x[8];
+        if (valid) {
+          const float4 v0 = *reinterpret_cast<const float4*>(qp + c * 8);
+          const float4 v1 = *reinterpret_cast<const float4*>(qp + c * 8 + 4);
+          x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
+          x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = x[2 * e] * qscale, x1 = x[2 * e + 1] * qscale;
+          hi[e] = Elem<T>::pack(x0, x1);
+          lo[e] = Elem<T>::pack(x0 - Elem<T>::lo(hi[e]), x1 - Elem<T>::hi(hi[e]));
+        }
+        const int h = c >> 3, ch = c & 7;
+        const uint32_t off = (uint32_t)(h * kRegion + r * 128 + ((ch ^ (r & 7)) << 4));
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(q_hi + off), "r"(hi[0]), "r"(hi[1]),
+                     "r"(hi[2]), "r"(hi[3])
+                     : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(q_lo + off), "r"(lo[0]), "r"(lo[1]),
+                     "r"(lo[2]), "r"(lo[3])
+                     : "memory");
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->q_ready));
+    }
+
+    float m_used = -INFINITY, l = 0.f;
+    bool alive = true;
+    for (int j = 0; j < nb && alive; ++j) {
+      alive = warp_wait_bar(smem_u32(&bars->s_full[j & 1]), (uint32_t)((j >> 1) & 1), a.err, SITE_CHUNK_PIPE);
+      if (!alive) break;
+      tc_fence_after();
+      const uint32_t scol = lane_base + (kColS * (uint32_t)(j & 1));
+      float sv[kBKV];
+#pragma unroll
+      for (int c = 0; c < kBKV / 16; ++c) {
+        uint32_t u[16];
+        tmem_ld16(scol + c * 16, u);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sv[c * 16 + e] = __uint_as_float(u[e]);
+      }
+      tmem_wait_ld();
+      const int key0 = j * kBKV;
+      float mx = -INFINITY;
+      if (key0 + kBKV - 1 > pos) {
+#pragma unroll
+        for (int c = 0; c < kBKV; ++c)
+          if (key0 + c > pos) sv[c] = -INFINITY;
+      }
+#pragma unroll
+      for (int c = 0; c < kBKV; ++c) mx = fmaxf(mx, sv[c]);
+      const float m_new = fmaxf(m_used, mx);
+      const bool need = m_new > m_used + kRescale;  // always on the first block with a visible key
+      const float sc = need ? exp2f(m_used - m_new) : 1.f;  // 0 while m_used is -inf
+      if (__any_sync(0xffffffffu, need && l > 0.f)) {
+        // O holds earlier blocks: rescale it once the previous P.V has landed
+        alive = warp_wait_bar(smem_u32(&bars->o_done), (uint32_t)((j - 1) & 1), a.err, SITE_CHUNK_PIPE);
+        if (!alive) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < kD / 16; ++c) {
+          uint32_t u[16];
+          tmem_ld16(lane_base + kColO + c * 16, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * sc);
+          tmem_st16(lane_base + kColO + c * 16, u);
+        }
+        tmem_wait_st();
+      }
+      if (need) {
+        l *= sc;
+        m_used = m_new;
+      }
+      // P = 2^(S - m), 16-bit, two keys per column, over the first 64 columns of this S buffer
+      float ls = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBKV / 32; ++c) {
+        uint32_t u[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = exp2f(sv[c * 32 + 2 * e] - m_used);
+          const float p1 = exp2f(sv[c * 32 + 2 * e + 1] - m_used);
+          ls += p0 + p1;
+          u[e] = Elem<T>::pack(p0, p1);
+        }
+        tmem_st16(scol + c * 16, u);
+      }
+      l += ls;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[j & 1]));
+    }
+    // ---- O / l -> output row ----
+    if (alive) alive = warp_wait_bar(smem_u32(&bars->o_done), (uint32_t)((nb - 1) & 1), a.err, SITE_CHUNK_PIPE);
+    if (alive) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      T* out = static_cast<T*>(a.out) + (size_t)(q0 + r) * a.ld_out + (size_t)hq * kD;
+#pragma unroll 1
+      for (int c = 0; c < kD / 16; ++c) {
+        uint32_t u[16];
+        tmem_ld16(lane_base + kColO + c * 16, u);
+        tmem_wait_ld();
+        uint32_t o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = Elem<T>::pack(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(out + c * 16);
+          dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<false>(tmem, kTmemCols);
+  }
+}
+
+template <typename T>
+int launch_t(const ChunkAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(chunk_attn_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return cuda_error(e, "chunk attention (tcgen05) attribute");
+    attr = true;
+  }
+  const dim3 grid((a.len + kBQ - 1) / kBQ, a.qh);
+  cudaError_t e = launch_pdl(chunk_attn_tc_kernel<T>, grid, dim3(kThreads), (size_t)kSmem, s, tmk, tmv, a);
+  if (e != cudaSuccess) return cuda_error(e, "chunk attention (tcgen05) launch");
+  count_launches(1);
+  return SAR_OK;
+}
+
+}  // namespace
+
+bool chunk_attention_tc_supported(const ChunkAttnArgs& a) {
+  return a.d == kD && a.page_size % kRun == 0 && a.qh % a.kvh == 0;
+}
+
+int launch_chunk_attention_tc(const ChunkAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              cudaStream_t s) {
+  if (a.len <= 0) return SAR_OK;
+  if (!chunk_attention_tc_supported(a))
+    return set_error(SAR_ERR_UNSUPPORTED, "chunk attention (tcgen05): head_dim 128, pages of a multiple of 16 keys");
+  if ((reinterpret_cast<uintptr_t>(a.q32) & 15) || (a.ld32 & 3) || (reinterpret_cast<uintptr_t>(a.out) & 15) ||
+      (a.ld_out & 7))
+    return set_error(SAR_ERR_INVALID_ARG, "chunk attention (tcgen05): misaligned query or output rows");
+  return a.storage == SAR_STORAGE_BF16 ? launch_t<__nv_bfloat16>(a, tmk, tmv, s) : launch_t<__half>(a, tmk, tmv, s);
+}
+
+}  // namespace sar

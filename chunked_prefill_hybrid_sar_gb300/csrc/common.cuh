@@ -23,6 +23,7 @@ enum ErrSite {
   SITE_DECODE_PIPE = 10,
   SITE_DECODE_BOUNDS = 11,
   SITE_CHUNK_BOUNDS = 20,
+  SITE_CHUNK_PIPE = 21,
   SITE_ROPE_BOUNDS = 30,
   SITE_EMBED_BOUNDS = 40,
 };

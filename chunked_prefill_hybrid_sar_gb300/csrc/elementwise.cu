@@ -35,8 +35,9 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // SRC selects where row r comes from: kSrcResidual reads the fp32 stream;
 // kSrcRows (bf16 rows of the stacked batch) and kSrcTokens (embedding rows of
 // token ids, storage type) are the step's first norm, which also writes the
-// row into the fp32 stream `h`.  `zero` (optional): row r of it, zero_cols
-// floats, is cleared (the LM head's split-K accumulator).
+// row into the fp32 stream `h`.  `zero` (optional): floats [0, zero_n) are
+// cleared, split evenly over the blocks (the LM head's split-K accumulator,
+// cleared by the step's first kernel).
 enum { kSrcResidual = 0, kSrcRows = 1, kSrcTokens = 2 };
 
 struct NormArgs {
@@ -48,7 +49,7 @@ struct NormArgs {
   void* y;
   const int32_t* ridx;    // kSrcResidual: optional source row per output row
   float* zero;
-  int zero_cols;
+  size_t zero_n;
   int hidden, vocab;
   float eps;
   int* err;
@@ -121,12 +122,14 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
     }
   }
   if (a.zero) {
-    float* zr = a.zero + (size_t)r * a.zero_cols;
-    if ((a.zero_cols & 3) == 0) {
-      float4* z4 = reinterpret_cast<float4*>(zr);
-      for (int i = threadIdx.x; i < (a.zero_cols >> 2); i += kNormThreads) z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-      for (int i = threadIdx.x; i < a.zero_cols; i += kNormThreads) zr[i] = 0.f;
+    // block r clears its share, a multiple of 4 floats (16-byte stores)
+    const size_t per = ((a.zero_n + gridDim.x - 1) / gridDim.x + 3) & ~(size_t)3;
+    const size_t z0 = per * r, z1 = min(a.zero_n, z0 + per);
+    if (z0 < z1) {
+      const size_t n4 = (z1 - z0) >> 2;
+      float4* z4 = reinterpret_cast<float4*>(a.zero + z0);
+      for (size_t i = threadIdx.x; i < n4; i += kNormThreads) z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (size_t i = z0 + 4 * n4 + threadIdx.x; i < z1; i += kNormThreads) a.zero[i] = 0.f;
     }
   }
 }
@@ -313,7 +316,7 @@ __global__ void __launch_bounds__(1024) argmax_kernel(const float* __restrict__ 
 }  // namespace
 
 int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hidden, float eps,
-                   const int32_t* row_index, int storage, cudaStream_t s, float* zero, int zero_cols) {
+                   const int32_t* row_index, int storage, cudaStream_t s) {
   if (rows <= 0) return SAR_OK;
   if (hidden % 4 || hidden > 4 * kNormThreads * kNormMaxVec)
     return set_error(SAR_ERR_UNSUPPORTED, "rmsnorm: hidden must be a multiple of 4 and at most 8192");
@@ -322,8 +325,6 @@ int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hid
   a.g = gain;
   a.y = y;
   a.ridx = row_index;
-  a.zero = zero;
-  a.zero_cols = zero_cols;
   a.hidden = hidden;
   a.eps = eps;
   cudaError_t e = storage == SAR_STORAGE_BF16
@@ -335,7 +336,8 @@ int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hid
 }
 
 int launch_input_norm(int in_kind, const void* in, const void* table, int vocab, float* h, const float* gain,
-                      void* y, int rows, int hidden, float eps, int storage, int* err, cudaStream_t s) {
+                      void* y, int rows, int hidden, float eps, int storage, int* err, cudaStream_t s,
+                      float* zero, size_t zero_n) {
   if (rows <= 0) return SAR_OK;
   if (hidden % 4 || hidden > 4 * kNormThreads * kNormMaxVec)
     return set_error(SAR_ERR_UNSUPPORTED, "rmsnorm: hidden must be a multiple of 4 and at most 8192");
@@ -349,6 +351,8 @@ int launch_input_norm(int in_kind, const void* in, const void* table, int vocab,
   a.vocab = vocab;
   a.eps = eps;
   a.err = err;
+  a.zero = zero;
+  a.zero_n = zero_n;
   const bool bf = storage == SAR_STORAGE_BF16;
   const dim3 g(rows), b(kNormThreads);
   cudaError_t e;

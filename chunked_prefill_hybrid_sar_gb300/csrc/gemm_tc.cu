@@ -35,6 +35,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc05.cuh"
 
 namespace sar {
 
@@ -44,145 +45,10 @@ constexpr int kThreads = 192;
 constexpr int kBK = 64;                   // K elements per stage (128 bytes)
 constexpr int kTileA = 128 * kBK * 2;     // one 128-row slab: 16 KB
 constexpr int kSmemLimit = 232448;        // 227 KB of dynamic shared memory
+constexpr int kSmemPerSm = 233472;        // 228 KB of shared memory per SM
 constexpr int kBarBytes = 1024;           // barriers + TMEM slot (+ alignment)
 constexpr int kSwapXchg = 64 * 17 * 4;    // swap-mode SwiGLU exchange buffer
 constexpr int kPrefetch = 16;             // K-slabs of the weight tile prefetched into L2 ahead
-
-// ---- tcgen05 wrappers ------------------------------------------------------
-
-// PAIR: the CTA pair of a 2-CTA cluster allocates the same columns in both
-// SMs' tensor memory (one warp of each CTA executes these).
-template <bool PAIR>
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  if constexpr (PAIR)
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-                 : "memory");
-  else
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-                 : "memory");
-}
-template <bool PAIR>
-__device__ __forceinline__ void tmem_relinquish() {
-  if constexpr (PAIR)
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-  else
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-template <bool PAIR>
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  if constexpr (PAIR)
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-  else
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// Address of the same shared-memory object in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
-}
-// TMA load into this CTA's shared memory whose completion is signalled on an
-// mbarrier of either CTA of the pair (`bar` a cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
-                                                 uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// PAIR: one thread of the leader CTA issues an M = 256 MMA over the pair:
-// A rows 0..127 and B rows 0..N/2-1 from the leader's shared memory, the rest
-// from the peer's (same offsets); D rows 0..127 land in the leader's tensor
-// memory, 128..255 in the peer's.
-template <bool PAIR>
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                        uint32_t accumulate) {
-  if constexpr (PAIR)
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  else
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Completion of the pair's MMAs so far, signalled on the same barrier offset
-// in both CTAs (mask 0b11).
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"((uint16_t)3)
-      : "memory");
-}
-
-// Arrive on the same barrier offset in every CTA of `mask` once this thread's
-// MMAs so far have completed.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// 32 lanes x 16 consecutive 32-bit columns: thread t of the warp gets lane
-// (warp quarter base + t), columns [col, col + 16).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes, 8-row atoms 1024 bytes apart (stride byte offset), sm_100 version.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
-  d |= (uint64_t)1 << 16;                   // leading byte offset (unused for SW128 K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset
-  d |= (uint64_t)1 << 46;                   // descriptor version
-  d |= (uint64_t)2 << 61;                   // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator, A and B of format
-// `fmt` (0 = f16, 1 = bf16; both operands always the same type), both
-// K-major, M = m (128, or 256 over a CTA pair), N = n.
-__device__ __forceinline__ uint32_t idesc_f16kind(int m, int n, uint32_t fmt) {
-  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
 
@@ -631,7 +497,8 @@ int make_tmap_16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols
 
 int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in_place) {
   const int cl_flag = variant & (SAR_GEMM_CLUSTER_1 | SAR_GEMM_CLUSTER_2 | SAR_GEMM_CLUSTER_4);
-  variant &= ~(SAR_GEMM_CLUSTER_1 | SAR_GEMM_CLUSTER_2 | SAR_GEMM_CLUSTER_4);
+  const bool two_ctas = (variant & SAR_GEMM_TWO_CTAS) != 0;
+  variant &= ~(SAR_GEMM_CLUSTER_1 | SAR_GEMM_CLUSTER_2 | SAR_GEMM_CLUSTER_4 | SAR_GEMM_TWO_CTAS);
   if (cl_flag & (cl_flag - 1)) return set_error(SAR_ERR_INVALID_ARG, "gemm: more than one cluster flag");
   if (M < 1 || N < 64 || K < 64 || N % 64 || K % 64)
     return set_error(SAR_ERR_UNSUPPORTED, "gemm: need M >= 1, N and K multiples of 64");
@@ -644,19 +511,21 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
   const bool can_split = epi == SAR_EPI_RESIDUAL && in_place;
   // SM clocks per 64-wide K slab of one tile: the larger of the MMA time
   // (128 x bn x 64 takes 2*bn clocks per 128-row sub-tile) and the time to
-  // stream its operands into shared memory (about 64 bytes per clock per SM)
+  // stream its operands into shared memory (about 86 bytes per clock per SM,
+  // as the 128x256 and CTA-pair tilings measure on the projection shapes)
   // (a pair tile: each SM computes its 128 rows x bn and loads half the weight rows)
   auto kslab_clocks = [](int msub, int bn, bool pair = false) -> long {
-    return std::max<long>(2L * msub * bn, (msub * 16384L + (pair ? bn / 2 : bn) * 128L) / 64);
+    return std::max<long>(2L * msub * bn, (msub * 16384L + (pair ? bn / 2 : bn) * 128L) / 86);
   };
-  auto best_split = [&](long tiles, long per_kb_work, int* splits) {
+  // slots: units running at once (SMs, SM pairs, or two CTAs per SM)
+  auto best_split = [&](long tiles, long per_kb_work, int* splits, long slots) {
     long best = -1;
     for (int sp = 1; sp <= (can_split ? 4 : 1); ++sp) {
       const long kb = (k_blocks + sp - 1) / sp;
       if (sp > 1 && kb < 8) break;
       const long units = tiles * sp;
       // waves x unit work, plus a small charge per extra split for the atomic adds
-      const long c = ((units + sms - 1) / sms) * kb * per_kb_work * (sp > 1 ? 21 : 20) / 20;
+      const long c = ((units + slots - 1) / slots) * kb * per_kb_work * (sp > 1 ? 21 : 20) / 20;
       if (best < 0 || c < best) {
         best = c;
         *splits = sp;
@@ -670,15 +539,18 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
       variant = SAR_GEMM_SWAP;
     } else {
       // makespan estimate: waves x per-unit MMA work
-      auto cost = [&](int msub, int bn) {
-        const long tiles = (long)((M + 128 * msub - 1) / (128 * msub)) * ((N + bn - 1) / bn);
+      auto cost = [&](int msub, int bn, bool pair) {
+        long m_tiles = (M + 128 * msub - 1) / (128 * msub);
+        if (pair) m_tiles = (m_tiles + 1) / 2;  // a pair unit covers two token tiles on two SMs
+        const long tiles = m_tiles * ((N + bn - 1) / bn);
         int sp = 1;
-        return best_split(tiles, kslab_clocks(msub, bn), &sp) * 1000 + tiles;  // tie-break: fewer tiles
+        return best_split(tiles, kslab_clocks(msub, bn, pair), &sp, pair ? sms / 2 : sms) * 1000 + tiles;
       };
       variant = SAR_GEMM_M128_N256;
-      long best = (N % 256 == 0) ? cost(1, 256) : -1;
-      if (best < 0 || cost(1, 128) < best) { variant = SAR_GEMM_M128_N128; best = cost(1, 128); }
-      if (cost(2, 128) < best) variant = SAR_GEMM_M256_N128;
+      long best = (N % 256 == 0) ? cost(1, 256, false) : -1;
+      if (best < 0 || cost(1, 128, false) < best) { variant = SAR_GEMM_M128_N128; best = cost(1, 128, false); }
+      if (cost(2, 128, false) < best) { variant = SAR_GEMM_M256_N128; best = cost(2, 128, false); }
+      if (N % 256 == 0 && cl_flag <= SAR_GEMM_CLUSTER_2 && cost(1, 256, true) < best) variant = SAR_GEMM_PAIR_N256;
     }
   }
   switch (variant) {
@@ -728,15 +600,20 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
   const int stage_bytes = c.msub * kTileA + (c.pair ? c.bn / 2 : c.bn) * kBK * 2;
   c.stage_bytes = stage_bytes;
   const int extra = kBarBytes + 1024 + ((c.swap && epi == SAR_EPI_SWIGLU) ? kSwapXchg : 0);
-  c.stages = std::min(8, (kSmemLimit - extra) / stage_bytes);
+  if (two_ctas && (!c.swap || c.bn > 128))
+    return set_error(SAR_ERR_UNSUPPORTED, "gemm: two CTAs per SM only with the swap tiling and M <= 128");
+  c.per_sm = two_ctas ? 2 : 1;
+  // two per SM: each gets half of the SM's shared memory (less 1 KB the system reserves per CTA)
+  const int smem_cap = two_ctas ? (kSmemPerSm / 2 - 1024) : kSmemLimit;
+  c.stages = std::min(8, (smem_cap - extra) / stage_bytes);
   if (c.stages < 2) return set_error(SAR_ERR_UNSUPPORTED, "gemm: tile does not fit shared memory");
   c.smem = c.stages * stage_bytes + extra;
   c.splits = 1;
-  best_split((long)c.m_tiles * c.n_tiles, c.swap ? kslab_clocks(1, c.bn) : kslab_clocks(c.msub, c.bn, c.pair),
-             &c.splits);
+  best_split((long)c.m_groups * c.n_tiles, c.swap ? kslab_clocks(1, c.bn) : kslab_clocks(c.msub, c.bn, c.pair),
+             &c.splits, (long)sms * c.per_sm / c.cl);
   c.kb_per_split = (k_blocks + c.splits - 1) / c.splits;
   c.splits = (k_blocks + c.kb_per_split - 1) / c.kb_per_split;  // no empty K range
-  c.grid = std::min(c.m_tiles * c.n_tiles * c.splits, sms) / c.cl * c.cl;  // whole clusters; refined at launch
+  c.grid = std::min(c.m_tiles * c.n_tiles * c.splits, sms * c.per_sm) / c.cl * c.cl;  // whole clusters; refined at launch
   *cfg = c;
   return SAR_OK;
 }

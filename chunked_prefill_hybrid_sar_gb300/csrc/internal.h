@@ -66,6 +66,7 @@ struct GemmCfg {
   int kb_per_split = 0;  // 64-wide K slabs per range
   int pair = 0;          // 2-CTA tiles: M = 256 MMAs over a CTA pair (cl = 2)
   int stage_bytes = 0;   // shared memory of one pipeline stage (per CTA)
+  int per_sm = 1;        // CTAs resident per SM (2: swap tiling, half the stages each)
   int cl = 1;            // CTAs per cluster sharing a weight tile by multicast (non-swap)
   int m_groups = 0;      // token-tile groups of cl tiles
 };
@@ -94,13 +95,13 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
 // ---- elementwise kernels (elementwise.cu) ----------------------------------
 // x: fp32 residual rows; y: storage-type rows; row_index (optional) gathers rows.
 int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hidden, float eps,
-                   const int32_t* row_index, int storage, cudaStream_t s, float* zero = nullptr,
-                   int zero_cols = 0);
+                   const int32_t* row_index, int storage, cudaStream_t s);
 // The step's first kernel: stacked input rows (bf16 hidden rows, or token ids
 // looked up in `table`) into the fp32 residual stream h and, normalised with
-// `gain`, into y (storage type).
+// `gain`, into y (storage type).  zero (optional): zero_n floats to clear.
 int launch_input_norm(int in_kind, const void* in, const void* table, int vocab, float* h, const float* gain,
-                      void* y, int rows, int hidden, float eps, int storage, int* err, cudaStream_t s);
+                      void* y, int rows, int hidden, float eps, int storage, int* err, cudaStream_t s,
+                      float* zero = nullptr, size_t zero_n = 0);
 int launch_embed(const int32_t* tokens, const void* table, float* out, int rows, int hidden, int vocab,
                  int storage, int* err, cudaStream_t s);
 int launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s);
@@ -162,5 +163,11 @@ struct ChunkAttnArgs {
   int* err;
 };
 int launch_chunk_attention(const ChunkAttnArgs& a, cudaStream_t s);
+// The same on the tcgen05 tensor cores (attn_chunk_tc.cu) for head_dim 128 and
+// pages of a multiple of 16 keys, reading the pages through the per-layer
+// tensor maps of the KV cache (16-key x 64-dim boxes).
+bool chunk_attention_tc_supported(const ChunkAttnArgs& a);
+int launch_chunk_attention_tc(const ChunkAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              cudaStream_t s);
 
 }  // namespace sar

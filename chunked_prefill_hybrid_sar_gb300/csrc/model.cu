@@ -329,10 +329,11 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
     LayerW& w = m->L[l];
     if (l == 0) {
       // a0 + a1: stacked rows (chunk first, then decodes) into the fp32
-      // residual stream, normalised for layer 0 in the same pass
+      // residual stream, normalised for layer 0 in the same pass; also clears
+      // the logits rows, which the LM head GEMM adds its K ranges into
       Prof pr(m, SAR_K_EMBED, s);
       SAR_TRY(sar::launch_input_norm(b->in_kind, in, m->embed, d.vocab, h, w.n1, m->xn, M, H, d.rms_eps, d.storage,
-                                     m->err, s));
+                                     m->err, s, logits, logits ? (size_t)p.R * d.vocab : 0));
     } else {
       Prof pr(m, SAR_K_RMSNORM, s);
       SAR_TRY(sar::launch_rmsnorm(h, w.n1, m->xn, M, H, d.rms_eps, nullptr, d.storage, s));
@@ -384,7 +385,10 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
       ca.num_pages = kv->num_pages;
       ca.storage = d.storage;
       ca.err = m->err;
-      SAR_TRY(sar::launch_chunk_attention(ca, s));
+      if (sar::chunk_attention_tc_supported(ca))
+        SAR_TRY(sar::launch_chunk_attention_tc(ca, kv->tmk[l], kv->tmv[l], s));
+      else
+        SAR_TRY(sar::launch_chunk_attention(ca, s));
     }
     if (p.Bd > 0) {
       Prof pr(m, SAR_K_DECODE_ATTN, s);
@@ -440,9 +444,7 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
   if (logits) {
     {
       Prof pr(m, SAR_K_HEAD_NORM, s);
-      // also clears the logits rows: the head GEMM adds its K ranges into them
-      SAR_TRY(sar::launch_rmsnorm(h, m->final_norm, m->hrows, p.R, H, d.rms_eps, md + p.o_rows, d.storage, s,
-                                  logits, d.vocab));
+      SAR_TRY(sar::launch_rmsnorm(h, m->final_norm, m->hrows, p.R, H, d.rms_eps, md + p.o_rows, d.storage, s));
     }
     {
       Prof pr(m, SAR_K_GEMM_HEAD, s);
@@ -667,6 +669,10 @@ int sar_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, void*
              void* layer_out, void* stream) {
   if (!m || !kv || !b || !in) return set_error(SAR_ERR_INVALID_ARG, "step: null argument");
   if (kv->m != m) return set_error(SAR_ERR_INVALID_ARG, "step: KV cache belongs to another model");
+  // the kernels move these with 16-byte (outputs) and 8-byte (bf16 input rows) accesses
+  if ((reinterpret_cast<uintptr_t>(hidden_out) & 15) || (reinterpret_cast<uintptr_t>(logits_out) & 15) ||
+      (b->in_kind == SAR_IN_HIDDEN && (reinterpret_cast<uintptr_t>(in) & 7)))
+    return set_error(SAR_ERR_INVALID_ARG, "step: hidden_out / logits_out must be 16-byte and in 8-byte aligned");
   float* h = hidden_out ? static_cast<float*>(hidden_out) : m->hres;
   return run_step(m, kv, b, in, h, logits_out, layer_out, static_cast<cudaStream_t>(stream));
 }

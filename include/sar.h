@@ -175,6 +175,8 @@ typedef struct sar_batch {
 } sar_batch;
 
 /* Runs every layer over the stacked rows M = Lp + n_decode and then the head.
+ * hidden_out and logits_out must be 16-byte aligned, bf16 `in` 8-byte aligned
+ * (else SAR_ERR_INVALID_ARG before any launch).
  *   in         device: bf16 [M, hidden] (SAR_IN_HIDDEN) or int32 [M] token ids
  *   hidden_out device fp32 [M, hidden]: last layer's residual stream (before
  *              the final norm); may be NULL

@@ -54,7 +54,11 @@ enum {
    * returns SAR_ERR_UNSUPPORTED. */
   SAR_GEMM_CLUSTER_1 = 0x100,
   SAR_GEMM_CLUSTER_2 = 0x200,
-  SAR_GEMM_CLUSTER_4 = 0x400
+  SAR_GEMM_CLUSTER_4 = 0x400,
+  /* Optional flag for the swap tiling with at most 128 token rows: two CTAs
+   * per SM, each with half the pipeline, so twice as many weight slabs are in
+   * flight per SM (the memory-bound regime). */
+  SAR_GEMM_TWO_CTAS = 0x1000
 };
 
 /* C = epilogue(A . W^T).  A [M, K], W [N, K] in the storage type `storage`

@@ -241,3 +241,31 @@ def test_gemm_pair_large(M, N, K):
     assert ((c.double().cpu() - ref).abs().max() / ref.abs().max()).item() < tol
     ref = ref + r.double()
     assert ((h.double().cpu() - ref).abs().max() / ref.abs().max()).item() < tol
+
+
+@pytest.mark.parametrize("M", [1, 40, 128])
+@pytest.mark.parametrize("epi", ["store", "residual", "swiglu", "f32"])
+def test_gemm_swap_two_ctas_per_sm(M, epi):
+    """Swap tiling with two CTAs per SM (half the stages each) equals the
+    one-CTA launch bit for bit; it is refused above 128 token rows."""
+    N, K = 2048, 2048
+    a, w, r = operands(M, N, K, 10)
+    a, w, r = a.to(DEV), w.to(DEV), r.to(DEV)
+    epi_id = {"store": sar.SAR_EPI_STORE, "residual": sar.SAR_EPI_RESIDUAL, "swiglu": sar.SAR_EPI_SWIGLU,
+              "f32": sar.SAR_EPI_F32}[epi]
+    cols = N // 2 if epi == "swiglu" else N
+    odt = torch.float32 if epi in ("residual", "f32") else torch.float16
+
+    def run(flag):
+        c = torch.full((M, cols), float("nan"), dtype=odt, device=DEV)
+        sar.gemm(a, w, c, residual=r if epi == "residual" else None, epilogue=epi_id,
+                 variant=sar.SAR_GEMM_SWAP | flag)
+        return c
+
+    base, two = run(0), run(sar.SAR_GEMM_TWO_CTAS)
+    torch.cuda.synchronize()
+    assert torch.equal(base, two)
+    with pytest.raises(sar.SarError):
+        sar.gemm(torch.zeros(200, K, dtype=torch.float16, device=DEV), w,
+                 torch.zeros(200, N, dtype=torch.float16, device=DEV),
+                 variant=sar.SAR_GEMM_SWAP | sar.SAR_GEMM_TWO_CTAS)
