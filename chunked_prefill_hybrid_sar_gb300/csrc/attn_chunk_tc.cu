@@ -6,10 +6,11 @@
 // attention, same page section 3.1; chunk k re-reads the KV of the k earlier
 // chunks, Sarathi-Serve digest section 4).
 //
-// One CTA = 128 query rows of one query head (192 threads):
-//   warp 0      TMA producer: each 128-key block is 8 runs of 16 keys x 2 dim
-//               halves of K and of V (one box each: 16 keys x 64 dims of one
-//               page, 128-byte swizzle) into a 2-stage ring.
+// One CTA = 128 query rows of one query head (224 threads):
+//   warps 0, 6  TMA producers of K and of V: each 128-key block is 8 runs of
+//               16 keys x 2 dim halves (one box each: 16 keys x 64 dims of one
+//               page, 128-byte swizzle) into a 2-stage ring per tensor; a K
+//               stage frees when S_j has been computed, a V stage after P_j V_j.
 //   warp 1      tensor memory (512 columns) and the single MMA-issuing thread:
 //               S_j = Q K_j^T (M 128 x N 128 x K 128; the fp32 queries enter
 //               as a high and a low 16-bit part, two MMAs each) into one of two
@@ -37,7 +38,7 @@ constexpr int kBQ = 128;                       // query rows per CTA (TMEM lanes
 constexpr int kBKV = 128;                      // keys per block
 constexpr int kRun = 16;                       // keys per TMA box (page sizes are multiples of it)
 constexpr int kRunsPerBlock = kBKV / kRun;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kRegion = 128 * 128;             // [128 rows][128 bytes]: 64 dims of 128 rows
 constexpr int kQBytes = 2 * kRegion;           // one 16-bit copy of the Q tile (two dim halves)
 constexpr int kKVBytes = 2 * kRegion;          // K (or V) of one block
@@ -50,7 +51,7 @@ constexpr uint32_t kColO = 256;
 constexpr float kRescale = 8.f;                // log2 of the growth tolerated before rescaling O
 
 struct Bars {
-  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
   uint64_t s_full[2], p_full[2];
   uint64_t o_done, q_ready, mma_done;
   uint32_t tmem_slot;
@@ -61,6 +62,14 @@ struct Bars {
 __device__ __forceinline__ uint32_t idesc_128x128(uint32_t fmt, uint32_t b_mn) {
   return (1u << 4) | (fmt << 7) | (fmt << 10) | (b_mn << 16) | ((uint32_t)(128 >> 3) << 17) |
          ((uint32_t)(128 >> 4) << 24);
+}
+
+// 2^x by the SFU's approximate exponential (relative error about 2^-22;
+// 2^-inf = 0), ample for a probability rounded to 16 bits next.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, int* err, int site) {
@@ -96,8 +105,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bars->kv_full[s]), 1);
-      mbar_init(smem_u32(&bars->kv_empty[s]), 1);
+      mbar_init(smem_u32(&bars->k_full[s]), 1);
+      mbar_init(smem_u32(&bars->k_empty[s]), 1);
+      mbar_init(smem_u32(&bars->v_full[s]), 1);
+      mbar_init(smem_u32(&bars->v_empty[s]), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars->s_full[s]), 1);
@@ -119,22 +130,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
   pdl_launch_dependents();
 
-  if (warp == 0) {
-    // ---------------- producer ----------------
+  if (warp == 0 || warp == 6) {
+    // ---------------- producers: warp 0 K, warp 6 V ----------------
     if (lane == 0) {
-      tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmv);
+      const bool is_k = warp == 0;
+      const CUtensorMap* map = is_k ? &tmk : &tmv;
+      uint64_t* full = is_k ? bars->k_full : bars->v_full;
+      uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+      tma_prefetch_desc(map);
       const int last_run = (n_keys - 1) / kRun;
       bool ok = (n_keys - 1) / a.page_size < a.bt_len;
-      if (!ok) report(a.err, SAR_ERR_BOUNDS, SITE_CHUNK_BOUNDS, n_keys);
+      if (!ok && is_k) report(a.err, SAR_ERR_BOUNDS, SITE_CHUNK_BOUNDS, n_keys);
       for (int j = 0; j < nb && ok; ++j) {
         const int s = j % kStages;
-        if (!mbar_wait(smem_u32(&bars->kv_empty[s]), (uint32_t)(((j / kStages) & 1) ^ 1), a.err, SITE_CHUNK_PIPE)) {
+        if (!mbar_wait(smem_u32(&empty[s]), (uint32_t)(((j / kStages) & 1) ^ 1), a.err, SITE_CHUNK_PIPE)) {
           ok = false;
           break;
         }
-        const uint32_t fb = smem_u32(&bars->kv_full[s]);
-        mbar_expect_tx(fb, 2u * kKVBytes);
+        const uint32_t fb = smem_u32(&full[s]);
+        const uint32_t dst = is_k ? k_reg(s) : v_reg(s);
+        mbar_expect_tx(fb, (uint32_t)kKVBytes);
 #pragma unroll 1
         for (int g = 0; g < kRunsPerBlock; ++g) {
           // runs past the last key repeat the last one (finite data, masked)
@@ -146,18 +161,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             page = 0;
           }
           const int row = (page * a.kvh + kh) * a.page_size + (key - bi * a.page_size);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tma_load_2d(k_reg(s) + h * kRegion + g * (kRun * 128), &tmk, h * 64, row, fb);
-            tma_load_2d(v_reg(s) + h * kRegion + g * (kRun * 128), &tmv, h * 64, row, fb);
-          }
+          tma_load_2d(dst + g * (kRun * 128), map, 0, row, fb);
+          tma_load_2d(dst + kRegion + g * (kRun * 128), map, 64, row, fb);
         }
       }
       // no copy may still be in flight when the CTA leaves
       const int first = max(0, nb - kStages);
       for (int j = first; j < nb && ok; ++j)
-        ok = mbar_wait(smem_u32(&bars->kv_empty[j % kStages]), (uint32_t)((j / kStages) & 1), a.err,
-                       SITE_CHUNK_PIPE);
+        ok = mbar_wait(smem_u32(&empty[j % kStages]), (uint32_t)((j / kStages) & 1), a.err, SITE_CHUNK_PIPE);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -168,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(smem_u32(&bars->q_ready), 0, a.err, SITE_CHUNK_PIPE);
       auto issue_s = [&](int j) -> bool {
         const int s = j % kStages;
-        if (!mbar_wait(smem_u32(&bars->kv_full[s]), (uint32_t)((j / kStages) & 1), a.err, SITE_CHUNK_PIPE))
+        if (!mbar_wait(smem_u32(&bars->k_full[s]), (uint32_t)((j / kStages) & 1), a.err, SITE_CHUNK_PIPE))
           return false;
         tc_fence_after();
         const uint32_t d = tmem + (kColS * (uint32_t)(j & 1));
@@ -180,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_f16<false>(d, sw128_desc(q_lo + off), bdesc, id_s, 1);
         }
         mma_commit(smem_u32(&bars->s_full[j & 1]));
+        mma_commit(smem_u32(&bars->k_empty[s]));
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -187,15 +199,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j + 1 < nb && !(ok = issue_s(j + 1))) break;
         if (!(ok = mbar_wait(smem_u32(&bars->p_full[j & 1]), (uint32_t)((j >> 1) & 1), a.err, SITE_CHUNK_PIPE)))
           break;
-        tc_fence_after();
         const int s = j % kStages;
+        if (!(ok = mbar_wait(smem_u32(&bars->v_full[s]), (uint32_t)((j / kStages) & 1), a.err, SITE_CHUNK_PIPE)))
+          break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBKV / 16; ++kk) {
           // 16 keys per step: P columns (two keys per 32-bit column), V rows
           const uint64_t bdesc = sw128_desc_mn(v_reg(s) + kk * (16 * 128), kRegion, 1024);
           mma_f16_ts(tmem + kColO, tmem + (kColS * (uint32_t)(j & 1)) + kk * 8, bdesc, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(smem_u32(&bars->kv_empty[s]));
+        mma_commit(smem_u32(&bars->v_empty[s]));
         mma_commit(smem_u32(&bars->o_done));
       }
       // every MMA issued has completed before tensor memory is released
@@ -270,8 +284,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBKV; ++c)
           if (key0 + c > pos) sv[c] = -INFINITY;
       }
+      {
+        // eight independent chains, then combine
+        float m8[8];
 #pragma unroll
-      for (int c = 0; c < kBKV; ++c) mx = fmaxf(mx, sv[c]);
+        for (int e = 0; e < 8; ++e) m8[e] = sv[e];
+#pragma unroll
+        for (int c = 8; c < kBKV; ++c) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx = fmaxf(mx, m8[e]);
+      }
       const float m_new = fmaxf(m_used, mx);
       const bool need = m_new > m_used + kRescale;  // always on the first block with a visible key
       const float sc = need ? exp2f(m_used - m_new) : 1.f;  // 0 while m_used is -inf
@@ -296,20 +318,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_new;
       }
       // P = 2^(S - m), 16-bit, two keys per column, over the first 64 columns of this S buffer
-      float ls = 0.f;
+      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < kBKV / 32; ++c) {
         uint32_t u[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = exp2f(sv[c * 32 + 2 * e] - m_used);
-          const float p1 = exp2f(sv[c * 32 + 2 * e + 1] - m_used);
-          ls += p0 + p1;
+          const float p0 = fast_exp2(sv[c * 32 + 2 * e] - m_used);
+          const float p1 = fast_exp2(sv[c * 32 + 2 * e + 1] - m_used);
+          ls[e & 7] += p0 + p1;
           u[e] = Elem<T>::pack(p0, p1);
         }
         tmem_st16(scol + c * 16, u);
       }
-      l += ls;
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
