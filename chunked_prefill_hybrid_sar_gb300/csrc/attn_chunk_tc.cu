@@ -6,8 +6,8 @@
 // attention, same page section 3.1; chunk k re-reads the KV of the k earlier
 // chunks, Sarathi-Serve digest section 4).
 //
-// One CTA = 128 query rows of one query head (224 threads):
-//   warps 0, 6  TMA producers of K and of V: each 128-key block is 8 runs of
+// One CTA = 128 query rows of one query head (352 threads):
+//   warps 0, 10 TMA producers of K and of V: each 128-key block is 8 runs of
 //               16 keys x 2 dim halves (one box each: 16 keys x 64 dims of one
 //               page, 128-byte swizzle) into a 2-stage ring per tensor; a K
 //               stage frees when S_j has been computed, a V stage after P_j V_j.
@@ -16,9 +16,11 @@
 //               as a high and a low 16-bit part, two MMAs each) into one of two
 //               S buffers, one block ahead of the softmax; then O += P_j V_j
 //               with P_j read from tensor memory and V_j as an MN-major operand.
-//   warps 2..5  one query row per thread (its TMEM lane): load and split the
-//               query, then per block the online softmax in base 2 on the S row,
-//               P (16-bit) written back over S for the next MMA; O is rescaled
+//   warps 2..9  two warps per row quarter (the TMEM lanes a warp may access),
+//               each with 64 of the 128 keys of every block: load and split the
+//               query, then per block the online softmax in base 2 (the two
+//               halves exchange their row maxima through shared memory), P
+//               (16-bit) written back over S for the next MMA; O is rescaled
 //               in tensor memory only when a row's maximum grows by more than
 //               2^8 (the stale maximum keeps P <= 256 otherwise); finally
 //               O / l is stored.
@@ -38,13 +40,14 @@ constexpr int kBQ = 128;                       // query rows per CTA (TMEM lanes
 constexpr int kBKV = 128;                      // keys per block
 constexpr int kRun = 16;                       // keys per TMA box (page sizes are multiples of it)
 constexpr int kRunsPerBlock = kBKV / kRun;
-constexpr int kThreads = 224;
+constexpr int kThreads = 352;                  // 11 warps
 constexpr int kRegion = 128 * 128;             // [128 rows][128 bytes]: 64 dims of 128 rows
 constexpr int kQBytes = 2 * kRegion;           // one 16-bit copy of the Q tile (two dim halves)
 constexpr int kKVBytes = 2 * kRegion;          // K (or V) of one block
 constexpr int kStages = 2;
 constexpr int kBarOff = 2 * kQBytes + kStages * 2 * kKVBytes;  // after Q hi, Q lo, stages
-constexpr int kSmem = 1024 + kBarOff + 256;
+constexpr int kRedOff = kBarOff + 256;         // softmax exchange: [3][2][128] floats
+constexpr int kSmem = 1024 + kRedOff + 3 * 2 * kBQ * 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 128;               // S buffer b at columns [b*128, b*128+128); P overwrites the first 64
 constexpr uint32_t kColO = 256;
@@ -112,10 +115,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars->s_full[s]), 1);
-      mbar_init(smem_u32(&bars->p_full[s]), 4);
+      mbar_init(smem_u32(&bars->p_full[s]), 8);
     }
     mbar_init(smem_u32(&bars->o_done), 1);
-    mbar_init(smem_u32(&bars->q_ready), 4);
+    mbar_init(smem_u32(&bars->q_ready), 8);
     mbar_init(smem_u32(&bars->mma_done), 1);
     fence_mbar_init();
   }
@@ -130,8 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
   pdl_launch_dependents();
 
-  if (warp == 0 || warp == 6) {
-    // ---------------- producers: warp 0 K, warp 6 V ----------------
+  if (warp == 0 || warp == 10) {
+    // ---------------- producers: warp 0 K, warp 10 V ----------------
     if (lane == 0) {
       const bool is_k = warp == 0;
       const CUtensorMap* map = is_k ? &tmk : &tmv;
@@ -218,22 +221,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- softmax / epilogue: one query row per thread ----------------
+    // ---------------- softmax / epilogue ----------------
+    // warps 2..9: row quarter qq = warp & 3 (the TMEM lanes this warp may
+    // access), column half hf: each row's 128 keys are split over two warps
+    // that exchange their partial maxima through shared memory.
     const int qq = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int r = qq * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(qq * 32) << 16);
     const bool valid = r < rows;
     const int pos = a.start_pos + q0 + r;  // this row's position; keys <= pos are visible
+    float* red = reinterpret_cast<float*>(smem + kRedOff);  // [2 parities][2 halves][128 rows]
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + qq) : "memory"); };
     {
-      // query row -> scaled, split into 16-bit high and low parts, swizzled as the MMA reads it
+      // this half of the query row -> scaled, split into 16-bit high and low
+      // parts, swizzled as the MMA reads it (dim half hf is Q region hf)
       const float qscale = rsqrtf((float)kD) * 1.4426950408889634f;
-      const float* qp = a.q32 + (size_t)(q0 + r) * a.ld32 + (size_t)hq * kD;
+      const float* qp = a.q32 + (size_t)(q0 + r) * a.ld32 + (size_t)hq * kD + hf * 64;
 #pragma unroll 1
-      for (int c = 0; c < kD / 8; ++c) {
+      for (int ch = 0; ch < 8; ++ch) {
         float x[8];
         if (valid) {
-          const float4 v0 = *reinterpret_cast<const float4*>(qp + c * 8);
-          const float4 v1 = *reinterpret_cast<const float4*>(qp + c * 8 + 4);
+          const float4 v0 = *reinterpret_cast<const float4*>(qp + ch * 8);
+          const float4 v1 = *reinterpret_cast<const float4*>(qp + ch * 8 + 4);
           x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
           x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
         } else {
@@ -247,8 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           hi[e] = Elem<T>::pack(x0, x1);
           lo[e] = Elem<T>::pack(x0 - Elem<T>::lo(hi[e]), x1 - Elem<T>::hi(hi[e]));
         }
-        const int h = c >> 3, ch = c & 7;
-        const uint32_t off = (uint32_t)(h * kRegion + r * 128 + ((ch ^ (r & 7)) << 4));
+        const uint32_t off = (uint32_t)(hf * kRegion + r * 128 + ((ch ^ (r & 7)) << 4));
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(q_hi + off), "r"(hi[0]), "r"(hi[1]),
                      "r"(hi[2]), "r"(hi[3])
                      : "memory");
@@ -262,65 +271,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     float m_used = -INFINITY, l = 0.f;
-    bool alive = true;
-    for (int j = 0; j < nb && alive; ++j) {
-      alive = warp_wait_bar(smem_u32(&bars->s_full[j & 1]), (uint32_t)((j >> 1) & 1), a.err, SITE_CHUNK_PIPE);
-      if (!alive) break;
+    bool alive = true;  // false once a wait gave up: work stops, the pair barriers stay matched
+    for (int j = 0; j < nb; ++j) {
+      if (alive) alive = warp_wait_bar(smem_u32(&bars->s_full[j & 1]), (uint32_t)((j >> 1) & 1), a.err, SITE_CHUNK_PIPE);
       tc_fence_after();
       const uint32_t scol = lane_base + (kColS * (uint32_t)(j & 1));
-      float sv[kBKV];
+      float sv[64];
+      if (alive) {
 #pragma unroll
-      for (int c = 0; c < kBKV / 16; ++c) {
-        uint32_t u[16];
-        tmem_ld16(scol + c * 16, u);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u[16];
+          tmem_ld16(scol + hf * 64 + c * 16, u);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) sv[c * 16 + e] = __uint_as_float(u[e]);
+          for (int e = 0; e < 16; ++e) sv[c * 16 + e] = __uint_as_float(u[e]);
+        }
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) sv[c] = 0.f;
       }
-      tmem_wait_ld();
-      const int key0 = j * kBKV;
-      float mx = -INFINITY;
-      if (key0 + kBKV - 1 > pos) {
+      const int key0 = j * kBKV + hf * 64;
+      if (key0 + 63 > pos) {
 #pragma unroll
-        for (int c = 0; c < kBKV; ++c)
+        for (int c = 0; c < 64; ++c)
           if (key0 + c > pos) sv[c] = -INFINITY;
       }
+      float pm;
       {
         // eight independent chains, then combine
         float m8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) m8[e] = sv[e];
 #pragma unroll
-        for (int c = 8; c < kBKV; ++c) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx = fmaxf(mx, m8[e]);
+        for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
+        pm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       }
+      // row maximum over both halves (double-buffered by block parity)
+      red[((j & 1) * 2 + hf) * kBQ + r] = pm;
+      pair_sync();
+      const float mx = fmaxf(pm, red[((j & 1) * 2 + (hf ^ 1)) * kBQ + r]);
       const float m_new = fmaxf(m_used, mx);
-      const bool need = m_new > m_used + kRescale;  // always on the first block with a visible key
+      const bool need = m_new > m_used + kRescale;  // always on the first block (key 0 is visible)
       const float sc = need ? exp2f(m_used - m_new) : 1.f;  // 0 while m_used is -inf
-      if (__any_sync(0xffffffffu, need && l > 0.f)) {
-        // O holds earlier blocks: rescale it once the previous P.V has landed
+      if (alive && __any_sync(0xffffffffu, need && l > 0.f)) {
+        // O holds earlier blocks: rescale this half once the previous P.V has landed
         alive = warp_wait_bar(smem_u32(&bars->o_done), (uint32_t)((j - 1) & 1), a.err, SITE_CHUNK_PIPE);
-        if (!alive) break;
-        tc_fence_after();
+        if (alive) {
+          tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < kD / 16; ++c) {
-          uint32_t u[16];
-          tmem_ld16(lane_base + kColO + c * 16, u);
-          tmem_wait_ld();
+          for (int c = 0; c < 4; ++c) {
+            uint32_t u[16];
+            tmem_ld16(lane_base + kColO + hf * 64 + c * 16, u);
+            tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * sc);
-          tmem_st16(lane_base + kColO + c * 16, u);
+            for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * sc);
+            tmem_st16(lane_base + kColO + hf * 64 + c * 16, u);
+          }
+          tmem_wait_st();
         }
-        tmem_wait_st();
       }
       if (need) {
         l *= sc;
         m_used = m_new;
       }
-      // P = 2^(S - m), 16-bit, two keys per column, over the first 64 columns of this S buffer
+      // P = 2^(S - m), 16-bit, two keys per column: this half's keys over
+      // columns [hf*32, hf*32 + 32) of the S buffer
       float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < kBKV / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t u[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -329,24 +347,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           ls[e & 7] += p0 + p1;
           u[e] = Elem<T>::pack(p0, p1);
         }
-        tmem_st16(scol + c * 16, u);
+        if (alive) tmem_st16(scol + hf * 32 + c * 16, u);
       }
       l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      tmem_wait_st();
+      if (alive) tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[j & 1]));
+      if (alive && lane == 0) mbar_arrive(smem_u32(&bars->p_full[j & 1]));
     }
-    // ---- O / l -> output row ----
+    // ---- O / l -> output row (this warp's 64 dims) ----
+    red[(2 * 2 + hf) * kBQ + r] = l;  // row sum over both halves
+    pair_sync();
+    const float lt = l + red[(2 * 2 + (hf ^ 1)) * kBQ + r];
     if (alive) alive = warp_wait_bar(smem_u32(&bars->o_done), (uint32_t)((nb - 1) & 1), a.err, SITE_CHUNK_PIPE);
     if (alive) {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      T* out = static_cast<T*>(a.out) + (size_t)(q0 + r) * a.ld_out + (size_t)hq * kD;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      T* out = static_cast<T*>(a.out) + (size_t)(q0 + r) * a.ld_out + (size_t)hq * kD + hf * 64;
 #pragma unroll 1
-      for (int c = 0; c < kD / 16; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t u[16];
-        tmem_ld16(lane_base + kColO + c * 16, u);
+        tmem_ld16(lane_base + kColO + hf * 64 + c * 16, u);
         tmem_wait_ld();
         uint32_t o[8];
 #pragma unroll
