@@ -111,7 +111,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     bt = a.bt + (size_t)b * a.bt_stride;
     btlen = a.bt_stride;
   } else {
-    const int4 item = reinterpret_cast<const int4*>(a.items)[blockIdx.x];
+    // planned items, KV head fastest, so the launch order is the plan's order
+    // (full key ranges first, the shorter remainders last, for a short drain)
+    const int4 item = reinterpret_cast<const int4*>(a.items)[blockIdx.x / a.kvh];
     b = item.x;
     kbeg = item.y;
     kend = item.z;
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     bt = a.bt + a.bt_off[b];
     btlen = a.bt_len[b];
   }
-  const int kh = blockIdx.y;
+  const int kh = COMPUTED ? (int)blockIdx.y : (int)(blockIdx.x % a.kvh);
   const int G = a.qh / a.kvh;
   const int nblk = (kend - kbeg + kBlockKeys - 1) / kBlockKeys;
 
@@ -364,7 +366,8 @@ int launch_impl(const DecodeAttnArgs& a, const CUtensorMap& tmk, const CUtensorM
     attr = true;
   }
   const int n_ctas = COMPUTED ? a.n_decode * a.max_splits : a.n_items;
-  launch_pdl(decode_attn_kernel<T, D, COMPUTED>, dim3(n_ctas, a.kvh), dim3(kWarps * 32), smem, s, tmk, tmv, a);
+  const dim3 grid = COMPUTED ? dim3(n_ctas, a.kvh) : dim3(n_ctas * a.kvh);
+  launch_pdl(decode_attn_kernel<T, D, COMPUTED>, grid, dim3(kWarps * 32), smem, s, tmk, tmv, a);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "decode attention launch");

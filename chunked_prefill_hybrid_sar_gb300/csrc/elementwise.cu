@@ -1,6 +1,8 @@
-// Row-wise kernels of the hybrid step: RMSNorm, rotary embedding fused with
-// the KV-page append, embedding gather and greedy argmax.  All are HBM-bound
-// and read/write each byte once with 16-byte accesses where the layout allows.
+// Row-wise kernels of the hybrid step: RMSNorm (the step's first one also
+// stacks the input rows or embeds the token ids into the fp32 residual stream,
+// writes the step's rotary table and clears the logits rows), bf16 -> fp32 and
+// weight conversion, greedy argmax.  All are HBM-bound and read/write each
+// byte once with 16-byte accesses where the layout allows.
 #include <float.h>
 
 #include <algorithm>
@@ -50,6 +52,12 @@ struct NormArgs {
   const int32_t* ridx;    // kSrcResidual: optional source row per output row
   float* zero;
   size_t zero_n;
+  // kSrcRows / kSrcTokens, optional: the step's rotary table cs[r][i] =
+  // (cos, sin) of pos[r] * inv_freq[i], i < half_d
+  const int32_t* pos;
+  const double* inv_freq;
+  float2* cs;
+  int half_d;
   int hidden, vocab;
   float eps;
   int* err;
@@ -81,6 +89,19 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
       ok = t >= 0 && t < a.vocab;
       if (!ok && threadIdx.x == 0) report(a.err, SAR_ERR_BOUNDS, SITE_EMBED_BOUNDS, t);
       sr = reinterpret_cast<const uint2*>(static_cast<const T*>(a.table) + (size_t)(ok ? t : 0) * a.hidden);
+    }
+    if (a.cs) {
+      // the angle pos * theta_i is formed and reduced modulo 2*pi in double
+      // precision, so long positions keep fp32 accuracy
+      const double p = (double)a.pos[r];
+      for (int i = threadIdx.x; i < a.half_d; i += kNormThreads) {
+        double ang = p * a.inv_freq[i];
+        const double two_pi = 6.283185307179586476925286766559;
+        ang -= two_pi * rint(ang * (1.0 / two_pi));
+        float sn, cn;
+        sincosf((float)ang, &sn, &cn);
+        a.cs[(size_t)r * a.half_d + i] = make_float2(cn, sn);
+      }
     }
     float4* hr = reinterpret_cast<float4*>(a.h + (size_t)r * a.hidden);
 #pragma unroll
@@ -187,83 +208,6 @@ __global__ void convert_rows_kernel(const __nv_bfloat16* __restrict__ src, T* __
   }
 }
 
-// Rotary embedding of the q and k heads of one row at its absolute position
-// (a chunk keeps numbering from its start position: "maintain an independent
-// position_id for each chunk", SARATHI technique write-up, section 6.1), then
-// the rotated k and the v of that row are written into the row's page slot.
-// Input is the QKV projection in fp32; q, k and v are rounded to the storage
-// type once, after the rotation, and the rotated q and k are also kept in
-// fp32 (in place) for the attention scores.
-// The angle pos * theta_i is formed and reduced modulo 2*pi in double
-// precision once per (row, frequency), so long positions keep fp32 accuracy.
-template <typename T>
-__global__ void rope_append_kernel(RopeArgs a) {
-  pdl_wait();
-  pdl_launch_dependents();
-  __shared__ float cs[64], sn[64];
-  const int r = blockIdx.x;
-  const int pos = a.pos[r];
-  const int slot = a.slot[r];
-  const int half = a.d >> 1;
-  for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    double ang = (double)pos * a.inv_freq[i];
-    const double two_pi = 6.283185307179586476925286766559;
-    ang -= two_pi * rint(ang * (1.0 / two_pi));
-    float s, c;
-    sincosf((float)ang, &s, &c);
-    cs[i] = c;
-    sn[i] = s;
-  }
-  __syncthreads();
-  const int page = slot / a.page_size;
-  const int off = slot - page * a.page_size;
-  const bool slot_ok = slot >= 0 && page < a.num_pages;
-  if (!slot_ok && threadIdx.x == 0) report(a.err, SAR_ERR_BOUNDS, SITE_ROPE_BOUNDS, slot);
-  const int width = (a.qh + 2 * a.kvh) * a.d;
-  T* row = reinterpret_cast<T*>(a.qkv) + (size_t)r * width;
-  float* row32 = a.qkv32 + (size_t)r * width;
-  T* k_cache = reinterpret_cast<T*>(a.k_cache);
-  T* v_cache = reinterpret_cast<T*>(a.v_cache);
-  const int n_pairs = (a.qh + a.kvh) * half;
-  for (int idx = threadIdx.x; idx < n_pairs; idx += blockDim.x) {
-    const int h = idx / half;
-    const int i = idx - h * half;
-    T* base = row + h * a.d;
-    float* base32 = row32 + h * a.d;
-    const float x1 = base32[i];
-    const float x2 = base32[i + half];
-    const float c = cs[i], s = sn[i];
-    const float r1 = x1 * c - x2 * s;
-    const float r2 = x2 * c + x1 * s;
-    base32[i] = r1;
-    base32[i + half] = r2;
-    const T y1 = Elem<T>::from(r1);
-    const T y2 = Elem<T>::from(r2);
-    base[i] = y1;
-    base[i + half] = y2;
-    if (h >= a.qh && slot_ok) {
-      const int kh = h - a.qh;
-      T* kc = k_cache + (((size_t)page * a.kvh + kh) * a.page_size + off) * a.d;
-      kc[i] = y1;
-      kc[i + half] = y2;
-    }
-  }
-  {
-    const float* vrow32 = row32 + (a.qh + a.kvh) * a.d;
-    T* vrow = row + (a.qh + a.kvh) * a.d;
-    const int nv = a.kvh * a.d;
-    for (int idx = threadIdx.x; idx < nv; idx += blockDim.x) {
-      const T v = Elem<T>::from(vrow32[idx]);
-      vrow[idx] = v;
-      if (slot_ok) {
-        const int kh = idx / a.d;
-        const int j = idx - kh * a.d;
-        v_cache[(((size_t)page * a.kvh + kh) * a.page_size + off) * a.d + j] = v;
-      }
-    }
-  }
-}
-
 // Greedy sampling: lowest index among the maxima of each row.
 __global__ void __launch_bounds__(1024) argmax_kernel(const float* __restrict__ logits, int vocab,
                                                      int32_t* __restrict__ out) {
@@ -337,7 +281,8 @@ int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hid
 
 int launch_input_norm(int in_kind, const void* in, const void* table, int vocab, float* h, const float* gain,
                       void* y, int rows, int hidden, float eps, int storage, int* err, cudaStream_t s,
-                      float* zero, size_t zero_n) {
+                      float* zero, size_t zero_n, const int32_t* pos, const double* inv_freq, float2* cs,
+                      int half_d) {
   if (rows <= 0) return SAR_OK;
   if (hidden % 4 || hidden > 4 * kNormThreads * kNormMaxVec)
     return set_error(SAR_ERR_UNSUPPORTED, "rmsnorm: hidden must be a multiple of 4 and at most 8192");
@@ -353,6 +298,10 @@ int launch_input_norm(int in_kind, const void* in, const void* table, int vocab,
   a.err = err;
   a.zero = zero;
   a.zero_n = zero_n;
+  a.pos = pos;
+  a.inv_freq = inv_freq;
+  a.cs = cs;
+  a.half_d = half_d;
   const bool bf = storage == SAR_STORAGE_BF16;
   const dim3 g(rows), b(kNormThreads);
   cudaError_t e;
@@ -400,17 +349,6 @@ int launch_convert_rows(const void* src, void* dst, int rows, int cols, int inte
     launch_pdl(convert_rows_kernel<__half>, dim3(rows), dim3(256), 0, s, sp, static_cast<__half*>(dst), rows, cols, interleave, up);
   count_launches(1);
   return cuda_error(cudaGetLastError(), "convert launch");
-}
-
-int launch_rope_append(const RopeArgs& a, cudaStream_t s) {
-  if (a.M <= 0) return SAR_OK;
-  if (a.d > 128 || a.d % 2) return set_error(SAR_ERR_UNSUPPORTED, "rope: head_dim > 128");
-  if (a.storage == SAR_STORAGE_BF16)
-    launch_pdl(rope_append_kernel<__nv_bfloat16>, dim3(a.M), dim3(256), 0, s, a);
-  else
-    launch_pdl(rope_append_kernel<__half>, dim3(a.M), dim3(256), 0, s, a);
-  count_launches(1);
-  return cuda_error(cudaGetLastError(), "rope launch");
 }
 
 int launch_argmax(const float* logits, int rows, int vocab, int32_t* out, cudaStream_t s) {

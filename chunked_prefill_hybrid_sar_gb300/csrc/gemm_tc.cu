@@ -23,6 +23,15 @@
 // CTA's MMAs released it (the empty barrier counts one multicast commit per
 // CTA).
 //
+// Epilogues: 16-bit store, fp32 store, fp32 residual add (in place, optionally
+// split-K with atomic adds), SwiGLU over 64-row gate/up block pairs, and the
+// fused rotary + KV append of the QKV projection: q and k rotated at their
+// rows' positions (rotate-half pairing, dims i and i + hd/2; "maintain an
+// independent position_id for each chunk", SARATHI technique write-up section
+// 6.1), written in fp32, k and v rounded once and stored into their rows'
+// page slots.  Tiles are head-aligned; in the swap tiling the two halves of a
+// head sit in different warps and meet through shared memory.
+//
 // Tilings: non-swap puts 128 token rows on the MMA M side (msub = 2 stacks two
 // such MMAs on one weight tile for 256-row tiles); swap puts 128 weight rows
 // on the M side and the tokens (padded to 16) on the N side, so a step with
@@ -48,6 +57,7 @@ constexpr int kSmemLimit = 232448;        // 227 KB of dynamic shared memory
 constexpr int kSmemPerSm = 233472;        // 228 KB of shared memory per SM
 constexpr int kBarBytes = 1024;           // barriers + TMEM slot (+ alignment)
 constexpr int kSwapXchg = 64 * 17 * 4;    // swap-mode SwiGLU exchange buffer
+constexpr int kSwapXchgRope = 128 * 17 * 4;  // swap-mode rotary exchange buffer
 constexpr int kPrefetch = 16;             // K-slabs of the weight tile prefetched into L2 ahead
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
@@ -57,6 +67,7 @@ struct Params {
   int bn, m_tiles, n_tiles, k_blocks, stages, stage_bytes, tmem_cols;
   int splits, kb_per_split;  // split-K: `splits` K ranges per tile (residual epilogue only)
   int cl, m_groups;          // cluster size sharing one weight tile (multicast); token-tile groups
+  RopeEpi rope;              // kEpiRope only
   void* c;
   const void* r;
   int* err;
@@ -137,8 +148,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (p.cl > 1) cluster_sync();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();
-  pdl_launch_dependents();
 
   const int rank = p.cl > 1 ? (int)cluster_ctarank() : 0;
   const int cid = blockIdx.x / p.cl, n_clusters = gridDim.x / p.cl;
@@ -146,10 +155,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles_total = p.m_groups * p.n_tiles * p.splits;  // work units per cluster
   const int acc_cols = MSUB * p.bn;
 
+  if (warp == 0 && lane == 0 && cid < n_tiles_total) {
+    // the weights do not depend on the previous kernel: start pulling this
+    // CTA's first weight slabs into L2 while that kernel drains
+    const Unit un = unit_of(p, cid, rank);
+    const void* w_map = SWAP ? (const void*)&tm_a : (const void*)&tm_b;
+    const int slice = PAIR ? p.bn / 2 : p.bn / p.cl;
+    const int w_row = SWAP ? un.nt * 128 : un.nt * p.bn + rank * slice;
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_b);
+    for (int kb = un.kb0; kb < un.kb0 + kPrefetch && kb < un.kb1; ++kb) tma_prefetch_l2(w_map, kb * kBK, w_row);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_desc(&tm_a);
-      tma_prefetch_desc(&tm_b);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -165,8 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // weight rows this CTA fetches: its multicast slice, or its half of the pair's tile
         const int slice = PAIR ? p.bn / 2 : p.bn / p.cl;
         const int w_row = SWAP ? a_row : b_row + rank * slice;
-        // (swap tiling: one CTA per weight tile, no reuse to gain from L2)
-        if (!SWAP)
+        // (swap tiling: one CTA per weight tile, no reuse to gain from L2;
+        // the first unit's first slabs were requested before the wait above)
+        if (!SWAP && t != cid)
           for (int kb = un.kb0; kb < un.kb0 + kPrefetch && kb < un.kb1; ++kb) tma_prefetch_l2(w_map, kb * kBK, w_row);
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (!SWAP && kb + kPrefetch < un.kb1) tma_prefetch_l2(w_map, (kb + kPrefetch) * kBK, w_row);
@@ -268,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int acc = i & 1;
       const uint32_t accph = (uint32_t)((i >> 1) & 1);
       if (alive) alive = warp_wait(smem_u32(&accf_bar[acc]), accph, p.err, SITE_GEMM_EPILOGUE);
-      if (!alive && !(SWAP && EPI == SAR_EPI_SWIGLU)) break;
+      if (!alive && !(SWAP && (EPI == SAR_EPI_SWIGLU || EPI == kEpiRope))) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * acc_cols);
 
@@ -278,7 +300,112 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int row = (mt * MSUB + s) * 128 + lrow;
           const bool row_ok = row < p.M;
           const uint32_t sbase = tbase + (uint32_t)(s * p.bn);
-          if constexpr (EPI == SAR_EPI_SWIGLU) {
+          if constexpr (EPI == kEpiRope) {
+            // head-aligned tile: q and k heads rotated (dim i with i + hd/2),
+            // all written in fp32 to C; k and v also rounded into their page slot
+            const RopeEpi& rp = p.rope;
+            const int half = rp.hd >> 1;
+            float* C = reinterpret_cast<float*>(p.c);
+            int page = -1, off = 0;
+            bool slot_ok = false;
+            if (row_ok) {
+              const int sl = rp.slot[row];
+              page = sl >= 0 ? sl / rp.page_size : -1;
+              off = sl - page * rp.page_size;
+              slot_ok = sl >= 0 && page < rp.num_pages;
+            }
+            const float2* cs = rp.cs + (size_t)(row_ok ? row : 0) * half;
+#pragma unroll 1
+            for (int hh = 0; hh < p.bn / rp.hd; ++hh) {
+              const int col0 = nt * p.bn + hh * rp.hd;  // first column of this head
+              const int head = col0 / rp.hd;
+              if (col0 >= p.N) break;
+              const bool is_v = head >= rp.qh + rp.kvh, is_k = !is_v && head >= rp.qh;
+              T* dst = nullptr;
+              if ((is_k || is_v) && slot_ok) {
+                const int kh = head - rp.qh - (is_v ? rp.kvh : 0);
+                dst = reinterpret_cast<T*>(is_v ? rp.v_cache : rp.k_cache) +
+                      (((size_t)page * rp.kvh + kh) * rp.page_size + off) * rp.hd;
+              }
+              if ((is_k || is_v) && row_ok && !slot_ok && hh == 0)
+                report(p.err, SAR_ERR_BOUNDS, SITE_ROPE_BOUNDS, row);
+              float* crow = C + (size_t)row * p.N + col0;
+              if (is_v) {
+#pragma unroll 1
+                for (int j = 0; j < rp.hd / 16; ++j) {
+                  uint32_t v[16];
+                  tmem_ld16(sbase + hh * rp.hd + j * 16, v);
+                  tmem_wait_ld();
+                  if (!row_ok) continue;
+                  float4* c4 = reinterpret_cast<float4*>(crow + j * 16);
+                  uint32_t o[8];
+#pragma unroll
+                  for (int e = 0; e < 4; ++e)
+                    c4[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                        __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) o[e] = Elem<T>::pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                  if (dst) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + j * 16);
+                    d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                    d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                  }
+                }
+              } else {
+                // the (cos, sin) pairs of the next 16 frequencies are loaded one
+                // chunk ahead, so their L2 latency overlaps this chunk's work
+                const float4* cs4 = reinterpret_cast<const float4*>(cs);
+                float4 cn[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) cn[e] = row_ok ? __ldg(cs4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+                for (int j = 0; j < half / 16; ++j) {
+                  float4 cc[8];
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) cc[e] = cn[e];
+                  if (row_ok && j + 1 < half / 16) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) cn[e] = __ldg(cs4 + (j + 1) * 8 + e);
+                  }
+                  uint32_t x1[16], x2[16];
+                  tmem_ld16(sbase + hh * rp.hd + j * 16, x1);
+                  tmem_ld16(sbase + hh * rp.hd + half + j * 16, x2);
+                  tmem_wait_ld();
+                  if (!row_ok) continue;
+                  float r1[16], r2[16];
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) {
+                    const float4 t4 = cc[e >> 1];
+                    const float tc = (e & 1) ? t4.z : t4.x, ts = (e & 1) ? t4.w : t4.y;
+                    const float a1 = __uint_as_float(x1[e]), a2 = __uint_as_float(x2[e]);
+                    r1[e] = a1 * tc - a2 * ts;
+                    r2[e] = a2 * tc + a1 * ts;
+                  }
+                  float4* c1 = reinterpret_cast<float4*>(crow + j * 16);
+                  float4* c2 = reinterpret_cast<float4*>(crow + half + j * 16);
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    c1[e] = make_float4(r1[4 * e], r1[4 * e + 1], r1[4 * e + 2], r1[4 * e + 3]);
+                    c2[e] = make_float4(r2[4 * e], r2[4 * e + 1], r2[4 * e + 2], r2[4 * e + 3]);
+                  }
+                  if (dst) {
+                    uint32_t o1[8], o2[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                      o1[e] = Elem<T>::pack(r1[2 * e], r1[2 * e + 1]);
+                      o2[e] = Elem<T>::pack(r2[2 * e], r2[2 * e + 1]);
+                    }
+                    uint4* d1 = reinterpret_cast<uint4*>(dst + j * 16);
+                    uint4* d2 = reinterpret_cast<uint4*>(dst + half + j * 16);
+                    d1[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                    d1[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+                    d2[0] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                    d2[1] = make_uint4(o2[4], o2[5], o2[6], o2[7]);
+                  }
+                }
+              }
+            }
+          } else if constexpr (EPI == SAR_EPI_SWIGLU) {
             // packed columns [h*128, h*128+64) gate, [h*128+64, h*128+128) up
             const int F = p.N >> 1;
             T* C = reinterpret_cast<T*>(p.c);
@@ -352,7 +479,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // swap: accumulator lane = weight row, TMEM column = token
         const int tok0 = mt * p.bn;
-        if constexpr (EPI == SAR_EPI_SWIGLU) {
+        if constexpr (EPI == kEpiRope) {
+          // lane = output column n of one or two heads; the rotation partner
+          // (dim i with i + hd/2) is lane ^ hd/2, exchanged through shared memory
+          const RopeEpi& rp = p.rope;
+          const int half = rp.hd >> 1;
+          const int n = nt * 128 + lrow;
+          const int head = n / rp.hd, local = n - head * rp.hd;
+          const bool first = local < half;
+          const int fi = first ? local : local - half;
+          const bool is_v = head >= rp.qh + rp.kvh, is_k = !is_v && head >= rp.qh;
+          const int kh = head - rp.qh - (is_v ? rp.kvh : 0);
+          T* cache = reinterpret_cast<T*>(is_v ? rp.v_cache : rp.k_cache);
+          float* C = reinterpret_cast<float*>(p.c);
+#pragma unroll 1
+          for (int j = 0; j < p.bn / 16; ++j) {
+            uint32_t v[16];
+            if (alive) {
+              tmem_ld16(tbase + j * 16, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) xchg[lrow * 17 + e] = __uint_as_float(v[e]);
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (alive && n < p.N) {
+              const int pl = lrow ^ half;
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int m = tok0 + j * 16 + e;
+                if (m >= p.M) continue;
+                const float x = __uint_as_float(v[e]);
+                float r = x;
+                if (!is_v) {
+                  const float y = xchg[pl * 17 + e];
+                  const float2 t = rp.cs[(size_t)m * half + fi];
+                  r = first ? x * t.x - y * t.y : x * t.x + y * t.y;
+                }
+                C[(size_t)m * p.N + n] = r;
+                if (is_k || is_v) {
+                  const int sl = rp.slot[m];
+                  const int page = sl >= 0 ? sl / rp.page_size : -1;
+                  if (sl >= 0 && page < rp.num_pages)
+                    cache[(((size_t)page * rp.kvh + kh) * rp.page_size + (sl - page * rp.page_size)) * rp.hd + local] =
+                        Elem<T>::from(r);
+                  else if (local == 0)
+                    report(p.err, SAR_ERR_BOUNDS, SITE_ROPE_BOUNDS, m);
+                }
+              }
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+          }
+        } else if constexpr (EPI == SAR_EPI_SWIGLU) {
           // A tile = one packed block pair: lanes 0..63 gate, 64..127 up
           const int F = p.N >> 1;
           const int ocol = nt * 64 + (lrow & 63);
@@ -445,6 +622,7 @@ const void* pick_kernel_t(int epi, bool swap, int msub, bool pair) {
   SAR_PICK(SAR_EPI_RESIDUAL)
   SAR_PICK(SAR_EPI_SWIGLU)
   SAR_PICK(SAR_EPI_F32)
+  SAR_PICK(kEpiRope)
 #undef SAR_PICK
   return nullptr;
 }
@@ -599,7 +777,8 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
   c.m_groups = c.m_tiles / c.cl;
   const int stage_bytes = c.msub * kTileA + (c.pair ? c.bn / 2 : c.bn) * kBK * 2;
   c.stage_bytes = stage_bytes;
-  const int extra = kBarBytes + 1024 + ((c.swap && epi == SAR_EPI_SWIGLU) ? kSwapXchg : 0);
+  const int extra = kBarBytes + 1024 +
+                    (!c.swap ? 0 : epi == SAR_EPI_SWIGLU ? kSwapXchg : epi == kEpiRope ? kSwapXchgRope : 0);
   if (two_ctas && (!c.swap || c.bn > 128))
     return set_error(SAR_ERR_UNSUPPORTED, "gemm: two CTAs per SM only with the swap tiling and M <= 128");
   c.per_sm = two_ctas ? 2 : 1;
@@ -619,12 +798,18 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
 }
 
 int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMap& w_map, int M, int N,
-                int K, int epi, int storage, void* c, const void* residual, int* err, cudaStream_t s) {
+                int K, int epi, int storage, void* c, const void* residual, int* err, cudaStream_t s,
+                const RopeEpi* rope) {
   const void* fn = pick_kernel(storage, epi, cfg.swap != 0, cfg.msub, cfg.pair != 0);
   if (!fn) return set_error(SAR_ERR_INVALID_ARG, "gemm: unknown epilogue");
   if (epi == SAR_EPI_RESIDUAL && residual == nullptr)
     return set_error(SAR_ERR_INVALID_ARG, "gemm: residual epilogue without residual");
+  if (epi == kEpiRope &&
+      (!rope || !rope->slot || !rope->cs || (rope->hd != 64 && rope->hd != 128) || N % 128 ||
+       N != (rope->qh + 2 * rope->kvh) * rope->hd || rope->page_size <= 0))
+    return set_error(SAR_ERR_INVALID_ARG, "gemm: rotary epilogue arguments");
   Params p;
+  if (rope) p.rope = *rope;
   p.M = M;
   p.N = N;
   p.K = K;
@@ -648,7 +833,7 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
       (cfg.swap && cfg.cl != 1) || (cfg.pair && (cfg.cl != 2 || cfg.msub != 1 || cfg.swap)) ||
       cfg.stage_bytes != cfg.msub * kTileA + (cfg.pair ? cfg.bn / 2 : cfg.bn) * kBK * 2)
     return set_error(SAR_ERR_INVALID_ARG, "gemm: inconsistent cluster configuration");
-  static bool attr_done[2][4][2][3][2] = {};
+  static bool attr_done[2][5][2][3][2] = {};
   bool& done = attr_done[storage == SAR_STORAGE_BF16][epi][cfg.swap][cfg.msub][cfg.pair];
   if (!done) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
@@ -676,7 +861,7 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
     lc.numAttrs = 2;
     // persistent grid: as many whole clusters as can be resident at once (the
     // SMs of a GPC need not divide into clusters evenly)
-    static int max_clusters[2][4][3][5][2][2] = {};
+    static int max_clusters[2][5][3][5][2][2] = {};
     int& mc = max_clusters[storage == SAR_STORAGE_BF16][epi][cfg.msub][cfg.cl][cfg.bn == 256][cfg.pair];
     if (mc == 0) {
       cudaLaunchConfig_t qc = lc;  // the cluster shape alone

@@ -80,6 +80,20 @@ inline int weight_box_index(const GemmCfg& c) {
   return rows == 32 ? 0 : rows == 64 ? 1 : rows == 128 ? 2 : 3;
 }
 
+// Epilogue of the fused QKV projection (internal, after the public SAR_EPI_*):
+// C (fp32 [M, (qh + 2 kvh) * hd]) receives q and k rotated at their rows'
+// positions and v as projected; k and v are also rounded once to the storage
+// type and written into their rows' page slots.
+constexpr int kEpiRope = 4;
+struct RopeEpi {
+  const int32_t* pos = nullptr;   // [M] absolute position of each row (unused: the table holds it)
+  const int32_t* slot = nullptr;  // [M] page * page_size + offset
+  const float2* cs = nullptr;     // [M][hd/2] (cos, sin) of pos * theta_i
+  void* k_cache = nullptr;        // layer base [num_pages][kvh][page_size][hd], storage type
+  void* v_cache = nullptr;
+  int qh = 0, kvh = 0, hd = 0, page_size = 0, num_pages = 0;
+};
+
 // Picks a tiling for C[M, .] = A[M, K] . W[N, K]^T (variant = SAR_GEMM_*).
 // Returns SAR_OK or SAR_ERR_UNSUPPORTED.
 // in_place: the residual epilogue writes into its own residual (C == R), which
@@ -88,9 +102,10 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
 
 // Launches with maps already encoded: `act_map` over the activations (rows M),
 // `w_map` over the weights; which one is the MMA's A operand depends on cfg.swap.
+// `rope` is required for (and only read by) kEpiRope.
 int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMap& w_map, int M,
                 int N, int K, int epi, int storage, void* c, const void* residual, int* err,
-                cudaStream_t s);
+                cudaStream_t s, const RopeEpi* rope = nullptr);
 
 // ---- elementwise kernels (elementwise.cu) ----------------------------------
 // x: fp32 residual rows; y: storage-type rows; row_index (optional) gathers rows.
@@ -99,9 +114,12 @@ int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hid
 // The step's first kernel: stacked input rows (bf16 hidden rows, or token ids
 // looked up in `table`) into the fp32 residual stream h and, normalised with
 // `gain`, into y (storage type).  zero (optional): zero_n floats to clear.
+// cs (optional): the step's rotary table [rows][half_d] of (cos, sin) of
+// pos[r] * inv_freq[i], shared by every layer's QKV epilogue.
 int launch_input_norm(int in_kind, const void* in, const void* table, int vocab, float* h, const float* gain,
                       void* y, int rows, int hidden, float eps, int storage, int* err, cudaStream_t s,
-                      float* zero = nullptr, size_t zero_n = 0);
+                      float* zero = nullptr, size_t zero_n = 0, const int32_t* pos = nullptr,
+                      const double* inv_freq = nullptr, float2* cs = nullptr, int half_d = 0);
 int launch_embed(const int32_t* tokens, const void* table, float* out, int rows, int hidden, int vocab,
                  int storage, int* err, cudaStream_t s);
 int launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s);
@@ -109,18 +127,6 @@ int launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s);
 // (up=1) into the 64-row-block gate/up packing.
 int launch_convert_rows(const void* src, void* dst, int rows, int cols, int interleave, int up, int storage,
                         cudaStream_t s);
-struct RopeArgs {
-  float* qkv32;              // [M, (qh + 2 kvh) * d] fp32 projection in; rotated q, k out (in place)
-  void* qkv;                 // [M, (qh + 2 kvh) * d], storage type (written)
-  const int32_t* pos;        // [M]
-  const int32_t* slot;       // [M] page * page_size + offset
-  const double* inv_freq;    // [d/2]
-  void* k_cache;             // layer base [num_pages][kvh][page][d], storage type
-  void* v_cache;
-  int M, qh, kvh, d, page_size, num_pages, storage;
-  int* err;
-};
-int launch_rope_append(const RopeArgs& a, cudaStream_t s);
 int launch_argmax(const float* logits, int rows, int vocab, int32_t* out, cudaStream_t s);
 
 // ---- attention (attn_decode.cu, attn_chunk.cu) -----------------------------

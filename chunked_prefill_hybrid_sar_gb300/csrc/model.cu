@@ -62,9 +62,10 @@ struct sar_model {
   double* inv_freq = nullptr;
   // workspace
   uint8_t* ws = nullptr;
-  st16 *xn = nullptr, *qkv = nullptr, *attn = nullptr, *act = nullptr, *hrows = nullptr;
+  st16 *xn = nullptr, *attn = nullptr, *act = nullptr, *hrows = nullptr;
+  float2* rope_cs = nullptr;  // [max_tokens][head_dim / 2] (cos, sin) of this step's positions
   float* hres = nullptr;   // residual stream, fp32
-  float* qkv32 = nullptr;  // QKV projection in fp32 (rotated q, k after the rotary kernel)
+  float* qkv32 = nullptr;  // QKV projection in fp32, q and k rotated by the projection's epilogue
   void* in_stage = nullptr;
   float* partials = nullptr;
   size_t partials_cap = 0;  // floats
@@ -137,13 +138,13 @@ int weight_maps(WMaps& maps, const void* w, int rows, int cols, int storage) {
 
 // GEMM over `rows` activation rows with the weight maps of one matrix.
 int run_gemm(sar_model* m, const st16* a, int rows, const WMaps& wmaps, int N, int K, int epi,
-             void* c, const void* r, cudaStream_t s) {
+             void* c, const void* r, cudaStream_t s, const sar::RopeEpi* rope = nullptr) {
   sar::GemmCfg cfg;
   SAR_TRY(sar::gemm_config(rows, N, K, epi, SAR_GEMM_AUTO, &cfg, c == r));
   CUtensorMap amap;
   SAR_TRY(sar::make_tmap_16(&amap, a, rows, K, cfg.swap ? cfg.b_box_rows : cfg.a_box_rows, m->d.storage));
   const CUtensorMap& wm = wmaps[sar::weight_box_index(cfg)];
-  return sar::gemm_launch(cfg, amap, wm, rows, N, K, epi, m->d.storage, c, r, m->err, s);
+  return sar::gemm_launch(cfg, amap, wm, rows, N, K, epi, m->d.storage, c, r, m->err, s, rope);
 }
 
 // ---- step planning -----------------------------------------------------------
@@ -184,10 +185,12 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
     SAR_TRY(check_bt(dc.block_table, dc.n_blocks, dc.ctx_len));
     total_keys += dc.ctx_len + 1;
   }
-  // decode work split: key ranges of `split` keys, enough CTAs to fill the GPU
+  // decode work split: key ranges of `split` keys, about four CTAs (two per
+  // resident slot) per SM; fewer, longer ranges measured faster than more,
+  // shorter ones (less set-up and merging per key), up to 2048 keys
   const int sms = sar::num_sms();
-  int64_t split = (total_keys * d.n_kv_heads) / (8LL * sms);
-  split = std::max<int64_t>(128, std::min<int64_t>(1024, (split + 15) / 16 * 16));
+  int64_t split = (total_keys * d.n_kv_heads) / (4LL * sms);
+  split = std::max<int64_t>(128, std::min<int64_t>(2048, (split + 15) / 16 * 16));
   std::vector<int32_t> items, pbeg(Bd, -1), pcnt(Bd, 0), nkeys(Bd), btoff(Bd), btlen(Bd), bt;
   std::vector<int32_t> tail_items;
   int n_parts = 0;
@@ -212,7 +215,15 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
     }
     if (ns > 1) n_parts += ns;
   }
-  items.insert(items.end(), tail_items.begin(), tail_items.end());
+  // remainders longest first, after every full range
+  {
+    std::vector<int> order(tail_items.size() / 4);
+    for (size_t t = 0; t < order.size(); ++t) order[t] = (int)t;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+      return tail_items[4 * x + 2] - tail_items[4 * x + 1] > tail_items[4 * y + 2] - tail_items[4 * y + 1];
+    });
+    for (int t : order) items.insert(items.end(), tail_items.begin() + 4 * t, tail_items.begin() + 4 * t + 4);
+  }
   // rows whose logits are returned: the chunk's last row, then every decode row
   std::vector<int32_t> rows;
   if (Lp > 0) rows.push_back(Lp - 1);
@@ -333,36 +344,30 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
       // the logits rows, which the LM head GEMM adds its K ranges into
       Prof pr(m, SAR_K_EMBED, s);
       SAR_TRY(sar::launch_input_norm(b->in_kind, in, m->embed, d.vocab, h, w.n1, m->xn, M, H, d.rms_eps, d.storage,
-                                     m->err, s, logits, logits ? (size_t)p.R * d.vocab : 0));
+                                     m->err, s, logits, logits ? (size_t)p.R * d.vocab : 0, md + p.o_pos,
+                                     m->inv_freq, m->rope_cs, d.head_dim / 2));
     } else {
       Prof pr(m, SAR_K_RMSNORM, s);
       SAR_TRY(sar::launch_rmsnorm(h, w.n1, m->xn, M, H, d.rms_eps, nullptr, d.storage, s));
     }
-    {
-      Prof pr(m, SAR_K_GEMM_QKV, s);
-      SAR_TRY(run_gemm(m, m->xn, M, w.m_qkv, m->qkv_n, H, SAR_EPI_F32, m->qkv32, nullptr, s));
-    }
     uint16_t* kc = kv->k + (size_t)l * kv->layer_elems;
     uint16_t* vc = kv->v + (size_t)l * kv->layer_elems;
     {
-      Prof pr(m, SAR_K_ROPE_APPEND, s);
-      sar::RopeArgs ra;
-      ra.qkv32 = m->qkv32;
-      ra.qkv = m->qkv;
-      ra.pos = md + p.o_pos;
-      ra.slot = md + p.o_slot;
-      ra.inv_freq = m->inv_freq;
-      ra.k_cache = kc;
-      ra.v_cache = vc;
-      ra.M = M;
-      ra.qh = d.n_q_heads;
-      ra.kvh = d.n_kv_heads;
-      ra.d = d.head_dim;
-      ra.page_size = kv->page_size;
-      ra.num_pages = kv->num_pages;
-      ra.storage = d.storage;
-      ra.err = m->err;
-      SAR_TRY(sar::launch_rope_append(ra, s));
+      // a2 + a3: the projection's epilogue rotates q and k at the rows'
+      // positions and appends k and v into their page slots
+      Prof pr(m, SAR_K_GEMM_QKV, s);
+      sar::RopeEpi rp;
+      rp.pos = md + p.o_pos;
+      rp.slot = md + p.o_slot;
+      rp.cs = m->rope_cs;
+      rp.k_cache = kc;
+      rp.v_cache = vc;
+      rp.qh = d.n_q_heads;
+      rp.kvh = d.n_kv_heads;
+      rp.hd = d.head_dim;
+      rp.page_size = kv->page_size;
+      rp.num_pages = kv->num_pages;
+      SAR_TRY(run_gemm(m, m->xn, M, w.m_qkv, m->qkv_n, H, sar::kEpiRope, m->qkv32, nullptr, s, &rp));
     }
     if (p.Lp > 0) {
       Prof pr(m, SAR_K_CHUNK_ATTN, s);
@@ -393,7 +398,7 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
     if (p.Bd > 0) {
       Prof pr(m, SAR_K_DECODE_ATTN, s);
       sar::DecodeAttnArgs da;
-      da.qkv = m->qkv + (size_t)p.Lp * m->qkv_n;  // zero-copy row split
+      da.qkv = nullptr;  // the fp32 query rows below are read instead
       da.out = m->attn + (size_t)p.Lp * m->qd;
       da.storage = d.storage;
       da.q32 = m->qkv32 + (size_t)p.Lp * m->qkv_n;
@@ -506,7 +511,7 @@ int sar_model_create(const sar_dims* dims, sar_model** out) {
   // step workspace
   const size_t T = d.max_tokens;
   const size_t R = (size_t)d.max_decodes + 1;
-  const size_t ws = align256(T * H * 2) + align256(T * m->qkv_n * 2) + align256(T * m->qd * 2) + align256(T * F * 2) +
+  const size_t ws = align256(T * H * 2) + align256(T * (d.head_dim / 2) * 8) + align256(T * m->qd * 2) + align256(T * F * 2) +
                     align256(T * H * 4) + align256(R * H * 2) + align256(T * H * 2) + align256(T * m->qkv_n * 4) + 256;
   e = cudaMalloc(&m->ws, ws);
   if (e == cudaSuccess) e = cudaMalloc(&m->err, 16);
@@ -518,7 +523,7 @@ int sar_model_create(const sar_dims* dims, sar_model** out) {
   }
   p = m->ws;
   m->xn = take(T * H * 2);
-  m->qkv = take(T * m->qkv_n * 2);
+  m->rope_cs = reinterpret_cast<float2*>(takef(T * (d.head_dim / 2) * 8));
   m->attn = take(T * m->qd * 2);
   m->act = take(T * F * 2);
   m->hres = takef(T * H * 4);
@@ -738,7 +743,7 @@ int sar_model_debug_buffer(sar_model* m, int32_t which, void** out) {
   if (!m || !out) return set_error(SAR_ERR_INVALID_ARG, "debug_buffer: null argument");
   switch (which) {
     case 0: *out = m->xn; break;
-    case 1: *out = m->qkv; break;
+    case 1: *out = m->rope_cs; break;
     case 2: *out = m->attn; break;
     case 3: *out = m->act; break;
     case 4: *out = m->hres; break;

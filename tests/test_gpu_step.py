@@ -114,7 +114,8 @@ def test_tiny_intermediates_first_step(tiny):
     M = 260
     # the normed-rows buffer holds the second norm (ahead of the FFN) after the step
     assert_close(debug_tensor(m, 0, M, dims.hidden).float().cpu(), y2, what="rmsnorm before FFN")
-    assert_close(debug_tensor(m, 1, M, 3 * dims.hidden).float().cpu(), qkv, what="qkv+rope")
+    qkv32 = harness.wrap(m.debug_buffer(5), M * 3 * dims.hidden, torch.float32).view(M, 3 * dims.hidden)
+    assert_close(qkv32.cpu(), qkv, what="qkv+rope")
     got_attn = debug_tensor(m, 2, M, dims.hidden).float().cpu().numpy()
     assert_close(got_attn[:256], attn[:256], what="chunk attention")
     assert_close(got_attn[256:], attn[256:], what="decode attention")

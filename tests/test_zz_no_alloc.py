@@ -44,7 +44,9 @@ def test_noalloc_decode_attention_matches_the_step_twice():
     dt = sar.storage_dtype(m.storage)
     # the step's own decode-attention rows (it split and merged them through its workspace)
     ref = harness.wrap(m.debug_buffer(2), n * dims.q_dim, dt).view(n, dims.q_dim).clone()
-    q_ptr = m.debug_buffer(1)  # rotated q|k|v rows of the same step
+    # rotated q|k|v rows of the same step (kept in fp32), in the storage type
+    qkv_rows = harness.wrap(m.debug_buffer(5), n * qkv_n, torch.float32).view(n, qkv_n).to(dt).contiguous()
+    q_ptr = qkv_rows.data_ptr()
     ctx_dev = torch.tensor(ctxs, dtype=torch.int32, device="cuda")
     bt_dev = torch.zeros(n, stride, dtype=torch.int32, device="cuda")
     for i, bt in enumerate(tables):
