@@ -144,6 +144,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int last_run = (n_keys - 1) / kRun;
       bool ok = (n_keys - 1) / a.page_size < a.bt_len;
       if (!ok && is_k) report(a.err, SAR_ERR_BOUNDS, SITE_CHUNK_BOUNDS, n_keys);
+      // the page of every 16-key run of a block, read from the block table one
+      // block ahead (all eight loads in flight together, not one per box);
+      // runs past the last key repeat the last one (finite data, masked)
+      int pg[kRunsPerBlock], po[kRunsPerBlock];
+      auto pages_of = [&](int j) {
+#pragma unroll
+        for (int g = 0; g < kRunsPerBlock; ++g) {
+          const int key = min(j * kRunsPerBlock + g, last_run) * kRun;
+          const int bi = key / a.page_size;
+          pg[g] = a.bt[bi];
+          po[g] = key - bi * a.page_size;
+        }
+      };
+      if (ok) pages_of(0);
       for (int j = 0; j < nb && ok; ++j) {
         const int s = j % kStages;
         if (!mbar_wait(smem_u32(&empty[s]), (uint32_t)(((j / kStages) & 1) ^ 1), a.err, SITE_CHUNK_PIPE)) {
@@ -153,20 +167,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t fb = smem_u32(&full[s]);
         const uint32_t dst = is_k ? k_reg(s) : v_reg(s);
         mbar_expect_tx(fb, (uint32_t)kKVBytes);
-#pragma unroll 1
+#pragma unroll
         for (int g = 0; g < kRunsPerBlock; ++g) {
-          // runs past the last key repeat the last one (finite data, masked)
-          const int key = min(j * kRunsPerBlock + g, last_run) * kRun;
-          const int bi = key / a.page_size;
-          int page = a.bt[bi];
+          int page = pg[g];
           if (page < 0 || page >= a.num_pages) {
             report(a.err, SAR_ERR_BOUNDS, SITE_CHUNK_BOUNDS, page);
             page = 0;
           }
-          const int row = (page * a.kvh + kh) * a.page_size + (key - bi * a.page_size);
+          const int row = (page * a.kvh + kh) * a.page_size + po[g];
           tma_load_2d(dst + g * (kRun * 128), map, 0, row, fb);
           tma_load_2d(dst + kRegion + g * (kRun * 128), map, 64, row, fb);
         }
+        if (j + 1 < nb) pages_of(j + 1);
       }
       // no copy may still be in flight when the CTA leaves
       const int first = max(0, nb - kStages);

@@ -134,10 +134,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   __syncwarp();
 
   // Issue block `j` of this CTA's range into stage s (lane 0 only).
-  auto issue = [&](int j, int s) -> bool {
+  // Page of this CTA's block j (-1 past the block table).
+  auto page_of = [&](int j) -> int {
+    const int bi = (kbeg + j * kBlockKeys) / a.page_size;
+    return (bi < btlen) ? bt[bi] : -1;
+  };
+  // Issue block `j` (its page looked up beforehand) into stage s (lane 0 only).
+  auto issue = [&](int j, int s, int page) -> bool {
     const int key0 = kbeg + j * kBlockKeys;
     const int bi = key0 / a.page_size;
-    const int page = (bi < btlen) ? bt[bi] : -1;
     if (page < 0 || page >= a.num_pages) {
       report(a.err, SAR_ERR_BOUNDS, SITE_DECODE_BOUNDS, key0);
       return false;
@@ -155,15 +160,24 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     return true;
   };
 
-  // first pages in flight before the query loads, so their latencies overlap
+  // first pages in flight before the query loads, so their latencies overlap;
+  // the block-table entry of the next block to issue is read one block ahead
   const int my_n = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
   bool ok = true;
   int issued = 0, consumed = 0;
+  int next_page = -1;
   if (lane == 0) {
-    for (int i = 0; i < kStages && i < my_n && ok; ++i) {
-      ok = issue(warp + i * kWarps, i);
-      if (ok) ++issued;
+    int first[kStages];
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) first[i] = i < my_n ? page_of(warp + i * kWarps) : -1;
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) {
+      if (i < my_n && ok) {
+        ok = issue(warp + i * kWarps, i, first[i]);
+        if (ok) ++issued;
+      }
     }
+    if (kStages < my_n) next_page = page_of(warp + kStages * kWarps);
   }
   ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 
@@ -266,8 +280,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     if (i + kStages < my_n) {
       int r = 1;
       if (lane == 0) {
-        r = issue(warp + (i + kStages) * kWarps, s) ? 1 : 0;
+        r = issue(warp + (i + kStages) * kWarps, s, next_page) ? 1 : 0;
         issued += r;
+        if (i + kStages + 1 < my_n) next_page = page_of(warp + (i + kStages + 1) * kWarps);
       }
       if (!__shfl_sync(0xffffffffu, r, 0)) ok = false;
     }
@@ -342,14 +357,29 @@ __global__ void decode_combine_kernel(DecodeAttnArgs a) {
   }
   if (cnt <= 1) return;
   const int dd = threadIdx.x;
-  float M = -INFINITY;
-  for (int i = 0; i < cnt; ++i) M = fmaxf(M, a.partials[((size_t)(p0 + i) * a.qh + hq) * (D + 2) + D]);
-  float L = 0.f, A = 0.f;
-  for (int i = 0; i < cnt; ++i) {
-    const float* pp = a.partials + ((size_t)(p0 + i) * a.qh + hq) * (D + 2);
-    const float sc = exp2f(pp[D] - M);
-    L = fmaf(pp[D + 1], sc, L);
-    A = fmaf(pp[dd], sc, A);
+  // partials four at a time, their loads in flight together, merged online
+  float M = -INFINITY, L = 0.f, A = 0.f;
+  for (int i0 = 0; i0 < cnt; i0 += 4) {
+    float pm[4], pl[4], pa[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool v = i0 + u < cnt;
+      const float* pp = a.partials + ((size_t)(p0 + (v ? i0 + u : 0)) * a.qh + hq) * (D + 2);
+      pm[u] = v ? pp[D] : -INFINITY;
+      pl[u] = v ? pp[D + 1] : 0.f;
+      pa[u] = v ? pp[dd] : 0.f;
+    }
+    const float mn = fmaxf(fmaxf(M, fmaxf(pm[0], pm[1])), fmaxf(pm[2], pm[3]));
+    const float rs = M == -INFINITY ? 0.f : exp2f(M - mn);
+    L *= rs;
+    A *= rs;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float sc = pm[u] == -INFINITY ? 0.f : exp2f(pm[u] - mn);
+      L = fmaf(pl[u], sc, L);
+      A = fmaf(pa[u], sc, A);
+    }
+    M = mn;
   }
   static_cast<T*>(a.out)[(size_t)b * a.ld_out + (size_t)hq * D + dd] = Elem<T>::from(A / L);
 }
