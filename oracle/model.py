@@ -14,8 +14,8 @@ Appendix table of evaluated models):
 * SwiGLU FFN ``(silu(y Wg^T) * (y Wu^T)) Wd^T``; residual adds after attention
   and after the FFN.
 
-Parity status: rms_norm, apply_rope, silu, attention, decoder_layer and the
-hybrid step are pinned by ``tests/test_oracle_*.py`` (closed forms, library
+Parity status: rms_norm, apply_rope, silu, attention (full causal and
+sliding-window), decoder_layer and the hybrid step are pinned by ``tests/test_oracle_*.py`` (closed forms, library
 special cases, brute force, chunked == one-shot, hybrid == serial).  The
 absolute hidden values of a random-initialised model have no printed worked
 example and are otherwise parity unpinned.
@@ -78,13 +78,19 @@ def silu(x: np.ndarray) -> np.ndarray:
     return x / (1.0 + np.exp(-x))
 
 
-def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos, k_pos) -> np.ndarray:
-    """Causal grouped-query attention.
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos, k_pos, window: int = 0) -> np.ndarray:
+    """Causal grouped-query attention, optionally over a sliding window.
 
     ``q[T, qh, d]``, ``k, v[S, kvh, d]``; query ``t`` attends to key ``s`` iff
     ``k_pos[s] <= q_pos[t]`` (the causal mask whose correctness across chunks
-    the *SARATHI technique write-up* §6.1 asks to check).  Query head ``h``
-    reads KV head ``h // (qh // kvh)``.  Scale ``1/sqrt(d)``, softmax over keys.
+    the *SARATHI technique write-up* §6.1 asks to check) and, when
+    ``window > 0``, also ``k_pos[s] > q_pos[t] - window``: the query sees the
+    ``window`` most recent positions, itself included.  The pages list
+    Mistral-7B's attention as GQA with a sliding window (*Sarathi-Serve
+    digest*, Appendix table of evaluated models) without stating the window or
+    its edge; this "W latest keys, self included" edge is the reading taken.
+    Query head ``h`` reads KV head ``h // (qh // kvh)``.  Scale ``1/sqrt(d)``,
+    softmax over the visible keys.
     """
     T, qh, d = q.shape
     S, kvh, _ = k.shape
@@ -92,6 +98,8 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos, k_pos) -> np.n
     q_pos = np.asarray(q_pos)
     k_pos = np.asarray(k_pos)
     visible = k_pos[None, :] <= q_pos[:, None]
+    if window > 0:
+        visible &= k_pos[None, :] > q_pos[:, None] - window
     out = np.empty_like(q)
     scale = 1.0 / np.sqrt(d)
     for h in range(qh):
@@ -103,6 +111,11 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos, k_pos) -> np.n
         p = p / p.sum(axis=1, keepdims=True)
         out[:, h, :] = p @ v[:, kh, :]
     return out
+
+
+def window_of(dims) -> int:
+    """The model's sliding window (0 = full causal attention)."""
+    return int(getattr(dims, "sliding_window", 0) or 0)
 
 
 @dataclasses.dataclass
@@ -157,7 +170,7 @@ def decoder_layer(x: np.ndarray, pos, w: dict, dims, cache: LayerCache) -> tuple
     K = np.concatenate([cache.k, k.astype(cache.k.dtype)], axis=0)
     V = np.concatenate([cache.v, v.astype(cache.v.dtype)], axis=0)
     k_pos = np.arange(K.shape[0])
-    a = attention(q, K, V, pos, k_pos).reshape(x.shape[0], dims.q_dim)
+    a = attention(q, K, V, pos, k_pos, window_of(dims)).reshape(x.shape[0], dims.q_dim)
     return post_attention(x, a, w, dims), LayerCache(K, V)
 
 
@@ -292,7 +305,7 @@ def hybrid_step(layers, head, dims, parts: list) -> tuple:
             c = caches[i][l]
             K = np.concatenate([c.k, k[r0:r1].astype(c.k.dtype)], axis=0)
             V = np.concatenate([c.v, v[r0:r1].astype(c.v.dtype)], axis=0)
-            a[r0:r1] = attention(q[r0:r1], K, V, pos[r0:r1], np.arange(K.shape[0]))
+            a[r0:r1] = attention(q[r0:r1], K, V, pos[r0:r1], np.arange(K.shape[0]), window_of(dims))
         h = post_attention(h, a.reshape(h.shape[0], dims.q_dim), w, dims)
         hidden.append(h)
     logits = None

@@ -41,6 +41,8 @@ class Dims:
     vocab: int = 0
     rms_eps: float = 1e-5
     rope_base: float = 10000.0
+    # keys a query may see, itself included (0 = the whole causal prefix)
+    sliding_window: int = 0
 
     @property
     def q_dim(self) -> int:

@@ -96,8 +96,10 @@ def test_silu_matches_torch_library():
 
 # ---------------------------------------------------------------- attention
 
-def brute_attention(q, k, v, q_pos, k_pos):
-    """Triple loop in float64: softmax over visible keys, one query/head at a time."""
+def brute_attention(q, k, v, q_pos, k_pos, window=0):
+    """Triple loop in float64: softmax over visible keys, one query/head at a time.
+    A key is visible when its distance back from the query, ``q_pos - k_pos``,
+    is in ``[0, window)`` (any non-negative distance when ``window`` is 0)."""
     T, qh, d = q.shape
     S, kvh, _ = k.shape
     g = qh // kvh
@@ -107,7 +109,8 @@ def brute_attention(q, k, v, q_pos, k_pos):
             kh = h // g
             sc = []
             for s in range(S):
-                if k_pos[s] <= q_pos[t]:
+                dist = q_pos[t] - k_pos[s]
+                if dist >= 0 and (window == 0 or dist < window):
                     sc.append((s, sum(q[t, h, i] * k[s, kh, i] for i in range(d)) / math.sqrt(d)))
             m = max(v_ for _, v_ in sc)
             den = sum(math.exp(v_ - m) for _, v_ in sc)
@@ -158,6 +161,123 @@ def test_decode_row_equals_library_attention_over_full_history():
     ref = F.scaled_dot_product_attention(tq, tk, tv).permute(1, 0, 2).numpy()
     out = om.attention(q, k, v, [ctx], np.arange(ctx + 1))
     np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- sliding window
+
+
+def test_window_one_sees_only_its_own_key():
+    # closed form: with one visible key the softmax is 1 there, the output is that value
+    rng = np.random.default_rng(21)
+    T, S, qh, kvh, d = 5, 12, 4, 2, 8
+    q = rng.standard_normal((T, qh, d))
+    k = rng.standard_normal((S, kvh, d))
+    v = rng.standard_normal((S, kvh, d))
+    q_pos = np.arange(7, 12)
+    out = om.attention(q, k, v, q_pos, np.arange(S), window=1)
+    for t in range(T):
+        for h in range(qh):
+            np.testing.assert_allclose(out[t, h], v[q_pos[t], h // (qh // kvh)], rtol=0, atol=1e-15)
+
+
+def test_window_two_is_a_two_key_softmax():
+    # closed form: the query mixes its own value and the previous one by sigmoid weights
+    rng = np.random.default_rng(22)
+    d = 16
+    q = rng.standard_normal((1, 1, d))
+    k = rng.standard_normal((9, 1, d))
+    v = rng.standard_normal((9, 1, d))
+    out = om.attention(q, k, v, [8], np.arange(9), window=2)
+    s7 = q[0, 0] @ k[7, 0] / math.sqrt(d)
+    s8 = q[0, 0] @ k[8, 0] / math.sqrt(d)
+    w8 = 1.0 / (1.0 + math.exp(s7 - s8))
+    np.testing.assert_allclose(out[0, 0], w8 * v[8, 0] + (1 - w8) * v[7, 0], rtol=1e-13, atol=1e-14)
+
+
+def test_window_covering_the_prefix_is_full_causal():
+    rng = np.random.default_rng(23)
+    T, S, qh, kvh, d = 6, 20, 4, 2, 8
+    q = rng.standard_normal((T, qh, d))
+    k = rng.standard_normal((S, kvh, d))
+    v = rng.standard_normal((S, kvh, d))
+    q_pos = np.arange(14, 20)
+    full = om.attention(q, k, v, q_pos, np.arange(S))
+    for w in (20, 21, 1000):
+        np.testing.assert_array_equal(om.attention(q, k, v, q_pos, np.arange(S), window=w), full)
+    assert np.abs(om.attention(q, k, v, q_pos, np.arange(S), window=19) - full).max() > 1e-6
+
+
+@pytest.mark.parametrize("window", [1, 3, 5, 9])
+def test_window_matches_brute_force(window):
+    rng = np.random.default_rng(24)
+    d, S, T, qh, kvh = 8, 13, 5, 6, 2
+    q = rng.standard_normal((T, qh, d))
+    k = rng.standard_normal((S, kvh, d))
+    v = rng.standard_normal((S, kvh, d))
+    q_pos = np.arange(8, 13)
+    np.testing.assert_allclose(om.attention(q, k, v, q_pos, np.arange(S), window=window),
+                               brute_attention(q, k, v, q_pos, np.arange(S), window), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("window", [4, 16, 31])
+def test_window_matches_torch_sdpa_band_mask(window):
+    # the library's attention with an explicit band mask (i - j in [0, window))
+    rng = np.random.default_rng(25)
+    T, d, qh, kvh = 40, 16, 8, 2
+    q = rng.standard_normal((T, qh, d))
+    k = rng.standard_normal((T, kvh, d))
+    v = rng.standard_normal((T, kvh, d))
+    i = torch.arange(T)[:, None]
+    j = torch.arange(T)[None, :]
+    band = (i - j >= 0) & (i - j < window)
+    tq = torch.from_numpy(q).permute(1, 0, 2)
+    tk = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(qh // kvh, dim=0)
+    tv = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(qh // kvh, dim=0)
+    ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=band).permute(1, 0, 2).numpy()
+    out = om.attention(q, k, v, np.arange(T), np.arange(T), window=window)
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_window_off_by_one_is_caught():
+    # a window that admits one key too many (>= instead of >) disagrees with the band reference
+    rng = np.random.default_rng(26)
+    T, d = 12, 8
+    q = rng.standard_normal((T, 1, d))
+    k = rng.standard_normal((T, 1, d))
+    v = rng.standard_normal((T, 1, d))
+    ref = brute_attention(q, k, v, np.arange(T), np.arange(T), 4)
+    wide = brute_attention(q, k, v, np.arange(T), np.arange(T), 5)
+    np.testing.assert_allclose(om.attention(q, k, v, np.arange(T), np.arange(T), window=4), ref,
+                               rtol=1e-10, atol=1e-12)
+    assert np.abs(wide - ref).max() > 1e-3
+
+
+@pytest.mark.parametrize("window", [5, 16, 40])
+def test_windowed_chunked_prefill_equals_one_shot(window):
+    import dataclasses
+    dims = dataclasses.replace(small_dims(layers=2), sliding_window=window)
+    layers, _, gen = np_layers(27, dims)
+    x = synth.normal(gen, (64, dims.hidden)).double().numpy()
+    one, _ = om.forward(layers, dims, x)
+    full, _ = om.forward(layers, small_dims(layers=2), x)
+    assert np.abs(one[-1] - full[-1]).max() > 1e-6  # the window changes the result
+    for chunk in (8, 24, 48):
+        ch, _ = om.chunked_prefill(layers, dims, x, chunk)
+        for a, b in zip(ch, one):
+            np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-11)
+
+
+@pytest.mark.parametrize("with_given", [False, True])
+def test_windowed_hybrid_batch_equals_serial_execution(with_given):
+    import dataclasses
+    dims = dataclasses.replace(small_dims(layers=2), sliding_window=7)
+    layers, head, gen = np_layers(28, dims)
+    parts = _parts_for(dims, layers, gen, with_given)
+    hyb, lh = om.hybrid_step(layers, head, dims, parts)
+    ser, ls = om.serial_step(layers, head, dims, parts)
+    for a, b in zip(hyb, ser):
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(lh, ls, rtol=1e-10, atol=1e-11)
 
 
 # ---------------------------------------------------------------- whole layer
