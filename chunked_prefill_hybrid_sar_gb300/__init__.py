@@ -90,7 +90,7 @@ class Model:
         self.storage = storage
         d = _lib.sar_dims(dims.n_layers, dims.hidden, dims.n_q_heads, dims.n_kv_heads, dims.head_dim,
                           dims.ffn, dims.vocab, dims.rms_eps, dims.rope_base, max_tokens, max_decodes,
-                          storage)
+                          storage, getattr(dims, "sliding_window", 0))
         h = ctypes.c_void_p()
         check(lib().sar_model_create(ctypes.byref(d), ctypes.byref(h)))
         self.h = h

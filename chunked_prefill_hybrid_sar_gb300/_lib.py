@@ -46,7 +46,7 @@ class sar_dims(ctypes.Structure):
     _fields_ = [("n_layers", i32), ("hidden", i32), ("n_q_heads", i32), ("n_kv_heads", i32),
                 ("head_dim", i32), ("ffn", i32), ("vocab", i32), ("rms_eps", ctypes.c_float),
                 ("rope_base", ctypes.c_float), ("max_tokens", i32), ("max_decodes", i32),
-                ("storage", i32)]
+                ("storage", i32), ("sliding_window", i32)]
 
 
 class sar_layer_weights(ctypes.Structure):

@@ -12,7 +12,9 @@
 // one query head (16 per warp); K/V
 // tiles of 64 keys are gathered page by page with 16-byte cp.async into an
 // XOR-swizzled shared layout (conflict-free ldmatrix), double buffered.
-// Keys past the causal limit are zero-filled and masked.
+// Keys past the causal limit are zero-filled and masked.  With a sliding
+// window of W keys the CTA starts at the tile holding its first row's oldest
+// visible key and masks, per row, the keys at or before (position - W).
 #include <float.h>
 
 #include "common.cuh"
@@ -80,6 +82,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
   const int nq = min(kBQ, a.len - q0);
   const int last_pos = a.start_pos + q0 + nq - 1;        // latest query position in this CTA
   const int n_tiles = last_pos / kBKV + 1;
+  const int t0 = a.window > 0 ? max(0, a.start_pos + q0 - a.window + 1) / kBKV : 0;  // first tile in any window
   const uint32_t sq_u = smem_u32(sq), skv_u = smem_u32(skv);
   const uint32_t sql_u = sq_u + kBQ * D * 2;
 
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
       cp_async16(vbase + swz<D>(r, ch), vs, ok ? 16 : 0);
     }
   };
-  load_kv(0, 0);
+  load_kv(t0, t0 & 1);
   cp_async_commit();
 
   const float sl2 = rsqrtf((float)D) * 1.4426950408889634f;
@@ -136,8 +139,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
   const int r_lo = warp * 16 + (lane >> 2);  // this thread's two query rows in the tile
   const int qpos0 = a.start_pos + q0 + r_lo;
   const int qpos1 = qpos0 + 8;
+  // oldest visible key of each row (keys below it are masked)
+  const int klo0 = a.window > 0 ? qpos0 - a.window + 1 : 0;
+  const int klo1 = a.window > 0 ? qpos1 - a.window + 1 : 0;
 
-  for (int t = 0; t < n_tiles; ++t) {
+  for (int t = t0; t < n_tiles; ++t) {
     if (t + 1 < n_tiles) load_kv(t + 1, (t + 1) & 1);
     cp_async_commit();
     cp_async_wait<1>();
@@ -168,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
         mma16816<T>(s[j], ql1[0], ql1[1], ql1[2], ql1[3], b2, b3);
       }
     }
-    // ---- causal mask + online softmax (base 2) ----
+    // ---- causal (and window) mask + online softmax (base 2) ----
     const int kpos0 = t * kBKV + 2 * (lane & 3);
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -176,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int kp = kpos0 + j * 8 + e;
-        s[j][e] = kp <= qpos0 ? s[j][e] * sl2 : -INFINITY;
-        s[j][2 + e] = kp <= qpos1 ? s[j][2 + e] * sl2 : -INFINITY;
+        s[j][e] = (kp <= qpos0 && kp >= klo0) ? s[j][e] * sl2 : -INFINITY;
+        s[j][2 + e] = (kp <= qpos1 && kp >= klo1) ? s[j][2 + e] * sl2 : -INFINITY;
         mx0 = fmaxf(mx0, s[j][e]);
         mx1 = fmaxf(mx1, s[j][2 + e]);
       }

@@ -24,6 +24,10 @@
 //               in tensor memory only when a row's maximum grows by more than
 //               2^8 (the stale maximum keeps P <= 256 otherwise); finally
 //               O / l is stored.
+// With a sliding window of W keys the CTA starts at the block holding its
+// first row's oldest visible key, (first position - W + 1), and masks the
+// keys each row may not see; a row whose window misses a whole block keeps a
+// maximum of -inf there, and its probabilities are then taken as 0.
 // Every wait is bounded; a timeout records SAR_ERR_TIMEOUT.
 #include <float.h>
 
@@ -104,7 +108,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = qt * kBQ;
   const int rows = min(kBQ, a.len - q0);
   const int n_keys = a.start_pos + q0 + rows;  // keys of the last row of this tile, inclusive of it
-  const int nb = (n_keys + kBKV - 1) / kBKV;
+  // blocks [j0, j0 + nb): from the one holding the first row's oldest visible key
+  const int j0 = a.window > 0 ? max(0, a.start_pos + q0 - a.window + 1) / kBKV : 0;
+  const int nb = (n_keys + kBKV - 1) / kBKV - j0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -148,10 +154,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // block ahead (all eight loads in flight together, not one per box);
       // runs past the last key repeat the last one (finite data, masked)
       int pg[kRunsPerBlock], po[kRunsPerBlock];
-      auto pages_of = [&](int j) {
+      auto pages_of = [&](int j) {  // j counts from block j0
 #pragma unroll
         for (int g = 0; g < kRunsPerBlock; ++g) {
-          const int key = min(j * kRunsPerBlock + g, last_run) * kRun;
+          const int key = min((j0 + j) * kRunsPerBlock + g, last_run) * kRun;
           const int bi = key / a.page_size;
           pg[g] = a.bt[bi];
           po[g] = key - bi * a.page_size;
@@ -302,11 +308,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) sv[c] = 0.f;
       }
-      const int key0 = j * kBKV + hf * 64;
+      const int key0 = (j0 + j) * kBKV + hf * 64;
       if (key0 + 63 > pos) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
           if (key0 + c > pos) sv[c] = -INFINITY;
+      }
+      if (a.window > 0 && key0 <= pos - a.window) {  // keys at or before pos - W are outside the window
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (key0 + c <= pos - a.window) sv[c] = -INFINITY;
       }
       float pm;
       {
@@ -323,10 +334,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       pair_sync();
       const float mx = fmaxf(pm, red[((j & 1) * 2 + (hf ^ 1)) * kBQ + r]);
       const float m_new = fmaxf(m_used, mx);
-      const bool need = m_new > m_used + kRescale;  // always on the first block (key 0 is visible)
+      // taken on the first block with a visible key (m_used is -inf before it)
+      const bool need = m_new > m_used + kRescale;
       const float sc = need ? exp2f(m_used - m_new) : 1.f;  // 0 while m_used is -inf
-      if (alive && __any_sync(0xffffffffu, need && l > 0.f)) {
-        // O holds earlier blocks: rescale this half once the previous P.V has landed
+      // O holds earlier blocks once the row has seen a visible key (a finite
+      // maximum, shared by both key halves; a half's own sum l may still be 0
+      // when a window masked all of its keys so far): rescale this warp's
+      // dimension half once the previous P.V has landed
+      if (alive && __any_sync(0xffffffffu, need && m_used != -INFINITY)) {
         alive = warp_wait_bar(smem_u32(&bars->o_done), (uint32_t)((j - 1) & 1), a.err, SITE_CHUNK_PIPE);
         if (alive) {
           tc_fence_after();
@@ -347,15 +362,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_new;
       }
       // P = 2^(S - m), 16-bit, two keys per column: this half's keys over
-      // columns [hf*32, hf*32 + 32) of the S buffer
+      // columns [hf*32, hf*32 + 32) of the S buffer; while no visible key has
+      // been seen (a window that starts past this block) every P is 0
+      const float mref = m_used == -INFINITY ? 0.f : m_used;
       float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t u[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = fast_exp2(sv[c * 32 + 2 * e] - m_used);
-          const float p1 = fast_exp2(sv[c * 32 + 2 * e + 1] - m_used);
+          const float p0 = fast_exp2(sv[c * 32 + 2 * e] - mref);
+          const float p1 = fast_exp2(sv[c * 32 + 2 * e + 1] - mref);
           ls[e & 7] += p0 + p1;
           u[e] = Elem<T>::pack(p0, p1);
         }
@@ -419,7 +436,7 @@ int launch_t(const ChunkAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& 
 }  // namespace
 
 bool chunk_attention_tc_supported(const ChunkAttnArgs& a) {
-  return a.d == kD && a.page_size % kRun == 0 && a.qh % a.kvh == 0;
+  return a.d == kD && a.page_size % kRun == 0 && a.qh % a.kvh == 0 && a.window >= 0;
 }
 
 int launch_chunk_attention_tc(const ChunkAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,

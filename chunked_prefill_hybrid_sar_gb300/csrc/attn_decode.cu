@@ -16,7 +16,10 @@
 //     as a high and a low 16-bit part so the scores keep fp32-like precision;
 //   * online softmax in base 2 on the accumulator fragments; the 4 warps'
 //     (max, sum, acc) are merged in shared memory; split items write
-//     unnormalised partials that decode_combine_kernel merges.
+//     unnormalised partials that decode_combine_kernel merges;
+//   * with a sliding window the host plans each decode's ranges from the
+//     16-key block holding its oldest visible key; keys below that key are
+//     masked (every block still holds at least one visible key).
 #include <cuda.h>
 #include <float.h>
 
@@ -95,6 +98,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   pdl_launch_dependents();
 
   int b, kbeg, kend, part, btlen;
+  int wlo = 0;  // oldest key inside the sliding window
   const int* bt;
   if constexpr (COMPUTED) {
     b = blockIdx.x / a.max_splits;
@@ -120,6 +124,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     part = item.w;
     bt = a.bt + a.bt_off[b];
     btlen = a.bt_len[b];
+    if (a.window > 0) wlo = max(0, a.nkeys[b] - a.window);
   }
   const int kh = COMPUTED ? (int)blockIdx.y : (int)(blockIdx.x % a.kvh);
   const int G = a.qh / a.kvh;
@@ -227,6 +232,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     ++consumed;
     const int j = warp + i * kWarps;
     const int nk = min(kBlockKeys, kend - (kbeg + j * kBlockKeys));
+    const int nlo = wlo - (kbeg + j * kBlockKeys);  // keys of this block below it are outside the window
     const uint32_t kb = smem_u32(ring + s * STAGE_BYTES);
     const uint32_t vb = kb + BLK_BYTES;
     const int mi = lane >> 3;
@@ -251,7 +257,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     for (int jn = 0; jn < 2; ++jn)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        if (jn * 8 + 2 * c4 + e >= nk) sc[jn][e] = -INFINITY;
+        const int kk = jn * 8 + 2 * c4 + e;
+        if (kk >= nk || kk < nlo) sc[jn][e] = -INFINITY;
         mx = fmaxf(mx, sc[jn][e]);
       }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));

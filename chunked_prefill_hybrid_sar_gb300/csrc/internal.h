@@ -147,6 +147,8 @@ struct DecodeAttnArgs {
   float* partials;           // [n_parts][qh][d + 2]
   int n_items, n_decode, ld, ld_out, qh, kvh, d, page_size, num_pages, storage;
   int* err;
+  // sliding window (planned items only): decode b sees keys [nkeys[b] - window, nkeys[b]); 0 = all
+  int window = 0;
   // device-computed work split (used by the entry point that allocates nothing)
   const int32_t* ctx_lens = nullptr;  // [n_decode]
   int split_keys = 0, max_splits = 0, bt_stride = 0;
@@ -167,6 +169,7 @@ struct ChunkAttnArgs {
   const int32_t* bt;         // block table of the prompt
   int bt_len, start_pos, len, ld, ld_out, qh, kvh, d, page_size, num_pages, storage;
   int* err;
+  int window = 0;            // the row at position p sees keys (p - window, p]; 0 = all of [0, p]
 };
 int launch_chunk_attention(const ChunkAttnArgs& a, cudaStream_t s);
 // The same on the tcgen05 tensor cores (attn_chunk_tc.cu) for head_dim 128 and

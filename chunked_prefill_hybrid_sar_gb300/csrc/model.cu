@@ -178,12 +178,15 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
     return SAR_OK;
   };
   if (b->has_prefill) SAR_TRY(check_bt(b->prefill.block_table, b->prefill.n_blocks, b->prefill.start_pos + Lp - 1));
+  // a decode with nk keys reads from the 16-key block holding its oldest
+  // visible key (the kernel masks the keys of that block before it)
+  auto first_key = [&](int nk) { return d.sliding_window > 0 ? std::max(0, nk - d.sliding_window) / 16 * 16 : 0; };
   int64_t total_keys = 0;
   for (int i = 0; i < Bd; ++i) {
     const sar_decode& dc = b->decode[i];
     if (dc.ctx_len < 0 || !dc.block_table) return set_error(SAR_ERR_INVALID_ARG, "step: bad decode entry");
     SAR_TRY(check_bt(dc.block_table, dc.n_blocks, dc.ctx_len));
-    total_keys += dc.ctx_len + 1;
+    total_keys += dc.ctx_len + 1 - first_key(dc.ctx_len + 1);
   }
   // decode work split: key ranges of `split` keys, about four CTAs (two per
   // resident slot) per SM; fewer, longer ranges measured faster than more,
@@ -202,13 +205,14 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
     const int nb = (dc.ctx_len / ps) + 1;
     btlen[i] = nb;
     bt.insert(bt.end(), dc.block_table, dc.block_table + nb);
-    const int ns = (int)((nk + split - 1) / split);
+    const int kfirst = first_key(nk);
+    const int ns = (int)((nk - kfirst + split - 1) / split);
     pcnt[i] = ns;
     if (ns > 1) {
       pbeg[i] = n_parts;
     }
     for (int sidx = 0; sidx < ns; ++sidx) {
-      const int k0 = (int)(sidx * split), k1 = std::min<int>(nk, (int)((sidx + 1) * split));
+      const int k0 = kfirst + (int)(sidx * split), k1 = std::min<int>(nk, kfirst + (int)((sidx + 1) * split));
       const int part = ns > 1 ? n_parts + sidx : -1;
       auto& dst = (k1 - k0 == split) ? items : tail_items;  // full ranges first
       dst.insert(dst.end(), {i, k0, k1, part});
@@ -390,6 +394,7 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
       ca.num_pages = kv->num_pages;
       ca.storage = d.storage;
       ca.err = m->err;
+      ca.window = d.sliding_window;
       if (sar::chunk_attention_tc_supported(ca))
         SAR_TRY(sar::launch_chunk_attention_tc(ca, kv->tmk[l], kv->tmv[l], s));
       else
@@ -423,6 +428,7 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
       da.page_size = kv->page_size;
       da.num_pages = kv->num_pages;
       da.err = m->err;
+      da.window = d.sliding_window;
       SAR_TRY(sar::launch_decode_attention(da, kv->tmk[l], kv->tmv[l], s));
     }
     {
@@ -467,7 +473,7 @@ int sar_model_create(const sar_dims* dims, sar_model** out) {
   if (!dims || !out) return set_error(SAR_ERR_INVALID_ARG, "model: null argument");
   const sar_dims& d = *dims;
   if (d.n_layers <= 0 || d.hidden <= 0 || d.n_q_heads <= 0 || d.n_kv_heads <= 0 || d.ffn <= 0 || d.vocab < 0 ||
-      d.max_tokens <= 0 || d.max_decodes < 0 || d.max_decodes > d.max_tokens)
+      d.max_tokens <= 0 || d.max_decodes < 0 || d.max_decodes > d.max_tokens || d.sliding_window < 0)
     return set_error(SAR_ERR_INVALID_ARG, "model: bad dims");
   if (d.head_dim != 64 && d.head_dim != 128) return set_error(SAR_ERR_UNSUPPORTED, "model: head_dim must be 64 or 128");
   if (d.n_q_heads % d.n_kv_heads || d.n_q_heads / d.n_kv_heads > 8)

@@ -86,6 +86,12 @@ typedef struct sar_dims {
   int32_t max_tokens;
   int32_t max_decodes;
   int32_t storage;
+  /* Sliding-window attention: a query at position p sees the keys at
+   * positions (p - sliding_window, p], itself included; 0 = every earlier
+   * position (full causal).  Mistral-7B's attention is listed as GQA with a
+   * sliding window (Sarathi-Serve digest, appendix table of evaluated
+   * models); the pages give no window length. */
+  int32_t sliding_window;
 } sar_dims;
 
 /* One layer's weights: device bf16, [out, in] row-major; norm gains bf16 [hidden]. */
@@ -208,8 +214,9 @@ int sar_sample_greedy(sar_model* m, const float* logits, int32_t rows, int32_t* 
  * cudaMalloc: code that runs while another component captures a CUDA graph on
  * the same stream, runtimes that hand out a fixed memory budget up front and
  * own every allocation, hosts that forbid allocation on the serving path.
- * It computes what the decode rows of sar_step compute -- every decode's
- * query heads against its own paged history of ctx_lens[b] + 1 keys -- but
+ * It computes what the decode rows of sar_step compute for a model without a
+ * sliding window -- every decode's query heads against its own paged history
+ * of all ctx_lens[b] + 1 keys (it takes no window argument) -- but
  * plans the key splits on the device and keeps the split partials in one
  * file-scope device array of 8 MiB, so it needs no workspace and no pinned
  * staging buffer.  Every GPU that loads the library holds that array until

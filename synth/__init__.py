@@ -194,6 +194,22 @@ def tiny_case(seed: int = 0, dtype=torch.float32):
                 decode_prompts=decode_prompts, decode_inputs=decode_inputs)
 
 
+SMALL_128 = Dims(n_layers=1, hidden=512, n_q_heads=4, n_kv_heads=2, head_dim=128, ffn=1024, vocab=0)
+
+
+def window_case(seed: int = 0, d: Dims = SMALL_128, prompt_len: int = 640, ctxs=(90, 200, 333, 700)):
+    """A one-layer case for sliding-window checks: a prompt of ``prompt_len``
+    N(0,1) rows (chunked by the caller) and decodes at contexts ``ctxs`` with
+    random N(0,1) K/V histories and one N(0,1) input row each.  Draw order
+    after the weights: the prompt, the decode inputs, then the histories."""
+    layers, _, gen = model_weights(seed, d, torch.bfloat16)
+    prompt = normal(gen, (prompt_len, d.hidden), 1.0, torch.bfloat16)
+    decode_inputs = normal(gen, (len(ctxs), d.hidden), 1.0, torch.bfloat16)
+    hist = [kv_history(gen, 1, c, d, torch.bfloat16)[0] for c in ctxs]
+    return dict(dims=d, layers=layers, prompt=prompt, ctxs=list(ctxs), decode_inputs=decode_inputs,
+                histories=hist)
+
+
 MISTRAL_STARTS = (0, 512, 1536)
 
 
