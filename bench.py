@@ -500,7 +500,7 @@ def run_trace_mode(args):
     from chunked_prefill_hybrid_sar_gb300 import harness, serve
 
     taus = [int(t) for t in args.taus.split(",")]
-    dims = synth.MISTRAL_7B
+    dims = dataclasses.replace(synth.MISTRAL_7B, sliding_window=args.window)
     m, _ = harness.load_synthetic_model(0, dims, max_tokens=max(taus), max_decodes=256)
     free, _ = torch.cuda.mem_get_info()
     page_bytes = dims.n_layers * 2 * dims.kv_dim * PAGE * 2
@@ -520,7 +520,8 @@ def run_trace_mode(args):
         summ["rows_per_step"] = res.rows / max(1, len(st))
         summ["tokens_per_s_wall"] = res.rows / res.wall_s
         runs[tau] = summ
-    out = {"mode": "trace", "workload": f"Mistral-7B shape, 32 layers + 32000 head, f16 storage; "
+    attn = f"sliding window {dims.sliding_window}" if dims.sliding_window else "full causal"
+    out = {"mode": "trace", "workload": f"Mistral-7B shape, 32 layers + 32000 head, {attn}, f16 storage; "
            f"{args.requests} requests, Poisson 4 req/s, prompt lognormal(median 1024, sigma 1, clip 64-8192), "
            f"output lognormal(median 256, sigma 1, clip 16-1024), greedy sampling, wall-clock arrivals",
            "kv_pages": n_pages, "page_size": PAGE, "per_tau": runs}
@@ -531,18 +532,22 @@ def run_trace_mode(args):
 # ------------------------------------------------------------------ long prompt
 
 def run_long_prompt(args):
-    """The Yi-34B shape (60 layers, 64000 head) prefilling one 16384-token
-    prompt in chunks of C tokens, each step carrying 128 decodes (contexts
-    uniform in [512, 8192], random KV): per chunk size the prefill time, the
+    """The Yi-34B shape (60 layers, 64000 head; or the 32-layer Mistral-7B
+    shape with ``--model mistral7b``) prefilling one 16384-token prompt in
+    chunks of C tokens, each step carrying 128 decodes (contexts uniform in
+    [512, 8192], random KV): per chunk size the prefill time, the
     chunk-attention time and the prior-chunk KV re-read the chunking implies
-    (N(N-1)/2 chunk loads per layer)."""
+    (N(N-1)/2 chunk loads per layer with full causal attention; with a
+    sliding window of W keys a chunk starting at s reads back only the
+    positions [s - W + 1, s))."""
     import torch
 
     import chunked_prefill_hybrid_sar_gb300 as sar
     from chunked_prefill_hybrid_sar_gb300 import harness
 
     chunks = [int(c) for c in args.chunks.split(",")]
-    dims = synth.YI_34B
+    dims = synth.MISTRAL_7B if args.model == "mistral7b" else synth.YI_34B
+    dims = dataclasses.replace(dims, sliding_window=args.window)
     if args.layers:
         dims = dataclasses.replace(dims, n_layers=args.layers)
     plen, n_dec = 16384, 128
@@ -588,7 +593,8 @@ def run_long_prompt(args):
         prof = m.profile_read()
         m.profile(False)
         ca_ms = prof["chunk_attn"][0]
-        reread = n * (n - 1) // 2 * C * kv_tok
+        W = dims.sliding_window
+        reread = sum(s - max(0, s - W + 1) if W > 0 else s for s in range(0, plen, C)) * kv_tok
         own = n * C * kv_tok
         per_c[C] = {"steps": n, "prefill_ms": sum(step_ms), "step_ms_mean": sum(step_ms) / n,
                     "step_ms_first": step_ms[0], "step_ms_last": step_ms[-1],
@@ -599,9 +605,12 @@ def run_long_prompt(args):
                     "chunk_attn_kv_gbs": (reread + own) / (ca_ms * 1e-3) / 1e9 if ca_ms else None,
                     "kernel_ms": {k: v[0] for k, v in prof.items() if v[1]}}
     m.sync_status()
-    out = {"mode": "long-prompt", "workload": f"Yi-34B shape ({dims.n_layers} layers, H 7168, 56q/8kv x 128, "
-           f"FFN 20480, head 64000), f16 storage; one {plen}-token prompt in chunks of C with {n_dec} decodes "
-           f"per step (ctx U[512,8192], random KV)", "per_chunk": per_c}
+    name = "Mistral-7B" if args.model == "mistral7b" else "Yi-34B"
+    attn = f"sliding window {dims.sliding_window}" if dims.sliding_window else "full causal"
+    out = {"mode": "long-prompt", "workload": f"{name} shape ({dims.n_layers} layers, H {dims.hidden}, "
+           f"{dims.n_q_heads}q/{dims.n_kv_heads}kv x {dims.head_dim}, FFN {dims.ffn}, head {dims.vocab}, "
+           f"{attn}), f16 storage; one {plen}-token prompt in chunks of C with {n_dec} decodes "
+           f"per step (ctx U[512,8192], random KV)", "sliding_window": dims.sliding_window, "per_chunk": per_c}
     print(json.dumps(out))
     return out
 
@@ -621,6 +630,9 @@ def main():
     ap.add_argument("--chunks", default="256,512,1024", help="long-prompt mode: chunk sizes")
     ap.add_argument("--layers", type=int, default=0, help="long-prompt mode: fewer layers (profiling)")
     ap.add_argument("--no-warmup", action="store_true", help="long-prompt mode: no untimed prefill first")
+    ap.add_argument("--model", choices=["yi34b", "mistral7b"], default="yi34b", help="long-prompt mode: model shape")
+    ap.add_argument("--window", type=int, default=0,
+                    help="long-prompt and trace modes: sliding-window attention of W keys (0 = full causal)")
     args = ap.parse_args()
     if args.mode == "sweep":
         run_sweep(args)
