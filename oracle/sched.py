@@ -7,8 +7,15 @@ Restates Algorithm 3 of the *Sarathi-Serve digest* (§2 Q2 item 2 and the
 2. adds one decode token for every running request whose prefill is done;
 3. if a request's prefill is unfinished, adds its next chunk,
    ``c = get_next_chunk_size(R, tau, n_t)``, ``n_t += c``;
-4. admits new requests while ``can_allocate`` and ``n_t < tau``;
+4. admits new requests while ``can_allocate`` and ``n_t < tau``, each with
+   its first chunk ``c = get_next_chunk_size(R_new, tau, n_t)``, ``n_t += c``
+   (the flowchart's admission loop), so one batch may carry several chunks;
 5. processes the hybrid batch, then drops finished requests.
+
+Every admitted request but the last fits whole in the budget left to it, and
+an ongoing chunk that stops short of its prompt's end fills the budget, so
+at most one prompt is unfinished after any iteration -- the "at most one
+ongoing prefill chunk" of the digest's §2 Q2 item 2.
 
 Readings where the pages are silent (the CUDA-side scheduler follows the same):
 
@@ -16,9 +23,13 @@ Readings where the pages are silent (the CUDA-side scheduler follows the same):
   "batch token count must be a multiple of the tile size" rule,
   *Sarathi-Serve digest* §2 Q2 item 3; *SARATHI reading notes* part 3 §3);
 * ``get_next_chunk_size = min(remaining prompt, tau - n_t)``;
-* at most one prompt is in its prefill phase at a time, so a new request is
-  admitted only when no unfinished prefill exists (one prefill chunk per
-  batch, *SARATHI technique write-up* §3.2); leftover budget stays unused;
+* ``max_chunks`` caps the chunks of one batch (0 = no cap: the admission
+  loop above).  ``max_chunks = 1`` is the one-chunk reading of *SARATHI
+  technique write-up* §3.2 ("one prefill chunk per batch"): a new request is
+  then admitted only when no prompt is unfinished, and leftover budget stays
+  unused;
+* admission is first-come-first-served with head-of-line blocking: the loop
+  stops at the first ready request that cannot be allocated;
 * waiting requests are served first-come-first-served by (arrival, id) and
   only once ``arrival <= now``;
 * ``can_allocate``: free pages >= ceil(prompt_len / page_size) + 1 and fewer
@@ -79,20 +90,31 @@ class Req:
 
 @dataclasses.dataclass
 class Batch:
-    """One iteration's decision: at most one chunk, then the decodes.
+    """One iteration's decision: the prefill chunks, then the decodes.
 
-    ``prefill``: ``(req, start_pos, len, block_table)`` or ``None``;
+    ``prefills``: list of ``(req, start_pos, len, block_table)`` (the ongoing
+    prompt's chunk first, then newly admitted requests in admission order);
     ``decodes``: list of ``(req, ctx_len, block_table)``; ``tokens``: input
     token id per batch row (chunk rows first) when prompt tokens are known.
     """
 
-    prefill: tuple | None
+    prefills: list
     decodes: list
     tokens: list | None
 
     @property
+    def prefill(self) -> tuple | None:
+        """The first chunk, or None."""
+        return self.prefills[0] if self.prefills else None
+
+    @property
     def n_tokens(self) -> int:
-        return (self.prefill[2] if self.prefill else 0) + len(self.decodes)
+        return sum(p[2] for p in self.prefills) + len(self.decodes)
+
+    @property
+    def logit_rows(self) -> int:
+        """Rows sampled: the last row of every chunk, then every decode."""
+        return len(self.prefills) + len(self.decodes)
 
 
 def round_budget(tau: int, tile: int) -> int:
@@ -103,7 +125,11 @@ def round_budget(tau: int, tile: int) -> int:
 
 
 class StallFreeScheduler:
-    def __init__(self, tau: int, tile: int, page_size: int, num_pages: int, max_batch: int):
+    def __init__(self, tau: int, tile: int, page_size: int, num_pages: int, max_batch: int,
+                 max_chunks: int = 0):
+        if max_chunks < 0:
+            raise ValueError("negative chunk cap")
+        self.max_chunks = max_chunks
         self.tau = round_budget(tau, tile)
         self.page_size = page_size
         self.max_batch = max_batch
@@ -134,49 +160,51 @@ class StallFreeScheduler:
                     r.pages.append(self.pool.alloc())
                 decodes.append(r)
                 n_t += 1
-        chunk = None
+        chunks = []
         ongoing = next((r for r in self.running if r.prefill_done < r.prompt_len), None)
         if ongoing is not None:
             c = min(ongoing.prompt_len - ongoing.prefill_done, self.tau - n_t)
             if c > 0:
-                chunk = (ongoing, ongoing.prefill_done, c)
+                chunks.append((ongoing, ongoing.prefill_done, c))
                 n_t += c
-        else:
+        if ongoing is None or self.max_chunks != 1:
             ready = sorted((r for r in self.waiting if r.arrival <= now),
                            key=lambda r: (r.arrival, r.req))
-            if ready and n_t < self.tau and self._can_allocate(ready[0]):
-                r = ready[0]
+            for r in ready:
+                if self.max_chunks and len(chunks) >= self.max_chunks:
+                    break
+                if not (n_t < self.tau and self._can_allocate(r)):
+                    break
                 self.waiting.remove(r)
                 for _ in range(-(-r.prompt_len // self.page_size)):
                     r.pages.append(self.pool.alloc())
                 self.running.append(r)
                 c = min(r.prompt_len, self.tau - n_t)
-                chunk = (r, 0, c)
+                chunks.append((r, 0, c))
                 n_t += c
         tokens = None
         if all(r.prompt_tokens is not None for r in self.running):
             tokens = []
-            if chunk:
-                r, s, c = chunk
+            for r, s, c in chunks:
                 tokens += r.prompt_tokens[s:s + c]
             for r in decodes:
                 tokens.append(r.tokens[-1] if r.tokens else 0)
         b = Batch(
-            prefill=(chunk[0].req, chunk[1], chunk[2], list(chunk[0].pages)) if chunk else None,
+            prefills=[(r.req, s, c, list(r.pages)) for r, s, c in chunks],
             decodes=[(r.req, r.prompt_len + r.generated - 1, list(r.pages)) for r in decodes],
             tokens=tokens,
         )
         self._last = b
-        self._last_objs = (chunk, decodes)
+        self._last_objs = (chunks, decodes)
         return b
 
     def commit(self, sampled) -> list[int]:
-        """Advance state with one sampled token per logits row (the chunk's last
-        row first, then each decode).  Returns the ids of finished requests."""
-        chunk, decodes = self._last_objs
+        """Advance state with one sampled token per logits row (each chunk's last
+        row first, in batch order, then each decode).  Returns the ids of
+        finished requests."""
+        chunks, decodes = self._last_objs
         i = 0
-        if chunk:
-            r, s, c = chunk
+        for r, s, c in chunks:
             r.prefill_done += c
             if r.prefill_done == r.prompt_len:
                 r.generated = 1
@@ -192,7 +220,7 @@ class StallFreeScheduler:
             r.pages = []
             self.running.remove(r)
             self.finished.append(r)
-        self._last_objs = (None, [])
+        self._last_objs = ([], [])
         return [r.req for r in done]
 
     def idle(self) -> bool:

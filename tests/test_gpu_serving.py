@@ -64,7 +64,7 @@ def test_trace_runs_and_replays_bit_exactly(mistral32):
     m.sync_status()
     assert res.steps > 0
     # replay: the oracle scheduler, same times, same sampled tokens -> same batches
-    o = osch.StallFreeScheduler(512, 128, kv.page_size, kv.num_pages, 256)
+    o = osch.StallFreeScheduler(512, 128, kv.page_size, kv.num_pages, 256, max_chunks=1)
     for r in trace:
         o.add(r.req, r.arrival, r.prompt_len, r.output_len, toks[r.req])
     for i, now in enumerate(res.now_log):

@@ -16,7 +16,7 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 def replay(trace, tau, tile=128, page_size=16, num_pages=4000, max_batch=64, dt=0.013,
            with_tokens=False, max_steps=100000):
     """Drive both schedulers with the same `now` sequence and sampled tokens."""
-    o = osch.StallFreeScheduler(tau, tile, page_size, num_pages, max_batch)
+    o = osch.StallFreeScheduler(tau, tile, page_size, num_pages, max_batch, max_chunks=1)
     c = sar.Scheduler(tau, tile, page_size, num_pages, max_batch)
     toks = synth.prompt_tokens(5, trace, 1000) if with_tokens else {}
     for r in trace:
