@@ -511,7 +511,7 @@ def run_trace_mode(args):
     toks = synth.prompt_tokens(1, trace, dims.vocab)
     runs = {}
     for tau in taus:
-        res = serve.run_trace(m, kv, trace, toks, tau=tau, keep_batches=False)
+        res = serve.run_trace(m, kv, trace, toks, tau=tau, keep_batches=False, max_chunks=args.max_chunks)
         m.sync_status()
         st = sorted(res.step_ms)
         summ = res.summary()
@@ -521,7 +521,9 @@ def run_trace_mode(args):
         summ["tokens_per_s_wall"] = res.rows / res.wall_s
         runs[tau] = summ
     attn = f"sliding window {dims.sliding_window}" if dims.sliding_window else "full causal"
-    out = {"mode": "trace", "workload": f"Mistral-7B shape, 32 layers + 32000 head, {attn}, f16 storage; "
+    adm = "one chunk per batch" if args.max_chunks == 1 else (
+        f"at most {args.max_chunks} chunks per batch" if args.max_chunks else "Algorithm 3 admission loop")
+    out = {"mode": "trace", "workload": f"Mistral-7B shape, 32 layers + 32000 head, {attn}, f16 storage, {adm}; "
            f"{args.requests} requests, Poisson 4 req/s, prompt lognormal(median 1024, sigma 1, clip 64-8192), "
            f"output lognormal(median 256, sigma 1, clip 16-1024), greedy sampling, wall-clock arrivals",
            "kv_pages": n_pages, "page_size": PAGE, "per_tau": runs}
@@ -631,6 +633,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="long-prompt mode: fewer layers (profiling)")
     ap.add_argument("--no-warmup", action="store_true", help="long-prompt mode: no untimed prefill first")
     ap.add_argument("--model", choices=["yi34b", "mistral7b"], default="yi34b", help="long-prompt mode: model shape")
+    ap.add_argument("--max-chunks", type=int, default=0,
+                    help="trace mode: prefill chunks per batch (0 = Algorithm 3's admission loop, 1 = one chunk)")
     ap.add_argument("--window", type=int, default=0,
                     help="long-prompt and trace modes: sliding-window attention of W keys (0 = full causal)")
     args = ap.parse_args()

@@ -44,9 +44,10 @@ def launch_count() -> int:
 
 
 class Batch:
-    """Owns the ctypes descriptor of one hybrid batch (chunk first, then decodes).
+    """Owns the ctypes descriptor of one hybrid batch (chunks first, then decodes).
 
-    ``prefill``: ``(req, start_pos, len, block_table)`` or ``None``;
+    ``prefill``: ``(req, start_pos, len, block_table)``, a list of such chunks
+    (each of a different request, rows stacked in list order) or ``None``;
     ``decodes``: iterable of ``(req, ctx_len, block_table)``.
     """
 
@@ -54,12 +55,25 @@ class Batch:
         self._keep = []
         b = _lib.sar_batch()
         b.in_kind = in_kind
-        if prefill is not None:
-            req, start, n, bt = prefill
+        if prefill is None:
+            chunks = []
+        elif isinstance(prefill, tuple):
+            chunks = [prefill]
+        else:
+            chunks = list(prefill)
+        pre = []
+        for req, start, n, bt in chunks:
             arr = _lib.i32_array(bt)
             self._keep.append(arr)
+            pre.append(_lib.sar_prefill(req, start, n, arr, len(bt)))
+        if pre:
             b.has_prefill = 1
-            b.prefill = _lib.sar_prefill(req, start, n, arr, len(bt))
+            b.prefill = pre[0]
+        if len(pre) > 1:
+            more = (_lib.sar_prefill * (len(pre) - 1))(*pre[1:])
+            self._keep.append(more)
+            b.n_more_prefill = len(pre) - 1
+            b.more_prefill = more
         decodes = list(decodes)
         dec = (_lib.sar_decode * max(1, len(decodes)))()
         for i, (req, ctx, bt) in enumerate(decodes):
@@ -70,7 +84,8 @@ class Batch:
         b.n_decode = len(decodes)
         b.decode = dec
         self.c = b
-        self.lp = prefill[2] if prefill is not None else 0
+        self.chunks = chunks
+        self.lp = sum(c[2] for c in chunks)
         self.bd = len(decodes)
 
     @property
@@ -79,7 +94,8 @@ class Batch:
 
     @property
     def logit_rows(self) -> int:
-        return (1 if self.lp else 0) + self.bd
+        """The last row of every chunk, then every decode row."""
+        return len(self.chunks) + self.bd
 
 
 class Model:
@@ -177,8 +193,9 @@ class KVCache:
 class Scheduler:
     """Stall-free scheduler (host only)."""
 
-    def __init__(self, tau: int, tile: int, page_size: int, num_pages: int, max_batch: int):
-        cfg = _lib.sar_sched_cfg(tau, tile, page_size, num_pages, max_batch)
+    def __init__(self, tau: int, tile: int, page_size: int, num_pages: int, max_batch: int,
+                 max_chunks: int = 0):
+        cfg = _lib.sar_sched_cfg(tau, tile, page_size, num_pages, max_batch, max_chunks)
         h = ctypes.c_void_p()
         check(lib().sar_sched_create(ctypes.byref(cfg), ctypes.byref(h)))
         self.h = h
@@ -188,21 +205,26 @@ class Scheduler:
         check(lib().sar_sched_add(self.h, req, arrival, prompt_len, output_len, arr))
 
     def next(self, now: float):
-        """Returns ``(prefill, decodes, tokens, c_batch)`` with Python lists copied out."""
+        """Returns ``(chunks, decodes, tokens, c_batch)`` with Python lists copied
+        out; ``chunks`` lists ``(req, start_pos, len, block_table)`` in row order."""
         b = _lib.sar_batch()
         tok = _lib.P_i32()
         check(lib().sar_sched_next(self.h, now, ctypes.byref(b), ctypes.byref(tok)))
-        pre = None
+
+        def chunk(p):
+            return (p.req, p.start_pos, p.len, [p.block_table[i] for i in range(p.n_blocks)])
+
+        chunks = []
         if b.has_prefill:
-            p = b.prefill
-            pre = (p.req, p.start_pos, p.len, [p.block_table[i] for i in range(p.n_blocks)])
+            chunks.append(chunk(b.prefill))
+            chunks += [chunk(b.more_prefill[i]) for i in range(b.n_more_prefill)]
         decs = []
         for i in range(b.n_decode):
             dd = b.decode[i]
             decs.append((dd.req, dd.ctx_len, [dd.block_table[j] for j in range(dd.n_blocks)]))
-        m = (pre[2] if pre else 0) + len(decs)
+        m = sum(c[2] for c in chunks) + len(decs)
         tokens = [tok[i] for i in range(m)] if bool(tok) else None
-        return pre, decs, tokens, b
+        return chunks, decs, tokens, b
 
     def commit(self, sampled) -> int:
         arr = _lib.i32_array(sampled)

@@ -64,12 +64,13 @@ class sar_decode(ctypes.Structure):
 
 class sar_batch(ctypes.Structure):
     _fields_ = [("has_prefill", i32), ("prefill", sar_prefill), ("n_decode", i32),
-                ("decode", ctypes.POINTER(sar_decode)), ("in_kind", i32)]
+                ("decode", ctypes.POINTER(sar_decode)), ("in_kind", i32), ("n_more_prefill", i32),
+                ("more_prefill", ctypes.POINTER(sar_prefill))]
 
 
 class sar_sched_cfg(ctypes.Structure):
     _fields_ = [("tau", i32), ("tile", i32), ("page_size", i32), ("num_pages", i32),
-                ("max_batch", i32)]
+                ("max_batch", i32), ("max_chunks", i32)]
 
 
 # name -> (restype, argtypes)

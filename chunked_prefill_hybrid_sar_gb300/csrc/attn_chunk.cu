@@ -6,6 +6,9 @@
 // correct, same page section 3.1).  Chunk k re-reads the KV of the k earlier
 // chunks -- the N(N-1)/2 re-read of the Sarathi-Serve digest, section 4.
 //
+// One launch serves every chunk of a batch: CTA x takes tile x of the step's
+// tile table (up to 64 consecutive rows of one prompt's chunk).
+//
 // Tiled online-softmax attention on warp-level 16-bit MMAs (m16n8k16, fp32
 // accumulate; the fp32 queries enter as a high and a low 16-bit part, so the
 // scores are as precise as the 16-bit keys allow): a CTA owns 64 query rows of
@@ -27,6 +30,7 @@ namespace {
 constexpr int kBQ = 64;      // query rows per CTA
 constexpr int kBKV = 64;     // keys per tile
 constexpr int kThreads = 128;
+static_assert(kBQ == kChunkTileRows, "the step plans tiles of kBQ rows");
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -73,16 +77,18 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
   uint8_t* sq = smem;                     // [2][64][D]: q split into a high and a low part
   uint8_t* skv = smem + 2 * kBQ * D * 2;  // [2 stages][K | V][64][D]
 
-  const int qt = gridDim.x - 1 - blockIdx.x;  // longest (latest) query tiles first
   const int hq = blockIdx.y;
   const int G = a.qh / a.kvh;
   const int kh = hq / G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q0 = qt * kBQ;
-  const int nq = min(kBQ, a.len - q0);
-  const int last_pos = a.start_pos + q0 + nq - 1;        // latest query position in this CTA
+  // this CTA's tile (the table lists the most keys first)
+  const int* tl = a.tiles + 8 * blockIdx.x;
+  const int row0 = tl[0], pos0 = tl[1], nq = tl[2];
+  const int32_t* bt = a.bt + tl[3];
+  const int bt_len = tl[4];
+  const int last_pos = pos0 + nq - 1;        // latest query position in this CTA
   const int n_tiles = last_pos / kBKV + 1;
-  const int t0 = a.window > 0 ? max(0, a.start_pos + q0 - a.window + 1) / kBKV : 0;  // first tile in any window
+  const int t0 = a.window > 0 ? max(0, pos0 - a.window + 1) / kBKV : 0;  // first key tile in any window
   const uint32_t sq_u = smem_u32(sq), skv_u = smem_u32(skv);
   const uint32_t sql_u = sq_u + kBQ * D * 2;
 
@@ -92,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
     const int r = c / CH, ch = c % CH;
     float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (r < nq) {
-      const float4* src = reinterpret_cast<const float4*>(a.q32 + (size_t)(q0 + r) * a.ld32 + (size_t)hq * D + ch * 8);
+      const float4* src = reinterpret_cast<const float4*>(a.q32 + (size_t)(row0 + r) * a.ld32 + (size_t)hq * D + ch * 8);
       const float4 x0 = src[0], x1 = src[1];
       f[0] = x0.x; f[1] = x0.y; f[2] = x0.z; f[3] = x0.w; f[4] = x1.x; f[5] = x1.y; f[6] = x1.z; f[7] = x1.w;
     }
@@ -114,8 +120,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
       const int r = c / CH, ch = c % CH;
       const int pos = t * kBKV + r;
       const int bi = pos / a.page_size;
-      bool ok = pos <= last_pos && bi < a.bt_len;
-      int page = ok ? a.bt[bi] : 0;
+      bool ok = pos <= last_pos && bi < bt_len;
+      int page = ok ? bt[bi] : 0;
       if (ok && (page < 0 || page >= a.num_pages)) {
         report(a.err, SAR_ERR_BOUNDS, SITE_CHUNK_BOUNDS, pos);
         ok = false;
@@ -137,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
   for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   const int r_lo = warp * 16 + (lane >> 2);  // this thread's two query rows in the tile
-  const int qpos0 = a.start_pos + q0 + r_lo;
+  const int qpos0 = pos0 + r_lo;
   const int qpos1 = qpos0 + 8;
   // oldest visible key of each row (keys below it are masked)
   const int klo0 = a.window > 0 ? qpos0 - a.window + 1 : 0;
@@ -240,15 +246,15 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
   const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
   const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-  const int row0 = q0 + r_lo, row1 = row0 + 8;
+  const int orow0 = row0 + r_lo, orow1 = orow0 + 8;
 #pragma unroll
   T* out = static_cast<T*>(a.out);
   for (int j = 0; j < D / 8; ++j) {
     const int col = hq * D + j * 8 + 2 * (lane & 3);
     if (r_lo < nq)
-      *reinterpret_cast<uint32_t*>(out + (size_t)row0 * a.ld_out + col) = Elem<T>::pack(o[j][0] * inv0, o[j][1] * inv0);
+      *reinterpret_cast<uint32_t*>(out + (size_t)orow0 * a.ld_out + col) = Elem<T>::pack(o[j][0] * inv0, o[j][1] * inv0);
     if (r_lo + 8 < nq)
-      *reinterpret_cast<uint32_t*>(out + (size_t)row1 * a.ld_out + col) = Elem<T>::pack(o[j][2] * inv1, o[j][3] * inv1);
+      *reinterpret_cast<uint32_t*>(out + (size_t)orow1 * a.ld_out + col) = Elem<T>::pack(o[j][2] * inv1, o[j][3] * inv1);
   }
 }
 
@@ -261,7 +267,7 @@ int launch_impl(const ChunkAttnArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return cuda_error(e, "chunk attention attribute");
     attr = true;
   }
-  dim3 grid((a.len + kBQ - 1) / kBQ, a.qh);
+  dim3 grid(a.n_tiles, a.qh);
   cudaError_t e = launch_pdl(chunk_attn_kernel<T, D>, grid, dim3(kThreads), smem, s, a);
   if (e != cudaSuccess) return cuda_error(e, "chunk attention launch");
   count_launches(1);
@@ -271,7 +277,7 @@ int launch_impl(const ChunkAttnArgs& a, cudaStream_t s) {
 }  // namespace
 
 int launch_chunk_attention(const ChunkAttnArgs& a, cudaStream_t s) {
-  if (a.len <= 0) return SAR_OK;
+  if (a.n_tiles <= 0) return SAR_OK;
   if (a.qh % a.kvh) return set_error(SAR_ERR_UNSUPPORTED, "chunk attention: qh % kvh");
   const bool bf = a.storage == SAR_STORAGE_BF16;
   if (a.d == 128) return bf ? launch_impl<__nv_bfloat16, 128>(a, s) : launch_impl<__half, 128>(a, s);

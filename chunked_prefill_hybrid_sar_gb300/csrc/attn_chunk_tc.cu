@@ -6,7 +6,9 @@
 // attention, same page section 3.1; chunk k re-reads the KV of the k earlier
 // chunks, Sarathi-Serve digest section 4).
 //
-// One CTA = 128 query rows of one query head (352 threads):
+// One CTA = one query tile (up to 128 consecutive rows of one prompt's chunk,
+// from the step's tile table, so one launch serves every chunk of a batch)
+// of one query head (352 threads):
 //   warps 0, 10 TMA producers of K and of V: each 128-key block is 8 runs of
 //               16 keys x 2 dim halves (one box each: 16 keys x 64 dims of one
 //               page, 128-byte swizzle) into a 2-stage ring per tensor; a K
@@ -56,6 +58,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 128;               // S buffer b at columns [b*128, b*128+128); P overwrites the first 64
 constexpr uint32_t kColO = 256;
 constexpr float kRescale = 8.f;                // log2 of the growth tolerated before rescaling O
+static_assert(kBQ == kChunkTileRowsTc, "the step plans tiles of kBQ rows");
 
 struct Bars {
   uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
@@ -101,16 +104,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int qt = gridDim.x - 1 - blockIdx.x;  // longest causal ranges first
   const int hq = blockIdx.y;
   const int G = a.qh / a.kvh;
   const int kh = hq / G;
-  const int q0 = qt * kBQ;
-  const int rows = min(kBQ, a.len - q0);
-  const int n_keys = a.start_pos + q0 + rows;  // keys of the last row of this tile, inclusive of it
-  // blocks [j0, j0 + nb): from the one holding the first row's oldest visible key
-  const int j0 = a.window > 0 ? max(0, a.start_pos + q0 - a.window + 1) / kBKV : 0;
-  const int nb = (n_keys + kBKV - 1) / kBKV - j0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -138,6 +134,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_slot;
   pdl_wait();
   pdl_launch_dependents();
+  // this CTA's tile (the table lists the most keys first)
+  const int4 tl = reinterpret_cast<const int4*>(a.tiles)[2 * blockIdx.x];
+  const int row0 = tl.x;   // batch row of the tile's first query
+  const int pos0 = tl.y;   // its position in the prompt
+  const int rows = tl.z;
+  const int32_t* bt = a.bt + tl.w;
+  const int bt_len = a.tiles[8 * blockIdx.x + 4];
+  const int n_keys = pos0 + rows;  // keys of the last row of this tile, inclusive of it
+  // blocks [j0, j0 + nb): from the one holding the first row's oldest visible key
+  const int j0 = a.window > 0 ? max(0, pos0 - a.window + 1) / kBKV : 0;
+  const int nb = (n_keys + kBKV - 1) / kBKV - j0;
 
   if (warp == 0 || warp == 10) {
     // ---------------- producers: warp 0 K, warp 10 V ----------------
@@ -148,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
       tma_prefetch_desc(map);
       const int last_run = (n_keys - 1) / kRun;
-      bool ok = (n_keys - 1) / a.page_size < a.bt_len;
+      bool ok = (n_keys - 1) / a.page_size < bt_len;
       if (!ok && is_k) report(a.err, SAR_ERR_BOUNDS, SITE_CHUNK_BOUNDS, n_keys);
       // the page of every 16-key run of a block, read from the block table one
       // block ahead (all eight loads in flight together, not one per box);
@@ -159,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int g = 0; g < kRunsPerBlock; ++g) {
           const int key = min((j0 + j) * kRunsPerBlock + g, last_run) * kRun;
           const int bi = key / a.page_size;
-          pg[g] = a.bt[bi];
+          pg[g] = bt[bi];
           po[g] = key - bi * a.page_size;
         }
       };
@@ -248,14 +255,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = qq * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(qq * 32) << 16);
     const bool valid = r < rows;
-    const int pos = a.start_pos + q0 + r;  // this row's position; keys <= pos are visible
+    const int pos = pos0 + r;  // this row's position; keys <= pos are visible
     float* red = reinterpret_cast<float*>(smem + kRedOff);  // [2 parities][2 halves][128 rows]
     auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + qq) : "memory"); };
     {
       // this half of the query row -> scaled, split into 16-bit high and low
       // parts, swizzled as the MMA reads it (dim half hf is Q region hf)
       const float qscale = rsqrtf((float)kD) * 1.4426950408889634f;
-      const float* qp = a.q32 + (size_t)(q0 + r) * a.ld32 + (size_t)hq * kD + hf * 64;
+      const float* qp = a.q32 + (size_t)(row0 + r) * a.ld32 + (size_t)hq * kD + hf * 64;
 #pragma unroll 1
       for (int ch = 0; ch < 8; ++ch) {
         float x[8];
@@ -392,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (alive) {
       tc_fence_after();
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      T* out = static_cast<T*>(a.out) + (size_t)(q0 + r) * a.ld_out + (size_t)hq * kD + hf * 64;
+      T* out = static_cast<T*>(a.out) + (size_t)(row0 + r) * a.ld_out + (size_t)hq * kD + hf * 64;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t u[16];
@@ -426,7 +433,7 @@ int launch_t(const ChunkAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& 
     if (e != cudaSuccess) return cuda_error(e, "chunk attention (tcgen05) attribute");
     attr = true;
   }
-  const dim3 grid((a.len + kBQ - 1) / kBQ, a.qh);
+  const dim3 grid(a.n_tiles, a.qh);
   cudaError_t e = launch_pdl(chunk_attn_tc_kernel<T>, grid, dim3(kThreads), (size_t)kSmem, s, tmk, tmv, a);
   if (e != cudaSuccess) return cuda_error(e, "chunk attention (tcgen05) launch");
   count_launches(1);
@@ -441,7 +448,7 @@ bool chunk_attention_tc_supported(const ChunkAttnArgs& a) {
 
 int launch_chunk_attention_tc(const ChunkAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                               cudaStream_t s) {
-  if (a.len <= 0) return SAR_OK;
+  if (a.n_tiles <= 0) return SAR_OK;
   if (!chunk_attention_tc_supported(a))
     return set_error(SAR_ERR_UNSUPPORTED, "chunk attention (tcgen05): head_dim 128, pages of a multiple of 16 keys");
   if ((reinterpret_cast<uintptr_t>(a.q32) & 15) || (a.ld32 & 3) || (reinterpret_cast<uintptr_t>(a.out) & 15) ||

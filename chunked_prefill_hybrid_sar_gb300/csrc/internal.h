@@ -161,16 +161,25 @@ int launch_decode_attention(const DecodeAttnArgs& a, const CUtensorMap& tmk, con
                             cudaStream_t s);
 
 struct ChunkAttnArgs {
-  const float* q32;          // chunk query rows [0, len) in fp32; row stride ld32
+  const float* q32;          // chunk query rows in fp32 (batch rows); row stride ld32
   int ld32;
-  void* out;                 // [len, qh*d]; row stride ld_out
+  void* out;                 // attention rows (batch rows); row stride ld_out
   const void* k_cache;
   const void* v_cache;
-  const int32_t* bt;         // block table of the prompt
-  int bt_len, start_pos, len, ld, ld_out, qh, kvh, d, page_size, num_pages, storage;
+  const int32_t* bt;         // the chunks' block tables, concatenated
+  // [n_tiles][8] query tiles, one CTA each, in launch order: first batch row,
+  // first position, rows (<= the kernel's tile rows), block-table offset into
+  // bt, block-table length, 3 unused; a tile's rows are consecutive positions
+  // of one prompt, whose keys [0, last position] sit in its block table
+  const int32_t* tiles;
+  int n_tiles;
+  int ld, ld_out, qh, kvh, d, page_size, num_pages, storage;
   int* err;
   int window = 0;            // the row at position p sees keys (p - window, p]; 0 = all of [0, p]
 };
+// Query rows per tile: the warp-MMA kernel (attn_chunk.cu) and the tcgen05 one.
+constexpr int kChunkTileRows = 64;
+constexpr int kChunkTileRowsTc = 128;
 int launch_chunk_attention(const ChunkAttnArgs& a, cudaStream_t s);
 // The same on the tcgen05 tensor cores (attn_chunk_tc.cu) for head_dim 128 and
 // pages of a multiple of 16 keys, reading the pages through the per-layer

@@ -2,7 +2,7 @@
 //
 // One step ("SARATHI: Efficient LLM Inference by Piggybacking Decodes with
 // Chunked Prefills", reading notes, part 2 section 3 -- merge, split, merge):
-//   rows [0, Lp) are the prefill chunk, rows [Lp, Lp+Bd) the decodes, all in
+//   rows [0, Lp) are the prefill chunks, rows [Lp, Lp+Bd) the decodes, all in
 //   one [M, H] residual buffer; per layer
 //     RMSNorm -> QKV GEMM (all rows) -> rotary + KV-page append (all rows) ->
 //     chunk attention on rows [0, Lp) | decode attention on rows [Lp, M),
@@ -15,6 +15,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <array>
 #include <cmath>
 #include <cstring>
 #include <string>
@@ -70,6 +71,7 @@ struct sar_model {
   float* partials = nullptr;
   size_t partials_cap = 0;  // floats
   float* logits_stage = nullptr;
+  size_t logits_stage_rows = 0;
   int* err = nullptr;
   // step metadata: pinned host ring + device buffer
   int32_t* meta_host[kMetaRing] = {};
@@ -152,16 +154,42 @@ struct Plan {
   int M = 0, Lp = 0, Bd = 0, R = 0;
   // offsets into the metadata block (int32 elements)
   size_t o_pos = 0, o_slot = 0, o_pbt = 0, o_nkeys = 0, o_btoff = 0, o_btlen = 0, o_pbeg = 0, o_pcnt = 0,
-         o_items = 0, o_bt = 0, o_rows = 0, total = 0;
-  int n_items = 0, n_parts = 0, pbt_len = 0;
+         o_items = 0, o_bt = 0, o_rows = 0, o_tiles = 0, total = 0;
+  int n_items = 0, n_parts = 0, n_tiles = 0;
 };
+
+// The batch's prefill chunks in row order: `prefill` (if has_prefill), then more_prefill[].
+std::vector<sar_prefill> batch_chunks(const sar_batch* b) {
+  std::vector<sar_prefill> c;
+  if (b->has_prefill) c.push_back(b->prefill);
+  for (int i = 0; i < b->n_more_prefill; ++i) c.push_back(b->more_prefill[i]);
+  return c;
+}
+
+// Query rows per CTA of the chunk-attention kernel the step will launch.
+int chunk_tile_rows(const sar_dims& d, const sar_kv* kv) {
+  sar::ChunkAttnArgs probe{};
+  probe.d = d.head_dim;
+  probe.page_size = kv->page_size;
+  probe.qh = d.n_q_heads;
+  probe.kvh = d.n_kv_heads;
+  probe.window = d.sliding_window;
+  return sar::chunk_attention_tc_supported(probe) ? sar::kChunkTileRowsTc : sar::kChunkTileRows;
+}
 
 int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* p, std::vector<int32_t>* meta) {
   const sar_dims& d = m->d;
   if (b->n_decode < 0 || (b->n_decode > 0 && !b->decode)) return set_error(SAR_ERR_INVALID_ARG, "step: bad decode list");
-  const int Lp = b->has_prefill ? b->prefill.len : 0;
-  if (b->has_prefill && (b->prefill.len <= 0 || b->prefill.start_pos < 0 || !b->prefill.block_table))
-    return set_error(SAR_ERR_INVALID_ARG, "step: bad prefill chunk");
+  if (b->n_more_prefill < 0 || (b->n_more_prefill > 0 && !b->more_prefill))
+    return set_error(SAR_ERR_INVALID_ARG, "step: bad chunk list");
+  const std::vector<sar_prefill> chunks = batch_chunks(b);
+  int64_t lp64 = 0;
+  for (const sar_prefill& c : chunks) {
+    if (c.len <= 0 || c.start_pos < 0 || !c.block_table) return set_error(SAR_ERR_INVALID_ARG, "step: bad prefill chunk");
+    lp64 += c.len;
+  }
+  if (lp64 > d.max_tokens) return set_error(SAR_ERR_INVALID_ARG, "step: Lp + Bd exceeds max_tokens");
+  const int Lp = (int)lp64;
   const int Bd = b->n_decode;
   const int M = Lp + Bd;
   if (M == 0) return set_error(SAR_ERR_INVALID_ARG, "step: empty batch");
@@ -177,7 +205,7 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
       if (bt[i] < 0 || bt[i] >= kv->num_pages) return set_error(SAR_ERR_BOUNDS, "step: page id out of range");
     return SAR_OK;
   };
-  if (b->has_prefill) SAR_TRY(check_bt(b->prefill.block_table, b->prefill.n_blocks, b->prefill.start_pos + Lp - 1));
+  for (const sar_prefill& c : chunks) SAR_TRY(check_bt(c.block_table, c.n_blocks, c.start_pos + c.len - 1));
   // a decode with nk keys reads from the 16-key block holding its oldest
   // visible key (the kernel masks the keys of that block before it)
   auto first_key = [&](int nk) { return d.sliding_window > 0 ? std::max(0, nk - d.sliding_window) / 16 * 16 : 0; };
@@ -228,10 +256,44 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
     });
     for (int t : order) items.insert(items.end(), tail_items.begin() + 4 * t, tail_items.begin() + 4 * t + 4);
   }
-  // rows whose logits are returned: the chunk's last row, then every decode row
+  // rows whose logits are returned: every chunk's last row, then every decode row
   std::vector<int32_t> rows;
-  if (Lp > 0) rows.push_back(Lp - 1);
+  {
+    int r0 = 0;
+    for (const sar_prefill& c : chunks) {
+      r0 += c.len;
+      rows.push_back(r0 - 1);
+    }
+  }
   for (int i = 0; i < Bd; ++i) rows.push_back(Lp + i);
+  // chunk block tables (each cut to the pages its positions use) and the
+  // chunk-attention tiles: {first batch row, first position, rows, block-table
+  // offset, block-table length}, the most keys first (the longest CTAs start first)
+  const int tile_rows = chunk_tile_rows(d, kv);
+  std::vector<int32_t> pbt, tiles;
+  {
+    std::vector<std::array<int32_t, 8>> tl;
+    int r0 = 0;
+    for (const sar_prefill& c : chunks) {
+      const int off = (int)pbt.size();
+      const int nb = (c.start_pos + c.len - 1) / ps + 1;
+      pbt.insert(pbt.end(), c.block_table, c.block_table + nb);
+      for (int q0 = 0; q0 < c.len; q0 += tile_rows) {
+        const int rws = std::min(tile_rows, c.len - q0);
+        const int first = d.sliding_window > 0 ? std::max(0, c.start_pos + q0 - d.sliding_window + 1) : 0;
+        const int keys = c.start_pos + q0 + rws - first;
+        tl.push_back({r0 + q0, c.start_pos + q0, rws, off, nb, keys, 0, 0});
+      }
+      r0 += c.len;
+    }
+    std::stable_sort(tl.begin(), tl.end(), [](const std::array<int32_t, 8>& x, const std::array<int32_t, 8>& y) {
+      return x[5] > y[5];
+    });
+    for (auto& t : tl) {
+      t[5] = 0;
+      tiles.insert(tiles.end(), t.begin(), t.end());
+    }
+  }
 
   p->M = M;
   p->Lp = Lp;
@@ -239,12 +301,12 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
   p->R = (int)rows.size();
   p->n_items = (int)items.size() / 4;
   p->n_parts = n_parts;
-  p->pbt_len = b->has_prefill ? (b->prefill.start_pos + Lp - 1) / ps + 1 : 0;
+  p->n_tiles = (int)tiles.size() / 8;
   size_t o = 0;
   auto take = [&](size_t n) { size_t r = o; o += (n + 3) & ~size_t(3); return r; };  // 16-byte aligned pieces
   p->o_pos = take(M);
   p->o_slot = take(M);
-  p->o_pbt = take(p->pbt_len);
+  p->o_pbt = take(pbt.size());
   p->o_nkeys = take(Bd);
   p->o_btoff = take(Bd);
   p->o_btlen = take(Bd);
@@ -253,20 +315,25 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
   p->o_items = take(items.size());
   p->o_bt = take(bt.size());
   p->o_rows = take(rows.size());
+  p->o_tiles = take(tiles.size());
   p->total = o;
   meta->assign(o, 0);
   int32_t* mt = meta->data();
-  for (int i = 0; i < Lp; ++i) {
-    const int pos = b->prefill.start_pos + i;
-    mt[p->o_pos + i] = pos;
-    mt[p->o_slot + i] = b->prefill.block_table[pos / ps] * ps + pos % ps;
+  {
+    int r = 0;
+    for (const sar_prefill& c : chunks)
+      for (int i = 0; i < c.len; ++i, ++r) {
+        const int pos = c.start_pos + i;
+        mt[p->o_pos + r] = pos;
+        mt[p->o_slot + r] = c.block_table[pos / ps] * ps + pos % ps;
+      }
   }
   for (int i = 0; i < Bd; ++i) {
     const int pos = b->decode[i].ctx_len;
     mt[p->o_pos + Lp + i] = pos;
     mt[p->o_slot + Lp + i] = b->decode[i].block_table[pos / ps] * ps + pos % ps;
   }
-  if (p->pbt_len) std::memcpy(mt + p->o_pbt, b->prefill.block_table, p->pbt_len * 4);
+  if (!pbt.empty()) std::memcpy(mt + p->o_pbt, pbt.data(), pbt.size() * 4);
   std::memcpy(mt + p->o_nkeys, nkeys.data(), Bd * 4);
   std::memcpy(mt + p->o_btoff, btoff.data(), Bd * 4);
   std::memcpy(mt + p->o_btlen, btlen.data(), Bd * 4);
@@ -275,6 +342,7 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
   std::memcpy(mt + p->o_items, items.data(), items.size() * 4);
   std::memcpy(mt + p->o_bt, bt.data(), bt.size() * 4);
   std::memcpy(mt + p->o_rows, rows.data(), rows.size() * 4);
+  if (!tiles.empty()) std::memcpy(mt + p->o_tiles, tiles.data(), tiles.size() * 4);
   return SAR_OK;
 }
 
@@ -382,9 +450,8 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
       ca.k_cache = kc;
       ca.v_cache = vc;
       ca.bt = md + p.o_pbt;
-      ca.bt_len = p.pbt_len;
-      ca.start_pos = b->prefill.start_pos;
-      ca.len = p.Lp;
+      ca.tiles = md + p.o_tiles;
+      ca.n_tiles = p.n_tiles;
       ca.ld = m->qkv_n;
       ca.ld_out = m->qd;
       ca.qh = d.n_q_heads;
@@ -478,8 +545,9 @@ int sar_model_create(const sar_dims* dims, sar_model** out) {
   if (d.head_dim != 64 && d.head_dim != 128) return set_error(SAR_ERR_UNSUPPORTED, "model: head_dim must be 64 or 128");
   if (d.n_q_heads % d.n_kv_heads || d.n_q_heads / d.n_kv_heads > 8)
     return set_error(SAR_ERR_UNSUPPORTED, "model: n_q_heads must be 1..8 times n_kv_heads");
-  if (d.hidden % 64 || d.ffn % 64 || (d.n_q_heads * d.head_dim) % 64 || (d.n_kv_heads * d.head_dim) % 64)
-    return set_error(SAR_ERR_UNSUPPORTED, "model: widths must be multiples of 64");
+  if (d.hidden % 64 || d.ffn % 64 || (d.n_q_heads * d.head_dim) % 64 || (d.n_kv_heads * d.head_dim) % 64 ||
+      d.vocab % 64)
+    return set_error(SAR_ERR_UNSUPPORTED, "model: widths (and the vocabulary) must be multiples of 64");
   if (d.storage != SAR_STORAGE_F16 && d.storage != SAR_STORAGE_BF16)
     return set_error(SAR_ERR_INVALID_ARG, "model: storage must be SAR_STORAGE_F16 or SAR_STORAGE_BF16");
   sar_model* m = new sar_model();
@@ -516,7 +584,7 @@ int sar_model_create(const sar_dims* dims, sar_model** out) {
   }
   // step workspace
   const size_t T = d.max_tokens;
-  const size_t R = (size_t)d.max_decodes + 1;
+  const size_t R = T;  // head rows: every chunk's last row and every decode row (at most all rows)
   const size_t ws = align256(T * H * 2) + align256(T * (d.head_dim / 2) * 8) + align256(T * m->qd * 2) + align256(T * F * 2) +
                     align256(T * H * 4) + align256(R * H * 2) + align256(T * H * 2) + align256(T * m->qkv_n * 4) + 256;
   e = cudaMalloc(&m->ws, ws);
@@ -693,13 +761,24 @@ int sar_step_host(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, 
   if (!m || !kv || !b || !in) return set_error(SAR_ERR_INVALID_ARG, "step_host: null argument");
   if (layer_out) return set_error(SAR_ERR_INVALID_ARG, "step_host: layer outputs are only returned on device");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int M = (b->has_prefill ? b->prefill.len : 0) + b->n_decode;
+  if (b->n_more_prefill < 0 || (b->n_more_prefill > 0 && !b->more_prefill))
+    return set_error(SAR_ERR_INVALID_ARG, "step_host: bad chunk list");
+  int64_t M = b->n_decode;
+  for (const sar_prefill& c : batch_chunks(b)) M += c.len;
   if (M <= 0 || M > m->d.max_tokens) return set_error(SAR_ERR_INVALID_ARG, "step_host: bad row count");
-  const int R = (b->has_prefill ? 1 : 0) + b->n_decode;
+  const int R = (b->has_prefill ? 1 : 0) + b->n_more_prefill + b->n_decode;
   const size_t in_bytes = b->in_kind == SAR_IN_TOKENS ? (size_t)M * 4 : (size_t)M * m->d.hidden * 2;
   SAR_TRY(check(cudaMemcpyAsync(m->in_stage, in, in_bytes, cudaMemcpyHostToDevice, s), "step_host: input copy"));
-  if (logits_out && !m->logits_stage) {
-    SAR_TRY(check(cudaMalloc(&m->logits_stage, (size_t)(m->d.max_decodes + 1) * m->d.vocab * 4), "step_host: logits stage"));
+  if (logits_out && (size_t)R > m->logits_stage_rows) {
+    if (m->logits_stage) {
+      SAR_TRY(check(cudaStreamSynchronize(s), "step_host: logits stage resize"));
+      cudaFree(m->logits_stage);
+      m->logits_stage = nullptr;
+      m->logits_stage_rows = 0;
+    }
+    const size_t rows = std::max<size_t>((size_t)R, (size_t)m->d.max_decodes + 1);
+    SAR_TRY(check(cudaMalloc(&m->logits_stage, rows * m->d.vocab * 4), "step_host: logits stage"));
+    m->logits_stage_rows = rows;
   }
   SAR_TRY(run_step(m, kv, b, m->in_stage, m->hres, logits_out ? m->logits_stage : nullptr, nullptr, s));
   if (hidden_out)

@@ -25,7 +25,7 @@ class TraceResult:
     busy_s: float = 0.0
     wall_s: float = 0.0
     now_log: list = dataclasses.field(default_factory=list)
-    batches: list = dataclasses.field(default_factory=list)     # (prefill, decodes) per step
+    batches: list = dataclasses.field(default_factory=list)     # (chunks, decodes) per step
     sampled: list = dataclasses.field(default_factory=list)     # token ids per step
     step_ms: list = dataclasses.field(default_factory=list)
     ttft: dict = dataclasses.field(default_factory=dict)        # req -> seconds
@@ -47,21 +47,23 @@ class TraceResult:
 
 def run_trace(model, kv, trace, prompt_tokens: dict, tau: int, tile: int = 128, max_batch: int = 256,
               now_log=None, max_steps: int | None = None, keep_batches: bool = True,
-              on_step=None) -> TraceResult:
+              on_step=None, max_chunks: int = 0) -> TraceResult:
     """Runs every request of ``trace`` to completion.
 
     ``now_log``: replay these times instead of the wall clock (one per step).
     ``on_step(i, batch, x, hidden, logits)`` is called after each step's launch.
+    ``max_chunks``: the scheduler's cap on prefill chunks per batch (0 = none).
     """
     dims = model.dims
-    sched = Scheduler(tau, tile, kv.page_size, kv.num_pages, max_batch)
+    sched = Scheduler(tau, tile, kv.page_size, kv.num_pages, max_batch, max_chunks=max_chunks)
     for r in trace:
         sched.add(r.req, r.arrival, r.prompt_len, r.output_len, prompt_tokens[r.req])
     res = TraceResult()
-    logits = torch.empty(max_batch + 1, dims.vocab, dtype=torch.float32, device="cuda")
+    max_rows = max_batch + tau  # every chunk's last row and every decode row
+    logits = torch.empty(max_rows, dims.vocab, dtype=torch.float32, device="cuda")
     tok_dev = torch.empty(tau, dtype=torch.int32, device="cuda")
-    sampled_dev = torch.empty(max_batch + 1, dtype=torch.int32, device="cuda")
-    sampled_host = torch.empty(max_batch + 1, dtype=torch.int32).pin_memory()
+    sampled_dev = torch.empty(max_rows, dtype=torch.int32, device="cuda")
+    sampled_host = torch.empty(max_rows, dtype=torch.int32).pin_memory()
     tok_host = torch.empty(tau, dtype=torch.int32).pin_memory()
     last_emit = {}
     by_req = {r.req: r for r in trace}
@@ -74,22 +76,22 @@ def run_trace(model, kv, trace, prompt_tokens: dict, tau: int, tile: int = 128, 
         if max_steps is not None and i >= max_steps:
             break
         now = now_log[i] if now_log is not None else time.perf_counter() - t0
-        pre, decs, tokens, _ = sched.next(now)
-        m = (pre[2] if pre else 0) + len(decs)
+        chunks, decs, tokens, _ = sched.next(now)
+        m = sum(c[2] for c in chunks) + len(decs)
         if m == 0:
             if now_log is None:
                 nxt = min((r.arrival for r in trace if r.arrival > now), default=now)
                 time.sleep(max(0.0, min(nxt - now, 0.05)))
             sched.commit([])
             res.now_log.append(now)
-            res.batches.append((None, []))
+            res.batches.append(([], []))
             res.sampled.append([])
             i += 1
             continue
         ts = time.perf_counter()
         tok_host[:m] = torch.tensor(tokens, dtype=torch.int32)
         tok_dev[:m].copy_(tok_host[:m], non_blocking=True)
-        b = Batch(pre, decs, in_kind=SAR_IN_TOKENS)
+        b = Batch(chunks, decs, in_kind=SAR_IN_TOKENS)
         rows = b.logit_rows
         model.step(kv, b, tok_dev[:m], logits_out=logits[:rows])
         model.sample_greedy(logits[:rows], rows, sampled_dev[:rows])
@@ -106,11 +108,10 @@ def run_trace(model, kv, trace, prompt_tokens: dict, tau: int, tile: int = 128, 
         res.rows += m
         res.now_log.append(now)
         if keep_batches:
-            res.batches.append((pre, decs))
+            res.batches.append((chunks, decs))
             res.sampled.append(sampled)
         # latency bookkeeping: the chunk that completes a prompt emits its first token
-        if pre is not None:
-            req, start, n, _ = pre
+        for req, start, n, _ in chunks:
             if start + n == by_req[req].prompt_len:
                 res.ttft[req] = wall - by_req[req].arrival
                 last_emit[req] = wall

@@ -170,25 +170,33 @@ typedef struct sar_decode {
 
 enum { SAR_IN_HIDDEN = 0, SAR_IN_TOKENS = 1 };
 
-/* At most one chunk (rows [0, Lp)) followed by n_decode decodes (rows
- * [Lp, Lp+n_decode)) -- the batch Algorithm 3 builds. */
+/* Prefill chunks followed by n_decode decodes -- the batch Algorithm 3
+ * builds (Sarathi-Serve digest, section 3 flowchart: the ongoing prompt's
+ * chunk, then the first chunks of newly admitted requests, then decodes).
+ * The chunks are `prefill` (when has_prefill) and then more_prefill[0 ..
+ * n_more_prefill), each of a different request; their rows are stacked in
+ * that order ([0, Lp) with Lp the sum of their lengths), then the decode
+ * rows [Lp, Lp+n_decode). */
 typedef struct sar_batch {
   int32_t has_prefill;
   sar_prefill prefill;
   int32_t n_decode;
   const sar_decode* decode; /* host array [n_decode] */
   int32_t in_kind;          /* SAR_IN_HIDDEN or SAR_IN_TOKENS */
+  int32_t n_more_prefill;   /* further chunks (0 = at most the one above) */
+  const sar_prefill* more_prefill; /* host array [n_more_prefill] */
 } sar_batch;
 
 /* Runs every layer over the stacked rows M = Lp + n_decode and then the head.
+ * A request may appear in at most one chunk or decode of a batch.
  * hidden_out and logits_out must be 16-byte aligned, bf16 `in` 8-byte aligned
  * (else SAR_ERR_INVALID_ARG before any launch).
  *   in         device: bf16 [M, hidden] (SAR_IN_HIDDEN) or int32 [M] token ids
  *   hidden_out device fp32 [M, hidden]: last layer's residual stream (before
  *              the final norm); may be NULL
- *   logits_out device fp32 [R, vocab], R = has_prefill + n_decode: logits of
- *              the chunk's last row (if any) then of every decode row; may be
- *              NULL (head skipped); must be NULL when vocab = 0
+ *   logits_out device fp32 [R, vocab], R = chunks + n_decode: logits of
+ *              every chunk's last row (in chunk order) then of every decode
+ *              row; may be NULL (head skipped); must be NULL when vocab = 0
  *   layer_out  device fp32 [n_layers, M, hidden]: every layer's output; may be NULL
  * New K/V of all rows are written into `kv`.  Asynchronous on `stream`; the
  * host block tables are consumed before the call returns. */
@@ -274,13 +282,19 @@ int sar_profile_read(sar_model* m, double* ms, int64_t* launches, int32_t n_kind
 
 /* tau: token budget, rounded down to a multiple of `tile` (must be >= tile).
  * page_size/num_pages: the KV pool the scheduler hands pages from.
- * max_batch: most requests holding pages at once. */
+ * max_batch: most requests holding pages at once.
+ * max_chunks: most prefill chunks in one batch; 0 = no cap (Algorithm 3's
+ * admission loop: after the ongoing prompt's chunk, waiting requests are
+ * admitted first come first served while they can be allocated and the
+ * budget lasts); 1 = one chunk per batch, a new request only when no prompt
+ * is unfinished. */
 typedef struct sar_sched_cfg {
   int32_t tau;
   int32_t tile;
   int32_t page_size;
   int32_t num_pages;
   int32_t max_batch;
+  int32_t max_chunks;
 } sar_sched_cfg;
 
 int sar_sched_create(const sar_sched_cfg* cfg, sar_sched** out);
@@ -291,14 +305,17 @@ int sar_sched_add(sar_sched* s, int32_t req, double arrival, int32_t prompt_len,
                   int32_t output_len, const int32_t* prompt_tokens);
 
 /* Builds the next batch at time `now` (requests with arrival <= now are
- * eligible): all running decodes, then at most one prefill chunk.  `out`
+ * eligible): all running decodes, then the unfinished prompt's next chunk
+ * (at most one prompt is unfinished at any time), then new requests' first
+ * chunks while the budget lasts (see max_chunks).  The first chunk is
+ * out->prefill, the others out->more_prefill.  `out`
  * points into scheduler-owned memory valid until the next call.  tokens_out
  * (nullable) receives a pointer to M input ids, or NULL if unknown.
  * Returns SAR_ERR_NO_PAGES if a decode needs a page and none is free. */
 int sar_sched_next(sar_sched* s, double now, sar_batch* out, const int32_t** tokens_out);
 
 /* Advances state with the sampled token of every logits row of the last
- * batch (chunk's last row first, then decodes).  n_finished (nullable)
+ * batch (each chunk's last row in chunk order, then decodes).  n_finished (nullable)
  * receives how many requests completed; their pages are returned. */
 int sar_sched_commit(sar_sched* s, const int32_t* sampled, int32_t n_sampled,
                      int32_t* n_finished);

@@ -210,6 +210,23 @@ def window_case(seed: int = 0, d: Dims = SMALL_128, prompt_len: int = 640, ctxs=
                 histories=hist)
 
 
+SMALL_128_HEAD = dataclasses.replace(SMALL_128, vocab=1024)
+
+
+def multi_chunk_case(seed: int = 0, d: Dims = SMALL_128_HEAD, prompt_lens=(300, 180, 90),
+                     ctxs=(70, 150, 260, 333)):
+    """A one-layer case for batches of several prefill chunks: prompts of
+    ``prompt_lens`` N(0,1) rows and decodes at contexts ``ctxs`` with random
+    N(0,1) K/V histories and one N(0,1) input row each.  Draw order after the
+    weights (and head): the prompts, the decode inputs, then the histories."""
+    layers, head, gen = model_weights(seed, d, torch.bfloat16)
+    prompts = [normal(gen, (n, d.hidden), 1.0, torch.bfloat16) for n in prompt_lens]
+    decode_inputs = normal(gen, (len(ctxs), d.hidden), 1.0, torch.bfloat16)
+    hist = [kv_history(gen, 1, c, d, torch.bfloat16)[0] for c in ctxs]
+    return dict(dims=d, layers=layers, head=head, prompts=prompts, ctxs=list(ctxs),
+                decode_inputs=decode_inputs, histories=hist)
+
+
 MISTRAL_STARTS = (0, 512, 1536)
 
 

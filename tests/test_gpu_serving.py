@@ -64,13 +64,13 @@ def test_trace_runs_and_replays_bit_exactly(mistral32):
     m.sync_status()
     assert res.steps > 0
     # replay: the oracle scheduler, same times, same sampled tokens -> same batches
-    o = osch.StallFreeScheduler(512, 128, kv.page_size, kv.num_pages, 256, max_chunks=1)
+    o = osch.StallFreeScheduler(512, 128, kv.page_size, kv.num_pages, 256)
     for r in trace:
         o.add(r.req, r.arrival, r.prompt_len, r.output_len, toks[r.req])
     for i, now in enumerate(res.now_log):
         ob = o.next(now)
-        pre, decs = res.batches[i]
-        assert (tuple(pre) if pre else None) == (tuple(ob.prefill) if ob.prefill else None), i
+        chunks, decs = res.batches[i]
+        assert [tuple(c) for c in chunks] == [tuple(c) for c in ob.prefills], i
         assert decs == ob.decodes, i
         o.commit(res.sampled[i])
     assert o.idle()
