@@ -490,7 +490,7 @@ def run_sweep(args):
 
 def run_trace_mode(args):
     """The 32-layer Mistral-7B shape served from a request trace (256 requests,
-    Poisson arrivals at 4 req/s, lognormal prompt / output lengths) by the
+    Poisson arrivals at 4 req/s by default, lognormal prompt / output lengths) by the
     stall-free scheduler at each token budget, arrivals on the wall clock.
     One JSON line with tokens/s, step latency and TTFT / TBT percentiles per
     budget."""
@@ -506,7 +506,7 @@ def run_trace_mode(args):
     page_bytes = dims.n_layers * 2 * dims.kv_dim * PAGE * 2
     n_pages = int(free * 0.8) // page_bytes
     kv = sar.KVCache(m, PAGE, n_pages)
-    trace = synth.request_trace(0, args.requests, rate=4.0, prompt_median=1024, prompt_clip=(64, 8192),
+    trace = synth.request_trace(0, args.requests, rate=args.rate, prompt_median=1024, prompt_clip=(64, 8192),
                                 out_median=256, out_clip=(16, 1024))
     toks = synth.prompt_tokens(1, trace, dims.vocab)
     runs = {}
@@ -524,7 +524,7 @@ def run_trace_mode(args):
     adm = "one chunk per batch" if args.max_chunks == 1 else (
         f"at most {args.max_chunks} chunks per batch" if args.max_chunks else "Algorithm 3 admission loop")
     out = {"mode": "trace", "workload": f"Mistral-7B shape, 32 layers + 32000 head, {attn}, f16 storage, {adm}; "
-           f"{args.requests} requests, Poisson 4 req/s, prompt lognormal(median 1024, sigma 1, clip 64-8192), "
+           f"{args.requests} requests, Poisson {args.rate:g} req/s, prompt lognormal(median 1024, sigma 1, clip 64-8192), "
            f"output lognormal(median 256, sigma 1, clip 16-1024), greedy sampling, wall-clock arrivals",
            "kv_pages": n_pages, "page_size": PAGE, "per_tau": runs}
     print(json.dumps(out))
@@ -633,6 +633,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="long-prompt mode: fewer layers (profiling)")
     ap.add_argument("--no-warmup", action="store_true", help="long-prompt mode: no untimed prefill first")
     ap.add_argument("--model", choices=["yi34b", "mistral7b"], default="yi34b", help="long-prompt mode: model shape")
+    ap.add_argument("--rate", type=float, default=4.0, help="trace mode: Poisson arrival rate (requests/s)")
     ap.add_argument("--max-chunks", type=int, default=0,
                     help="trace mode: prefill chunks per batch (0 = Algorithm 3's admission loop, 1 = one chunk)")
     ap.add_argument("--window", type=int, default=0,
