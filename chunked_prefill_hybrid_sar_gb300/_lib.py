@@ -32,6 +32,7 @@ SAR_GEMM_AUTO, SAR_GEMM_M128_N128, SAR_GEMM_M128_N256, SAR_GEMM_SWAP, SAR_GEMM_M
 SAR_GEMM_CLUSTER_1, SAR_GEMM_CLUSTER_2, SAR_GEMM_CLUSTER_4 = 0x100, 0x200, 0x400
 SAR_GEMM_PAIR_N256, SAR_GEMM_PAIR_N128 = 5, 6
 SAR_GEMM_TWO_CTAS = 0x1000
+SAR_GEMM_STREAM_K = 0x2000
 
 KERNEL_KINDS = ("embed", "rmsnorm", "gemm_qkv", "rope_append", "chunk_attn", "decode_attn", "gemm_o",
                 "gemm_gateup", "gemm_down", "head_norm", "gemm_head")

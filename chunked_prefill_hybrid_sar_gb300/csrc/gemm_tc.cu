@@ -66,6 +66,7 @@ struct Params {
   int M, N, K;
   int bn, m_tiles, n_tiles, k_blocks, stages, stage_bytes, tmem_cols;
   int splits, kb_per_split;  // split-K: `splits` K ranges per tile (residual epilogue only)
+  int sk;                    // stream-K: equal shares of every token group's (weight tile, K slab) runs (residual only)
   int cl, m_groups;          // cluster size sharing one weight tile (multicast); token-tile groups
   RopeEpi rope;              // kEpiRope only
   void* c;
@@ -90,6 +91,49 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int u, int rank) {
   w.kb0 = sp * p.kb_per_split;
   w.kb1 = min(p.k_blocks, w.kb0 + p.kb_per_split);
   return w;
+}
+
+// A cluster's work: units cid, cid + C, ... (split-K units), or with
+// stream-K one token group's equal share of its (weight tile, K slab) runs:
+// cluster c takes group g = c % G and share j = c / G of the S = n_tiles x
+// k_blocks slabs, [j*S/Cg, (j+1)*S/Cg) with Cg = C / G clusters per group,
+// cut at weight-tile boundaries.  Clusters j of every group walk the same
+// weight slabs at the same time, so each slab leaves HBM once and the other
+// groups read it from L2 (as the groups of one split-K unit do).
+struct Work {
+  int t, end, step, g;
+};
+__device__ __forceinline__ Work work_begin(const Params& p, int cid, int n_clusters) {
+  Work w;
+  if (p.sk) {
+    const int cg = n_clusters / p.m_groups;  // clusters per token group (the rest idle)
+    const int j = cid / p.m_groups;
+    const long long S = (long long)p.n_tiles * p.k_blocks;
+    w.g = cid % p.m_groups;
+    w.t = j < cg ? (int)(S * j / cg) : 0;
+    w.end = j < cg ? (int)(S * (j + 1) / cg) : 0;
+    w.step = 0;
+  } else {
+    w.t = cid;
+    w.end = p.m_groups * p.n_tiles * p.splits;
+    w.step = n_clusters;
+    w.g = 0;
+  }
+  return w;
+}
+__device__ __forceinline__ bool work_next(const Params& p, Work& w, int rank, Unit& un) {
+  if (w.t >= w.end) return false;
+  if (p.sk) {
+    un.nt = w.t / p.k_blocks;
+    un.mt = w.g * p.cl + rank;
+    un.kb0 = w.t - un.nt * p.k_blocks;
+    un.kb1 = min(p.k_blocks, un.kb0 + (w.end - w.t));
+    w.t += un.kb1 - un.kb0;
+    return true;
+  }
+  un = unit_of(p, w.t, rank);
+  w.t += w.step;
+  return true;
 }
 
 __device__ __forceinline__ void next_stage(int& stage, uint32_t& phase, int stages) {
@@ -152,13 +196,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rank = p.cl > 1 ? (int)cluster_ctarank() : 0;
   const int cid = blockIdx.x / p.cl, n_clusters = gridDim.x / p.cl;
   const uint16_t cl_mask = (uint16_t)((1u << p.cl) - 1u);
-  const int n_tiles_total = p.m_groups * p.n_tiles * p.splits;  // work units per cluster
   const int acc_cols = MSUB * p.bn;
+  Unit un0;
+  Work w0 = work_begin(p, cid, n_clusters);
 
-  if (warp == 0 && lane == 0 && cid < n_tiles_total) {
+  if (warp == 0 && lane == 0 && work_next(p, w0, rank, un0)) {
     // the weights do not depend on the previous kernel: start pulling this
     // CTA's first weight slabs into L2 while that kernel drains
-    const Unit un = unit_of(p, cid, rank);
+    const Unit& un = un0;
     const void* w_map = SWAP ? (const void*)&tm_a : (const void*)&tm_b;
     const int slice = PAIR ? p.bn / 2 : p.bn / p.cl;
     const int w_row = SWAP ? un.nt * 128 : un.nt * p.bn + rank * slice;
@@ -174,8 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = cid; t < n_tiles_total && ok; t += n_clusters) {
-        const Unit un = unit_of(p, t, rank);
+      Work wk = work_begin(p, cid, n_clusters);
+      Unit un;
+      for (bool first = true; ok && work_next(p, wk, rank, un); first = false) {
         const int mt = un.mt, nt = un.nt;
         // A rows: tokens (non-swap) or weights (swap); B rows: the other one.
         const int a_row = SWAP ? nt * 128 : mt * 128 * MSUB;
@@ -188,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int w_row = SWAP ? a_row : b_row + rank * slice;
         // (swap tiling: one CTA per weight tile, no reuse to gain from L2;
         // the first unit's first slabs were requested before the wait above)
-        if (!SWAP && t != cid)
+        if (!SWAP && !first)
           for (int kb = un.kb0; kb < un.kb0 + kPrefetch && kb < un.kb1; ++kb) tma_prefetch_l2(w_map, kb * kBK, w_row);
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (!SWAP && kb + kPrefetch < un.kb1) tma_prefetch_l2(w_map, (kb + kPrefetch) * kBK, w_row);
@@ -237,13 +283,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       int i = 0;
-      for (int t = cid; t < n_tiles_total && ok; t += n_clusters, ++i) {
+      Work wk = work_begin(p, cid, n_clusters);
+      Unit un;
+      for (; ok && work_next(p, wk, rank, un); ++i) {
         const int acc = i & 1;
         const uint32_t accph = (uint32_t)((i >> 1) & 1);
         if (!mbar_wait(smem_u32(&acce_bar[acc]), accph ^ 1u, p.err, SITE_GEMM_MMA)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * acc_cols);
-        const Unit un = unit_of(p, t, rank);
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.err, SITE_GEMM_MMA)) {
             ok = false;
@@ -284,9 +331,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lrow = q * 32 + lane;     // accumulator lane = row of the MMA's M side
     int i = 0;
     bool alive = true;  // false once a wait gave up: loads/stores stop, barriers stay matched
-    for (int t = cid; t < n_tiles_total; t += n_clusters, ++i) {
-      const Unit un = unit_of(p, t, rank);
+    Work wk = work_begin(p, cid, n_clusters);
+    Unit un;
+    for (; work_next(p, wk, rank, un); ++i) {
       const int mt = un.mt, nt = un.nt;
+      // a share of a tile's K range adds into C; a whole tile writes C = D + R
+      const bool partial = p.splits > 1 || un.kb0 != 0 || un.kb1 != p.k_blocks;
+      (void)partial;
       const int acc = i & 1;
       const uint32_t accph = (uint32_t)((i >> 1) & 1);
       if (alive) alive = warp_wait(smem_u32(&accf_bar[acc]), accph, p.err, SITE_GEMM_EPILOGUE);
@@ -451,8 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float4* rs = reinterpret_cast<const float4*>(
                     reinterpret_cast<const float*>(p.r) + (size_t)row * p.N + col);
                 float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.c) + (size_t)row * p.N + col);
-                if (p.splits > 1) {
-                  // split-K: every K range adds its share into C (== R) in place
+                if (partial) {
+                  // split-K / stream-K: every K range adds its share into C (== R) in place
 #pragma unroll
                   for (int e = 0; e < 4; ++e)
                     atomicAdd(&dst[e], make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
@@ -575,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if constexpr (EPI == SAR_EPI_F32) {
                 reinterpret_cast<float*>(p.c)[idx] = f;
               } else if constexpr (EPI == SAR_EPI_RESIDUAL) {
-                if (p.splits > 1)
+                if (partial)
                   atomicAdd(reinterpret_cast<float*>(p.c) + idx, f);
                 else
                   reinterpret_cast<float*>(p.c)[idx] = f + reinterpret_cast<const float*>(p.r)[idx];
@@ -676,7 +727,9 @@ int make_tmap_16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols
 int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in_place) {
   const int cl_flag = variant & (SAR_GEMM_CLUSTER_1 | SAR_GEMM_CLUSTER_2 | SAR_GEMM_CLUSTER_4);
   const bool two_ctas = (variant & SAR_GEMM_TWO_CTAS) != 0;
-  variant &= ~(SAR_GEMM_CLUSTER_1 | SAR_GEMM_CLUSTER_2 | SAR_GEMM_CLUSTER_4 | SAR_GEMM_TWO_CTAS);
+  const bool want_sk = (variant & SAR_GEMM_STREAM_K) != 0;
+  variant &= ~(SAR_GEMM_CLUSTER_1 | SAR_GEMM_CLUSTER_2 | SAR_GEMM_CLUSTER_4 | SAR_GEMM_TWO_CTAS | SAR_GEMM_STREAM_K);
+  const bool auto_variant = variant == SAR_GEMM_AUTO;
   if (cl_flag & (cl_flag - 1)) return set_error(SAR_ERR_INVALID_ARG, "gemm: more than one cluster flag");
   if (M < 1 || N < 64 || K < 64 || N % 64 || K % 64)
     return set_error(SAR_ERR_UNSUPPORTED, "gemm: need M >= 1, N and K multiples of 64");
@@ -788,11 +841,25 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
   if (c.stages < 2) return set_error(SAR_ERR_UNSUPPORTED, "gemm: tile does not fit shared memory");
   c.smem = c.stages * stage_bytes + extra;
   c.splits = 1;
-  best_split((long)c.m_groups * c.n_tiles, c.swap ? kslab_clocks(1, c.bn) : kslab_clocks(c.msub, c.bn, c.pair),
-             &c.splits, (long)sms * c.per_sm / c.cl);
+  const long per_kb = c.swap ? kslab_clocks(1, c.bn) : kslab_clocks(c.msub, c.bn, c.pair);
+  const long slots = (long)sms * c.per_sm / c.cl;
+  const long split_cost = best_split((long)c.m_groups * c.n_tiles, per_kb, &c.splits, slots);
+  if (want_sk && (!can_split || c.swap || c.m_groups > slots))
+    return set_error(SAR_ERR_UNSUPPORTED,
+                     "gemm: stream-K needs a non-swap tiling, the in-place residual epilogue and a cluster per token group");
+  // stream-K only on request: on the projections of a 512-row step it measured
+  // slower than the best split-K (O 32.1 vs 27.2 us, down 51.7 vs 48.3 us), as
+  // its extra partial-tile atomic adds all land at the end of the kernel
+  (void)split_cost;
+  (void)auto_variant;
+  if (want_sk) {
+    c.sk = 1;
+    c.splits = 1;
+  }
   c.kb_per_split = (k_blocks + c.splits - 1) / c.splits;
   c.splits = (k_blocks + c.kb_per_split - 1) / c.kb_per_split;  // no empty K range
-  c.grid = std::min(c.m_tiles * c.n_tiles * c.splits, sms * c.per_sm) / c.cl * c.cl;  // whole clusters; refined at launch
+  c.grid = c.sk ? (int)(slots * c.cl)
+                : std::min(c.m_tiles * c.n_tiles * c.splits, sms * c.per_sm) / c.cl * c.cl;  // refined at launch
   *cfg = c;
   return SAR_OK;
 }
@@ -819,8 +886,9 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   p.k_blocks = K / kBK;
   p.splits = cfg.splits;
   p.kb_per_split = cfg.kb_per_split;
-  if (cfg.splits > 1 && c != residual)
-    return set_error(SAR_ERR_INVALID_ARG, "gemm: split-K needs the residual output in place");
+  p.sk = cfg.sk;
+  if ((cfg.splits > 1 || cfg.sk) && (c != residual || epi != SAR_EPI_RESIDUAL))
+    return set_error(SAR_ERR_INVALID_ARG, "gemm: split-K / stream-K needs the residual output in place");
   p.stages = cfg.stages;
   p.stage_bytes = cfg.stage_bytes;
   p.tmem_cols = pow2_at_least(2 * cfg.msub * cfg.bn);
@@ -872,7 +940,10 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
       if (e != cudaSuccess || mc < 1) return cuda_error(e != cudaSuccess ? e : cudaErrorInvalidConfiguration,
                                                          "gemm: cluster occupancy");
     }
-    grid = std::min(cfg.m_groups * cfg.n_tiles * cfg.splits, mc) * cfg.cl;
+    // stream-K: every resident cluster takes a share
+    grid = (cfg.sk ? mc : std::min(cfg.m_groups * cfg.n_tiles * cfg.splits, mc)) * cfg.cl;
+    if (cfg.sk && mc < cfg.m_groups)
+      return set_error(SAR_ERR_UNSUPPORTED, "gemm: stream-K needs a resident cluster per token group");
   }
   lc.gridDim = dim3(grid);
   cudaError_t e = cudaLaunchKernelExC(&lc, fn, args);

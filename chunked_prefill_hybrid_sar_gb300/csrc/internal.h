@@ -69,6 +69,7 @@ struct GemmCfg {
   int per_sm = 1;        // CTAs resident per SM (2: swap tiling, half the stages each)
   int cl = 1;            // CTAs per cluster sharing a weight tile by multicast (non-swap)
   int m_groups = 0;      // token-tile groups of cl tiles
+  int sk = 0;            // stream-K: equal K-slab shares over all resident clusters (residual epilogue)
 };
 
 // Box rows of the weight maps a model keeps per matrix (index i: 32 << i); the

@@ -58,7 +58,15 @@ enum {
   /* Optional flag for the swap tiling with at most 128 token rows: two CTAs
    * per SM, each with half the pipeline, so twice as many weight slabs are in
    * flight per SM (the memory-bound regime). */
-  SAR_GEMM_TWO_CTAS = 0x1000
+  SAR_GEMM_TWO_CTAS = 0x1000,
+  /* Optional flag for the in-place fp32 residual epilogue (non-swap tilings):
+   * stream-K.  Every resident CTA (pair) takes an equal, contiguous share of
+   * all tiles' 64-wide K slabs, so a few tiles spread over all SMs instead of
+   * leaving a partial wave; a share that covers part of a tile's K range adds
+   * its partial sum into C atomically (as split-K does).  Each token group's
+   * weight slabs are shared out separately, so the groups read a weight slab
+   * at the same time (once from HBM).  AUTO does not take it. */
+  SAR_GEMM_STREAM_K = 0x2000
 };
 
 /* C = epilogue(A . W^T).  A [M, K], W [N, K] in the storage type `storage`

@@ -269,3 +269,41 @@ def test_gemm_swap_two_ctas_per_sm(M, epi):
         sar.gemm(torch.zeros(200, K, dtype=torch.float16, device=DEV), w,
                  torch.zeros(200, N, dtype=torch.float16, device=DEV),
                  variant=sar.SAR_GEMM_SWAP | sar.SAR_GEMM_TWO_CTAS)
+
+
+@pytest.mark.parametrize("M,N,K,variant,flags", [
+    (512, 4096, 4096, "pair256", 0),         # the O projection at 512 rows
+    (512, 4096, 14336, "pair256", 0),        # the down projection at 512 rows
+    (1000, 6144, 4096, "pair128", 0),        # ragged token tiles, an all-padding partner tile
+    (300, 1024, 4096, "m128n256", 0),        # single CTAs, ragged rows
+    (512, 2048, 8192, "m128n256", sar.SAR_GEMM_CLUSTER_2),  # with weight multicast
+    (100, 192, 320, "m128n128", 0),          # fewer K slabs than CTAs: most shares are empty
+])
+def test_gemm_stream_k_residual_in_place(M, N, K, variant, flags):
+    """Stream-K: every resident CTA (pair) takes an equal run of all tiles' K
+    slabs and adds partial tiles atomically; the result equals one full-K
+    accumulation up to fp32 rounding."""
+    a, w, r = operands(M, N, K, 11)
+    h = r.to(DEV).clone()
+    sar.gemm(a.to(DEV), w.to(DEV), h, residual=h, epilogue=sar.SAR_EPI_RESIDUAL,
+             variant=VARIANTS[variant] | flags | sar.SAR_GEMM_STREAM_K)
+    torch.cuda.synchronize()
+    ref = a.double() @ w.double().T + r.double()
+    tol = max(1e-5, 3e-7 * K ** 0.5)
+    assert ((h.double().cpu() - ref).abs().max() / ref.abs().max()).item() < tol
+
+
+def test_gemm_stream_k_is_refused_where_partial_sums_cannot_add():
+    a = torch.zeros(512, 1024, dtype=torch.float16, device=DEV)
+    w = torch.zeros(1024, 1024, dtype=torch.float16, device=DEV)
+    c16 = torch.zeros(512, 1024, dtype=torch.float16, device=DEV)
+    c32 = torch.zeros(512, 1024, dtype=torch.float32, device=DEV)
+    r32 = torch.zeros(512, 1024, dtype=torch.float32, device=DEV)
+    with pytest.raises(sar.SarError):  # a stored (rounded) output
+        sar.gemm(a, w, c16, variant=sar.SAR_GEMM_PAIR_N256 | sar.SAR_GEMM_STREAM_K)
+    with pytest.raises(sar.SarError):  # residual out of place
+        sar.gemm(a, w, c32, residual=r32, epilogue=sar.SAR_EPI_RESIDUAL,
+                 variant=sar.SAR_GEMM_PAIR_N256 | sar.SAR_GEMM_STREAM_K)
+    with pytest.raises(sar.SarError):  # swap tiling
+        sar.gemm(a[:64], w, c32[:64], residual=c32[:64], epilogue=sar.SAR_EPI_RESIDUAL,
+                 variant=sar.SAR_GEMM_SWAP | sar.SAR_GEMM_STREAM_K)
