@@ -180,11 +180,18 @@ def run_ours(args):
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
     dims, m, kv, cases, ctxs = setup_gpu()
+    if args.overlap:
+        m.set_overlap(True)
     hid = torch.empty(TAU, dims.hidden, dtype=torch.float32, device="cuda")
     logits = torch.empty(BD + 1, dims.vocab, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
+    graphs, graph_launches = None, 0
+
     def step(i):
+        if graphs:
+            graphs[i % len(cases)].launch()
+            return
         b, x = cases[i % len(cases)]
         m.step(kv, b, x, hidden_out=hid, logits_out=logits)
 
@@ -192,6 +199,14 @@ def run_ours(args):
         step(i)
     torch.cuda.synchronize()
     m.sync_status()
+    if args.graph:
+        # one captured step per case (the cases repeat unchanged)
+        l0 = sar.launch_count()
+        graphs = [sar.StepGraph(m, kv, b, x, hidden_out=hid, logits_out=logits) for b, x in cases]
+        graph_launches = (sar.launch_count() - l0) / len(cases)
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
 
     def barrier():
         if world > 1:
@@ -211,6 +226,9 @@ def run_ours(args):
         barrier()
         wall = time.perf_counter() - t0
     launches = sar.launch_count() - launches0
+    if graphs:
+        launches = int(graph_launches * args.steps)  # kernels inside the replayed graphs
+        graphs = None  # the per-kernel pass and the end-to-end leg launch kernel by kernel
     ms = ev0.elapsed_time(ev1)
     m.sync_status()
     if world > 1:
@@ -298,7 +316,9 @@ def run_ours(args):
                "scaling": "weak", "vs_baseline": None,
                "dtype": "f16 storage (bf16 weights converted exactly), fp32 accumulate and residual",
                "data": "synthetic (seeded random-init weights and KV histories)",
-               "config": config_block(world), "e2e": e2e, "gpu_launches": launches,
+               "config": dict(config_block(world), attn_streams=2 if args.overlap else 1,
+                              launch="cuda graph per case" if args.graph else "kernel by kernel"),
+               "e2e": e2e, "gpu_launches": launches,
                "roofline": roof, "step_roofline_ms": t_roof * 1e3,
                "step_roofline_frac": (t_roof * 1e3) / (ms / args.steps),
                "kernels": kernels, "clocks": clk.summary(), "wall_s": wall, "cpu_baseline": cpu}
@@ -533,6 +553,73 @@ def run_trace_mode(args):
 
 # ------------------------------------------------------------------ long prompt
 
+def run_decode_graph(args):
+    """The 32-layer Mistral-7B shape taking decode-only steps (64 decodes,
+    contexts uniform in [128, 4096], random KV): the step launched kernel by
+    kernel against the same step replayed as a captured CUDA graph, each
+    device-timed over the steps and host-timed per step with the sampled
+    logits read back (the serving loop's pattern)."""
+    import torch
+
+    import chunked_prefill_hybrid_sar_gb300 as sar
+    from chunked_prefill_hybrid_sar_gb300 import harness
+
+    dims = synth.MISTRAL_7B
+    n_dec = 64
+    m, _ = harness.load_synthetic_model(0, dims, max_tokens=n_dec, max_decodes=n_dec)
+    ctxs = synth.uniform_int(synth.generator(1), n_dec, 128, 4096)
+    n_pages = sum(c // PAGE + 1 for c in ctxs) + 8
+    kv = sar.KVCache(m, PAGE, n_pages)
+    gen = synth.generator(2, "cuda")
+    for l in range(dims.n_layers):
+        for kind in (0, 1):
+            pv = harness.page_view(kv, l, kind, dims)
+            pv.copy_(torch.randn(pv.shape, generator=gen, device="cuda").to(pv.dtype))
+    alloc = harness.PageAllocator(range(n_pages))
+    b = sar.Batch(None, [(i, c, alloc.take(c // PAGE + 1)) for i, c in enumerate(ctxs)],
+                  in_kind=sar.SAR_IN_TOKENS)
+    tok = ((torch.arange(n_dec, dtype=torch.int32) * 7 + 3) % dims.vocab).cuda()
+    logits = torch.empty(n_dec, dims.vocab, dtype=torch.float32, device="cuda")
+    host_logits = torch.empty(n_dec, dims.vocab, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+    l0 = sar.launch_count()
+    g = sar.StepGraph(m, kv, b, tok, logits_out=logits)
+    per_step_launches = sar.launch_count() - l0
+
+    def eager():
+        m.step(kv, b, tok, logits_out=logits)
+
+    out = {}
+    for name, fn in (("kernel_by_kernel", eager), ("graph", g.launch)):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dev_ms = e0.elapsed_time(e1) / args.steps
+        host = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            fn()
+            host_logits.copy_(logits, non_blocking=True)
+            stream.synchronize()
+            host.append((time.perf_counter() - t0) * 1e3)
+        host.sort()
+        out[name] = {"device_ms_per_step": dev_ms, "host_ms_per_step_p50": host[len(host) // 2],
+                     "host_ms_per_step_min": host[0]}
+    m.sync_status()
+    g.close()
+    res = {"mode": "decode-graph", "workload": f"Mistral-7B shape, 32 layers + 32000 head, f16 storage; "
+           f"decode-only steps of {n_dec} decodes (ctx U[128,4096], random KV), token inputs, logits read back",
+           "kernels_per_step": per_step_launches, "steps": args.steps, "per_launch": out}
+    print(json.dumps(res))
+    return res
+
+
 def run_long_prompt(args):
     """The Yi-34B shape (60 layers, 64000 head; or the 32-layer Mistral-7B
     shape with ``--model mistral7b``) prefilling one 16384-token prompt in
@@ -624,9 +711,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=6)
     ap.add_argument("--impl", choices=["sar", "reference"], default="sar")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
-    ap.add_argument("--mode", choices=["step", "sweep", "trace", "long-prompt"], default="step",
+    ap.add_argument("--mode", choices=["step", "sweep", "trace", "long-prompt", "decode-graph"], default="step",
                     help="step: the tau=512 hybrid step (default); sweep: tile-quantisation sweep; "
-                         "trace: 32-layer serving trace; long-prompt: 60-layer chunked 16k prefill")
+                         "trace: 32-layer serving trace; long-prompt: 60-layer chunked 16k prefill; "
+                         "decode-graph: 32-layer decode-only steps, kernel by kernel vs CUDA graph")
     ap.add_argument("--taus", default="256,512,1024", help="trace mode: token budgets")
     ap.add_argument("--requests", type=int, default=256, help="trace mode: requests of the trace")
     ap.add_argument("--chunks", default="256,512,1024", help="long-prompt mode: chunk sizes")
@@ -634,6 +722,10 @@ def main():
     ap.add_argument("--no-warmup", action="store_true", help="long-prompt mode: no untimed prefill first")
     ap.add_argument("--model", choices=["yi34b", "mistral7b"], default="yi34b", help="long-prompt mode: model shape")
     ap.add_argument("--rate", type=float, default=4.0, help="trace mode: Poisson arrival rate (requests/s)")
+    ap.add_argument("--graph", action="store_true",
+                    help="step mode: replay each case as a captured CUDA graph in the timed region")
+    ap.add_argument("--overlap", action="store_true",
+                    help="step mode: chunk attention on a second stream, concurrent with decode attention")
     ap.add_argument("--max-chunks", type=int, default=0,
                     help="trace mode: prefill chunks per batch (0 = Algorithm 3's admission loop, 1 = one chunk)")
     ap.add_argument("--window", type=int, default=0,
@@ -647,6 +739,9 @@ def main():
         return
     if args.mode == "long-prompt":
         run_long_prompt(args)
+        return
+    if args.mode == "decode-graph":
+        run_decode_graph(args)
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -17,7 +17,7 @@ from ._lib import (SAR_EPI_F32, SAR_EPI_RESIDUAL, SAR_EPI_STORE, SAR_EPI_SWIGLU,
                    SAR_IN_HIDDEN, SAR_IN_TOKENS, SAR_STORAGE_BF16, SAR_STORAGE_F16, KERNEL_KINDS,
                    SarError, check, lib)
 
-__all__ = ["Model", "KVCache", "Scheduler", "Batch", "SarError", "lib", "check", "gemm", "rmsnorm",
+__all__ = ["Model", "KVCache", "Scheduler", "Batch", "StepGraph", "SarError", "lib", "check", "gemm", "rmsnorm",
            "launch_count", "KERNEL_KINDS", "SAR_IN_HIDDEN", "SAR_IN_TOKENS", "SAR_STORAGE_F16",
            "SAR_STORAGE_BF16", "storage_dtype"]
 
@@ -139,6 +139,10 @@ class Model:
     def profile(self, on: bool) -> None:
         check(lib().sar_profile_enable(self.h, 1 if on else 0))
 
+    def set_overlap(self, on: bool) -> None:
+        """Chunk attention on a second stream, concurrent with decode attention."""
+        check(lib().sar_model_set_overlap(self.h, 1 if on else 0))
+
     def profile_read(self) -> dict:
         n = len(KERNEL_KINDS)
         ms = (ctypes.c_double * n)()
@@ -154,6 +158,38 @@ class Model:
     def close(self) -> None:
         if self.h:
             check(lib().sar_model_destroy(self.h))
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class StepGraph:
+    """One step captured as a CUDA graph (``sar_graph_*``): fixed input and
+    output buffers; ``update`` re-points it at a batch whose plan has the same
+    shape, ``launch`` runs it."""
+
+    def __init__(self, model: "Model", kv: "KVCache", batch: Batch, inp, hidden_out=None, logits_out=None,
+                 layer_out=None, stream=None):
+        self._keep = (batch, inp, hidden_out, logits_out, layer_out)
+        h = ctypes.c_void_p()
+        check(lib().sar_graph_create(model.h, kv.h, ctypes.byref(batch.c), _ptr(inp), _ptr(hidden_out),
+                                     _ptr(logits_out), _ptr(layer_out), _stream(stream), ctypes.byref(h)))
+        self.h = h
+
+    def update(self, batch: Batch, stream=None) -> None:
+        check(lib().sar_graph_update(self.h, ctypes.byref(batch.c), _stream(stream)))
+        self._keep = (batch,) + self._keep[1:]
+
+    def launch(self, stream=None) -> None:
+        check(lib().sar_graph_launch(self.h, _stream(stream)))
+
+    def close(self) -> None:
+        if self.h:
+            check(lib().sar_graph_destroy(self.h))
             self.h = None
 
     def __del__(self):

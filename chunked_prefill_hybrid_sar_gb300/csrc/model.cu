@@ -80,8 +80,14 @@ struct sar_model {
   int meta_slot = 0;
   int32_t* meta_dev = nullptr;
   size_t meta_dev_cap = 0;
-  // profiling
+  // two-stream attention split
+  bool overlap = false;
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaStream_t capture = nullptr;  // steps are captured into graphs here (never the legacy stream)
+  // profiling (off while a step is being captured into a graph)
   bool prof = false;
+  bool capturing = false;
   std::vector<EventPair> ev_used, ev_free;
   double prof_ms[SAR_K_COUNT] = {};
   int64_t prof_n[SAR_K_COUNT] = {};
@@ -107,7 +113,7 @@ int check(cudaError_t e, const char* what) { return cuda_error(e, what); }
 
 // ---- profiling helpers -----------------------------------------------------
 EventPair* prof_begin(sar_model* m, int kind, cudaStream_t s) {
-  if (!m->prof) return nullptr;
+  if (!m->prof || m->capturing) return nullptr;
   EventPair ep;
   if (!m->ev_free.empty()) {
     ep = m->ev_free.back();
@@ -122,7 +128,7 @@ EventPair* prof_begin(sar_model* m, int kind, cudaStream_t s) {
   return &m->ev_used.back();
 }
 void prof_end(sar_model* m, cudaStream_t s) {
-  if (!m->prof || m->ev_used.empty()) return;
+  if (!m->prof || m->capturing || m->ev_used.empty()) return;
   cudaEventRecord(m->ev_used.back().b, s);
 }
 
@@ -209,12 +215,21 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
   // a decode with nk keys reads from the 16-key block holding its oldest
   // visible key (the kernel masks the keys of that block before it)
   auto first_key = [&](int nk) { return d.sliding_window > 0 ? std::max(0, nk - d.sliding_window) / 16 * 16 : 0; };
+  // the work split is sized from the keys a decode's pages can hold (at most
+  // the window's span), not from its exact count, so that the plan's shape --
+  // item and partial counts -- stays the same while a decode's context grows
+  // within its pages (a captured step graph can then be re-pointed at the
+  // next step); a decode's last range may be short or empty
+  auto span_of = [&](int ctx) {
+    const int cap = (ctx / ps + 1) * ps;
+    return d.sliding_window > 0 ? std::min(cap, d.sliding_window + 15) : cap;
+  };
   int64_t total_keys = 0;
   for (int i = 0; i < Bd; ++i) {
     const sar_decode& dc = b->decode[i];
     if (dc.ctx_len < 0 || !dc.block_table) return set_error(SAR_ERR_INVALID_ARG, "step: bad decode entry");
     SAR_TRY(check_bt(dc.block_table, dc.n_blocks, dc.ctx_len));
-    total_keys += dc.ctx_len + 1 - first_key(dc.ctx_len + 1);
+    total_keys += span_of(dc.ctx_len);
   }
   // decode work split: key ranges of `split` keys, about four CTAs (two per
   // resident slot) per SM; fewer, longer ranges measured faster than more,
@@ -234,13 +249,14 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
     btlen[i] = nb;
     bt.insert(bt.end(), dc.block_table, dc.block_table + nb);
     const int kfirst = first_key(nk);
-    const int ns = (int)((nk - kfirst + split - 1) / split);
+    const int ns = (int)((span_of(dc.ctx_len) + split - 1) / split);
     pcnt[i] = ns;
     if (ns > 1) {
       pbeg[i] = n_parts;
     }
     for (int sidx = 0; sidx < ns; ++sidx) {
-      const int k0 = kfirst + (int)(sidx * split), k1 = std::min<int>(nk, kfirst + (int)((sidx + 1) * split));
+      const int k0 = kfirst + (int)(sidx * split);
+      const int k1 = std::max(k0, std::min<int>(nk, kfirst + (int)((sidx + 1) * split)));
       const int part = ns > 1 ? n_parts + sidx : -1;
       auto& dst = (k1 - k0 == split) ? items : tail_items;  // full ranges first
       dst.insert(dst.end(), {i, k0, k1, part});
@@ -386,26 +402,20 @@ int ensure_partials(sar_model* m, size_t floats) {
   return SAR_OK;
 }
 
-// The step proper, on device buffers.
-int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float* h, float* logits,
-             void* layer_out, cudaStream_t s) {
+// Checks the model state and plans the step (host only).
+int plan_step(sar_model* m, sar_kv* kv, const sar_batch* b, bool logits, Plan* p, std::vector<int32_t>* meta) {
   const sar_dims& d = m->d;
   for (int l = 0; l < d.n_layers; ++l)
     if (!m->L[l].set) return set_error(SAR_ERR_INVALID_ARG, "step: layer weights not set");
   if (logits && (d.vocab == 0 || !m->head_set)) return set_error(SAR_ERR_INVALID_ARG, "step: logits requested without a head");
-  Plan p;
-  std::vector<int32_t> meta;
-  SAR_TRY(validate_and_plan(m, kv, b, &p, &meta));
-  SAR_TRY(ensure_meta(m, p.total));
-  SAR_TRY(ensure_partials(m, (size_t)std::max(p.n_parts, 1) * d.n_q_heads * (d.head_dim + 2)));
-  // stage the metadata through a pinned ring buffer
-  const int slot = m->meta_slot;
-  m->meta_slot = (slot + 1) % kMetaRing;
-  SAR_TRY(check(cudaEventSynchronize(m->meta_ev[slot]), "meta ring wait"));
-  std::memcpy(m->meta_host[slot], meta.data(), p.total * 4);
-  SAR_TRY(check(cudaMemcpyAsync(m->meta_dev, m->meta_host[slot], p.total * 4, cudaMemcpyHostToDevice, s), "meta copy"));
-  SAR_TRY(check(cudaEventRecord(m->meta_ev[slot], s), "meta event"));
-  const int32_t* md = m->meta_dev;
+  return validate_and_plan(m, kv, b, p, meta);
+}
+
+// Launches the step's kernels on `s`, reading the plan's metadata at device
+// address `md` and keeping decode split partials in `partials`.
+int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, const int32_t* md, float* partials,
+                const void* in, float* h, float* logits, void* layer_out, cudaStream_t s) {
+  const sar_dims& d = m->d;
   const int M = p.M, H = d.hidden;
 
   for (int l = 0; l < d.n_layers; ++l) {
@@ -441,6 +451,15 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
       rp.num_pages = kv->num_pages;
       SAR_TRY(run_gemm(m, m->xn, M, w.m_qkv, m->qkv_n, H, sar::kEpiRope, m->qkv32, nullptr, s, &rp));
     }
+    // two-stream split: chunk attention forks onto the side stream after the
+    // QKV projection and joins before the O projection
+    const bool ov = m->overlap && (!m->prof || m->capturing) && p.Lp > 0 && p.Bd > 0;
+    cudaStream_t sc = s;
+    if (ov) {
+      SAR_TRY(check(cudaEventRecord(m->ev_fork, s), "overlap: fork"));
+      SAR_TRY(check(cudaStreamWaitEvent(m->side, m->ev_fork, 0), "overlap: side wait"));
+      sc = m->side;
+    }
     if (p.Lp > 0) {
       Prof pr(m, SAR_K_CHUNK_ATTN, s);
       sar::ChunkAttnArgs ca;
@@ -463,9 +482,9 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
       ca.err = m->err;
       ca.window = d.sliding_window;
       if (sar::chunk_attention_tc_supported(ca))
-        SAR_TRY(sar::launch_chunk_attention_tc(ca, kv->tmk[l], kv->tmv[l], s));
+        SAR_TRY(sar::launch_chunk_attention_tc(ca, kv->tmk[l], kv->tmv[l], sc));
       else
-        SAR_TRY(sar::launch_chunk_attention(ca, s));
+        SAR_TRY(sar::launch_chunk_attention(ca, sc));
     }
     if (p.Bd > 0) {
       Prof pr(m, SAR_K_DECODE_ATTN, s);
@@ -484,7 +503,7 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
       da.bt = md + p.o_bt;
       da.parts_begin = md + p.o_pbeg;
       da.parts_count = md + p.o_pcnt;
-      da.partials = p.n_parts > 0 ? m->partials : nullptr;
+      da.partials = p.n_parts > 0 ? partials : nullptr;
       da.n_items = p.n_items;
       da.n_decode = p.Bd;
       da.ld = m->qkv_n;
@@ -497,6 +516,10 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
       da.err = m->err;
       da.window = d.sliding_window;
       SAR_TRY(sar::launch_decode_attention(da, kv->tmk[l], kv->tmv[l], s));
+    }
+    if (ov) {
+      SAR_TRY(check(cudaEventRecord(m->ev_join, m->side), "overlap: join"));
+      SAR_TRY(check(cudaStreamWaitEvent(s, m->ev_join, 0), "overlap: main wait"));
     }
     {
       Prof pr(m, SAR_K_GEMM_O, s);
@@ -530,6 +553,24 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
     }
   }
   return SAR_OK;
+}
+
+// The step proper, on device buffers: plan, stage the metadata through the
+// pinned ring into the model's device buffer, launch.
+int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float* h, float* logits,
+             void* layer_out, cudaStream_t s) {
+  Plan p;
+  std::vector<int32_t> meta;
+  SAR_TRY(plan_step(m, kv, b, logits != nullptr, &p, &meta));
+  SAR_TRY(ensure_meta(m, p.total));
+  SAR_TRY(ensure_partials(m, (size_t)std::max(p.n_parts, 1) * m->d.n_q_heads * (m->d.head_dim + 2)));
+  const int slot = m->meta_slot;
+  m->meta_slot = (slot + 1) % kMetaRing;
+  SAR_TRY(check(cudaEventSynchronize(m->meta_ev[slot]), "meta ring wait"));
+  std::memcpy(m->meta_host[slot], meta.data(), p.total * 4);
+  SAR_TRY(check(cudaMemcpyAsync(m->meta_dev, m->meta_host[slot], p.total * 4, cudaMemcpyHostToDevice, s), "meta copy"));
+  SAR_TRY(check(cudaEventRecord(m->meta_ev[slot], s), "meta event"));
+  return launch_step(m, kv, b, p, m->meta_dev, m->partials, in, h, logits, layer_out, s);
 }
 
 }  // namespace
@@ -667,6 +708,10 @@ int sar_model_destroy(sar_model* m) {
     if (m->meta_host[i]) cudaFreeHost(m->meta_host[i]);
     if (m->meta_ev[i]) cudaEventDestroy(m->meta_ev[i]);
   }
+  if (m->ev_fork) cudaEventDestroy(m->ev_fork);
+  if (m->ev_join) cudaEventDestroy(m->ev_join);
+  if (m->side) cudaStreamDestroy(m->side);
+  if (m->capture) cudaStreamDestroy(m->capture);
   for (auto& ep : m->ev_used) { cudaEventDestroy(ep.a); cudaEventDestroy(ep.b); }
   for (auto& ep : m->ev_free) { cudaEventDestroy(ep.a); cudaEventDestroy(ep.b); }
   cudaFree(m->meta_dev);
@@ -795,6 +840,19 @@ int sar_sample_greedy(sar_model* m, const float* logits, int32_t rows, int32_t* 
   return sar::launch_argmax(logits, rows, m->d.vocab, tokens_out, static_cast<cudaStream_t>(stream));
 }
 
+int sar_model_set_overlap(sar_model* m, int32_t on) {
+  if (!m) return set_error(SAR_ERR_INVALID_ARG, "overlap: null model");
+  if (on && !m->side) {
+    int lo = 0, hi = 0;
+    SAR_TRY(check(cudaDeviceGetStreamPriorityRange(&lo, &hi), "overlap: stream priorities"));
+    SAR_TRY(check(cudaStreamCreateWithPriority(&m->side, cudaStreamNonBlocking, hi), "overlap: side stream"));
+    SAR_TRY(check(cudaEventCreateWithFlags(&m->ev_fork, cudaEventDisableTiming), "overlap: fork event"));
+    SAR_TRY(check(cudaEventCreateWithFlags(&m->ev_join, cudaEventDisableTiming), "overlap: join event"));
+  }
+  m->overlap = on != 0;
+  return SAR_OK;
+}
+
 int sar_profile_enable(sar_model* m, int32_t on) {
   if (!m) return set_error(SAR_ERR_INVALID_ARG, "profile: null model");
   m->prof = on != 0;
@@ -864,6 +922,124 @@ int sar_op_rmsnorm(const void* x, const void* gain, void* y, int32_t rows, int32
   if (storage != SAR_STORAGE_F16 && storage != SAR_STORAGE_BF16) return set_error(SAR_ERR_INVALID_ARG, "op_rmsnorm: bad storage");
   return sar::launch_rmsnorm(static_cast<const float*>(x), static_cast<const float*>(gain), y, rows, hidden, eps,
                              nullptr, storage, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+// ---- CUDA graphs of a step -------------------------------------------------
+
+struct sar_graph {
+  sar_model* m = nullptr;
+  sar_kv* kv = nullptr;
+  Plan p;
+  int in_kind = 0;
+  int32_t* md = nullptr;       // the graph's own device copy of the step metadata
+  int32_t* md_host = nullptr;  // pinned staging for sar_graph_update
+  float* partials = nullptr;   // the graph's own decode split partials
+  cudaEvent_t staged = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+namespace {
+
+// Two plans launch the same kernels with the same grids and argument
+// addresses when every size and metadata offset agrees.
+bool same_shape(const Plan& a, const Plan& b) {
+  return a.M == b.M && a.Lp == b.Lp && a.Bd == b.Bd && a.R == b.R && a.n_items == b.n_items &&
+         a.n_parts == b.n_parts && a.n_tiles == b.n_tiles && a.total == b.total && a.o_pos == b.o_pos &&
+         a.o_slot == b.o_slot && a.o_pbt == b.o_pbt && a.o_nkeys == b.o_nkeys && a.o_btoff == b.o_btoff &&
+         a.o_btlen == b.o_btlen && a.o_pbeg == b.o_pbeg && a.o_pcnt == b.o_pcnt && a.o_items == b.o_items &&
+         a.o_bt == b.o_bt && a.o_rows == b.o_rows && a.o_tiles == b.o_tiles;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sar_graph_destroy(sar_graph* g) {
+  if (!g) return SAR_OK;
+  if (g->staged) cudaEventSynchronize(g->staged);
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  if (g->staged) cudaEventDestroy(g->staged);
+  if (g->md_host) cudaFreeHost(g->md_host);
+  cudaFree(g->md);
+  cudaFree(g->partials);
+  delete g;
+  return SAR_OK;
+}
+
+int sar_graph_create(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, void* hidden_out,
+                     float* logits_out, void* layer_out, void* stream, sar_graph** out) {
+  if (!m || !kv || !b || !in || !out) return set_error(SAR_ERR_INVALID_ARG, "graph: null argument");
+  if (kv->m != m) return set_error(SAR_ERR_INVALID_ARG, "graph: cache of another model");
+  if ((reinterpret_cast<uintptr_t>(hidden_out) & 15) || (reinterpret_cast<uintptr_t>(logits_out) & 15))
+    return set_error(SAR_ERR_INVALID_ARG, "graph: outputs must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  sar_graph* g = new sar_graph();
+  g->m = m;
+  g->kv = kv;
+  g->in_kind = b->in_kind;
+  std::vector<int32_t> meta;
+  int rc = plan_step(m, kv, b, logits_out != nullptr, &g->p, &meta);
+  // everything the captured launches point at is allocated and filled before the capture
+  const size_t parts = (size_t)std::max(g->p.n_parts, 1) * m->d.n_q_heads * (m->d.head_dim + 2);
+  if (rc == SAR_OK) rc = check(cudaMalloc(&g->md, g->p.total * 4), "graph: metadata");
+  if (rc == SAR_OK) rc = check(cudaMallocHost(&g->md_host, g->p.total * 4), "graph: metadata staging");
+  if (rc == SAR_OK) rc = check(cudaMalloc(&g->partials, parts * 4), "graph: partials");
+  if (rc == SAR_OK) rc = check(cudaEventCreateWithFlags(&g->staged, cudaEventDisableTiming), "graph: event");
+  if (rc == SAR_OK) {
+    std::memcpy(g->md_host, meta.data(), g->p.total * 4);
+    rc = check(cudaMemcpyAsync(g->md, g->md_host, g->p.total * 4, cudaMemcpyHostToDevice, s), "graph: metadata copy");
+  }
+  if (rc == SAR_OK) rc = check(cudaEventRecord(g->staged, s), "graph: staged");
+  if (rc == SAR_OK) rc = check(cudaStreamSynchronize(s), "graph: synchronise");
+  if (rc == SAR_OK && m->overlap && !m->side) rc = sar_model_set_overlap(m, 1);
+  // capture on the model's own stream (the caller's may be the legacy stream,
+  // which cannot be captured); the graph then launches on any stream
+  if (rc == SAR_OK && !m->capture)
+    rc = check(cudaStreamCreateWithFlags(&m->capture, cudaStreamNonBlocking), "graph: capture stream");
+  if (rc == SAR_OK) {
+    cudaStream_t cs = m->capture;
+    rc = check(cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal), "graph: begin capture");
+    if (rc == SAR_OK) {
+      m->capturing = true;
+      const int lrc = launch_step(m, kv, b, g->p, g->md, g->partials, in, static_cast<float*>(hidden_out ? hidden_out : m->hres),
+                                  logits_out, layer_out, cs);
+      m->capturing = false;
+      const int erc = check(cudaStreamEndCapture(cs, &g->graph), "graph: end capture");
+      rc = lrc != SAR_OK ? lrc : erc;
+    }
+  }
+  if (rc == SAR_OK) rc = check(cudaGraphInstantiate(&g->exec, g->graph, 0), "graph: instantiate");
+  if (rc != SAR_OK) {
+    sar_graph_destroy(g);
+    return rc;
+  }
+  *out = g;
+  return SAR_OK;
+}
+
+int sar_graph_update(sar_graph* g, const sar_batch* b, void* stream) {
+  if (!g || !b) return set_error(SAR_ERR_INVALID_ARG, "graph: null argument");
+  if (b->in_kind != g->in_kind) return set_error(SAR_ERR_INVALID_ARG, "graph: input kind differs from the captured step");
+  Plan p;
+  std::vector<int32_t> meta;
+  SAR_TRY(plan_step(g->m, g->kv, b, false, &p, &meta));
+  if (!same_shape(p, g->p))
+    return set_error(SAR_ERR_INVALID_ARG, "graph: the batch's plan differs in shape from the captured step");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  SAR_TRY(check(cudaEventSynchronize(g->staged), "graph: staging wait"));
+  std::memcpy(g->md_host, meta.data(), p.total * 4);
+  SAR_TRY(check(cudaMemcpyAsync(g->md, g->md_host, p.total * 4, cudaMemcpyHostToDevice, s), "graph: metadata copy"));
+  return check(cudaEventRecord(g->staged, s), "graph: staged");
+}
+
+int sar_graph_launch(sar_graph* g, void* stream) {
+  if (!g) return set_error(SAR_ERR_INVALID_ARG, "graph: null graph");
+  SAR_TRY(check(cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream)), "graph: launch"));
+  return SAR_OK;
 }
 
 }  // extern "C"

@@ -53,6 +53,7 @@ enum {
 typedef struct sar_model sar_model;
 typedef struct sar_kv sar_kv;
 typedef struct sar_sched sar_sched;
+typedef struct sar_graph sar_graph;
 
 /* Thread-local text of the last error (never NULL). */
 const char* sar_last_error(void);
@@ -210,6 +211,32 @@ int sar_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, void*
 int sar_step_host(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, void* hidden_out,
                   float* logits_out, void* layer_out, void* stream);
 
+/* ---- one step as a CUDA graph ------------------------------------------ */
+
+/* Captures the step of batch `b` into a CUDA graph (the pages batch steps
+ * with CUDA graphs to cut launch overhead, SARATHI technique write-up,
+ * section 3.3).  The graph keeps its own device copy of the step's metadata
+ * (positions, slots, block tables, the decode and chunk work plans) and its
+ * own decode split partials; it reads `in` and writes hidden_out /
+ * logits_out / layer_out at the addresses given here (device buffers, as for
+ * sar_step; hidden_out may be NULL).  Nothing runs on the GPU but the
+ * metadata copy: launch the graph to run the step.  Returns any error
+ * sar_step would return for `b`, before capturing. */
+int sar_graph_create(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, void* hidden_out,
+                     float* logits_out, void* layer_out, void* stream, sar_graph** out);
+
+/* Points the graph at another batch whose plan has the same shape (the same
+ * row, chunk-tile, decode-item, split and block-table counts, so the same
+ * grids and metadata layout), copying its metadata on `stream` ahead of the
+ * next launch there; SAR_ERR_INVALID_ARG otherwise (the graph is unchanged).
+ * The caller puts the batch's inputs into the captured `in` buffer. */
+int sar_graph_update(sar_graph* g, const sar_batch* b, void* stream);
+
+/* Runs the captured step on `stream`. */
+int sar_graph_launch(sar_graph* g, void* stream);
+
+int sar_graph_destroy(sar_graph* g);
+
 /* Greedy sampling: tokens_out[r] = argmax_v logits[r, v] (lowest index on
  * ties), device fp32 [rows, vocab] -> device int32 [rows]. */
 int sar_sample_greedy(sar_model* m, const float* logits, int32_t rows, int32_t* tokens_out,
@@ -273,6 +300,15 @@ enum {
 
 /* When on, sar_step records an event pair around every kernel group. */
 int sar_profile_enable(sar_model* m, int32_t on);
+
+/* When on, a step that has both prefill chunks and decodes runs the chunk
+ * attention on a second (high-priority) stream concurrently with the decode
+ * attention, forked after the QKV projection and joined before the O
+ * projection by events -- the pages' two-stream split of the hybrid batch
+ * (SARATHI technique write-up, section 3.3).  Results are identical either
+ * way (the two kernels write disjoint rows).  Off by default; ignored while
+ * profiling.  Creates the stream and events on first use. */
+int sar_model_set_overlap(sar_model* m, int32_t on);
 
 /* Synchronises, then returns per kind the accumulated milliseconds and the
  * number of timed launches since the last reset, and resets them. */

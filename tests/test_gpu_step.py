@@ -248,3 +248,34 @@ def test_mistral_layer_hybrid_step(mistral, start):
     assert_close(got[:lp], ref_h[0][:lp], what="chunk rows")
     assert_close(got[lp:], ref_h[0][lp:], what="decode rows")
     assert_close(logits.cpu().numpy(), ref_l, what="logits")
+
+
+def test_mistral_layer_attention_overlap_is_identical(mistral):
+    """Chunk attention on a second stream, concurrent with decode attention:
+    the same kernels write the same disjoint rows, so the step agrees with the
+    one-stream step up to the order of the split-K atomic adds in the O and
+    down projections (which differs from run to run on one stream too)."""
+    case, m, kv, dec_bt, prompt_bt, w, head = mistral
+    dims, lp = case["dims"], case["lp"]
+    start = 1536
+    prompt = case["prompts"][start]
+    bt = prompt_bt[start]
+    for s0 in range(0, start, 512):
+        m.step(kv, sar.Batch((start, s0, 512, bt), []), prompt[s0:s0 + 512].cuda())
+    decs = [(100 + i, c, dec_bt[i]) for i, c in enumerate(case["ctxs"])]
+    b = sar.Batch((start, start, lp, bt), decs)
+    x = torch.cat([prompt[start:start + lp], case["decode_inputs"]]).cuda()
+    outs = []
+    for on in (False, True, False):
+        m.set_overlap(on)
+        hid = torch.empty(512, dims.hidden, dtype=torch.float32, device="cuda")
+        logits = torch.empty(65, dims.vocab, dtype=torch.float32, device="cuda")
+        m.step(kv, b, x, hidden_out=hid, logits_out=logits)
+        m.sync_status()
+        outs.append((hid, logits))
+    m.set_overlap(False)
+    torch.cuda.synchronize()
+    for hid, logits in outs[1:]:
+        for got, ref in ((hid, outs[0][0]), (logits, outs[0][1])):
+            rel = ((got.double() - ref.double()).norm() / ref.double().norm()).item()
+            assert rel <= 1e-4, rel
