@@ -4,7 +4,9 @@ at start positions 0, 512 and 1536 (cycled) with 64 piggybacked decodes whose
 contexts are uniform in [128, 4096].
 
 Prints one JSON line.  ``value`` is hybrid-batch tokens/s (rows of the
-stacked batch per second) over the timed steps with inputs resident in HBM;
+stacked batch per second) over the timed steps with inputs resident in HBM,
+each case's step replayed from a captured CUDA graph (``--no-graph``: launched
+kernel by kernel);
 ``e2e`` is the same metric through the host-buffer C entry point with the
 host<->device copies inside the timed region.  ``--impl reference`` times the
 CPU oracle on a bounded sample of the same workload instead.
@@ -722,8 +724,9 @@ def main():
     ap.add_argument("--no-warmup", action="store_true", help="long-prompt mode: no untimed prefill first")
     ap.add_argument("--model", choices=["yi34b", "mistral7b"], default="yi34b", help="long-prompt mode: model shape")
     ap.add_argument("--rate", type=float, default=4.0, help="trace mode: Poisson arrival rate (requests/s)")
-    ap.add_argument("--graph", action="store_true",
-                    help="step mode: replay each case as a captured CUDA graph in the timed region")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="step mode: launch kernel by kernel in the timed region instead of replaying each "
+                         "case's captured CUDA graph")
     ap.add_argument("--overlap", action="store_true",
                     help="step mode: chunk attention on a second stream, concurrent with decode attention")
     ap.add_argument("--max-chunks", type=int, default=0,
