@@ -266,7 +266,7 @@ def run_ours(args):
     # DRAM bytes read + written per launch (dram__bytes_read.sum +
     # dram__bytes_write.sum) from one ncu capture of the current kernels on this
     # workload; decode attention counts both of its kernels
-    traffic = {"decode_attn": 526.8e6, "gemm_gateup": 256.2e6}.get(dom)
+    traffic = {"decode_attn": 526.4e6, "gemm_gateup": 256.2e6}.get(dom)
     if dom in flops:
         ach = kernels[dom]["tflops"]
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": tf_sust, "unit": "TFLOP/s",
