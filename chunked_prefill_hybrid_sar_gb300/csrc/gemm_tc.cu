@@ -790,13 +790,14 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
     case SAR_GEMM_M256_N128: c.swap = 0; c.msub = 2; c.bn = 128; break;
     case SAR_GEMM_PAIR_N256: c.swap = 0; c.msub = 1; c.bn = 256; c.pair = 1; break;
     case SAR_GEMM_PAIR_N128: c.swap = 0; c.msub = 1; c.bn = 128; c.pair = 1; break;
+    case SAR_GEMM_PAIR_N192: c.swap = 0; c.msub = 1; c.bn = 192; c.pair = 1; break;
     case SAR_GEMM_SWAP:
       if (M > 256) return set_error(SAR_ERR_UNSUPPORTED, "gemm: swap tiling needs M <= 256");
       c.swap = 1; c.msub = 1; c.bn = (M + 15) / 16 * 16; break;
     default: return set_error(SAR_ERR_INVALID_ARG, "gemm: unknown variant");
   }
-  if (!c.swap && N % c.bn && epi == SAR_EPI_SWIGLU)
-    return set_error(SAR_ERR_UNSUPPORTED, "gemm: SwiGLU tiles must not straddle N");
+  if (!c.swap && (N % c.bn || c.bn % 128) && epi == SAR_EPI_SWIGLU)
+    return set_error(SAR_ERR_UNSUPPORTED, "gemm: SwiGLU tiles must not straddle N and hold whole gate/up blocks");
   if (c.swap) {
     if (cl_flag > SAR_GEMM_CLUSTER_1) return set_error(SAR_ERR_UNSUPPORTED, "gemm: swap tiling takes no cluster");
     c.m_tiles = 1;
@@ -873,6 +874,7 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
     return set_error(SAR_ERR_INVALID_ARG, "gemm: residual epilogue without residual");
   if (epi == kEpiRope &&
       (!rope || !rope->slot || !rope->cs || (rope->hd != 64 && rope->hd != 128) || N % 128 ||
+       (!cfg.swap && cfg.bn % rope->hd) ||
        N != (rope->qh + 2 * rope->kvh) * rope->hd || rope->page_size <= 0))
     return set_error(SAR_ERR_INVALID_ARG, "gemm: rotary epilogue arguments");
   Params p;

@@ -45,6 +45,8 @@ enum {
                              128 token rows and half of the weight rows, so each SM
                              loads half the weight tile                             */
   SAR_GEMM_PAIR_N128 = 6, /* the same with 128 weight rows per tile                 */
+  SAR_GEMM_PAIR_N192 = 7, /* the same with 192 weight rows per tile (not for the
+                             SwiGLU epilogue, whose gate/up blocks are 128 wide)    */
   /* Optional flags OR-ed into a non-swap tiling (or AUTO): how many CTAs of a
    * thread-block cluster share one weight tile.  Each fetches 1/c of the tile's
    * rows from L2 and multicasts it to all, so the weights leave L2 once per

@@ -41,6 +41,7 @@ VARIANTS = {
     "swap": sar.SAR_GEMM_SWAP,
     "pair256": sar.SAR_GEMM_PAIR_N256,
     "pair128": sar.SAR_GEMM_PAIR_N128,
+    "pair192": sar.SAR_GEMM_PAIR_N192,
 }
 
 SHAPES = [(1, 256, 256), (16, 512, 256), (65, 768, 512), (128, 256, 1024), (200, 1024, 256),
@@ -62,7 +63,7 @@ def test_gemm_store(M, N, K, variant, dt):
 
 
 @pytest.mark.parametrize("M", [3, 130, 384])
-@pytest.mark.parametrize("variant", ["auto", "m128n256", "swap", "m256n128", "pair256", "pair128"])
+@pytest.mark.parametrize("variant", ["auto", "m128n256", "swap", "m256n128", "pair256", "pair128", "pair192"])
 @pytest.mark.parametrize("dt", list(DTYPES))
 def test_gemm_residual_in_place(M, variant, dt):
     """fp32 residual stream: h = h + a . w^T in place, no rounding to 16 bits."""
@@ -115,6 +116,14 @@ def test_gemm_f32_head(M, dt):
     ref = a.double() @ w.double().T
     got = c.double().cpu()
     assert ((got - ref).abs().max() / ref.abs().max()).item() < 1e-5
+
+
+def test_gemm_pair192_refuses_swiglu():
+    a = torch.zeros(256, 256, dtype=torch.float16, device=DEV)
+    w = torch.zeros(768, 256, dtype=torch.float16, device=DEV)
+    out = torch.zeros(256, 384, dtype=torch.float16, device=DEV)
+    with pytest.raises(sar.SarError):
+        sar.gemm(a, w, out, epilogue=sar.SAR_EPI_SWIGLU, variant=sar.SAR_GEMM_PAIR_N192)
 
 
 def test_gemm_unsupported_shapes_are_rejected():
