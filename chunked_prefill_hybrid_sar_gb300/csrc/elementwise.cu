@@ -65,11 +65,20 @@ struct NormArgs {
 
 template <typename T, int SRC>
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a) {
+  const int nv = a.hidden >> 2;
+  // the gains are weights, not the previous kernel's output: fetch them while
+  // that kernel drains
+  const float4* gr = reinterpret_cast<const float4*>(a.g);
+  float4 gv[kNormMaxVec];
+#pragma unroll
+  for (int k = 0; k < kNormMaxVec; ++k) {
+    const int i = threadIdx.x + k * kNormThreads;
+    if (i < nv) gv[k] = __ldg(gr + i);
+  }
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float red[32];
   const int r = blockIdx.x;
-  const int nv = a.hidden >> 2;
   float4 v[kNormMaxVec];
   bool ok = true;
   if constexpr (SRC == kSrcResidual) {
@@ -131,15 +140,13 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
   }
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / (float)a.hidden + a.eps);
-  const float4* gr = reinterpret_cast<const float4*>(a.g);
   uint2* yr = reinterpret_cast<uint2*>(static_cast<T*>(a.y) + (size_t)r * a.hidden);
 #pragma unroll
   for (int k = 0; k < kNormMaxVec; ++k) {
     const int i = threadIdx.x + k * kNormThreads;
     if (i < nv) {
-      const float4 gv = gr[i];
-      yr[i] = make_uint2(Elem<T>::pack(v[k].x * inv * gv.x, v[k].y * inv * gv.y),
-                         Elem<T>::pack(v[k].z * inv * gv.z, v[k].w * inv * gv.w));
+      yr[i] = make_uint2(Elem<T>::pack(v[k].x * inv * gv[k].x, v[k].y * inv * gv[k].y),
+                         Elem<T>::pack(v[k].z * inv * gv[k].z, v[k].w * inv * gv[k].w));
     }
   }
   if (a.zero) {
