@@ -228,9 +228,10 @@ def run_ours(args):
         barrier()
         wall = time.perf_counter() - t0
     launches = sar.launch_count() - launches0
+    graph_set = graphs
     if graphs:
         launches = int(graph_launches * args.steps)  # kernels inside the replayed graphs
-        graphs = None  # the per-kernel pass and the end-to-end leg launch kernel by kernel
+        graphs = None  # the per-kernel pass launches kernel by kernel
     ms = ev0.elapsed_time(ev1)
     m.sync_status()
     if world > 1:
@@ -290,16 +291,26 @@ def run_ours(args):
               + op_t(0, dab) + op_t(2 * (BD + 1) * dims.hidden * dims.vocab, head_bytes)
               + 4 * op_t(0, TAU * wb * 2))
 
-    # end to end: host buffers through the host entry point
+    # end to end: host buffers through the host entry points, one step at a
+    # time (each step's input rows in from pinned memory, its result -- the
+    # logits of every sampled row -- back, then the next step): the captured
+    # graph of each case (sar_graph_launch_host), or with --no-graph the
+    # planning entry point (sar_step_host)
     pin_in = [x.cpu().pin_memory() for _, x in cases]
-    h_hid = torch.empty(TAU, dims.hidden, dtype=torch.float32).pin_memory()
     h_log = torch.empty(BD + 1, dims.vocab, dtype=torch.float32).pin_memory()
-    for i in range(2):
-        m.step_host(kv, cases[i % 3][0], pin_in[i % 3], hidden_out=h_hid, logits_out=h_log)
+
+    def e2e_step(i):
+        if graph_set:
+            graph_set[i % 3].launch_host(pin_in[i % 3], logits_out=h_log)
+        else:
+            m.step_host(kv, cases[i % 3][0], pin_in[i % 3], logits_out=h_log)
+
+    for i in range(3):
+        e2e_step(i)
     barrier()
     t0 = time.perf_counter()
     for i in range(args.steps):
-        m.step_host(kv, cases[i % 3][0], pin_in[i % 3], hidden_out=h_hid, logits_out=h_log)
+        e2e_step(i)
     barrier()
     e2e_s = time.perf_counter() - t0
     if world > 1:
@@ -308,7 +319,8 @@ def run_ours(args):
         e2e_s = t.item()
     e2e = {"value": TAU * args.steps * world / e2e_s, "unit": UNIT,
            "h2d_bytes_per_step": TAU * dims.hidden * 2,
-           "d2h_bytes_per_step": TAU * dims.hidden * 4 + (BD + 1) * dims.vocab * 4}
+           "d2h_bytes_per_step": (BD + 1) * dims.vocab * 4,
+           "api": "sar_graph_launch_host" if graph_set else "sar_step_host"}
 
     out = None
     if rank == 0:

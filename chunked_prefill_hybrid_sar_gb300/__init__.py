@@ -188,6 +188,10 @@ class StepGraph:
     def launch(self, stream=None) -> None:
         check(lib().sar_graph_launch(self.h, _stream(stream)))
 
+    def launch_host(self, inp, logits_out=None, hidden_out=None, stream=None) -> None:
+        """Host input in, the captured step, host logits / hidden rows out (synchronous)."""
+        check(lib().sar_graph_launch_host(self.h, _ptr(inp), _ptr(logits_out), _ptr(hidden_out), _stream(stream)))
+
     def close(self) -> None:
         if self.h:
             check(lib().sar_graph_destroy(self.h))

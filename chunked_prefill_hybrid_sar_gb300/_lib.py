@@ -94,6 +94,7 @@ SIGNATURES = {
     "sar_graph_create": (i32, [vp, vp, ctypes.POINTER(sar_batch), vp, vp, vp, vp, vp, ctypes.POINTER(vp)]),
     "sar_graph_update": (i32, [vp, ctypes.POINTER(sar_batch), vp]),
     "sar_graph_launch": (i32, [vp, vp]),
+    "sar_graph_launch_host": (i32, [vp, vp, vp, vp, vp]),
     "sar_graph_destroy": (i32, [vp]),
     "sar_profile_read": (i32, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64), i32]),
     "sar_sched_create": (i32, [ctypes.POINTER(sar_sched_cfg), ctypes.POINTER(vp)]),

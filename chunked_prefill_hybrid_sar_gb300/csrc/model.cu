@@ -933,6 +933,10 @@ struct sar_graph {
   sar_kv* kv = nullptr;
   Plan p;
   int in_kind = 0;
+  // the captured step's buffers (for sar_graph_launch_host)
+  void* in = nullptr;
+  float* hidden = nullptr;
+  float* logits = nullptr;
   int32_t* md = nullptr;       // the graph's own device copy of the step metadata
   int32_t* md_host = nullptr;  // pinned staging for sar_graph_update
   float* partials = nullptr;   // the graph's own decode split partials
@@ -981,6 +985,9 @@ int sar_graph_create(sar_model* m, sar_kv* kv, const sar_batch* b, const void* i
   g->m = m;
   g->kv = kv;
   g->in_kind = b->in_kind;
+  g->in = const_cast<void*>(in);
+  g->hidden = static_cast<float*>(hidden_out);
+  g->logits = logits_out;
   std::vector<int32_t> meta;
   int rc = plan_step(m, kv, b, logits_out != nullptr, &g->p, &meta);
   // everything the captured launches point at is allocated and filled before the capture
@@ -1040,6 +1047,23 @@ int sar_graph_launch(sar_graph* g, void* stream) {
   if (!g) return set_error(SAR_ERR_INVALID_ARG, "graph: null graph");
   SAR_TRY(check(cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream)), "graph: launch"));
   return SAR_OK;
+}
+
+int sar_graph_launch_host(sar_graph* g, const void* in, float* logits_out, float* hidden_out, void* stream) {
+  if (!g || !in) return set_error(SAR_ERR_INVALID_ARG, "graph: null argument");
+  if ((logits_out && !g->logits) || (hidden_out && !g->hidden))
+    return set_error(SAR_ERR_INVALID_ARG, "graph: output not captured");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t M = (size_t)g->p.M, H = (size_t)g->m->d.hidden;
+  const size_t in_bytes = g->in_kind == SAR_IN_TOKENS ? M * 4 : M * H * 2;
+  SAR_TRY(check(cudaMemcpyAsync(g->in, in, in_bytes, cudaMemcpyHostToDevice, s), "graph: input copy"));
+  SAR_TRY(check(cudaGraphLaunch(g->exec, s), "graph: launch"));
+  if (logits_out)
+    SAR_TRY(check(cudaMemcpyAsync(logits_out, g->logits, (size_t)g->p.R * g->m->d.vocab * 4, cudaMemcpyDeviceToHost, s),
+                  "graph: logits copy"));
+  if (hidden_out)
+    SAR_TRY(check(cudaMemcpyAsync(hidden_out, g->hidden, M * H * 4, cudaMemcpyDeviceToHost, s), "graph: hidden copy"));
+  return check(cudaStreamSynchronize(s), "graph: synchronise");
 }
 
 }  // extern "C"

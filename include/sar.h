@@ -235,6 +235,14 @@ int sar_graph_update(sar_graph* g, const sar_batch* b, void* stream);
 /* Runs the captured step on `stream`. */
 int sar_graph_launch(sar_graph* g, void* stream);
 
+/* The captured step with HOST buffers: copies `in` (host, the captured input's
+ * size and kind) into the captured input buffer, runs the graph, copies the
+ * captured logits (R x vocab fp32) and/or hidden rows (M x hidden fp32) to the
+ * host buffers that are not NULL, and returns once they are in host memory.
+ * Each output requested must have been captured (non-NULL at create time).
+ * Pinned host memory makes the copies asynchronous to the host. */
+int sar_graph_launch_host(sar_graph* g, const void* in, float* logits_out, float* hidden_out, void* stream);
+
 int sar_graph_destroy(sar_graph* g);
 
 /* Greedy sampling: tokens_out[r] = argmax_v logits[r, v] (lowest index on

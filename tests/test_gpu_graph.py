@@ -150,3 +150,34 @@ def test_graph_update_refuses_another_shape(mistral):
     m.sync_status()
     g.close()
     kv.close()
+
+
+def test_graph_launch_host_copies_in_and_out(mistral):
+    """Host input rows in, the captured step, host logits and hidden rows out."""
+    case, m = mistral
+    dims, lp, start = case["dims"], case["lp"], 512
+    prompt = case["prompts"][start]
+    kv, dec_bt, bt = mistral_kv(case, m)
+    m.step(kv, sar.Batch((0, 0, 512, bt), []), prompt[:512].cuda())
+    decs = [(100 + i, c, dec_bt[i]) for i, c in enumerate(case["ctxs"])]
+    b = sar.Batch((0, start, lp, bt), decs)
+    x_host = torch.cat([prompt[start:start + lp], case["decode_inputs"]]).contiguous().pin_memory()
+    x_dev = torch.zeros_like(x_host, device="cuda")
+    hid = torch.empty(512, dims.hidden, dtype=torch.float32, device="cuda")
+    logits = torch.empty(65, dims.vocab, dtype=torch.float32, device="cuda")
+    g = sar.StepGraph(m, kv, b, x_dev, hidden_out=hid, logits_out=logits)
+    h_log = torch.full((65, dims.vocab), float("nan")).pin_memory()
+    h_hid = torch.full((512, dims.hidden), float("nan")).pin_memory()
+    g.launch_host(x_host, logits_out=h_log, hidden_out=h_hid)
+    assert torch.equal(x_dev.cpu(), x_host)
+    ref_l, ref_h = logits.cpu(), hid.cpu()
+    assert torch.equal(h_log, ref_l) and torch.equal(h_hid, ref_h)
+    # the same step launched on the device buffers agrees
+    eh = torch.empty_like(hid)
+    el = torch.empty_like(logits)
+    m.step(kv, b, x_dev, hidden_out=eh, logits_out=el)
+    torch.cuda.synchronize()
+    assert rel(el.cpu(), ref_l) <= 1e-4 and rel(eh.cpu(), ref_h) <= 1e-4
+    m.sync_status()
+    g.close()
+    kv.close()
