@@ -52,6 +52,8 @@ struct NormArgs {
   const int32_t* ridx;    // kSrcResidual: optional source row per output row
   float* zero;
   size_t zero_n;
+  float* zero2;           // a second region to clear (a split-K accumulator of the next GEMM)
+  size_t zero2_n;
   // kSrcRows / kSrcTokens, optional: the step's rotary table cs[r][i] =
   // (cos, sin) of pos[r] * inv_freq[i], i < half_d
   const int32_t* pos;
@@ -149,16 +151,89 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
                          Elem<T>::pack(v[k].z * inv * gv[k].z, v[k].w * inv * gv[k].w));
     }
   }
-  if (a.zero) {
-    // block r clears its share, a multiple of 4 floats (16-byte stores)
-    const size_t per = ((a.zero_n + gridDim.x - 1) / gridDim.x + 3) & ~(size_t)3;
-    const size_t z0 = per * r, z1 = min(a.zero_n, z0 + per);
+  // block r clears its share of each region, a multiple of 4 floats (16-byte stores)
+  auto clear = [&](float* z, size_t n) {
+    const size_t per = ((n + gridDim.x - 1) / gridDim.x + 3) & ~(size_t)3;
+    const size_t z0 = per * r, z1 = min(n, z0 + per);
     if (z0 < z1) {
       const size_t n4 = (z1 - z0) >> 2;
-      float4* z4 = reinterpret_cast<float4*>(a.zero + z0);
+      float4* z4 = reinterpret_cast<float4*>(z + z0);
       for (size_t i = threadIdx.x; i < n4; i += kNormThreads) z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (size_t i = z0 + 4 * n4 + threadIdx.x; i < z1; i += kNormThreads) a.zero[i] = 0.f;
+      for (size_t i = z0 + 4 * n4 + threadIdx.x; i < z1; i += kNormThreads) z[i] = 0.f;
     }
+  };
+  if (a.zero) clear(a.zero, a.zero_n);
+  if (a.zero2) clear(a.zero2, a.zero2_n);
+}
+
+// The rotary embedding and KV-page append for rows whose QKV projection was
+// accumulated split-K into fp32 (the small-row steps): per row, q and k heads
+// are rotated in place (dim i with i + hd/2, the (cos, sin) table of the
+// row's position), and k and v are rounded once into the row's page slot --
+// what the fused QKV epilogue does for larger steps.  One block per row.
+template <typename T>
+__global__ void rope_append_kernel(float* qkv, int ld, RopeEpi rp, int* err) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int r = blockIdx.x;
+  const int half = rp.hd >> 1, hq4 = half >> 2;  // 4 pairs per item
+  const int heads = rp.qh + 2 * rp.kvh;
+  const int sl = rp.slot[r];
+  const int page = sl >= 0 ? sl / rp.page_size : -1;
+  const int off = sl - page * rp.page_size;
+  const bool slot_ok = sl >= 0 && page < rp.num_pages;
+  if (!slot_ok && threadIdx.x == 0) report(err, SAR_ERR_BOUNDS, SITE_ROPE_BOUNDS, r);
+  float* row = qkv + (size_t)r * ld;
+  const float4* cs4 = reinterpret_cast<const float4*>(rp.cs + (size_t)r * half);
+  for (int it = threadIdx.x; it < heads * hq4; it += blockDim.x) {
+    const int head = it / hq4, i = (it - head * hq4) * 4;
+    const bool is_v = head >= rp.qh + rp.kvh, is_k = !is_v && head >= rp.qh;
+    float4* p1 = reinterpret_cast<float4*>(row + head * rp.hd + i);
+    float4* p2 = reinterpret_cast<float4*>(row + head * rp.hd + half + i);
+    float4 a = *p1, b = *p2;
+    if (!is_v) {
+      const float4 c01 = cs4[i >> 1], c23 = cs4[(i >> 1) + 1];  // (cos, sin) of pairs i..i+3
+      const float c[4] = {c01.x, c01.z, c23.x, c23.z}, sn[4] = {c01.y, c01.w, c23.y, c23.w};
+      const float x1[4] = {a.x, a.y, a.z, a.w}, x2[4] = {b.x, b.y, b.z, b.w};
+      float y1[4], y2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        y1[e] = x1[e] * c[e] - x2[e] * sn[e];
+        y2[e] = x2[e] * c[e] + x1[e] * sn[e];
+      }
+      a = make_float4(y1[0], y1[1], y1[2], y1[3]);
+      b = make_float4(y2[0], y2[1], y2[2], y2[3]);
+      *p1 = a;
+      *p2 = b;
+    }
+    if ((is_k || is_v) && slot_ok) {
+      const int kh = head - rp.qh - (is_v ? rp.kvh : 0);
+      T* dst = static_cast<T*>(is_v ? rp.v_cache : rp.k_cache) + (((size_t)page * rp.kvh + kh) * rp.page_size + off) * rp.hd;
+      *reinterpret_cast<uint2*>(dst + i) = make_uint2(Elem<T>::pack(a.x, a.y), Elem<T>::pack(a.z, a.w));
+      *reinterpret_cast<uint2*>(dst + half + i) = make_uint2(Elem<T>::pack(b.x, b.y), Elem<T>::pack(b.z, b.w));
+    }
+  }
+}
+
+// silu(gate) * up from the gate/up projection accumulated split-K into fp32
+// (the packed layout: 64-row gate and up blocks interleaved), rounded once to
+// the storage type; what the fused SwiGLU epilogue does for larger steps.
+template <typename T>
+__global__ void swiglu_finish_kernel(const float* __restrict__ gu, T* __restrict__ act, int rows, int F) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const size_t n4 = (size_t)rows * F / 4;
+  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n4; q += (size_t)gridDim.x * blockDim.x) {
+    const size_t o = q * 4;
+    const size_t r = o / F;
+    const int f = (int)(o - r * F);
+    const int blk = f >> 6, j = f & 63;
+    const float* src = gu + r * 2 * (size_t)F + (size_t)blk * 128 + j;
+    const float4 g = *reinterpret_cast<const float4*>(src);
+    const float4 u = *reinterpret_cast<const float4*>(src + 64);
+    auto sl = [](float x) { return x / (1.0f + __expf(-x)); };
+    *reinterpret_cast<uint2*>(act + o) =
+        make_uint2(Elem<T>::pack(sl(g.x) * u.x, sl(g.y) * u.y), Elem<T>::pack(sl(g.z) * u.z, sl(g.w) * u.w));
   }
 }
 
@@ -267,7 +342,7 @@ __global__ void __launch_bounds__(1024) argmax_kernel(const float* __restrict__ 
 }  // namespace
 
 int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hidden, float eps,
-                   const int32_t* row_index, int storage, cudaStream_t s) {
+                   const int32_t* row_index, int storage, cudaStream_t s, float* zero, size_t zero_n) {
   if (rows <= 0) return SAR_OK;
   if (hidden % 4 || hidden > 4 * kNormThreads * kNormMaxVec)
     return set_error(SAR_ERR_UNSUPPORTED, "rmsnorm: hidden must be a multiple of 4 and at most 8192");
@@ -278,6 +353,8 @@ int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hid
   a.ridx = row_index;
   a.hidden = hidden;
   a.eps = eps;
+  a.zero = zero;
+  a.zero_n = zero_n;
   cudaError_t e = storage == SAR_STORAGE_BF16
                       ? launch_pdl(rmsnorm_kernel<__nv_bfloat16, kSrcResidual>, dim3(rows), dim3(kNormThreads), 0, s, a)
                       : launch_pdl(rmsnorm_kernel<__half, kSrcResidual>, dim3(rows), dim3(kNormThreads), 0, s, a);
@@ -289,7 +366,7 @@ int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hid
 int launch_input_norm(int in_kind, const void* in, const void* table, int vocab, float* h, const float* gain,
                       void* y, int rows, int hidden, float eps, int storage, int* err, cudaStream_t s,
                       float* zero, size_t zero_n, const int32_t* pos, const double* inv_freq, float2* cs,
-                      int half_d) {
+                      int half_d, float* zero2, size_t zero2_n) {
   if (rows <= 0) return SAR_OK;
   if (hidden % 4 || hidden > 4 * kNormThreads * kNormMaxVec)
     return set_error(SAR_ERR_UNSUPPORTED, "rmsnorm: hidden must be a multiple of 4 and at most 8192");
@@ -305,6 +382,8 @@ int launch_input_norm(int in_kind, const void* in, const void* table, int vocab,
   a.err = err;
   a.zero = zero;
   a.zero_n = zero_n;
+  a.zero2 = zero2;
+  a.zero2_n = zero2_n;
   a.pos = pos;
   a.inv_freq = inv_freq;
   a.cs = cs;
@@ -319,6 +398,33 @@ int launch_input_norm(int in_kind, const void* in, const void* table, int vocab,
     e = bf ? launch_pdl(rmsnorm_kernel<__nv_bfloat16, kSrcRows>, g, b, 0, s, a)
            : launch_pdl(rmsnorm_kernel<__half, kSrcRows>, g, b, 0, s, a);
   if (e != cudaSuccess) return cuda_error(e, "input norm launch");
+  count_launches(1);
+  return SAR_OK;
+}
+
+int launch_rope_append(float* qkv, int ld, int rows, const RopeEpi& rp, int storage, int* err, cudaStream_t s) {
+  if (rows <= 0) return SAR_OK;
+  if ((rp.hd != 64 && rp.hd != 128) || ld != (rp.qh + 2 * rp.kvh) * rp.hd || !rp.slot || !rp.cs)
+    return set_error(SAR_ERR_INVALID_ARG, "rope/append: bad arguments");
+  cudaError_t e = storage == SAR_STORAGE_BF16
+                      ? launch_pdl(rope_append_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, qkv, ld, rp, err)
+                      : launch_pdl(rope_append_kernel<__half>, dim3(rows), dim3(256), 0, s, qkv, ld, rp, err);
+  if (e != cudaSuccess) return cuda_error(e, "rope/append launch");
+  count_launches(1);
+  return SAR_OK;
+}
+
+int launch_swiglu_finish(const float* gu, void* act, int rows, int F, int storage, cudaStream_t s) {
+  if (rows <= 0) return SAR_OK;
+  if (F % 64) return set_error(SAR_ERR_INVALID_ARG, "swiglu: F must be a multiple of 64");
+  const size_t n4 = (size_t)rows * F / 4;
+  const int blocks = (int)std::min<size_t>((n4 + 255) / 256, (size_t)num_sms() * 8);
+  cudaError_t e = storage == SAR_STORAGE_BF16
+                      ? launch_pdl(swiglu_finish_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, s, gu,
+                                   static_cast<__nv_bfloat16*>(act), rows, F)
+                      : launch_pdl(swiglu_finish_kernel<__half>, dim3(blocks), dim3(256), 0, s, gu,
+                                   static_cast<__half*>(act), rows, F);
+  if (e != cudaSuccess) return cuda_error(e, "swiglu launch");
   count_launches(1);
   return SAR_OK;
 }

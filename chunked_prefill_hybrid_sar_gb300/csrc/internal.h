@@ -110,8 +110,10 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
 
 // ---- elementwise kernels (elementwise.cu) ----------------------------------
 // x: fp32 residual rows; y: storage-type rows; row_index (optional) gathers rows.
+// zero (optional): zero_n floats to clear, split over the blocks.
 int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hidden, float eps,
-                   const int32_t* row_index, int storage, cudaStream_t s);
+                   const int32_t* row_index, int storage, cudaStream_t s, float* zero = nullptr,
+                   size_t zero_n = 0);
 // The step's first kernel: stacked input rows (bf16 hidden rows, or token ids
 // looked up in `table`) into the fp32 residual stream h and, normalised with
 // `gain`, into y (storage type).  zero (optional): zero_n floats to clear.
@@ -120,7 +122,13 @@ int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hid
 int launch_input_norm(int in_kind, const void* in, const void* table, int vocab, float* h, const float* gain,
                       void* y, int rows, int hidden, float eps, int storage, int* err, cudaStream_t s,
                       float* zero = nullptr, size_t zero_n = 0, const int32_t* pos = nullptr,
-                      const double* inv_freq = nullptr, float2* cs = nullptr, int half_d = 0);
+                      const double* inv_freq = nullptr, float2* cs = nullptr, int half_d = 0,
+                      float* zero2 = nullptr, size_t zero2_n = 0);
+// Small-row steps, whose QKV and gate/up projections accumulate split-K into
+// fp32: the rotary embedding + KV-page append over qkv rows [rows][ld] in
+// place, and silu(gate)*up from the packed fp32 gate/up rows [rows][2F].
+int launch_rope_append(float* qkv, int ld, int rows, const RopeEpi& rp, int storage, int* err, cudaStream_t s);
+int launch_swiglu_finish(const float* gu, void* act, int rows, int F, int storage, cudaStream_t s);
 int launch_embed(const int32_t* tokens, const void* table, float* out, int rows, int hidden, int vocab,
                  int storage, int* err, cudaStream_t s);
 int launch_bf16_to_f32(const void* src, float* dst, size_t n, cudaStream_t s);

@@ -30,6 +30,7 @@ using sar::cuda_error;
 namespace {
 
 constexpr int kMetaRing = 4;
+constexpr int kSmallStepRows = 256;  // steps this small use the swap tiling (tokens on the MMA's N side)
 
 using st16 = uint16_t;  // one element of the storage type (fp16 or bf16)
 using WMaps = CUtensorMap[sar::kWeightBoxes];  // one weight matrix, every box height
@@ -67,6 +68,7 @@ struct sar_model {
   float2* rope_cs = nullptr;  // [max_tokens][head_dim / 2] (cos, sin) of this step's positions
   float* hres = nullptr;   // residual stream, fp32
   float* qkv32 = nullptr;  // QKV projection in fp32, q and k rotated by the projection's epilogue
+  float* gu32 = nullptr;   // small steps: gate/up projection accumulated split-K in fp32
   void* in_stage = nullptr;
   float* partials = nullptr;
   size_t partials_cap = 0;  // floats
@@ -417,6 +419,21 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
                 const void* in, float* h, float* logits, void* layer_out, cudaStream_t s) {
   const sar_dims& d = m->d;
   const int M = p.M, H = d.hidden;
+  // Small steps (the swap tiling): a weight tile per CTA leaves most SMs idle
+  // for the QKV and gate/up projections (48 and 224 tiles at Mistral's
+  // shape), so when the tiling's cost model splits K they accumulate split-K
+  // into fp32 scratch cleared by the preceding norm, and small kernels apply
+  // the rotary embedding + KV append and silu(gate)*up afterwards.
+  bool qkv_split = false, gu_split = false;
+  if (M <= kSmallStepRows && m->gu32) {
+    sar::GemmCfg gc;
+    qkv_split = sar::gemm_config(M, m->qkv_n, H, SAR_EPI_RESIDUAL, SAR_GEMM_AUTO, &gc, true) == SAR_OK &&
+                gc.swap && gc.splits > 1;
+    gu_split = sar::gemm_config(M, 2 * d.ffn, H, SAR_EPI_RESIDUAL, SAR_GEMM_AUTO, &gc, true) == SAR_OK &&
+               gc.swap && gc.splits > 1;
+  }
+  float* qkv_zero = qkv_split ? m->qkv32 : nullptr;
+  const size_t qkv_zero_n = qkv_split ? (size_t)M * m->qkv_n : 0;
 
   for (int l = 0; l < d.n_layers; ++l) {
     LayerW& w = m->L[l];
@@ -427,10 +444,10 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
       Prof pr(m, SAR_K_EMBED, s);
       SAR_TRY(sar::launch_input_norm(b->in_kind, in, m->embed, d.vocab, h, w.n1, m->xn, M, H, d.rms_eps, d.storage,
                                      m->err, s, logits, logits ? (size_t)p.R * d.vocab : 0, md + p.o_pos,
-                                     m->inv_freq, m->rope_cs, d.head_dim / 2));
+                                     m->inv_freq, m->rope_cs, d.head_dim / 2, qkv_zero, qkv_zero_n));
     } else {
       Prof pr(m, SAR_K_RMSNORM, s);
-      SAR_TRY(sar::launch_rmsnorm(h, w.n1, m->xn, M, H, d.rms_eps, nullptr, d.storage, s));
+      SAR_TRY(sar::launch_rmsnorm(h, w.n1, m->xn, M, H, d.rms_eps, nullptr, d.storage, s, qkv_zero, qkv_zero_n));
     }
     uint16_t* kc = kv->k + (size_t)l * kv->layer_elems;
     uint16_t* vc = kv->v + (size_t)l * kv->layer_elems;
@@ -449,7 +466,12 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
       rp.hd = d.head_dim;
       rp.page_size = kv->page_size;
       rp.num_pages = kv->num_pages;
-      SAR_TRY(run_gemm(m, m->xn, M, w.m_qkv, m->qkv_n, H, sar::kEpiRope, m->qkv32, nullptr, s, &rp));
+      if (qkv_split) {
+        SAR_TRY(run_gemm(m, m->xn, M, w.m_qkv, m->qkv_n, H, SAR_EPI_RESIDUAL, m->qkv32, m->qkv32, s));
+        SAR_TRY(sar::launch_rope_append(m->qkv32, m->qkv_n, M, rp, d.storage, m->err, s));
+      } else {
+        SAR_TRY(run_gemm(m, m->xn, M, w.m_qkv, m->qkv_n, H, sar::kEpiRope, m->qkv32, nullptr, s, &rp));
+      }
     }
     // two-stream split: chunk attention forks onto the side stream after the
     // QKV projection and joins before the O projection
@@ -527,11 +549,17 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
     }
     {
       Prof pr(m, SAR_K_RMSNORM, s);
-      SAR_TRY(sar::launch_rmsnorm(h, w.n2, m->xn, M, H, d.rms_eps, nullptr, d.storage, s));
+      SAR_TRY(sar::launch_rmsnorm(h, w.n2, m->xn, M, H, d.rms_eps, nullptr, d.storage, s,
+                                  gu_split ? m->gu32 : nullptr, gu_split ? (size_t)M * 2 * d.ffn : 0));
     }
     {
       Prof pr(m, SAR_K_GEMM_GATEUP, s);
-      SAR_TRY(run_gemm(m, m->xn, M, w.m_gu, 2 * d.ffn, H, SAR_EPI_SWIGLU, m->act, nullptr, s));
+      if (gu_split) {
+        SAR_TRY(run_gemm(m, m->xn, M, w.m_gu, 2 * d.ffn, H, SAR_EPI_RESIDUAL, m->gu32, m->gu32, s));
+        SAR_TRY(sar::launch_swiglu_finish(m->gu32, m->act, M, d.ffn, d.storage, s));
+      } else {
+        SAR_TRY(run_gemm(m, m->xn, M, w.m_gu, 2 * d.ffn, H, SAR_EPI_SWIGLU, m->act, nullptr, s));
+      }
     }
     {
       Prof pr(m, SAR_K_GEMM_DOWN, s);
@@ -626,8 +654,10 @@ int sar_model_create(const sar_dims* dims, sar_model** out) {
   // step workspace
   const size_t T = d.max_tokens;
   const size_t R = T;  // head rows: every chunk's last row and every decode row (at most all rows)
+  const size_t Ts = std::min<size_t>(T, kSmallStepRows);  // rows of the small steps' split-K gate/up scratch
   const size_t ws = align256(T * H * 2) + align256(T * (d.head_dim / 2) * 8) + align256(T * m->qd * 2) + align256(T * F * 2) +
-                    align256(T * H * 4) + align256(R * H * 2) + align256(T * H * 2) + align256(T * m->qkv_n * 4) + 256;
+                    align256(T * H * 4) + align256(R * H * 2) + align256(T * H * 2) + align256(T * m->qkv_n * 4) +
+                    align256(Ts * 2 * F * 4) + 256;
   e = cudaMalloc(&m->ws, ws);
   if (e == cudaSuccess) e = cudaMalloc(&m->err, 16);
   if (e == cudaSuccess) e = cudaMemset(m->err, 0, 16);
@@ -645,6 +675,7 @@ int sar_model_create(const sar_dims* dims, sar_model** out) {
   m->hrows = take(R * H * 2);
   m->in_stage = take(T * H * 2);
   m->qkv32 = takef(T * m->qkv_n * 4);
+  m->gu32 = takef(Ts * 2 * F * 4);
   // rotary frequencies base^(-2i/d), double precision
   std::vector<double> inv(d.head_dim / 2);
   for (int i = 0; i < d.head_dim / 2; ++i) inv[i] = std::pow((double)d.rope_base, -2.0 * i / d.head_dim);

@@ -5,8 +5,10 @@ The graph keeps its own copy of the step's metadata; ``update`` swaps in the
 metadata of another batch with the same plan shape (here: the decodes one
 token further, within the same pages).  Bars: the oracle's (per-layer hidden
 max-abs <= 3e-2, relative L2 <= 1e-2); graph vs kernel-by-kernel relative L2
-<= 1e-4 (the split-K projections add their K ranges atomically, in an order
-that differs from run to run).
+<= 1e-3 (the split-K projections add their K ranges atomically, in an order
+that differs from run to run; in small steps that includes the QKV
+projection, whose k and v are then rounded to 16 bits, so a last-bit
+difference can flip a stored key).
 """
 
 import numpy as np
@@ -19,6 +21,8 @@ from chunked_prefill_hybrid_sar_gb300 import harness
 from oracle import model as om
 
 pytestmark = pytest.mark.gpu
+
+RUN_TO_RUN = 1e-3
 
 
 def rel(a, b):
@@ -80,8 +84,8 @@ def test_graph_step_equals_kernel_by_kernel_and_oracle(mistral):
         torch.cuda.synchronize()
         outs[mode] = (hid.cpu(), logits.cpu())
         kv.close()
-    assert rel(outs["graph"][0], outs["eager"][0]) <= 1e-4
-    assert rel(outs["graph"][1], outs["eager"][1]) <= 1e-4
+    assert rel(outs["graph"][0], outs["eager"][0]) <= RUN_TO_RUN
+    assert rel(outs["graph"][1], outs["eager"][1]) <= RUN_TO_RUN
     w = om.layer_weights_np(case["layers"][0])
     head = om.layer_weights_np(case["head"])
     parts = [om.Part(x=om.to_np(prompt), lo=start, is_prefill=True)]
@@ -127,10 +131,10 @@ def test_graph_update_replays_the_next_decode_step(mistral):
         runs[mode] = got
         kv.close()
     for t in range(2):
-        assert rel(runs["graph"][t][0], runs["eager"][t][0]) <= 1e-4, t
-        assert rel(runs["graph"][t][1], runs["eager"][t][1]) <= 1e-4, t
+        assert rel(runs["graph"][t][0], runs["eager"][t][0]) <= RUN_TO_RUN, t
+        assert rel(runs["graph"][t][1], runs["eager"][t][1]) <= RUN_TO_RUN, t
     # the second step differs from the first (the keys written by the first are attended)
-    assert rel(runs["graph"][1][0], runs["graph"][0][0]) > 1e-4
+    assert rel(runs["graph"][1][0], runs["graph"][0][0]) > RUN_TO_RUN
 
 
 def test_graph_update_refuses_another_shape(mistral):
@@ -177,7 +181,7 @@ def test_graph_launch_host_copies_in_and_out(mistral):
     el = torch.empty_like(logits)
     m.step(kv, b, x_dev, hidden_out=eh, logits_out=el)
     torch.cuda.synchronize()
-    assert rel(el.cpu(), ref_l) <= 1e-4 and rel(eh.cpu(), ref_h) <= 1e-4
+    assert rel(el.cpu(), ref_l) <= RUN_TO_RUN and rel(eh.cpu(), ref_h) <= RUN_TO_RUN
     m.sync_status()
     g.close()
     kv.close()

@@ -70,3 +70,18 @@ def test_rows_at_tile_edges_match_oracle(sweep, M):
     got = hid.cpu().numpy().astype(np.float64)
     assert_close(got[:lp], chunk_ref[:lp], f"M={M} chunk rows")
     assert_close(got[lp:], dec_ref, f"M={M} decode rows")
+
+
+@pytest.mark.parametrize("bd", [1, 8, 32])
+def test_decode_only_steps_match_oracle(sweep, bd):
+    """Decode-only steps (the small-row regime: QKV and gate/up accumulate
+    split-K in fp32, then the rotary/append and SwiGLU kernels)."""
+    case, m, kv, dec_bt, prompt_bt, chunk_ref, dec_ref = sweep
+    dims, ctx = case["dims"], case["ctx"]
+    decs = [(100 + i, ctx, dec_bt[i]) for i in range(bd)]
+    x = case["decode_inputs"][:bd].cuda().contiguous()
+    hid = torch.empty(bd, dims.hidden, dtype=torch.float32, device="cuda")
+    m.step(kv, sar.Batch(None, decs), x, hidden_out=hid)
+    m.sync_status()
+    torch.cuda.synchronize()
+    assert_close(hid.cpu().numpy().astype(np.float64), dec_ref[:bd], f"Bd={bd} decode rows")
