@@ -63,13 +63,29 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        # sampling every 5 ms; the timed region starts once the first sample has
+        # arrived, so every later sample falls inside it (or just after it ends)
+        import threading
+        self.lines, self.first = [], threading.Event()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "20"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "--format=csv,noheader,nounits", "-lms", "5"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except OSError:
             self.proc = None
+            return self
+
+        def reader():
+            for line in self.proc.stdout:
+                self.lines.append(line)
+                self.first.set()
+            self.first.set()
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        self.first.wait(timeout=10)
+        self.skip = len(self.lines)  # samples taken before the timed region
         return self
 
     def __exit__(self, *exc):
@@ -77,10 +93,12 @@ class ClockSampler:
         if self.proc:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
+                self.proc.wait()
+            self.thread.join(timeout=5)
+            self.out = "".join(self.lines[self.skip:])
 
     def summary(self):
         sms, maxs, reasons = [], [], set()
@@ -721,7 +739,7 @@ def run_long_prompt(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=6)
     ap.add_argument("--impl", choices=["sar", "reference"], default="sar")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
