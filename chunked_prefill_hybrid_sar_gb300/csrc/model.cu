@@ -251,21 +251,23 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
     btlen[i] = nb;
     bt.insert(bt.end(), dc.block_table, dc.block_table + nb);
     const int kfirst = first_key(nk);
-    const int ns = (int)((span_of(dc.ctx_len) + split - 1) / split);
+    const int span = span_of(dc.ctx_len);
+    const int ns = (int)((span + split - 1) / split);
+    // equal ranges (16-key multiples) rather than full ranges plus a remainder
+    const int len = ((span + ns - 1) / ns + 15) / 16 * 16;
     pcnt[i] = ns;
     if (ns > 1) {
       pbeg[i] = n_parts;
     }
     for (int sidx = 0; sidx < ns; ++sidx) {
-      const int k0 = kfirst + (int)(sidx * split);
-      const int k1 = std::max(k0, std::min<int>(nk, kfirst + (int)((sidx + 1) * split)));
+      const int k0 = kfirst + sidx * len;
+      const int k1 = std::max(k0, std::min(nk, k0 + len));
       const int part = ns > 1 ? n_parts + sidx : -1;
-      auto& dst = (k1 - k0 == split) ? items : tail_items;  // full ranges first
-      dst.insert(dst.end(), {i, k0, k1, part});
+      tail_items.insert(tail_items.end(), {i, k0, k1, part});
     }
     if (ns > 1) n_parts += ns;
   }
-  // remainders longest first, after every full range
+  // longest ranges first, so the grid's last CTAs are its shortest
   {
     std::vector<int> order(tail_items.size() / 4);
     for (size_t t = 0; t < order.size(); ++t) order[t] = (int)t;
@@ -1080,6 +1082,17 @@ int sar_graph_launch(sar_graph* g, void* stream) {
   return SAR_OK;
 }
 
+namespace {
+
+// Host <-> device copy of a step's rows (UVA picks the direction).  A grid-wide
+// copy kernel over pinned memory measured no faster than the copy engine here:
+// the host link, not the engine, sets the rate.
+int host_copy(void* dst, const void* src, size_t n, cudaStream_t s) {
+  return check(cudaMemcpyAsync(dst, src, n, cudaMemcpyDefault, s), "host copy");
+}
+
+}  // namespace
+
 int sar_graph_launch_host(sar_graph* g, const void* in, float* logits_out, float* hidden_out, void* stream) {
   if (!g || !in) return set_error(SAR_ERR_INVALID_ARG, "graph: null argument");
   if ((logits_out && !g->logits) || (hidden_out && !g->hidden))
@@ -1087,13 +1100,10 @@ int sar_graph_launch_host(sar_graph* g, const void* in, float* logits_out, float
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t M = (size_t)g->p.M, H = (size_t)g->m->d.hidden;
   const size_t in_bytes = g->in_kind == SAR_IN_TOKENS ? M * 4 : M * H * 2;
-  SAR_TRY(check(cudaMemcpyAsync(g->in, in, in_bytes, cudaMemcpyHostToDevice, s), "graph: input copy"));
+  SAR_TRY(host_copy(g->in, in, in_bytes, s));
   SAR_TRY(check(cudaGraphLaunch(g->exec, s), "graph: launch"));
-  if (logits_out)
-    SAR_TRY(check(cudaMemcpyAsync(logits_out, g->logits, (size_t)g->p.R * g->m->d.vocab * 4, cudaMemcpyDeviceToHost, s),
-                  "graph: logits copy"));
-  if (hidden_out)
-    SAR_TRY(check(cudaMemcpyAsync(hidden_out, g->hidden, M * H * 4, cudaMemcpyDeviceToHost, s), "graph: hidden copy"));
+  if (logits_out) SAR_TRY(host_copy(logits_out, g->logits, (size_t)g->p.R * g->m->d.vocab * 4, s));
+  if (hidden_out) SAR_TRY(host_copy(hidden_out, g->hidden, M * H * 4, s));
   return check(cudaStreamSynchronize(s), "graph: synchronise");
 }
 

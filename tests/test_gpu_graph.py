@@ -176,6 +176,10 @@ def test_graph_launch_host_copies_in_and_out(mistral):
     assert torch.equal(x_dev.cpu(), x_host)
     ref_l, ref_h = logits.cpu(), hid.cpu()
     assert torch.equal(h_log, ref_l) and torch.equal(h_hid, ref_h)
+    # pageable host buffers take the copy engine instead of the copy kernel
+    p_log = torch.full((65, dims.vocab), float("nan"))
+    g.launch_host(x_host.clone(), logits_out=p_log)
+    assert rel(p_log, ref_l) <= RUN_TO_RUN
     # the same step launched on the device buffers agrees
     eh = torch.empty_like(hid)
     el = torch.empty_like(logits)
