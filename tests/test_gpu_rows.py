@@ -85,3 +85,43 @@ def test_decode_only_steps_match_oracle(sweep, bd):
     m.sync_status()
     torch.cuda.synchronize()
     assert_close(hid.cpu().numpy().astype(np.float64), dec_ref[:bd], f"Bd={bd} decode rows")
+
+
+@pytest.mark.parametrize("storage", [sar.SAR_STORAGE_F16, sar.SAR_STORAGE_BF16], ids=["f16", "bf16"])
+def test_small_step_split_path_both_storage_types(storage):
+    """A decode-only step of a layer wide enough (H 1024, K = 16 slabs) that the
+    small-step QKV and gate/up projections split K, in fp16 and in bf16
+    storage (the rotary/append and SwiGLU finishing kernels of each type)."""
+    import dataclasses
+    dims = synth.Dims(n_layers=1, hidden=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn=2048, vocab=0)
+    case = synth.window_case(3, d=dims, prompt_len=16, ctxs=(40, 200, 333, 517, 700, 64, 129, 999))
+    m = harness.load_model(dims, case["layers"], None, max_tokens=64, max_decodes=8, storage=storage)
+    n_pages = sum(c // PS + 1 for c in case["ctxs"]) + 4
+    kv = sar.KVCache(m, PS, n_pages)
+    alloc = harness.PageAllocator(synth.page_permutation(synth.generator(9), n_pages))
+    decs = []
+    for i, c in enumerate(case["ctxs"]):
+        bt = alloc.take(c // PS + 1)
+        k, v = case["histories"][i]
+        harness.write_history(kv, dims, 0, k, v, bt)
+        decs.append((10 + i, c, bt))
+    x = case["decode_inputs"].cuda().contiguous()
+    hid = torch.empty(len(decs), dims.hidden, dtype=torch.float32, device="cuda")
+    m.step(kv, sar.Batch(None, decs), x, hidden_out=hid)
+    m.sync_status()
+    torch.cuda.synchronize()
+    w = om.layer_weights_np(case["layers"][0])
+    parts = [om.Part(x=om.to_np(case["decode_inputs"][i:i + 1]), lo=c,
+                     given=[om.LayerCache(om.to_np(k), om.to_np(v))])
+             for i, (c, (k, v)) in enumerate(zip(case["ctxs"], case["histories"]))]
+    ref, _ = om.hybrid_step([w], None, dims, parts)
+    assert_close(hid.cpu().numpy().astype(np.float64), ref[0], f"storage {storage}")
+    # the new keys were appended into the pages (rotary applied): read one back
+    got_k = harness.read_history(kv, dims, 0, 0, decs[0][2], case["ctxs"][0] + 1)[-1].float().cpu().numpy()
+    y = om.rms_norm(om.to_np(case["decode_inputs"][0:1]), w["norm1"], dims.rms_eps)
+    k_ref = om.apply_rope((y @ w["wk"].T).reshape(1, dims.n_kv_heads, dims.head_dim), [case["ctxs"][0]],
+                          dims.rope_base)[0]
+    tol = 2e-2 if storage == sar.SAR_STORAGE_BF16 else 4e-3
+    assert np.abs(got_k - k_ref).max() <= tol * max(1.0, np.abs(k_ref).max())
+    kv.close()
+    m.close()
