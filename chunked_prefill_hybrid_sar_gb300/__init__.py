@@ -290,6 +290,29 @@ class Scheduler:
             pass
 
 
+_LAYOUT = ("M", "Lp", "Bd", "R", "n_items", "n_parts", "n_tiles", "tile_rows", "o_pos", "o_slot", "o_pbt",
+           "o_nkeys", "o_btoff", "o_btlen", "o_pbeg", "o_pcnt", "o_items", "o_bt", "o_rows", "o_tiles", "total")
+
+
+def plan_inspect(dims, batch: Batch, page_size: int, num_pages: int, sms: int, max_tokens: int,
+                 max_decodes: int, storage: int = SAR_STORAGE_F16) -> dict:
+    """The step planner on the host alone (``sar_plan_inspect``): the plan's
+    sizes and array offsets, and the metadata block as a list of int32."""
+    d = _lib.sar_dims(dims.n_layers, dims.hidden, dims.n_q_heads, dims.n_kv_heads, dims.head_dim,
+                      dims.ffn, dims.vocab, dims.rms_eps, dims.rope_base, max_tokens, max_decodes,
+                      storage, getattr(dims, "sliding_window", 0))
+    lay = (ctypes.c_int32 * len(_LAYOUT))()
+    n = ctypes.c_int64()
+    check(lib().sar_plan_inspect(ctypes.byref(d), page_size, num_pages, sms, ctypes.byref(batch.c), lay, None, 0,
+                                 ctypes.byref(n)))
+    meta = (ctypes.c_int32 * max(1, n.value))()
+    check(lib().sar_plan_inspect(ctypes.byref(d), page_size, num_pages, sms, ctypes.byref(batch.c), lay, meta,
+                                 n.value, ctypes.byref(n)))
+    out = dict(zip(_LAYOUT, list(lay)))
+    out["meta"] = list(meta)[:n.value]
+    return out
+
+
 def _storage_of(t) -> int:
     import torch
     return SAR_STORAGE_BF16 if t.dtype == torch.bfloat16 else SAR_STORAGE_F16

@@ -105,6 +105,8 @@ SIGNATURES = {
     "sar_sched_destroy": (i32, [vp]),
     "sar_op_gemm": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
     "sar_op_rmsnorm": (i32, [vp, vp, vp, i32, i32, ctypes.c_float, i32, vp]),
+    "sar_plan_inspect": (i32, [ctypes.POINTER(sar_dims), i32, i32, i32, ctypes.POINTER(sar_batch), P_i32, P_i32,
+                               i64, ctypes.POINTER(i64)]),
     "sar_model_debug_buffer": (i32, [vp, i32, ctypes.POINTER(vp)]),
     "sar_decode_attention_noalloc": (i32, [vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32,
                                            vp, i32, vp, i32, i32, vp, vp]),

@@ -174,19 +174,36 @@ std::vector<sar_prefill> batch_chunks(const sar_batch* b) {
   return c;
 }
 
+// What the planner needs to know about the model, the cache and the device.
+struct PlanEnv {
+  sar_dims d;
+  int page_size = 0, num_pages = 0, sms = 0;
+  bool has_embed = false;
+};
+
+PlanEnv plan_env(const sar_model* m, const sar_kv* kv) {
+  PlanEnv e;
+  e.d = m->d;
+  e.page_size = kv->page_size;
+  e.num_pages = kv->num_pages;
+  e.sms = sar::num_sms();
+  e.has_embed = m->embed != nullptr;
+  return e;
+}
+
 // Query rows per CTA of the chunk-attention kernel the step will launch.
-int chunk_tile_rows(const sar_dims& d, const sar_kv* kv) {
+int chunk_tile_rows(const sar_dims& d, int page_size) {
   sar::ChunkAttnArgs probe{};
   probe.d = d.head_dim;
-  probe.page_size = kv->page_size;
+  probe.page_size = page_size;
   probe.qh = d.n_q_heads;
   probe.kvh = d.n_kv_heads;
   probe.window = d.sliding_window;
   return sar::chunk_attention_tc_supported(probe) ? sar::kChunkTileRowsTc : sar::kChunkTileRows;
 }
 
-int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* p, std::vector<int32_t>* meta) {
-  const sar_dims& d = m->d;
+int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vector<int32_t>* meta) {
+  const sar_dims& d = env.d;
   if (b->n_decode < 0 || (b->n_decode > 0 && !b->decode)) return set_error(SAR_ERR_INVALID_ARG, "step: bad decode list");
   if (b->n_more_prefill < 0 || (b->n_more_prefill > 0 && !b->more_prefill))
     return set_error(SAR_ERR_INVALID_ARG, "step: bad chunk list");
@@ -204,13 +221,14 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
   if (M > d.max_tokens) return set_error(SAR_ERR_INVALID_ARG, "step: Lp + Bd exceeds max_tokens");
   if (Bd > d.max_decodes) return set_error(SAR_ERR_INVALID_ARG, "step: Bd exceeds max_decodes");
   if (b->in_kind != SAR_IN_HIDDEN && b->in_kind != SAR_IN_TOKENS) return set_error(SAR_ERR_INVALID_ARG, "step: bad in_kind");
-  if (b->in_kind == SAR_IN_TOKENS && (d.vocab == 0 || !m->embed)) return set_error(SAR_ERR_INVALID_ARG, "step: token input without an embedding");
-  const int ps = kv->page_size;
+  if (b->in_kind == SAR_IN_TOKENS && (d.vocab == 0 || !env.has_embed))
+    return set_error(SAR_ERR_INVALID_ARG, "step: token input without an embedding");
+  const int ps = env.page_size;
   auto check_bt = [&](const int32_t* bt, int nb, int last_pos) -> int {
     if (nb < 0 || (int64_t)nb * ps <= last_pos) return set_error(SAR_ERR_INVALID_ARG, "step: block table does not cover the positions");
     const int need = last_pos / ps + 1;
     for (int i = 0; i < need; ++i)
-      if (bt[i] < 0 || bt[i] >= kv->num_pages) return set_error(SAR_ERR_BOUNDS, "step: page id out of range");
+      if (bt[i] < 0 || bt[i] >= env.num_pages) return set_error(SAR_ERR_BOUNDS, "step: page id out of range");
     return SAR_OK;
   };
   for (const sar_prefill& c : chunks) SAR_TRY(check_bt(c.block_table, c.n_blocks, c.start_pos + c.len - 1));
@@ -236,7 +254,7 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
   // decode work split: key ranges of `split` keys, about four CTAs (two per
   // resident slot) per SM; fewer, longer ranges measured faster than more,
   // shorter ones (less set-up and merging per key), up to 2048 keys
-  const int sms = sar::num_sms();
+  const int sms = env.sms;
   int64_t split = (total_keys * d.n_kv_heads) / (4LL * sms);
   split = std::max<int64_t>(128, std::min<int64_t>(2048, (split + 15) / 16 * 16));
   std::vector<int32_t> items, pbeg(Bd, -1), pcnt(Bd, 0), nkeys(Bd), btoff(Bd), btlen(Bd), bt;
@@ -289,7 +307,7 @@ int validate_and_plan(sar_model* m, const sar_kv* kv, const sar_batch* b, Plan* 
   // chunk block tables (each cut to the pages its positions use) and the
   // chunk-attention tiles: {first batch row, first position, rows, block-table
   // offset, block-table length}, the most keys first (the longest CTAs start first)
-  const int tile_rows = chunk_tile_rows(d, kv);
+  const int tile_rows = chunk_tile_rows(d, ps);
   std::vector<int32_t> pbt, tiles;
   {
     std::vector<std::array<int32_t, 8>> tl;
@@ -412,7 +430,7 @@ int plan_step(sar_model* m, sar_kv* kv, const sar_batch* b, bool logits, Plan* p
   for (int l = 0; l < d.n_layers; ++l)
     if (!m->L[l].set) return set_error(SAR_ERR_INVALID_ARG, "step: layer weights not set");
   if (logits && (d.vocab == 0 || !m->head_set)) return set_error(SAR_ERR_INVALID_ARG, "step: logits requested without a head");
-  return validate_and_plan(m, kv, b, p, meta);
+  return validate_and_plan(plan_env(m, kv), b, p, meta);
 }
 
 // Launches the step's kernels on `s`, reading the plan's metadata at device
@@ -947,6 +965,33 @@ int sar_op_gemm(const void* a, const void* w, void* c, const void* residual, int
   SAR_TRY(sar::make_tmap_16(&amap, a, M, K, cfg.swap ? cfg.b_box_rows : cfg.a_box_rows, storage));
   SAR_TRY(sar::make_tmap_16(&wmap, w, N, K, cfg.swap ? cfg.a_box_rows : cfg.b_box_rows, storage));
   return sar::gemm_launch(cfg, amap, wmap, M, N, K, epilogue, storage, c, residual, err, static_cast<cudaStream_t>(stream));
+}
+
+int sar_plan_inspect(const sar_dims* dims, int32_t page_size, int32_t num_pages, int32_t sms, const sar_batch* b,
+                     int32_t* layout, int32_t* meta, int64_t meta_cap, int64_t* meta_n) {
+  if (!dims || !b || !layout || sms <= 0 || page_size <= 0 || num_pages <= 0)
+    return set_error(SAR_ERR_INVALID_ARG, "plan_inspect: bad argument");
+  PlanEnv env;
+  env.d = *dims;
+  env.page_size = page_size;
+  env.num_pages = num_pages;
+  env.sms = sms;
+  env.has_embed = dims->vocab > 0;
+  Plan p;
+  std::vector<int32_t> v;
+  SAR_TRY(validate_and_plan(env, b, &p, &v));
+  const int32_t l[21] = {p.M, p.Lp, p.Bd, p.R, p.n_items, p.n_parts, p.n_tiles, chunk_tile_rows(env.d, page_size),
+                         (int32_t)p.o_pos, (int32_t)p.o_slot, (int32_t)p.o_pbt, (int32_t)p.o_nkeys,
+                         (int32_t)p.o_btoff, (int32_t)p.o_btlen, (int32_t)p.o_pbeg, (int32_t)p.o_pcnt,
+                         (int32_t)p.o_items, (int32_t)p.o_bt, (int32_t)p.o_rows, (int32_t)p.o_tiles,
+                         (int32_t)p.total};
+  std::memcpy(layout, l, sizeof(l));
+  if (meta_n) *meta_n = (int64_t)v.size();
+  if (meta) {
+    if ((int64_t)v.size() > meta_cap) return set_error(SAR_ERR_INVALID_ARG, "plan_inspect: metadata buffer too small");
+    std::memcpy(meta, v.data(), v.size() * 4);
+  }
+  return SAR_OK;
 }
 
 int sar_op_rmsnorm(const void* x, const void* gain, void* y, int32_t rows, int32_t hidden, float eps, int32_t storage,

@@ -1,0 +1,184 @@
+"""The library's step planner on the host (sar_plan_inspect), no GPU: every
+batch row's position and page slot, the chunk-attention tiles, the decode
+work split (key ranges, partials, sliding-window start), the logits rows, and
+the plan shape a captured step graph relies on."""
+
+import dataclasses
+
+import numpy as np
+import pytest
+
+import chunked_prefill_hybrid_sar_gb300 as sar
+import synth
+
+PS = 16
+
+
+def unpack(r):
+    m = r["meta"]
+
+    def arr(off, n):
+        return m[off:off + n]
+
+    out = dict(r)
+    out["pos"] = arr(r["o_pos"], r["M"])
+    out["slot"] = arr(r["o_slot"], r["M"])
+    bd = r["Bd"]
+    out["nkeys"] = arr(r["o_nkeys"], bd)
+    out["btoff"] = arr(r["o_btoff"], bd)
+    out["btlen"] = arr(r["o_btlen"], bd)
+    out["pbeg"] = arr(r["o_pbeg"], bd)
+    out["pcnt"] = arr(r["o_pcnt"], bd)
+    out["items"] = [tuple(arr(r["o_items"] + 4 * i, 4)) for i in range(r["n_items"])]
+    out["bt"] = arr(r["o_bt"], sum(out["btlen"]))
+    out["rows"] = arr(r["o_rows"], r["R"])
+    out["tiles"] = [tuple(arr(r["o_tiles"] + 8 * i, 8)) for i in range(r["n_tiles"])]
+    out["pbt"] = m[r["o_pbt"]:r["o_nkeys"]]
+    return out
+
+
+def random_batch(rng, n_chunks, n_dec, max_ctx=3000, pages=20000):
+    perm = rng.permutation(pages).tolist()
+    nxt = 0
+
+    def take(n):
+        nonlocal nxt
+        out = perm[nxt:nxt + n]
+        nxt += n
+        return out
+
+    chunks, decs = [], []
+    for i in range(n_chunks):
+        start = int(rng.integers(0, 1500))
+        ln = int(rng.integers(1, 200))
+        chunks.append((i, start, ln, take((start + ln - 1) // PS + 1 + int(rng.integers(0, 3)))))
+    for i in range(n_dec):
+        ctx = int(rng.integers(0, max_ctx))
+        decs.append((100 + i, ctx, take(ctx // PS + 1 + int(rng.integers(0, 2)))))
+    return chunks, decs
+
+
+def plan(dims, chunks, decs, sms=152, max_tokens=1024, max_decodes=128, pages=20000):
+    b = sar.Batch(chunks if chunks else None, decs)
+    return unpack(sar.plan_inspect(dims, b, PS, pages, sms, max_tokens, max_decodes))
+
+
+DIMS = [synth.MISTRAL_LAYER, dataclasses.replace(synth.MISTRAL_LAYER, sliding_window=1000),
+        dataclasses.replace(synth.MISTRAL_LAYER, sliding_window=100), synth.TINY]
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("dims", DIMS, ids=["full", "w1000", "w100", "tiny"])
+def test_plan_invariants_on_random_batches(seed, dims):
+    rng = np.random.default_rng(seed)
+    chunks, decs = random_batch(rng, int(rng.integers(0, 4)), int(rng.integers(0 if seed else 1, 70)))
+    if not chunks and not decs:
+        decs = [(1, 5, [0])]
+    p = plan(dims, chunks, decs)
+    W = dims.sliding_window
+    # rows: chunks in order, then decodes; positions and page slots
+    row = 0
+    for req, start, ln, bt in chunks:
+        for i in range(ln):
+            pos = start + i
+            assert p["pos"][row] == pos and p["slot"][row] == bt[pos // PS] * PS + pos % PS
+            row += 1
+    for req, ctx, bt in decs:
+        assert p["pos"][row] == ctx and p["slot"][row] == bt[ctx // PS] * PS + ctx % PS
+        row += 1
+    assert row == p["M"] == p["Lp"] + p["Bd"]
+    # logits rows: each chunk's last row, then every decode row
+    ends = np.cumsum([c[2] for c in chunks]).tolist()
+    assert p["rows"] == [e - 1 for e in ends] + [p["Lp"] + i for i in range(len(decs))]
+    # chunk tiles: each chunk's rows exactly once, consecutive positions, its own block table
+    covered = {}
+    r0 = 0
+    chunk_of_row = {}
+    for ci, (req, start, ln, bt) in enumerate(chunks):
+        for i in range(ln):
+            chunk_of_row[r0 + i] = (ci, start + i)
+        r0 += ln
+    keys = []
+    for t in p["tiles"]:
+        row0, pos0, rows, off, blen = t[:5]
+        assert 0 < rows <= p["tile_rows"]
+        ci, pfirst = chunk_of_row[row0]
+        req, start, ln, bt = chunks[ci]
+        assert pos0 == pfirst
+        nb = (start + ln - 1) // PS + 1
+        assert blen == nb and p["pbt"][off:off + nb] == bt[:nb]
+        for i in range(rows):
+            assert chunk_of_row[row0 + i] == (ci, pos0 + i)
+            assert row0 + i not in covered
+            covered[row0 + i] = True
+        first = max(0, pos0 - W + 1) if W else 0
+        keys.append(pos0 + rows - first)
+    assert sorted(covered) == list(range(p["Lp"]))
+    assert keys == sorted(keys, reverse=True)  # the most keys first
+    # decode work: each decode's visible keys [first, nk) covered once by 16-aligned ranges
+    by_dec = {}
+    for d, k0, k1, part in p["items"]:
+        by_dec.setdefault(d, []).append((k0, k1, part))
+    lengths = [k1 - k0 for _, k0, k1, _ in p["items"]]
+    assert lengths == sorted(lengths, reverse=True)  # longest first
+    seen_parts = set()
+    for i, (req, ctx, bt) in enumerate(decs):
+        nk = ctx + 1
+        assert p["nkeys"][i] == nk
+        nb = ctx // PS + 1
+        assert p["btlen"][i] == nb and p["bt"][p["btoff"][i]:p["btoff"][i] + nb] == bt[:nb]
+        first = max(0, nk - W) // 16 * 16 if W else 0
+        rs = sorted(by_dec[i])
+        assert len(rs) == p["pcnt"][i]
+        assert rs[0][0] == first and all(k0 % 16 == 0 for k0, _, _ in rs)
+        at = first
+        for k0, k1, part in rs:
+            assert k1 >= k0
+            if k1 > k0:
+                assert k0 == at
+                at = k1
+        assert at == nk
+        if len(rs) == 1:
+            assert rs[0][2] == -1 and p["pbeg"][i] == -1
+        else:
+            parts = sorted(part for _, _, part in rs)
+            assert parts == list(range(p["pbeg"][i], p["pbeg"][i] + len(rs)))
+            seen_parts |= set(parts)
+    assert seen_parts == set(range(p["n_parts"]))
+
+
+def test_tile_rows_follow_the_chunk_kernel():
+    p = plan(synth.MISTRAL_LAYER, [(0, 0, 300, list(range(19)))], [])
+    assert p["tile_rows"] == 128 and p["n_tiles"] == 3
+    p = plan(synth.TINY, [(0, 0, 300, list(range(19)))], [])
+    assert p["tile_rows"] == 64 and p["n_tiles"] == 5
+
+
+def test_plan_shape_is_stable_while_contexts_grow_within_their_pages():
+    """What sar_graph_update needs: the next decode step of the same requests,
+    one token further within the same page counts, has the same plan shape."""
+    rng = np.random.default_rng(3)
+    ctxs = [int(c) for c in rng.integers(100, 4000, 64)]
+    ctxs = [c - (c % 16) for c in ctxs]  # room for one more token in the last page
+    bts = [list(range(1000 * i, 1000 * i + c // PS + 1)) for i, c in enumerate(ctxs)]
+    a = plan(synth.MISTRAL_LAYER, [], [(i, c, bts[i]) for i, c in enumerate(ctxs)], pages=70000)
+    b = plan(synth.MISTRAL_LAYER, [], [(i, c + 1, bts[i]) for i, c in enumerate(ctxs)], pages=70000)
+    keys = [k for k in a if k.startswith("o_") or k in ("M", "Lp", "Bd", "R", "n_items", "n_parts", "n_tiles",
+                                                         "total")]
+    assert all(a[k] == b[k] for k in keys)
+    assert a["items"] != b["items"]  # the ranges themselves follow the contexts
+
+
+def test_plan_rejects_bad_batches():
+    d = synth.MISTRAL_LAYER
+    with pytest.raises(sar.SarError):  # block table too short for the chunk
+        plan(d, [(0, 0, 40, [1, 2])], [])
+    with pytest.raises(sar.SarError) as e:  # page id out of range
+        plan(d, [], [(0, 20, [5, 99999])])
+    assert e.value.code == 5
+    with pytest.raises(sar.SarError):  # more rows than max_tokens
+        plan(d, [(0, 0, 600, list(range(40))), (1, 0, 600, list(range(40, 80)))], [])
+    with pytest.raises(sar.SarError):  # more decodes than max_decodes
+        plan(d, [], [(i, 3, [i]) for i in range(200)], max_decodes=128)
+    with pytest.raises(sar.SarError):  # an empty chunk
+        plan(d, [(0, 0, 8, [0]), (1, 0, 0, [1])], [])
