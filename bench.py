@@ -45,6 +45,27 @@ def dist_env():
     return world, rank, local
 
 
+# Replicas only: every rank runs its own model on its own GPU (the step does
+# not shard), the ranks meet at barriers around the timed region, the slowest
+# rank's time is the job's, and the job's value counts every rank's rows.
+
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest of every rank's x (the job's time is the slowest rank's)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(rows_per_rank: int, world: int, seconds: float) -> float:
+    """Rows of every rank over the job's (slowest rank's) time."""
+    return rows_per_rank * world / seconds
+
+
 def config_block(n):
     return {"workload": WORKLOAD, "layers": 1, "tau": TAU, "lp": TAU - BD, "bd": BD,
             "starts": list(STARTS), "page_size": PAGE, "parallelism": f"replicas x{n}",
@@ -252,12 +273,8 @@ def run_ours(args):
         graphs = None  # the per-kernel pass launches kernel by kernel
     ms = ev0.elapsed_time(ev1)
     m.sync_status()
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = t.item()
-    rows = TAU * args.steps * world
-    value = rows / (ms / 1e3)
+    ms = max_over_ranks(ms, world)
+    value = whole_job_rate(TAU * args.steps, world, ms / 1e3)
 
     # per-kernel times: the same steps again with an event pair around every kernel
     m.profile(True)
@@ -331,11 +348,8 @@ def run_ours(args):
         e2e_step(i)
     barrier()
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = t.item()
-    e2e = {"value": TAU * args.steps * world / e2e_s, "unit": UNIT,
+    e2e_s = max_over_ranks(e2e_s, world)
+    e2e = {"value": whole_job_rate(TAU * args.steps, world, e2e_s), "unit": UNIT,
            "h2d_bytes_per_step": TAU * dims.hidden * 2,
            "d2h_bytes_per_step": (BD + 1) * dims.vocab * 4,
            "api": "sar_graph_launch_host" if graph_set else "sar_step_host"}
