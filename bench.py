@@ -687,6 +687,7 @@ def run_long_prompt(args):
         dims = dataclasses.replace(dims, n_layers=args.layers)
     plen, n_dec = 16384, 128
     m, _ = harness.load_synthetic_model(0, dims, max_tokens=max(chunks) + n_dec, max_decodes=n_dec)
+    m.set_chunk_split(args.chunk_split)
     tokens, ctxs = synth.long_prompt_case(0, dims, prompt_len=plen, n_decode=n_dec, ctx_range=(512, 8192))
     n_pages = plen // PAGE + sum(c // PAGE + 1 for c in ctxs) + 8
     kv = sar.KVCache(m, PAGE, n_pages)
@@ -745,7 +746,8 @@ def run_long_prompt(args):
     out = {"mode": "long-prompt", "workload": f"{name} shape ({dims.n_layers} layers, H {dims.hidden}, "
            f"{dims.n_q_heads}q/{dims.n_kv_heads}kv x {dims.head_dim}, FFN {dims.ffn}, head {dims.vocab}, "
            f"{attn}), f16 storage; one {plen}-token prompt in chunks of C with {n_dec} decodes "
-           f"per step (ctx U[512,8192], random KV)", "sliding_window": dims.sliding_window, "per_chunk": per_c}
+           f"per step (ctx U[512,8192], random KV)", "sliding_window": dims.sliding_window,
+           "chunk_split": bool(args.chunk_split), "per_chunk": per_c}
     print(json.dumps(out))
     return out
 
@@ -775,6 +777,8 @@ def main():
                     help="step mode: chunk attention on a second stream, concurrent with decode attention")
     ap.add_argument("--max-chunks", type=int, default=0,
                     help="trace mode: prefill chunks per batch (0 = Algorithm 3's admission loop, 1 = one chunk)")
+    ap.add_argument("--chunk-split", action="store_true",
+                    help="long-prompt mode: key-range splits of chunk-attention tiles that leave SMs idle")
     ap.add_argument("--window", type=int, default=0,
                     help="long-prompt and trace modes: sliding-window attention of W keys (0 = full causal)")
     args = ap.parse_args()

@@ -140,6 +140,10 @@ class Model:
     def profile(self, on: bool) -> None:
         check(lib().sar_profile_enable(self.h, 1 if on else 0))
 
+    def set_chunk_split(self, on: bool) -> None:
+        """Key-range splits of chunk-attention tiles when they leave SMs idle."""
+        check(lib().sar_model_set_chunk_split(self.h, 1 if on else 0))
+
     def set_overlap(self, on: bool) -> None:
         """Chunk attention on a second stream, concurrent with decode attention."""
         check(lib().sar_model_set_overlap(self.h, 1 if on else 0))
@@ -291,11 +295,12 @@ class Scheduler:
 
 
 _LAYOUT = ("M", "Lp", "Bd", "R", "n_items", "n_parts", "n_tiles", "tile_rows", "o_pos", "o_slot", "o_pbt",
-           "o_nkeys", "o_btoff", "o_btlen", "o_pbeg", "o_pcnt", "o_items", "o_bt", "o_rows", "o_tiles", "total")
+           "o_nkeys", "o_btoff", "o_btlen", "o_pbeg", "o_pcnt", "o_items", "o_bt", "o_rows", "o_tiles", "total",
+           "n_comb", "n_cparts", "o_comb")
 
 
 def plan_inspect(dims, batch: Batch, page_size: int, num_pages: int, sms: int, max_tokens: int,
-                 max_decodes: int, storage: int = SAR_STORAGE_F16) -> dict:
+                 max_decodes: int, storage: int = SAR_STORAGE_F16, chunk_split: bool = False) -> dict:
     """The step planner on the host alone (``sar_plan_inspect``): the plan's
     sizes and array offsets, and the metadata block as a list of int32."""
     d = _lib.sar_dims(dims.n_layers, dims.hidden, dims.n_q_heads, dims.n_kv_heads, dims.head_dim,
@@ -303,10 +308,11 @@ def plan_inspect(dims, batch: Batch, page_size: int, num_pages: int, sms: int, m
                       storage, getattr(dims, "sliding_window", 0))
     lay = (ctypes.c_int32 * len(_LAYOUT))()
     n = ctypes.c_int64()
-    check(lib().sar_plan_inspect(ctypes.byref(d), page_size, num_pages, sms, ctypes.byref(batch.c), lay, None, 0,
-                                 ctypes.byref(n)))
+    cs = 1 if chunk_split else 0
+    check(lib().sar_plan_inspect(ctypes.byref(d), page_size, num_pages, sms, cs, ctypes.byref(batch.c), lay, None,
+                                 0, ctypes.byref(n)))
     meta = (ctypes.c_int32 * max(1, n.value))()
-    check(lib().sar_plan_inspect(ctypes.byref(d), page_size, num_pages, sms, ctypes.byref(batch.c), lay, meta,
+    check(lib().sar_plan_inspect(ctypes.byref(d), page_size, num_pages, sms, cs, ctypes.byref(batch.c), lay, meta,
                                  n.value, ctypes.byref(n)))
     out = dict(zip(_LAYOUT, list(lay)))
     out["meta"] = list(meta)[:n.value]

@@ -91,6 +91,7 @@ SIGNATURES = {
     "sar_sample_greedy": (i32, [vp, vp, i32, vp, vp]),
     "sar_profile_enable": (i32, [vp, i32]),
     "sar_model_set_overlap": (i32, [vp, i32]),
+    "sar_model_set_chunk_split": (i32, [vp, i32]),
     "sar_graph_create": (i32, [vp, vp, ctypes.POINTER(sar_batch), vp, vp, vp, vp, vp, ctypes.POINTER(vp)]),
     "sar_graph_update": (i32, [vp, ctypes.POINTER(sar_batch), vp]),
     "sar_graph_launch": (i32, [vp, vp]),
@@ -105,8 +106,8 @@ SIGNATURES = {
     "sar_sched_destroy": (i32, [vp]),
     "sar_op_gemm": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
     "sar_op_rmsnorm": (i32, [vp, vp, vp, i32, i32, ctypes.c_float, i32, vp]),
-    "sar_plan_inspect": (i32, [ctypes.POINTER(sar_dims), i32, i32, i32, ctypes.POINTER(sar_batch), P_i32, P_i32,
-                               i64, ctypes.POINTER(i64)]),
+    "sar_plan_inspect": (i32, [ctypes.POINTER(sar_dims), i32, i32, i32, i32, ctypes.POINTER(sar_batch), P_i32,
+                               P_i32, i64, ctypes.POINTER(i64)]),
     "sar_model_debug_buffer": (i32, [vp, i32, ctypes.POINTER(vp)]),
     "sar_decode_attention_noalloc": (i32, [vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32,
                                            vp, i32, vp, i32, i32, vp, vp]),

@@ -30,6 +30,10 @@
 // first row's oldest visible key, (first position - W + 1), and masks the
 // keys each row may not see; a row whose window misses a whole block keeps a
 // maximum of -inf there, and its probabilities are then taken as 0.
+// When a step has too few query tiles to fill the SMs, the planner splits a
+// tile's key blocks over several CTAs: each writes its unnormalised O with the
+// row's maximum and sum, and chunk_combine_kernel merges them (the split-K
+// form of the decode attention's long contexts).
 // Every wait is bounded; a timeout records SAR_ERR_TIMEOUT.
 #include <float.h>
 
@@ -140,11 +144,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pos0 = tl.y;   // its position in the prompt
   const int rows = tl.z;
   const int32_t* bt = a.bt + tl.w;
-  const int bt_len = a.tiles[8 * blockIdx.x + 4];
+  const int4 tl2 = reinterpret_cast<const int4*>(a.tiles)[2 * blockIdx.x + 1];
+  const int bt_len = tl2.x;
   const int n_keys = pos0 + rows;  // keys of the last row of this tile, inclusive of it
-  // blocks [j0, j0 + nb): from the one holding the first row's oldest visible key
-  const int j0 = a.window > 0 ? max(0, pos0 - a.window + 1) / kBKV : 0;
-  const int nb = (n_keys + kBKV - 1) / kBKV - j0;
+  // blocks [j0, j0 + nb): planned from the block holding the first row's
+  // oldest visible key to the last row's, or one share of that range
+  const int j0 = tl2.y;
+  const int nb = tl2.z - tl2.y;
+  const int part = tl2.w;
 
   if (warp == 0 || warp == 10) {
     // ---------------- producers: warp 0 K, warp 10 V ----------------
@@ -396,7 +403,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     pair_sync();
     const float lt = l + red[(2 * 2 + (hf ^ 1)) * kBQ + r];
     if (alive) alive = warp_wait_bar(smem_u32(&bars->o_done), (uint32_t)((nb - 1) & 1), a.err, SITE_CHUNK_PIPE);
-    if (alive) {
+    if (alive && part >= 0) {
+      // one share of the tile's keys: O unnormalised, with the row's maximum
+      // (base 2) and sum, for chunk_combine_kernel
+      tc_fence_after();
+      float* pp = a.partials + (((size_t)part * kBQ + r) * a.qh + hq) * (kD + 4);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[16];
+        tmem_ld16(lane_base + kColO + hf * 64 + c * 16, u);
+        tmem_wait_ld();
+        float4* dst = reinterpret_cast<float4*>(pp + hf * 64 + c * 16);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          dst[e] = make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]), __uint_as_float(u[4 * e + 2]),
+                               __uint_as_float(u[4 * e + 3]));
+      }
+      if (hf == 0) *reinterpret_cast<float2*>(pp + kD) = make_float2(m_used, lt);
+    } else if (alive) {
       tc_fence_after();
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       T* out = static_cast<T*>(a.out) + (size_t)(row0 + r) * a.ld_out + (size_t)hq * kD + hf * 64;
@@ -425,6 +449,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Merges the shares of a split tile: out = sum_i O_i 2^(m_i - M) / sum_i l_i 2^(m_i - M)
+// per (row, head, dim); a share with no visible key has m = -inf and weighs 0.
+template <typename T>
+__global__ void chunk_combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ comb, void* out,
+                                     int ld_out, int qh) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int4 c = reinterpret_cast<const int4*>(comb)[blockIdx.x];  // first row, rows, first slot, slots
+  const int r = blockIdx.y, hq = blockIdx.z, d = threadIdx.x;
+  if (r >= c.y) return;
+  auto rec = [&](int i) { return partials + (((size_t)(c.z + i) * kBQ + r) * qh + hq) * (kD + 4); };
+  float M = -INFINITY;
+  for (int i = 0; i < c.w; ++i) M = fmaxf(M, rec(i)[kD]);
+  float L = 0.f, A = 0.f;
+  for (int i = 0; i < c.w; ++i) {
+    const float* p = rec(i);
+    const float sc = (p[kD] == -INFINITY) ? 0.f : exp2f(p[kD] - M);
+    L = fmaf(p[kD + 1], sc, L);
+    A = fmaf(p[d], sc, A);
+  }
+  static_cast<T*>(out)[(size_t)(c.x + r) * ld_out + (size_t)hq * kD + d] = Elem<T>::from(L > 0.f ? A / L : 0.f);
+}
+
 template <typename T>
 int launch_t(const ChunkAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t s) {
   static bool attr = false;
@@ -437,6 +484,12 @@ int launch_t(const ChunkAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& 
   cudaError_t e = launch_pdl(chunk_attn_tc_kernel<T>, grid, dim3(kThreads), (size_t)kSmem, s, tmk, tmv, a);
   if (e != cudaSuccess) return cuda_error(e, "chunk attention (tcgen05) launch");
   count_launches(1);
+  if (a.n_comb > 0) {
+    e = launch_pdl(chunk_combine_kernel<T>, dim3(a.n_comb, kBQ, a.qh), dim3(kD), 0, s, a.partials, a.comb, a.out,
+                   a.ld_out, a.qh);
+    if (e != cudaSuccess) return cuda_error(e, "chunk combine launch");
+    count_launches(1);
+  }
   return SAR_OK;
 }
 
@@ -454,6 +507,8 @@ int launch_chunk_attention_tc(const ChunkAttnArgs& a, const CUtensorMap& tmk, co
   if ((reinterpret_cast<uintptr_t>(a.q32) & 15) || (a.ld32 & 3) || (reinterpret_cast<uintptr_t>(a.out) & 15) ||
       (a.ld_out & 7))
     return set_error(SAR_ERR_INVALID_ARG, "chunk attention (tcgen05): misaligned query or output rows");
+  if (a.n_comb > 0 && (!a.partials || !a.comb || (reinterpret_cast<uintptr_t>(a.partials) & 15)))
+    return set_error(SAR_ERR_INVALID_ARG, "chunk attention (tcgen05): split tiles without a partials buffer");
   return a.storage == SAR_STORAGE_BF16 ? launch_t<__nv_bfloat16>(a, tmk, tmv, s) : launch_t<__half>(a, tmk, tmv, s);
 }
 

@@ -178,10 +178,18 @@ struct ChunkAttnArgs {
   const int32_t* bt;         // the chunks' block tables, concatenated
   // [n_tiles][8] query tiles, one CTA each, in launch order: first batch row,
   // first position, rows (<= the kernel's tile rows), block-table offset into
-  // bt, block-table length, 3 unused; a tile's rows are consecutive positions
-  // of one prompt, whose keys [0, last position] sit in its block table
+  // bt, block-table length, first and end 128-key block, partial slot (-1: the
+  // tile's whole key range, written to out); a tile's rows are consecutive
+  // positions of one prompt, whose keys [0, last position] sit in its block
+  // table.  The warp-MMA kernel reads the first five only.
   const int32_t* tiles;
   int n_tiles;
+  // key-range splits (tcgen05 kernel): unnormalised partials
+  // [slot][128 rows][qh][head_dim + 4] (O, then the row's maximum and sum),
+  // and [n_comb][4] merges {first batch row, rows, first slot, slots}
+  float* partials = nullptr;
+  const int32_t* comb = nullptr;
+  int n_comb = 0;
   int ld, ld_out, qh, kvh, d, page_size, num_pages, storage;
   int* err;
   int window = 0;            // the row at position p sees keys (p - window, p]; 0 = all of [0, p]

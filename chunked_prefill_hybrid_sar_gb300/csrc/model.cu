@@ -84,6 +84,8 @@ struct sar_model {
   size_t meta_dev_cap = 0;
   // two-stream attention split
   bool overlap = false;
+  // key-range splits of chunk-attention tiles (changes the summation order)
+  bool chunk_split = false;
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   cudaStream_t capture = nullptr;  // steps are captured into graphs here (never the legacy stream)
@@ -162,8 +164,8 @@ struct Plan {
   int M = 0, Lp = 0, Bd = 0, R = 0;
   // offsets into the metadata block (int32 elements)
   size_t o_pos = 0, o_slot = 0, o_pbt = 0, o_nkeys = 0, o_btoff = 0, o_btlen = 0, o_pbeg = 0, o_pcnt = 0,
-         o_items = 0, o_bt = 0, o_rows = 0, o_tiles = 0, total = 0;
-  int n_items = 0, n_parts = 0, n_tiles = 0;
+         o_items = 0, o_bt = 0, o_rows = 0, o_tiles = 0, o_comb = 0, total = 0;
+  int n_items = 0, n_parts = 0, n_tiles = 0, n_comb = 0, n_cparts = 0;
 };
 
 // The batch's prefill chunks in row order: `prefill` (if has_prefill), then more_prefill[].
@@ -179,6 +181,7 @@ struct PlanEnv {
   sar_dims d;
   int page_size = 0, num_pages = 0, sms = 0;
   bool has_embed = false;
+  bool chunk_split = false;
 };
 
 PlanEnv plan_env(const sar_model* m, const sar_kv* kv) {
@@ -188,6 +191,7 @@ PlanEnv plan_env(const sar_model* m, const sar_kv* kv) {
   e.num_pages = kv->num_pages;
   e.sms = sar::num_sms();
   e.has_embed = m->embed != nullptr;
+  e.chunk_split = m->chunk_split;
   return e;
 }
 
@@ -306,11 +310,17 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
   for (int i = 0; i < Bd; ++i) rows.push_back(Lp + i);
   // chunk block tables (each cut to the pages its positions use) and the
   // chunk-attention tiles: {first batch row, first position, rows, block-table
-  // offset, block-table length}, the most keys first (the longest CTAs start first)
+  // offset, block-table length, first and end 128-key block, partial slot},
+  // the most keys first (the longest CTAs start first)
   const int tile_rows = chunk_tile_rows(d, ps);
-  std::vector<int32_t> pbt, tiles;
+  std::vector<int32_t> pbt, tiles, comb;
+  int n_cparts = 0;
   {
-    std::vector<std::array<int32_t, 8>> tl;
+    struct Tile {
+      std::array<int32_t, 8> e;
+      int keys;
+    };
+    std::vector<Tile> tl;
     int r0 = 0;
     for (const sar_prefill& c : chunks) {
       const int off = (int)pbt.size();
@@ -318,19 +328,47 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
       pbt.insert(pbt.end(), c.block_table, c.block_table + nb);
       for (int q0 = 0; q0 < c.len; q0 += tile_rows) {
         const int rws = std::min(tile_rows, c.len - q0);
-        const int first = d.sliding_window > 0 ? std::max(0, c.start_pos + q0 - d.sliding_window + 1) : 0;
-        const int keys = c.start_pos + q0 + rws - first;
-        tl.push_back({r0 + q0, c.start_pos + q0, rws, off, nb, keys, 0, 0});
+        const int pos0 = c.start_pos + q0;
+        const int first = d.sliding_window > 0 ? std::max(0, pos0 - d.sliding_window + 1) : 0;
+        const int kb0 = first / sar::kChunkTileRowsTc, kb1 = (pos0 + rws + sar::kChunkTileRowsTc - 1) / sar::kChunkTileRowsTc;
+        tl.push_back({{r0 + q0, pos0, rws, off, nb, kb0, kb1, -1}, pos0 + rws - first});
       }
       r0 += c.len;
     }
-    std::stable_sort(tl.begin(), tl.end(), [](const std::array<int32_t, 8>& x, const std::array<int32_t, 8>& y) {
-      return x[5] > y[5];
-    });
-    for (auto& t : tl) {
-      t[5] = 0;
-      tiles.insert(tiles.end(), t.begin(), t.end());
+    // Key-range splits (tcgen05 kernel, one CTA per SM): when the tiles x
+    // heads fill at most half the SMs, each tile's key blocks are shared out
+    // over s = min(4, SMs / CTAs) CTAs (at least two blocks each) so that the
+    // shares still run in one wave; a merge kernel combines them.  Past one
+    // wave the shares' extra partial traffic and the merge cost more than the
+    // shorter tail saves (Yi-34B, 112 CTAs in four shares: chunk attention
+    // 13% slower; Mistral-7B, 64 CTAs in two: 33% faster).
+    int s = 1;
+    if (env.chunk_split && tile_rows == sar::kChunkTileRowsTc && !tl.empty()) {
+      const long ctas = (long)tl.size() * d.n_q_heads, slots = std::max(1, sms);
+      s = (int)std::min<long>(4, slots / ctas);
+      if (s < 2) s = 1;
     }
+    std::vector<Tile> ent;
+    for (const Tile& t : tl) {
+      const int nbk = t.e[6] - t.e[5];
+      const int ss = std::min(s, nbk / 2);
+      if (ss <= 1) {
+        ent.push_back(t);
+        continue;
+      }
+      comb.insert(comb.end(), {t.e[0], t.e[2], n_cparts, ss});
+      for (int i = 0; i < ss; ++i) {
+        Tile x = t;
+        x.e[5] = t.e[5] + (int)((long)nbk * i / ss);
+        x.e[6] = t.e[5] + (int)((long)nbk * (i + 1) / ss);
+        x.e[7] = n_cparts + i;
+        x.keys = (x.e[6] - x.e[5]) * sar::kChunkTileRowsTc;
+        ent.push_back(x);
+      }
+      n_cparts += ss;
+    }
+    std::stable_sort(ent.begin(), ent.end(), [](const Tile& x, const Tile& y) { return x.keys > y.keys; });
+    for (const Tile& t : ent) tiles.insert(tiles.end(), t.e.begin(), t.e.end());
   }
 
   p->M = M;
@@ -340,6 +378,8 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
   p->n_items = (int)items.size() / 4;
   p->n_parts = n_parts;
   p->n_tiles = (int)tiles.size() / 8;
+  p->n_comb = (int)comb.size() / 4;
+  p->n_cparts = n_cparts;
   size_t o = 0;
   auto take = [&](size_t n) { size_t r = o; o += (n + 3) & ~size_t(3); return r; };  // 16-byte aligned pieces
   p->o_pos = take(M);
@@ -354,6 +394,7 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
   p->o_bt = take(bt.size());
   p->o_rows = take(rows.size());
   p->o_tiles = take(tiles.size());
+  p->o_comb = take(comb.size());
   p->total = o;
   meta->assign(o, 0);
   int32_t* mt = meta->data();
@@ -381,6 +422,7 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
   std::memcpy(mt + p->o_bt, bt.data(), bt.size() * 4);
   std::memcpy(mt + p->o_rows, rows.data(), rows.size() * 4);
   if (!tiles.empty()) std::memcpy(mt + p->o_tiles, tiles.data(), tiles.size() * 4);
+  if (!comb.empty()) std::memcpy(mt + p->o_comb, comb.data(), comb.size() * 4);
   return SAR_OK;
 }
 
@@ -409,6 +451,16 @@ int ensure_meta(sar_model* m, size_t n) {
     m->meta_dev_cap = cap;
   }
   return SAR_OK;
+}
+
+// One partials buffer per step: the decode split partials [parts][qh][d + 2],
+// then (256-byte aligned) the chunk key-range partials [slots][128][qh][d + 4].
+size_t decode_partials_floats(const Plan& p, const sar_dims& d) {
+  return ((size_t)p.n_parts * d.n_q_heads * (d.head_dim + 2) + 63) & ~(size_t)63;
+}
+size_t partials_floats(const Plan& p, const sar_dims& d) {
+  return std::max<size_t>(64, decode_partials_floats(p, d) +
+                                  (size_t)p.n_cparts * sar::kChunkTileRowsTc * d.n_q_heads * (d.head_dim + 4));
 }
 
 int ensure_partials(sar_model* m, size_t floats) {
@@ -523,6 +575,9 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
       ca.storage = d.storage;
       ca.err = m->err;
       ca.window = d.sliding_window;
+      ca.partials = partials + decode_partials_floats(p, d);
+      ca.comb = md + p.o_comb;
+      ca.n_comb = p.n_comb;
       if (sar::chunk_attention_tc_supported(ca))
         SAR_TRY(sar::launch_chunk_attention_tc(ca, kv->tmk[l], kv->tmv[l], sc));
       else
@@ -611,7 +666,7 @@ int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float
   std::vector<int32_t> meta;
   SAR_TRY(plan_step(m, kv, b, logits != nullptr, &p, &meta));
   SAR_TRY(ensure_meta(m, p.total));
-  SAR_TRY(ensure_partials(m, (size_t)std::max(p.n_parts, 1) * m->d.n_q_heads * (m->d.head_dim + 2)));
+  SAR_TRY(ensure_partials(m, partials_floats(p, m->d)));
   const int slot = m->meta_slot;
   m->meta_slot = (slot + 1) % kMetaRing;
   SAR_TRY(check(cudaEventSynchronize(m->meta_ev[slot]), "meta ring wait"));
@@ -891,6 +946,12 @@ int sar_sample_greedy(sar_model* m, const float* logits, int32_t rows, int32_t* 
   return sar::launch_argmax(logits, rows, m->d.vocab, tokens_out, static_cast<cudaStream_t>(stream));
 }
 
+int sar_model_set_chunk_split(sar_model* m, int32_t on) {
+  if (!m) return set_error(SAR_ERR_INVALID_ARG, "chunk_split: null model");
+  m->chunk_split = on != 0;
+  return SAR_OK;
+}
+
 int sar_model_set_overlap(sar_model* m, int32_t on) {
   if (!m) return set_error(SAR_ERR_INVALID_ARG, "overlap: null model");
   if (on && !m->side) {
@@ -967,8 +1028,8 @@ int sar_op_gemm(const void* a, const void* w, void* c, const void* residual, int
   return sar::gemm_launch(cfg, amap, wmap, M, N, K, epilogue, storage, c, residual, err, static_cast<cudaStream_t>(stream));
 }
 
-int sar_plan_inspect(const sar_dims* dims, int32_t page_size, int32_t num_pages, int32_t sms, const sar_batch* b,
-                     int32_t* layout, int32_t* meta, int64_t meta_cap, int64_t* meta_n) {
+int sar_plan_inspect(const sar_dims* dims, int32_t page_size, int32_t num_pages, int32_t sms, int32_t chunk_split,
+                     const sar_batch* b, int32_t* layout, int32_t* meta, int64_t meta_cap, int64_t* meta_n) {
   if (!dims || !b || !layout || sms <= 0 || page_size <= 0 || num_pages <= 0)
     return set_error(SAR_ERR_INVALID_ARG, "plan_inspect: bad argument");
   PlanEnv env;
@@ -977,14 +1038,15 @@ int sar_plan_inspect(const sar_dims* dims, int32_t page_size, int32_t num_pages,
   env.num_pages = num_pages;
   env.sms = sms;
   env.has_embed = dims->vocab > 0;
+  env.chunk_split = chunk_split != 0;
   Plan p;
   std::vector<int32_t> v;
   SAR_TRY(validate_and_plan(env, b, &p, &v));
-  const int32_t l[21] = {p.M, p.Lp, p.Bd, p.R, p.n_items, p.n_parts, p.n_tiles, chunk_tile_rows(env.d, page_size),
+  const int32_t l[24] = {p.M, p.Lp, p.Bd, p.R, p.n_items, p.n_parts, p.n_tiles, chunk_tile_rows(env.d, page_size),
                          (int32_t)p.o_pos, (int32_t)p.o_slot, (int32_t)p.o_pbt, (int32_t)p.o_nkeys,
                          (int32_t)p.o_btoff, (int32_t)p.o_btlen, (int32_t)p.o_pbeg, (int32_t)p.o_pcnt,
                          (int32_t)p.o_items, (int32_t)p.o_bt, (int32_t)p.o_rows, (int32_t)p.o_tiles,
-                         (int32_t)p.total};
+                         (int32_t)p.total, p.n_comb, p.n_cparts, (int32_t)p.o_comb};
   std::memcpy(layout, l, sizeof(l));
   if (meta_n) *meta_n = (int64_t)v.size();
   if (meta) {
@@ -1032,7 +1094,8 @@ bool same_shape(const Plan& a, const Plan& b) {
          a.n_parts == b.n_parts && a.n_tiles == b.n_tiles && a.total == b.total && a.o_pos == b.o_pos &&
          a.o_slot == b.o_slot && a.o_pbt == b.o_pbt && a.o_nkeys == b.o_nkeys && a.o_btoff == b.o_btoff &&
          a.o_btlen == b.o_btlen && a.o_pbeg == b.o_pbeg && a.o_pcnt == b.o_pcnt && a.o_items == b.o_items &&
-         a.o_bt == b.o_bt && a.o_rows == b.o_rows && a.o_tiles == b.o_tiles;
+         a.o_bt == b.o_bt && a.o_rows == b.o_rows && a.o_tiles == b.o_tiles && a.n_comb == b.n_comb &&
+         a.n_cparts == b.n_cparts && a.o_comb == b.o_comb;
 }
 
 }  // namespace
@@ -1069,7 +1132,7 @@ int sar_graph_create(sar_model* m, sar_kv* kv, const sar_batch* b, const void* i
   std::vector<int32_t> meta;
   int rc = plan_step(m, kv, b, logits_out != nullptr, &g->p, &meta);
   // everything the captured launches point at is allocated and filled before the capture
-  const size_t parts = (size_t)std::max(g->p.n_parts, 1) * m->d.n_q_heads * (m->d.head_dim + 2);
+  const size_t parts = partials_floats(g->p, m->d);
   if (rc == SAR_OK) rc = check(cudaMalloc(&g->md, g->p.total * 4), "graph: metadata");
   if (rc == SAR_OK) rc = check(cudaMallocHost(&g->md_host, g->p.total * 4), "graph: metadata staging");
   if (rc == SAR_OK) rc = check(cudaMalloc(&g->partials, parts * 4), "graph: partials");

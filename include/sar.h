@@ -318,6 +318,15 @@ int sar_profile_enable(sar_model* m, int32_t on);
  * profiling.  Creates the stream and events on first use. */
 int sar_model_set_overlap(sar_model* m, int32_t on);
 
+/* When on, a step whose chunk-attention query tiles x heads would leave SMs
+ * idle (a short chunk deep into a long prompt) shares each tile's keys out over
+ * up to four CTAs and merges their partial results (the split form decode
+ * attention uses for long contexts).  Off by default: the merged sums are
+ * rounded in another order than an unsplit tile's, so a chunked prefill and a
+ * one-shot prefill of the same prompt no longer agree as closely (over the
+ * 60-layer Yi-34B shape: relative L2 6e-3 instead of below 1e-3). */
+int sar_model_set_chunk_split(sar_model* m, int32_t on);
+
 /* Synchronises, then returns per kind the accumulated milliseconds and the
  * number of timed launches since the last reset, and resets them. */
 int sar_profile_read(sar_model* m, double* ms, int64_t* launches, int32_t n_kinds);

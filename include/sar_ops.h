@@ -98,9 +98,10 @@ int sar_op_rmsnorm(const void* x, const void* gain, void* y, int32_t rows, int32
 int sar_model_debug_buffer(sar_model* m, int32_t which, void** out);
 
 /* The step planner on the host alone (no GPU, no model): plans batch `b` as
- * sar_step would for a model of `dims`, a cache of num_pages pages of
- * page_size tokens and a device of `sms` SMs (sar_step plans for the current
- * device's), with the same validation and errors.  layout (int32[21])
+ * sar_step would for a model of `dims` (with chunk_split as set by
+ * sar_model_set_chunk_split), a cache of num_pages pages of page_size tokens
+ * and a device of `sms` SMs (sar_step plans for the current device's), with
+ * the same validation and errors.  layout (int32[24])
  * receives M, Lp, Bd, R, decode work items, decode partials, chunk tiles,
  * rows per chunk tile, then the offsets (int32 elements) of the metadata
  * block's arrays -- row positions, row page slots, chunk block tables,
@@ -108,11 +109,14 @@ int sar_model_debug_buffer(sar_model* m, int32_t which, void** out);
  * first partial, partial count, work items [4 each: decode, first key, end
  * key, partial or -1], decode block tables, logits rows, chunk tiles [8 each:
  * first batch row, first position, rows, block-table offset, block-table
- * length, 0, 0, 0] -- and its total length.  The block itself (what the step
- * ships to the device) is copied to meta (int32[meta_cap], may be NULL) and
- * its length to *meta_n. */
+ * length, first and end 128-key block, key-range partial slot or -1] -- its
+ * total length, then the chunk key-range merges, their partial slots and the
+ * merges' offset [4 each: first batch row, rows, first slot, slots].  The
+ * block itself (what the step ships to the device) is copied to meta
+ * (int32[meta_cap], may be NULL) and its length to *meta_n. */
 int sar_plan_inspect(const sar_dims* dims, int32_t page_size, int32_t num_pages, int32_t sms,
-                     const sar_batch* b, int32_t* layout, int32_t* meta, int64_t meta_cap, int64_t* meta_n);
+                     int32_t chunk_split, const sar_batch* b, int32_t* layout, int32_t* meta, int64_t meta_cap,
+                     int64_t* meta_n);
 
 #ifdef __cplusplus
 }

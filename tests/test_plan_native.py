@@ -33,6 +33,7 @@ def unpack(r):
     out["bt"] = arr(r["o_bt"], sum(out["btlen"]))
     out["rows"] = arr(r["o_rows"], r["R"])
     out["tiles"] = [tuple(arr(r["o_tiles"] + 8 * i, 8)) for i in range(r["n_tiles"])]
+    out["comb"] = [tuple(arr(r["o_comb"] + 4 * i, 4)) for i in range(r["n_comb"])]
     out["pbt"] = m[r["o_pbt"]:r["o_nkeys"]]
     return out
 
@@ -58,9 +59,9 @@ def random_batch(rng, n_chunks, n_dec, max_ctx=3000, pages=20000):
     return chunks, decs
 
 
-def plan(dims, chunks, decs, sms=152, max_tokens=1024, max_decodes=128, pages=20000):
+def plan(dims, chunks, decs, sms=152, max_tokens=1024, max_decodes=128, pages=20000, chunk_split=True):
     b = sar.Batch(chunks if chunks else None, decs)
-    return unpack(sar.plan_inspect(dims, b, PS, pages, sms, max_tokens, max_decodes))
+    return unpack(sar.plan_inspect(dims, b, PS, pages, sms, max_tokens, max_decodes, chunk_split=chunk_split))
 
 
 DIMS = [synth.MISTRAL_LAYER, dataclasses.replace(synth.MISTRAL_LAYER, sliding_window=1000),
@@ -99,22 +100,48 @@ def test_plan_invariants_on_random_batches(seed, dims):
             chunk_of_row[r0 + i] = (ci, start + i)
         r0 += ln
     keys = []
+    shares = {}
     for t in p["tiles"]:
-        row0, pos0, rows, off, blen = t[:5]
+        row0, pos0, rows, off, blen, kb0, kb1, part = t
         assert 0 < rows <= p["tile_rows"]
         ci, pfirst = chunk_of_row[row0]
         req, start, ln, bt = chunks[ci]
         assert pos0 == pfirst
         nb = (start + ln - 1) // PS + 1
         assert blen == nb and p["pbt"][off:off + nb] == bt[:nb]
+        first = max(0, pos0 - W + 1) if W else 0
+        assert kb0 < kb1
+        if part < 0:  # the tile's whole key range, 128-key blocks
+            assert (kb0, kb1) == (first // 128, -(-(pos0 + rows) // 128))
+            for i in range(rows):
+                assert chunk_of_row[row0 + i] == (ci, pos0 + i)
+                assert row0 + i not in covered
+                covered[row0 + i] = True
+            keys.append(pos0 + rows - first)
+        else:
+            shares[part] = t
+            keys.append((kb1 - kb0) * 128)
+    assert keys == sorted(keys, reverse=True)  # the most keys first
+    # split tiles: each merge's shares partition the tile's key blocks
+    seen = set()
+    for row0, rows, p0, cnt in p["comb"]:
+        assert cnt >= 2
+        grp = [shares[q] for q in range(p0, p0 + cnt)]
+        seen |= set(range(p0, p0 + cnt))
+        assert all(g[0] == row0 and g[2] == rows for g in grp)
+        pos0 = grp[0][1]
+        first = max(0, pos0 - W + 1) if W else 0
+        lo, hi = first // 128, -(-(pos0 + rows) // 128)
+        rng_ = sorted((g[5], g[6]) for g in grp)
+        assert rng_[0][0] == lo and rng_[-1][1] == hi
+        assert all(a[1] == b[0] for a, b in zip(rng_, rng_[1:])) and all(b - a >= 2 for a, b in rng_)
+        ci, _ = chunk_of_row[row0]
         for i in range(rows):
             assert chunk_of_row[row0 + i] == (ci, pos0 + i)
             assert row0 + i not in covered
             covered[row0 + i] = True
-        first = max(0, pos0 - W + 1) if W else 0
-        keys.append(pos0 + rows - first)
+    assert seen == set(shares) == set(range(p["n_cparts"]))
     assert sorted(covered) == list(range(p["Lp"]))
-    assert keys == sorted(keys, reverse=True)  # the most keys first
     # decode work: each decode's visible keys [first, nk) covered once by 16-aligned ranges
     by_dec = {}
     for d, k0, k1, part in p["items"]:
@@ -145,6 +172,28 @@ def test_plan_invariants_on_random_batches(seed, dims):
             assert parts == list(range(p["pbeg"][i], p["pbeg"][i] + len(rs)))
             seen_parts |= set(parts)
     assert seen_parts == set(range(p["n_parts"]))
+
+
+def test_key_ranges_split_only_when_tiles_leave_sms_idle():
+    # the tau = 512 step: 4 tiles x 32 heads = 128 CTAs -- splitting would not shorten it
+    p = plan(synth.MISTRAL_LAYER, [(0, 1536, 448, list(range(125)))], [])
+    assert p["n_comb"] == 0 and p["n_tiles"] == 4
+    # a 256-row chunk deep into a long prompt: 2 tiles x 32 heads = 64 CTAs -> two shares each
+    p = plan(synth.MISTRAL_LAYER, [(0, 8192, 256, list(range(528)))], [])
+    assert p["n_comb"] == 2 and p["n_tiles"] == 4 and p["n_cparts"] == 4
+    # a 128-row chunk: 1 tile x 32 heads = 32 CTAs -> four shares
+    p = plan(synth.MISTRAL_LAYER, [(0, 8192, 128, list(range(520)))], [])
+    assert p["n_comb"] == 1 and p["n_tiles"] == 4 and p["n_cparts"] == 4
+    # the Yi-34B shape (56 heads): 2 tiles -> 112 CTAs, more than half the SMs: not split
+    yi = dataclasses.replace(synth.YI_34B, n_layers=1)
+    p = plan(yi, [(0, 8192, 256, list(range(528)))], [])
+    assert p["n_comb"] == 0 and p["n_tiles"] == 2
+    # a tile with fewer than four key blocks is not split
+    p = plan(synth.MISTRAL_LAYER, [(0, 0, 200, list(range(13)))], [])
+    assert p["n_comb"] == 0
+    # and nothing is split unless the model asks for it
+    p = plan(synth.MISTRAL_LAYER, [(0, 8192, 256, list(range(528)))], [], chunk_split=False)
+    assert p["n_comb"] == 0 and p["n_tiles"] == 2
 
 
 def test_tile_rows_follow_the_chunk_kernel():
