@@ -327,32 +327,49 @@ def run_ours(args):
               + 4 * op_t(0, TAU * wb * 2))
 
     # end to end: host buffers through the host entry points, one step at a
-    # time (each step's input rows in from pinned memory, its result -- the
-    # logits of every sampled row -- back, then the next step): the captured
-    # graph of each case (sar_graph_launch_host), or with --no-graph the
-    # planning entry point (sar_step_host)
+    # time (each step's input rows in from pinned memory, its result back,
+    # then the next step).  With the captured graph of each case the result is
+    # every sampled row's greedy token id, picked on the device
+    # (sar_graph_launch_host_tokens: the serving loop's round trip); the same
+    # loop reading back the whole logits rows instead (sar_graph_launch_host)
+    # is reported beside it.  With --no-graph: the planning entry point
+    # (sar_step_host), logits back.
     pin_in = [x.cpu().pin_memory() for _, x in cases]
     h_log = torch.empty(BD + 1, dims.vocab, dtype=torch.float32).pin_memory()
+    h_tok = torch.empty(BD + 1, dtype=torch.int32).pin_memory()
 
-    def e2e_step(i):
+    def e2e_run(step_fn):
+        for i in range(3):
+            step_fn(i)
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            step_fn(i)
+        barrier()
+        return max_over_ranks(time.perf_counter() - t0, world)
+
+    def logits_step(i):
         if graph_set:
             graph_set[i % 3].launch_host(pin_in[i % 3], logits_out=h_log)
         else:
             m.step_host(kv, cases[i % 3][0], pin_in[i % 3], logits_out=h_log)
 
-    for i in range(3):
-        e2e_step(i)
-    barrier()
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        e2e_step(i)
-    barrier()
-    e2e_s = time.perf_counter() - t0
-    e2e_s = max_over_ranks(e2e_s, world)
-    e2e = {"value": whole_job_rate(TAU * args.steps, world, e2e_s), "unit": UNIT,
-           "h2d_bytes_per_step": TAU * dims.hidden * 2,
-           "d2h_bytes_per_step": (BD + 1) * dims.vocab * 4,
-           "api": "sar_graph_launch_host" if graph_set else "sar_step_host"}
+    def tokens_step(i):
+        graph_set[i % 3].launch_host_tokens(pin_in[i % 3], h_tok)
+
+    e2e_log_s = e2e_run(logits_step)
+    e2e_logits = {"value": whole_job_rate(TAU * args.steps, world, e2e_log_s), "unit": UNIT,
+                  "h2d_bytes_per_step": TAU * dims.hidden * 2,
+                  "d2h_bytes_per_step": (BD + 1) * dims.vocab * 4,
+                  "api": "sar_graph_launch_host" if graph_set else "sar_step_host"}
+    if graph_set:
+        e2e_s = e2e_run(tokens_step)
+        e2e = {"value": whole_job_rate(TAU * args.steps, world, e2e_s), "unit": UNIT,
+               "h2d_bytes_per_step": TAU * dims.hidden * 2,
+               "d2h_bytes_per_step": (BD + 1) * 4,
+               "api": "sar_graph_launch_host_tokens (greedy token ids of the 65 sampled rows back)"}
+    else:
+        e2e = e2e_logits
 
     out = None
     if rank == 0:
@@ -364,7 +381,7 @@ def run_ours(args):
                "data": "synthetic (seeded random-init weights and KV histories)",
                "config": dict(config_block(world), attn_streams=2 if args.overlap else 1,
                               launch="cuda graph per case" if args.graph else "kernel by kernel"),
-               "e2e": e2e, "gpu_launches": launches,
+               "e2e": e2e, "e2e_logits_readback": e2e_logits, "gpu_launches": launches,
                "roofline": roof, "step_roofline_ms": t_roof * 1e3,
                "step_roofline_frac": (t_roof * 1e3) / (ms / args.steps),
                "kernels": kernels, "clocks": clk.summary(), "wall_s": wall, "cpu_baseline": cpu}

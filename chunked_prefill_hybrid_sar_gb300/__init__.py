@@ -196,6 +196,12 @@ class StepGraph:
         """Host input in, the captured step, host logits / hidden rows out (synchronous)."""
         check(lib().sar_graph_launch_host(self.h, _ptr(inp), _ptr(logits_out), _ptr(hidden_out), _stream(stream)))
 
+    def launch_host_tokens(self, inp, tokens_out, stream=None) -> None:
+        """Host input in, the captured step, each logits row's greedy pick out
+        (host int32 [R], synchronous)."""
+        check(lib().sar_graph_launch_host_tokens(self.h, _ptr(inp), ctypes.cast(_ptr(tokens_out), _lib.P_i32),
+                                                 _stream(stream)))
+
     def close(self) -> None:
         if self.h:
             check(lib().sar_graph_destroy(self.h))

@@ -92,6 +92,7 @@ SIGNATURES = {
     "sar_profile_enable": (i32, [vp, i32]),
     "sar_model_set_overlap": (i32, [vp, i32]),
     "sar_model_set_chunk_split": (i32, [vp, i32]),
+    "sar_graph_launch_host_tokens": (i32, [vp, vp, P_i32, vp]),
     "sar_graph_create": (i32, [vp, vp, ctypes.POINTER(sar_batch), vp, vp, vp, vp, vp, ctypes.POINTER(vp)]),
     "sar_graph_update": (i32, [vp, ctypes.POINTER(sar_batch), vp]),
     "sar_graph_launch": (i32, [vp, vp]),

@@ -1080,6 +1080,7 @@ struct sar_graph {
   int32_t* md = nullptr;       // the graph's own device copy of the step metadata
   int32_t* md_host = nullptr;  // pinned staging for sar_graph_update
   float* partials = nullptr;   // the graph's own decode split partials
+  int32_t* tokens = nullptr;   // greedy picks of the captured logits rows
   cudaEvent_t staged = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
@@ -1111,6 +1112,7 @@ int sar_graph_destroy(sar_graph* g) {
   if (g->md_host) cudaFreeHost(g->md_host);
   cudaFree(g->md);
   cudaFree(g->partials);
+  cudaFree(g->tokens);
   delete g;
   return SAR_OK;
 }
@@ -1136,6 +1138,8 @@ int sar_graph_create(sar_model* m, sar_kv* kv, const sar_batch* b, const void* i
   if (rc == SAR_OK) rc = check(cudaMalloc(&g->md, g->p.total * 4), "graph: metadata");
   if (rc == SAR_OK) rc = check(cudaMallocHost(&g->md_host, g->p.total * 4), "graph: metadata staging");
   if (rc == SAR_OK) rc = check(cudaMalloc(&g->partials, parts * 4), "graph: partials");
+  if (rc == SAR_OK && logits_out)
+    rc = check(cudaMalloc(&g->tokens, std::max<size_t>(16, (size_t)g->p.R * 4)), "graph: token ids");
   if (rc == SAR_OK) rc = check(cudaEventCreateWithFlags(&g->staged, cudaEventDisableTiming), "graph: event");
   if (rc == SAR_OK) {
     std::memcpy(g->md_host, meta.data(), g->p.total * 4);
@@ -1212,6 +1216,19 @@ int sar_graph_launch_host(sar_graph* g, const void* in, float* logits_out, float
   SAR_TRY(check(cudaGraphLaunch(g->exec, s), "graph: launch"));
   if (logits_out) SAR_TRY(host_copy(logits_out, g->logits, (size_t)g->p.R * g->m->d.vocab * 4, s));
   if (hidden_out) SAR_TRY(host_copy(hidden_out, g->hidden, M * H * 4, s));
+  return check(cudaStreamSynchronize(s), "graph: synchronise");
+}
+
+int sar_graph_launch_host_tokens(sar_graph* g, const void* in, int32_t* tokens_out, void* stream) {
+  if (!g || !in || !tokens_out) return set_error(SAR_ERR_INVALID_ARG, "graph: null argument");
+  if (!g->logits) return set_error(SAR_ERR_INVALID_ARG, "graph: logits not captured");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t M = (size_t)g->p.M, H = (size_t)g->m->d.hidden;
+  const size_t in_bytes = g->in_kind == SAR_IN_TOKENS ? M * 4 : M * H * 2;
+  SAR_TRY(host_copy(g->in, in, in_bytes, s));
+  SAR_TRY(check(cudaGraphLaunch(g->exec, s), "graph: launch"));
+  SAR_TRY(sar::launch_argmax(g->logits, g->p.R, g->m->d.vocab, g->tokens, s));
+  SAR_TRY(host_copy(tokens_out, g->tokens, (size_t)g->p.R * 4, s));
   return check(cudaStreamSynchronize(s), "graph: synchronise");
 }
 

@@ -243,6 +243,15 @@ int sar_graph_launch(sar_graph* g, void* stream);
  * Pinned host memory makes the copies asynchronous to the host. */
 int sar_graph_launch_host(sar_graph* g, const void* in, float* logits_out, float* hidden_out, void* stream);
 
+/* The captured step with HOST buffers, sampled greedily on the device: copies
+ * `in` as sar_graph_launch_host does, runs the graph, picks each captured
+ * logits row's argmax (as sar_sample_greedy: lowest index on ties) into the
+ * graph's own device array and copies the R token ids to `tokens_out` (host
+ * int32 [R], the rows of sar_batch's logits order); returns once they are in
+ * host memory.  The logits must have been captured.  This is a serving step's
+ * round trip: the host needs the next tokens, not the logits. */
+int sar_graph_launch_host_tokens(sar_graph* g, const void* in, int32_t* tokens_out, void* stream);
+
 int sar_graph_destroy(sar_graph* g);
 
 /* Greedy sampling: tokens_out[r] = argmax_v logits[r, v] (lowest index on

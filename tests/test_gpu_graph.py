@@ -176,6 +176,14 @@ def test_graph_launch_host_copies_in_and_out(mistral):
     assert torch.equal(x_dev.cpu(), x_host)
     ref_l, ref_h = logits.cpu(), hid.cpu()
     assert torch.equal(h_log, ref_l) and torch.equal(h_hid, ref_h)
+    # greedy token ids instead of logits: each captured row's argmax, lowest index on ties
+    toks = torch.full((65,), -1, dtype=torch.int32).pin_memory()
+    g.launch_host_tokens(x_host, toks)
+    assert torch.equal(toks, logits.cpu().argmax(dim=1).to(torch.int32))
+    nolog = sar.StepGraph(m, kv, b, x_dev, hidden_out=hid)
+    with pytest.raises(sar.SarError):  # no logits captured
+        nolog.launch_host_tokens(x_host, toks)
+    nolog.close()
     # pageable host buffers take the copy engine instead of the copy kernel
     p_log = torch.full((65, dims.vocab), float("nan"))
     g.launch_host(x_host.clone(), logits_out=p_log)
