@@ -150,6 +150,21 @@ __device__ __forceinline__ void tma_prefetch_l2(const void* tmap, int32_t c0, in
 // kernel launched normally); nothing global that a previous kernel writes or
 // reads may be touched before it.  pdl_launch_dependents(): the next kernel
 // may start launching once every CTA of this one has called it or exited.
+// Shared -> global tile reduction: adds the box at [src] (the tensor map's
+// layout and swizzle) into the tensor at (c0, c1); element-wise atomic.
+__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, int32_t c0, int32_t c1, uint32_t src) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];"
+               ::"l"(tmap), "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// All but the newest group have finished reading their shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_all_but_one() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// Every committed group has completed (its global writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -40,6 +40,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
 #include <string>
 
 #include "common.cuh"
@@ -59,6 +60,9 @@ constexpr int kBarBytes = 1024;           // barriers + TMEM slot (+ alignment)
 constexpr int kSwapXchg = 64 * 17 * 4;    // swap-mode SwiGLU exchange buffer
 constexpr int kSwapXchgRope = 128 * 17 * 4;  // swap-mode rotary exchange buffer
 constexpr int kPrefetch = 16;             // K-slabs of the weight tile prefetched into L2 ahead
+constexpr int kEpiBox = 32;               // TMA-reduction epilogue: 32 rows x 32 fp32 columns per box
+constexpr int kEpiBoxBytes = kEpiBox * kEpiBox * 4;
+constexpr int kEpiStage = 4 * 2 * kEpiBoxBytes;  // two boxes per epilogue warp
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
 
@@ -68,6 +72,7 @@ struct Params {
   int splits, kb_per_split;  // split-K: `splits` K ranges per tile (residual epilogue only)
   int sk;                    // stream-K: equal shares of every token group's (weight tile, K slab) runs (residual only)
   int cl, m_groups;          // cluster size sharing one weight tile (multicast); token-tile groups
+  int tma_out;               // residual epilogue through TMA reductions (the third tensor map)
   RopeEpi rope;              // kEpiRope only
   void* c;
   const void* r;
@@ -155,7 +160,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* er
 template <typename T, int EPI, bool SWAP, int MSUB, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const Params p) {
+                   const __grid_constant__ CUtensorMap tm_c, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -169,6 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acce_bar = accf_bar + 2;        // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
   float* xchg = reinterpret_cast<float*>(bar_area + kBarBytes);  // swap SwiGLU only
+  // TMA-reduction epilogue (non-swap): each epilogue warp's two 4 KB boxes, 1024-byte aligned
+  const uint32_t epi_stage = smem_u32(bar_area + kBarBytes);
+  (void)epi_stage;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -331,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lrow = q * 32 + lane;     // accumulator lane = row of the MMA's M side
     int i = 0;
     bool alive = true;  // false once a wait gave up: loads/stores stop, barriers stay matched
+    int epi_n = 0;      // TMA-reduction boxes issued by this warp
     Work wk = work_begin(p, cid, n_clusters);
     Unit un;
     for (; work_next(p, wk, rank, un); ++i) {
@@ -482,6 +491,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                   dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
                 }
               }
+            }
+          } else if (EPI == SAR_EPI_RESIDUAL && p.tma_out) {
+            // in place, C += D: this warp's 32 rows x 32 columns at a time go
+            // through shared memory (128-byte swizzle, conflict-free) and are
+            // added into C by one TMA reduction (element-wise atomic, so K
+            // ranges of a split tile may land in any order); rows past M are
+            // clipped by the tensor map
+            const int row0 = (mt * MSUB + s) * 128 + q * 32;
+#pragma unroll 1
+            for (int j = 0; j < p.bn / kEpiBox; ++j) {
+              const int col = nt * p.bn + j * kEpiBox;
+              if (col >= p.N) break;
+              uint32_t v0[16], v1[16];
+              tmem_ld16(sbase + j * kEpiBox, v0);
+              tmem_ld16(sbase + j * kEpiBox + 16, v1);
+              tmem_wait_ld();
+              const uint32_t box = epi_stage + (uint32_t)((q * 2 + (epi_n & 1)) * kEpiBoxBytes);
+              if (lane == 0) bulk_wait_read_all_but_one();  // the box used two reductions ago is read
+              __syncwarp();
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const uint32_t* v = c < 4 ? v0 : v1;
+                const int e = (c & 3) * 4;
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 box + (uint32_t)(lane * 128 + ((c ^ (lane & 7)) << 4))),
+                             "r"(v[e]), "r"(v[e + 1]), "r"(v[e + 2]), "r"(v[e + 3])
+                             : "memory");
+              }
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA unit
+              __syncwarp();
+              if (lane == 0) {
+                tma_reduce_add_2d(&tm_c, col, row0, box);
+                bulk_commit();
+              }
+              ++epi_n;
             }
           } else {
 #pragma unroll 1
@@ -645,6 +689,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (alive) mbar_arrive(smem_u32(&acce_bar[acc]));
       }
     }
+    // the TMA reductions have written C before the CTA (and its shared memory) goes
+    if (epi_n > 0 && lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -720,6 +767,25 @@ int make_tmap_16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols
   CUresult r = fn(map, dt, 2, const_cast<void*>(ptr), dims, strides, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(SAR_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
+  return SAR_OK;
+}
+
+// fp32 [rows, cols] row-major, boxes of box_rows x box_cols (box_cols * 4 =
+// 128 bytes: 128-byte swizzle), for the epilogue's TMA reductions.
+int make_tmap_f32_box(CUtensorMap* map, void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                      uint32_t box_cols) {
+  auto fn = encode_fn();
+  if (!fn) return set_error(SAR_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (cols * 4) % 16 || rows == 0 || box_cols * 4 != 128)
+    return set_error(SAR_ERR_INVALID_ARG, "tensor map (fp32 output): pointer/stride not 16-byte aligned");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return set_error(SAR_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
   return SAR_OK;
 }
@@ -831,8 +897,11 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
   c.m_groups = c.m_tiles / c.cl;
   const int stage_bytes = c.msub * kTileA + (c.pair ? c.bn / 2 : c.bn) * kBK * 2;
   c.stage_bytes = stage_bytes;
+  // the in-place residual epilogue of the non-swap tilings adds through TMA reductions
+  c.tma_out = (!c.swap && epi == SAR_EPI_RESIDUAL && in_place) ? 1 : 0;
   const int extra = kBarBytes + 1024 +
-                    (!c.swap ? 0 : epi == SAR_EPI_SWIGLU ? kSwapXchg : epi == kEpiRope ? kSwapXchgRope : 0);
+                    (c.swap ? (epi == SAR_EPI_SWIGLU ? kSwapXchg : epi == kEpiRope ? kSwapXchgRope : 0)
+                            : (c.tma_out ? kEpiStage : 0));
   if (two_ctas && (!c.swap || c.bn > 128))
     return set_error(SAR_ERR_UNSUPPORTED, "gemm: two CTAs per SM only with the swap tiling and M <= 128");
   c.per_sm = two_ctas ? 2 : 1;
@@ -899,6 +968,15 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   p.c = c;
   p.r = residual;
   p.err = err;
+  p.tma_out = cfg.tma_out;
+  CUtensorMap tc_map;
+  std::memset(&tc_map, 0, sizeof(tc_map));
+  if (cfg.tma_out) {
+    if (epi != SAR_EPI_RESIDUAL || c != residual || cfg.swap)
+      return set_error(SAR_ERR_INVALID_ARG, "gemm: TMA-reduction epilogue needs the residual output in place");
+    const int mrc = make_tmap_f32_box(&tc_map, c, (uint64_t)M, (uint64_t)N, kEpiBox, kEpiBox);
+    if (mrc != SAR_OK) return mrc;
+  }
   if (cfg.cl < 1 || cfg.m_tiles % cfg.cl || cfg.m_groups * cfg.cl != cfg.m_tiles || cfg.bn % (8 * cfg.cl) ||
       (cfg.swap && cfg.cl != 1) || (cfg.pair && (cfg.cl != 2 || cfg.msub != 1 || cfg.swap)) ||
       cfg.stage_bytes != cfg.msub * kTileA + (cfg.pair ? cfg.bn / 2 : cfg.bn) * kBK * 2)
@@ -912,7 +990,7 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   }
   const CUtensorMap& ta = cfg.swap ? w_map : act_map;
   const CUtensorMap& tb = cfg.swap ? act_map : w_map;
-  void* args[] = {const_cast<CUtensorMap*>(&ta), const_cast<CUtensorMap*>(&tb), &p};
+  void* args[] = {const_cast<CUtensorMap*>(&ta), const_cast<CUtensorMap*>(&tb), &tc_map, &p};
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute attr[2];
   lc.blockDim = dim3(kThreads);

@@ -70,6 +70,7 @@ struct GemmCfg {
   int cl = 1;            // CTAs per cluster sharing a weight tile by multicast (non-swap)
   int m_groups = 0;      // token-tile groups of cl tiles
   int sk = 0;            // stream-K: equal K-slab shares over all resident clusters (residual epilogue)
+  int tma_out = 0;       // the in-place residual epilogue adds its tile through TMA reductions (non-swap)
 };
 
 // Box rows of the weight maps a model keeps per matrix (index i: 32 << i); the
