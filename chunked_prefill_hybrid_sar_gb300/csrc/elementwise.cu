@@ -300,7 +300,33 @@ __global__ void __launch_bounds__(1024) argmax_kernel(const float* __restrict__ 
   const float* row = logits + (size_t)blockIdx.x * vocab;
   float best = -FLT_MAX;
   int besti = 0x7fffffff;
-  for (int i = threadIdx.x; i < vocab; i += blockDim.x) {
+  // each thread scans its entries in increasing index order (so the first of
+  // equal maxima stays); rows whose start is 16-byte aligned are read as
+  // float4, eight loads in flight per thread
+  int tail = 0;
+  if ((vocab & 3) == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    const int n4 = vocab >> 2;
+    constexpr int kU = 8;
+    for (int base = 0; base < n4; base += kU * (int)blockDim.x) {
+      float4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = base + u * (int)blockDim.x + (int)threadIdx.x;
+        v[u] = i < n4 ? __ldg(r4 + i) : make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = 4 * (base + u * (int)blockDim.x + (int)threadIdx.x);
+        if (v[u].x > best) { best = v[u].x; besti = i; }
+        if (v[u].y > best) { best = v[u].y; besti = i + 1; }
+        if (v[u].z > best) { best = v[u].z; besti = i + 2; }
+        if (v[u].w > best) { best = v[u].w; besti = i + 3; }
+      }
+    }
+    tail = vocab;  // nothing left
+  }
+  for (int i = tail + (int)threadIdx.x; i < vocab; i += blockDim.x) {
     const float v = row[i];
     if (v > best) {
       best = v;
