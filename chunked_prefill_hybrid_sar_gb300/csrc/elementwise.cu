@@ -101,6 +101,14 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
       if (!ok && threadIdx.x == 0) report(a.err, SAR_ERR_BOUNDS, SITE_EMBED_BOUNDS, t);
       sr = reinterpret_cast<const uint2*>(static_cast<const T*>(a.table) + (size_t)(ok ? t : 0) * a.hidden);
     }
+    // the row's loads first, then the rotary table (its double-precision
+    // steps overlap their latency), then the fp32 copy of the row
+    uint2 u[kNormMaxVec];
+#pragma unroll
+    for (int k = 0; k < kNormMaxVec; ++k) {
+      const int i = threadIdx.x + k * kNormThreads;
+      if (i < nv) u[k] = sr[i];
+    }
     if (a.cs) {
       // the angle pos * theta_i is formed and reduced modulo 2*pi in double
       // precision, so long positions keep fp32 accuracy
@@ -119,11 +127,10 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
     for (int k = 0; k < kNormMaxVec; ++k) {
       const int i = threadIdx.x + k * kNormThreads;
       if (i < nv) {
-        const uint2 u = sr[i];
         if constexpr (SRC == kSrcRows)
-          v[k] = make_float4(bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y));
+          v[k] = make_float4(bf16lo(u[k].x), bf16hi(u[k].x), bf16lo(u[k].y), bf16hi(u[k].y));
         else
-          v[k] = make_float4(Elem<T>::lo(u.x), Elem<T>::hi(u.x), Elem<T>::lo(u.y), Elem<T>::hi(u.y));
+          v[k] = make_float4(Elem<T>::lo(u[k].x), Elem<T>::hi(u[k].x), Elem<T>::lo(u[k].y), Elem<T>::hi(u[k].y));
         if (!ok) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         hr[i] = v[k];
       }
