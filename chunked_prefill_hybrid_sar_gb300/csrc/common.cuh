@@ -46,6 +46,14 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// silu(x) = x / (1 + e^-x) with the approximate exponential and divide: the
+// result is rounded to 16 bits next, so their few-ulp fp32 errors never show,
+// and an IEEE divide per element would take the epilogue warps' issue slots
+// (which they share with the MMA-issuing warp).  For x below about -88 the
+// denominator overflows and the approximate divide gives 0, the limit.  Every
+// kernel that forms silu(gate) * up uses this one definition.
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -154,6 +162,12 @@ __device__ __forceinline__ void tma_prefetch_l2(const void* tmap, int32_t c0, in
 // layout and swizzle) into the tensor at (c0, c1); element-wise atomic.
 __device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, int32_t c0, int32_t c1, uint32_t src) {
   asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];"
+               ::"l"(tmap), "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+}
+// Shared -> global tile store of the box at [src] into the tensor at (c0, c1).
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t c0, int32_t c1, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
                ::"l"(tmap), "r"(c0), "r"(c1), "r"(src)
                : "memory");
 }

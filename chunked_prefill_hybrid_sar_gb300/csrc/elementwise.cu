@@ -238,7 +238,7 @@ __global__ void swiglu_finish_kernel(const float* __restrict__ gu, T* __restrict
     const float* src = gu + r * 2 * (size_t)F + (size_t)blk * 128 + j;
     const float4 g = *reinterpret_cast<const float4*>(src);
     const float4 u = *reinterpret_cast<const float4*>(src + 64);
-    auto sl = [](float x) { return x / (1.0f + __expf(-x)); };
+    auto sl = [](float x) { return silu(x); };
     *reinterpret_cast<uint2*>(act + o) =
         make_uint2(Elem<T>::pack(sl(g.x) * u.x, sl(g.y) * u.y), Elem<T>::pack(sl(g.z) * u.z, sl(g.w) * u.w));
   }

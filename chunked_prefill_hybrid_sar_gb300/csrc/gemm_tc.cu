@@ -24,7 +24,10 @@
 // CTA).
 //
 // Epilogues: 16-bit store, fp32 store, fp32 residual add (in place, optionally
-// split-K with atomic adds), SwiGLU over 64-row gate/up block pairs, and the
+// split-K; in the non-swap tilings each warp stages 32-row boxes in swizzled
+// shared memory and adds them with TMA reductions, in the swap tiling with
+// atomic adds), SwiGLU over 64-row gate/up block pairs (non-swap: staged boxes
+// written by TMA stores), and the
 // fused rotary + KV append of the QKV projection: q and k rotated at their
 // rows' positions (rotate-half pairing, dims i and i + hd/2; "maintain an
 // independent position_id for each chunk", SARATHI technique write-up section
@@ -60,11 +63,10 @@ constexpr int kBarBytes = 1024;           // barriers + TMEM slot (+ alignment)
 constexpr int kSwapXchg = 64 * 17 * 4;    // swap-mode SwiGLU exchange buffer
 constexpr int kSwapXchgRope = 128 * 17 * 4;  // swap-mode rotary exchange buffer
 constexpr int kPrefetch = 16;             // K-slabs of the weight tile prefetched into L2 ahead
-constexpr int kEpiBox = 32;               // TMA-reduction epilogue: 32 rows x 32 fp32 columns per box
+constexpr int kEpiBox = 32;               // TMA epilogue boxes: 32 rows x 128 bytes (32 fp32 or 64 16-bit columns)
 constexpr int kEpiBoxBytes = kEpiBox * kEpiBox * 4;
 constexpr int kEpiStage = 4 * 2 * kEpiBoxBytes;  // two boxes per epilogue warp
 
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
 
 struct Params {
   int M, N, K;
@@ -174,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acce_bar = accf_bar + 2;        // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
   float* xchg = reinterpret_cast<float*>(bar_area + kBarBytes);  // swap SwiGLU only
-  // TMA-reduction epilogue (non-swap): each epilogue warp's two 4 KB boxes, 1024-byte aligned
+  // TMA epilogues (non-swap): each epilogue warp's two 4 KB boxes, 1024-byte aligned
   const uint32_t epi_stage = smem_u32(bar_area + kBarBytes);
   (void)epi_stage;
 
@@ -464,6 +466,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                   }
                 }
               }
+            }
+          } else if (EPI == SAR_EPI_SWIGLU && p.tma_out) {
+            // packed columns [h*128, h*128+64) gate, [h*128+64, h*128+128) up:
+            // this warp's 32 rows x 64 outputs per block pair go through shared
+            // memory (128-byte swizzle) to one TMA store; rows past M are clipped
+            const int F = p.N >> 1;
+            const int row0 = (mt * MSUB + s) * 128 + q * 32;
+#pragma unroll 1
+            for (int h = 0; h < p.bn / 128; ++h) {
+              const int ocol = nt * (p.bn / 2) + h * 64;
+              if (ocol >= F) break;
+              const uint32_t box = epi_stage + (uint32_t)((q * 2 + (epi_n & 1)) * kEpiBoxBytes);
+              if (lane == 0) bulk_wait_read_all_but_one();  // the box used two stores ago is read
+              __syncwarp();
+#pragma unroll 1
+              for (int j = 0; j < 4; ++j) {
+                uint32_t g[16], u[16];
+                tmem_ld16(sbase + h * 128 + j * 16, g);
+                tmem_ld16(sbase + h * 128 + 64 + j * 16, u);
+                tmem_wait_ld();
+                uint32_t o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const float a0 = silu(__uint_as_float(g[2 * e])) * __uint_as_float(u[2 * e]);
+                  const float a1 = silu(__uint_as_float(g[2 * e + 1])) * __uint_as_float(u[2 * e + 1]);
+                  o[e] = Elem<T>::pack(a0, a1);
+                }
+                // outputs j*16 .. j*16+15 of this row: 16-byte chunks 2j and 2j+1
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 box + (uint32_t)(lane * 128 + (((2 * j) ^ (lane & 7)) << 4))),
+                             "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                             : "memory");
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 box + (uint32_t)(lane * 128 + (((2 * j + 1) ^ (lane & 7)) << 4))),
+                             "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                             : "memory");
+              }
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA unit
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tm_c, ocol, row0, box);
+                bulk_commit();
+              }
+              ++epi_n;
             }
           } else if constexpr (EPI == SAR_EPI_SWIGLU) {
             // packed columns [h*128, h*128+64) gate, [h*128+64, h*128+128) up
@@ -898,7 +944,8 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
   const int stage_bytes = c.msub * kTileA + (c.pair ? c.bn / 2 : c.bn) * kBK * 2;
   c.stage_bytes = stage_bytes;
   // the in-place residual epilogue of the non-swap tilings adds through TMA reductions
-  c.tma_out = (!c.swap && epi == SAR_EPI_RESIDUAL && in_place) ? 1 : 0;
+  // (the SwiGLU epilogue stores through TMA too)
+  c.tma_out = (!c.swap && ((epi == SAR_EPI_RESIDUAL && in_place) || epi == SAR_EPI_SWIGLU)) ? 1 : 0;
   const int extra = kBarBytes + 1024 +
                     (c.swap ? (epi == SAR_EPI_SWIGLU ? kSwapXchg : epi == kEpiRope ? kSwapXchgRope : 0)
                             : (c.tma_out ? kEpiStage : 0));
@@ -972,9 +1019,13 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   CUtensorMap tc_map;
   std::memset(&tc_map, 0, sizeof(tc_map));
   if (cfg.tma_out) {
-    if (epi != SAR_EPI_RESIDUAL || c != residual || cfg.swap)
-      return set_error(SAR_ERR_INVALID_ARG, "gemm: TMA-reduction epilogue needs the residual output in place");
-    const int mrc = make_tmap_f32_box(&tc_map, c, (uint64_t)M, (uint64_t)N, kEpiBox, kEpiBox);
+    int mrc = SAR_OK;
+    if (cfg.swap || (epi == SAR_EPI_RESIDUAL && c != residual) || (epi != SAR_EPI_RESIDUAL && epi != SAR_EPI_SWIGLU))
+      return set_error(SAR_ERR_INVALID_ARG, "gemm: TMA epilogue needs the residual output in place, or SwiGLU");
+    if (epi == SAR_EPI_RESIDUAL)
+      mrc = make_tmap_f32_box(&tc_map, c, (uint64_t)M, (uint64_t)N, kEpiBox, kEpiBox);
+    else  // SwiGLU output [M, N / 2] of the storage type, boxes of 32 rows x 64 columns
+      mrc = make_tmap_16(&tc_map, c, (uint64_t)M, (uint64_t)(N / 2), kEpiBox, storage);
     if (mrc != SAR_OK) return mrc;
   }
   if (cfg.cl < 1 || cfg.m_tiles % cfg.cl || cfg.m_groups * cfg.cl != cfg.m_tiles || cfg.bn % (8 * cfg.cl) ||
