@@ -392,6 +392,82 @@ __global__ void __launch_bounds__(kThreads, 1)
               if ((is_k || is_v) && row_ok && !slot_ok && hh == 0)
                 report(p.err, SAR_ERR_BOUNDS, SITE_ROPE_BOUNDS, row);
               float* crow = C + (size_t)row * p.N + col0;
+              if (p.tma_out && rp.hd == 128) {
+                // fp32 q|k|v of this head through shared memory: per round two
+                // 32x32 boxes, columns [32bp, 32bp+32) and [64+32bp, 96+32bp) --
+                // the rotate-half partners -- each written by one TMA store
+                // (rows past M clipped); k and v also go to their page slot
+                const int row0 = (mt * MSUB + s) * 128 + q * 32;
+                const float4* cs4 = reinterpret_cast<const float4*>(cs);
+#pragma unroll 1
+                for (int bp = 0; bp < 2; ++bp) {
+                  if (lane == 0) bulk_wait_read_all();  // both staging boxes have been read
+                  __syncwarp();
+                  const uint32_t b0 = epi_stage + (uint32_t)(q * 2 * kEpiBoxBytes), b1 = b0 + kEpiBoxBytes;
+#pragma unroll 1
+                  for (int jj = 0; jj < 2; ++jj) {
+                    const int j = bp * 2 + jj;  // 16-column chunk of each half
+                    uint32_t x1[16], x2[16];
+                    tmem_ld16(sbase + hh * 128 + j * 16, x1);
+                    tmem_ld16(sbase + hh * 128 + 64 + j * 16, x2);
+                    float r1[16], r2[16];
+                    if (is_v) {
+                      tmem_wait_ld();
+#pragma unroll
+                      for (int e = 0; e < 16; ++e) {
+                        r1[e] = __uint_as_float(x1[e]);
+                        r2[e] = __uint_as_float(x2[e]);
+                      }
+                    } else {
+                      float4 cc[8];
+#pragma unroll
+                      for (int e = 0; e < 8; ++e) cc[e] = row_ok ? __ldg(cs4 + j * 8 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                      tmem_wait_ld();
+#pragma unroll
+                      for (int e = 0; e < 16; ++e) {
+                        const float4 t4 = cc[e >> 1];
+                        const float tc = (e & 1) ? t4.z : t4.x, ts = (e & 1) ? t4.w : t4.y;
+                        const float a1 = __uint_as_float(x1[e]), a2 = __uint_as_float(x2[e]);
+                        r1[e] = a1 * tc - a2 * ts;
+                        r2[e] = a2 * tc + a1 * ts;
+                      }
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                      const uint32_t off = (uint32_t)(lane * 128 + (((4 * jj + c) ^ (lane & 7)) << 4));
+                      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(b0 + off), "f"(r1[4 * c]),
+                                   "f"(r1[4 * c + 1]), "f"(r1[4 * c + 2]), "f"(r1[4 * c + 3])
+                                   : "memory");
+                      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(b1 + off), "f"(r2[4 * c]),
+                                   "f"(r2[4 * c + 1]), "f"(r2[4 * c + 2]), "f"(r2[4 * c + 3])
+                                   : "memory");
+                    }
+                    if (dst) {
+                      uint32_t o1[8], o2[8];
+#pragma unroll
+                      for (int e = 0; e < 8; ++e) {
+                        o1[e] = Elem<T>::pack(r1[2 * e], r1[2 * e + 1]);
+                        o2[e] = Elem<T>::pack(r2[2 * e], r2[2 * e + 1]);
+                      }
+                      uint4* d1 = reinterpret_cast<uint4*>(dst + j * 16);
+                      uint4* d2 = reinterpret_cast<uint4*>(dst + 64 + j * 16);
+                      d1[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                      d1[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+                      d2[0] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                      d2[1] = make_uint4(o2[4], o2[5], o2[6], o2[7]);
+                    }
+                  }
+                  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA unit
+                  __syncwarp();
+                  if (lane == 0) {
+                    tma_store_2d(&tm_c, col0 + 32 * bp, row0, b0);
+                    tma_store_2d(&tm_c, col0 + 64 + 32 * bp, row0, b1);
+                    bulk_commit();
+                  }
+                  epi_n += 2;
+                }
+                continue;
+              }
               if (is_v) {
 #pragma unroll 1
                 for (int j = 0; j < rp.hd / 16; ++j) {
@@ -945,7 +1021,7 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
   c.stage_bytes = stage_bytes;
   // the in-place residual epilogue of the non-swap tilings adds through TMA reductions
   // (the SwiGLU epilogue stores through TMA too)
-  c.tma_out = (!c.swap && ((epi == SAR_EPI_RESIDUAL && in_place) || epi == SAR_EPI_SWIGLU)) ? 1 : 0;
+  c.tma_out = (!c.swap && ((epi == SAR_EPI_RESIDUAL && in_place) || epi == SAR_EPI_SWIGLU || epi == kEpiRope)) ? 1 : 0;
   const int extra = kBarBytes + 1024 +
                     (c.swap ? (epi == SAR_EPI_SWIGLU ? kSwapXchg : epi == kEpiRope ? kSwapXchgRope : 0)
                             : (c.tma_out ? kEpiStage : 0));
@@ -1015,14 +1091,16 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   p.c = c;
   p.r = residual;
   p.err = err;
-  p.tma_out = cfg.tma_out;
+  // (the rotary epilogue's TMA path covers head_dim 128)
+  p.tma_out = (cfg.tma_out && !(epi == kEpiRope && rope->hd != 128)) ? 1 : 0;
   CUtensorMap tc_map;
   std::memset(&tc_map, 0, sizeof(tc_map));
-  if (cfg.tma_out) {
+  if (p.tma_out) {
     int mrc = SAR_OK;
-    if (cfg.swap || (epi == SAR_EPI_RESIDUAL && c != residual) || (epi != SAR_EPI_RESIDUAL && epi != SAR_EPI_SWIGLU))
-      return set_error(SAR_ERR_INVALID_ARG, "gemm: TMA epilogue needs the residual output in place, or SwiGLU");
-    if (epi == SAR_EPI_RESIDUAL)
+    if (cfg.swap || (epi == SAR_EPI_RESIDUAL && c != residual) ||
+        (epi != SAR_EPI_RESIDUAL && epi != SAR_EPI_SWIGLU && epi != kEpiRope))
+      return set_error(SAR_ERR_INVALID_ARG, "gemm: TMA epilogue needs the residual output in place, SwiGLU or rotary");
+    if (epi == SAR_EPI_RESIDUAL || epi == kEpiRope)
       mrc = make_tmap_f32_box(&tc_map, c, (uint64_t)M, (uint64_t)N, kEpiBox, kEpiBox);
     else  // SwiGLU output [M, N / 2] of the storage type, boxes of 32 rows x 64 columns
       mrc = make_tmap_16(&tc_map, c, (uint64_t)M, (uint64_t)(N / 2), kEpiBox, storage);
