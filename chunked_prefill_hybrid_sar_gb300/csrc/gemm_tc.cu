@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lrow = q * 32 + lane;     // accumulator lane = row of the MMA's M side
     int i = 0;
     bool alive = true;  // false once a wait gave up: loads/stores stop, barriers stay matched
-    int epi_n = 0;      // TMA-reduction boxes issued by this warp
+    int epi_n = 0;      // TMA epilogue boxes (reductions or stores) issued by this warp
     Work wk = work_begin(p, cid, n_clusters);
     Unit un;
     for (; work_next(p, wk, rank, un); ++i) {
