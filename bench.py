@@ -394,41 +394,45 @@ def run_ours(args):
 
 # ------------------------------------------------------------------ oracle arm
 
-def oracle_sample(n_decode=8, start=0, seed=3):
-    """A bounded sample of the workload for the CPU oracle: one hybrid step
-    with the 448-token chunk at `start` and `n_decode` of the decodes."""
-    import torch
-
+def oracle_cases(seed=3):
+    """The workload's cases for the CPU oracle: per chunk start (0, 512,
+    1536) one hybrid step of the 448-token chunk and all 64 decodes (contexts
+    uniform in [128, 4096], random K/V histories), drawn by the same recipe
+    as the GPU cases with another seed.  Returns (dims, weights, head, the
+    steps' parts, rows per step)."""
     from oracle import model as om
 
-    dims = synth.MISTRAL_LAYER
-    case = synth.mistral_layer_case(seed, n_decode=n_decode, tau=TAU, starts=(start,))
-    # keep the chunk at Lp = 448 rows as in the workload
-    lp = TAU - BD
-    gen = synth.generator(seed + 11)
-    prompt = synth.normal(gen, (start + lp, dims.hidden), dtype=torch.bfloat16)
+    case = synth.mistral_layer_case(seed, n_decode=BD, tau=TAU, starts=synth.MISTRAL_STARTS)
+    dims = case["dims"]
     w = om.layer_weights_np(case["layers"][0])
     head = om.layer_weights_np(case["head"])
-    parts = [om.Part(x=om.to_np(prompt), lo=start, is_prefill=True)]
+    decs = []
     for i, c in enumerate(case["ctxs"]):
         k, v = case["histories"][i]
-        parts.append(om.Part(x=om.to_np(case["decode_inputs"][i:i + 1]), lo=c,
-                             given=[om.LayerCache(om.to_np(k), om.to_np(v))]))
-    rows = lp + n_decode
-    return dims, w, head, parts, rows
+        decs.append(om.Part(x=om.to_np(case["decode_inputs"][i:i + 1]), lo=c,
+                            given=[om.LayerCache(om.to_np(k), om.to_np(v))]))
+    steps = [[om.Part(x=om.to_np(case["prompts"][s]), lo=s, is_prefill=True)] + decs
+             for s in synth.MISTRAL_STARTS]
+    return dims, w, head, steps, case["lp"] + BD
+
+
+def oracle_sample_text(n_steps, dt):
+    return (f"{n_steps} oracle hybrid steps (float64 NumPy) of the workload itself, the chunk at start "
+            f"{'/'.join(str(s) for s in synth.MISTRAL_STARTS)} in turn with all {BD} decodes "
+            f"({TAU} rows each; {dt:.1f} s; the oracle computes a chunk by running its prompt prefix)")
 
 
 def cpu_baseline(args):
     from oracle import model as om
 
-    dims, w, head, parts, rows = oracle_sample()
+    dims, w, head, steps, rows = oracle_cases()
     t0 = time.perf_counter()
-    om.hybrid_step([w], head, dims, parts)
+    for parts in steps:
+        om.hybrid_step([w], head, dims, parts)
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0))
-    return {"value": rows / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"one oracle hybrid step (float64 NumPy): 448-row chunk at start 0 + 8 decodes "
-                      f"of the workload's shape ({rows} rows, {dt:.1f} s)"}
+    return {"value": rows * len(steps) / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": oracle_sample_text(len(steps), dt)}
 
 
 def run_reference(args):
@@ -437,12 +441,12 @@ def run_reference(args):
         return None
     from oracle import model as om
 
-    dims, w, head, parts, rows = oracle_sample()
-    for _ in range(min(args.warmup, 1)):
-        om.hybrid_step([w], head, dims, parts)
+    dims, w, head, steps, rows = oracle_cases()
+    for i in range(min(args.warmup, 1)):
+        om.hybrid_step([w], head, dims, steps[i % len(steps)])
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        om.hybrid_step([w], head, dims, parts)
+    for i in range(args.steps):  # the cases in turn, as the GPU arm cycles them
+        om.hybrid_step([w], head, dims, steps[i % len(steps)])
     dt = time.perf_counter() - t0
     value = rows * args.steps / dt
     cores = len(os.sched_getaffinity(0))
@@ -451,7 +455,7 @@ def run_reference(args):
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "config": config_block(world),
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                            "sample": f"per step one oracle hybrid step: 448-row chunk + 8 decodes ({rows} rows)"},
+                            "sample": oracle_sample_text(args.steps, dt)},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
     return out
