@@ -11,8 +11,7 @@ import ctypes
 
 from . import _lib
 from ._lib import (SAR_EPI_F32, SAR_EPI_RESIDUAL, SAR_EPI_STORE, SAR_EPI_SWIGLU, SAR_GEMM_AUTO,
-                   SAR_GEMM_CLUSTER_1, SAR_GEMM_CLUSTER_2, SAR_GEMM_CLUSTER_4, SAR_GEMM_PAIR_N128,
-                   SAR_GEMM_PAIR_N192,
+                   SAR_GEMM_PAIR_N128, SAR_GEMM_PAIR_N192,
                    SAR_GEMM_PAIR_N256, SAR_GEMM_STREAM_K, SAR_GEMM_TWO_CTAS,
                    SAR_GEMM_M128_N128, SAR_GEMM_M128_N256, SAR_GEMM_M256_N128, SAR_GEMM_SWAP,
                    SAR_IN_HIDDEN, SAR_IN_TOKENS, SAR_STORAGE_BF16, SAR_STORAGE_F16, KERNEL_KINDS,

@@ -29,7 +29,6 @@ SAR_IN_TOKENS = 1
 SAR_STORAGE_F16, SAR_STORAGE_BF16 = 0, 1
 SAR_EPI_STORE, SAR_EPI_RESIDUAL, SAR_EPI_SWIGLU, SAR_EPI_F32 = 0, 1, 2, 3
 SAR_GEMM_AUTO, SAR_GEMM_M128_N128, SAR_GEMM_M128_N256, SAR_GEMM_SWAP, SAR_GEMM_M256_N128 = 0, 1, 2, 3, 4
-SAR_GEMM_CLUSTER_1, SAR_GEMM_CLUSTER_2, SAR_GEMM_CLUSTER_4 = 0x100, 0x200, 0x400
 SAR_GEMM_PAIR_N256, SAR_GEMM_PAIR_N128, SAR_GEMM_PAIR_N192 = 5, 6, 7
 SAR_GEMM_TWO_CTAS = 0x1000
 SAR_GEMM_STREAM_K = 0x2000

@@ -1,7 +1,7 @@
 // Projection / FFN / LM-head GEMM on the 5th-generation tensor cores.
 //
 // C = epilogue(A . W^T) with A = activations [M, K] and W = weights [N, K],
-// both bf16 and K-major.  This is the "one GEMM per weight over the stacked
+// both of the 16-bit storage type (fp16 by default, or bf16) and K-major.  This is the "one GEMM per weight over the stacked
 // [Lp+Bd, H] rows" of the hybrid step ("SARATHI: Efficient LLM Inference by
 // Piggybacking Decodes with Chunked Prefills", reading notes, part 2 section 3).
 //
@@ -9,19 +9,18 @@
 //   warp 0       TMA producer: 64-wide K slabs of the A and B tiles into a ring
 //                of shared-memory stages (128-byte swizzle), mbarrier tx counts.
 //   warp 1       allocates tensor memory; lane 0 issues tcgen05.mma
-//                (kind::f16, bf16 x bf16 -> fp32, M = 128, N = bn, K = 16) and
+//                (kind::f16, 16-bit x 16-bit of one type -> fp32, M = 128 or 256, N = bn, K = 16) and
 //                tcgen05.commit's each stage back to the producer.
 //   warps 2..5   epilogue: tcgen05.ld of the fp32 accumulator (each warp owns
 //                the 32 TMEM lanes of its warp-id % 4), fused epilogue, global
 //                stores.  Two accumulators alternate so the epilogue of one
 //                tile overlaps the MMAs of the next.
 //
-// Clusters (non-swap): the CTAs of a 2- or 4-CTA cluster take consecutive
-// token tiles of one weight tile; each fetches 1/cl of the weight rows of every
-// K slab and multicasts them into all the cluster's shared memories, so the
-// weights leave L2 once per cluster.  A stage is refilled only after every
-// CTA's MMAs released it (the empty barrier counts one multicast commit per
-// CTA).
+// CTA pairs (cta_group::2): the two CTAs of a 2-CTA cluster take two
+// consecutive token tiles of one 256-row weight tile; each loads its own 128
+// token rows and half of the weight rows, and the leader issues one M = 256
+// MMA over both CTAs' shared memory.  No other tiling uses a cluster, and no
+// load is multicast: every CTA's TMA loads fill its own shared memory only.
 //
 // Epilogues: 16-bit store, fp32 store, fp32 residual add (in place, optionally
 // split-K; in the non-swap tilings each warp stages 32-row boxes in swizzled
@@ -73,7 +72,7 @@ struct Params {
   int bn, m_tiles, n_tiles, k_blocks, stages, stage_bytes, tmem_cols;
   int splits, kb_per_split;  // split-K: `splits` K ranges per tile (residual epilogue only)
   int sk;                    // stream-K: equal shares of every token group's (weight tile, K slab) runs (residual only)
-  int cl, m_groups;          // cluster size sharing one weight tile (multicast); token-tile groups
+  int cl, m_groups;          // CTAs per cluster (2: CTA pair, else 1); token-tile groups
   int tma_out;               // residual epilogue through TMA reductions (the third tensor map)
   RopeEpi rope;              // kEpiRope only
   void* c;
@@ -82,9 +81,9 @@ struct Params {
 };
 
 // Work unit u of a cluster -> (token tile, weight tile, K-slab range).  The
-// `cl` CTAs of a cluster take consecutive token tiles of one weight tile (and
-// share that tile by multicast); token-tile groups vary fastest so clusters
-// running at the same time also share the weight slab in L2.
+// `cl` CTAs of a cluster (a CTA pair, or one CTA) take consecutive token tiles
+// of one weight tile; token-tile groups vary fastest so clusters running at
+// the same time share the weight slab in L2.
 struct Unit {
   int mt, nt, kb0, kb1;
 };
@@ -183,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
-      // multicast: released by every CTA of the cluster; pair: by the leader's MMAs
-      mbar_init(smem_u32(&empty_bar[s]), PAIR ? 1u : (uint32_t)p.cl);
+      // released by this CTA's MMAs (pair: by the leader's, which read both CTAs' stages)
+      mbar_init(smem_u32(&empty_bar[s]), 1u);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&accf_bar[s]), 1);
@@ -199,13 +198,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (p.cl > 1) cluster_sync();  // peers' barriers are initialised before any multicast
+  if (p.cl > 1) cluster_sync();  // the pair's barriers are initialised before either CTA's loads
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const int rank = p.cl > 1 ? (int)cluster_ctarank() : 0;
   const int cid = blockIdx.x / p.cl, n_clusters = gridDim.x / p.cl;
-  const uint16_t cl_mask = (uint16_t)((1u << p.cl) - 1u);
   const int acc_cols = MSUB * p.bn;
   Unit un0;
   Work w0 = work_begin(p, cid, n_clusters);
@@ -215,8 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // CTA's first weight slabs into L2 while that kernel drains
     const Unit& un = un0;
     const void* w_map = SWAP ? (const void*)&tm_a : (const void*)&tm_b;
-    const int slice = PAIR ? p.bn / 2 : p.bn / p.cl;
-    const int w_row = SWAP ? un.nt * 128 : un.nt * p.bn + rank * slice;
+    const int w_row = SWAP ? un.nt * 128 : un.nt * p.bn + (PAIR ? rank * (p.bn / 2) : 0);
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
     for (int kb = un.kb0; kb < un.kb0 + kPrefetch && kb < un.kb1; ++kb) tma_prefetch_l2(w_map, kb * kBK, w_row);
@@ -239,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the weight tile streams from HBM: pull it into L2 kPrefetch K-slabs ahead
         // of the shared-memory ring so the ring's loads hit L2
         const void* w_map = SWAP ? (const void*)&tm_a : (const void*)&tm_b;
-        // weight rows this CTA fetches: its multicast slice, or its half of the pair's tile
-        const int slice = PAIR ? p.bn / 2 : p.bn / p.cl;
+        // weight rows this CTA fetches: the whole tile, or its half of the pair's tile
+        const int slice = PAIR ? p.bn / 2 : 0;
         const int w_row = SWAP ? a_row : b_row + rank * slice;
         // (swap tiling: one CTA per weight tile, no reuse to gain from L2;
         // the first unit's first slabs were requested before the wait above)
@@ -267,17 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int s = 0; s < MSUB; ++s)
             tma_load_2d(smem_u32(st + s * kTileA), &tm_a, kb * kBK, a_row + s * 128, fb);
-          if (p.cl > 1)
-            tma_load_2d_mc(smem_u32(st + MSUB * kTileA + rank * slice * 128), &tm_b, kb * kBK, b_row + rank * slice,
-                           fb, cl_mask);
-          else
-            tma_load_2d(smem_u32(st + MSUB * kTileA), &tm_b, kb * kBK, b_row, fb);
+          tma_load_2d(smem_u32(st + MSUB * kTileA), &tm_b, kb * kBK, b_row, fb);
           next_stage(stage, phase, stages);
         }
       }
       if (p.cl > 1) {
-        // every CTA of the cluster has released the last fills: no peer will
-        // arrive on this CTA's barriers after it leaves
+        // pair: the leader's MMAs have released the last fills, so its commits
+        // arrive on no barrier of this CTA after it leaves
         for (int i = 0; i < stages && ok; ++i) {
           ok = mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.err, SITE_GEMM_PRODUCER);
           next_stage(stage, phase, stages);
@@ -320,8 +313,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (PAIR)
             mma_commit_pair(smem_u32(&empty_bar[stage]));
-          else if (p.cl > 1)
-            mma_commit_mc(smem_u32(&empty_bar[stage]), cl_mask);
           else
             mma_commit(smem_u32(&empty_bar[stage]));
           next_stage(stage, phase, stages);
@@ -818,7 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (p.cl > 1) cluster_sync();  // no CTA leaves while a peer may still address it
+  if (p.cl > 1) cluster_sync();  // neither CTA of a pair leaves while the other may still address it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<PAIR>(tmem_base, (uint32_t)p.tmem_cols);
@@ -913,12 +904,10 @@ int make_tmap_f32_box(CUtensorMap* map, void* ptr, uint64_t rows, uint64_t cols,
 }
 
 int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in_place) {
-  const int cl_flag = variant & (SAR_GEMM_CLUSTER_1 | SAR_GEMM_CLUSTER_2 | SAR_GEMM_CLUSTER_4);
   const bool two_ctas = (variant & SAR_GEMM_TWO_CTAS) != 0;
   const bool want_sk = (variant & SAR_GEMM_STREAM_K) != 0;
-  variant &= ~(SAR_GEMM_CLUSTER_1 | SAR_GEMM_CLUSTER_2 | SAR_GEMM_CLUSTER_4 | SAR_GEMM_TWO_CTAS | SAR_GEMM_STREAM_K);
+  variant &= ~(SAR_GEMM_TWO_CTAS | SAR_GEMM_STREAM_K);
   const bool auto_variant = variant == SAR_GEMM_AUTO;
-  if (cl_flag & (cl_flag - 1)) return set_error(SAR_ERR_INVALID_ARG, "gemm: more than one cluster flag");
   if (M < 1 || N < 64 || K < 64 || N % 64 || K % 64)
     return set_error(SAR_ERR_UNSUPPORTED, "gemm: need M >= 1, N and K multiples of 64");
   if (epi == SAR_EPI_SWIGLU && N % 128)
@@ -969,7 +958,7 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
       long best = (N % 256 == 0) ? cost(1, 256, false) : -1;
       if (best < 0 || cost(1, 128, false) < best) { variant = SAR_GEMM_M128_N128; best = cost(1, 128, false); }
       if (cost(2, 128, false) < best) { variant = SAR_GEMM_M256_N128; best = cost(2, 128, false); }
-      if (N % 256 == 0 && cl_flag <= SAR_GEMM_CLUSTER_2 && cost(1, 256, true) < best) variant = SAR_GEMM_PAIR_N256;
+      if (N % 256 == 0 && cost(1, 256, true) < best) variant = SAR_GEMM_PAIR_N256;
     }
   }
   switch (variant) {
@@ -987,7 +976,6 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
   if (!c.swap && (N % c.bn || c.bn % 128) && epi == SAR_EPI_SWIGLU)
     return set_error(SAR_ERR_UNSUPPORTED, "gemm: SwiGLU tiles must not straddle N and hold whole gate/up blocks");
   if (c.swap) {
-    if (cl_flag > SAR_GEMM_CLUSTER_1) return set_error(SAR_ERR_UNSUPPORTED, "gemm: swap tiling takes no cluster");
     c.m_tiles = 1;
     c.n_tiles = (N + 127) / 128;
     c.a_box_rows = 128;   // weights
@@ -996,25 +984,15 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
   } else {
     c.m_tiles = (M + 128 * c.msub - 1) / (128 * c.msub);
     c.n_tiles = (N + c.bn - 1) / c.bn;
-    // token tiles of one weight tile run as a cluster that multicasts the tile
+    // a CTA pair is a 2-CTA cluster over two token tiles; every other tiling is one CTA
     if (c.pair) {
-      if (cl_flag && cl_flag != SAR_GEMM_CLUSTER_2)
-        return set_error(SAR_ERR_UNSUPPORTED, "gemm: a pair tiling is a cluster of 2");
       c.cl = 2;
       c.m_tiles += c.m_tiles & 1;  // an odd last tile pairs with an all-padding one
-    } else if (cl_flag == SAR_GEMM_CLUSTER_1) c.cl = 1;
-    else if (cl_flag == SAR_GEMM_CLUSTER_2) c.cl = 2;
-    else if (cl_flag == SAR_GEMM_CLUSTER_4) c.cl = 4;
-    else {
-      // pairs only: a GPC's SMs do not divide into clusters of 4, which then
-      // leaves SMs idle; and only when the work spans two or more waves (below
-      // that the cluster launch costs more than the L2 traffic it saves)
-      const long units = (long)c.m_tiles * c.n_tiles;
-      c.cl = (c.m_tiles % 2 == 0 && units >= 2L * sms) ? 2 : 1;
+    } else {
+      c.cl = 1;
     }
-    if (c.m_tiles % c.cl) return set_error(SAR_ERR_UNSUPPORTED, "gemm: cluster size does not divide the token tiles");
     c.a_box_rows = 128;          // tokens
-    c.b_box_rows = c.bn / c.cl;  // this CTA's slice (or half) of the weight tile
+    c.b_box_rows = c.bn / c.cl;  // the weight tile, or this CTA's half of the pair's
   }
   c.m_groups = c.m_tiles / c.cl;
   const int stage_bytes = c.msub * kTileA + (c.pair ? c.bn / 2 : c.bn) * kBK * 2;
@@ -1106,8 +1084,8 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
       mrc = make_tmap_16(&tc_map, c, (uint64_t)M, (uint64_t)(N / 2), kEpiBox, storage);
     if (mrc != SAR_OK) return mrc;
   }
-  if (cfg.cl < 1 || cfg.m_tiles % cfg.cl || cfg.m_groups * cfg.cl != cfg.m_tiles || cfg.bn % (8 * cfg.cl) ||
-      (cfg.swap && cfg.cl != 1) || (cfg.pair && (cfg.cl != 2 || cfg.msub != 1 || cfg.swap)) ||
+  if (cfg.cl != (cfg.pair ? 2 : 1) || cfg.m_tiles % cfg.cl || cfg.m_groups * cfg.cl != cfg.m_tiles ||
+      cfg.bn % (8 * cfg.cl) || (cfg.pair && (cfg.msub != 1 || cfg.swap)) ||
       cfg.stage_bytes != cfg.msub * kTileA + (cfg.pair ? cfg.bn / 2 : cfg.bn) * kBK * 2)
     return set_error(SAR_ERR_INVALID_ARG, "gemm: inconsistent cluster configuration");
   static bool attr_done[2][5][2][3][2] = {};

@@ -67,14 +67,14 @@ struct GemmCfg {
   int pair = 0;          // 2-CTA tiles: M = 256 MMAs over a CTA pair (cl = 2)
   int stage_bytes = 0;   // shared memory of one pipeline stage (per CTA)
   int per_sm = 1;        // CTAs resident per SM (2: swap tiling, half the stages each)
-  int cl = 1;            // CTAs per cluster sharing a weight tile by multicast (non-swap)
+  int cl = 1;            // CTAs per cluster: 2 for a CTA pair, else 1
   int m_groups = 0;      // token-tile groups of cl tiles
   int sk = 0;            // stream-K: equal K-slab shares over all resident clusters (residual epilogue)
   int tma_out = 0;       // the in-place residual epilogue adds its tile through TMA reductions (non-swap)
 };
 
 // Box rows of the weight maps a model keeps per matrix (index i: 32 << i); the
-// GEMM reads the weight tile through the map whose box is bn / cl rows
+// GEMM reads the weight tile through the map whose box is bn / cl rows (a pair CTA: its half)
 // (swap tiling: 128).
 constexpr int kWeightBoxes = 4;
 inline int weight_box_index(const GemmCfg& c) {

@@ -94,15 +94,6 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
       : "memory");
 }
 
-// Arrive on the same barrier offset in every CTA of `mask` once this thread's
-// MMAs so far have completed.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)

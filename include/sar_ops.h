@@ -47,16 +47,6 @@ enum {
   SAR_GEMM_PAIR_N128 = 6, /* the same with 128 weight rows per tile                 */
   SAR_GEMM_PAIR_N192 = 7, /* the same with 192 weight rows per tile (not for the
                              SwiGLU epilogue, whose gate/up blocks are 128 wide)    */
-  /* Optional flags OR-ed into a non-swap tiling (or AUTO): how many CTAs of a
-   * thread-block cluster share one weight tile.  Each fetches 1/c of the tile's
-   * rows from L2 and multicasts it to all, so the weights leave L2 once per
-   * cluster instead of once per token tile.  Without a flag the library takes
-   * 2 when the token tiles are even in number and the tiles fill two or more
-   * waves of the SMs, else 1.  A size the token tiles do not divide into
-   * returns SAR_ERR_UNSUPPORTED. */
-  SAR_GEMM_CLUSTER_1 = 0x100,
-  SAR_GEMM_CLUSTER_2 = 0x200,
-  SAR_GEMM_CLUSTER_4 = 0x400,
   /* Optional flag for the swap tiling with at most 128 token rows: two CTAs
    * per SM, each with half the pipeline, so twice as many weight slabs are in
    * flight per SM (the memory-bound regime). */

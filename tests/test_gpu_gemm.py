@@ -172,67 +172,6 @@ def test_gemm_residual_out_of_place_does_not_split():
     assert ((c.double().cpu() - ref).abs().max() / ref.abs().max()).item() < 1e-5
 
 
-CLUSTERS = {1: sar.SAR_GEMM_CLUSTER_1, 2: sar.SAR_GEMM_CLUSTER_2, 4: sar.SAR_GEMM_CLUSTER_4}
-
-
-@pytest.mark.parametrize("M,variant", [(512, "m128n256"), (500, "m128n128"), (1024, "m256n128"),
-                                       (256, "m128n256"), (2048, "m128n256")])
-@pytest.mark.parametrize("cl", [1, 2, 4])
-@pytest.mark.parametrize("epi", ["store", "residual", "swiglu", "f32"])
-def test_gemm_cluster_multicast(M, variant, cl, epi):
-    """Clusters of 2 or 4 CTAs whose token tiles share one weight tile, each
-    fetching a slice of it and multicasting it to all, give the unclustered
-    result bit for bit (the same MMAs over the same shared-memory tiles)."""
-    tiles = -(-M // (256 if variant == "m256n128" else 128))
-    if tiles % cl:
-        pytest.skip("cluster size does not divide the token tiles")
-    N, K = 1024, 1024
-    dtype = torch.float16
-    a, w, r = operands(M, N, K, 7, dtype)
-    a, w, r = a.to(DEV), w.to(DEV), r.to(DEV)
-    epi_id = {"store": sar.SAR_EPI_STORE, "residual": sar.SAR_EPI_RESIDUAL, "swiglu": sar.SAR_EPI_SWIGLU,
-              "f32": sar.SAR_EPI_F32}[epi]
-    out_cols = N // 2 if epi == "swiglu" else N
-    out_dt = torch.float32 if epi in ("residual", "f32") else dtype
-
-    def run(flag):
-        c = torch.full((M, out_cols), float("nan"), dtype=out_dt, device=DEV)
-        # out of place: the residual epilogue then never splits K, so both runs add in one order
-        sar.gemm(a, w, c, residual=r if epi == "residual" else None, epilogue=epi_id,
-                 variant=VARIANTS[variant] | flag)
-        return c
-
-    base = run(sar.SAR_GEMM_CLUSTER_1)
-    got = run(CLUSTERS[cl])
-    torch.cuda.synchronize()
-    assert torch.equal(got, base)
-    if epi == "f32":
-        ref = a.double().cpu() @ w.double().cpu().T
-        assert ((got.double().cpu() - ref).abs().max() / ref.abs().max()).item() < 1e-5
-
-
-def test_gemm_cluster_split_k_residual_in_place():
-    """Split-K and multicast together: 4 token tiles in one cluster, K = 8192."""
-    M, N, K = 512, 2048, 8192
-    a, w, r = operands(M, N, K, 8)
-    h = r.to(DEV).clone()
-    sar.gemm(a.to(DEV), w.to(DEV), h, residual=h, epilogue=sar.SAR_EPI_RESIDUAL,
-             variant=sar.SAR_GEMM_M128_N256 | sar.SAR_GEMM_CLUSTER_4)
-    torch.cuda.synchronize()
-    ref = a.double() @ w.double().T + r.double()
-    assert ((h.double().cpu() - ref).abs().max() / ref.abs().max()).item() < 1e-5
-
-
-def test_gemm_cluster_rejects_sizes_that_do_not_divide():
-    a = torch.zeros(384, 256, dtype=torch.float16, device=DEV)
-    w = torch.zeros(256, 256, dtype=torch.float16, device=DEV)
-    c = torch.zeros(384, 256, dtype=torch.float16, device=DEV)
-    with pytest.raises(sar.SarError):
-        sar.gemm(a, w, c, variant=sar.SAR_GEMM_M128_N128 | sar.SAR_GEMM_CLUSTER_2)
-    with pytest.raises(sar.SarError):
-        sar.gemm(a[:200], w, c[:200], variant=sar.SAR_GEMM_SWAP | sar.SAR_GEMM_CLUSTER_2)
-
-
 @pytest.mark.parametrize("M,N,K", [(512, 28672, 4096), (512, 4096, 14336), (1000, 6144, 4096)])
 def test_gemm_pair_large(M, N, K):
     """CTA-pair tiles at projection shapes: store and split-K residual in place."""
@@ -285,7 +224,7 @@ def test_gemm_swap_two_ctas_per_sm(M, epi):
     (512, 4096, 14336, "pair256", 0),        # the down projection at 512 rows
     (1000, 6144, 4096, "pair128", 0),        # ragged token tiles, an all-padding partner tile
     (300, 1024, 4096, "m128n256", 0),        # single CTAs, ragged rows
-    (512, 2048, 8192, "m128n256", sar.SAR_GEMM_CLUSTER_2),  # with weight multicast
+    (512, 2048, 8192, "m128n256", 0),        # four token groups, K = 8192
     (100, 192, 320, "m128n128", 0),          # fewer K slabs than CTAs: most shares are empty
 ])
 def test_gemm_stream_k_residual_in_place(M, N, K, variant, flags):
