@@ -15,8 +15,9 @@ Appendix table of evaluated models):
   and after the FFN.
 
 Parity status: rms_norm, apply_rope, silu, attention (full causal and
-sliding-window), decoder_layer and the hybrid step are pinned by ``tests/test_oracle_*.py`` (closed forms, library
-special cases, brute force, chunked == one-shot, hybrid == serial).  The
+sliding-window), decoder_layer, final_logits (with the sampled-row choice)
+and the hybrid step are pinned by ``tests/test_oracle_*.py`` (closed forms,
+library special cases, brute force, chunked == one-shot, hybrid == serial).  The
 absolute hidden values of a random-initialised model have no printed worked
 example and are otherwise parity unpinned.
 """
@@ -213,7 +214,9 @@ def chunked_prefill(layers: list, dims, x: np.ndarray, chunk: int) -> tuple:
 
 
 def final_logits(h_rows: np.ndarray, head: dict, dims) -> np.ndarray:
-    """Final RMSNorm and LM head on the rows whose next token is sampled."""
+    """Final RMSNorm and LM head on the rows whose next token is sampled
+    (after the last layer, each sequence's last position feeds the sampler:
+    *Sarathi-Serve overview* §3.2, logits then sampling)."""
     y = rms_norm(h_rows, head["final_norm"], dims.rms_eps)
     return y @ head["lm_head"].T
 
@@ -310,6 +313,12 @@ def hybrid_step(layers, head, dims, parts: list) -> tuple:
         hidden.append(h)
     logits = None
     if head:
-        last = bounds[1:] - 1
-        logits = final_logits(h[last], head, dims)
+        logits = final_logits(h[sampled_rows(parts)], head, dims)
     return hidden, logits
+
+
+def sampled_rows(parts: list) -> np.ndarray:
+    """Stacked-row index of each part's last position, the one whose next
+    token is sampled: a chunk's last row (rows are chunk-first, then decodes
+    in order: *SARATHI reading notes* part 2 §3), and each decode's only row."""
+    return np.cumsum([p.n_rows for p in parts]) - 1

@@ -416,6 +416,92 @@ def test_hybrid_rows_are_chunk_first_then_decodes_in_order():
     np.testing.assert_allclose(hyb[0][12 + 1], alone[0][-1], rtol=1e-10, atol=1e-11)
 
 
+# ---------------------------------------------------------------- final norm + LM head
+
+def torch_logits(h_rows, head, dims):
+    """Final norm and LM head composed from library routines (float64)."""
+    h = torch.from_numpy(np.asarray(h_rows, dtype=np.float64))
+    g = torch.from_numpy(head["final_norm"])
+    return F.linear(F.rms_norm(h, (dims.hidden,), g, eps=dims.rms_eps), torch.from_numpy(head["lm_head"])).numpy()
+
+
+def _head_with_gain(head, dims, seed):
+    rng = np.random.default_rng(seed)
+    head = dict(head)
+    head["final_norm"] = 1 + 0.3 * rng.standard_normal(dims.hidden)  # non-unit: a dropped norm shows
+    return head
+
+
+def test_final_logits_match_torch_composition():
+    dims = small_dims()
+    _, head, gen = np_layers(21, dims)
+    head = _head_with_gain(head, dims, 21)
+    h = 3.0 * synth.normal(gen, (6, dims.hidden)).double().numpy()
+    np.testing.assert_allclose(om.final_logits(h, head, dims), torch_logits(h, head, dims), rtol=1e-11, atol=1e-12)
+
+
+def test_final_logits_closed_form_constant_row():
+    # a row of constant c normalises to c / sqrt(c^2 + eps) in every column,
+    # so its logits are that factor times lm_head @ gain
+    dims = small_dims()
+    _, head, _ = np_layers(22, dims)
+    head = _head_with_gain(head, dims, 22)
+    for c in (-2.5, 0.01, 7.0):
+        got = om.final_logits(np.full((1, dims.hidden), c), head, dims)[0]
+        want = c / math.sqrt(c * c + dims.rms_eps) * (head["lm_head"] @ head["final_norm"])
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
+
+
+def _logits_pin_holds(parts, hidden, logits, head, dims):
+    """The hybrid step's logits are the library composition on each part's
+    last stacked row; the rows are counted here from the parts' own lengths."""
+    rows, r = [], 0
+    for p in parts:
+        r += (p.end - p.lo)
+        rows.append(r - 1)
+    want = torch_logits(hidden[-1][rows], head, dims)
+    return logits.shape == want.shape and np.allclose(logits, want, rtol=1e-10, atol=1e-11)
+
+
+@pytest.mark.parametrize("with_given", [False, True])
+def test_hybrid_logits_are_last_row_of_each_part(with_given):
+    dims = small_dims(layers=2)
+    layers, head, gen = np_layers(23, dims)
+    head = _head_with_gain(head, dims, 23)
+    parts = _parts_for(dims, layers, gen, with_given)
+    hyb, lg = om.hybrid_step(layers, head, dims, parts)
+    assert lg.shape == (len(parts), dims.vocab)
+    assert _logits_pin_holds(parts, hyb, lg, head, dims)
+
+
+def test_planted_head_mistakes_are_caught(monkeypatch):
+    """Each planted mistake in the oracle's head breaks one of the pins above."""
+    dims = small_dims(layers=2)
+    layers, head, gen = np_layers(24, dims)
+    head = _head_with_gain(head, dims, 24)
+    parts = _parts_for(dims, layers, gen, False)
+    h = 3.0 * synth.normal(gen, (5, dims.hidden)).double().numpy()
+    # the final norm dropped
+    with monkeypatch.context() as m:
+        m.setattr(om, "final_logits", lambda rows, hd, d: rows @ hd["lm_head"].T)
+        assert not np.allclose(om.final_logits(h, head, dims), torch_logits(h, head, dims), rtol=1e-6)
+        hyb, lg = om.hybrid_step(layers, head, dims, parts)
+        assert not _logits_pin_holds(parts, hyb, lg, head, dims)
+    # the gain dropped from the final norm
+    with monkeypatch.context() as m:
+        m.setattr(om, "final_logits",
+                  lambda rows, hd, d: om.rms_norm(rows, np.ones(d.hidden), d.rms_eps) @ hd["lm_head"].T)
+        assert not np.allclose(om.final_logits(h, head, dims), torch_logits(h, head, dims), rtol=1e-6)
+    # the chunk's first row sampled instead of its last
+    with monkeypatch.context() as m:
+        m.setattr(om, "sampled_rows", lambda ps: np.cumsum([0] + [p.n_rows for p in ps])[:-1])
+        hyb, lg = om.hybrid_step(layers, head, dims, parts)
+        assert not _logits_pin_holds(parts, hyb, lg, head, dims)
+    # unpatched, every pin holds
+    hyb, lg = om.hybrid_step(layers, head, dims, parts)
+    assert _logits_pin_holds(parts, hyb, lg, head, dims)
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _mutant_cases():
