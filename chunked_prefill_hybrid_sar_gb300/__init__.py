@@ -18,6 +18,7 @@ from ._lib import (SAR_EPI_F32, SAR_EPI_RESIDUAL, SAR_EPI_STORE, SAR_EPI_SWIGLU,
                    SarError, check, lib)
 
 __all__ = ["Model", "KVCache", "Scheduler", "Batch", "StepGraph", "SarError", "lib", "check", "gemm", "rmsnorm",
+           "op_sync_status", "op_wait_check",
            "launch_count", "KERNEL_KINDS", "SAR_IN_HIDDEN", "SAR_IN_TOKENS", "SAR_STORAGE_F16",
            "SAR_STORAGE_BF16", "storage_dtype"]
 
@@ -335,6 +336,17 @@ def gemm(a, w, c, residual=None, epilogue=SAR_EPI_STORE, variant=SAR_GEMM_AUTO, 
     N = w.shape[0]
     check(lib().sar_op_gemm(_ptr(a), _ptr(w), _ptr(c), _ptr(residual), M, N, K, epilogue, variant,
                             _storage_of(a), _stream(stream)))
+
+
+def op_sync_status() -> None:
+    """Synchronise the device and raise if a single-kernel entry point's
+    kernel recorded a failure (timeout or bounds) since the last call."""
+    check(lib().sar_op_sync_status())
+
+
+def op_wait_check(limit_ns: int, arrivals: int, stream=None) -> None:
+    """Run the bounded-wait check kernel (see ``sar_op_wait_check``)."""
+    check(lib().sar_op_wait_check(int(limit_ns), int(arrivals), _stream(stream)))
 
 
 def rmsnorm(x, gain, y, eps: float, stream=None) -> None:

@@ -31,6 +31,7 @@ SAR_EPI_STORE, SAR_EPI_RESIDUAL, SAR_EPI_SWIGLU, SAR_EPI_F32 = 0, 1, 2, 3
 SAR_GEMM_AUTO, SAR_GEMM_M128_N128, SAR_GEMM_M128_N256, SAR_GEMM_SWAP, SAR_GEMM_M256_N128 = 0, 1, 2, 3, 4
 SAR_GEMM_PAIR_N256, SAR_GEMM_PAIR_N128, SAR_GEMM_PAIR_N192 = 5, 6, 7
 SAR_GEMM_TWO_CTAS = 0x1000
+SAR_Q_F32 = 0x100
 SAR_GEMM_STREAM_K = 0x2000
 
 KERNEL_KINDS = ("embed", "rmsnorm", "gemm_qkv", "rope_append", "chunk_attn", "decode_attn", "gemm_o",
@@ -106,6 +107,8 @@ SIGNATURES = {
     "sar_sched_destroy": (i32, [vp]),
     "sar_op_gemm": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
     "sar_op_rmsnorm": (i32, [vp, vp, vp, i32, i32, ctypes.c_float, i32, vp]),
+    "sar_op_sync_status": (i32, []),
+    "sar_op_wait_check": (i32, [i64, i32, vp]),
     "sar_plan_inspect": (i32, [ctypes.POINTER(sar_dims), i32, i32, i32, i32, ctypes.POINTER(sar_batch), P_i32,
                                P_i32, i64, ctypes.POINTER(i64)]),
     "sar_model_debug_buffer": (i32, [vp, i32, ctypes.POINTER(vp)]),

@@ -261,12 +261,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_kernel(ChunkAttnArgs a
 template <typename T, int D>
 int launch_impl(const ChunkAttnArgs& a, cudaStream_t s) {
   const size_t smem = (size_t)2 * kBQ * D * 2 + (size_t)2 * 2 * kBKV * D * 2;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_attn_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_error(e, "chunk attention attribute");
-    attr = true;
-  }
+  const int arc = ensure_smem_attr(reinterpret_cast<const void*>(&chunk_attn_kernel<T, D>), (int)smem,
+                                   "chunk attention attribute");
+  if (arc != SAR_OK) return arc;
   dim3 grid(a.n_tiles, a.qh);
   cudaError_t e = launch_pdl(chunk_attn_kernel<T, D>, grid, dim3(kThreads), smem, s, a);
   if (e != cudaSuccess) return cuda_error(e, "chunk attention launch");

@@ -474,12 +474,9 @@ __global__ void chunk_combine_kernel(const float* __restrict__ partials, const i
 
 template <typename T>
 int launch_t(const ChunkAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_attn_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return cuda_error(e, "chunk attention (tcgen05) attribute");
-    attr = true;
-  }
+  const int arc = ensure_smem_attr(reinterpret_cast<const void*>(&chunk_attn_tc_kernel<T>), kSmem,
+                                   "chunk attention (tcgen05) attribute");
+  if (arc != SAR_OK) return arc;
   const dim3 grid(a.n_tiles, a.qh);
   cudaError_t e = launch_pdl(chunk_attn_tc_kernel<T>, grid, dim3(kThreads), (size_t)kSmem, s, tmk, tmv, a);
   if (e != cudaSuccess) return cuda_error(e, "chunk attention (tcgen05) launch");

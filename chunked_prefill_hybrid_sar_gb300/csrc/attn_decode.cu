@@ -395,13 +395,9 @@ template <typename T, int D, bool COMPUTED = false>
 int launch_impl(const DecodeAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t s) {
   constexpr int STAGE_BYTES = 2 * (D / 64) * kBlockKeys * 128;
   const size_t smem = 1024 + (size_t)kWarps * kStages * STAGE_BYTES + (size_t)kWarps * kStages * 8;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<T, D, COMPUTED>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_error(e, "decode attention attribute");
-    attr = true;
-  }
+  const int arc = ensure_smem_attr(reinterpret_cast<const void*>(&decode_attn_kernel<T, D, COMPUTED>), (int)smem,
+                                   "decode attention attribute");
+  if (arc != SAR_OK) return arc;
   const int n_ctas = COMPUTED ? a.n_decode * a.max_splits : a.n_items;
   const dim3 grid = COMPUTED ? dim3(n_ctas, a.kvh) : dim3(n_ctas * a.kvh);
   launch_pdl(decode_attn_kernel<T, D, COMPUTED>, grid, dim3(kWarps * 32), smem, s, tmk, tmv, a);
@@ -485,6 +481,8 @@ extern "C" int sar_decode_attention_noalloc(const void* q, int32_t q_stride, con
   if (n_decode <= 0 || max_ctx < 0 || num_pages <= 0 || bt_stride <= 0 || n_kv_heads <= 0 || page_size <= 0 ||
       n_q_heads % n_kv_heads || (int64_t)(max_ctx / page_size + 1) > bt_stride)
     return set_error(SAR_ERR_INVALID_ARG, "decode_attention_noalloc: bad sizes or block table too short");
+  const bool q_f32 = (storage & SAR_Q_F32) != 0;  // query rows in fp32 (q_stride in floats)
+  storage &= ~SAR_Q_F32;
   if ((head_dim != 64 && head_dim != 128) || page_size % kBlockKeys || n_q_heads / n_kv_heads > 8 ||
       q_stride < n_q_heads * head_dim || out_stride < n_q_heads * head_dim)
     return set_error(SAR_ERR_UNSUPPORTED, "decode_attention_noalloc: shape not supported");
@@ -519,6 +517,10 @@ extern "C" int sar_decode_attention_noalloc(const void* q, int32_t q_stride, con
   }
   DecodeAttnArgs a{};
   a.qkv = q;
+  if (q_f32) {
+    a.q32 = static_cast<const float*>(q);
+    a.ld32 = q_stride;
+  }
   a.out = out;
   a.k_cache = k_pages;
   a.v_cache = v_pages;

@@ -26,10 +26,12 @@ enum ErrSite {
   SITE_CHUNK_PIPE = 21,
   SITE_ROPE_BOUNDS = 30,
   SITE_EMBED_BOUNDS = 40,
+  SITE_WAIT_CHECK = 50,
 };
 
 // A wait that has not finished after this long gives up (normal waits take
-// microseconds; a stuck pipeline must return rather than hold the GPU).
+// microseconds; a stuck pipeline must return rather than hold the GPU).  The
+// step's kernels use this default; mbar_wait takes the limit as an argument.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ void report(int* err, int code, int site, int detail) {
@@ -121,15 +123,17 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs, records SAR_ERR_TIMEOUT and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err, int site) {
+// limit_ns (about; checked every 32 tries), records SAR_ERR_TIMEOUT at `site`
+// and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err, int site,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try(bar, parity)) return true;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       report(err, SAR_ERR_TIMEOUT, site, (int)parity);
       return false;
     }

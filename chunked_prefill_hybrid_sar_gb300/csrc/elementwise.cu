@@ -504,4 +504,25 @@ int launch_argmax(const float* logits, int rows, int vocab, int32_t* out, cudaSt
   return cuda_error(cudaGetLastError(), "argmax launch");
 }
 
+// The bounded-wait path on its own: one thread initialises a barrier that
+// expects two arrivals, arrives `arrivals` times and waits for the phase with
+// mbar_wait's limit set to `limit_ns`.  With fewer than two arrivals the phase
+// never completes, so the wait runs out, records SAR_ERR_TIMEOUT in `err` and
+// the kernel returns; nothing else is in flight.
+__global__ void wait_check_kernel(uint64_t limit_ns, int arrivals, int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 2);
+  fence_mbar_init();
+  for (int i = 0; i < arrivals; ++i) mbar_arrive(b);
+  mbar_wait(b, 0, err, SITE_WAIT_CHECK, limit_ns);
+}
+
+int launch_wait_check(uint64_t limit_ns, int arrivals, int* err, cudaStream_t s) {
+  wait_check_kernel<<<1, 32, 0, s>>>(limit_ns, arrivals, err);
+  count_launches(1);
+  return cuda_error(cudaGetLastError(), "wait check launch");
+}
+
 }  // namespace sar

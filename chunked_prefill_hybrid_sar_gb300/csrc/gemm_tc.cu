@@ -1088,13 +1088,7 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
       cfg.bn % (8 * cfg.cl) || (cfg.pair && (cfg.msub != 1 || cfg.swap)) ||
       cfg.stage_bytes != cfg.msub * kTileA + (cfg.pair ? cfg.bn / 2 : cfg.bn) * kBK * 2)
     return set_error(SAR_ERR_INVALID_ARG, "gemm: inconsistent cluster configuration");
-  static bool attr_done[2][5][2][3][2] = {};
-  bool& done = attr_done[storage == SAR_STORAGE_BF16][epi][cfg.swap][cfg.msub][cfg.pair];
-  if (!done) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    if (e != cudaSuccess) return cuda_error(e, "gemm: set smem attribute");
-    done = true;
-  }
+  SAR_TRY(ensure_smem_attr(fn, kSmemLimit, "gemm: set smem attribute"));
   const CUtensorMap& ta = cfg.swap ? w_map : act_map;
   const CUtensorMap& tb = cfg.swap ? act_map : w_map;
   void* args[] = {const_cast<CUtensorMap*>(&ta), const_cast<CUtensorMap*>(&tb), &tc_map, &p};
@@ -1116,17 +1110,12 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
     lc.numAttrs = 2;
     // persistent grid: as many whole clusters as can be resident at once (the
     // SMs of a GPC need not divide into clusters evenly)
-    static int max_clusters[2][5][3][5][2][2] = {};
-    int& mc = max_clusters[storage == SAR_STORAGE_BF16][epi][cfg.msub][cfg.cl][cfg.bn == 256][cfg.pair];
-    if (mc == 0) {
-      cudaLaunchConfig_t qc = lc;  // the cluster shape alone
-      qc.gridDim = dim3(cfg.cl * 64);
-      qc.attrs = &attr[1];
-      qc.numAttrs = 1;
-      cudaError_t e = cudaOccupancyMaxActiveClusters(&mc, fn, &qc);
-      if (e != cudaSuccess || mc < 1) return cuda_error(e != cudaSuccess ? e : cudaErrorInvalidConfiguration,
-                                                         "gemm: cluster occupancy");
-    }
+    cudaLaunchConfig_t qc = lc;  // the cluster shape alone
+    qc.gridDim = dim3(cfg.cl * 64);
+    qc.attrs = &attr[1];
+    qc.numAttrs = 1;
+    int mc = 0;
+    SAR_TRY(max_active_clusters(fn, qc, cfg.cl, &mc, "gemm: cluster occupancy"));
     // stream-K: every resident cluster takes a share
     grid = (cfg.sk ? mc : std::min(cfg.m_groups * cfg.n_tiles * cfg.splits, mc)) * cfg.cl;
     if (cfg.sk && mc < cfg.m_groups)

@@ -12,6 +12,13 @@
 #include "../../include/sar.h"
 #include "../../include/sar_ops.h"
 
+// Returns the status of `x` from the enclosing function unless it is SAR_OK.
+#define SAR_TRY(x)                  \
+  do {                              \
+    int _rc = (x);                  \
+    if (_rc != SAR_OK) return _rc;  \
+  } while (0)
+
 namespace sar {
 
 // ---- errors / bookkeeping (api.cpp) ----------------------------------------
@@ -19,6 +26,15 @@ int set_error(int code, const std::string& msg);
 int cuda_error(cudaError_t e, const char* what);
 void count_launches(int64_t n);
 int num_sms();
+// Raises kernel `fn`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device): the attribute belongs to the device's
+// context, so a process that drives several devices (or threads that race
+// a first call) sets it on each.  Thread-safe.
+int ensure_smem_attr(const void* fn, int bytes, const char* what);
+// Resident clusters of `fn` for the launch shape `qc` (cluster attribute
+// included) on the current device, computed once per (kernel, cluster size,
+// device).  Thread-safe.
+int max_active_clusters(const void* fn, const cudaLaunchConfig_t& qc, int cl, int* out, const char* what);
 
 // Kernels of a step are launched with programmatic stream serialisation: the
 // next kernel's CTAs may become resident while the previous kernel drains and
@@ -112,6 +128,9 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
 // ---- elementwise kernels (elementwise.cu) ----------------------------------
 // x: fp32 residual rows; y: storage-type rows; row_index (optional) gathers rows.
 // zero (optional): zero_n floats to clear, split over the blocks.
+// One-thread kernel whose barrier completes only with two arrivals; it
+// arrives `arrivals` times and waits with a limit of limit_ns.
+int launch_wait_check(uint64_t limit_ns, int arrivals, int* err, cudaStream_t s);
 int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hidden, float eps,
                    const int32_t* row_index, int storage, cudaStream_t s, float* zero = nullptr,
                    size_t zero_n = 0);

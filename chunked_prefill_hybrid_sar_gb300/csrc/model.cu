@@ -18,6 +18,8 @@
 #include <array>
 #include <cmath>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -109,11 +111,28 @@ namespace {
 
 int check(cudaError_t e, const char* what) { return cuda_error(e, what); }
 
-#define SAR_TRY(x)                  \
-  do {                              \
-    int _rc = (x);                  \
-    if (_rc != SAR_OK) return _rc;  \
-  } while (0)
+// The device error record [code, site, detail, 0] of the single-kernel entry
+// points on the current device, allocated (and zeroed) at its first use there.
+std::mutex g_op_flags_mu;
+std::map<int, int*> g_op_flags;
+int op_flags(int** out) {
+  int dev = 0;
+  SAR_TRY(check(cudaGetDevice(&dev), "op flags: current device"));
+  std::lock_guard<std::mutex> lk(g_op_flags_mu);
+  int*& f = g_op_flags[dev];
+  if (!f) {
+    int* p = nullptr;
+    SAR_TRY(check(cudaMalloc(&p, 16), "op flags: allocate"));
+    const int rc = check(cudaMemset(p, 0, 16), "op flags: clear");
+    if (rc != SAR_OK) {
+      cudaFree(p);
+      return rc;
+    }
+    f = p;
+  }
+  *out = f;
+  return SAR_OK;
+}
 
 // ---- profiling helpers -----------------------------------------------------
 EventPair* prof_begin(sar_model* m, int kind, cudaStream_t s) {
@@ -1015,17 +1034,34 @@ int sar_op_gemm(const void* a, const void* w, void* c, const void* residual, int
   if (!a || !w || !c) return set_error(SAR_ERR_INVALID_ARG, "op_gemm: null pointer");
   if (epilogue < SAR_EPI_STORE || epilogue > SAR_EPI_F32) return set_error(SAR_ERR_INVALID_ARG, "op_gemm: bad epilogue");
   if (storage != SAR_STORAGE_F16 && storage != SAR_STORAGE_BF16) return set_error(SAR_ERR_INVALID_ARG, "op_gemm: bad storage");
-  static int* err = nullptr;
-  if (!err) {
-    SAR_TRY(check(cudaMalloc(&err, 16), "op_gemm: flag buffer"));
-    SAR_TRY(check(cudaMemset(err, 0, 16), "op_gemm: flag buffer"));
-  }
+  int* err = nullptr;
+  SAR_TRY(op_flags(&err));
   sar::GemmCfg cfg;
   SAR_TRY(sar::gemm_config(M, N, K, epilogue, variant, &cfg, epilogue == SAR_EPI_RESIDUAL && c == residual));
   CUtensorMap amap, wmap;
   SAR_TRY(sar::make_tmap_16(&amap, a, M, K, cfg.swap ? cfg.b_box_rows : cfg.a_box_rows, storage));
   SAR_TRY(sar::make_tmap_16(&wmap, w, N, K, cfg.swap ? cfg.a_box_rows : cfg.b_box_rows, storage));
   return sar::gemm_launch(cfg, amap, wmap, M, N, K, epilogue, storage, c, residual, err, static_cast<cudaStream_t>(stream));
+}
+
+int sar_op_wait_check(int64_t limit_ns, int32_t arrivals, void* stream) {
+  if (limit_ns <= 0 || arrivals < 0 || arrivals > 2) return set_error(SAR_ERR_INVALID_ARG, "op_wait_check: bad argument");
+  int* err = nullptr;
+  SAR_TRY(op_flags(&err));
+  return sar::launch_wait_check((uint64_t)limit_ns, arrivals, err, static_cast<cudaStream_t>(stream));
+}
+
+int sar_op_sync_status(void) {
+  int* err = nullptr;
+  SAR_TRY(op_flags(&err));
+  int h[4] = {0, 0, 0, 0};
+  SAR_TRY(check(cudaDeviceSynchronize(), "op_sync_status: device synchronise"));
+  SAR_TRY(check(cudaMemcpy(h, err, 16, cudaMemcpyDeviceToHost), "op_sync_status: read flags"));
+  SAR_TRY(check(cudaMemset(err, 0, 16), "op_sync_status: clear flags"));
+  if (h[0] != 0)
+    return set_error(h[0], "device flag: code " + std::to_string(h[0]) + " at site " + std::to_string(h[1]) +
+                               " (detail " + std::to_string(h[2]) + ")");
+  return SAR_OK;
 }
 
 int sar_plan_inspect(const sar_dims* dims, int32_t page_size, int32_t num_pages, int32_t sms, int32_t chunk_split,

@@ -279,8 +279,13 @@ int sar_sample_greedy(sar_model* m, const float* logits, int32_t rows, int32_t* 
  *   ctx_lens     device int32 [n_decode]; max_ctx (host) bounds them
  *   block_tables device int32 [n_decode][bt_stride], row b = decode b's pages in order
  *   out          device rows of the storage type, row b at out + b*out_stride
- *   storage      SAR_STORAGE_F16 or SAR_STORAGE_BF16 (q, pages and out)
- *   err_flag     device int32[4] or NULL: first device-side failure (code, site, detail)
+ *   storage      SAR_STORAGE_F16 or SAR_STORAGE_BF16 (pages and out; q too,
+ *                unless SAR_Q_F32 is OR-ed in: then q rows are fp32 and
+ *                q_stride counts floats, as the step's own fp32 queries are)
+ *   err_flag     device int32[4] or NULL: first device-side failure (code, site, detail).
+ *                A decode whose ctx_lens[b] + 1 exceeds what max_ctx planned
+ *                for is skipped and its out rows are left as they were; only
+ *                err_flag (SAR_ERR_BOUNDS) tells, so pass one.
  * The first call on a device looks up the array's device address with that
  * device current; make that first call before any stream capture.  Calls
  * share the array and keep its last contents (every partial is written before
@@ -290,6 +295,7 @@ int sar_sample_greedy(sar_model* m, const float* logits, int32_t rows, int32_t* 
  * n_decode * ceil((max_ctx+1)/split) * n_q_heads * (head_dim+2) * 4 bytes, fit
  * in 8 MiB; when none does the call returns SAR_ERR_INVALID_ARG before any
  * launch. */
+enum { SAR_Q_F32 = 0x100 };
 int sar_decode_attention_noalloc(const void* q, int32_t q_stride, const void* k_pages,
                                  const void* v_pages, int32_t num_pages, int32_t page_size,
                                  int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,

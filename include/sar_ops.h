@@ -69,6 +69,25 @@ enum {
 int sar_op_gemm(const void* a, const void* w, void* c, const void* residual, int32_t M, int32_t N,
                 int32_t K, int32_t epilogue, int32_t variant, int32_t storage, void* stream);
 
+/* Device-side status of the single-kernel entry points (sar_op_gemm,
+ * sar_op_wait_check) on the current device.  Their kernels record the first
+ * failure -- a bounded wait that gave up (SAR_ERR_TIMEOUT) or an index out of
+ * bounds (SAR_ERR_BOUNDS) -- in one record per device instead of trapping.
+ * This call synchronises the device, reads the record, clears it and returns
+ * its code (SAR_OK if none); sar_last_error() then names the kernel site and
+ * a detail.  The record is shared by every stream and thread on the device. */
+int sar_op_sync_status(void);
+
+/* Exercises the bounded wait that every pipelined kernel uses (no counterpart
+ * in the pages; the bound keeps a stuck pipeline from holding the GPU).  One
+ * thread initialises a shared-memory barrier that needs two arrivals, arrives
+ * `arrivals` times (0..2) and waits for it with a limit of limit_ns
+ * nanoseconds (> 0).  With two arrivals the wait completes; with fewer it
+ * runs out after about limit_ns, the kernel records SAR_ERR_TIMEOUT for
+ * sar_op_sync_status() and returns, and the context stays usable.  Async on
+ * `stream`. */
+int sar_op_wait_check(int64_t limit_ns, int32_t arrivals, void* stream);
+
 /* y = x * rsqrt(mean(x^2) + eps) * gain per row: x fp32 [rows, hidden] (the
  * residual stream), gain fp32 [hidden], y [rows, hidden] in `storage`. */
 int sar_op_rmsnorm(const void* x, const void* gain, void* y, int32_t rows, int32_t hidden,

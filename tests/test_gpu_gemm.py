@@ -15,6 +15,15 @@ DEV = "cuda"
 DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16}
 
 
+@pytest.fixture(autouse=True)
+def no_device_flags():
+    """Every GEMM test ends with the kernels' device status read back: a
+    bounded wait that gave up or a bounds check that fired fails the test."""
+    sar.op_sync_status()
+    yield
+    sar.op_sync_status()
+
+
 def operands(M, N, K, seed=0, dtype=torch.float16):
     g = synth.generator(seed)
     a = synth.normal(g, (M, K), dtype=torch.bfloat16).to(dtype)

@@ -47,6 +47,9 @@ def test_invalid_arguments_are_rejected_with_a_message():
     assert b"tile" in lib.sar_last_error()
     assert lib.sar_model_create(None, ctypes.byref(h)) == _lib.SAR_ERR_INVALID_ARG
     assert lib.sar_step(None, None, None, None, None, None, None, None) == _lib.SAR_ERR_INVALID_ARG
+    # argument checks come before any device work
+    assert lib.sar_op_wait_check(0, 1, None) == _lib.SAR_ERR_INVALID_ARG
+    assert lib.sar_op_wait_check(1000, 3, None) == _lib.SAR_ERR_INVALID_ARG
 
 
 def test_launch_counter_starts_without_gpu_work():
