@@ -156,7 +156,7 @@ def peaks():
 
 # ------------------------------------------------------------------ our arm
 
-def setup_gpu(seed=0):
+def setup_gpu(seed=0, storage=None):
     import torch
 
     import chunked_prefill_hybrid_sar_gb300 as sar
@@ -166,7 +166,8 @@ def setup_gpu(seed=0):
     gen = synth.generator(seed, "cuda")
     layers = [synth.layer_weights(gen, dims, torch.bfloat16, "cuda")]
     head = synth.head_weights(gen, dims, torch.bfloat16, "cuda")
-    m = harness.load_model(dims, layers, head, max_tokens=TAU, max_decodes=BD)
+    m = harness.load_model(dims, layers, head, max_tokens=TAU, max_decodes=BD,
+                           storage=sar.SAR_STORAGE_F16 if storage is None else storage)
     del layers, head
     cg = synth.generator(seed + 1)
     ctxs = synth.uniform_int(cg, BD, 128, 4096)
@@ -201,6 +202,70 @@ def decode_attention_bytes(dims, ctxs):
     kv = sum(c + 1 for c in ctxs) * dims.n_kv_heads * dims.head_dim * 2 * 2
     qo = len(ctxs) * dims.q_dim * 2 * 2
     return kv + qo
+
+
+def chunk_attention_flops(dims, lp, start):
+    """Algorithmic flops of the chunk's causal attention: each query at
+    position start + i scores and sums start + i + 1 keys (2 d flops each for
+    q.k and for p.v) in every query head."""
+    keys = lp * start + lp * (lp + 1) // 2
+    return 4 * dims.head_dim * dims.n_q_heads * keys
+
+
+# DRAM bytes read + written per launch (dram__bytes_read.sum +
+# dram__bytes_write.sum) from one ncu capture on this workload, with the
+# source files of the kernel they were taken on and those files' SHA-256
+# prefix: a figure whose kernel source has changed since is reported as null.
+TRAFFIC = {
+    "decode_attn": {"bytes": 526.4e6, "files": ("csrc/attn_decode.cu",), "sha": "",
+                    "capture": "profiles/decode_attn_mistral_layer.md"},
+}
+
+
+def source_sha(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "chunked_prefill_hybrid_sar_gb300", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_of(kernel):
+    t = TRAFFIC.get(kernel)
+    if not t:
+        return None, "no capture of this kernel"
+    cur = source_sha(t["files"])
+    if cur != t["sha"]:
+        return None, f"kernel source changed since the capture in {t['capture']} (sha {cur})"
+    return t["bytes"], f"ncu capture, {t['capture']} (kernel source sha {cur})"
+
+
+def step_roofline(dims, ctxs, hbm, tf):
+    """Per-operator max(T_math, T_mem) summed over the step, and the
+    concurrent-overlap bound max(sum T_math, sum T_mem), at peaks (hbm GB/s,
+    tf TFLOP/s).  Chunk attention is averaged over the three chunk starts."""
+    wb = 2 * dims.hidden
+    lp = TAU - BD
+    ops = {  # name: (flops, bytes)
+        "gemm_qkv": (gemm_flops(dims, TAU)["gemm_qkv"], wb * (dims.q_dim + 2 * dims.kv_dim) + TAU * wb),
+        "gemm_o": (gemm_flops(dims, TAU)["gemm_o"], wb * dims.q_dim + TAU * dims.q_dim * 2 + TAU * dims.hidden * 8),
+        "gemm_gateup": (gemm_flops(dims, TAU)["gemm_gateup"], wb * 2 * dims.ffn + TAU * wb + TAU * dims.ffn * 2),
+        "gemm_down": (gemm_flops(dims, TAU)["gemm_down"], 2 * dims.ffn * dims.hidden + TAU * dims.ffn * 2
+                      + TAU * dims.hidden * 8),
+        "chunk_attn": (sum(chunk_attention_flops(dims, lp, s) for s in STARTS) / len(STARTS),
+                       sum((s + lp) for s in STARTS) / len(STARTS) * dims.kv_dim * 2 * 2),
+        "decode_attn": (sum(4 * dims.head_dim * dims.n_q_heads * (c + 1) for c in ctxs),
+                        decode_attention_bytes(dims, ctxs)),
+        "gemm_head": (2 * (BD + 1) * dims.hidden * dims.vocab, dims.vocab * dims.hidden * 2),
+        # four row passes: input + first norm, second norm, final norm (sampled rows), each reading
+        # fp32 rows and writing 16-bit rows; counted as full passes over the stacked rows
+        "norms": (0, 3 * TAU * dims.hidden * (4 + 2)),
+    }
+    t = {k: max(f / (tf * 1e12), b / (hbm * 1e9)) for k, (f, b) in ops.items()}
+    t_math = sum(f for f, _ in ops.values()) / (tf * 1e12)
+    t_mem = sum(b for _, b in ops.values()) / (hbm * 1e9)
+    return sum(t.values()), max(t_math, t_mem), t, t_math, t_mem
 
 
 def gemm_flops(dims, rows):
@@ -299,32 +364,34 @@ def run_ours(args):
     if "gemm_head" in kernels:
         kernels["gemm_head"]["gbs"] = head_bytes / (kernels["gemm_head"]["ms_per_launch"] * 1e-3) / 1e9
     dom = max(kernels, key=lambda k: kernels[k]["share"])
-    # DRAM bytes read + written per launch (dram__bytes_read.sum +
-    # dram__bytes_write.sum) from one ncu capture of the current kernels on this
-    # workload; decode attention counts both of its kernels
-    traffic = {"decode_attn": 526.4e6, "gemm_gateup": 256.2e6}.get(dom)
+    traffic, traffic_src = traffic_of(dom)
+    # the timed region lasts milliseconds at full clocks: the burst peak applies
     if dom in flops:
         ach = kernels[dom]["tflops"]
-        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": tf_sust, "unit": "TFLOP/s",
-                "frac": ach / tf_sust, "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 sustained", "algorithmic_per_launch": flops[dom]}
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": tf_burst, "unit": "TFLOP/s",
+                "frac": ach / tf_burst, "traffic": traffic, "traffic_source": traffic_src,
+                "peak_source": f"{peak_src} bf16 burst", "algorithmic_per_launch": flops[dom]}
     else:
         byts = dab if dom == "decode_attn" else head_bytes
         ach = byts / (kernels[dom]["ms_per_launch"] * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-                "frac": ach / hbm, "traffic": traffic, "peak_source": f"{peak_src} HBM copy",
-                "algorithmic_per_launch": byts}
+                "frac": ach / hbm, "traffic": traffic, "traffic_source": traffic_src,
+                "peak_source": f"{peak_src} HBM copy", "algorithmic_per_launch": byts}
 
-    # step roofline: sum over operators of max(T_math, T_mem), measured peaks
-    def op_t(fl, by):
-        return max(fl / (tf_sust * 1e12), by / (hbm * 1e9))
-    wb = 2 * dims.hidden
-    t_roof = (op_t(flops["gemm_qkv"], wb * (dims.q_dim + 2 * dims.kv_dim) + TAU * wb * 2)
-              + op_t(flops["gemm_o"], wb * dims.q_dim)
-              + op_t(flops["gemm_gateup"], wb * 2 * dims.ffn)
-              + op_t(flops["gemm_down"], 2 * dims.ffn * dims.hidden)
-              + op_t(0, dab) + op_t(2 * (BD + 1) * dims.hidden * dims.vocab, head_bytes)
-              + 4 * op_t(0, TAU * wb * 2))
+    # step roofline: per-operator max(T_math, T_mem) summed, and the overlap
+    # bound, at the burst peak (the timed region is milliseconds long at full
+    # clocks) and at the sustained one
+    step_ms = ms / args.steps
+    t_roof, t_overlap, t_ops, t_math, t_mem = step_roofline(dims, ctxs, hbm, tf_burst)
+    t_roof_s, t_overlap_s, _, _, _ = step_roofline(dims, ctxs, hbm, tf_sust)
+    roof_step = {"per_op_sum_ms": t_roof * 1e3, "per_op_frac": t_roof * 1e3 / step_ms,
+                 "overlap_bound_ms": t_overlap * 1e3, "overlap_frac": t_overlap * 1e3 / step_ms,
+                 "sum_t_math_ms": t_math * 1e3, "sum_t_mem_ms": t_mem * 1e3,
+                 "per_op_ms": {k: v * 1e3 for k, v in t_ops.items()},
+                 "peaks": f"{peak_src}: bf16 burst {tf_burst} TFLOP/s, HBM {hbm} GB/s",
+                 "sustained_peak": {"per_op_sum_ms": t_roof_s * 1e3, "per_op_frac": t_roof_s * 1e3 / step_ms,
+                                    "overlap_bound_ms": t_overlap_s * 1e3,
+                                    "overlap_frac": t_overlap_s * 1e3 / step_ms, "tflops": tf_sust}}
 
     # end to end: host buffers through the host entry points, one step at a
     # time (each step's input rows in from pinned memory, its result back,
@@ -357,19 +424,45 @@ def run_ours(args):
     def tokens_step(i):
         graph_set[i % 3].launch_host_tokens(pin_in[i % 3], h_tok)
 
+    def replanned_tokens_step(i):
+        # the serving loop's step: plan the batch on the host and re-point the
+        # captured graph at it (sar_graph_update), then run it with host buffers
+        graph_set[i % 3].update(cases[i % 3][0])
+        graph_set[i % 3].launch_host_tokens(pin_in[i % 3], h_tok)
+
+    def planned_logits_step(i):
+        m.step_host(kv, cases[i % 3][0], pin_in[i % 3], logits_out=h_log)
+
+    h2d = TAU * dims.hidden * 2
     e2e_log_s = e2e_run(logits_step)
     e2e_logits = {"value": whole_job_rate(TAU * args.steps, world, e2e_log_s), "unit": UNIT,
-                  "h2d_bytes_per_step": TAU * dims.hidden * 2,
-                  "d2h_bytes_per_step": (BD + 1) * dims.vocab * 4,
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": (BD + 1) * dims.vocab * 4,
                   "api": "sar_graph_launch_host" if graph_set else "sar_step_host"}
+    e2e_eager_s = e2e_run(planned_logits_step)
+    e2e_eager = {"value": whole_job_rate(TAU * args.steps, world, e2e_eager_s), "unit": UNIT,
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": (BD + 1) * dims.vocab * 4,
+                 "api": "sar_step_host (host planning, kernel-by-kernel launch, logits back)"}
+    e2e_fixed = None
     if graph_set:
-        e2e_s = e2e_run(tokens_step)
+        e2e_s = e2e_run(replanned_tokens_step)
         e2e = {"value": whole_job_rate(TAU * args.steps, world, e2e_s), "unit": UNIT,
-               "h2d_bytes_per_step": TAU * dims.hidden * 2,
-               "d2h_bytes_per_step": (BD + 1) * 4,
-               "api": "sar_graph_launch_host_tokens (greedy token ids of the 65 sampled rows back)"}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": (BD + 1) * 4,
+               "api": "sar_graph_update (the step planned on the host) + sar_graph_launch_host_tokens "
+                      "(greedy token ids of the 65 sampled rows back)"}
+        e2e_fixed_s = e2e_run(tokens_step)
+        e2e_fixed = {"value": whole_job_rate(TAU * args.steps, world, e2e_fixed_s), "unit": UNIT,
+                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": (BD + 1) * 4,
+                     "api": "sar_graph_launch_host_tokens without replanning"}
     else:
-        e2e = e2e_logits
+        e2e = e2e_eager
+
+    # the same workload with bf16 storage of weights, activations and KV
+    bf16 = None
+    if not args.no_bf16:
+        for g in graph_set or []:
+            g.close()
+        graph_set = None
+        bf16 = bf16_storage_line(args, world)
 
     out = None
     if rank == 0:
@@ -381,9 +474,11 @@ def run_ours(args):
                "data": "synthetic (seeded random-init weights and KV histories)",
                "config": dict(config_block(world), attn_streams=2 if args.overlap else 1,
                               launch="cuda graph per case" if args.graph else "kernel by kernel"),
-               "e2e": e2e, "e2e_logits_readback": e2e_logits, "gpu_launches": launches,
+               "e2e": e2e, "e2e_no_replan": e2e_fixed, "e2e_logits_readback": e2e_logits,
+               "e2e_eager_planned": e2e_eager, "gpu_launches": launches,
                "roofline": roof, "step_roofline_ms": t_roof * 1e3,
-               "step_roofline_frac": (t_roof * 1e3) / (ms / args.steps),
+               "step_roofline_frac": (t_roof * 1e3) / step_ms, "step_roofline": roof_step,
+               "bf16_storage": bf16,
                "kernels": kernels, "clocks": clk.summary(), "wall_s": wall, "cpu_baseline": cpu}
         print(json.dumps(out))
     if world > 1:
@@ -392,50 +487,133 @@ def run_ours(args):
     return out
 
 
+def bf16_storage_line(args, world):
+    """The step of the same workload on a model that stores weights,
+    activations and KV in bf16 (fp32 accumulation and residual), each case
+    replayed from its captured graph; device-timed like the main line."""
+    import torch
+
+    import chunked_prefill_hybrid_sar_gb300 as sar
+
+    dims, m, kv, cases, _ = setup_gpu(storage=sar.SAR_STORAGE_BF16)
+    hid = torch.empty(TAU, dims.hidden, dtype=torch.float32, device="cuda")
+    logits = torch.empty(BD + 1, dims.vocab, dtype=torch.float32, device="cuda")
+    graphs = [sar.StepGraph(m, kv, b, x, hidden_out=hid, logits_out=logits) for b, x in cases]
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        graphs[i % 3].launch()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        graphs[i % 3].launch()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    m.sync_status()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    for g in graphs:
+        g.close()
+    m.close()
+    kv.close()
+    return {"value": whole_job_rate(TAU * args.steps, world, ms / 1e3), "unit": UNIT,
+            "ms_per_step": ms / args.steps, "dtype": "bf16 storage, fp32 accumulate and residual",
+            "launch": "cuda graph per case",
+            "parity": "bf16 storage meets the per-layer bars on the tiny layer; on this layer bf16 "
+                      "rounding of the activations alone exceeds max-abs 3e-2, hence fp16 storage for the "
+                      "main line"}
+
+
 # ------------------------------------------------------------------ oracle arm
 
-def oracle_cases(seed=3):
+def oracle_cases(seed=3, dtype="float64"):
     """The workload's cases for the CPU oracle: per chunk start (0, 512,
     1536) one hybrid step of the 448-token chunk and all 64 decodes (contexts
     uniform in [128, 4096], random K/V histories), drawn by the same recipe
-    as the GPU cases with another seed.  Returns (dims, weights, head, the
+    as the GPU cases with another seed, as arrays of ``dtype`` (the oracle
+    computes in the type of its inputs).  Returns (dims, weights, head, the
     steps' parts, rows per step)."""
+    import numpy as np
+
     from oracle import model as om
 
+    dt = np.dtype(dtype)
     case = synth.mistral_layer_case(seed, n_decode=BD, tau=TAU, starts=synth.MISTRAL_STARTS)
     dims = case["dims"]
-    w = om.layer_weights_np(case["layers"][0])
-    head = om.layer_weights_np(case["head"])
+    w = om.layer_weights_np(case["layers"][0], dt)
+    head = om.layer_weights_np(case["head"], dt)
     decs = []
     for i, c in enumerate(case["ctxs"]):
         k, v = case["histories"][i]
-        decs.append(om.Part(x=om.to_np(case["decode_inputs"][i:i + 1]), lo=c,
-                            given=[om.LayerCache(om.to_np(k), om.to_np(v))]))
-    steps = [[om.Part(x=om.to_np(case["prompts"][s]), lo=s, is_prefill=True)] + decs
+        decs.append(om.Part(x=om.to_np(case["decode_inputs"][i:i + 1], dt), lo=c,
+                            given=[om.LayerCache(om.to_np(k, dt), om.to_np(v, dt))]))
+    steps = [[om.Part(x=om.to_np(case["prompts"][s], dt), lo=s, is_prefill=True)] + decs
              for s in synth.MISTRAL_STARTS]
     return dims, w, head, steps, case["lp"] + BD
 
 
-def oracle_sample_text(n_steps, dt):
-    return (f"{n_steps} oracle hybrid steps (float64 NumPy) of the workload itself, the chunk at start "
-            f"{'/'.join(str(s) for s in synth.MISTRAL_STARTS)} in turn with all {BD} decodes "
+def oracle_sample_text(n_steps, dt, dtype="float64"):
+    starts = synth.MISTRAL_STARTS[:min(n_steps, len(synth.MISTRAL_STARTS))]
+    return (f"{n_steps} oracle hybrid steps ({dtype} NumPy) of the workload itself, the chunk at start "
+            f"{'/'.join(str(s) for s in starts)} in turn with all {BD} decodes "
             f"({TAU} rows each; {dt:.1f} s; the oracle computes a chunk by running its prompt prefix)")
 
 
-def cpu_baseline(args):
+def oracle_leg(dtype="float64", min_s=10.0, max_passes=4):
+    """Times the oracle on the workload's cases in turn (start 0 first), whole
+    passes over the three cases until at least ``min_s`` seconds of work (at
+    most ``max_passes``); with ``max_passes`` 0, steps until ``min_s`` (at
+    least one).  Returns (tokens/s, steps, seconds)."""
     from oracle import model as om
 
-    dims, w, head, steps, rows = oracle_cases()
-    # passes over the three cases until at least 10 s of oracle work (at most four)
+    dims, w, head, steps, rows = oracle_cases(dtype=dtype)
     n = 0
     t0 = time.perf_counter()
-    while n < 4 * len(steps) and (n % len(steps) or n == 0 or time.perf_counter() - t0 < 10.0):
-        om.hybrid_step([w], head, dims, steps[n % len(steps)])
-        n += 1
+    if max_passes:
+        while n < max_passes * len(steps) and (n % len(steps) or n == 0 or time.perf_counter() - t0 < min_s):
+            om.hybrid_step([w], head, dims, steps[n % len(steps)])
+            n += 1
+    else:
+        while n == 0 or time.perf_counter() - t0 < min_s:
+            om.hybrid_step([w], head, dims, steps[n % len(steps)])
+            n += 1
     dt = time.perf_counter() - t0
+    return rows * n / dt, n, dt
+
+
+def cpu_leg_subprocess(dtype, threads, min_s):
+    """One oracle leg in a fresh interpreter whose BLAS and OpenMP pools are
+    limited to ``threads`` (set before NumPy loads); returns its JSON."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = str(threads)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-leg", dtype, "--cpu-leg-min-s", str(min_s)],
+                       env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout).strip().splitlines()[-1:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(args):
+    """The oracle as it stands (float64) on all the host's cores, with the
+    fp32 oracle on all cores and on one thread beside it."""
+    value, n, dt = oracle_leg("float64")
     cores = len(os.sched_getaffinity(0))
-    return {"value": rows * n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": oracle_sample_text(n, dt)}
+    out = {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": oracle_sample_text(n, dt)}
+    f32_all = cpu_leg_subprocess("float32", cores, 5.0)
+    f32_one = cpu_leg_subprocess("float32", 1, 5.0)
+    out["variants"] = {
+        "float32_all_cores": dict(f32_all, cores=cores),
+        "float32_one_thread": dict(f32_one, cores=1),
+    }
+    return out
+
+
+def run_cpu_leg(args):
+    value, n, dt = oracle_leg(args.cpu_leg, min_s=args.cpu_leg_min_s, max_passes=0)
+    print(json.dumps({"value": value, "unit": UNIT, "kind": "oracle",
+                      "sample": oracle_sample_text(n, dt, args.cpu_leg)}))
 
 
 def run_reference(args):
@@ -805,7 +983,14 @@ def main():
                     help="long-prompt mode: key-range splits of chunk-attention tiles that leave SMs idle")
     ap.add_argument("--window", type=int, default=0,
                     help="long-prompt and trace modes: sliding-window attention of W keys (0 = full causal)")
+    ap.add_argument("--cpu-leg", choices=["float64", "float32"], default=None,
+                    help="internal: time one oracle leg on this process's threads and print its JSON")
+    ap.add_argument("--cpu-leg-min-s", type=float, default=5.0)
+    ap.add_argument("--no-bf16", action="store_true", help="step mode: skip the bf16-storage line")
     args = ap.parse_args()
+    if args.cpu_leg:
+        run_cpu_leg(args)
+        return
     if args.mode == "sweep":
         run_sweep(args)
         return

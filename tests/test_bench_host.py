@@ -46,3 +46,31 @@ def test_peaks_come_from_the_measured_file_else_the_fallback(tmp_path, monkeypat
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6689.1, "bf16_tflops": 1941.1,
                                                                "bf16_tflops_sustained": 1735.0}))
     assert bench.peaks() == (6689.1, 1941.1, 1735.0, "measured")
+
+
+def test_step_roofline_terms_and_overlap_bound():
+    import synth
+    dims = synth.MISTRAL_LAYER
+    ctxs = [128, 4096, 1000]
+    per_op, overlap, ops, t_math, t_mem = bench.step_roofline(dims, ctxs, 8000.0, 2000.0)
+    # QKV: 2 * 512 * 4096 * 6144 flops at 2000 TFLOP/s (math-bound at 512 rows)
+    assert abs(ops["gemm_qkv"] - 2 * 512 * 4096 * 6144 / 2e15) < 1e-12
+    # decode attention: every key and value once + q/out rows at 8000 GB/s (memory-bound)
+    kv = sum(c + 1 for c in ctxs) * 8 * 128 * 2 * 2 + 3 * 4096 * 2 * 2
+    assert abs(ops["decode_attn"] - kv / 8e12) < 1e-12
+    # chunk attention averaged over the three starts: keys of query i at start s are s + i + 1
+    want = sum(4 * 128 * 32 * sum(s + i + 1 for i in range(448)) for s in (0, 512, 1536)) / 3 / 2e15
+    assert abs(ops["chunk_attn"] - want) < 1e-12  # math-bound: its keys are a few MB
+    assert abs(per_op - sum(ops.values())) < 1e-15
+    assert overlap == max(t_math, t_mem) and overlap <= per_op
+
+
+def test_traffic_is_null_once_the_kernel_source_changed(monkeypatch):
+    t = dict(bench.TRAFFIC["decode_attn"])
+    monkeypatch.setitem(bench.TRAFFIC, "decode_attn", dict(t, sha=bench.source_sha(t["files"])))
+    val, src = bench.traffic_of("decode_attn")
+    assert val == t["bytes"] and "ncu capture" in src
+    monkeypatch.setitem(bench.TRAFFIC, "decode_attn", dict(t, sha="0" * 16))
+    val, src = bench.traffic_of("decode_attn")
+    assert val is None and "changed" in src
+    assert bench.traffic_of("gemm_o")[0] is None
