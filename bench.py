@@ -675,7 +675,13 @@ def run_sweep(args):
     lin_flops = 2 * (dims.hidden * (dims.q_dim + 2 * dims.kv_dim) + dims.q_dim * dims.hidden
                      + 3 * dims.hidden * dims.ffn)
 
-    def time_gemm(M, name, variant, reps=5):
+    rows_list = [int(r) for r in args.rows.split(",")] if args.rows else list(SWEEP_ROWS)
+    if args.variants:
+        variants = {k: variants[k] for k in args.variants.split(",")}
+    reps_default = args.reps
+
+    def time_gemm(M, name, variant, reps=None):
+        reps = reps_default if reps is None else reps
         wt, epi = shapes[name]
         K = wt.shape[1]
         a = torch.randn(M, K, device="cuda").to(torch.float16)
@@ -699,7 +705,7 @@ def run_sweep(args):
         return ts[len(ts) // 2]
 
     gemm = {}
-    for M in SWEEP_ROWS:
+    for M in rows_list:
         gemm[M] = {}
         for vn, v in variants.items():
             if vn == "swap" and M > 256:
@@ -715,6 +721,11 @@ def run_sweep(args):
                 row["tflops"] = M * lin_flops / (row["linear_ms"] * 1e-3) / 1e12
                 row["frac_of_sustained_peak"] = row["tflops"] / tf_sust
             gemm[M][vn] = row
+    if args.gemm_only:
+        out = {"mode": "sweep", "workload": "Mistral-7B-shaped layer projections, rows " + str(rows_list) +
+               "; f16 storage; L2 flushed (256 MB write) before every timed launch", "gemm_ms": gemm}
+        print(json.dumps(out))
+        return out
     per_tok_2048 = gemm[2048]["auto"]["linear_ms"] / 2048
     equiv = {}
     for bd in SWEEP_DECODE_ONLY:
@@ -795,6 +806,74 @@ def run_trace_mode(args):
            f"{args.requests} requests, Poisson {args.rate:g} req/s, prompt lognormal(median 1024, sigma 1, clip 64-8192), "
            f"output lognormal(median 256, sigma 1, clip 16-1024), greedy sampling, wall-clock arrivals",
            "kv_pages": n_pages, "page_size": PAGE, "per_tau": runs}
+    print(json.dumps(out))
+    return out
+
+
+# ------------------------------------------------------------------ throughput vs batch
+
+FIG3_PREFILL_B = (1, 2, 4, 8)
+FIG3_DECODE_B = (1, 2, 4, 8, 16, 32, 64, 128, 256)
+
+
+def run_batch_sweep(args):
+    """Prefill and decode throughput against batch size on the 32-layer
+    Mistral-7B shape at prompt length 1024 (the pages' motivating
+    measurement: prefill saturates the GPU at small batches, decode throughput
+    keeps growing with the batch).  Prefill: one step over B whole 1024-token
+    prompts (B chunks, B x 1024 rows); decode: one step of B decodes whose
+    contexts hold 1024 tokens (random KV), token inputs.  Each step is replayed
+    from a captured graph and device-timed; tokens/s counts the step's rows."""
+    import torch
+
+    import chunked_prefill_hybrid_sar_gb300 as sar
+    from chunked_prefill_hybrid_sar_gb300 import harness
+
+    dims = synth.MISTRAL_7B
+    plen = 1024
+    max_rows = max(FIG3_PREFILL_B) * plen
+    m, _ = harness.load_synthetic_model(0, dims, max_tokens=max_rows, max_decodes=max(FIG3_DECODE_B))
+    pages_per = plen // PAGE + 1
+    n_pages = max(max(FIG3_PREFILL_B), max(FIG3_DECODE_B)) * pages_per + 8
+    kv = sar.KVCache(m, PAGE, n_pages)
+    gen = synth.generator(2, "cuda")
+    for l in range(dims.n_layers):
+        for kind in (0, 1):
+            pv = harness.page_view(kv, l, kind, dims)
+            pv.copy_(torch.randn(pv.shape, generator=gen, device="cuda").to(pv.dtype))
+    tables = [list(range(i * pages_per, (i + 1) * pages_per)) for i in range(n_pages // pages_per)]
+    stream = torch.cuda.current_stream()
+
+    def time_step(batch, inp, logits_rows):
+        logits = torch.empty(logits_rows, dims.vocab, dtype=torch.float32, device="cuda")
+        g = sar.StepGraph(m, kv, batch, inp, logits_out=logits)
+        for _ in range(3):
+            g.launch()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, args.steps // 10)
+        e0.record(stream)
+        for _ in range(reps):
+            g.launch()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        g.close()
+        return e0.elapsed_time(e1) / reps
+
+    tok = torch.randint(0, dims.vocab, (max_rows,), generator=synth.generator(3), dtype=torch.int32).cuda()
+    prefill, decode = {}, {}
+    for B in FIG3_PREFILL_B:
+        b = sar.Batch([(i, 0, plen, tables[i]) for i in range(B)], [], in_kind=sar.SAR_IN_TOKENS)
+        ms = time_step(b, tok[:B * plen].contiguous(), B)
+        prefill[B] = {"ms_per_step": ms, "tokens_per_s": B * plen / (ms * 1e-3)}
+    for B in FIG3_DECODE_B:
+        b = sar.Batch(None, [(i, plen, tables[i]) for i in range(B)], in_kind=sar.SAR_IN_TOKENS)
+        ms = time_step(b, tok[:B].contiguous(), B)
+        decode[B] = {"ms_per_step": ms, "tokens_per_s": B / (ms * 1e-3)}
+    m.sync_status()
+    out = {"mode": "batch-sweep", "workload": "Mistral-7B shape, 32 layers + 32000 head, f16 storage; prompt 1024: "
+           "prefill steps of B whole prompts, decode steps of B decodes at context 1024 (random KV); "
+           "captured graph per step, device-timed", "prefill": prefill, "decode": decode}
     print(json.dumps(out))
     return out
 
@@ -961,10 +1040,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=6)
     ap.add_argument("--impl", choices=["sar", "reference"], default="sar")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
-    ap.add_argument("--mode", choices=["step", "sweep", "trace", "long-prompt", "decode-graph"], default="step",
+    ap.add_argument("--mode", choices=["step", "sweep", "trace", "long-prompt", "decode-graph", "batch-sweep"],
+                    default="step",
                     help="step: the tau=512 hybrid step (default); sweep: tile-quantisation sweep; "
                          "trace: 32-layer serving trace; long-prompt: 60-layer chunked 16k prefill; "
-                         "decode-graph: 32-layer decode-only steps, kernel by kernel vs CUDA graph")
+                         "decode-graph: 32-layer decode-only steps, kernel by kernel vs CUDA graph; "
+                         "batch-sweep: 32-layer prefill and decode tokens/s against batch size at prompt 1024")
     ap.add_argument("--taus", default="256,512,1024", help="trace mode: token budgets")
     ap.add_argument("--requests", type=int, default=256, help="trace mode: requests of the trace")
     ap.add_argument("--chunks", default="256,512,1024", help="long-prompt mode: chunk sizes")
@@ -983,6 +1064,10 @@ def main():
                     help="long-prompt mode: key-range splits of chunk-attention tiles that leave SMs idle")
     ap.add_argument("--window", type=int, default=0,
                     help="long-prompt and trace modes: sliding-window attention of W keys (0 = full causal)")
+    ap.add_argument("--rows", default="", help="sweep mode: stacked row counts (default: the configured list)")
+    ap.add_argument("--variants", default="", help="sweep mode: tilings (m128n128, m128n256, m256n128, swap, auto)")
+    ap.add_argument("--reps", type=int, default=5, help="sweep mode: timed launches per GEMM")
+    ap.add_argument("--gemm-only", action="store_true", help="sweep mode: the per-GEMM part only")
     ap.add_argument("--cpu-leg", choices=["float64", "float32"], default=None,
                     help="internal: time one oracle leg on this process's threads and print its JSON")
     ap.add_argument("--cpu-leg-min-s", type=float, default=5.0)
@@ -1002,6 +1087,9 @@ def main():
         return
     if args.mode == "decode-graph":
         run_decode_graph(args)
+        return
+    if args.mode == "batch-sweep":
+        run_batch_sweep(args)
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -67,7 +67,7 @@ static_assert(kBQ == kChunkTileRowsTc, "the step plans tiles of kBQ rows");
 struct Bars {
   uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
   uint64_t s_full[2], p_full[2];
-  uint64_t o_done, q_ready, mma_done;
+  uint64_t o_done, q_ready, mma_done;  // o_done: each P.V; mma_done: once, after every MMA
   uint32_t tmem_slot;
 };
 
@@ -211,6 +211,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t fmt = Elem<T>::kMmaFormat;
       const uint32_t id_s = idesc_128x128(fmt, 0), id_pv = idesc_128x128(fmt, 1);
+      // descriptors built once: a byte offset b within shared memory moves a
+      // descriptor's start-address field (address / 16) by b / 16, so each MMA
+      // adds a constant (this thread issues 24 small MMAs per key block and
+      // shares its scheduler with two softmax warps)
+      const uint64_t dq_hi = sw128_desc(q_hi), dq_lo = sw128_desc(q_lo);
+      static_assert(kStages == 2, "one descriptor per stage, chosen by a select");
+      const uint64_t dk0 = sw128_desc(k_reg(0)), dk1 = sw128_desc(k_reg(1));
+      const uint64_t dv0 = sw128_desc_mn(v_reg(0), kRegion, 1024), dv1 = sw128_desc_mn(v_reg(1), kRegion, 1024);
       bool ok = mbar_wait(smem_u32(&bars->q_ready), 0, a.err, SITE_CHUNK_PIPE);
       auto issue_s = [&](int j) -> bool {
         const int s = j % kStages;
@@ -218,12 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           return false;
         tc_fence_after();
         const uint32_t d = tmem + (kColS * (uint32_t)(j & 1));
+        const uint64_t db = s ? dk1 : dk0;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (uint32_t)((kk >> 2) * kRegion + (kk & 3) * 32);
-          const uint64_t bdesc = sw128_desc(k_reg(s) + off);
-          mma_f16<false>(d, sw128_desc(q_hi + off), bdesc, id_s, kk != 0);
-          mma_f16<false>(d, sw128_desc(q_lo + off), bdesc, id_s, 1);
+          const uint64_t o = (uint64_t)(((kk >> 2) * kRegion + (kk & 3) * 32) >> 4);
+          mma_f16<false>(d, dq_hi + o, db + o, id_s, kk != 0);
+          mma_f16<false>(d, dq_lo + o, db + o, id_s, 1);
         }
         mma_commit(smem_u32(&bars->s_full[j & 1]));
         mma_commit(smem_u32(&bars->k_empty[s]));
@@ -238,11 +246,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(smem_u32(&bars->v_full[s]), (uint32_t)((j / kStages) & 1), a.err, SITE_CHUNK_PIPE)))
           break;
         tc_fence_after();
+        const uint32_t pcol = tmem + (kColS * (uint32_t)(j & 1));
+        const uint64_t dvs = s ? dv1 : dv0;
 #pragma unroll
         for (int kk = 0; kk < kBKV / 16; ++kk) {
-          // 16 keys per step: P columns (two keys per 32-bit column), V rows
-          const uint64_t bdesc = sw128_desc_mn(v_reg(s) + kk * (16 * 128), kRegion, 1024);
-          mma_f16_ts(tmem + kColO, tmem + (kColS * (uint32_t)(j & 1)) + kk * 8, bdesc, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          // 16 keys per step: P columns (two keys per 32-bit column), V rows (16 x 128 bytes)
+          mma_f16_ts(tmem + kColO, pcol + kk * 8, dvs + (uint64_t)(kk * (16 * 128 / 16)), id_pv,
+                     (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(smem_u32(&bars->v_empty[s]));
         mma_commit(smem_u32(&bars->o_done));
@@ -402,7 +412,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     red[(2 * 2 + hf) * kBQ + r] = l;  // row sum over both halves
     pair_sync();
     const float lt = l + red[(2 * 2 + (hf ^ 1)) * kBQ + r];
-    if (alive) alive = warp_wait_bar(smem_u32(&bars->o_done), (uint32_t)((nb - 1) & 1), a.err, SITE_CHUNK_PIPE);
+    // O is final once every MMA has completed: mma_done completes once, after
+    // the last P.V (o_done's parity cannot say that: with the last two P.V
+    // still in flight, the phase of parity (nb - 1) & 1 two blocks back has
+    // already completed)
+    if (alive) alive = warp_wait_bar(smem_u32(&bars->mma_done), 0, a.err, SITE_CHUNK_PIPE);
     if (alive && part >= 0) {
       // one share of the tile's keys: O unnormalised, with the row's maximum
       // (base 2) and sum, for chunk_combine_kernel

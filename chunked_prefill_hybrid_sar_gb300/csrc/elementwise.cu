@@ -54,12 +54,13 @@ struct NormArgs {
   size_t zero_n;
   float* zero2;           // a second region to clear (a split-K accumulator of the next GEMM)
   size_t zero2_n;
-  // kSrcRows / kSrcTokens, optional: the step's rotary table cs[r][i] =
-  // (cos, sin) of pos[r] * inv_freq[i], i < half_d
+  // kSrcRows / kSrcTokens, optional: the step's rotary table, (cos, sin) of
+  // pos[r] * inv_freq[i], i < half_d, at float2 index ((i / 2) * cs_ld + r) * 2
+  // + i % 2 (frequency pairs major, rows adjacent)
   const int32_t* pos;
   const double* inv_freq;
   float2* cs;
-  int half_d;
+  int half_d, cs_ld;
   int hidden, vocab;
   float eps;
   int* err;
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
         ang -= two_pi * rint(ang * (1.0 / two_pi));
         float sn, cn;
         sincosf((float)ang, &sn, &cn);
-        a.cs[(size_t)r * a.half_d + i] = make_float2(cn, sn);
+        a.cs[((size_t)(i >> 1) * a.cs_ld + r) * 2 + (i & 1)] = make_float2(cn, sn);
       }
     }
     float4* hr = reinterpret_cast<float4*>(a.h + (size_t)r * a.hidden);
@@ -191,7 +192,7 @@ __global__ void rope_append_kernel(float* qkv, int ld, RopeEpi rp, int* err) {
   const bool slot_ok = sl >= 0 && page < rp.num_pages;
   if (!slot_ok && threadIdx.x == 0) report(err, SAR_ERR_BOUNDS, SITE_ROPE_BOUNDS, r);
   float* row = qkv + (size_t)r * ld;
-  const float4* cs4 = reinterpret_cast<const float4*>(rp.cs + (size_t)r * half);
+  const float4* cs4 = reinterpret_cast<const float4*>(rp.cs) + r;  // pair i of this row at cs4[i * cs_ld]
   for (int it = threadIdx.x; it < heads * hq4; it += blockDim.x) {
     const int head = it / hq4, i = (it - head * hq4) * 4;
     const bool is_v = head >= rp.qh + rp.kvh, is_k = !is_v && head >= rp.qh;
@@ -199,7 +200,7 @@ __global__ void rope_append_kernel(float* qkv, int ld, RopeEpi rp, int* err) {
     float4* p2 = reinterpret_cast<float4*>(row + head * rp.hd + half + i);
     float4 a = *p1, b = *p2;
     if (!is_v) {
-      const float4 c01 = cs4[i >> 1], c23 = cs4[(i >> 1) + 1];  // (cos, sin) of pairs i..i+3
+      const float4 c01 = cs4[(size_t)(i >> 1) * rp.cs_ld], c23 = cs4[(size_t)((i >> 1) + 1) * rp.cs_ld];  // (cos, sin) of i..i+3
       const float c[4] = {c01.x, c01.z, c23.x, c23.z}, sn[4] = {c01.y, c01.w, c23.y, c23.w};
       const float x1[4] = {a.x, a.y, a.z, a.w}, x2[4] = {b.x, b.y, b.z, b.w};
       float y1[4], y2[4];
@@ -399,7 +400,7 @@ int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hid
 int launch_input_norm(int in_kind, const void* in, const void* table, int vocab, float* h, const float* gain,
                       void* y, int rows, int hidden, float eps, int storage, int* err, cudaStream_t s,
                       float* zero, size_t zero_n, const int32_t* pos, const double* inv_freq, float2* cs,
-                      int half_d, float* zero2, size_t zero2_n) {
+                      int half_d, int cs_ld, float* zero2, size_t zero2_n) {
   if (rows <= 0) return SAR_OK;
   if (hidden % 4 || hidden > 4 * kNormThreads * kNormMaxVec)
     return set_error(SAR_ERR_UNSUPPORTED, "rmsnorm: hidden must be a multiple of 4 and at most 8192");
@@ -421,6 +422,8 @@ int launch_input_norm(int in_kind, const void* in, const void* table, int vocab,
   a.inv_freq = inv_freq;
   a.cs = cs;
   a.half_d = half_d;
+  a.cs_ld = cs_ld;
+  if (cs && (cs_ld < rows || half_d % 2)) return set_error(SAR_ERR_INVALID_ARG, "input norm: rotary table stride");
   const bool bf = storage == SAR_STORAGE_BF16;
   const dim3 g(rows), b(kNormThreads);
   cudaError_t e;
@@ -437,7 +440,7 @@ int launch_input_norm(int in_kind, const void* in, const void* table, int vocab,
 
 int launch_rope_append(float* qkv, int ld, int rows, const RopeEpi& rp, int storage, int* err, cudaStream_t s) {
   if (rows <= 0) return SAR_OK;
-  if ((rp.hd != 64 && rp.hd != 128) || ld != (rp.qh + 2 * rp.kvh) * rp.hd || !rp.slot || !rp.cs)
+  if ((rp.hd != 64 && rp.hd != 128) || ld != (rp.qh + 2 * rp.kvh) * rp.hd || !rp.slot || !rp.cs || rp.cs_ld < rows)
     return set_error(SAR_ERR_INVALID_ARG, "rope/append: bad arguments");
   cudaError_t e = storage == SAR_STORAGE_BF16
                       ? launch_pdl(rope_append_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, qkv, ld, rp, err)

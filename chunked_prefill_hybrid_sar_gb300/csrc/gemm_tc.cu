@@ -161,7 +161,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* er
 template <typename T, int EPI, bool SWAP, int MSUB, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const __grid_constant__ CUtensorMap tm_c, const Params p) {
+                   const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_kp,
+                   const __grid_constant__ CUtensorMap tm_vp, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -361,13 +362,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* C = reinterpret_cast<float*>(p.c);
             int page = -1, off = 0;
             bool slot_ok = false;
+            const int sl = row_ok ? rp.slot[row] : -1;
             if (row_ok) {
-              const int sl = rp.slot[row];
               page = sl >= 0 ? sl / rp.page_size : -1;
               off = sl - page * rp.page_size;
               slot_ok = sl >= 0 && page < rp.num_pages;
             }
-            const float2* cs = rp.cs + (size_t)(row_ok ? row : 0) * half;
+            // k/v rows by TMA store (TMA path): each half-warp's 16 rows whose
+            // slots are one whole page-aligned run of 16 (a chunk's rows)
+            // leave as one 16-row box per dim half; other rows (decodes, a
+            // chunk's ragged edges) are stored by their threads
+            const int sl_b = __shfl_sync(0xffffffffu, sl, lane & 16);
+            const unsigned runs = __ballot_sync(0xffffffffu, row_ok && slot_ok && sl_b >= 0 && (sl_b & 15) == 0 &&
+                                                                 sl == sl_b + (lane & 15));
+            const bool run0 = (runs & 0xffffu) == 0xffffu, run1 = (runs >> 16) == 0xffffu;
+            const bool in_run = (lane < 16) ? run0 : run1;
+            const int pg_b0 = __shfl_sync(0xffffffffu, page, 0), of_b0 = __shfl_sync(0xffffffffu, off, 0);
+            const int pg_b1 = __shfl_sync(0xffffffffu, page, 16), of_b1 = __shfl_sync(0xffffffffu, off, 16);
+            bool after_kv = false;  // the last staging use was a k/v head's
+            // this row's (cos, sin) pairs: pair i at csr[i * cs_ld] (rows adjacent, so a
+            // warp's 32 rows load one 512-byte run)
+            const float4* csr = reinterpret_cast<const float4*>(rp.cs) + (row_ok ? row : 0);
+            const size_t cld = (size_t)rp.cs_ld;
+            float4 cs_next[8];  // TMA path: the next (cos, sin) chunk, loaded one chunk ahead
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cs_next[e] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
             for (int hh = 0; hh < p.bn / rp.hd; ++hh) {
               const int col0 = nt * p.bn + hh * rp.hd;  // first column of this head
@@ -383,18 +402,130 @@ __global__ void __launch_bounds__(kThreads, 1)
               if ((is_k || is_v) && row_ok && !slot_ok && hh == 0)
                 report(p.err, SAR_ERR_BOUNDS, SITE_ROPE_BOUNDS, row);
               float* crow = C + (size_t)row * p.N + col0;
+              if (p.tma_out && rp.hd == 128 && (is_k || is_v)) {
+                // k / v head: rotated (k) and rounded once; no fp32 copy (the
+                // attention kernels read k and v from the pages).  The warp's
+                // 32 rows are staged as 16-bit [2 dim halves][32 rows][128 B]
+                // (128-byte swizzle) in its 8 KB for this head and the page-run
+                // boxes go out by TMA into the cache's tensor map
+                const uint32_t stg = epi_stage + (uint32_t)(q * 4 * kEpiBoxBytes + hh * 8192);
+                if (lane == 0) bulk_wait_read_all();  // earlier stores have read the staging
+                __syncwarp();
+                if (is_k && row_ok) {
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) cs_next[e] = __ldg(csr + e * cld);
+                }
+#pragma unroll 1
+                for (int j = 0; j < 4; ++j) {
+                  uint32_t x1[16], x2[16];
+                  tmem_ld16(sbase + hh * 128 + j * 16, x1);
+                  tmem_ld16(sbase + hh * 128 + 64 + j * 16, x2);
+                  float r1[16], r2[16];
+                  if (is_v) {
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                      r1[e] = __uint_as_float(x1[e]);
+                      r2[e] = __uint_as_float(x2[e]);
+                    }
+                  } else {
+                    float4 cc[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) cc[e] = cs_next[e];
+                    if (row_ok && j < 3) {
+#pragma unroll
+                      for (int e = 0; e < 8; ++e) cs_next[e] = __ldg(csr + ((j + 1) * 8 + e) * cld);
+                    }
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                      const float4 t4 = cc[e >> 1];
+                      const float tc = (e & 1) ? t4.z : t4.x, ts = (e & 1) ? t4.w : t4.y;
+                      const float a1 = __uint_as_float(x1[e]), a2 = __uint_as_float(x2[e]);
+                      r1[e] = a1 * tc - a2 * ts;
+                      r2[e] = a2 * tc + a1 * ts;
+                    }
+                  }
+                  uint32_t o1[8], o2[8];
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) {
+                    o1[e] = Elem<T>::pack(r1[2 * e], r1[2 * e + 1]);
+                    o2[e] = Elem<T>::pack(r2[2 * e], r2[2 * e + 1]);
+                  }
+                  if (in_run) {
+                    // dims [16j, 16j + 16) of each half: 16-byte chunks 2j and 2j + 1 of the row
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                      const uint32_t cofs = (uint32_t)(lane * 128 + (((2 * j + c) ^ (lane & 7)) << 4));
+                      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg + cofs), "r"(o1[4 * c]),
+                                   "r"(o1[4 * c + 1]), "r"(o1[4 * c + 2]), "r"(o1[4 * c + 3])
+                                   : "memory");
+                      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg + 4096 + cofs), "r"(o2[4 * c]),
+                                   "r"(o2[4 * c + 1]), "r"(o2[4 * c + 2]), "r"(o2[4 * c + 3])
+                                   : "memory");
+                    }
+                  } else if (dst) {
+                    uint4* d1 = reinterpret_cast<uint4*>(dst + j * 16);
+                    uint4* d2 = reinterpret_cast<uint4*>(dst + 64 + j * 16);
+                    d1[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                    d1[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+                    d2[0] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                    d2[1] = make_uint4(o2[4], o2[5], o2[6], o2[7]);
+                  }
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA unit
+                __syncwarp();
+                if (lane == 0 && (run0 || run1)) {
+                  const CUtensorMap* kvmap = is_v ? &tm_vp : &tm_kp;
+                  const int kh = head - rp.qh - (is_v ? rp.kvh : 0);
+                  if (run0) {
+                    const int kr = (pg_b0 * rp.kvh + kh) * rp.page_size + of_b0;
+                    tma_store_2d(kvmap, 0, kr, stg);
+                    tma_store_2d(kvmap, 64, kr, stg + 4096);
+                  }
+                  if (run1) {
+                    const int kr = (pg_b1 * rp.kvh + kh) * rp.page_size + of_b1;
+                    tma_store_2d(kvmap, 0, kr, stg + 2048);
+                    tma_store_2d(kvmap, 64, kr, stg + 4096 + 2048);
+                  }
+                  bulk_commit();
+                }
+                ++epi_n;
+                after_kv = true;
+                continue;
+              }
               if (p.tma_out && rp.hd == 128) {
-                // fp32 q|k|v of this head through shared memory: per round two
+                // q head: fp32 rows through shared memory: per round two
                 // 32x32 boxes, columns [32bp, 32bp+32) and [64+32bp, 96+32bp) --
                 // the rotate-half partners -- each written by one TMA store
-                // (rows past M clipped); k and v also go to their page slot
+                // (rows past M clipped).  Rounds alternate between two box
+                // pairs, so a round waits only for the stores of the round
+                // before last.  The (cos, sin) chunk of the next 16
+                // frequencies is loaded one chunk ahead (into the next head's
+                // first chunk), so its L2 latency overlaps this chunk's work.
                 const int row0 = (mt * MSUB + s) * 128 + q * 32;
-                const float4* cs4 = reinterpret_cast<const float4*>(cs);
+                const int heads = p.bn / rp.hd;
+                auto rotates = [&](int h) {
+                  const int c0 = nt * p.bn + h * rp.hd;
+                  return h < heads && c0 < p.N && c0 / rp.hd < rp.qh + rp.kvh;
+                };
+                if (hh == 0 && row_ok && rotates(0)) {
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) cs_next[e] = __ldg(csr + e * cld);
+                }
 #pragma unroll 1
                 for (int bp = 0; bp < 2; ++bp) {
-                  if (lane == 0) bulk_wait_read_all();  // both staging boxes have been read
+                  const uint32_t b0 = epi_stage + (uint32_t)((q * 4 + (epi_n >> 1 & 1) * 2) * kEpiBoxBytes);
+                  const uint32_t b1 = b0 + kEpiBoxBytes;
+                  if (lane == 0) {
+                    // the pair used two rounds ago has been read (all stores, after a k/v head's staging)
+                    if (after_kv)
+                      bulk_wait_read_all();
+                    else
+                      bulk_wait_read_all_but_one();
+                  }
+                  after_kv = false;
                   __syncwarp();
-                  const uint32_t b0 = epi_stage + (uint32_t)(q * 2 * kEpiBoxBytes), b1 = b0 + kEpiBoxBytes;
 #pragma unroll 1
                   for (int jj = 0; jj < 2; ++jj) {
                     const int j = bp * 2 + jj;  // 16-column chunk of each half
@@ -412,7 +543,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                       float4 cc[8];
 #pragma unroll
-                      for (int e = 0; e < 8; ++e) cc[e] = row_ok ? __ldg(cs4 + j * 8 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                      for (int e = 0; e < 8; ++e) cc[e] = cs_next[e];
+                      // the chunk after this one: j + 1 of this head, else chunk 0 of the next
+                      const bool more = j < 3 || rotates(hh + 1);
+                      if (row_ok && more) {
+                        const int jn = (j + 1) & 3;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) cs_next[e] = __ldg(csr + (jn * 8 + e) * cld);
+                      }
                       tmem_wait_ld();
 #pragma unroll
                       for (int e = 0; e < 16; ++e) {
@@ -432,20 +570,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                       asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(b1 + off), "f"(r2[4 * c]),
                                    "f"(r2[4 * c + 1]), "f"(r2[4 * c + 2]), "f"(r2[4 * c + 3])
                                    : "memory");
-                    }
-                    if (dst) {
-                      uint32_t o1[8], o2[8];
-#pragma unroll
-                      for (int e = 0; e < 8; ++e) {
-                        o1[e] = Elem<T>::pack(r1[2 * e], r1[2 * e + 1]);
-                        o2[e] = Elem<T>::pack(r2[2 * e], r2[2 * e + 1]);
-                      }
-                      uint4* d1 = reinterpret_cast<uint4*>(dst + j * 16);
-                      uint4* d2 = reinterpret_cast<uint4*>(dst + 64 + j * 16);
-                      d1[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-                      d1[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
-                      d2[0] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
-                      d2[1] = make_uint4(o2[4], o2[5], o2[6], o2[7]);
                     }
                   }
                   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA unit
@@ -483,10 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               } else {
                 // the (cos, sin) pairs of the next 16 frequencies are loaded one
                 // chunk ahead, so their L2 latency overlaps this chunk's work
-                const float4* cs4 = reinterpret_cast<const float4*>(cs);
                 float4 cn[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) cn[e] = row_ok ? __ldg(cs4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int e = 0; e < 8; ++e) cn[e] = row_ok ? __ldg(csr + e * cld) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
                 for (int j = 0; j < half / 16; ++j) {
                   float4 cc[8];
@@ -494,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   for (int e = 0; e < 8; ++e) cc[e] = cn[e];
                   if (row_ok && j + 1 < half / 16) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) cn[e] = __ldg(cs4 + (j + 1) * 8 + e);
+                    for (int e = 0; e < 8; ++e) cn[e] = __ldg(csr + ((j + 1) * 8 + e) * cld);
                   }
                   uint32_t x1[16], x2[16];
                   tmem_ld16(sbase + hh * rp.hd + j * 16, x1);
@@ -720,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float r = x;
                 if (!is_v) {
                   const float y = xchg[pl * 17 + e];
-                  const float2 t = rp.cs[(size_t)m * half + fi];
+                  const float2 t = rp.cs[((size_t)(fi >> 1) * rp.cs_ld + m) * 2 + (fi & 1)];
                   r = first ? x * t.x - y * t.y : x * t.x + y * t.y;
                 }
                 C[(size_t)m * p.N + n] = r;
@@ -1000,9 +1123,10 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
   // the in-place residual epilogue of the non-swap tilings adds through TMA reductions
   // (the SwiGLU epilogue stores through TMA too)
   c.tma_out = (!c.swap && ((epi == SAR_EPI_RESIDUAL && in_place) || epi == SAR_EPI_SWIGLU || epi == kEpiRope)) ? 1 : 0;
+  // (the rotary epilogue alternates two box pairs per warp)
   const int extra = kBarBytes + 1024 +
                     (c.swap ? (epi == SAR_EPI_SWIGLU ? kSwapXchg : epi == kEpiRope ? kSwapXchgRope : 0)
-                            : (c.tma_out ? kEpiStage : 0));
+                            : (c.tma_out ? (epi == kEpiRope ? 2 * kEpiStage : kEpiStage) : 0));
   if (two_ctas && (!c.swap || c.bn > 128))
     return set_error(SAR_ERR_UNSUPPORTED, "gemm: two CTAs per SM only with the swap tiling and M <= 128");
   c.per_sm = two_ctas ? 2 : 1;
@@ -1043,7 +1167,7 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   if (epi == SAR_EPI_RESIDUAL && residual == nullptr)
     return set_error(SAR_ERR_INVALID_ARG, "gemm: residual epilogue without residual");
   if (epi == kEpiRope &&
-      (!rope || !rope->slot || !rope->cs || (rope->hd != 64 && rope->hd != 128) || N % 128 ||
+      (!rope || !rope->slot || !rope->cs || rope->cs_ld < M || (rope->hd != 64 && rope->hd != 128) || N % 128 ||
        (!cfg.swap && cfg.bn % rope->hd) ||
        N != (rope->qh + 2 * rope->kvh) * rope->hd || rope->page_size <= 0))
     return set_error(SAR_ERR_INVALID_ARG, "gemm: rotary epilogue arguments");
@@ -1071,8 +1195,15 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   p.err = err;
   // (the rotary epilogue's TMA path covers head_dim 128)
   p.tma_out = (cfg.tma_out && !(epi == kEpiRope && rope->hd != 128)) ? 1 : 0;
-  CUtensorMap tc_map;
+  CUtensorMap tc_map, kp_map, vp_map;
   std::memset(&tc_map, 0, sizeof(tc_map));
+  std::memset(&kp_map, 0, sizeof(kp_map));
+  std::memset(&vp_map, 0, sizeof(vp_map));
+  if (epi == kEpiRope && p.tma_out) {
+    if (!rope->kmap || !rope->vmap) return set_error(SAR_ERR_INVALID_ARG, "gemm: rotary epilogue without page maps");
+    kp_map = *rope->kmap;
+    vp_map = *rope->vmap;
+  }
   if (p.tma_out) {
     int mrc = SAR_OK;
     if (cfg.swap || (epi == SAR_EPI_RESIDUAL && c != residual) ||
@@ -1091,7 +1222,7 @@ int gemm_launch(const GemmCfg& cfg, const CUtensorMap& act_map, const CUtensorMa
   SAR_TRY(ensure_smem_attr(fn, kSmemLimit, "gemm: set smem attribute"));
   const CUtensorMap& ta = cfg.swap ? w_map : act_map;
   const CUtensorMap& tb = cfg.swap ? act_map : w_map;
-  void* args[] = {const_cast<CUtensorMap*>(&ta), const_cast<CUtensorMap*>(&tb), &tc_map, &p};
+  void* args[] = {const_cast<CUtensorMap*>(&ta), const_cast<CUtensorMap*>(&tb), &tc_map, &kp_map, &vp_map, &p};
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute attr[2];
   lc.blockDim = dim3(kThreads);

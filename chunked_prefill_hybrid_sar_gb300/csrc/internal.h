@@ -106,9 +106,17 @@ constexpr int kEpiRope = 4;
 struct RopeEpi {
   const int32_t* pos = nullptr;   // [M] absolute position of each row (unused: the table holds it)
   const int32_t* slot = nullptr;  // [M] page * page_size + offset
-  const float2* cs = nullptr;     // [M][hd/2] (cos, sin) of pos * theta_i
+  // (cos, sin) of pos * theta_i, frequency-major so that consecutive rows are
+  // adjacent: the float4 (cos, sin of frequency 2i; cos, sin of 2i + 1) of
+  // row r is at cs4(i * cs_ld + r), cs_ld >= the step's rows
+  const float2* cs = nullptr;
+  int cs_ld = 0;
   void* k_cache = nullptr;        // layer base [num_pages][kvh][page_size][hd], storage type
   void* v_cache = nullptr;
+  // the layer's pages as tensor maps (16-row x 64-column boxes, make_kv_tmap):
+  // head_dim 128 k/v rows of page-aligned 16-row runs are stored through them
+  const CUtensorMap* kmap = nullptr;
+  const CUtensorMap* vmap = nullptr;
   int qh = 0, kvh = 0, hd = 0, page_size = 0, num_pages = 0;
 };
 
@@ -137,12 +145,12 @@ int launch_rmsnorm(const float* x, const float* gain, void* y, int rows, int hid
 // The step's first kernel: stacked input rows (bf16 hidden rows, or token ids
 // looked up in `table`) into the fp32 residual stream h and, normalised with
 // `gain`, into y (storage type).  zero (optional): zero_n floats to clear.
-// cs (optional): the step's rotary table [rows][half_d] of (cos, sin) of
+// cs (optional): the step's rotary table (the RopeEpi layout, row stride cs_ld) of (cos, sin) of
 // pos[r] * inv_freq[i], shared by every layer's QKV epilogue.
 int launch_input_norm(int in_kind, const void* in, const void* table, int vocab, float* h, const float* gain,
                       void* y, int rows, int hidden, float eps, int storage, int* err, cudaStream_t s,
                       float* zero = nullptr, size_t zero_n = 0, const int32_t* pos = nullptr,
-                      const double* inv_freq = nullptr, float2* cs = nullptr, int half_d = 0,
+                      const double* inv_freq = nullptr, float2* cs = nullptr, int half_d = 0, int cs_ld = 0,
                       float* zero2 = nullptr, size_t zero2_n = 0);
 // Small-row steps, whose QKV and gate/up projections accumulate split-K into
 // fp32: the rotary embedding + KV-page append over qkv rows [rows][ld] in

@@ -67,7 +67,7 @@ struct sar_model {
   // workspace
   uint8_t* ws = nullptr;
   st16 *xn = nullptr, *attn = nullptr, *act = nullptr, *hrows = nullptr;
-  float2* rope_cs = nullptr;  // [max_tokens][head_dim / 2] (cos, sin) of this step's positions
+  float2* rope_cs = nullptr;  // (cos, sin) of this step's positions, [head_dim / 4][max_tokens] float4 pairs
   float* hres = nullptr;   // residual stream, fp32
   float* qkv32 = nullptr;  // QKV projection in fp32, q and k rotated by the projection's epilogue
   float* gu32 = nullptr;   // small steps: gate/up projection accumulated split-K in fp32
@@ -535,7 +535,7 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
       Prof pr(m, SAR_K_EMBED, s);
       SAR_TRY(sar::launch_input_norm(b->in_kind, in, m->embed, d.vocab, h, w.n1, m->xn, M, H, d.rms_eps, d.storage,
                                      m->err, s, logits, logits ? (size_t)p.R * d.vocab : 0, md + p.o_pos,
-                                     m->inv_freq, m->rope_cs, d.head_dim / 2, qkv_zero, qkv_zero_n));
+                                     m->inv_freq, m->rope_cs, d.head_dim / 2, d.max_tokens, qkv_zero, qkv_zero_n));
     } else {
       Prof pr(m, SAR_K_RMSNORM, s);
       SAR_TRY(sar::launch_rmsnorm(h, w.n1, m->xn, M, H, d.rms_eps, nullptr, d.storage, s, qkv_zero, qkv_zero_n));
@@ -550,6 +550,7 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
       rp.pos = md + p.o_pos;
       rp.slot = md + p.o_slot;
       rp.cs = m->rope_cs;
+      rp.cs_ld = d.max_tokens;
       rp.k_cache = kc;
       rp.v_cache = vc;
       rp.qh = d.n_q_heads;
@@ -557,6 +558,8 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
       rp.hd = d.head_dim;
       rp.page_size = kv->page_size;
       rp.num_pages = kv->num_pages;
+      rp.kmap = &kv->tmk[l];
+      rp.vmap = &kv->tmv[l];
       if (qkv_split) {
         SAR_TRY(run_gemm(m, m->xn, M, w.m_qkv, m->qkv_n, H, SAR_EPI_RESIDUAL, m->qkv32, m->qkv32, s));
         SAR_TRY(sar::launch_rope_append(m->qkv32, m->qkv_n, M, rp, d.storage, m->err, s));

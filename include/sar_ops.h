@@ -96,14 +96,19 @@ int sar_op_rmsnorm(const void* x, const void* gain, void* y, int32_t rows, int32
 /* Device address of a step workspace buffer, valid until sar_model_destroy;
  * after a step on a one-layer model it holds that layer's intermediates.
  *   0: normed rows     [max_tokens, hidden] (storage type)
- *   1: rotary table    fp32 pairs [max_tokens, head_dim / 2]: (cos, sin) of
- *                      each row's position times theta_i
+ *   1: rotary table    fp32, (cos, sin) of each row's position times theta_i:
+ *                      for row r and frequency i, at float index
+ *                      4 * ((i / 2) * max_tokens + r) + 2 * (i % 2) (frequency
+ *                      pairs major, so a warp's 32 rows read 512 contiguous bytes)
  *   2: attention rows  [max_tokens, n_q_heads * head_dim] (storage type)
  *   3: SwiGLU rows     [max_tokens, ffn] (storage type)
  *   4: residual stream fp32 [max_tokens, hidden] (when the step had no hidden_out)
  *   5: q|k|v rows      fp32 [max_tokens, (n_q_heads + 2 n_kv_heads) * head_dim]
  *                      (the projection with q and k rotated; k and v are
- *                      also in the pages, rounded to the storage type) */
+ *                      also in the pages, rounded to the storage type; for
+ *                      head_dim 128 and more than 256 rows only q is kept in
+ *                      fp32 -- the attention kernels read k and v from the
+ *                      pages) */
 int sar_model_debug_buffer(sar_model* m, int32_t which, void** out);
 
 /* The step planner on the host alone (no GPU, no model): plans batch `b` as
