@@ -271,7 +271,9 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
   for (int i = 0; i < Bd; ++i) {
     const sar_decode& dc = b->decode[i];
     if (dc.ctx_len < 0 || !dc.block_table) return set_error(SAR_ERR_INVALID_ARG, "step: bad decode entry");
-    SAR_TRY(check_bt(dc.block_table, dc.n_blocks, dc.ctx_len));
+    // (the page ids themselves are range-checked as they are copied below)
+    if (dc.n_blocks < 0 || (int64_t)dc.n_blocks * ps <= dc.ctx_len)
+      return set_error(SAR_ERR_INVALID_ARG, "step: block table does not cover the positions");
     total_keys += span_of(dc.ctx_len);
   }
   // decode work split: key ranges of `split` keys, about four CTAs (two per
@@ -280,8 +282,22 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
   const int sms = env.sms;
   int64_t split = (total_keys * d.n_kv_heads) / (4LL * sms);
   split = std::max<int64_t>(128, std::min<int64_t>(2048, (split + 15) / 16 * 16));
-  std::vector<int32_t> items, pbeg(Bd, -1), pcnt(Bd, 0), nkeys(Bd), btoff(Bd), btlen(Bd), bt;
-  std::vector<int32_t> tail_items;
+  // scratch arrays kept per thread, so a step's planning allocates nothing
+  // once they have grown to the batch's size
+  thread_local std::vector<int32_t> items, pbeg, pcnt, nkeys, btoff, btlen, bt, tail_items, rows, pbt, tiles, comb;
+  thread_local std::vector<int> order;
+  items.clear();
+  bt.clear();
+  tail_items.clear();
+  rows.clear();
+  pbt.clear();
+  tiles.clear();
+  comb.clear();
+  pbeg.assign(Bd, -1);
+  pcnt.assign(Bd, 0);
+  nkeys.resize(Bd);
+  btoff.resize(Bd);
+  btlen.resize(Bd);
   int n_parts = 0;
   for (int i = 0; i < Bd; ++i) {
     const sar_decode& dc = b->decode[i];
@@ -290,7 +306,20 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
     btoff[i] = (int32_t)bt.size();
     const int nb = (dc.ctx_len / ps) + 1;
     btlen[i] = nb;
-    bt.insert(bt.end(), dc.block_table, dc.block_table + nb);
+    {
+      // copy the pages the positions use, checking each id on the way
+      const size_t o0 = bt.size();
+      bt.resize(o0 + nb);
+      int32_t* dst = bt.data() + o0;
+      const int32_t* src = dc.block_table;
+      uint32_t bad = 0;
+      for (int k = 0; k < nb; ++k) {
+        const int32_t v = src[k];
+        dst[k] = v;
+        bad |= (uint32_t)v >= (uint32_t)env.num_pages ? 1u : 0u;
+      }
+      if (bad) return set_error(SAR_ERR_BOUNDS, "step: page id out of range");
+    }
     const int kfirst = first_key(nk);
     const int span = span_of(dc.ctx_len);
     const int ns = (int)((span + split - 1) / split);
@@ -310,7 +339,7 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
   }
   // longest ranges first, so the grid's last CTAs are its shortest
   {
-    std::vector<int> order(tail_items.size() / 4);
+    order.resize(tail_items.size() / 4);
     for (size_t t = 0; t < order.size(); ++t) order[t] = (int)t;
     std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
       return tail_items[4 * x + 2] - tail_items[4 * x + 1] > tail_items[4 * y + 2] - tail_items[4 * y + 1];
@@ -318,7 +347,6 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
     for (int t : order) items.insert(items.end(), tail_items.begin() + 4 * t, tail_items.begin() + 4 * t + 4);
   }
   // rows whose logits are returned: every chunk's last row, then every decode row
-  std::vector<int32_t> rows;
   {
     int r0 = 0;
     for (const sar_prefill& c : chunks) {
@@ -332,7 +360,6 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
   // offset, block-table length, first and end 128-key block, partial slot},
   // the most keys first (the longest CTAs start first)
   const int tile_rows = chunk_tile_rows(d, ps);
-  std::vector<int32_t> pbt, tiles, comb;
   int n_cparts = 0;
   {
     struct Tile {
@@ -415,7 +442,7 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
   p->o_tiles = take(tiles.size());
   p->o_comb = take(comb.size());
   p->total = o;
-  meta->assign(o, 0);
+  meta->resize(o);  // every array is written below; the 16-byte padding between them is never read
   int32_t* mt = meta->data();
   {
     int r = 0;
@@ -685,7 +712,7 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
 int run_step(sar_model* m, sar_kv* kv, const sar_batch* b, const void* in, float* h, float* logits,
              void* layer_out, cudaStream_t s) {
   Plan p;
-  std::vector<int32_t> meta;
+  thread_local std::vector<int32_t> meta;  // keeps its capacity from step to step
   SAR_TRY(plan_step(m, kv, b, logits != nullptr, &p, &meta));
   SAR_TRY(ensure_meta(m, p.total));
   SAR_TRY(ensure_partials(m, partials_floats(p, m->d)));
@@ -1216,7 +1243,7 @@ int sar_graph_update(sar_graph* g, const sar_batch* b, void* stream) {
   if (!g || !b) return set_error(SAR_ERR_INVALID_ARG, "graph: null argument");
   if (b->in_kind != g->in_kind) return set_error(SAR_ERR_INVALID_ARG, "graph: input kind differs from the captured step");
   Plan p;
-  std::vector<int32_t> meta;
+  thread_local std::vector<int32_t> meta;  // keeps its capacity from update to update
   SAR_TRY(plan_step(g->m, g->kv, b, false, &p, &meta));
   if (!same_shape(p, g->p))
     return set_error(SAR_ERR_INVALID_ARG, "graph: the batch's plan differs in shape from the captured step");
