@@ -15,10 +15,9 @@
 //               stage frees when S_j has been computed, a V stage after P_j V_j.
 //   warp 1      tensor memory (512 columns) and the single MMA-issuing thread:
 //               S_j = Q K_j^T (M 128 x N 128 x K 128; the fp32 queries enter
-//               as a high and a low 16-bit part, two MMAs each) into one of three
-//               S buffers, two blocks ahead of the softmax (so the next S is
-//               ready when a block's softmax ends); then O += P_j V_j with P_j
-//               read from tensor memory and V_j as an MN-major operand.
+//               as a high and a low 16-bit part, two MMAs each) into one of two
+//               S buffers, one block ahead of the softmax; then O += P_j V_j
+//               with P_j read from tensor memory and V_j as an MN-major operand.
 //   warps 2..9  two warps per row quarter (the TMEM lanes a warp may access),
 //               each with 64 of the 128 keys of every block: load and split the
 //               query, then per block the online softmax in base 2 (the two
@@ -60,16 +59,15 @@ constexpr int kBarOff = 2 * kQBytes + kStages * 2 * kKVBytes;  // after Q hi, Q 
 constexpr int kRedOff = kBarOff + 256;         // softmax exchange: [3][2][128] floats
 constexpr int kSmem = 1024 + kRedOff + 3 * 2 * kBQ * 4;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSBufs = 3;                      // S buffers: S_j in buffer j % 3, issued two blocks ahead
 constexpr uint32_t kColS = 128;               // S buffer b at columns [b*128, b*128+128); P overwrites the first 64
-constexpr uint32_t kColO = kSBufs * kColS;     // O at columns [384, 512)
+constexpr uint32_t kColO = 256;
 constexpr float kRescale = 8.f;                // log2 of the growth tolerated before rescaling O
 static_assert(kBQ == kChunkTileRowsTc, "the step plans tiles of kBQ rows");
 
 struct Bars {
   uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
-  uint64_t s_full[kSBufs], p_full[kSBufs];
-  uint64_t o_done[2], q_ready, mma_done;  // o_done[j % 2]: P.V of block j; mma_done: once, after every MMA
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_done, q_ready, mma_done;  // o_done: each P.V; mma_done: once, after every MMA
   uint32_t tmem_slot;
 };
 
@@ -121,12 +119,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->v_full[s]), 1);
       mbar_init(smem_u32(&bars->v_empty[s]), 1);
     }
-    for (int b = 0; b < kSBufs; ++b) {
-      mbar_init(smem_u32(&bars->s_full[b]), 1);
-      mbar_init(smem_u32(&bars->p_full[b]), 8);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars->s_full[s]), 1);
+      mbar_init(smem_u32(&bars->p_full[s]), 8);
     }
-    mbar_init(smem_u32(&bars->o_done[0]), 1);
-    mbar_init(smem_u32(&bars->o_done[1]), 1);
+    mbar_init(smem_u32(&bars->o_done), 1);
     mbar_init(smem_u32(&bars->q_ready), 8);
     mbar_init(smem_u32(&bars->mma_done), 1);
     fence_mbar_init();
@@ -228,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(smem_u32(&bars->k_full[s]), (uint32_t)((j / kStages) & 1), a.err, SITE_CHUNK_PIPE))
           return false;
         tc_fence_after();
-        const uint32_t d = tmem + (kColS * (uint32_t)(j % kSBufs));
+        const uint32_t d = tmem + (kColS * (uint32_t)(j & 1));
         const uint64_t db = s ? dk1 : dk0;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -236,24 +233,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_f16<false>(d, dq_hi + o, db + o, id_s, kk != 0);
           mma_f16<false>(d, dq_lo + o, db + o, id_s, 1);
         }
-        mma_commit(smem_u32(&bars->s_full[j % kSBufs]));
+        mma_commit(smem_u32(&bars->s_full[j & 1]));
         mma_commit(smem_u32(&bars->k_empty[s]));
         return true;
       };
-      // S_0 and S_1, then per block j: S_{j+2} (into the buffer block j - 1's
-      // P.V has just been issued from), P_j V_j
       if (ok) ok = issue_s(0);
-      if (ok && nb > 1) ok = issue_s(1);
       for (int j = 0; j < nb && ok; ++j) {
-        if (j + 2 < nb && !(ok = issue_s(j + 2))) break;
-        if (!(ok = mbar_wait(smem_u32(&bars->p_full[j % kSBufs]), (uint32_t)((j / kSBufs) & 1), a.err,
-                             SITE_CHUNK_PIPE)))
+        if (j + 1 < nb && !(ok = issue_s(j + 1))) break;
+        if (!(ok = mbar_wait(smem_u32(&bars->p_full[j & 1]), (uint32_t)((j >> 1) & 1), a.err, SITE_CHUNK_PIPE)))
           break;
         const int s = j % kStages;
         if (!(ok = mbar_wait(smem_u32(&bars->v_full[s]), (uint32_t)((j / kStages) & 1), a.err, SITE_CHUNK_PIPE)))
           break;
         tc_fence_after();
-        const uint32_t pcol = tmem + (kColS * (uint32_t)(j % kSBufs));
+        const uint32_t pcol = tmem + (kColS * (uint32_t)(j & 1));
         const uint64_t dvs = s ? dv1 : dv0;
 #pragma unroll
         for (int kk = 0; kk < kBKV / 16; ++kk) {
@@ -262,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(smem_u32(&bars->v_empty[s]));
-        mma_commit(smem_u32(&bars->o_done[j & 1]));
+        mma_commit(smem_u32(&bars->o_done));
       }
       // every MMA issued has completed before tensor memory is released
       mma_commit(smem_u32(&bars->mma_done));
@@ -322,10 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_used = -INFINITY, l = 0.f;
     bool alive = true;  // false once a wait gave up: work stops, the pair barriers stay matched
     for (int j = 0; j < nb; ++j) {
-      if (alive)
-        alive = warp_wait_bar(smem_u32(&bars->s_full[j % kSBufs]), (uint32_t)((j / kSBufs) & 1), a.err, SITE_CHUNK_PIPE);
+      if (alive) alive = warp_wait_bar(smem_u32(&bars->s_full[j & 1]), (uint32_t)((j >> 1) & 1), a.err, SITE_CHUNK_PIPE);
       tc_fence_after();
-      const uint32_t scol = lane_base + (kColS * (uint32_t)(j % kSBufs));
+      const uint32_t scol = lane_base + (kColS * (uint32_t)(j & 1));
       float sv[64];
       if (alive) {
 #pragma unroll
@@ -374,11 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // when a window masked all of its keys so far): rescale this warp's
       // dimension half once the previous P.V has landed
       if (alive && __any_sync(0xffffffffu, need && m_used != -INFINITY)) {
-        // P.V of block j - 1 has landed: o_done[(j - 1) % 2] completes once per
-        // two blocks, and the P.V three blocks back is done (S_j followed it),
-        // so this parity cannot alias
-        alive = warp_wait_bar(smem_u32(&bars->o_done[(j - 1) & 1]), (uint32_t)(((j - 1) >> 1) & 1), a.err,
-                              SITE_CHUNK_PIPE);
+        alive = warp_wait_bar(smem_u32(&bars->o_done), (uint32_t)((j - 1) & 1), a.err, SITE_CHUNK_PIPE);
         if (alive) {
           tc_fence_after();
 #pragma unroll 1
@@ -418,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (alive) tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (alive && lane == 0) mbar_arrive(smem_u32(&bars->p_full[j % kSBufs]));
+      if (alive && lane == 0) mbar_arrive(smem_u32(&bars->p_full[j & 1]));
     }
     // ---- O / l -> output row (this warp's 64 dims) ----
     red[(2 * 2 + hf) * kBQ + r] = l;  // row sum over both halves
