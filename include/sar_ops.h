@@ -106,7 +106,7 @@ int sar_op_rmsnorm(const void* x, const void* gain, void* y, int32_t rows, int32
  *   5: q|k|v rows      fp32 [max_tokens, (n_q_heads + 2 n_kv_heads) * head_dim]
  *                      (the projection with q and k rotated; k and v are
  *                      also in the pages, rounded to the storage type; for
- *                      head_dim 128 and more than 256 rows only q is kept in
+ *                      head_dim 128 and more than 128 rows only q is kept in
  *                      fp32 -- the attention kernels read k and v from the
  *                      pages) */
 int sar_model_debug_buffer(sar_model* m, int32_t which, void** out);
