@@ -276,11 +276,12 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
       return set_error(SAR_ERR_INVALID_ARG, "step: block table does not cover the positions");
     total_keys += span_of(dc.ctx_len);
   }
-  // decode work split: key ranges of `split` keys, about two CTAs per SM
-  // (one per resident slot), up to 4096 keys; fewer, longer ranges measured
-  // faster than more, shorter ones (less set-up and merging per key, and a
-  // shorter drain at the end of the grid): on the tau = 512 step 93.6 us at
-  // two per SM against 97.4 at four, 104 at three or six, 111 at eight
+  // decode work split: key ranges of `split` keys, a resident slot's share of
+  // the whole launch (two CTAs resident per SM), up to 4096 keys -- with each
+  // decode's ranges rounded up, about 2-4 CTAs per SM; fewer, longer ranges
+  // measured faster than more, shorter ones (less set-up and merging per key):
+  // on the tau = 512 step 93.6 us at a slot's share against 97.4 at half of
+  // it, 104 at two thirds or a third, 111 at a quarter
   const int sms = env.sms;
   int64_t split = (total_keys * d.n_kv_heads) / (2LL * sms);
   split = std::max<int64_t>(128, std::min<int64_t>(4096, (split + 15) / 16 * 16));

@@ -231,3 +231,19 @@ def test_plan_rejects_bad_batches():
         plan(d, [], [(i, 3, [i]) for i in range(200)], max_decodes=128)
     with pytest.raises(sar.SarError):  # an empty chunk
         plan(d, [(0, 0, 8, [0]), (1, 0, 0, [1])], [])
+
+
+def test_decode_ranges_are_a_resident_slots_share():
+    """The tau = 512 workload's 64 decodes (contexts uniform in [128, 4096]):
+    ranges of at most 4096 keys, each about one resident slot's share of the
+    launch (two CTAs resident per SM), so that with every decode's ranges
+    rounded up the (range x KV head) CTAs come to two to four per SM."""
+    rng = np.random.default_rng(0)
+    ctxs = [int(c) for c in rng.integers(128, 4097, 64)]
+    bts = [list(range(300 * i, 300 * i + c // PS + 1)) for i, c in enumerate(ctxs)]
+    for sms in (152, 148, 132):
+        p = plan(synth.MISTRAL_LAYER, [], [(i, c, bts[i]) for i, c in enumerate(ctxs)], sms=sms, pages=20000)
+        lengths = [k1 - k0 for _, k0, k1, _ in p["items"]]
+        assert max(lengths) <= 4096
+        ctas = len(p["items"]) * synth.MISTRAL_LAYER.n_kv_heads
+        assert 2 * sms <= ctas <= 4 * sms, (sms, ctas)
