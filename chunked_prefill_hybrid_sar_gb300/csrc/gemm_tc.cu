@@ -343,6 +343,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       (void)partial;
       const int acc = i & 1;
       const uint32_t accph = (uint32_t)((i >> 1) & 1);
+      // rotary epilogue (TMA path): the tile's first (cos, sin) chunk is
+      // loaded while the MMAs still run, so its L2 latency is off the epilogue
+      float4 cs_next[8];
+      bool cs_ready = false;
+      if constexpr (EPI == kEpiRope && !SWAP) {
+        const int row = mt * MSUB * 128 + lrow;
+        if (p.tma_out && p.rope.hd == 128 && row < p.M) {
+          const float4* csr0 = reinterpret_cast<const float4*>(p.rope.cs) + row;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) cs_next[e] = __ldg(csr0 + e * (size_t)p.rope.cs_ld);
+          cs_ready = true;
+        }
+      }
+      (void)cs_ready;
       if (alive) alive = warp_wait(smem_u32(&accf_bar[acc]), accph, p.err, SITE_GEMM_EPILOGUE);
       if (!alive && !(SWAP && (EPI == SAR_EPI_SWIGLU || EPI == kEpiRope))) break;
       tc_fence_after();
@@ -384,9 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // warp's 32 rows load one 512-byte run)
             const float4* csr = reinterpret_cast<const float4*>(rp.cs) + (row_ok ? row : 0);
             const size_t cld = (size_t)rp.cs_ld;
-            float4 cs_next[8];  // TMA path: the next (cos, sin) chunk, loaded one chunk ahead
+            // (TMA path: cs_next holds the next (cos, sin) chunk, loaded one chunk ahead)
+            if (!cs_ready) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) cs_next[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int e = 0; e < 8; ++e) cs_next[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll 1
             for (int hh = 0; hh < p.bn / rp.hd; ++hh) {
               const int col0 = nt * p.bn + hh * rp.hd;  // first column of this head
@@ -411,7 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t stg = epi_stage + (uint32_t)(q * 4 * kEpiBoxBytes + hh * 8192);
                 if (lane == 0) bulk_wait_read_all();  // earlier stores have read the staging
                 __syncwarp();
-                if (is_k && row_ok) {
+                // chunk 0 of this head (the tile's first, for s == 0 and head 0, already loaded)
+                if (is_k && row_ok && !(cs_ready && s == 0 && hh == 0)) {
 #pragma unroll
                   for (int e = 0; e < 8; ++e) cs_next[e] = __ldg(csr + e * cld);
                 }
@@ -509,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const int c0 = nt * p.bn + h * rp.hd;
                   return h < heads && c0 < p.N && c0 / rp.hd < rp.qh + rp.kvh;
                 };
-                if (hh == 0 && row_ok && rotates(0)) {
+                if (hh == 0 && row_ok && rotates(0) && !(cs_ready && s == 0)) {
 #pragma unroll
                   for (int e = 0; e < 8; ++e) cs_next[e] = __ldg(csr + e * cld);
                 }
