@@ -11,13 +11,17 @@
 // of one query head (352 threads):
 //   warps 0, 10 TMA producers of K and of V: each 128-key block is 8 runs of
 //               16 keys x 2 dim halves (one box each: 16 keys x 64 dims of one
-//               page, 128-byte swizzle) into a 2-stage ring per tensor; a K
-//               stage frees when S_j has been computed, a V stage after P_j V_j.
+//               page, 128-byte swizzle) into a ring of 3 K and one of 2 V
+//               stages; a K stage frees when S_j has been computed (S runs two
+//               blocks ahead, so K is fetched three ahead), a V stage after
+//               P_j V_j.  Eight lanes issue a block's sixteen boxes, with the
+//               pages read from the block table a group of blocks ahead.
 //   warp 1      tensor memory (512 columns) and the single MMA-issuing thread:
-//               S_j = Q K_j^T (M 128 x N 128 x K 128; the fp32 queries enter
-//               as a high and a low 16-bit part, two MMAs each) into one of two
-//               S buffers, one block ahead of the softmax; then O += P_j V_j
-//               with P_j read from tensor memory and V_j as an MN-major operand.
+//               S_j = Q K_j^T (M 128 x N 128 x K 128; the fp32 queries are
+//               rounded once to the storage type, as the keys are) into one of three
+//               S buffers, two blocks ahead of the softmax (so the next S is
+//               ready when a block's softmax ends); then O += P_j V_j with P_j
+//               read from tensor memory and V_j as an MN-major operand.
 //   warps 2..9  two warps per row quarter (the TMEM lanes a warp may access),
 //               each with 64 of the 128 keys of every block: load and split the
 //               query, then per block the online softmax in base 2 (the two
@@ -54,20 +58,27 @@ constexpr int kThreads = 352;                  // 11 warps
 constexpr int kRegion = 128 * 128;             // [128 rows][128 bytes]: 64 dims of 128 rows
 constexpr int kQBytes = 2 * kRegion;           // one 16-bit copy of the Q tile (two dim halves)
 constexpr int kKVBytes = 2 * kRegion;          // K (or V) of one block
-constexpr int kStages = 2;
-constexpr int kBarOff = 2 * kQBytes + kStages * 2 * kKVBytes;  // after Q hi, Q lo, stages
+constexpr int kKStages = 3;                    // one per S buffer: S_j's barrier frees K stage j % 3
+constexpr int kVStages = 2;                    // one per P.V barrier: o_done[j % 2] frees V stage j % 2
+constexpr int kBarOff = kQBytes + (kKStages + kVStages) * kKVBytes;  // after Q, the K stages, the V stages
 constexpr int kRedOff = kBarOff + 256;         // softmax exchange: [3][2][128] floats
 constexpr int kSmem = 1024 + kRedOff + 3 * 2 * kBQ * 4;
+static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t kTmemCols = 512;
+constexpr int kSBufs = 3;                      // S buffers: S_j in buffer j % 3, issued two blocks ahead
 constexpr uint32_t kColS = 128;               // S buffer b at columns [b*128, b*128+128); P overwrites the first 64
-constexpr uint32_t kColO = 256;
+static_assert(kKStages == kSBufs, "K stages are freed by the S barriers");
+constexpr uint32_t kColO = kSBufs * kColS;     // O at columns [384, 512)
 constexpr float kRescale = 8.f;                // log2 of the growth tolerated before rescaling O
 static_assert(kBQ == kChunkTileRowsTc, "the step plans tiles of kBQ rows");
 
 struct Bars {
-  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
-  uint64_t s_full[2], p_full[2];
-  uint64_t o_done, q_ready, mma_done;  // o_done: each P.V; mma_done: once, after every MMA
+  // a K stage is free again once S_j (buffer j % 3, stage j % 3) has landed,
+  // a V stage once P_j V_j has: s_full and o_done serve as the rings' empty
+  // barriers
+  uint64_t k_full[kKStages], v_full[kVStages];
+  uint64_t s_full[kSBufs], p_full[kSBufs];
+  uint64_t o_done[2], q_ready, mma_done;  // o_done[j % 2]: P.V of block j; mma_done: once, after every MMA
   uint32_t tmem_slot;
 };
 
@@ -102,9 +113,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   // Q hi, Q lo, then per stage K then V; each a pair of 16 KB dim-half regions
-  const uint32_t q_hi = sbase, q_lo = sbase + kQBytes;
-  auto k_reg = [&](int s) { return sbase + 2 * kQBytes + (uint32_t)(s * 2 * kKVBytes); };
-  auto v_reg = [&](int s) { return sbase + 2 * kQBytes + (uint32_t)(s * 2 * kKVBytes + kKVBytes); };
+  const uint32_t q_s = sbase;
+  auto k_reg = [&](int s) { return sbase + kQBytes + (uint32_t)(s * kKVBytes); };
+  auto v_reg = [&](int s) { return sbase + kQBytes + (uint32_t)((kKStages + s) * kKVBytes); };
   Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -113,17 +124,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kh = hq / G;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(smem_u32(&bars->k_full[s]), 1);
-      mbar_init(smem_u32(&bars->k_empty[s]), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(smem_u32(&bars->v_full[s]), 1);
-      mbar_init(smem_u32(&bars->v_empty[s]), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&bars->s_full[s]), 1);
-      mbar_init(smem_u32(&bars->p_full[s]), 8);
+    for (int b = 0; b < kSBufs; ++b) {
+      mbar_init(smem_u32(&bars->s_full[b]), 1);
+      mbar_init(smem_u32(&bars->p_full[b]), 8);
     }
-    mbar_init(smem_u32(&bars->o_done), 1);
+    mbar_init(smem_u32(&bars->o_done[0]), 1);
+    mbar_init(smem_u32(&bars->o_done[1]), 1);
     mbar_init(smem_u32(&bars->q_ready), 8);
     mbar_init(smem_u32(&bars->mma_done), 1);
     fence_mbar_init();
@@ -155,55 +167,69 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 || warp == 10) {
     // ---------------- producers: warp 0 K, warp 10 V ----------------
-    if (lane == 0) {
-      const bool is_k = warp == 0;
-      const CUtensorMap* map = is_k ? &tmk : &tmv;
-      uint64_t* full = is_k ? bars->k_full : bars->v_full;
-      uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
-      tma_prefetch_desc(map);
-      const int last_run = (n_keys - 1) / kRun;
-      bool ok = (n_keys - 1) / a.page_size < bt_len;
-      if (!ok && is_k) report(a.err, SAR_ERR_BOUNDS, SITE_CHUNK_BOUNDS, n_keys);
-      // the page of every 16-key run of a block, read from the block table one
-      // block ahead (all eight loads in flight together, not one per box);
-      // runs past the last key repeat the last one (finite data, masked)
-      int pg[kRunsPerBlock], po[kRunsPerBlock];
-      auto pages_of = [&](int j) {  // j counts from block j0
-#pragma unroll
-        for (int g = 0; g < kRunsPerBlock; ++g) {
-          const int key = min((j0 + j) * kRunsPerBlock + g, last_run) * kRun;
-          const int bi = key / a.page_size;
-          pg[g] = bt[bi];
-          po[g] = key - bi * a.page_size;
-        }
-      };
-      if (ok) pages_of(0);
-      for (int j = 0; j < nb && ok; ++j) {
-        const int s = j % kStages;
-        if (!mbar_wait(smem_u32(&empty[s]), (uint32_t)(((j / kStages) & 1) ^ 1), a.err, SITE_CHUNK_PIPE)) {
-          ok = false;
-          break;
-        }
-        const uint32_t fb = smem_u32(&full[s]);
-        const uint32_t dst = is_k ? k_reg(s) : v_reg(s);
-        mbar_expect_tx(fb, (uint32_t)kKVBytes);
-#pragma unroll
-        for (int g = 0; g < kRunsPerBlock; ++g) {
-          int page = pg[g];
-          if (page < 0 || page >= a.num_pages) {
-            report(a.err, SAR_ERR_BOUNDS, SITE_CHUNK_BOUNDS, page);
-            page = 0;
-          }
-          const int row = (page * a.kvh + kh) * a.page_size + po[g];
-          tma_load_2d(dst + g * (kRun * 128), map, 0, row, fb);
-          tma_load_2d(dst + kRegion + g * (kRun * 128), map, 64, row, fb);
-        }
-        if (j + 1 < nb) pages_of(j + 1);
+    // The whole warp serves one ring: lane 0 waits for a free stage and arms
+    // its barrier, lanes 0..7 issue the two boxes of run g = lane, and the
+    // page of every run is read from the block table four to eight blocks
+    // ahead (lane L holds run L % 8 of block L / 8 of a group of four), so
+    // neither the table's latency nor a serial chain of sixteen copy issues
+    // sits between a freed stage and its next block.
+    const bool is_k = warp == 0;
+    const CUtensorMap* map = is_k ? &tmk : &tmv;
+    uint64_t* full = is_k ? bars->k_full : bars->v_full;
+    uint64_t* empty = is_k ? bars->s_full : bars->o_done;
+    const int stages = is_k ? kKStages : kVStages;
+    if (lane == 0) tma_prefetch_desc(map);
+    const int last_run = (n_keys - 1) / kRun;
+    bool ok = (n_keys - 1) / a.page_size < bt_len;
+    if (!ok && is_k && lane == 0) report(a.err, SAR_ERR_BOUNDS, SITE_CHUNK_BOUNDS, n_keys);
+    const int g = lane & 7, sub = lane >> 3;
+    // runs past the last key repeat the last one (finite data, masked)
+    auto page_of = [&](int jb, int& page, int& off) {  // block jb + sub counts from block j0
+      const int key = min((j0 + jb + sub) * kRunsPerBlock + g, last_run) * kRun;
+      const int bi = key / a.page_size;
+      page = bt[bi];
+      off = key - bi * a.page_size;
+    };
+    int pa = 0, oa = 0, pb = 0, ob = 0;  // this group of four blocks, the next
+    if (ok) {
+      page_of(0, pa, oa);
+      if (nb > 4) page_of(4, pb, ob);
+    }
+    for (int j = 0; j < nb && ok; ++j) {
+      const int i = j & 3;
+      if (i == 0 && j > 0) {
+        pa = pb;
+        oa = ob;
+        if (j + 4 < nb) page_of(j + 4, pb, ob);
       }
-      // no copy may still be in flight when the CTA leaves
-      const int first = max(0, nb - kStages);
+      const int s = j % stages;
+      int w = 1;
+      if (lane == 0) w = mbar_wait(smem_u32(&empty[s]), (uint32_t)(((j / stages) & 1) ^ 1), a.err, SITE_CHUNK_PIPE);
+      if (!__shfl_sync(0xffffffffu, w, 0)) {
+        ok = false;
+        break;
+      }
+      const uint32_t fb = smem_u32(&full[s]);
+      const uint32_t dst = is_k ? k_reg(s) : v_reg(s);
+      if (lane == 0) mbar_expect_tx(fb, (uint32_t)kKVBytes);
+      __syncwarp();
+      int page = __shfl_sync(0xffffffffu, pa, (i << 3) | g);
+      const int po = __shfl_sync(0xffffffffu, oa, (i << 3) | g);
+      if (lane < kRunsPerBlock) {
+        if (page < 0 || page >= a.num_pages) {
+          report(a.err, SAR_ERR_BOUNDS, SITE_CHUNK_BOUNDS, page);
+          page = 0;
+        }
+        const int row = (page * a.kvh + kh) * a.page_size + po;
+        tma_load_2d(dst + g * (kRun * 128), map, 0, row, fb);
+        tma_load_2d(dst + kRegion + g * (kRun * 128), map, 64, row, fb);
+      }
+    }
+    // no copy may still be in flight when the CTA leaves
+    if (lane == 0) {
+      const int first = max(0, nb - stages);
       for (int j = first; j < nb && ok; ++j)
-        ok = mbar_wait(smem_u32(&empty[j % kStages]), (uint32_t)((j / kStages) & 1), a.err, SITE_CHUNK_PIPE);
+        ok = mbar_wait(smem_u32(&empty[j % stages]), (uint32_t)((j / stages) & 1), a.err, SITE_CHUNK_PIPE);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -213,40 +239,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_s = idesc_128x128(fmt, 0), id_pv = idesc_128x128(fmt, 1);
       // descriptors built once: a byte offset b within shared memory moves a
       // descriptor's start-address field (address / 16) by b / 16, so each MMA
-      // adds a constant (this thread issues 24 small MMAs per key block and
+      // adds a constant (this thread issues 16 small MMAs per key block and
       // shares its scheduler with two softmax warps)
-      const uint64_t dq_hi = sw128_desc(q_hi), dq_lo = sw128_desc(q_lo);
-      static_assert(kStages == 2, "one descriptor per stage, chosen by a select");
-      const uint64_t dk0 = sw128_desc(k_reg(0)), dk1 = sw128_desc(k_reg(1));
+      const uint64_t dq = sw128_desc(q_s);
+      static_assert(kKStages == 3 && kVStages == 2, "one descriptor per stage, chosen by a select");
+      const uint64_t dk0 = sw128_desc(k_reg(0)), dk1 = sw128_desc(k_reg(1)), dk2 = sw128_desc(k_reg(2));
       const uint64_t dv0 = sw128_desc_mn(v_reg(0), kRegion, 1024), dv1 = sw128_desc_mn(v_reg(1), kRegion, 1024);
       bool ok = mbar_wait(smem_u32(&bars->q_ready), 0, a.err, SITE_CHUNK_PIPE);
       auto issue_s = [&](int j) -> bool {
-        const int s = j % kStages;
-        if (!mbar_wait(smem_u32(&bars->k_full[s]), (uint32_t)((j / kStages) & 1), a.err, SITE_CHUNK_PIPE))
+        const int s = j % kKStages;
+        if (!mbar_wait(smem_u32(&bars->k_full[s]), (uint32_t)((j / kKStages) & 1), a.err, SITE_CHUNK_PIPE))
           return false;
         tc_fence_after();
-        const uint32_t d = tmem + (kColS * (uint32_t)(j & 1));
-        const uint64_t db = s ? dk1 : dk0;
+        const uint32_t d = tmem + (kColS * (uint32_t)(j % kSBufs));
+        const uint64_t db = s == 0 ? dk0 : (s == 1 ? dk1 : dk2);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint64_t o = (uint64_t)(((kk >> 2) * kRegion + (kk & 3) * 32) >> 4);
-          mma_f16<false>(d, dq_hi + o, db + o, id_s, kk != 0);
-          mma_f16<false>(d, dq_lo + o, db + o, id_s, 1);
+          mma_f16<false>(d, dq + o, db + o, id_s, kk != 0);
         }
-        mma_commit(smem_u32(&bars->s_full[j & 1]));
-        mma_commit(smem_u32(&bars->k_empty[s]));
+        mma_commit(smem_u32(&bars->s_full[j % kSBufs]));
         return true;
       };
+      // S_0 and S_1, then per block j: S_{j+2} (into the buffer block j - 1's
+      // P.V has just been issued from), P_j V_j
       if (ok) ok = issue_s(0);
+      if (ok && nb > 1) ok = issue_s(1);
       for (int j = 0; j < nb && ok; ++j) {
-        if (j + 1 < nb && !(ok = issue_s(j + 1))) break;
-        if (!(ok = mbar_wait(smem_u32(&bars->p_full[j & 1]), (uint32_t)((j >> 1) & 1), a.err, SITE_CHUNK_PIPE)))
+        if (j + 2 < nb && !(ok = issue_s(j + 2))) break;
+        if (!(ok = mbar_wait(smem_u32(&bars->p_full[j % kSBufs]), (uint32_t)((j / kSBufs) & 1), a.err,
+                             SITE_CHUNK_PIPE)))
           break;
-        const int s = j % kStages;
-        if (!(ok = mbar_wait(smem_u32(&bars->v_full[s]), (uint32_t)((j / kStages) & 1), a.err, SITE_CHUNK_PIPE)))
+        const int s = j % kVStages;
+        if (!(ok = mbar_wait(smem_u32(&bars->v_full[s]), (uint32_t)((j / kVStages) & 1), a.err, SITE_CHUNK_PIPE)))
           break;
         tc_fence_after();
-        const uint32_t pcol = tmem + (kColS * (uint32_t)(j & 1));
+        const uint32_t pcol = tmem + (kColS * (uint32_t)(j % kSBufs));
         const uint64_t dvs = s ? dv1 : dv0;
 #pragma unroll
         for (int kk = 0; kk < kBKV / 16; ++kk) {
@@ -254,8 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_f16_ts(tmem + kColO, pcol + kk * 8, dvs + (uint64_t)(kk * (16 * 128 / 16)), id_pv,
                      (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(smem_u32(&bars->v_empty[s]));
-        mma_commit(smem_u32(&bars->o_done));
+        mma_commit(smem_u32(&bars->o_done[j & 1]));
       }
       // every MMA issued has completed before tensor memory is released
       mma_commit(smem_u32(&bars->mma_done));
@@ -276,8 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* red = reinterpret_cast<float*>(smem + kRedOff);  // [2 parities][2 halves][128 rows]
     auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + qq) : "memory"); };
     {
-      // this half of the query row -> scaled, split into 16-bit high and low
-      // parts, swizzled as the MMA reads it (dim half hf is Q region hf)
+      // this half of the query row -> scaled by log2(e) / sqrt(d), rounded
+      // to 16 bits, swizzled as the MMA reads it (dim half hf is Q region hf)
       const float qscale = rsqrtf((float)kD) * 1.4426950408889634f;
       const float* qp = a.q32 + (size_t)(row0 + r) * a.ld32 + (size_t)hq * kD + hf * 64;
 #pragma unroll 1
@@ -292,19 +319,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = 0.f;
         }
-        uint32_t hi[4], lo[4];
+        uint32_t qv[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float x0 = x[2 * e] * qscale, x1 = x[2 * e + 1] * qscale;
-          hi[e] = Elem<T>::pack(x0, x1);
-          lo[e] = Elem<T>::pack(x0 - Elem<T>::lo(hi[e]), x1 - Elem<T>::hi(hi[e]));
-        }
+        for (int e = 0; e < 4; ++e) qv[e] = Elem<T>::pack(x[2 * e] * qscale, x[2 * e + 1] * qscale);
         const uint32_t off = (uint32_t)(hf * kRegion + r * 128 + ((ch ^ (r & 7)) << 4));
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(q_hi + off), "r"(hi[0]), "r"(hi[1]),
-                     "r"(hi[2]), "r"(hi[3])
-                     : "memory");
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(q_lo + off), "r"(lo[0]), "r"(lo[1]),
-                     "r"(lo[2]), "r"(lo[3])
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(q_s + off), "r"(qv[0]), "r"(qv[1]),
+                     "r"(qv[2]), "r"(qv[3])
                      : "memory");
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
@@ -315,9 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_used = -INFINITY, l = 0.f;
     bool alive = true;  // false once a wait gave up: work stops, the pair barriers stay matched
     for (int j = 0; j < nb; ++j) {
-      if (alive) alive = warp_wait_bar(smem_u32(&bars->s_full[j & 1]), (uint32_t)((j >> 1) & 1), a.err, SITE_CHUNK_PIPE);
+      if (alive)
+        alive = warp_wait_bar(smem_u32(&bars->s_full[j % kSBufs]), (uint32_t)((j / kSBufs) & 1), a.err, SITE_CHUNK_PIPE);
       tc_fence_after();
-      const uint32_t scol = lane_base + (kColS * (uint32_t)(j & 1));
+      const uint32_t scol = lane_base + (kColS * (uint32_t)(j % kSBufs));
       float sv[64];
       if (alive) {
 #pragma unroll
@@ -366,7 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // when a window masked all of its keys so far): rescale this warp's
       // dimension half once the previous P.V has landed
       if (alive && __any_sync(0xffffffffu, need && m_used != -INFINITY)) {
-        alive = warp_wait_bar(smem_u32(&bars->o_done), (uint32_t)((j - 1) & 1), a.err, SITE_CHUNK_PIPE);
+        // P.V of block j - 1 has landed: o_done[(j - 1) % 2] completes once per
+        // two blocks, and the P.V three blocks back is done (S_j followed it),
+        // so this parity cannot alias
+        alive = warp_wait_bar(smem_u32(&bars->o_done[(j - 1) & 1]), (uint32_t)(((j - 1) >> 1) & 1), a.err,
+                              SITE_CHUNK_PIPE);
         if (alive) {
           tc_fence_after();
 #pragma unroll 1
@@ -406,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (alive) tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (alive && lane == 0) mbar_arrive(smem_u32(&bars->p_full[j & 1]));
+      if (alive && lane == 0) mbar_arrive(smem_u32(&bars->p_full[j % kSBufs]));
     }
     // ---- O / l -> output row (this warp's 64 dims) ----
     red[(2 * 2 + hf) * kBQ + r] = l;  // row sum over both halves
