@@ -61,7 +61,11 @@ constexpr int kSmemPerSm = 233472;        // 228 KB of shared memory per SM
 constexpr int kBarBytes = 1024;           // barriers + TMEM slot (+ alignment)
 constexpr int kSwapXchg = 64 * 17 * 4;    // swap-mode SwiGLU exchange buffer
 constexpr int kSwapXchgRope = 128 * 17 * 4;  // swap-mode rotary exchange buffer
-constexpr int kPrefetch = 16;             // K-slabs of the weight tile prefetched into L2 ahead
+// K-slabs of the weight tile prefetched into L2 ahead of the shared-memory
+// ring (which holds 5-8 more).  A short distance: deep prefetches queue ahead
+// of the ring's own loads (the tau = 512 step took 329.4 us at 16 slabs, 326.2
+// at 8, 323.7 at 1-4, 325.0 with none)
+constexpr int kPrefetch = 3;
 constexpr int kEpiBox = 32;               // TMA epilogue boxes: 32 rows x 128 bytes (32 fp32 or 64 16-bit columns)
 constexpr int kEpiBoxBytes = kEpiBox * kEpiBox * 4;
 constexpr int kEpiStage = 4 * 2 * kEpiBoxBytes;  // two boxes per epilogue warp
@@ -344,12 +348,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int acc = i & 1;
       const uint32_t accph = (uint32_t)((i >> 1) & 1);
       // rotary epilogue (TMA path): the tile's first (cos, sin) chunk is
-      // loaded while the MMAs still run, so its L2 latency is off the epilogue
+      // loaded while the MMAs still run, so its L2 latency is off the epilogue.
+      // On this CTA's last tile the operand stages are idle once its MMAs have
+      // completed: each warp then copies its 32 rows' whole (cos, sin) table
+      // (32 float4 per row, 16 KB) into them in one batch, instead of paying
+      // the L2 latency once per 16-frequency chunk
+      const bool last_unit = wk.t >= wk.end;
       float4 cs_next[8];
       bool cs_ready = false;
+      bool cs_smem = false;
+      const uint32_t cs_base = smem_u32(smem) + (uint32_t)(q * 32 * 32 * 16);
       if constexpr (EPI == kEpiRope && !SWAP) {
         const int row = mt * MSUB * 128 + lrow;
-        if (p.tma_out && p.rope.hd == 128 && row < p.M) {
+        // (a tile of v heads only rotates nothing)
+        const bool rotated = (nt * p.bn) / p.rope.hd < p.rope.qh + p.rope.kvh;
+        cs_smem = last_unit && rotated && p.tma_out && p.rope.hd == 128 && MSUB == 1 &&
+                  4 * 32 * 32 * 16 <= p.stages * p.stage_bytes;
+        if (p.tma_out && p.rope.hd == 128 && row < p.M && !cs_smem) {
           const float4* csr0 = reinterpret_cast<const float4*>(p.rope.cs) + row;
 #pragma unroll
           for (int e = 0; e < 8; ++e) cs_next[e] = __ldg(csr0 + e * (size_t)p.rope.cs_ld);
@@ -361,6 +376,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!alive && !(SWAP && (EPI == SAR_EPI_SWIGLU || EPI == kEpiRope))) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * acc_cols);
+      if constexpr (EPI == kEpiRope && !SWAP) {
+        // every MMA of this CTA has completed (and with it every stage load):
+        // the stages are free for this warp's [32 float4][32 rows] table
+        const int row = mt * MSUB * 128 + lrow;
+        if (cs_smem && row < p.M) {
+          const float4* csr0 = reinterpret_cast<const float4*>(p.rope.cs) + row;
+#pragma unroll 8
+          for (int e = 0; e < 32; ++e) cp_async16(cs_base + (uint32_t)((e * 32 + lane) * 16), csr0 + e * (size_t)p.rope.cs_ld, 16);
+          cp_async_commit();
+          cp_async_wait<0>();  // this lane reads back only its own row's entries
+        }
+      }
 
       if constexpr (!SWAP) {
 #pragma unroll 1
@@ -428,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) bulk_wait_read_all();  // earlier stores have read the staging
                 __syncwarp();
                 // chunk 0 of this head (the tile's first, for s == 0 and head 0, already loaded)
-                if (is_k && row_ok && !(cs_ready && s == 0 && hh == 0)) {
+                if (is_k && row_ok && !cs_smem && !(cs_ready && s == 0 && hh == 0)) {
 #pragma unroll
                   for (int e = 0; e < 8; ++e) cs_next[e] = __ldg(csr + e * cld);
                 }
@@ -447,11 +474,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                   } else {
                     float4 cc[8];
+                    if (cs_smem) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) cc[e] = cs_next[e];
-                    if (row_ok && j < 3) {
+                      for (int e = 0; e < 8; ++e) cc[e] = lds_f4(cs_base + (uint32_t)(((j * 8 + e) * 32 + lane) * 16));
+                    } else {
 #pragma unroll
-                      for (int e = 0; e < 8; ++e) cs_next[e] = __ldg(csr + ((j + 1) * 8 + e) * cld);
+                      for (int e = 0; e < 8; ++e) cc[e] = cs_next[e];
+                      if (row_ok && j < 3) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) cs_next[e] = __ldg(csr + ((j + 1) * 8 + e) * cld);
+                      }
                     }
                     tmem_wait_ld();
 #pragma unroll
@@ -526,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const int c0 = nt * p.bn + h * rp.hd;
                   return h < heads && c0 < p.N && c0 / rp.hd < rp.qh + rp.kvh;
                 };
-                if (hh == 0 && row_ok && rotates(0) && !(cs_ready && s == 0)) {
+                if (hh == 0 && row_ok && rotates(0) && !cs_smem && !(cs_ready && s == 0)) {
 #pragma unroll
                   for (int e = 0; e < 8; ++e) cs_next[e] = __ldg(csr + e * cld);
                 }
@@ -559,14 +591,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                       }
                     } else {
                       float4 cc[8];
+                      if (cs_smem) {
 #pragma unroll
-                      for (int e = 0; e < 8; ++e) cc[e] = cs_next[e];
-                      // the chunk after this one: j + 1 of this head, else chunk 0 of the next
-                      const bool more = j < 3 || rotates(hh + 1);
-                      if (row_ok && more) {
-                        const int jn = (j + 1) & 3;
+                        for (int e = 0; e < 8; ++e) cc[e] = lds_f4(cs_base + (uint32_t)(((j * 8 + e) * 32 + lane) * 16));
+                      } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) cs_next[e] = __ldg(csr + (jn * 8 + e) * cld);
+                        for (int e = 0; e < 8; ++e) cc[e] = cs_next[e];
+                        // the chunk after this one: j + 1 of this head, else chunk 0 of the next
+                        const bool more = j < 3 || rotates(hh + 1);
+                        if (row_ok && more) {
+                          const int jn = (j + 1) & 3;
+#pragma unroll
+                          for (int e = 0; e < 8; ++e) cs_next[e] = __ldg(csr + (jn * 8 + e) * cld);
+                        }
                       }
                       tmem_wait_ld();
 #pragma unroll
