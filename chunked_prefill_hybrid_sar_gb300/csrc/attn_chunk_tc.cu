@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
-  pdl_wait();
+  if (!a.wait_at_end) pdl_wait();
   pdl_launch_dependents();
   // this CTA's tile (the table lists the most keys first)
   const int4 tl = reinterpret_cast<const int4*>(a.tiles)[2 * blockIdx.x];
@@ -486,6 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc<false>(tmem, kTmemCols);
   }
+  // (run behind the decode attention kernel: the kernels after this one wait
+  // for this grid only, so it completes after that one)
+  if (a.wait_at_end) pdl_wait();
 }
 
 // Merges the shares of a split tile: out = sum_i O_i 2^(m_i - M) / sum_i l_i 2^(m_i - M)

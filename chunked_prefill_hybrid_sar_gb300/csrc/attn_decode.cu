@@ -404,7 +404,7 @@ int launch_impl(const DecodeAttnArgs& a, const CUtensorMap& tmk, const CUtensorM
   count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "decode attention launch");
-  if (a.partials) {
+  if (a.partials && !a.defer_combine) {
     launch_pdl(decode_combine_kernel<T, D, COMPUTED>, dim3(a.n_decode, a.qh), dim3(D), 0, s, a);
     count_launches(1);
     e = cudaGetLastError();
@@ -429,6 +429,22 @@ int make_kv_tmap(CUtensorMap* map, const void* pages, int num_pages, int kvh, in
                  int storage) {
   // rows = (page, head, slot) triples, columns = head_dim; boxes of 16 slots x 64 dimensions
   return make_tmap_16(map, pages, (uint64_t)num_pages * kvh * page_size, head_dim, kBlockKeys, storage);
+}
+
+int launch_decode_combine(const DecodeAttnArgs& a, cudaStream_t s) {
+  if (a.n_items <= 0 || !a.partials) return SAR_OK;
+  const bool bf = a.storage == SAR_STORAGE_BF16;
+  if (a.d == 128)
+    launch_pdl(bf ? decode_combine_kernel<__nv_bfloat16, 128> : decode_combine_kernel<__half, 128>,
+               dim3(a.n_decode, a.qh), dim3(128), 0, s, a);
+  else if (a.d == 64)
+    launch_pdl(bf ? decode_combine_kernel<__nv_bfloat16, 64> : decode_combine_kernel<__half, 64>,
+               dim3(a.n_decode, a.qh), dim3(64), 0, s, a);
+  else
+    return set_error(SAR_ERR_UNSUPPORTED, "decode combine: head_dim must be 64 or 128");
+  count_launches(1);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SAR_OK : cuda_error(e, "decode combine launch");
 }
 
 int launch_decode_attention(const DecodeAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,

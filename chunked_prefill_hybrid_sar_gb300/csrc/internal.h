@@ -189,6 +189,9 @@ struct DecodeAttnArgs {
   // device-computed work split (used by the entry point that allocates nothing)
   const int32_t* ctx_lens = nullptr;  // [n_decode]
   int split_keys = 0, max_splits = 0, bt_stride = 0;
+  // the partials' merge is launched separately (launch_decode_combine), so
+  // that another kernel can run between the two
+  bool defer_combine = false;
 };
 // Tensor map over one layer's K or V pages viewed as rows of head_dim values
 // (one row per page x head x slot), 16-row x 64-column boxes, 128-byte swizzle.
@@ -196,6 +199,8 @@ int make_kv_tmap(CUtensorMap* map, const void* pages, int num_pages, int kvh, in
                  int storage);
 int launch_decode_attention(const DecodeAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                             cudaStream_t s);
+// The merge of a deferred launch (nothing to do when there are no partials).
+int launch_decode_combine(const DecodeAttnArgs& a, cudaStream_t s);
 
 struct ChunkAttnArgs {
   const float* q32;          // chunk query rows in fp32 (batch rows); row stride ld32
@@ -221,6 +226,11 @@ struct ChunkAttnArgs {
   int ld, ld_out, qh, kvh, d, page_size, num_pages, storage;
   int* err;
   int window = 0;            // the row at position p sees keys (p - window, p]; 0 = all of [0, p]
+  // tcgen05 kernel launched right behind the decode attention kernel, whose
+  // output it does not read: it starts without waiting for that kernel (its
+  // inputs were complete before that kernel released its dependents) and
+  // waits for it only before exiting, so the kernels after it still see both
+  int wait_at_end = 0;
 };
 // Query rows per tile: the warp-MMA kernel (attn_chunk.cu) and the tcgen05 one.
 constexpr int kChunkTileRows = 64;

@@ -606,9 +606,8 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
       SAR_TRY(check(cudaStreamWaitEvent(m->side, m->ev_fork, 0), "overlap: side wait"));
       sc = m->side;
     }
+    sar::ChunkAttnArgs ca{};
     if (p.Lp > 0) {
-      Prof pr(m, SAR_K_CHUNK_ATTN, s);
-      sar::ChunkAttnArgs ca;
       ca.q32 = m->qkv32;
       ca.ld32 = m->qkv_n;
       ca.out = m->attn;
@@ -630,14 +629,9 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
       ca.partials = partials + decode_partials_floats(p, d);
       ca.comb = md + p.o_comb;
       ca.n_comb = p.n_comb;
-      if (sar::chunk_attention_tc_supported(ca))
-        SAR_TRY(sar::launch_chunk_attention_tc(ca, kv->tmk[l], kv->tmv[l], sc));
-      else
-        SAR_TRY(sar::launch_chunk_attention(ca, sc));
     }
+    sar::DecodeAttnArgs da{};
     if (p.Bd > 0) {
-      Prof pr(m, SAR_K_DECODE_ATTN, s);
-      sar::DecodeAttnArgs da;
       da.qkv = nullptr;  // the fp32 query rows below are read instead
       da.out = m->attn + (size_t)p.Lp * m->qd;
       da.storage = d.storage;
@@ -664,7 +658,33 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
       da.num_pages = kv->num_pages;
       da.err = m->err;
       da.window = d.sliding_window;
+    }
+    auto run_chunk = [&](cudaStream_t st) -> int {
+      Prof pr(m, SAR_K_CHUNK_ATTN, s);
+      if (sar::chunk_attention_tc_supported(ca)) return sar::launch_chunk_attention_tc(ca, kv->tmk[l], kv->tmv[l], st);
+      return sar::launch_chunk_attention(ca, st);
+    };
+    // The chunk and decode attention kernels read the QKV projection's output
+    // only.  When both run on this stream with the tcgen05 chunk kernel, the
+    // decode kernel goes first and the chunk kernel right behind it, without
+    // waiting for it: its CTAs take the SMs the decode kernel's draining tail
+    // leaves idle (a memory-bound kernel's last, shortest ranges), and it
+    // waits for the decode kernel only before exiting; the decodes' merge
+    // follows.  (Not while profiling: the per-kernel events would serialise
+    // the two anyway.)
+    const bool behind = !ov && !m->prof && p.Lp > 0 && p.Bd > 0 && sar::chunk_attention_tc_supported(ca);
+    if (behind) {
+      da.defer_combine = true;
+      ca.wait_at_end = 1;
       SAR_TRY(sar::launch_decode_attention(da, kv->tmk[l], kv->tmv[l], s));
+      SAR_TRY(run_chunk(s));
+      SAR_TRY(sar::launch_decode_combine(da, s));
+    } else {
+      if (p.Lp > 0) SAR_TRY(run_chunk(sc));
+      if (p.Bd > 0) {
+        Prof pr(m, SAR_K_DECODE_ATTN, s);
+        SAR_TRY(sar::launch_decode_attention(da, kv->tmk[l], kv->tmv[l], s));
+      }
     }
     if (ov) {
       SAR_TRY(check(cudaEventRecord(m->ev_join, m->side), "overlap: join"));
