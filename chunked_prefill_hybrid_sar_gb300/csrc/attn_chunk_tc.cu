@@ -64,6 +64,7 @@ constexpr int kBarOff = kQBytes + (kKStages + kVStages) * kKVBytes;  // after Q,
 constexpr int kRedOff = kBarOff + 256;         // softmax exchange: [3][2][128] floats
 constexpr int kSmem = 1024 + kRedOff + 3 * 2 * kBQ * 4;
 static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
+static_assert(kVStages * kKVBytes >= kBQ * kD * 4, "the fp32 query rows are staged in the V stages");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSBufs = 3;                      // S buffers: S_j in buffer j % 3, issued two blocks ahead
 constexpr uint32_t kColS = 128;               // S buffer b at columns [b*128, b*128+128); P overwrites the first 64
@@ -191,6 +192,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       off = key - bi * a.page_size;
     };
     int pa = 0, oa = 0, pb = 0, ob = 0;  // this group of four blocks, the next
+    if (!is_k && ok) {
+      // the V stages hold the fp32 query rows until Q is ready
+      int w = 1;
+      if (lane == 0) w = mbar_wait(smem_u32(&bars->q_ready), 0, a.err, SITE_CHUNK_PIPE);
+      ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+    }
     if (ok) {
       page_of(0, pa, oa);
       if (nb > 4) page_of(4, pb, ob);
@@ -304,15 +311,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + qq) : "memory"); };
     {
       // this half of the query row -> scaled by log2(e) / sqrt(d), rounded
-      // to 16 bits, swizzled as the MMA reads it (dim half hf is Q region hf)
+      // to 16 bits, swizzled as the MMA reads it (dim half hf is Q region hf).
+      // The fp32 rows are first copied into the V stages (idle until Q is
+      // ready) with all sixteen 16-byte copies of a thread in flight at once,
+      // [128 rows][32 chunks of 16 B], chunk c of row r at slot c ^ (r % 32)
       const float qscale = rsqrtf((float)kD) * 1.4426950408889634f;
       const float* qp = a.q32 + (size_t)(row0 + r) * a.ld32 + (size_t)hq * kD + hf * 64;
+      const uint32_t qstg = v_reg(0) + (uint32_t)(r * 512);
+      if (valid) {
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc)
+          cp_async16(qstg + (uint32_t)((((hf * 16 + cc) ^ (r & 31))) << 4), qp + cc * 4, 16);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();  // a thread reads back only its own copies
 #pragma unroll 1
       for (int ch = 0; ch < 8; ++ch) {
         float x[8];
         if (valid) {
-          const float4 v0 = *reinterpret_cast<const float4*>(qp + ch * 8);
-          const float4 v1 = *reinterpret_cast<const float4*>(qp + ch * 8 + 4);
+          const float4 v0 = lds_f4(qstg + (uint32_t)(((hf * 16 + 2 * ch) ^ (r & 31)) << 4));
+          const float4 v1 = lds_f4(qstg + (uint32_t)(((hf * 16 + 2 * ch + 1) ^ (r & 31)) << 4));
           x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
           x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
         } else {
