@@ -1120,11 +1120,15 @@ int gemm_config(int M, int N, int K, int epi, int variant, GemmCfg* cfg, bool in
   };
   GemmCfg c;
   if (variant == SAR_GEMM_AUTO) {
-    // swap (tokens on the MMA's N side) only while one 128-row token tile
-    // would hold them all: from 129 rows on, 128-row token tiles fill more
-    // SMs per weight slab (measured at 256 rows on the Mistral-shaped layer:
-    // QKV 29.3 vs 39.6 us, gate/up 74.4 vs 88.7 us with 128x128 tiles)
-    if (M <= 128) {
+    // swap (tokens on the MMA's N side) only up to 32 rows: above that the
+    // 128-row token tiles do as well or better (Mistral-shaped layer, the
+    // four projections with L2 flushed: 48 and 64 rows 133.7 vs 137.9 us,
+    // 96 rows 137.8 vs 143.9 us, 128 rows 139.9 vs 150.1 us; 256 rows: QKV
+    // 29.3 vs 39.6 us, gate/up 74.4 vs 88.7 us), as the swap tiling's split-K
+    // sums go through fp32 scratch and a finishing kernel where the 128-row
+    // tiles fuse their epilogues; at 8 rows and fewer swap is far ahead
+    // (131.7 vs 150.1 us)
+    if (M <= 32) {
       variant = SAR_GEMM_SWAP;
     } else {
       // makespan estimate: waves x per-unit MMA work

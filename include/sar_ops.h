@@ -106,9 +106,9 @@ int sar_op_rmsnorm(const void* x, const void* gain, void* y, int32_t rows, int32
  *   5: q|k|v rows      fp32 [max_tokens, (n_q_heads + 2 n_kv_heads) * head_dim]
  *                      (the projection with q and k rotated; k and v are
  *                      also in the pages, rounded to the storage type; for
- *                      head_dim 128 and more than 128 rows only q is kept in
- *                      fp32 -- the attention kernels read k and v from the
- *                      pages) */
+ *                      head_dim 128 and more than 32 rows -- a QKV projection
+ *                      on 128-row token tiles -- only q is kept in fp32; the
+ *                      attention kernels read k and v from the pages) */
 int sar_model_debug_buffer(sar_model* m, int32_t which, void** out);
 
 /* The step planner on the host alone (no GPU, no model): plans batch `b` as
