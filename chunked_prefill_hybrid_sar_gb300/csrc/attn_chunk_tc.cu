@@ -120,7 +120,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int hq = blockIdx.y;
+  // one CTA per (tile, query head), heads fastest: the launch order is the
+  // tile table's (most keys first), so the longest tiles start first
+  const int tile_i = blockIdx.x / a.qh;
+  const int hq = blockIdx.x - tile_i * a.qh;
   const int G = a.qh / a.kvh;
   const int kh = hq / G;
 
@@ -152,12 +155,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!a.wait_at_end) pdl_wait();
   pdl_launch_dependents();
   // this CTA's tile (the table lists the most keys first)
-  const int4 tl = reinterpret_cast<const int4*>(a.tiles)[2 * blockIdx.x];
+  const int4 tl = reinterpret_cast<const int4*>(a.tiles)[2 * tile_i];
   const int row0 = tl.x;   // batch row of the tile's first query
   const int pos0 = tl.y;   // its position in the prompt
   const int rows = tl.z;
   const int32_t* bt = a.bt + tl.w;
-  const int4 tl2 = reinterpret_cast<const int4*>(a.tiles)[2 * blockIdx.x + 1];
+  const int4 tl2 = reinterpret_cast<const int4*>(a.tiles)[2 * tile_i + 1];
   const int bt_len = tl2.x;
   const int n_keys = pos0 + rows;  // keys of the last row of this tile, inclusive of it
   // blocks [j0, j0 + nb): planned from the block holding the first row's
@@ -537,7 +540,7 @@ int launch_t(const ChunkAttnArgs& a, const CUtensorMap& tmk, const CUtensorMap& 
   const int arc = ensure_smem_attr(reinterpret_cast<const void*>(&chunk_attn_tc_kernel<T>), kSmem,
                                    "chunk attention (tcgen05) attribute");
   if (arc != SAR_OK) return arc;
-  const dim3 grid(a.n_tiles, a.qh);
+  const dim3 grid(a.n_tiles * a.qh);
   cudaError_t e = launch_pdl(chunk_attn_tc_kernel<T>, grid, dim3(kThreads), (size_t)kSmem, s, tmk, tmv, a);
   if (e != cudaSuccess) return cuda_error(e, "chunk attention (tcgen05) launch");
   count_launches(1);
