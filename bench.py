@@ -671,13 +671,16 @@ def run_sweep(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     variants = {"m128n128": sar.SAR_GEMM_M128_N128, "m128n256": sar.SAR_GEMM_M128_N256,
                 "m256n128": sar.SAR_GEMM_M256_N128, "swap": sar.SAR_GEMM_SWAP, "auto": sar.SAR_GEMM_AUTO}
+    # CTA-pair tilings and stream-K on request only (not in the default sweep)
+    extra_variants = {"pair256": sar.SAR_GEMM_PAIR_N256, "pair128": sar.SAR_GEMM_PAIR_N128,
+                      "pair192": sar.SAR_GEMM_PAIR_N192, "pair256_sk": sar.SAR_GEMM_PAIR_N256 | sar.SAR_GEMM_STREAM_K}
     _, _, tf_sust, _ = peaks()
     lin_flops = 2 * (dims.hidden * (dims.q_dim + 2 * dims.kv_dim) + dims.q_dim * dims.hidden
                      + 3 * dims.hidden * dims.ffn)
 
     rows_list = [int(r) for r in args.rows.split(",")] if args.rows else list(SWEEP_ROWS)
     if args.variants:
-        variants = {k: variants[k] for k in args.variants.split(",")}
+        variants = {k: {**variants, **extra_variants}[k] for k in args.variants.split(",")}
     reps_default = args.reps
 
     def time_gemm(M, name, variant, reps=None):
