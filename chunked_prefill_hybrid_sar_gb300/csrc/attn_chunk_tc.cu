@@ -508,8 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc<false>(tmem, kTmemCols);
   }
   // (run behind the decode attention kernel: the kernels after this one wait
-  // for this grid only, so it completes after that one)
-  if (a.wait_at_end) pdl_wait();
+  // for this grid only, so it completes after that one -- its last CTA alone
+  // waits, every other CTA leaves its SM to the rest of the grid)
+  if (a.wait_at_end && blockIdx.x == gridDim.x - 1) pdl_wait();
 }
 
 // Merges the shares of a split tile: out = sum_i O_i 2^(m_i - M) / sum_i l_i 2^(m_i - M)

@@ -228,8 +228,8 @@ struct ChunkAttnArgs {
   int window = 0;            // the row at position p sees keys (p - window, p]; 0 = all of [0, p]
   // tcgen05 kernel launched right behind the decode attention kernel, whose
   // output it does not read: it starts without waiting for that kernel (its
-  // inputs were complete before that kernel released its dependents) and
-  // waits for it only before exiting, so the kernels after it still see both
+  // inputs were complete before that kernel released its dependents) and its
+  // last CTA waits for it before exiting, so the kernels after it see both
   int wait_at_end = 0;
 };
 // Query rows per tile: the warp-MMA kernel (attn_chunk.cu) and the tcgen05 one.
