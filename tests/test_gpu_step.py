@@ -250,6 +250,35 @@ def test_mistral_layer_hybrid_step(mistral, start):
     assert_close(logits.cpu().numpy(), ref_l, what="logits")
 
 
+def test_mistral_layer_launch_orders_give_identical_attention(mistral):
+    """The step launches decode attention first and the chunk kernel right
+    behind it, without a start wait (it takes the SMs of the decode grid's
+    draining tail); kernel-by-kernel profiling keeps the chunk-then-decode
+    order.  The attention kernels and their inputs are the same, so the
+    attention rows of both orders are bit-identical."""
+    case, m, kv, dec_bt, prompt_bt, w, head = mistral
+    dims, lp = case["dims"], case["lp"]
+    start = 1536
+    prompt = case["prompts"][start]
+    bt = prompt_bt[start]
+    for s0 in range(0, start, 512):
+        m.step(kv, sar.Batch((start, s0, 512, bt), []), prompt[s0:s0 + 512].cuda())
+    decs = [(100 + i, c, dec_bt[i]) for i, c in enumerate(case["ctxs"])]
+    b = sar.Batch((start, start, lp, bt), decs)
+    x = torch.cat([prompt[start:start + lp], case["decode_inputs"]]).cuda()
+    rows = []
+    for prof in (False, True, False):
+        m.profile(prof)
+        m.step(kv, b, x)
+        m.sync_status()
+        torch.cuda.synchronize()
+        rows.append(debug_tensor(m, 2, lp + len(decs), dims.q_dim).clone())
+    m.profile(False)
+    m.profile_read()
+    assert torch.isfinite(rows[0].float()).all()
+    assert torch.equal(rows[0], rows[1]) and torch.equal(rows[0], rows[2])
+
+
 def test_mistral_layer_attention_overlap_is_identical(mistral):
     """Chunk attention on a second stream, concurrent with decode attention:
     the same kernels write the same disjoint rows, so the step agrees with the
