@@ -169,9 +169,10 @@ int weight_maps(WMaps& maps, const void* w, int rows, int cols, int storage) {
 
 // GEMM over `rows` activation rows with the weight maps of one matrix.
 int run_gemm(sar_model* m, const st16* a, int rows, const WMaps& wmaps, int N, int K, int epi,
-             void* c, const void* r, cudaStream_t s, const sar::RopeEpi* rope = nullptr) {
+             void* c, const void* r, cudaStream_t s, const sar::RopeEpi* rope = nullptr,
+             int variant = SAR_GEMM_AUTO) {
   sar::GemmCfg cfg;
-  SAR_TRY(sar::gemm_config(rows, N, K, epi, SAR_GEMM_AUTO, &cfg, c == r));
+  SAR_TRY(sar::gemm_config(rows, N, K, epi, variant, &cfg, c == r));
   CUtensorMap amap;
   SAR_TRY(sar::make_tmap_16(&amap, a, rows, K, cfg.swap ? cfg.b_box_rows : cfg.a_box_rows, m->d.storage));
   const CUtensorMap& wm = wmaps[sar::weight_box_index(cfg)];
@@ -724,7 +725,12 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
     }
     {
       Prof pr(m, SAR_K_GEMM_HEAD, s);
-      SAR_TRY(run_gemm(m, m->hrows, p.R, m->m_head, d.vocab, H, SAR_EPI_RESIDUAL, logits, logits, s));
+      // the LM head streams its whole weight (262 MB at Mistral's shape) for a
+      // few sampled rows: the swap tiling shares its K slabs out over every SM
+      // (65 rows, standalone, L2 flushed: 62.2 us against 65.2 us for AUTO's
+      // 128x256 tiles on 125 SMs), and it stays ahead up to 128 rows
+      SAR_TRY(run_gemm(m, m->hrows, p.R, m->m_head, d.vocab, H, SAR_EPI_RESIDUAL, logits, logits, s, nullptr,
+                       p.R <= 128 ? SAR_GEMM_SWAP : SAR_GEMM_AUTO));
     }
   }
   return SAR_OK;
