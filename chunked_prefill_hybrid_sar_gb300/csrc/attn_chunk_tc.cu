@@ -23,8 +23,9 @@
 //               ready when a block's softmax ends); then O += P_j V_j with P_j
 //               read from tensor memory and V_j as an MN-major operand.
 //   warps 2..9  two warps per row quarter (the TMEM lanes a warp may access),
-//               each with 64 of the 128 keys of every block: load and split the
-//               query, then per block the online softmax in base 2 (the two
+//               each with 64 of the 128 keys of every block: stage the fp32
+//               query rows through the (still idle) V stages, scale and round
+//               them into Q, then per block the online softmax in base 2 (the two
 //               halves exchange their row maxima through shared memory), P
 //               (16-bit) written back over S for the next MMA; O is rescaled
 //               in tensor memory only when a row's maximum grows by more than
@@ -38,6 +39,10 @@
 // tile's key blocks over several CTAs: each writes its unnormalised O with the
 // row's maximum and sum, and chunk_combine_kernel merges them (the split-K
 // form of the decode attention's long contexts).
+// CTAs run (tile, head) units heads fastest, in the tile table's order (most
+// keys first).  Launched right behind decode attention (wait_at_end), the
+// kernel starts without waiting for that kernel and only its last CTA waits
+// for it before exiting.
 // Every wait is bounded; a timeout records SAR_ERR_TIMEOUT.
 #include <float.h>
 
