@@ -443,12 +443,39 @@ def run_ours(args):
                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": (BD + 1) * dims.vocab * 4,
                  "api": "sar_step_host (host planning, kernel-by-kernel launch, logits back)"}
     e2e_fixed = None
+    e2e_pipe = None
     if graph_set:
         e2e_s = e2e_run(replanned_tokens_step)
         e2e = {"value": whole_job_rate(TAU * args.steps, world, e2e_s), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": (BD + 1) * 4,
                "api": "sar_graph_update (the step planned on the host) + sar_graph_launch_host_tokens "
                       "(greedy token ids of the 65 sampled rows back)"}
+        # the same serving loop with step i+1 planned (sar_graph_update) and
+        # enqueued -- its input copied on the graph's own copy stream -- while
+        # step i runs, and step i's token ids waited for after that
+        toks = [torch.empty(BD + 1, dtype=torch.int32).pin_memory() for _ in range(3)]
+
+        def pipelined(n):
+            prev = None
+            for i in range(n):
+                g = graph_set[i % 3]
+                g.update(cases[i % 3][0])
+                g.enqueue_host_tokens(pin_in[i % 3], toks[i % 3])
+                if prev is not None:
+                    prev.wait()
+                prev = g
+            prev.wait()
+
+        pipelined(3)
+        barrier()
+        t0 = time.perf_counter()
+        pipelined(args.steps)
+        barrier()
+        e2e_pipe_s = max_over_ranks(time.perf_counter() - t0, world)
+        e2e_pipe = {"value": whole_job_rate(TAU * args.steps, world, e2e_pipe_s), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": (BD + 1) * 4,
+                    "api": "sar_graph_update + sar_graph_enqueue_host_tokens, sar_graph_wait one step late "
+                           "(the next step planned and its input copied while the current one runs)"}
         e2e_fixed_s = e2e_run(tokens_step)
         e2e_fixed = {"value": whole_job_rate(TAU * args.steps, world, e2e_fixed_s), "unit": UNIT,
                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": (BD + 1) * 4,
@@ -474,7 +501,8 @@ def run_ours(args):
                "data": "synthetic (seeded random-init weights and KV histories)",
                "config": dict(config_block(world), attn_streams=2 if args.overlap else 1,
                               launch="cuda graph per case" if args.graph else "kernel by kernel"),
-               "e2e": e2e, "e2e_no_replan": e2e_fixed, "e2e_logits_readback": e2e_logits,
+               "e2e": e2e, "e2e_pipelined": e2e_pipe, "e2e_no_replan": e2e_fixed,
+               "e2e_logits_readback": e2e_logits,
                "e2e_eager_planned": e2e_eager, "gpu_launches": launches,
                "roofline": roof, "step_roofline_ms": t_roof * 1e3,
                "step_roofline_frac": (t_roof * 1e3) / step_ms, "step_roofline": roof_step,

@@ -202,6 +202,19 @@ class StepGraph:
         check(lib().sar_graph_launch_host_tokens(self.h, _ptr(inp), ctypes.cast(_ptr(tokens_out), _lib.P_i32),
                                                  _stream(stream)))
 
+    def enqueue_host_tokens(self, inp, tokens_out, stream=None) -> None:
+        """As launch_host_tokens, but returns once the step is enqueued (the
+        input copy on the graph's own copy stream); ``wait`` then waits for
+        it.  ``inp`` must stay unchanged and ``tokens_out`` unread until then."""
+        check(lib().sar_graph_enqueue_host_tokens(self.h, _ptr(inp), ctypes.cast(_ptr(tokens_out), _lib.P_i32),
+                                                  _stream(stream)))
+        self._pending = (inp, tokens_out)
+
+    def wait(self) -> None:
+        """Waits for the last enqueue_host_tokens step of this graph."""
+        check(lib().sar_graph_wait(self.h))
+        self._pending = None
+
     def close(self) -> None:
         if self.h:
             check(lib().sar_graph_destroy(self.h))

@@ -35,7 +35,7 @@ SAR_Q_F32 = 0x100
 SAR_GEMM_STREAM_K = 0x2000
 
 KERNEL_KINDS = ("embed", "rmsnorm", "gemm_qkv", "rope_append", "chunk_attn", "decode_attn", "gemm_o",
-                "gemm_gateup", "gemm_down", "head_norm", "gemm_head")
+                "gemm_gateup", "gemm_down", "head_norm", "gemm_head", "decode_combine")
 
 i32 = ctypes.c_int32
 i64 = ctypes.c_int64
@@ -93,6 +93,8 @@ SIGNATURES = {
     "sar_model_set_overlap": (i32, [vp, i32]),
     "sar_model_set_chunk_split": (i32, [vp, i32]),
     "sar_graph_launch_host_tokens": (i32, [vp, vp, P_i32, vp]),
+    "sar_graph_enqueue_host_tokens": (i32, [vp, vp, P_i32, vp]),
+    "sar_graph_wait": (i32, [vp]),
     "sar_graph_create": (i32, [vp, vp, ctypes.POINTER(sar_batch), vp, vp, vp, vp, vp, ctypes.POINTER(vp)]),
     "sar_graph_update": (i32, [vp, ctypes.POINTER(sar_batch), vp]),
     "sar_graph_launch": (i32, [vp, vp]),

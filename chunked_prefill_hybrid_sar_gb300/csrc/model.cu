@@ -683,8 +683,16 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
     } else {
       if (p.Lp > 0) SAR_TRY(run_chunk(sc));
       if (p.Bd > 0) {
-        Prof pr(m, SAR_K_DECODE_ATTN, s);
-        SAR_TRY(sar::launch_decode_attention(da, kv->tmk[l], kv->tmv[l], s));
+        // the merge of the key-range partials launched (and timed) on its own
+        da.defer_combine = true;
+        {
+          Prof pr(m, SAR_K_DECODE_ATTN, s);
+          SAR_TRY(sar::launch_decode_attention(da, kv->tmk[l], kv->tmv[l], s));
+        }
+        if (da.partials) {
+          Prof pr(m, SAR_K_DECODE_COMBINE, s);
+          SAR_TRY(sar::launch_decode_combine(da, s));
+        }
       }
     }
     if (ov) {
@@ -1179,6 +1187,12 @@ struct sar_graph {
   cudaEvent_t staged = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
+  // sar_graph_enqueue_host_tokens: the input copy's own stream (so that it can
+  // run while an earlier step computes), the copy's completion, and the
+  // enqueued step's (token ids in host memory)
+  cudaStream_t copy = nullptr;
+  cudaEvent_t in_ready = nullptr;
+  cudaEvent_t done = nullptr;
 };
 
 namespace {
@@ -1201,6 +1215,11 @@ extern "C" {
 int sar_graph_destroy(sar_graph* g) {
   if (!g) return SAR_OK;
   if (g->staged) cudaEventSynchronize(g->staged);
+  if (g->done) cudaEventSynchronize(g->done);
+  if (g->copy) cudaStreamSynchronize(g->copy);
+  if (g->in_ready) cudaEventDestroy(g->in_ready);
+  if (g->done) cudaEventDestroy(g->done);
+  if (g->copy) cudaStreamDestroy(g->copy);
   if (g->exec) cudaGraphExecDestroy(g->exec);
   if (g->graph) cudaGraphDestroy(g->graph);
   if (g->staged) cudaEventDestroy(g->staged);
@@ -1325,6 +1344,35 @@ int sar_graph_launch_host_tokens(sar_graph* g, const void* in, int32_t* tokens_o
   SAR_TRY(sar::launch_argmax(g->logits, g->p.R, g->m->d.vocab, g->tokens, s));
   SAR_TRY(host_copy(tokens_out, g->tokens, (size_t)g->p.R * 4, s));
   return check(cudaStreamSynchronize(s), "graph: synchronise");
+}
+
+int sar_graph_enqueue_host_tokens(sar_graph* g, const void* in, int32_t* tokens_out, void* stream) {
+  if (!g || !in || !tokens_out) return set_error(SAR_ERR_INVALID_ARG, "graph: null argument");
+  if (!g->logits) return set_error(SAR_ERR_INVALID_ARG, "graph: logits not captured");
+  if (!g->copy) {
+    SAR_TRY(check(cudaStreamCreateWithFlags(&g->copy, cudaStreamNonBlocking), "graph: copy stream"));
+    SAR_TRY(check(cudaEventCreateWithFlags(&g->in_ready, cudaEventDisableTiming), "graph: event"));
+    SAR_TRY(check(cudaEventCreateWithFlags(&g->done, cudaEventDisableTiming), "graph: event"));
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t M = (size_t)g->p.M, H = (size_t)g->m->d.hidden;
+  const size_t in_bytes = g->in_kind == SAR_IN_TOKENS ? M * 4 : M * H * 2;
+  // the input buffer is rewritten once this graph's previous step has ended
+  // (a no-op wait before the first enqueue)
+  SAR_TRY(check(cudaStreamWaitEvent(g->copy, g->done, 0), "graph: copy wait"));
+  SAR_TRY(host_copy(g->in, in, in_bytes, g->copy));
+  SAR_TRY(check(cudaEventRecord(g->in_ready, g->copy), "graph: input copied"));
+  SAR_TRY(check(cudaStreamWaitEvent(s, g->in_ready, 0), "graph: input wait"));
+  SAR_TRY(check(cudaGraphLaunch(g->exec, s), "graph: launch"));
+  SAR_TRY(sar::launch_argmax(g->logits, g->p.R, g->m->d.vocab, g->tokens, s));
+  SAR_TRY(host_copy(tokens_out, g->tokens, (size_t)g->p.R * 4, s));
+  return check(cudaEventRecord(g->done, s), "graph: step enqueued");
+}
+
+int sar_graph_wait(sar_graph* g) {
+  if (!g) return set_error(SAR_ERR_INVALID_ARG, "graph: null graph");
+  if (!g->done) return SAR_OK;
+  return check(cudaEventSynchronize(g->done), "graph: wait");
 }
 
 }  // extern "C"

@@ -252,6 +252,22 @@ int sar_graph_launch_host(sar_graph* g, const void* in, float* logits_out, float
  * round trip: the host needs the next tokens, not the logits. */
 int sar_graph_launch_host_tokens(sar_graph* g, const void* in, int32_t* tokens_out, void* stream);
 
+/* sar_graph_launch_host_tokens without the wait, for a serving loop that
+ * plans and stages the next step while this one runs: the copy of `in` goes
+ * on the graph's own copy stream (created on first use) once the graph's
+ * previous enqueued step has ended, and can therefore run while other work
+ * computes on `stream`; the captured step waits for it on `stream`, then the
+ * greedy picks and their copy into `tokens_out` follow there.  Returns once
+ * everything is enqueued.  `in` must stay unchanged and `tokens_out` unread
+ * until sar_graph_wait(g) returns.  Steps enqueued on one stream run in
+ * order; a sar_graph_update of another graph may be called in between (its
+ * metadata copy is ordered on the stream it is given). */
+int sar_graph_enqueue_host_tokens(sar_graph* g, const void* in, int32_t* tokens_out, void* stream);
+
+/* Waits for the graph's last sar_graph_enqueue_host_tokens step: its token
+ * ids are then in host memory.  Returns at once if none was enqueued. */
+int sar_graph_wait(sar_graph* g);
+
 int sar_graph_destroy(sar_graph* g);
 
 /* Greedy sampling: tokens_out[r] = argmax_v logits[r, v] (lowest index on
@@ -318,6 +334,7 @@ enum {
   SAR_K_GEMM_DOWN,
   SAR_K_HEAD_NORM,
   SAR_K_GEMM_HEAD,
+  SAR_K_DECODE_COMBINE, /* the merge of the decodes' key-range partials */
   SAR_K_COUNT
 };
 

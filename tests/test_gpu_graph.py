@@ -180,6 +180,32 @@ def test_graph_launch_host_copies_in_and_out(mistral):
     toks = torch.full((65,), -1, dtype=torch.int32).pin_memory()
     g.launch_host_tokens(x_host, toks)
     assert torch.equal(toks, logits.cpu().argmax(dim=1).to(torch.int32))
+    # enqueued steps (the input copied on the graph's own copy stream while
+    # the previous step runs), two graphs of the batch alternating with
+    # different input rows, each step waited for one step late: the same token
+    # ids as the waited launches of the same inputs
+    g.wait()  # nothing enqueued yet
+    x_dev2 = torch.zeros_like(x_host, device="cuda")
+    logits2 = torch.empty_like(logits)
+    g2 = sar.StepGraph(m, kv, b, x_dev2, logits_out=logits2)
+    x_host2 = torch.flip(x_host, dims=(1,)).contiguous().pin_memory()
+    ref2 = torch.full((65,), -1, dtype=torch.int32).pin_memory()
+    g2.launch_host_tokens(x_host2, ref2)
+    assert torch.equal(ref2, logits2.cpu().argmax(dim=1).to(torch.int32))
+    assert not torch.equal(ref2, toks)
+    outs = [torch.full((65,), -1, dtype=torch.int32).pin_memory() for _ in range(6)]
+    prev = None
+    for i in range(6):
+        gi, xi = (g, x_host) if i % 2 == 0 else (g2, x_host2)
+        gi.enqueue_host_tokens(xi, outs[i])
+        if prev is not None:
+            prev.wait()
+        prev = gi
+    prev.wait()
+    for i in range(6):
+        assert torch.equal(outs[i], toks if i % 2 == 0 else ref2), i
+    assert torch.equal(x_dev.cpu(), x_host) and torch.equal(x_dev2.cpu(), x_host2)
+    g2.close()
     nolog = sar.StepGraph(m, kv, b, x_dev, hidden_out=hid)
     with pytest.raises(sar.SarError):  # no logits captured
         nolog.launch_host_tokens(x_host, toks)
