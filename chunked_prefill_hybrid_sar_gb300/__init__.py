@@ -315,7 +315,7 @@ class Scheduler:
 
 _LAYOUT = ("M", "Lp", "Bd", "R", "n_items", "n_parts", "n_tiles", "tile_rows", "o_pos", "o_slot", "o_pbt",
            "o_nkeys", "o_btoff", "o_btlen", "o_pbeg", "o_pcnt", "o_items", "o_bt", "o_rows", "o_tiles", "total",
-           "n_comb", "n_cparts", "o_comb")
+           "n_comb", "n_cparts", "o_comb", "chunk_pairs")
 
 
 def plan_inspect(dims, batch: Batch, page_size: int, num_pages: int, sms: int, max_tokens: int,

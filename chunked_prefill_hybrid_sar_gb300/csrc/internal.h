@@ -231,6 +231,11 @@ struct ChunkAttnArgs {
   // inputs were complete before that kernel released its dependents) and its
   // last CTA waits for it before exiting, so the kernels after it see both
   int wait_at_end = 0;
+  // tcgen05 kernel: the tile table lists tile pairs (entries 2i, 2i + 1: two
+  // query tiles of one prompt's chunk over the same key blocks, the second
+  // possibly with 0 rows), one CTA per pair and head; full causal attention
+  // and whole key ranges only
+  int dual = 0;
 };
 // Query rows per tile: the warp-MMA kernel (attn_chunk.cu) and the tcgen05 one.
 constexpr int kChunkTileRows = 64;

@@ -186,6 +186,7 @@ struct Plan {
   size_t o_pos = 0, o_slot = 0, o_pbt = 0, o_nkeys = 0, o_btoff = 0, o_btlen = 0, o_pbeg = 0, o_pcnt = 0,
          o_items = 0, o_bt = 0, o_rows = 0, o_tiles = 0, o_comb = 0, total = 0;
   int n_items = 0, n_parts = 0, n_tiles = 0, n_comb = 0, n_cparts = 0;
+  int chunk_dual = 0;  // the chunk tile table lists tile pairs (the two-tile kernel)
 };
 
 // The batch's prefill chunks in row order: `prefill` (if has_prefill), then more_prefill[].
@@ -371,8 +372,10 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
       int keys;
     };
     std::vector<Tile> tl;
+    std::vector<std::pair<int, int>> chunk_tiles;  // (first entry of tl, count) per chunk
     int r0 = 0;
     for (const sar_prefill& c : chunks) {
+      const int t_first = (int)tl.size();
       const int off = (int)pbt.size();
       const int nb = (c.start_pos + c.len - 1) / ps + 1;
       pbt.insert(pbt.end(), c.block_table, c.block_table + nb);
@@ -383,6 +386,7 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
         const int kb0 = first / sar::kChunkTileRowsTc, kb1 = (pos0 + rws + sar::kChunkTileRowsTc - 1) / sar::kChunkTileRowsTc;
         tl.push_back({{r0 + q0, pos0, rws, off, nb, kb0, kb1, -1}, pos0 + rws - first});
       }
+      chunk_tiles.push_back({t_first, (int)tl.size() - t_first});
       r0 += c.len;
     }
     // Key-range splits (tcgen05 kernel, one CTA per SM): when the tiles x
@@ -398,7 +402,50 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
       s = (int)std::min<long>(4, slots / ctas);
       if (s < 2) s = 1;
     }
+    // Tile pairs (one CTA per pair of consecutive tiles of a chunk and head,
+    // sharing their key blocks; a chunk's odd last tile pairs with an empty
+    // one) when the one-tile grid needs more waves than the pair grid by a
+    // margin: a pair takes ~1.9 times a tile's time per key block (both are
+    // bound by their MMAs; the pair's two softmax chains only fill the
+    // one-tile kernel's short waits), so pairs win where they save waves --
+    // 4 tiles x 56 heads (224 CTAs on 152 SMs, two waves) run as 112 pairs in
+    // one -- and not where one-tile CTAs fill their waves about as well.
+    // Full causal attention and whole key ranges only.
+    bool dual = false;
+    p->chunk_dual = 0;
+    if (s == 1 && d.sliding_window == 0 && tile_rows == sar::kChunkTileRowsTc && !tl.empty()) {
+      long pairs = 0;
+      for (const auto& ct : chunk_tiles) pairs += (ct.second + 1) / 2;
+      const long slots = std::max(1, sms);
+      const long w1 = ((long)tl.size() * d.n_q_heads + slots - 1) / slots;
+      const long w2 = (pairs * d.n_q_heads + slots - 1) / slots;
+      dual = 19 * w2 < 10 * w1;
+    }
     std::vector<Tile> ent;
+    if (dual) {
+      struct Pair {
+        Tile a, b;
+        int keys;
+      };
+      std::vector<Pair> pr;
+      for (const auto& ct : chunk_tiles)
+        for (int i = 0; i < ct.second; i += 2) {
+          const Tile& ta = tl[ct.first + i];
+          Tile tb = ta;
+          if (i + 1 < ct.second)
+            tb = tl[ct.first + i + 1];
+          else
+            tb.e[2] = 0;  // no second tile: 0 rows over the first one's key blocks
+          pr.push_back({ta, tb, std::max(ta.keys, tb.keys)});
+        }
+      std::stable_sort(pr.begin(), pr.end(), [](const Pair& x, const Pair& y) { return x.keys > y.keys; });
+      for (const Pair& q : pr) {
+        tiles.insert(tiles.end(), q.a.e.begin(), q.a.e.end());
+        tiles.insert(tiles.end(), q.b.e.begin(), q.b.e.end());
+      }
+      p->chunk_dual = 1;
+      tl.clear();  // nothing left for the one-tile table below
+    }
     for (const Tile& t : tl) {
       const int nbk = t.e[6] - t.e[5];
       const int ss = std::min(s, nbk / 2);
@@ -630,6 +677,7 @@ int launch_step(sar_model* m, sar_kv* kv, const sar_batch* b, const Plan& p, con
       ca.partials = partials + decode_partials_floats(p, d);
       ca.comb = md + p.o_comb;
       ca.n_comb = p.n_comb;
+      ca.dual = p.chunk_dual;
     }
     sar::DecodeAttnArgs da{};
     if (p.Bd > 0) {
@@ -1145,11 +1193,11 @@ int sar_plan_inspect(const sar_dims* dims, int32_t page_size, int32_t num_pages,
   Plan p;
   std::vector<int32_t> v;
   SAR_TRY(validate_and_plan(env, b, &p, &v));
-  const int32_t l[24] = {p.M, p.Lp, p.Bd, p.R, p.n_items, p.n_parts, p.n_tiles, chunk_tile_rows(env.d, page_size),
+  const int32_t l[25] = {p.M, p.Lp, p.Bd, p.R, p.n_items, p.n_parts, p.n_tiles, chunk_tile_rows(env.d, page_size),
                          (int32_t)p.o_pos, (int32_t)p.o_slot, (int32_t)p.o_pbt, (int32_t)p.o_nkeys,
                          (int32_t)p.o_btoff, (int32_t)p.o_btlen, (int32_t)p.o_pbeg, (int32_t)p.o_pcnt,
                          (int32_t)p.o_items, (int32_t)p.o_bt, (int32_t)p.o_rows, (int32_t)p.o_tiles,
-                         (int32_t)p.total, p.n_comb, p.n_cparts, (int32_t)p.o_comb};
+                         (int32_t)p.total, p.n_comb, p.n_cparts, (int32_t)p.o_comb, p.chunk_dual};
   std::memcpy(layout, l, sizeof(l));
   if (meta_n) *meta_n = (int64_t)v.size();
   if (meta) {
@@ -1205,7 +1253,7 @@ bool same_shape(const Plan& a, const Plan& b) {
          a.o_slot == b.o_slot && a.o_pbt == b.o_pbt && a.o_nkeys == b.o_nkeys && a.o_btoff == b.o_btoff &&
          a.o_btlen == b.o_btlen && a.o_pbeg == b.o_pbeg && a.o_pcnt == b.o_pcnt && a.o_items == b.o_items &&
          a.o_bt == b.o_bt && a.o_rows == b.o_rows && a.o_tiles == b.o_tiles && a.n_comb == b.n_comb &&
-         a.n_cparts == b.n_cparts && a.o_comb == b.o_comb;
+         a.n_cparts == b.n_cparts && a.o_comb == b.o_comb && a.chunk_dual == b.chunk_dual;
 }
 
 }  // namespace

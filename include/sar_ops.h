@@ -115,7 +115,7 @@ int sar_model_debug_buffer(sar_model* m, int32_t which, void** out);
  * sar_step would for a model of `dims` (with chunk_split as set by
  * sar_model_set_chunk_split), a cache of num_pages pages of page_size tokens
  * and a device of `sms` SMs (sar_step plans for the current device's), with
- * the same validation and errors.  layout (int32[24])
+ * the same validation and errors.  layout (int32[25])
  * receives M, Lp, Bd, R, decode work items, decode partials, chunk tiles,
  * rows per chunk tile, then the offsets (int32 elements) of the metadata
  * block's arrays -- row positions, row page slots, chunk block tables,
@@ -125,7 +125,10 @@ int sar_model_debug_buffer(sar_model* m, int32_t which, void** out);
  * first batch row, first position, rows, block-table offset, block-table
  * length, first and end 128-key block, key-range partial slot or -1] -- its
  * total length, then the chunk key-range merges, their partial slots and the
- * merges' offset [4 each: first batch row, rows, first slot, slots].  The
+ * merges' offset [4 each: first batch row, rows, first slot, slots], then 1
+ * when the chunk tiles are listed in pairs (entries 2i and 2i + 1: two query
+ * tiles of one chunk, the second possibly of 0 rows, one CTA per pair and
+ * head), else 0.  The
  * block itself (what the step ships to the device) is copied to meta
  * (int32[meta_cap], may be NULL) and its length to *meta_n. */
 int sar_plan_inspect(const sar_dims* dims, int32_t page_size, int32_t num_pages, int32_t sms,

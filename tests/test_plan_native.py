@@ -99,6 +99,9 @@ def test_plan_invariants_on_random_batches(seed, dims):
         for i in range(ln):
             chunk_of_row[r0 + i] = (ci, start + i)
         r0 += ln
+    if p["chunk_pairs"]:  # no key-range splits planned, and enough tiles for pairs
+        check_pair_table(p, chunks)
+        return
     keys = []
     shares = {}
     for t in p["tiles"]:
@@ -247,3 +250,96 @@ def test_decode_ranges_are_a_resident_slots_share():
         assert max(lengths) <= 4096
         ctas = len(p["items"]) * synth.MISTRAL_LAYER.n_kv_heads
         assert 2 * sms <= ctas <= 4 * sms, (sms, ctas)
+
+
+def check_pair_table(p, chunks):
+    """A pair table: entries 2i, 2i + 1 are two consecutive query tiles of one
+    chunk (or a chunk's odd last tile and an empty partner over the same key
+    blocks); every chunk row once; pairs with the most keys first."""
+    tiles = p["tiles"]
+    assert len(tiles) % 2 == 0 and p["n_comb"] == 0
+    chunk_of_row = {}
+    r0 = 0
+    for ci, (req, start, ln, bt) in enumerate(chunks):
+        for i in range(ln):
+            chunk_of_row[r0 + i] = (ci, start + i)
+        r0 += ln
+    covered = set()
+    keys = []
+    for i in range(0, len(tiles), 2):
+        a, b = tiles[i], tiles[i + 1]
+        ra0, pa0, rows_a, off_a, blen_a, kb0_a, kb1_a, part_a = a
+        rb0, pb0, rows_b, off_b, blen_b, kb0_b, kb1_b, part_b = b
+        assert part_a == part_b == -1 and kb0_a == kb0_b == 0
+        ci, pfirst = chunk_of_row[ra0]
+        req, start, ln, bt = chunks[ci]
+        nb = (start + ln - 1) // PS + 1
+        assert pa0 == pfirst and blen_a == nb and p["pbt"][off_a:off_a + nb] == bt[:nb]
+        assert 0 < rows_a <= 128 and kb1_a == -(-(pa0 + rows_a) // 128)
+        if rows_b == 0:  # an odd last tile's empty partner: the first tile's key blocks
+            assert b == (ra0, pa0, 0, off_a, blen_a, kb0_a, kb1_a, -1)
+            assert pa0 + rows_a == start + ln
+        else:  # the chunk's next tile
+            assert rows_a == 128 and (rb0, pb0) == (ra0 + 128, pa0 + 128)
+            assert (off_b, blen_b) == (off_a, blen_a) and kb1_b == -(-(pb0 + rows_b) // 128)
+        for t in (a, b):
+            for r in range(t[0], t[0] + t[2]):
+                assert r not in covered and chunk_of_row[r] == (ci, t[1] + r - t[0])
+                covered.add(r)
+        keys.append(max(pa0 + rows_a, pb0 + rows_b))
+    assert covered == set(chunk_of_row)
+    assert keys == sorted(keys, reverse=True)
+
+
+def test_chunk_tiles_run_in_pairs_where_that_saves_a_wave():
+    yi = dataclasses.replace(synth.YI_34B, n_layers=1)
+    # a 512-row chunk of a long Yi-34B prompt: 4 tiles x 56 heads = 224 CTAs
+    # (two waves on 152 SMs) -> 2 pairs x 56 = 112 CTAs (one)
+    chunks = [(0, 8192, 512, list(range(544)))]
+    p = plan(yi, chunks, [], chunk_split=False)
+    assert p["chunk_pairs"] == 1 and p["n_tiles"] == 4
+    check_pair_table(p, chunks)
+    # three tiles: the last one pairs with an empty tile
+    chunks = [(0, 4096, 384, list(range(280)))]
+    p = plan(yi, chunks, [(9, 100, [600, 601, 602, 603, 604, 605, 606])], chunk_split=False)
+    assert p["chunk_pairs"] == 1 and p["n_tiles"] == 4
+    check_pair_table(p, chunks)
+    # two chunks of two tiles each: pairs never mix prompts
+    chunks = [(0, 2048, 256, list(range(144))), (1, 6000, 256, list(range(200, 592)))]
+    p = plan(yi, chunks, [], chunk_split=False)
+    assert p["chunk_pairs"] == 1 and p["n_tiles"] == 4
+    check_pair_table(p, chunks)
+    # one-tile CTAs that fit one wave stay one per CTA: the tau = 512 Mistral
+    # step (4 x 32 = 128 CTAs), a 256-row Yi chunk (2 x 56 = 112)
+    p = plan(synth.MISTRAL_LAYER, [(0, 1536, 448, list(range(125)))], [], chunk_split=False)
+    assert p["chunk_pairs"] == 0
+    p = plan(yi, [(0, 8192, 256, list(range(528)))], [], chunk_split=False)
+    assert p["chunk_pairs"] == 0
+    # three waves of one-tile CTAs against two of pairs: not worth the pairs'
+    # longer blocks (8 tiles x 56 = 448 CTAs, 224 pairs)
+    p = plan(yi, [(0, 8192, 1024, list(range(576)))], [], chunk_split=False, max_tokens=1024)
+    assert p["chunk_pairs"] == 0
+    # a whole 2048-token prompt at once (16 tiles x 56): pairs
+    chunks = [(0, 0, 2048, list(range(128)))]
+    p = plan(yi, chunks, [], chunk_split=False, max_tokens=2048)
+    assert p["chunk_pairs"] == 1 and p["n_tiles"] == 16
+    check_pair_table(p, chunks)
+    # no pairs with a sliding window or with key-range splits planned
+    w = dataclasses.replace(yi, sliding_window=4096)
+    assert plan(w, [(0, 8192, 512, list(range(544)))], [], chunk_split=False)["chunk_pairs"] == 0
+    p = plan(synth.MISTRAL_LAYER, [(0, 8192, 256, list(range(528)))], [], chunk_split=True)
+    assert p["chunk_pairs"] == 0 and p["n_comb"] == 2
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_pair_tables_on_random_batches(seed):
+    rng = np.random.default_rng(100 + seed)
+    yi = dataclasses.replace(synth.YI_34B, n_layers=1)
+    # few SMs, so that small random batches take pairs too
+    chunks, decs = random_batch(rng, int(rng.integers(1, 4)), int(rng.integers(0, 20)))
+    for sms in (8, 40, 152):
+        p = plan(yi, chunks, decs, chunk_split=False, sms=sms)
+        if p["chunk_pairs"]:
+            check_pair_table(p, chunks)
+        else:
+            assert all(t[2] > 0 for t in p["tiles"])
