@@ -300,21 +300,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * acc_cols);
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
+          // the stage's descriptors are built before its wait: between two
+          // MMAs this thread issues only a constant step of each descriptor
+          // (the issue of an MMA is accepted at the pipe's pace, and any
+          // arithmetic between two issues adds to every MMA's time)
+          const uint32_t a_base = smem_u32(smem + stage * p.stage_bytes);
+          uint64_t adesc[MSUB];
+#pragma unroll
+          for (int s = 0; s < MSUB; ++s) adesc[s] = sw128_desc(a_base + s * kTileA);
+          const uint64_t bdesc = sw128_desc(a_base + MSUB * kTileA);
+          const uint32_t acc0 = kb != un.kb0 ? 1u : 0u;
           if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.err, SITE_GEMM_MMA)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(smem + stage * p.stage_bytes);
-          const uint32_t b_base = a_base + MSUB * kTileA;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t bdesc = sw128_desc(b_base + kk * 32);
 #pragma unroll
-            for (int s = 0; s < MSUB; ++s) {
-              const uint64_t adesc = sw128_desc(a_base + s * kTileA + kk * 32);
-              mma_f16<PAIR>(d_tmem + (uint32_t)(s * p.bn), adesc, bdesc, idesc, (kb != un.kb0) || (kk != 0));
-            }
+            for (int s = 0; s < MSUB; ++s)
+              // K step kk: 32 bytes into the 128-byte swizzled rows (address field in 16-byte units)
+              mma_f16<PAIR>(d_tmem + (uint32_t)(s * p.bn), adesc[s] + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2),
+                            idesc, kk != 0 ? 1u : acc0);
           }
           if (PAIR)
             mma_commit_pair(smem_u32(&empty_bar[stage]));
