@@ -95,9 +95,42 @@ def test_tile_pairs_against_the_oracle(layer):
     k = harness.read_history(kv, dims, 0, 0, bt, keys).double().cpu().numpy()
     v = harness.read_history(kv, dims, 0, 1, bt, keys).double().cpu().numpy()
     # every tile's first and last rows, and a stride through the rest
-    sel = sorted(set(list(range(0, n, 37)) + [t * 128 for t in range(8)] + [min(n, t * 128 + 128) - 1 for t in range(8)]))
+    sel = sorted(set(list(range(0, n, 37)) + [t * 128 for t in range(8)] +
+                     [min(n, t * 128 + 128) - 1 for t in range(8)]))
     ref = om.attention(q[sel], k, v, start + np.array(sel), np.arange(keys)).reshape(len(sel), -1)
     g = got[sel]
     err = np.abs(g - ref).max()
     rel = np.linalg.norm(g - ref) / np.linalg.norm(ref)
     assert err <= MAX_ABS and rel <= REL_L2, f"max-abs {err:.3e}, rel-L2 {rel:.3e}"
+
+
+def test_tile_pairs_of_two_prompts_in_one_batch(layer):
+    """Two prompts' 512-row chunks in one batch (8 tiles x 32 heads: pairs,
+    each within one prompt) against each chunk stepped alone (4 tiles x 32
+    heads: one tile per CTA): bit-identical attention rows."""
+    case, m, _, _ = layer
+    dims = m.dims
+    prompt = case["prompt"]
+    n_pages = PROMPT // PS + 8
+    perm = list(synth.page_permutation(synth.generator(12), n_pages))
+    bts = [perm[:1024 // PS], perm[1024 // PS:2048 // PS]]
+    xs = [prompt[:1024], prompt[1024:2048]]  # two different prompts of 1024 tokens
+    kv = sar.KVCache(m, PS, n_pages)
+    try:
+        for i in range(2):  # their first chunks, one per step
+            chunk_rows(m, kv, bts[i], xs[i], 0, 512)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        both = sar.Batch([(0, 512, 512, bts[0]), (1, 512, 512, bts[1])], [])
+        p = sar.plan_inspect(dims, both, PS, n_pages, sms, 1024, 8)
+        assert p["chunk_pairs"] == 1 and p["n_tiles"] == 8
+        x = torch.cat([xs[0][512:1024], xs[1][512:1024]]).cuda().contiguous()
+        m.step(kv, both, x)
+        m.sync_status()
+        torch.cuda.synchronize()
+        pairs = harness.wrap(m.debug_buffer(2), 1024 * dims.q_dim, sar.storage_dtype(m.storage)).view(
+            1024, dims.q_dim).clone()
+        alone = torch.cat([chunk_rows(m, kv, bts[i], xs[i], 512, 512) for i in range(2)])
+        assert torch.isfinite(alone.float()).all()
+        assert torch.equal(pairs, alone)
+    finally:
+        kv.close()
