@@ -249,9 +249,15 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
   if (b->in_kind == SAR_IN_TOKENS && (d.vocab == 0 || !env.has_embed))
     return set_error(SAR_ERR_INVALID_ARG, "step: token input without an embedding");
   const int ps = env.page_size;
+  // a position's page and offset: shifts and masks for the usual power-of-two
+  // page sizes (the planner runs on the host before every step, and an integer
+  // division per row was most of its time)
+  const int ps_shift = (ps & (ps - 1)) == 0 ? __builtin_ctz((unsigned)ps) : -1;
+  auto page_of_pos = [&](int pos) { return ps_shift >= 0 ? pos >> ps_shift : pos / ps; };
+  auto off_of_pos = [&](int pos) { return ps_shift >= 0 ? pos & (ps - 1) : pos % ps; };
   auto check_bt = [&](const int32_t* bt, int nb, int last_pos) -> int {
     if (nb < 0 || (int64_t)nb * ps <= last_pos) return set_error(SAR_ERR_INVALID_ARG, "step: block table does not cover the positions");
-    const int need = last_pos / ps + 1;
+    const int need = page_of_pos(last_pos) + 1;
     for (int i = 0; i < need; ++i)
       if (bt[i] < 0 || bt[i] >= env.num_pages) return set_error(SAR_ERR_BOUNDS, "step: page id out of range");
     return SAR_OK;
@@ -266,7 +272,7 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
   // within its pages (a captured step graph can then be re-pointed at the
   // next step); a decode's last range may be short or empty
   auto span_of = [&](int ctx) {
-    const int cap = (ctx / ps + 1) * ps;
+    const int cap = (page_of_pos(ctx) + 1) * ps;
     return d.sliding_window > 0 ? std::min(cap, d.sliding_window + 15) : cap;
   };
   int64_t total_keys = 0;
@@ -287,10 +293,11 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
   const int sms = env.sms;
   int64_t split = (total_keys * d.n_kv_heads) / (2LL * sms);
   split = std::max<int64_t>(128, std::min<int64_t>(4096, (split + 15) / 16 * 16));
+  const int split32 = (int)split;
   // scratch arrays kept per thread, so a step's planning allocates nothing
   // once they have grown to the batch's size
   thread_local std::vector<int32_t> items, pbeg, pcnt, nkeys, btoff, btlen, bt, tail_items, rows, pbt, tiles, comb;
-  thread_local std::vector<int> order;
+  thread_local std::vector<uint64_t> order;
   items.clear();
   bt.clear();
   tail_items.clear();
@@ -309,7 +316,7 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
     const int nk = dc.ctx_len + 1;
     nkeys[i] = nk;
     btoff[i] = (int32_t)bt.size();
-    const int nb = (dc.ctx_len / ps) + 1;
+    const int nb = page_of_pos(dc.ctx_len) + 1;
     btlen[i] = nb;
     {
       // copy the pages the positions use, checking each id on the way
@@ -327,7 +334,7 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
     }
     const int kfirst = first_key(nk);
     const int span = span_of(dc.ctx_len);
-    const int ns = (int)((span + split - 1) / split);
+    const int ns = (span + split32 - 1) / split32;
     // equal ranges (16-key multiples) rather than full ranges plus a remainder
     const int len = ((span + ns - 1) / ns + 15) / 16 * 16;
     pcnt[i] = ns;
@@ -342,14 +349,19 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
     }
     if (ns > 1) n_parts += ns;
   }
-  // longest ranges first, so the grid's last CTAs are its shortest
+  // longest ranges first, so the grid's last CTAs are its shortest (equal
+  // lengths in planning order: one sort of (length, index) keys)
   {
-    order.resize(tail_items.size() / 4);
-    for (size_t t = 0; t < order.size(); ++t) order[t] = (int)t;
-    std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
-      return tail_items[4 * x + 2] - tail_items[4 * x + 1] > tail_items[4 * y + 2] - tail_items[4 * y + 1];
-    });
-    for (int t : order) items.insert(items.end(), tail_items.begin() + 4 * t, tail_items.begin() + 4 * t + 4);
+    const size_t n_items = tail_items.size() / 4;
+    order.resize(n_items);
+    for (size_t t = 0; t < n_items; ++t) {
+      const uint32_t len = (uint32_t)(tail_items[4 * t + 2] - tail_items[4 * t + 1]);
+      order[t] = ((uint64_t)(0xFFFFFFFFu - len) << 32) | (uint64_t)t;
+    }
+    std::sort(order.begin(), order.end());
+    items.resize(4 * n_items);
+    for (size_t t = 0; t < n_items; ++t)
+      std::memcpy(items.data() + 4 * t, tail_items.data() + 4 * (order[t] & 0xFFFFFFFFu), 16);
   }
   // rows whose logits are returned: every chunk's last row, then every decode row
   {
@@ -377,7 +389,7 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
     for (const sar_prefill& c : chunks) {
       const int t_first = (int)tl.size();
       const int off = (int)pbt.size();
-      const int nb = (c.start_pos + c.len - 1) / ps + 1;
+      const int nb = page_of_pos(c.start_pos + c.len - 1) + 1;
       pbt.insert(pbt.end(), c.block_table, c.block_table + nb);
       for (int q0 = 0; q0 < c.len; q0 += tile_rows) {
         const int rws = std::min(tile_rows, c.len - q0);
@@ -497,17 +509,22 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
   int32_t* mt = meta->data();
   {
     int r = 0;
-    for (const sar_prefill& c : chunks)
+    for (const sar_prefill& c : chunks) {
+      int pg = page_of_pos(c.start_pos), off = off_of_pos(c.start_pos);
       for (int i = 0; i < c.len; ++i, ++r) {
-        const int pos = c.start_pos + i;
-        mt[p->o_pos + r] = pos;
-        mt[p->o_slot + r] = c.block_table[pos / ps] * ps + pos % ps;
+        mt[p->o_pos + r] = c.start_pos + i;
+        mt[p->o_slot + r] = c.block_table[pg] * ps + off;
+        if (++off == ps) {
+          off = 0;
+          ++pg;
+        }
       }
+    }
   }
   for (int i = 0; i < Bd; ++i) {
     const int pos = b->decode[i].ctx_len;
     mt[p->o_pos + Lp + i] = pos;
-    mt[p->o_slot + Lp + i] = b->decode[i].block_table[pos / ps] * ps + pos % ps;
+    mt[p->o_slot + Lp + i] = b->decode[i].block_table[page_of_pos(pos)] * ps + off_of_pos(pos);
   }
   if (!pbt.empty()) std::memcpy(mt + p->o_pbt, pbt.data(), pbt.size() * 4);
   std::memcpy(mt + p->o_nkeys, nkeys.data(), Bd * 4);
