@@ -205,6 +205,12 @@ def test_graph_launch_host_copies_in_and_out(mistral):
     for i in range(6):
         assert torch.equal(outs[i], toks if i % 2 == 0 else ref2), i
     assert torch.equal(x_dev.cpu(), x_host) and torch.equal(x_dev2.cpu(), x_host2)
+    with pytest.raises(sar.SarError):  # no logits captured: nothing to pick tokens from
+        nolog2 = sar.StepGraph(m, kv, b, x_dev2, hidden_out=hid)
+        try:
+            nolog2.enqueue_host_tokens(x_host2, toks)
+        finally:
+            nolog2.close()
     g2.close()
     nolog = sar.StepGraph(m, kv, b, x_dev, hidden_out=hid)
     with pytest.raises(sar.SarError):  # no logits captured
