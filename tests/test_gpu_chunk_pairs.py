@@ -29,12 +29,13 @@ PROMPT = 2048
 MAX_ABS, REL_L2 = 3e-2, 1e-2
 
 
-@pytest.fixture(scope="module")
-def layer():
-    # one Mistral-shaped layer (32 query heads over 8 KV heads x 128), no head
+@pytest.fixture(scope="module", params=[sar.SAR_STORAGE_F16, sar.SAR_STORAGE_BF16], ids=["f16", "bf16"])
+def layer(request):
+    # one Mistral-shaped layer (32 query heads over 8 KV heads x 128), no head,
+    # in either storage type (the kernels' two instantiations)
     case = synth.tile_sweep_case(0, rows=(PROMPT,), n_decode=0)
     dims = case["dims"]
-    m = harness.load_model(dims, case["layers"], None, max_tokens=1024, max_decodes=8)
+    m = harness.load_model(dims, case["layers"], None, max_tokens=1024, max_decodes=8, storage=request.param)
     n_pages = PROMPT // PS + 8
     bt = list(synth.page_permutation(synth.generator(11), n_pages))[:PROMPT // PS]
     kv = sar.KVCache(m, PS, n_pages)
