@@ -417,9 +417,9 @@ int validate_and_plan(const PlanEnv& env, const sar_batch* b, Plan* p, std::vect
     // Tile pairs (one CTA per pair of consecutive tiles of a chunk and head,
     // sharing their key blocks; a chunk's odd last tile pairs with an empty
     // one) when the one-tile grid needs more waves than the pair grid by a
-    // margin: a pair takes ~1.9 times a tile's time per key block (both are
-    // bound by their MMAs; the pair's two softmax chains only fill the
-    // one-tile kernel's short waits), so pairs win where they save waves --
+    // margin: a pair takes ~1.9 times a tile's time per key block (one set of
+    // softmax warps serves both tiles, and the softmax chain sets the pace of
+    // either kernel), so pairs win where they save waves --
     // 4 tiles x 56 heads (224 CTAs on 152 SMs, two waves) run as 112 pairs in
     // one -- and not where one-tile CTAs fill their waves about as well.
     // Full causal attention and whole key ranges only.
