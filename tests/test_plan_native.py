@@ -343,3 +343,28 @@ def test_pair_tables_on_random_batches(seed):
             check_pair_table(p, chunks)
         else:
             assert all(t[2] > 0 for t in p["tiles"])
+
+
+@pytest.mark.parametrize("ps", [16, 48, 64])
+def test_row_slots_for_other_page_sizes(ps):
+    """Positions map to (page, offset) slots for any page size the kernels
+    take (multiples of 16; powers of two take the shift-and-mask path, others
+    the division), for chunk rows that cross pages and for decode rows."""
+    rng = np.random.default_rng(ps)
+    pages = 4000
+    perm = rng.permutation(pages).tolist()
+    start, ln = 3 * ps - 5, 2 * ps + 9  # starts inside a page, ends inside another
+    cbt = perm[:(start + ln - 1) // ps + 1]
+    decs = []
+    o = len(cbt)
+    for i, ctx in enumerate([0, ps - 1, ps, 5 * ps + 3]):
+        n = ctx // ps + 1
+        decs.append((10 + i, ctx, perm[o:o + n]))
+        o += n
+    b = sar.Batch((0, start, ln, cbt), decs)
+    r = unpack(sar.plan_inspect(synth.MISTRAL_LAYER, b, ps, pages, 152, 512, 8))
+    for i in range(ln):
+        pos = start + i
+        assert r["pos"][i] == pos and r["slot"][i] == cbt[pos // ps] * ps + pos % ps
+    for k, (req, ctx, bt) in enumerate(decs):
+        assert r["pos"][ln + k] == ctx and r["slot"][ln + k] == bt[ctx // ps] * ps + ctx % ps
